@@ -1,0 +1,220 @@
+"""Quantizers of the quantized linear layer (oracle side).
+
+TEST INFRASTRUCTURE ONLY - see the package docstring.
+
+All arithmetic is float32, one IEEE operation at a time, in the order the
+pages write it; integer rounding is round-half-to-even ("LLM and AIGC
+quantization", notation paragraph: hand examples use round-half-to-even).
+
+Functions and the passages they follow:
+
+* quantize_affine / dequantize_affine - q = round(x/s) + z, x^ = s (q - z)
+  ("Chapter 9 - Quantization kernels", section 9.2; zero-point added on
+  quantize and subtracted on dequantize).
+* quant_sym_rows / quant_int8_sym - per-token symmetric int8: s = max|x| / 127, codes in
+  [-127, 127] ("LLM and AIGC quantization", "Symmetric and asymmetric":
+  s = max|x| / q_max, q_max = 2^(b-1) - 1; "Granularity": per-token
+  dynamic scales for W8A8).  Also used per output channel for W8A8 weights.
+* quant_int8_asym - per-token asymmetric int8 mapping [min, max] onto
+  [-128, 127] with an integer zero-point so that 0 is exact (same section;
+  the zero-point form of the W8A8 epilogue page, section 2).
+* quant_w4_g128 - asymmetric unsigned 4-bit weights, one fp16 scale and one
+  4-bit zero-point per 128 consecutive K elements of a row (AWQ offline flow,
+  ``pseudo_quant``: s = clamp(max - min, 1e-5) / 15, z = round(-min / s),
+  q = clamp(round(w / s) + z, 0, 15)).
+* nvfp4_global_scale / nvfp4_quantize / nvfp4_dequantize - 16-element blocks
+  of E2M1 with an E4M3 block scale absmax / 6, elements divided by the
+  decoded scale and rounded to the nearest E2M1 value ("LLM and AIGC
+  quantization", "Block-scaled formats", the 16-element NVFP4 example), with
+  a per-tensor fp32 second-level scale.
+* arc_perm / arc_quantize_activation / arc_quantize_weight - ARCQuant
+  residual-channel augmentation ("NVFP4 quantization and ARCQuant",
+  sections 2.1 and 2.2): reorder channels by magnitude, quantize, re-quantize
+  the residual of the first S channels and append it along K; weights get
+  the same order and a copy of their first S columns.
+
+Readings where the pages are silent (each is also listed in the design
+notes):
+
+* quant_int8_sym: an all-zero row uses s = 1 (all codes 0).
+* quant_int8_asym: the range always includes 0 (min <= 0 <= max) because the
+  zero-point must make 0 exactly representable; the range is floored at
+  1e-5 as in the AWQ code; z = -128 - round(min / s) and the code is
+  round(x / s) + z (round first, then add the integer zero-point).
+* quant_w4_g128: the scale is rounded to fp16 first and the rounded value is
+  the one used to quantize (it is what dequantization uses); z is clamped to
+  [0, 15].
+* NVFP4: the per-tensor scale is g = amax(|X|) / (6 * 448) so block scales
+  land in E4M3 range (the pages' example sets it to 1); a block whose decoded
+  scale d = dec(s) * g is 0 gets all-zero codes; the residual of the ARCQuant
+  channels uses the same g as the main part.
+* arc_perm: calibration statistic = max over rows of |X| per channel, taken
+  on X itself; channels sorted by descending statistic, ties by ascending
+  channel index.
+
+Parity pins: tests/test_oracle_pins.py.
+"""
+
+import numpy as np
+
+from .formats import e2m1_decode, e2m1_encode, e4m3_decode, e4m3_encode
+
+F32 = np.float32
+
+
+def quantize_affine(x, s, z, qmin, qmax):
+    """q = clamp(round(x / s) + z, qmin, qmax), float32 division, RNE."""
+    x = np.asarray(x, dtype=np.float32)
+    s = np.asarray(s, dtype=np.float32)
+    r = np.rint(x / s).astype(np.float64)
+    return np.clip(r + np.asarray(z, dtype=np.float64), qmin, qmax).astype(np.int64)
+
+
+def dequantize_affine(q, s, z):
+    """x^ = s * (q - z), in float64."""
+    return np.asarray(s, dtype=np.float64) * (np.asarray(q, dtype=np.float64) - np.asarray(z, dtype=np.float64))
+
+
+def quant_sym_rows(x, qmax):
+    """Per-row symmetric quantization with codes in [-qmax, qmax].
+
+    s = max|x| / qmax (float32), q = clamp(round(x / s), -qmax, qmax); an
+    all-zero row uses s = 1.  Returns (q int64, s float32 [rows]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x).max(axis=1)
+    s = a / F32(qmax)
+    s = np.where(a == 0, F32(1.0), s).astype(np.float32)
+    q = np.clip(np.rint(x / s[:, None]), -qmax, qmax).astype(np.int64)
+    return q, s
+
+
+def quant_int8_sym(x):
+    """Per-row symmetric int8.  x: float32 [rows][K] -> (q int8, s float32 [rows])."""
+    q, s = quant_sym_rows(x, 127)
+    return q.astype(np.int8), s
+
+
+def quant_int8_asym(x):
+    """Per-row asymmetric int8.  x: float32 [rows][K] -> (q int8, s float32, z int32)."""
+    x = np.asarray(x, dtype=np.float32)
+    mn = np.minimum(x.min(axis=1), F32(0.0))
+    mx = np.maximum(x.max(axis=1), F32(0.0))
+    s = (np.maximum(mx - mn, F32(1e-5)) / F32(255.0)).astype(np.float32)
+    z = (-128 - np.rint(mn / s).astype(np.int64)).astype(np.int32)
+    r = np.rint(x / s[:, None]).astype(np.int64)
+    q = np.clip(r + z[:, None].astype(np.int64), -128, 127).astype(np.int8)
+    return q, s, z
+
+
+def quant_w4_g128(w, group=128):
+    """Asymmetric 4-bit group quantization of weights W [N][K] (float32).
+
+    Returns (codes uint8 [N][K] in 0..15, scales float16 [N][K/group],
+    zeros uint8 [N][K/group] in 0..15).
+    """
+    w = np.asarray(w, dtype=np.float32)
+    n, k = w.shape
+    if k % group:
+        raise ValueError("K must be a multiple of the group size")
+    g = w.reshape(n, k // group, group)
+    mx = g.max(axis=2)
+    mn = g.min(axis=2)
+    s16 = (np.maximum(mx - mn, F32(1e-5)) / F32(15.0)).astype(np.float16)
+    s = s16.astype(np.float32)
+    z = np.clip(np.rint(-mn / s), 0, 15)
+    q = np.clip(np.rint(g / s[:, :, None]) + z[:, :, None], 0, 15)
+    return q.reshape(n, k).astype(np.uint8), s16, z.astype(np.uint8)
+
+
+def nvfp4_global_scale(x):
+    """Per-tensor second-level scale g = amax(|x|) / (6 * 448), float32."""
+    x = np.asarray(x, dtype=np.float32)
+    return F32(np.abs(x).max()) / F32(2688.0)
+
+
+def _block_divisor(sf, g):
+    """Decoded block scale times the per-tensor scale, d = dec(sf) * g (float32)."""
+    return (e4m3_decode(sf).astype(np.float32) * F32(g)).astype(np.float32)
+
+
+def nvfp4_quantize(x, g):
+    """NVFP4 block quantization of x [rows][K] (float32, K % 16 == 0).
+
+    Per 16-element block b of a row:
+      s_b  = E4M3((max|x_b| / 6) / g)
+      d_b  = dec(s_b) * g
+      q    = E2M1(x / d_b)           (all zero when d_b == 0)
+    Returns (codes uint8 [rows][K], sf uint8 [rows][K/16]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    rows, k = x.shape
+    if k % 16:
+        raise ValueError("K must be a multiple of 16")
+    g = F32(g)
+    blocks = x.reshape(rows, k // 16, 16)
+    amax = np.abs(blocks).max(axis=2)
+    v = (amax / F32(6.0)) / g
+    sf = e4m3_encode(v)
+    d = _block_divisor(sf, g)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = blocks / d[:, :, None]
+    q = e2m1_encode(y)
+    q[d == 0] = 0
+    return q.reshape(rows, k), sf
+
+
+def nvfp4_dequantize(codes, sf, g):
+    """Exact float64 value of each NVFP4 element: e2m1(q) * dec(s) * g."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    rows, k = codes.shape
+    e = e2m1_decode(codes).reshape(rows, k // 16, 16)
+    sc = e4m3_decode(sf)[:, :, None] * np.float64(F32(g))
+    return (e * sc).reshape(rows, k)
+
+
+def arc_perm(x):
+    """Channel order by descending max over rows of |x|, ties by ascending index."""
+    x = np.asarray(x, dtype=np.float32)
+    stat = np.abs(x).max(axis=0)
+    return np.argsort(-stat.astype(np.float64), kind="stable").astype(np.int32)
+
+
+def arc_quantize_activation(x, perm, s_res, g):
+    """ARCQuant activation quantization.
+
+    1. reorder channels: xs = x[:, perm]
+    2. main part: NVFP4(xs) with per-tensor scale g
+    3. residual of the first S reordered channels:
+       r = xs[:, :S] - e2m1(q) * d      (float32, the divisor d of step 2)
+    4. NVFP4(r) with the same g, appended along K
+    Returns (codes [rows][K+S], sf [rows][(K+S)/16]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    rows, k = x.shape
+    if s_res % 16 or s_res < 0 or s_res > k:
+        raise ValueError("S must be a multiple of 16 in [0, K]")
+    xs = x[:, np.asarray(perm)] if perm is not None else x
+    q, sf = nvfp4_quantize(xs, g)
+    if s_res == 0:
+        return q, sf
+    d = _block_divisor(sf[:, : s_res // 16], g)                      # [rows][S/16]
+    e = e2m1_decode(q[:, :s_res]).astype(np.float32).reshape(rows, s_res // 16, 16)
+    deq = (e * d[:, :, None]).astype(np.float32)                      # one float32 multiply
+    r = (xs[:, :s_res].reshape(rows, s_res // 16, 16) - deq).astype(np.float32)
+    qr, sfr = nvfp4_quantize(r.reshape(rows, s_res), g)
+    return np.concatenate([q, qr], axis=1), np.concatenate([sf, sfr], axis=1)
+
+
+def arc_quantize_weight(w, perm, s_res, g):
+    """ARCQuant weight side: NVFP4(W[:, perm]) with the codes and scales of the
+    first S columns copied (not recomputed) and appended along K."""
+    w = np.asarray(w, dtype=np.float32)
+    if s_res % 16 or s_res < 0 or s_res > w.shape[1]:
+        raise ValueError("S must be a multiple of 16 in [0, K]")
+    ws = w[:, np.asarray(perm)] if perm is not None else w
+    q, sf = nvfp4_quantize(ws, g)
+    if s_res == 0:
+        return q, sf
+    return (np.concatenate([q, q[:, :s_res]], axis=1),
+            np.concatenate([sf, sf[:, : s_res // 16]], axis=1))

@@ -1,0 +1,615 @@
+"""Pins of the CPU oracle to facts fixed outside the oracle itself.
+
+Each check ties an oracle function to a value printed on one of the pages
+(fixtures under tests/golden/, each naming its source), to a closed form, to
+an independent library routine (torch's float8_e4m3fn), to exact brute force
+on tiny inputs, or to an invariant of the mathematics.  The mutation tests at
+the end plant plausible mistakes in the oracle and check that a pin fails.
+"""
+
+import fractions
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import formats as ofmt
+from oracle import gemm as ogemm
+from oracle import quant as oquant
+from conftest import load_golden
+
+F32 = np.float32
+
+
+# --------------------------------------------------------------------------
+# Affine quantization (Chapter 9, section 9.2; LLM quantization, linear
+# quantization / symmetric and asymmetric / granularity)
+# --------------------------------------------------------------------------
+
+def pin_int8_range_example():
+    g = load_golden("int8_range_example.json")
+    s_exact = g["scale_exact_num"] / g["scale_exact_den"]
+    for s in (s_exact, g["scale_printed"]):
+        for x, q in g["quantize"]:
+            assert int(oracle.quantize_affine(x, s, 0, -128, 127)) == q
+    d = g["dequantize_printed"]
+    x = float(oracle.dequantize_affine(d["q"], g["scale_printed"], 0))
+    assert abs(x - d["x"]) < 5e-4
+    assert abs(abs(x - 1.5) - d["abs_err_printed"]) < 5e-4
+
+
+def test_int8_range_example():
+    pin_int8_range_example()
+
+
+def pin_linear_ruler():
+    """The 4-bit ruler over [-1.5, 3.0]: spacing 0.3, zero-point 5, via the
+    group weight quantizer on a group spanning that range."""
+    g = load_golden("linear_ruler.json")
+    w = np.linspace(g["x_min"], g["x_max"], 128, dtype=np.float32)[None, :]
+    codes, s16, z = oracle.quant_w4_g128(w, group=128)
+    assert abs(float(s16[0, 0]) - g["scale"]) < 1e-3     # fp16 rounding of 0.3
+    assert int(z[0, 0]) == g["zero_point"]
+    for code, value in g["code_to_value"]:
+        i = int(np.argmin(np.abs(w[0] - value)))
+        assert int(codes[0, i]) == code
+    # every element is reproduced to within half a step
+    deq = (codes.astype(np.float64) - z.astype(np.float64)) * float(s16[0, 0])
+    assert np.max(np.abs(deq - w)) <= float(s16[0, 0]) / 2 + 1e-6
+
+
+def test_linear_ruler():
+    pin_linear_ruler()
+
+
+def pin_sym_asym_vector():
+    g = load_golden("sym_asym_vector.json")
+    x = np.array(g["x"], dtype=np.float32)[None, :]
+    # symmetric INT4: s = max|x| / 7, codes -7..7
+    q, s = oracle.quant_sym_rows(x, g["sym_int4"]["qmax"])
+    assert q.min() >= -7 and q.max() <= 7
+    mse_sym = np.mean((oracle.dequantize_affine(q, s[:, None], 0) - x) ** 2)
+    assert abs(mse_sym - g["sym_int4"]["mse_printed"]) < 5e-5
+    # asymmetric unsigned INT4 (the group quantizer with a group of 8)
+    codes, s16, z = oracle.quant_w4_g128(x, group=8)
+    a = g["asym_uint4"]
+    assert int(z[0, 0]) == a["zero_point"]
+    deq = oracle.dequantize_affine(codes, float(s16[0, 0]), float(z[0, 0]))
+    assert abs(np.mean((deq - x) ** 2) - a["mse_printed"]) < 5e-5
+    assert abs(deq[0, 5] - a["x_minus_2_80_dequant_printed"]) < 5e-3
+    assert abs((float(z[0, 0]) - 2.80 / float(s16[0, 0])) - a["grid_shift_in_steps_printed"]) < 5e-3
+    assert abs((mse_sym - np.mean((deq - x) ** 2)) / mse_sym - g["asym_vs_sym_improvement_printed"]) < 0.01
+    # INT8 symmetric: scale about 1/18 of INT4's, MSE about 460x smaller
+    q8, s8 = oracle.quant_int8_sym(x)
+    r = g["int8_vs_int4"]
+    assert abs(float(s[0]) / float(s8[0]) - r["scale_ratio_printed"]) < 0.5
+    mse8 = np.mean((oracle.dequantize_affine(q8, s8[:, None], 0) - x) ** 2)
+    assert abs(mse_sym / mse8 / r["mse_ratio_printed"] - 1) < 0.02
+    # the GELU vector
+    ge = g["gelu"]
+    xg = np.array(ge["x"], dtype=np.float32)[None, :]
+    qg, sg = oracle.quant_sym_rows(xg, 7)
+    assert abs(np.mean((oracle.dequantize_affine(qg, sg[:, None], 0) - xg) ** 2) - ge["sym_int4_mse_printed"]) < 5e-6
+    cg, s16g, zg = oracle.quant_w4_g128(xg, group=8)
+    assert int(zg[0, 0]) == ge["asym_zero_point"]
+    assert abs(float(s16g[0, 0]) - ge["asym_scale_num"] / ge["asym_scale_den"]) < 2e-4
+    deqg = oracle.dequantize_affine(cg, float(s16g[0, 0]), float(zg[0, 0]))
+    assert abs(np.mean((deqg - xg) ** 2) - ge["asym_uint4_mse_printed"]) < 5e-6
+
+
+def test_sym_asym_vector():
+    pin_sym_asym_vector()
+
+
+def pin_granularity():
+    g = load_golden("granularity_example.json")
+    w = np.array(g["W"], dtype=np.float32)
+    s_t = np.abs(w).max() / F32(7)
+    assert abs(float(s_t) - g["per_tensor"]["scale_printed"]) < 5e-5
+    q_t = oracle.quantize_affine(w, s_t, 0, -7, 7)
+    assert q_t[0].tolist() == g["per_tensor"]["row1_codes"]
+    mse_row1 = np.mean((oracle.dequantize_affine(q_t[0], s_t, 0) - w[0]) ** 2)
+    assert abs(mse_row1 - g["per_tensor"]["row1_mse_printed"]) < 5e-5
+    pc = g["per_channel_row1"]
+    q, s = oracle.quant_sym_rows(w, 7)
+    assert q[0].tolist() == pc["codes"]                     # 3.5 -> 4 (RNE tie)
+    assert abs(float(s[0]) - pc["scale_num"] / pc["scale_den"]) < 1e-7
+    deq = oracle.dequantize_affine(q[0], s[0], 0)
+    assert np.max(np.abs(deq - np.array(pc["dequant_printed"]))) < 5e-4
+    assert abs(np.mean((deq - w[0]) ** 2) - pc["mse_printed"]) < 5e-5
+
+
+def test_granularity():
+    pin_granularity()
+
+
+def test_round_half_to_even():
+    # ties at the integer level go to the even integer
+    xs = np.array([0.5, 1.5, 2.5, -0.5, -1.5, -2.5], dtype=np.float32)
+    assert oracle.quantize_affine(xs, 1.0, 0, -128, 127).tolist() == [0, 2, 2, 0, -2, -2]
+
+
+def test_int8_sym_properties():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((64, 96)).astype(np.float16).astype(np.float32)
+    x[3] = 0.0
+    q, s = oracle.quant_int8_sym(x)
+    assert q.dtype == np.int8 and q.min() >= -127
+    assert s[3] == 1.0 and not q[3].any()
+    nz = np.arange(64) != 3
+    # the largest magnitude in each row maps to +-127
+    assert np.all(np.abs(q[nz]).max(axis=1) == 127)
+    # every element is reproduced to within half a step
+    err = np.abs(q.astype(np.float64) * s[:, None] - x)
+    assert np.all(err <= s[:, None].astype(np.float64) * (0.5 + 2e-5))
+
+
+def test_int8_asym_properties():
+    rng = np.random.default_rng(12)
+    x = rng.uniform(-1, 3, size=(64, 96)).astype(np.float16).astype(np.float32)
+    x[5] = np.abs(x[5])          # a row that does not straddle 0
+    q, s, z = oracle.quant_int8_asym(x)
+    assert q.dtype == np.int8 and z.dtype == np.int32
+    assert np.all((z >= -128) & (z <= 127))
+    # 0 is exactly representable: dequant(z) == 0
+    assert np.all(oracle.dequantize_affine(z, s, z) == 0)
+    # the row minimum (or 0) maps to -128; everything within half a step
+    mn = np.minimum(x.min(axis=1), 0)
+    i = np.argmin(x, axis=1)
+    assert np.all(q[np.arange(64), i][mn < 0] == -128)
+    deq = oracle.dequantize_affine(q, s[:, None], z[:, None])
+    assert np.all(np.abs(deq - x) <= s[:, None].astype(np.float64) * (0.5 + 2e-5))
+
+
+def test_w4_g128_properties():
+    rng = np.random.default_rng(13)
+    w = (rng.standard_normal((8, 512)) * 0.02).astype(np.float32)
+    codes, s16, z = oracle.quant_w4_g128(w)
+    assert codes.shape == (8, 512) and s16.shape == (8, 4) and s16.dtype == np.float16
+    assert codes.max() <= 15 and z.max() <= 15
+    deq = (codes.reshape(8, 4, 128).astype(np.float64) - z[..., None]) * s16[..., None].astype(np.float64)
+    assert np.all(np.abs(deq.reshape(8, 512) - w) <= s16.astype(np.float64).repeat(128, axis=1) * (0.5 + 2e-5))
+
+
+# --------------------------------------------------------------------------
+# Integer formats and packing (LLM quantization, "Integers", "W4A16")
+# --------------------------------------------------------------------------
+
+def test_int4_twos_complement():
+    g = load_golden("int_formats.json")
+    for bits, v in g["int4_twos_complement"]:
+        assert oracle.int4_decode(int(bits, 2), signed=True) == v
+    for bits, v in g["int4_unsigned"]:
+        assert oracle.int4_decode(int(bits, 2), signed=False) == v
+    # signed codes q - 8 with zero-point z - 8 dequantize identically
+    q = np.arange(16)
+    for z in range(16):
+        assert np.array_equal(oracle.dequantize_affine(q, 0.02, z), oracle.dequantize_affine(q - 8, 0.02, z - 8))
+
+
+def test_packing_example():
+    g = load_golden("int_formats.json")["packing"]
+    packed = oracle.pack_u4(np.array(g["codes"], dtype=np.uint8))
+    assert packed.view("<u4")[0] == int(g["word_hex"], 16)
+    assert oracle.unpack_u4(packed, 8).tolist() == g["codes"]
+    # q_i << 4i, read back by shifting right 4i and masking
+    word = int(g["word_hex"], 16)
+    assert [(word >> (4 * i)) & 0xF for i in range(8)] == g["codes"]
+
+
+def test_int4_unpack_magic_constants():
+    """The constants of the register-level INT4 -> FP16/BF16 unpack."""
+    torch = pytest.importorskip("torch")
+    g = load_golden("int4_unpack_magic.json")
+
+    def h(bits):
+        return float(np.array([int(bits, 16)], dtype=np.uint16).view(np.float16)[0])
+
+    def b(bits):
+        return float(torch.from_numpy(np.array([int(bits, 16)], dtype=np.uint16).view(np.int16)).view(torch.bfloat16).float()[0])
+
+    f = g["fp16"]
+    assert h(f["EX"]) == f["EX_value"] and h(f["SUB"]) == f["SUB_value"]
+    assert h(f["MUL"]) == f["MUL_value"] and h(f["ADD"]) == f["ADD_value"]
+    e = g["example"]
+    assert h(e["or_bits"]) == e["or_value"] and e["or_value"] - e["minus"] == e["int_value"]
+    assert abs(e["int_value"] * e["s"] - e["dequant"]) < 1e-12
+    # every nibble n: (0x6400 | n) - 0x6408 == n - 8 and (1024 + 16n)/16 - 72 == n - 8
+    for n in range(16):
+        assert h(hex(0x6400 | n)) - h(f["SUB"]) == n - 8
+        assert h(hex(0x6400 | (n << 4))) * h(f["MUL"]) + h(f["ADD"]) == n - 8
+    bf = g["bf16"]
+    assert b(bf["EX"]) == bf["EX_value"] and b(bf["MUL"]) == bf["MUL_value"] and b(bf["ADD"]) == bf["ADD_value"]
+    for n in range(16):
+        assert b(hex(0x4300 | n)) * b(bf["MUL"]) + b(bf["ADD"]) == n - 8
+
+
+# --------------------------------------------------------------------------
+# FP4 E2M1 / FP8 E4M3-FN (LLM quantization, "Floating point", "FP8")
+# --------------------------------------------------------------------------
+
+def pin_fp_formats():
+    g = load_golden("fp_formats.json")
+    assert oracle.e2m1_decode(np.arange(8)).tolist() == g["e2m1_magnitudes"]
+    assert oracle.e2m1_decode(np.arange(8, 16)).tolist() == [-v for v in g["e2m1_magnitudes"]]
+    mags = oracle.e4m3_finite_magnitudes()
+    assert mags.max() == g["e4m3fn_max"] == 1.75 * 2 ** 8
+    x, bits, val = g["e4m3_encode"][0]
+    c = int(oracle.e4m3_encode(np.float32(x)))
+    assert c == int(bits.replace(" ", ""), 2) and oracle.e4m3_decode(c) == val
+    x, _, val = g["e4m3_encode"][1]
+    assert oracle.e4m3_decode(oracle.e4m3_encode(np.float32(x))) == val
+    for lo, hi, step in g["e4m3_spacing"]:
+        inside = mags[(mags >= lo) & (mags <= hi)]
+        assert np.all(np.diff(inside) == step)
+    for x, v in g["e4m3_rounding_printed"]:
+        assert oracle.e4m3_decode(oracle.e4m3_encode(np.float32(x))) == v
+
+
+def test_fp_formats():
+    pin_fp_formats()
+
+
+def pin_e2m1_ties_even():
+    mags = np.array(oracle.E2M1_MAGNITUDES)
+    for c in range(7):
+        mid = (mags[c] + mags[c + 1]) / 2
+        even = c if c % 2 == 0 else c + 1
+        for sign in (1, -1):
+            code = int(oracle.e2m1_encode(np.float32(sign * mid)))
+            assert code & 7 == even
+            above = np.nextafter(np.float32(mid), np.float32(10))
+            below = np.nextafter(np.float32(mid), np.float32(-10))
+            assert int(oracle.e2m1_encode(sign * above)) & 7 == c + 1
+            assert int(oracle.e2m1_encode(sign * below)) & 7 == c
+    # saturation and signed zero
+    assert int(oracle.e2m1_encode(np.float32(7.0))) == 7
+    assert int(oracle.e2m1_encode(np.float32(1e30))) == 7
+    assert int(oracle.e2m1_encode(np.float32(-1e30))) == 15
+    assert int(oracle.e2m1_encode(np.float32(-0.1))) == 8
+    assert int(oracle.e2m1_encode(np.float32(0.0))) == 0
+    for c in range(16):
+        assert int(oracle.e2m1_encode(np.float32(oracle.e2m1_decode(c) if c != 8 else -0.0))) == c
+
+
+def test_e2m1_ties_even():
+    pin_e2m1_ties_even()
+
+
+def test_e4m3_against_torch():
+    """Exhaustive decode and a dense encode sweep against torch's float8_e4m3fn."""
+    torch = pytest.importorskip("torch")
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    assert np.array_equal(oracle.e4m3_decode(codes), ref)
+    mags = oracle.e4m3_finite_magnitudes()
+    mids = (mags[:-1] + mags[1:]) / 2
+    pts = np.concatenate([mags, mids]).astype(np.float32)
+    pts = np.concatenate([pts, np.nextafter(pts, np.float32(0)), np.nextafter(pts, np.float32(1e9))])
+    rng = np.random.default_rng(5)
+    pts = np.concatenate([pts, (rng.random(20000) * 460).astype(np.float32),
+                          np.exp2(rng.uniform(-14, 9, 20000)).astype(np.float32)])
+    pts = pts[(pts >= 0) & (pts < 448)]
+    pts = np.concatenate([pts, -pts])
+    tq = torch.from_numpy(pts).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(pts), tq)
+    # saturation beyond 448 (the pages' 500 -> 448)
+    assert np.all(oracle.e4m3_encode(np.array([449, 470, 480, 500, 1e6], dtype=np.float32)) == 0x7E)
+
+
+# --------------------------------------------------------------------------
+# NVFP4 (LLM quantization, "Block-scaled formats")
+# --------------------------------------------------------------------------
+
+def pin_nvfp4_block():
+    g = load_golden("nvfp4_block.json")
+    x = np.array(g["block"], dtype=np.float32)[None, :]
+    q, sf = oracle.nvfp4_quantize(x, np.float32(1.0))
+    assert int(sf[0, 0]) == int(g["block_scale_bits"].replace(" ", ""), 2)
+    assert oracle.e4m3_decode(sf[0, 0]) == g["block_scale_e4m3"]
+    assert oracle.e2m1_decode(q[0]).tolist() == g["codes_values"]
+    deq = oracle.nvfp4_dequantize(q, sf, np.float32(1.0))
+    assert abs(np.mean((deq - x) ** 2) - g["mse_printed"]) < 5e-5
+    w = g["worst"]
+    i = g["block"].index(w["x"])
+    assert abs(x[0, i] / g["block_scale_e4m3"] - w["scaled_printed"]) < 5e-3
+    assert oracle.e2m1_decode(q[0, i]) == w["value"]
+    assert abs(deq[0, i] - w["dequant_printed"]) < 5e-3
+    qs, ss = oracle.quant_sym_rows(x, 7)
+    assert abs(np.mean((oracle.dequantize_affine(qs, ss[:, None], 0) - x) ** 2) - g["sym_int4_mse_printed"]) < 5e-5
+
+
+def test_nvfp4_block():
+    pin_nvfp4_block()
+
+
+def test_nvfp4_global_scale_properties():
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((32, 256)).astype(np.float16).astype(np.float32)
+    x[7, 100] = 37.0
+    gsc = oracle.nvfp4_global_scale(x)
+    assert gsc.dtype == np.float32
+    q, sf = oracle.nvfp4_quantize(x, gsc)
+    # the block holding the tensor's largest magnitude gets the top scale 448
+    assert sf[7, 100 // 16] == 0x7E
+    assert oracle.e2m1_decode(q[7, 100]) == 6.0
+    # every block: |x| / d <= 6 up to rounding of the scale, elements within a half step of the grid
+    deq = oracle.nvfp4_dequantize(q, sf, gsc)
+    d = oracle.e4m3_decode(sf).repeat(16, axis=1) * float(gsc)
+    assert np.all(np.abs(deq - x) <= d * 1.0 + 1e-12)
+    # an all-zero block has scale code 0 and zero codes
+    x2 = x.copy()
+    x2[0, :16] = 0
+    q2, sf2 = oracle.nvfp4_quantize(x2, gsc)
+    assert sf2[0, 0] == 0 and not q2[0, :16].any()
+
+
+def test_arc_perm_order_and_ties():
+    x = np.array([[1, -5, 2, 5, 0], [-3, 1, 2, -1, 0]], dtype=np.float32)
+    # column maxima of |x|: [3, 5, 2, 5, 0] -> 1, 3 (tie, lower index first), 0, 2, 4
+    assert oracle.arc_perm(x).tolist() == [1, 3, 0, 2, 4]
+
+
+def _arc_case(seed=3, t=24, k=128, n=20, s_res=32):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((t, k)).astype(np.float32)
+    out = rng.choice(k, 6, replace=False)
+    x[:, out] *= 50
+    x = x.astype(np.float16).astype(np.float32)
+    w = (rng.standard_normal((n, k)) * 0.02).astype(np.float32)
+    return x, w, s_res
+
+
+def test_arc_s0_is_plain_nvfp4():
+    x, w, _ = _arc_case()
+    perm = oracle.arc_perm(x)
+    g = oracle.nvfp4_global_scale(x)
+    qa, sfa = oracle.arc_quantize_activation(x, perm, 0, g)
+    qb, sfb = oracle.nvfp4_quantize(x[:, perm], g)
+    assert np.array_equal(qa, qb) and np.array_equal(sfa, sfb)
+
+
+def test_arc_weight_columns_copied():
+    x, w, s = _arc_case()
+    perm = oracle.arc_perm(x)
+    gw = oracle.nvfp4_global_scale(w)
+    q, sf = oracle.arc_quantize_weight(w, perm, s, gw)
+    k = w.shape[1]
+    assert q.shape == (w.shape[0], k + s) and sf.shape == (w.shape[0], (k + s) // 16)
+    assert np.array_equal(q[:, k:], q[:, :s]) and np.array_equal(sf[:, k // 16:], sf[:, : s // 16])
+
+
+def pin_arc_residual_reduces_error():
+    """Adding the re-quantized residual of the outlier channels must bring
+    the augmented product closer to the exact X W^T than plain NVFP4 RTN."""
+    x, w, s = _arc_case()
+    perm = oracle.arc_perm(x)
+    gx, gw = oracle.nvfp4_global_scale(x), oracle.nvfp4_global_scale(w)
+    exact = x.astype(np.float64) @ w.astype(np.float64).T
+    qa, sfa = oracle.arc_quantize_activation(x, perm, s, gx)
+    qb, sfb = oracle.arc_quantize_weight(w, perm, s, gw)
+    y_arc = oracle.nvfp4_gemm_reference(qa, sfa, gx, qb, sfb, gw)
+    qa0, sfa0 = oracle.arc_quantize_activation(x, perm, 0, gx)
+    qb0, sfb0 = oracle.arc_quantize_weight(w, perm, 0, gw)
+    y_rtn = oracle.nvfp4_gemm_reference(qa0, sfa0, gx, qb0, sfb0, gw)
+    e_arc = np.linalg.norm(y_arc - exact)
+    e_rtn = np.linalg.norm(y_rtn - exact)
+    assert e_arc < 0.9 * e_rtn
+    # the main part plus the residual reproduces the outlier channels better
+    main = oracle.nvfp4_dequantize(qa[:, : x.shape[1]], sfa[:, : x.shape[1] // 16], gx)[:, :s]
+    res = oracle.nvfp4_dequantize(qa[:, x.shape[1]:], sfa[:, x.shape[1] // 16:], gx)
+    xs = x[:, perm][:, :s]
+    assert np.linalg.norm(main + res - xs) < 0.5 * np.linalg.norm(main - xs)
+
+
+def test_arc_residual_reduces_error():
+    pin_arc_residual_reduces_error()
+
+
+def test_nvfp4_gemm_block_permutation_invariance():
+    x, w, s = _arc_case()
+    gx, gw = oracle.nvfp4_global_scale(x), oracle.nvfp4_global_scale(w)
+    qa, sfa = oracle.nvfp4_quantize(x, gx)
+    qb, sfb = oracle.nvfp4_quantize(w, gw)
+    y = oracle.nvfp4_gemm_reference(qa, sfa, gx, qb, sfb, gw)
+    nb = x.shape[1] // 16
+    bp = np.random.default_rng(0).permutation(nb)
+    cols = (bp[:, None] * 16 + np.arange(16)).reshape(-1)
+    y2 = oracle.nvfp4_gemm_reference(qa[:, cols], sfa[:, bp], gx, qb[:, cols], sfb[:, bp], gw)
+    assert np.allclose(y, y2, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# GEMMs: brute force on tiny inputs, the pages' W8A8 example, azp identity
+# --------------------------------------------------------------------------
+
+def pin_w8a8_example():
+    g = load_golden("w8a8_example.json")
+    xq = np.array(g["Xq"], dtype=np.int8)
+    wq = np.array(g["Wq"], dtype=np.int8)
+    d = oracle.int8_gemm_exact(xq, wq)
+    assert d[0, 0] == g["D11_printed"]
+    sx = np.array(g["scale_x_absmax"], dtype=np.float32) / F32(g["qmax"])
+    sw = np.array(g["scale_w_absmax"], dtype=np.float32) / F32(g["qmax"])
+    assert np.allclose(sx, g["scale_x_printed"], atol=5e-7) and np.allclose(sw, g["scale_w_printed"], atol=5e-7)
+    y = oracle.w8a8_epilogue(d, sx, sw)
+    assert np.max(np.abs(y - np.array(g["Y_printed"]))) < 1.5e-4
+    assert 127 ** 2 == g["max_single_product_printed"]
+    assert abs(4096 * 127 ** 2 - g["k4096_sum_bound_printed"]) / g["k4096_sum_bound_printed"] < 0.01
+    # worst case of the int32 accumulator at K = 4096 (activation code -128)
+    assert 4096 * 128 * 127 < 2 ** 31
+
+
+def test_w8a8_example():
+    pin_w8a8_example()
+
+
+def _fr(v):
+    return fractions.Fraction(float(v))
+
+
+def pin_azp_identity():
+    """s_a s_b (A^ B^^T - z (1 . B^)) + bias equals dequantize-then-multiply,
+    exactly (rational arithmetic), for per-token and per-tensor zero-points."""
+    rng = np.random.default_rng(7)
+    for trial in range(4):
+        t, k, n = 3, 5, 4
+        a = rng.integers(-128, 128, size=(t, k)).astype(np.int8)
+        b = rng.integers(-127, 128, size=(n, k)).astype(np.int8)
+        sa = rng.uniform(0.01, 0.1, size=t).astype(np.float32)
+        sb = rng.uniform(0.01, 0.1, size=n).astype(np.float32)
+        bias = rng.standard_normal(n).astype(np.float16)
+        per_token = trial % 2 == 0
+        z = rng.integers(-128, 128, size=t).astype(np.int32) if per_token else np.full(t, int(rng.integers(-128, 128)), np.int32)
+        adj = oracle.azp_adj_from_weight(b)
+        d = oracle.int8_gemm_exact(a, b)
+        if per_token:
+            out = oracle.w8a8_epilogue(d, sa, sb, azp=z, azp_adj=adj, bias=bias)
+        else:
+            out = oracle.w8a8_epilogue(d, sa, sb, azp=None, azp_adj=int(z[0]) * adj, bias=bias)
+        for i, j in itertools.product(range(t), range(n)):
+            exact = sum(_fr(sa[i]) * (int(a[i, kk]) - int(z[i])) * _fr(sb[j]) * int(b[j, kk]) for kk in range(k)) + _fr(bias[j])
+            assert abs(_fr(out[i, j]) - exact) <= abs(exact) * fractions.Fraction(1, 10 ** 12) + fractions.Fraction(1, 10 ** 15)
+
+
+def test_azp_identity():
+    pin_azp_identity()
+
+
+def pin_w4a16_brute_force():
+    rng = np.random.default_rng(9)
+    t, n, k, group = 2, 3, 64, 32
+    x = rng.standard_normal((t, k)).astype(np.float16)
+    codes = rng.integers(0, 16, size=(n, k)).astype(np.uint8)
+    scales = rng.uniform(0.005, 0.02, size=(n, k // group)).astype(np.float16)
+    zeros = rng.integers(0, 16, size=(n, k // group)).astype(np.uint8)
+    for zz in (zeros, None):
+        y = oracle.w4a16_reference(x, codes, scales, zz, group)
+        y2 = oracle.w4a16_reference_packed(x, oracle.pack_u4(codes), scales, None if zz is None else oracle.pack_u4(zz), group)
+        assert np.array_equal(y, y2)
+        for i in range(t):
+            for j in range(n):
+                acc = 0.0
+                for kk in range(k):
+                    zp = 8 if zz is None else int(zz[j, kk // group])
+                    acc += float(x[i, kk]) * float(scales[j, kk // group]) * (int(codes[j, kk]) - zp)
+                assert abs(y[i, j] - acc) <= 1e-12 * (1 + abs(acc))
+
+
+def test_w4a16_brute_force():
+    pin_w4a16_brute_force()
+
+
+def pin_nvfp4_gemm_brute_force():
+    rng = np.random.default_rng(10)
+    t, n, k = 2, 3, 48
+    qa = rng.integers(0, 16, size=(t, k)).astype(np.uint8)
+    qb = rng.integers(0, 16, size=(n, k)).astype(np.uint8)
+    sfa = rng.integers(0, 0x7E, size=(t, k // 16)).astype(np.uint8)
+    sfb = rng.integers(0, 0x7E, size=(n, k // 16)).astype(np.uint8)
+    ga, gb = np.float32(0.37), np.float32(1.7)
+    y = oracle.nvfp4_gemm_reference(qa, sfa, ga, qb, sfb, gb)
+    e2 = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+
+    def val(c):
+        return (-1 if c & 8 else 1) * e2[c & 7]
+
+    def sc(c):
+        e, m = (c >> 3) & 15, c & 7
+        return (m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+
+    for i in range(t):
+        for j in range(n):
+            acc = 0.0
+            for bb in range(k // 16):
+                part = sum(val(int(qa[i, bb * 16 + u])) * val(int(qb[j, bb * 16 + u])) for u in range(16))
+                acc += sc(int(sfa[i, bb])) * sc(int(sfb[j, bb])) * part
+            acc *= float(ga) * float(gb)
+            assert abs(y[i, j] - acc) <= 1e-12 * (1 + abs(acc))
+
+
+def test_nvfp4_gemm_brute_force():
+    pin_nvfp4_gemm_brute_force()
+
+
+# --------------------------------------------------------------------------
+# Planted mistakes: each must make at least one pin fail
+# --------------------------------------------------------------------------
+
+def _mut_e2m1_ties_odd(monkeypatch):
+    orig = ofmt._nearest_code
+
+    def bad(mag, table):
+        idx = orig(mag, table)
+        mids = (table[:-1] + table[1:]) / 2
+        on = np.isin(np.asarray(mag, dtype=np.float64), mids)
+        return np.where(on & (idx % 2 == 0), np.maximum(idx - 1, 0), idx)
+
+    monkeypatch.setattr(ofmt, "_nearest_code", bad)
+    return pin_e2m1_ties_even
+
+
+def _mut_azp_sign(monkeypatch):
+    orig = ogemm.w8a8_epilogue
+
+    def bad(dhat, sa, sb, azp=None, azp_adj=None, bias=None):
+        return orig(dhat, sa, sb, None if azp is None else -np.asarray(azp), None if azp_adj is None else (-np.asarray(azp_adj) if azp is None else azp_adj), bias)
+
+    monkeypatch.setattr(oracle, "w8a8_epilogue", bad)
+    return pin_azp_identity
+
+
+def _mut_azp_adj_axis(monkeypatch):
+    def bad(b):
+        b = np.asarray(b, dtype=np.int64)
+        return np.resize(b.sum(axis=0), b.shape[0]).astype(np.int32)
+
+    monkeypatch.setattr(oracle, "azp_adj_from_weight", bad)
+    return pin_azp_identity
+
+
+def _mut_residual_sign(monkeypatch):
+    orig = oquant.nvfp4_quantize
+    calls = {"n": 0}
+
+    def bad(x, g):
+        calls["n"] += 1
+        q, sf = orig(x, g)
+        return (q ^ 8, sf) if calls["n"] % 2 == 0 else (q, sf)
+
+    monkeypatch.setattr(oquant, "nvfp4_quantize", bad)
+    return pin_arc_residual_reduces_error
+
+
+def _mut_w8a8_transposed(monkeypatch):
+    monkeypatch.setattr(oracle, "int8_gemm_exact", lambda a, b: ogemm.int8_gemm_exact(a, b[:, ::-1]))
+    return pin_w8a8_example
+
+
+def _mut_w4_zero_dropped(monkeypatch):
+    orig = ogemm.w4a16_reference
+    monkeypatch.setattr(oracle, "w4a16_reference", lambda x, c, s, z, g=128: orig(x, c, s, None, g))
+    return pin_w4a16_brute_force
+
+
+def _mut_nvfp4_scale_not_decoded(monkeypatch):
+    monkeypatch.setattr(oquant, "_block_divisor", lambda sf, g: (sf.astype(np.float32) * np.float32(g)).astype(np.float32))
+    return pin_nvfp4_block
+
+
+def _mut_sym_qmax(monkeypatch):
+    orig = oquant.quant_sym_rows
+    monkeypatch.setattr(oracle, "quant_sym_rows", lambda x, qmax: orig(x, qmax + 1))
+    return pin_granularity
+
+
+MUTATIONS = [_mut_e2m1_ties_odd, _mut_azp_sign, _mut_azp_adj_axis, _mut_residual_sign,
+             _mut_w8a8_transposed, _mut_w4_zero_dropped, _mut_nvfp4_scale_not_decoded, _mut_sym_qmax]
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
+def test_planted_mistake_is_caught(monkeypatch, mutation):
+    pin = mutation(monkeypatch)
+    with pytest.raises(AssertionError):
+        pin()
