@@ -1,0 +1,269 @@
+/*
+ * qlin.h - C ABI of the GB300 (sm_103a) quantized linear layer library.
+ *
+ * Y = X . W^T with dequantization fused into the matrix product, in three
+ * forms:
+ *   - W4A16: group-wise (g = 128) unsigned 4-bit weights with fp16 scales and
+ *     4-bit zero-points, fp16 activations, fp16 output.
+ *   - W8A8: per-token int8 activations (symmetric, or asymmetric with an
+ *     integer zero-point), per-channel symmetric int8 weights, int32
+ *     accumulation, fused epilogue s_a . s_b . (D^ - azp . azp_adj) + bias.
+ *   - NVFP4 W4A4: E2M1 values in 16-element blocks with E4M3 block scales and
+ *     an fp32 per-tensor scale, optionally with ARCQuant residual channels
+ *     appended along K.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory: every pointer argument is a DEVICE pointer (cudaMalloc / a torch
+ *   CUDA tensor) unless stated otherwise.  The caller owns all memory.  The
+ *   library allocates nothing, keeps no pointer after it returns and has no
+ *   state except one device error word per device (see qlin_get_device_error).
+ * Layout: all matrices are row-major with dense rows (row pitch = number of
+ *   columns x element size).  W is [N][K] (nn.Linear.weight layout, K
+ *   contiguous); X and Y are [T][K] and [T][N].  4-bit codes are packed two
+ *   per byte along the row: element 2i in the low nibble of byte i.
+ * Alignment: every base pointer must be 16-byte aligned and every row pitch a
+ *   multiple of 16 bytes (checked; QLIN_ERR_ALIGNMENT otherwise).
+ * Streams: work is enqueued on `stream` (0 = legacy default stream).  No
+ *   entry point synchronizes, except qlin_get_device_error.
+ * Errors: arguments are checked on the host before anything is launched; a
+ *   failed check launches nothing.  A failed launch returns QLIN_ERR_CUDA.
+ *   Nothing is thrown across the ABI and nothing aborts.  The text of the last
+ *   failure on the calling thread is available from qlin_last_error_message.
+ * Device: the current device must be compute capability 10.3 (GB300);
+ *   anything else returns QLIN_ERR_UNSUPPORTED.
+ * Empty problems (T == 0 or N == 0) are valid and launch nothing.
+ *
+ * Sources: the method is restated from five web pages (a CUDA engineering
+ * book chapter on quantization kernels; "CUDA-Practice 07"; "LLM and AIGC
+ * quantization: from number formats to W4A4"; "vLLM W8A8 quantized GEMM:
+ * CUTLASS epilogue design"; "NVFP4 quantization and ARCQuant").  Each entry
+ * point cites the passage that defines its operation.
+ */
+#ifndef QLIN_H_
+#define QLIN_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QLIN_OK = 0,
+  QLIN_ERR_INVALID_ARG = 1, /* a size, pointer or option is out of range        */
+  QLIN_ERR_ALIGNMENT = 2,   /* a base pointer or row pitch is not 16-byte aligned */
+  QLIN_ERR_UNSUPPORTED = 3, /* wrong GPU, or an option this build does not cover */
+  QLIN_ERR_CUDA = 4,        /* a CUDA runtime call or a kernel launch failed     */
+  QLIN_ERR_TIMEOUT = 5      /* a kernel gave up a bounded wait (device error word) */
+} qlin_status;
+
+typedef enum {
+  QLIN_F16 = 0,
+  QLIN_BF16 = 1,
+  QLIN_F32 = 2,
+  QLIN_I32 = 3
+} qlin_dtype;
+
+typedef enum {
+  /* activations: append the NVFP4 re-quantized residual of the first S
+     (reordered) channels */
+  QLIN_NVFP4_RESIDUAL = 0,
+  /* weights: append a copy of the codes and scales of the first S
+     (reordered) channels */
+  QLIN_NVFP4_DUPLICATE = 1
+} qlin_nvfp4_mode;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* qlin_status_string(qlin_status status);
+
+/* Text of the last failure reported on the calling thread (static per-thread
+   storage; empty string if none). */
+const char* qlin_last_error_message(void);
+
+/* Library ABI version (major * 100 + minor). */
+int qlin_version(void);
+
+/* Reads and clears the device error word of the current device.  Kernels that
+   wait on barriers give up after a bounded time and record a nonzero code
+   there instead of hanging.  Synchronizes `stream` first.  *code_out (host
+   pointer, may be NULL) receives the raw code (0 = none).  Returns
+   QLIN_ERR_TIMEOUT if a code was set, QLIN_OK otherwise. */
+qlin_status qlin_get_device_error(cudaStream_t stream, int32_t* code_out);
+
+/* ------------------------------------------------------------------------
+ * a0 - W4A16 weight preparation (offline, at load time)
+ *
+ * Asymmetric unsigned 4-bit group quantization of W [N][K], one scale and one
+ * zero-point per `group` consecutive K elements of a row, following the AWQ
+ * offline flow ("LLM and AIGC quantization", AWQ section, pseudo_quant):
+ *   s = fp16( max(max_g w - min_g w, 1e-5) / 15 )   (float32 ops, RNE to fp16)
+ *   z = clamp(rint(-min_g w / s), 0, 15)
+ *   q = clamp(rint(w / s) + z, 0, 15)
+ * with s the fp16-rounded scale (the value dequantization uses).
+ *   w       [N][K] of w_dtype (F32, F16 or BF16)
+ *   group   128 (the only group size of this build; else QLIN_ERR_UNSUPPORTED)
+ *   wq      out, uint8 [N][K/2], packed codes
+ *   scales  out, fp16 [N][K/group]
+ *   zeros   out, uint8 [N][ceil(K/group / 2)], packed zero-points
+ * K must be a multiple of `group`; the zero-point and scale rows are dense
+ * (their row pitch need not be 16-byte aligned).
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_quant_w4_g128(const void* w, qlin_dtype w_dtype, int64_t N, int64_t K, int64_t group,
+                               uint8_t* wq, void* scales, uint8_t* zeros, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * a1 - W4A16 fused dequant GEMV / skinny GEMM
+ *
+ * Y[t,n] = sum_g s[n,g] . sum_{k in g} X[t,k] . (q[n,k] - z[n,g])
+ * ("Chapter 9 - Quantization kernels", section 9.5 dequant-fused GEMM and
+ * 9.6 INT4 unpack; "LLM and AIGC quantization", section W4A16).  The 4-bit
+ * codes are unpacked in registers with the zero-point folded into the
+ * conversion; products are exact and accumulate in fp32; the group scale is
+ * applied once per group in fp32; Y is rounded once to fp16.
+ *   x       fp16 [T][K]
+ *   wq      uint8 [N][K/2] packed codes (element 2i in the low nibble)
+ *   scales  fp16 [N][K/group]
+ *   zeros   uint8 [N][ceil(K/group / 2)] packed zero-points, or NULL meaning
+ *           the symmetric zero-point 8 for every group
+ *   group   128
+ *   y       out, fp16 [T][N]
+ * 1 <= T <= 64 (decode / skinny shapes), K a multiple of `group`.
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq,
+                            const void* scales, const uint8_t* zeros, int64_t group, void* y,
+                            cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * b1 - per-token int8 activation quantization
+ *
+ * Symmetric (azp == NULL): s_t = max_k |x| / 127 (s_t = 1 for an all-zero
+ *   row), q = clamp(rint(x / s_t), -127, 127)
+ *   ("LLM and AIGC quantization", symmetric quantization, q_max = 2^(b-1)-1;
+ *   per-token dynamic scales).
+ * Asymmetric (azp != NULL): mn = min(min_k x, 0), mx = max(max_k x, 0),
+ *   s_t = max(mx - mn, 1e-5) / 255, z_t = -128 - rint(mn / s_t),
+ *   q = clamp(rint(x / s_t) + z_t, -128, 127); dequantization is
+ *   s_t (q - z_t) ("vLLM W8A8 ... CUTLASS epilogue design", section 1:
+ *   A = s_a (A^ - J z_a)).
+ * All arithmetic is IEEE float32 division/subtraction, round-half-to-even.
+ * Also used per output channel for the W8A8 weights (rows = N).
+ *   x      [T][K] of x_dtype (F16, BF16 or F32)
+ *   q      out, int8 [T][K]
+ *   scale  out, float32 [T]
+ *   azp    out, int32 [T], or NULL for the symmetric form
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
+                                float* scale, int32_t* azp, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * a0 - W8A8 zero-point adjustment (offline, at load time)
+ *
+ * azp_adj[n] = sum_k B^[n,k]  (1 . B^, the per-output-channel sum of the int8
+ * weight codes; "vLLM W8A8 ... CUTLASS epilogue design", sections 2 and 5:
+ * it depends on the weights only and is computed once at load time).
+ *   b        int8 [N][K]
+ *   azp_adj  out, int32 [N]
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_int8_row_sum(const int8_t* b, int64_t N, int64_t K, int32_t* azp_adj, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * b2 + b3 - int8 GEMM with int32 accumulation and the fused epilogue
+ *
+ * D^ = A^ . B^^T (exact int32), then
+ *   out = s_a . s_b . (D^ - azp . azp_adj) + bias      (one final rounding)
+ * evaluated as float(D^ - azp . azp_adj) * s_b * s_a + bias in float32
+ * ("vLLM W8A8 ... CUTLASS epilogue design", sections 2.1-2.4 and 3; "LLM
+ * and AIGC quantization", W8A8 section).  The four epilogues:
+ *   ScaledEpilogue            azp == NULL, azp_adj == NULL, bias == NULL
+ *   ScaledEpilogueBias        azp == NULL, azp_adj == NULL, bias != NULL
+ *   ScaledEpilogueAzp         azp == NULL, azp_adj != NULL (azp_adj already
+ *                             holds z . (1 . B^), the per-tensor form)
+ *   ScaledEpilogueAzpPerToken azp != NULL, azp_adj != NULL
+ * A missing bias means 0.
+ *   a          int8 [T][K]   (per-token quantized activations)
+ *   b          int8 [N][K]   (per-channel symmetric weights)
+ *   scale_a    float32 [scale_a_numel], scale_a_numel 1 or T
+ *   scale_b    float32 [scale_b_numel], scale_b_numel 1 or N
+ *   azp        int32 [T] or NULL
+ *   azp_adj    int32 [N] or NULL (must be non-NULL when azp is non-NULL)
+ *   bias       [N] of bias_dtype (F16, BF16 or F32) or NULL
+ *   out        [T][N] of out_dtype: F16 or BF16; or I32, which writes the raw
+ *              accumulator D^ and ignores the epilogue arguments (test hook)
+ * K must be a multiple of 16.  GB300 has no int8 tensor-core MMA: the
+ * contraction runs on the bf16 tensor cores on exact bf16 copies of the int8
+ * codes, in K chunks whose partial sums are exact in fp32, converted to int32
+ * and added in int32, so D^ is bit-exact.
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_t N, int64_t K,
+                           const float* scale_a, int64_t scale_a_numel, const float* scale_b,
+                           int64_t scale_b_numel, const int32_t* azp, const int32_t* azp_adj,
+                           const void* bias, qlin_dtype bias_dtype, void* out, qlin_dtype out_dtype,
+                           cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * c0 - NVFP4 calibration helpers (offline / set-up)
+ *
+ * qlin_nvfp4_global_scale: g = max |x| / (6 . 448) over the whole tensor, the
+ *   per-tensor fp32 scale that puts every block scale in E4M3 range.
+ *   x [rows][K] of x_dtype; g out, float32 [1] (device).
+ * qlin_arc_perm: ARCQuant channel order ("NVFP4 quantization and ARCQuant",
+ *   section 2.1: channels reordered by descending magnitude): perm[i] = the
+ *   channel with the i-th largest max over rows of |x|, ties by ascending
+ *   channel index.  x [rows][K] of x_dtype; perm out, int32 [K].  K <= 16384.
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_nvfp4_global_scale(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, float* g,
+                                    cudaStream_t stream);
+qlin_status qlin_arc_perm(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, int32_t* perm,
+                          cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * c1 - NVFP4 quantization with ARCQuant residual channels
+ *
+ * Per row, over the reordered channels xs = x[:, perm] (perm NULL = identity),
+ * per 16-element block b ("LLM and AIGC quantization", block-scaled formats,
+ * the NVFP4 example; "NVFP4 quantization and ARCQuant", sections 2.1, 3.1):
+ *   sf_b = E4M3( (max_b |xs| / 6) / g )          (RNE, saturating at 448)
+ *   d_b  = dec(sf_b) . g
+ *   q    = E2M1( xs / d_b )                      (RNE ties-to-even; 0 if d_b == 0)
+ * then, for the first S reordered channels, columns K .. K+S-1 hold
+ *   mode RESIDUAL:  NVFP4 of r = xs - e2m1(q) . d_b (float32), same g
+ *   mode DUPLICATE: a copy of the codes and scales of columns 0 .. S-1
+ *   x      [rows][K] of x_dtype (F16, BF16 or F32)
+ *   perm   int32 [K] permutation of 0..K-1, or NULL
+ *   S      0 <= S <= K, a multiple of 16
+ *   g      float32 [1] device scalar
+ *   q      out, uint8 [rows][(K+S)/2]  packed E2M1 codes
+ *   sf     out, uint8 [rows][(K+S)/16] E4M3 block scales (row pitch need not
+ *          be 16-byte aligned)
+ * K must be a multiple of 32 (so packed rows are 16-byte aligned).
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const int32_t* perm,
+                             int64_t S, qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
+                             cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * c2 - NVFP4 block-scaled GEMM
+ *
+ * Y[t,n] = g_a . g_b . sum_b sfa[t,b] . sfb[n,b] . sum_{k in b} a[t,k] . b[n,k]
+ * over the (augmented) K, fp32 accumulation on the block-scaled fp4 tensor
+ * cores, one final rounding ("LLM and AIGC quantization", block-scaled
+ * formats: the tensor core applies the block scales during accumulation;
+ * "NVFP4 quantization and ARCQuant", section 2.2: Y ~ sX_aug QX_aug
+ * (sW_aug QW_aug)^T).
+ *   a, b      uint8 [T][K/2], [N][K/2]   packed E2M1 codes
+ *   sfa, sfb  uint8 [T][K/16], [N][K/16] E4M3 block scales (row-major)
+ *   g_a, g_b  float32 [1] device scalars
+ *   out       [T][N] of out_dtype (BF16 or F16)
+ * K must be a multiple of 64 (the tensor-core K step).
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,
+                            int64_t T, int64_t N, int64_t K, const float* g_a, const float* g_b, void* out,
+                            qlin_dtype out_dtype, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLIN_H_ */

@@ -1,0 +1,222 @@
+"""GB300-native quantized linear layer: thin Python binding of libqlin.so.
+
+Every function here has the name of a C entry point declared in
+include/qlin.h and does argument marshalling only: it reads sizes, dtypes
+and device pointers from torch tensors, passes them with the current CUDA
+stream, and raises QlinError on a non-OK status.  All computation happens in
+the library's CUDA kernels; there is no CPU or PyTorch fallback.  If the
+library has not been built, the first call raises.
+
+Outputs are caller-allocated tensors, exactly as in the C ABI.
+"""
+
+import ctypes
+import os
+
+from .buildlib import LIB_PATH, build  # noqa: F401
+
+__all__ = [
+    "QlinError", "lib", "build",
+    "QLIN_F16", "QLIN_BF16", "QLIN_F32", "QLIN_I32", "QLIN_NVFP4_RESIDUAL", "QLIN_NVFP4_DUPLICATE",
+    "qlin_version", "qlin_get_device_error",
+    "qlin_quant_w4_g128", "qlin_w4a16_gemm", "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm",
+    "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
+]
+
+QLIN_F16, QLIN_BF16, QLIN_F32, QLIN_I32 = 0, 1, 2, 3
+QLIN_NVFP4_RESIDUAL, QLIN_NVFP4_DUPLICATE = 0, 1
+
+_STATUS = {0: "QLIN_OK", 1: "QLIN_ERR_INVALID_ARG", 2: "QLIN_ERR_ALIGNMENT", 3: "QLIN_ERR_UNSUPPORTED",
+           4: "QLIN_ERR_CUDA", 5: "QLIN_ERR_TIMEOUT"}
+
+
+class QlinError(RuntimeError):
+    def __init__(self, status, fn, message):
+        self.status = status
+        super().__init__("%s failed: %s (%s)" % (fn, _STATUS.get(status, status), message))
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int
+_SIGS = {
+    "qlin_version": ([], ctypes.c_int),
+    "qlin_status_string": ([_I32], ctypes.c_char_p),
+    "qlin_last_error_message": ([], ctypes.c_char_p),
+    "qlin_get_device_error": ([_P, _P], _I32),
+    "qlin_quant_w4_g128": ([_P, _I32, _I64, _I64, _I64, _P, _P, _P, _P], _I32),
+    "qlin_w4a16_gemm": ([_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P], _I32),
+    "qlin_quant_act_int8": ([_P, _I32, _I64, _I64, _P, _P, _P, _P], _I32),
+    "qlin_int8_row_sum": ([_P, _I64, _I64, _P, _P], _I32),
+    "qlin_w8a8_gemm": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
+    "qlin_nvfp4_global_scale": ([_P, _I32, _I64, _I64, _P, _P], _I32),
+    "qlin_arc_perm": ([_P, _I32, _I64, _I64, _P, _P], _I32),
+    "qlin_quant_nvfp4": ([_P, _I32, _I64, _I64, _P, _I64, _I32, _P, _P, _P, _P], _I32),
+    "qlin_nvfp4_gemm": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P], _I32),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded libqlin.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libqlin.so is not built (run quantized_linear_layer_gb300.build())")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(h, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = h
+    return _lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    return {torch.float16: QLIN_F16, torch.bfloat16: QLIN_BF16, torch.float32: QLIN_F32,
+            torch.int32: QLIN_I32}[t.dtype]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, status):
+    if status != 0:
+        msg = lib().qlin_last_error_message().decode(errors="replace")
+        raise QlinError(status, fn, msg)
+
+
+def _need(t, *dtypes, contiguous=True, name="tensor"):
+    if t is None:
+        return
+    if t.dtype not in dtypes:
+        raise TypeError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtypes))
+    if contiguous and not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+
+
+def qlin_version():
+    return lib().qlin_version()
+
+
+def qlin_get_device_error(stream=None):
+    """Reads and clears the device error word; returns the raw code (0 = none)."""
+    code = ctypes.c_int32(0)
+    st = lib().qlin_get_device_error(_stream(stream), ctypes.byref(code))
+    if st not in (0, 5):
+        _check("qlin_get_device_error", st)
+    return code.value
+
+
+def qlin_quant_w4_g128(w, wq, scales, zeros, group=128, stream=None):
+    """W [N][K] -> packed codes wq uint8 [N][K/2], fp16 scales [N][K/g], packed zeros uint8 [N][ceil(K/g/2)]."""
+    torch = _torch()
+    _need(w, torch.float32, torch.float16, torch.bfloat16, name="w")
+    _need(wq, torch.uint8, name="wq"); _need(scales, torch.float16, name="scales"); _need(zeros, torch.uint8, name="zeros")
+    n, k = w.shape
+    _check("qlin_quant_w4_g128", lib().qlin_quant_w4_g128(_ptr(w), _dtype_code(w), n, k, group, _ptr(wq),
+                                                         _ptr(scales), _ptr(zeros), _stream(stream)))
+
+
+def qlin_w4a16_gemm(x, wq, scales, zeros, y, group=128, stream=None):
+    """y[T][N] = x[T][K] . dequant(wq, scales, zeros)^T (zeros None = symmetric, z = 8)."""
+    torch = _torch()
+    _need(x, torch.float16, name="x"); _need(wq, torch.uint8, name="wq"); _need(scales, torch.float16, name="scales")
+    _need(zeros, torch.uint8, name="zeros"); _need(y, torch.float16, name="y")
+    t, k = x.shape
+    n = wq.shape[0]
+    _check("qlin_w4a16_gemm", lib().qlin_w4a16_gemm(_ptr(x), t, n, k, _ptr(wq), _ptr(scales), _ptr(zeros), group,
+                                                   _ptr(y), _stream(stream)))
+
+
+def qlin_quant_act_int8(x, q, scale, azp=None, stream=None):
+    """Per-row int8 quantization of x [T][K]; azp None = symmetric."""
+    torch = _torch()
+    _need(x, torch.float16, torch.bfloat16, torch.float32, name="x"); _need(q, torch.int8, name="q")
+    _need(scale, torch.float32, name="scale"); _need(azp, torch.int32, name="azp")
+    t, k = x.shape
+    _check("qlin_quant_act_int8", lib().qlin_quant_act_int8(_ptr(x), _dtype_code(x), t, k, _ptr(q), _ptr(scale),
+                                                           _ptr(azp), _stream(stream)))
+
+
+def qlin_int8_row_sum(b, azp_adj, stream=None):
+    """azp_adj[n] = sum_k b[n, k] for int8 b [N][K]."""
+    torch = _torch()
+    _need(b, torch.int8, name="b"); _need(azp_adj, torch.int32, name="azp_adj")
+    n, k = b.shape
+    _check("qlin_int8_row_sum", lib().qlin_int8_row_sum(_ptr(b), n, k, _ptr(azp_adj), _stream(stream)))
+
+
+def qlin_w8a8_gemm(a, b, scale_a, scale_b, out, azp=None, azp_adj=None, bias=None, stream=None):
+    """out = s_a s_b (a . b^T - azp azp_adj) + bias; out int32 gives the raw accumulator."""
+    torch = _torch()
+    _need(a, torch.int8, name="a"); _need(b, torch.int8, name="b")
+    _need(scale_a, torch.float32, name="scale_a"); _need(scale_b, torch.float32, name="scale_b")
+    _need(azp, torch.int32, name="azp"); _need(azp_adj, torch.int32, name="azp_adj")
+    _need(bias, torch.float16, torch.bfloat16, torch.float32, name="bias")
+    _need(out, torch.float16, torch.bfloat16, torch.int32, name="out")
+    t, k = a.shape
+    n = b.shape[0]
+    sa_n = 0 if scale_a is None else scale_a.numel()
+    sb_n = 0 if scale_b is None else scale_b.numel()
+    bias_dt = QLIN_F16 if bias is None else _dtype_code(bias)
+    _check("qlin_w8a8_gemm", lib().qlin_w8a8_gemm(_ptr(a), _ptr(b), t, n, k, _ptr(scale_a), sa_n, _ptr(scale_b), sb_n,
+                                                 _ptr(azp), _ptr(azp_adj), _ptr(bias), bias_dt, _ptr(out),
+                                                 _dtype_code(out), _stream(stream)))
+
+
+def qlin_nvfp4_global_scale(x, g, stream=None):
+    """g[0] = max|x| / (6 * 448)."""
+    torch = _torch()
+    _need(x, torch.float16, torch.bfloat16, torch.float32, name="x"); _need(g, torch.float32, name="g")
+    rows, k = x.shape
+    _check("qlin_nvfp4_global_scale", lib().qlin_nvfp4_global_scale(_ptr(x), _dtype_code(x), rows, k, _ptr(g),
+                                                                   _stream(stream)))
+
+
+def qlin_arc_perm(x, perm, stream=None):
+    """perm = channels by descending max|x| over rows (ties: lower index first)."""
+    torch = _torch()
+    _need(x, torch.float16, torch.bfloat16, torch.float32, name="x"); _need(perm, torch.int32, name="perm")
+    rows, k = x.shape
+    _check("qlin_arc_perm", lib().qlin_arc_perm(_ptr(x), _dtype_code(x), rows, k, _ptr(perm), _stream(stream)))
+
+
+def qlin_quant_nvfp4(x, g, q, sf, perm=None, S=0, mode=QLIN_NVFP4_RESIDUAL, stream=None):
+    """NVFP4 codes q uint8 [rows][(K+S)/2] and E4M3 scales sf uint8 [rows][(K+S)/16]."""
+    torch = _torch()
+    _need(x, torch.float16, torch.bfloat16, torch.float32, name="x"); _need(g, torch.float32, name="g")
+    _need(q, torch.uint8, name="q"); _need(sf, torch.uint8, name="sf"); _need(perm, torch.int32, name="perm")
+    rows, k = x.shape
+    _check("qlin_quant_nvfp4", lib().qlin_quant_nvfp4(_ptr(x), _dtype_code(x), rows, k, _ptr(perm), S, mode, _ptr(g),
+                                                     _ptr(q), _ptr(sf), _stream(stream)))
+
+
+def qlin_nvfp4_gemm(a, sfa, b, sfb, g_a, g_b, out, stream=None):
+    """out[T][N] = g_a g_b (dequant(a, sfa) . dequant(b, sfb)^T)."""
+    torch = _torch()
+    for t_, nm in ((a, "a"), (sfa, "sfa"), (b, "b"), (sfb, "sfb")):
+        _need(t_, torch.uint8, name=nm)
+    _need(g_a, torch.float32, name="g_a"); _need(g_b, torch.float32, name="g_b")
+    _need(out, torch.bfloat16, torch.float16, name="out")
+    t = a.shape[0]
+    k = a.shape[1] * 2
+    n = b.shape[0]
+    _check("qlin_nvfp4_gemm", lib().qlin_nvfp4_gemm(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), t, n, k, _ptr(g_a),
+                                                   _ptr(g_b), _ptr(out), _dtype_code(out), _stream(stream)))

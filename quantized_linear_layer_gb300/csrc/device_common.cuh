@@ -1,0 +1,114 @@
+// Device-side helpers shared by the kernels: vector loads, element loads of
+// the supported input dtypes, warp reductions, and the device error word.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace qlin {
+
+// Error codes recorded in the device error word (first one wins).
+enum : int32_t {
+  kDevErrNone = 0,
+  kDevErrTimeoutBase = 0x1000,  // + site id: a bounded barrier wait expired
+  kDevErrBadIndex = 0x2000,     // an index argument (e.g. a channel permutation) was out of range
+};
+
+__device__ __forceinline__ void record_device_error(int32_t* err, int32_t code) {
+  if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+// 16-byte read-only load that does not allocate in L1 (streamed weights).
+__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// 16-byte read-only load through L1 (small operands reused across warps).
+__device__ __forceinline__ uint4 ldg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Eight consecutive input elements of the given dtype, widened to float32
+// (exact for fp16 and bf16).  `p` must be 16-byte aligned for F16/BF16 and
+// 32-byte aligned (two 16-byte loads) for F32.
+template <int DT>
+struct Vec8Loader;
+
+template <>
+struct Vec8Loader<0> {  // F16
+  static __device__ __forceinline__ void load(const void* p, float* v) {
+    uint4 u = ldg_v4(p);
+    const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = __half22float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+};
+
+template <>
+struct Vec8Loader<1> {  // BF16
+  static __device__ __forceinline__ void load(const void* p, float* v) {
+    uint4 u = ldg_v4(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+};
+
+template <>
+struct Vec8Loader<2> {  // F32
+  static __device__ __forceinline__ void load(const void* p, float* v) {
+    uint4 a = ldg_v4(p);
+    uint4 b = ldg_v4(static_cast<const char*>(p) + 16);
+    v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+    v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+    v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+    v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+  }
+};
+
+// One element of the given dtype as float32.
+template <int DT>
+__device__ __forceinline__ float load_elem(const void* base, int64_t i) {
+  if constexpr (DT == 0) return __half2float(static_cast<const __half*>(base)[i]);
+  else if constexpr (DT == 1) return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]);
+  else return static_cast<const float*>(base)[i];
+}
+
+template <int DT>
+__host__ __device__ constexpr int elem_bytes() { return DT == 2 ? 4 : 2; }
+
+}  // namespace qlin

@@ -1,0 +1,297 @@
+// NVFP4 quantization with ARCQuant residual channels, and its two set-up
+// helpers (per-tensor scale, channel order).
+//
+// Per 16-element block b of a row of the reordered channels xs = x[:, perm]
+// ("LLM and AIGC quantization: from number formats to W4A4", block-scaled
+// formats, the 16-element NVFP4 example; "NVFP4 quantization and ARCQuant",
+// sections 2.1 and 3.1):
+//   sf_b = E4M3( (max_b |xs| / 6) / g )     round-to-nearest-even, saturating
+//   d_b  = dec(sf_b) . g
+//   q    = E2M1( xs / d_b )                 round-to-nearest-even, saturating
+// The first S reordered channels then get, in columns K .. K+S-1, either the
+// NVFP4 re-quantization of the residual r = xs - e2m1(q) . d_b (activations)
+// or a copy of their codes and scales (weights: "copy rather than compute").
+//
+// Every rounding decision is taken in IEEE float32 as written (true division,
+// separate multiply and subtract); the E4M3 and E2M1 encodes use the
+// hardware's round-to-nearest-even saturating conversions.
+#include <type_traits>
+
+#include "device_common.cuh"
+#include "qlin_internal.h"
+
+namespace qlin {
+namespace {
+
+constexpr int kNvThreads = 256;
+
+__device__ __forceinline__ uint32_t f32_to_e4m3(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+  return r & 0xFFu;
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  uint32_t h2;
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(code));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// Two floats -> one byte of two E2M1 codes, `lo` in bits 0-3, `hi` in 4-7.
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// One byte of two E2M1 codes -> the two values (low nibble first).
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
+  uint32_t h2;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h2) : "r"(byte));
+  const __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
+// Quantize one 16-element block; returns the scale code, writes 8 code bytes.
+__device__ __forceinline__ uint32_t quant_block16(const float* v, float g, uint32_t* packed /*[2]*/, float* d_out) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const float scaled = (amax == 0.0f) ? 0.0f : __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+  const uint32_t sfc = f32_to_e4m3(scaled);
+  const float d = __fmul_rn(e4m3_to_f32(sfc), g);
+  packed[0] = 0u;
+  packed[1] = 0u;
+  if (d != 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t byte = f32x2_to_e2m1x2(__fdiv_rn(v[2 * i], d), __fdiv_rn(v[2 * i + 1], d));
+      packed[i >> 2] |= byte << (8 * (i & 3));
+    }
+  }
+  *d_out = d;
+  return sfc;
+}
+
+// One CTA per row: the row is staged in shared memory in its input dtype,
+// then each thread quantizes 16-element blocks of the reordered row.
+template <int DT>
+__global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __restrict__ x, int K,
+                                                                  const int32_t* __restrict__ perm, int S,
+                                                                  int mode, const float* __restrict__ gp,
+                                                                  uint8_t* __restrict__ q,
+                                                                  uint8_t* __restrict__ sf,
+                                                                  int32_t* __restrict__ err) {
+  extern __shared__ __align__(16) unsigned char row_smem[];
+  const int64_t row = blockIdx.x;
+  const int tid = threadIdx.x;
+  constexpr int EB = elem_bytes<DT>();
+  const char* xr = static_cast<const char*>(x) + row * (int64_t)K * EB;
+  const int row_bytes = K * EB;
+  for (int off = tid * 16; off < row_bytes; off += kNvThreads * 16)
+    *reinterpret_cast<uint4*>(row_smem + off) = ldg_v4(xr + off);
+  __syncthreads();
+
+  const float g = __ldg(gp);
+  const int Kaug = K + S;
+  uint8_t* qr = q + row * (int64_t)(Kaug / 2);
+  uint8_t* sfr = sf + row * (int64_t)(Kaug / 16);
+  const int nblk = K / 16;
+  const int sblk = S / 16;
+  // A channel index outside [0, K) is recorded in the device error word and
+  // read as channel 0, so the shared-memory gather stays in bounds.
+  auto channel = [&](int p) -> int {
+    if (static_cast<unsigned>(p) >= static_cast<unsigned>(K)) {
+      record_device_error(err, kDevErrBadIndex);
+      return 0;
+    }
+    return p;
+  };
+  for (int b = tid; b < nblk; b += kNvThreads) {
+    float v[16];
+    if (perm != nullptr) {
+      const int4* pp = reinterpret_cast<const int4*>(perm + b * 16);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int4 p4 = __ldg(pp + i);
+        v[4 * i + 0] = load_elem<DT>(row_smem, channel(p4.x));
+        v[4 * i + 1] = load_elem<DT>(row_smem, channel(p4.y));
+        v[4 * i + 2] = load_elem<DT>(row_smem, channel(p4.z));
+        v[4 * i + 3] = load_elem<DT>(row_smem, channel(p4.w));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = load_elem<DT>(row_smem, b * 16 + i);
+    }
+    uint32_t packed[2];
+    float d;
+    const uint32_t sfc = quant_block16(v, g, packed, &d);
+    *reinterpret_cast<uint2*>(qr + b * 8) = make_uint2(packed[0], packed[1]);
+    sfr[b] = static_cast<uint8_t>(sfc);
+    if (b < sblk) {
+      if (mode == QLIN_NVFP4_DUPLICATE) {
+        *reinterpret_cast<uint2*>(qr + (K / 2) + b * 8) = make_uint2(packed[0], packed[1]);
+        sfr[nblk + b] = static_cast<uint8_t>(sfc);
+      } else {
+        // residual r = x - e2m1(q) * d, one float32 multiply then one subtract
+        float r[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 e = e2m1x2_to_f32x2((packed[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+          r[2 * i] = __fsub_rn(v[2 * i], __fmul_rn(e.x, d));
+          r[2 * i + 1] = __fsub_rn(v[2 * i + 1], __fmul_rn(e.y, d));
+        }
+        uint32_t rp[2];
+        float rd;
+        const uint32_t rsf = quant_block16(r, g, rp, &rd);
+        *reinterpret_cast<uint2*>(qr + (K / 2) + b * 8) = make_uint2(rp[0], rp[1]);
+        sfr[nblk + b] = static_cast<uint8_t>(rsf);
+      }
+    }
+  }
+}
+
+// max |x| over the tensor into the bits of *g (non-negative floats order like
+// their bit patterns); *g must be zero beforehand.
+template <int DT>
+__global__ void absmax_bits_kernel(const void* __restrict__ x, int64_t nvec, unsigned int* __restrict__ out) {
+  float m = 0.0f;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
+    float v[8];
+    Vec8Loader<DT>::load(static_cast<const char*>(x) + i * 8 * elem_bytes<DT>(), v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+  }
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(m));
+}
+
+__global__ void global_scale_finish_kernel(float* g) {
+  *g = __fdiv_rn(*g, 2688.0f);  // 6 * 448
+}
+
+// Column maxima of |x| into the bits of perm[k]; perm must be zero beforehand.
+// Thread handles 8 consecutive columns over a slice of rows.
+template <int DT>
+__global__ void col_absmax_kernel(const void* __restrict__ x, int64_t rows, int K, int rows_per_cta,
+                                  unsigned int* __restrict__ out) {
+  const int vec = blockIdx.x * blockDim.x + threadIdx.x;
+  if (vec * 8 >= K) return;
+  const int64_t r0 = (int64_t)blockIdx.y * rows_per_cta;
+  const int64_t r1 = min(rows, r0 + rows_per_cta);
+  float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int64_t r = r0; r < r1; ++r) {
+    float v[8];
+    Vec8Loader<DT>::load(static_cast<const char*>(x) + (r * K + (int64_t)vec * 8) * elem_bytes<DT>(), v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m[j] = fmaxf(m[j], fabsf(v[j]));
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) atomicMax(out + vec * 8 + j, __float_as_uint(m[j]));
+}
+
+// Single-CTA bitonic sort of (statistic, channel) keys: ascending order of
+// (~bits << 32 | channel) is descending statistic with ties by channel.
+__global__ void __launch_bounds__(1024) perm_sort_kernel(int32_t* __restrict__ perm, int K, int n_pow2) {
+  extern __shared__ unsigned long long keys[];
+  for (int i = threadIdx.x; i < n_pow2; i += blockDim.x) {
+    keys[i] = (i < K) ? ((static_cast<unsigned long long>(~static_cast<unsigned int>(perm[i])) << 32) |
+                         static_cast<unsigned int>(i))
+                      : ~0ull;
+  }
+  __syncthreads();
+  for (int size = 2; size <= n_pow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n_pow2; i += blockDim.x) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool up = (i & size) == 0;
+          const unsigned long long a = keys[i], b = keys[j];
+          if ((a > b) == up) { keys[i] = b; keys[j] = a; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < K; i += blockDim.x) perm[i] = static_cast<int32_t>(keys[i] & 0xFFFFFFFFull);
+}
+
+template <typename F>
+cudaError_t dispatch_dtype(qlin_dtype dt, F&& f) {
+  switch (dt) {
+    case QLIN_F16: return f(std::integral_constant<int, 0>{});
+    case QLIN_BF16: return f(std::integral_constant<int, 1>{});
+    default: return f(std::integral_constant<int, 2>{});
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const int32_t* perm,
+                               int64_t S, qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
+                               cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  return dispatch_dtype(x_dtype, [&](auto dt) -> cudaError_t {
+    constexpr int DT = decltype(dt)::value;
+    const size_t smem = static_cast<size_t>(K) * elem_bytes<DT>();
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(nvfp4_quant_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    nvfp4_quant_kernel<DT><<<static_cast<unsigned>(rows), kNvThreads, smem, stream>>>(
+        x, static_cast<int>(K), perm, static_cast<int>(S), static_cast<int>(mode), g, q, sf, device_error_word());
+    return cudaGetLastError();
+  });
+}
+
+cudaError_t launch_nvfp4_global_scale(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, float* g,
+                                      cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(g, 0, sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  const int64_t nvec = rows * K / 8;
+  if (nvec > 0) {
+    e = dispatch_dtype(x_dtype, [&](auto dt) -> cudaError_t {
+      constexpr int DT = decltype(dt)::value;
+      int64_t blocks = (nvec + 255) / 256;
+      const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+      if (blocks > cap) blocks = cap;
+      absmax_bits_kernel<DT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+          x, nvec, reinterpret_cast<unsigned int*>(g));
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return e;
+  }
+  global_scale_finish_kernel<<<1, 1, 0, stream>>>(g);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_arc_perm(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, int32_t* perm,
+                            cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(perm, 0, sizeof(int32_t) * K, stream);
+  if (e != cudaSuccess) return e;
+  if (rows > 0) {
+    e = dispatch_dtype(x_dtype, [&](auto dt) -> cudaError_t {
+      constexpr int DT = decltype(dt)::value;
+      const int vecs = static_cast<int>(K / 8);
+      const int threads = 128;
+      const int rows_per_cta = 64;
+      dim3 grid((vecs + threads - 1) / threads, static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta));
+      col_absmax_kernel<DT><<<grid, threads, 0, stream>>>(x, rows, static_cast<int>(K), rows_per_cta,
+                                                          reinterpret_cast<unsigned int*>(perm));
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return e;
+  }
+  int n = 1;
+  while (n < K) n <<= 1;
+  const size_t smem = sizeof(unsigned long long) * n;
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(perm_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  perm_sort_kernel<<<1, 1024, smem, stream>>>(perm, static_cast<int>(K), n);
+  return cudaGetLastError();
+}
+
+}  // namespace qlin

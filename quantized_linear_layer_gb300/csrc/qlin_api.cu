@@ -1,0 +1,325 @@
+// The C ABI of the library: argument checks, status codes, the per-device
+// error word, and dispatch to the kernel launchers.  Host code only.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "qlin_internal.h"
+
+namespace qlin {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+thread_local char g_last_error[512] = {0};
+
+qlin_status fail(qlin_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+qlin_status ok() {
+  g_last_error[0] = '\0';
+  return QLIN_OK;
+}
+
+qlin_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(QLIN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+  bool probed = false;
+  bool supported = false;
+  int sm_count = 0;
+  int32_t* err_word = nullptr;
+};
+
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_device_mutex;
+
+// The per-device error word lives in this translation unit.
+__device__ int32_t g_device_error_word;
+
+qlin_status probe_current_device(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(QLIN_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_device_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.supported = (major == 10 && minor == 3);
+    d.sm_count = sms;
+    if (d.supported) {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_device_error_word)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+      d.err_word = static_cast<int32_t*>(p);
+    }
+    d.probed = true;
+  }
+  if (!d.supported) return fail(QLIN_ERR_UNSUPPORTED, "device %d is not compute capability 10.3 (GB300)", dev);
+  *out = &d;
+  return QLIN_OK;
+}
+
+DeviceInfo* current_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  return &g_devices[dev];
+}
+
+bool is_float_dtype(qlin_dtype d) { return d == QLIN_F16 || d == QLIN_BF16 || d == QLIN_F32; }
+int64_t dtype_bytes(qlin_dtype d) { return d == QLIN_F32 || d == QLIN_I32 ? 4 : 2; }
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+}  // namespace
+
+int32_t* device_error_word() {
+  DeviceInfo* d = current_info();
+  return d != nullptr ? d->err_word : nullptr;
+}
+
+int sm_count() {
+  DeviceInfo* d = current_info();
+  return (d != nullptr && d->sm_count > 0) ? d->sm_count : 152;
+}
+
+}  // namespace qlin
+
+using namespace qlin;
+
+#define QLIN_REQUIRE(cond, status, ...) \
+  do {                                  \
+    if (!(cond)) return fail(status, __VA_ARGS__); \
+  } while (0)
+
+#define QLIN_DEVICE()                          \
+  do {                                         \
+    DeviceInfo* info_ = nullptr;               \
+    qlin_status st_ = probe_current_device(&info_); \
+    if (st_ != QLIN_OK) return st_;            \
+  } while (0)
+
+#define QLIN_LAUNCH(expr, what)                       \
+  do {                                                \
+    cudaError_t e_ = (expr);                          \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    return ok();                                      \
+  } while (0)
+
+extern "C" {
+
+const char* qlin_status_string(qlin_status status) {
+  switch (status) {
+    case QLIN_OK: return "QLIN_OK";
+    case QLIN_ERR_INVALID_ARG: return "QLIN_ERR_INVALID_ARG";
+    case QLIN_ERR_ALIGNMENT: return "QLIN_ERR_ALIGNMENT";
+    case QLIN_ERR_UNSUPPORTED: return "QLIN_ERR_UNSUPPORTED";
+    case QLIN_ERR_CUDA: return "QLIN_ERR_CUDA";
+    case QLIN_ERR_TIMEOUT: return "QLIN_ERR_TIMEOUT";
+  }
+  return "QLIN_ERR_UNKNOWN";
+}
+
+const char* qlin_last_error_message(void) { return g_last_error; }
+
+int qlin_version(void) { return 100; }
+
+qlin_status qlin_get_device_error(cudaStream_t stream, int32_t* code_out) {
+  DeviceInfo* info = nullptr;
+  qlin_status st = probe_current_device(&info);
+  if (st != QLIN_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int32_t code = 0;
+  if ((e = cudaMemcpy(&code, info->err_word, sizeof(code), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read device error word");
+  if (code != 0) {
+    const int32_t zero = 0;
+    if ((e = cudaMemcpy(info->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "clear device error word");
+  }
+  if (code_out != nullptr) *code_out = code;
+  if (code != 0) return fail(QLIN_ERR_TIMEOUT, "device error word was 0x%x", code);
+  return ok();
+}
+
+qlin_status qlin_quant_w4_g128(const void* w, qlin_dtype w_dtype, int64_t N, int64_t K, int64_t group,
+                               uint8_t* wq, void* scales, uint8_t* zeros, cudaStream_t stream) {
+  QLIN_REQUIRE(group == 128, QLIN_ERR_UNSUPPORTED, "group size %lld (only 128 is built)", (long long)group);
+  QLIN_REQUIRE(is_float_dtype(w_dtype), QLIN_ERR_INVALID_ARG, "w_dtype must be F16, BF16 or F32");
+  QLIN_REQUIRE(N >= 0 && N <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad sizes N=%lld K=%lld",
+               (long long)N, (long long)K);
+  QLIN_REQUIRE(K % group == 0, QLIN_ERR_INVALID_ARG, "K=%lld is not a multiple of the group size", (long long)K);
+  if (N == 0) return ok();
+  QLIN_REQUIRE(w && wq && scales && zeros, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(w) && aligned16(wq), QLIN_ERR_ALIGNMENT, "w and wq must be 16-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(scales) & 1u) == 0, QLIN_ERR_ALIGNMENT, "scales must be 2-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_quant_w4_g128(w, w_dtype, N, K, wq, scales, zeros, stream), "quant_w4_g128 launch");
+}
+
+qlin_status qlin_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq,
+                            const void* scales, const uint8_t* zeros, int64_t group, void* y,
+                            cudaStream_t stream) {
+  QLIN_REQUIRE(group == 128, QLIN_ERR_UNSUPPORTED, "group size %lld (only 128 is built)", (long long)group);
+  QLIN_REQUIRE(T >= 0 && T <= 64, QLIN_ERR_INVALID_ARG, "T=%lld outside [0, 64]", (long long)T);
+  QLIN_REQUIRE(N >= 0 && N <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad sizes N=%lld K=%lld",
+               (long long)N, (long long)K);
+  QLIN_REQUIRE(K % group == 0, QLIN_ERR_INVALID_ARG, "K=%lld is not a multiple of the group size", (long long)K);
+  if (T == 0 || N == 0) return ok();
+  QLIN_REQUIRE(x && wq && scales && y, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(x) && aligned16(wq), QLIN_ERR_ALIGNMENT, "x and wq must be 16-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(scales) & 1u) == 0 && (reinterpret_cast<uintptr_t>(y) & 1u) == 0,
+               QLIN_ERR_ALIGNMENT, "scales and y must be 2-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_w4a16_gemm(x, T, N, K, wq, scales, zeros, y, stream), "w4a16_gemm launch");
+}
+
+qlin_status qlin_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
+                                float* scale, int32_t* azp, cudaStream_t stream) {
+  QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");
+  QLIN_REQUIRE(T >= 0 && T <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad sizes T=%lld K=%lld",
+               (long long)T, (long long)K);
+  QLIN_REQUIRE(K % 16 == 0, QLIN_ERR_ALIGNMENT, "K=%lld is not a multiple of 16", (long long)K);
+  if (T == 0) return ok();
+  QLIN_REQUIRE(x && q && scale, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(x) && aligned16(q), QLIN_ERR_ALIGNMENT, "x and q must be 16-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(scale) & 3u) == 0 && (reinterpret_cast<uintptr_t>(azp) & 3u) == 0,
+               QLIN_ERR_ALIGNMENT, "scale and azp must be 4-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_quant_act_int8(x, x_dtype, T, K, q, scale, azp, stream), "quant_act_int8 launch");
+}
+
+qlin_status qlin_int8_row_sum(const int8_t* b, int64_t N, int64_t K, int32_t* azp_adj, cudaStream_t stream) {
+  QLIN_REQUIRE(N >= 0 && N <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad sizes N=%lld K=%lld",
+               (long long)N, (long long)K);
+  QLIN_REQUIRE(K % 16 == 0, QLIN_ERR_ALIGNMENT, "K=%lld is not a multiple of 16", (long long)K);
+  if (N == 0) return ok();
+  QLIN_REQUIRE(b && azp_adj, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(b), QLIN_ERR_ALIGNMENT, "b must be 16-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(azp_adj) & 3u) == 0, QLIN_ERR_ALIGNMENT, "azp_adj must be 4-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_int8_row_sum(b, N, K, azp_adj, stream), "int8_row_sum launch");
+}
+
+qlin_status qlin_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_t N, int64_t K,
+                           const float* scale_a, int64_t scale_a_numel, const float* scale_b,
+                           int64_t scale_b_numel, const int32_t* azp, const int32_t* azp_adj,
+                           const void* bias, qlin_dtype bias_dtype, void* out, qlin_dtype out_dtype,
+                           cudaStream_t stream) {
+  QLIN_REQUIRE(T >= 0 && T <= kMaxDim && N >= 0 && N <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG,
+               "bad sizes T=%lld N=%lld K=%lld", (long long)T, (long long)N, (long long)K);
+  QLIN_REQUIRE(K % 16 == 0, QLIN_ERR_ALIGNMENT, "K=%lld is not a multiple of 16", (long long)K);
+  QLIN_REQUIRE(out_dtype == QLIN_F16 || out_dtype == QLIN_BF16 || out_dtype == QLIN_I32, QLIN_ERR_INVALID_ARG,
+               "out_dtype must be F16, BF16 or I32");
+  const bool raw = out_dtype == QLIN_I32;
+  if (!raw) {
+    QLIN_REQUIRE(scale_a_numel == 1 || scale_a_numel == T, QLIN_ERR_INVALID_ARG,
+                 "scale_a_numel=%lld must be 1 or T", (long long)scale_a_numel);
+    QLIN_REQUIRE(scale_b_numel == 1 || scale_b_numel == N, QLIN_ERR_INVALID_ARG,
+                 "scale_b_numel=%lld must be 1 or N", (long long)scale_b_numel);
+    QLIN_REQUIRE(azp == nullptr || azp_adj != nullptr, QLIN_ERR_INVALID_ARG,
+                 "per-token azp needs azp_adj (the per-channel sum of the weight codes)");
+    QLIN_REQUIRE(bias == nullptr || is_float_dtype(bias_dtype), QLIN_ERR_INVALID_ARG,
+                 "bias_dtype must be F16, BF16 or F32");
+  }
+  if (T == 0 || N == 0) return ok();
+  QLIN_REQUIRE(a && b && out, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(raw || (scale_a && scale_b), QLIN_ERR_INVALID_ARG, "null scale pointer");
+  QLIN_REQUIRE(aligned16(a) && aligned16(b) && aligned16(out), QLIN_ERR_ALIGNMENT,
+               "a, b and out must be 16-byte aligned");
+  QLIN_REQUIRE((N * dtype_bytes(out_dtype)) % 16 == 0, QLIN_ERR_ALIGNMENT,
+               "the out row pitch (N x element size) must be a multiple of 16 bytes");
+  QLIN_DEVICE();
+  W8A8Epilogue epi;
+  epi.scale_a = scale_a;
+  epi.scale_a_per_row = scale_a_numel != 1;
+  epi.scale_b = scale_b;
+  epi.scale_b_per_col = scale_b_numel != 1;
+  epi.azp = raw ? nullptr : azp;
+  epi.azp_adj = raw ? nullptr : azp_adj;
+  epi.bias = raw ? nullptr : bias;
+  epi.bias_dtype = bias_dtype;
+  epi.out_dtype = out_dtype;
+  QLIN_LAUNCH(launch_w8a8_gemm(a, b, T, N, K, epi, out, stream), "w8a8_gemm launch");
+}
+
+qlin_status qlin_nvfp4_global_scale(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, float* g,
+                                    cudaStream_t stream) {
+  QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");
+  QLIN_REQUIRE(rows >= 0 && K > 0 && rows * K / K == rows, QLIN_ERR_INVALID_ARG, "bad sizes");
+  QLIN_REQUIRE(K % 16 == 0, QLIN_ERR_ALIGNMENT, "K=%lld is not a multiple of 16", (long long)K);
+  QLIN_REQUIRE(g != nullptr && (rows == 0 || x != nullptr), QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(x) && (reinterpret_cast<uintptr_t>(g) & 3u) == 0, QLIN_ERR_ALIGNMENT,
+               "x must be 16-byte aligned and g 4-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_nvfp4_global_scale(x, x_dtype, rows, K, g, stream), "nvfp4_global_scale launch");
+}
+
+qlin_status qlin_arc_perm(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, int32_t* perm,
+                          cudaStream_t stream) {
+  QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");
+  QLIN_REQUIRE(rows >= 0 && rows <= kMaxDim && K > 0 && K <= 16384, QLIN_ERR_INVALID_ARG,
+               "bad sizes rows=%lld K=%lld (K <= 16384)", (long long)rows, (long long)K);
+  QLIN_REQUIRE(K % 16 == 0, QLIN_ERR_ALIGNMENT, "K=%lld is not a multiple of 16", (long long)K);
+  QLIN_REQUIRE(perm != nullptr && (rows == 0 || x != nullptr), QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(x) && aligned16(perm), QLIN_ERR_ALIGNMENT, "x and perm must be 16-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_arc_perm(x, x_dtype, rows, K, perm, stream), "arc_perm launch");
+}
+
+qlin_status qlin_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const int32_t* perm,
+                             int64_t S, qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
+                             cudaStream_t stream) {
+  QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");
+  QLIN_REQUIRE(mode == QLIN_NVFP4_RESIDUAL || mode == QLIN_NVFP4_DUPLICATE, QLIN_ERR_INVALID_ARG, "bad mode");
+  QLIN_REQUIRE(rows >= 0 && rows <= kMaxDim && K > 0, QLIN_ERR_INVALID_ARG, "bad sizes rows=%lld K=%lld",
+               (long long)rows, (long long)K);
+  QLIN_REQUIRE(K * dtype_bytes(x_dtype) <= 160 * 1024, QLIN_ERR_UNSUPPORTED,
+               "a row of %lld elements does not fit the shared-memory staging buffer", (long long)K);
+  QLIN_REQUIRE(S >= 0 && S <= K && S % 16 == 0, QLIN_ERR_INVALID_ARG, "S=%lld must be a multiple of 16 in [0, K]",
+               (long long)S);
+  QLIN_REQUIRE(K % 32 == 0 && (K + S) % 32 == 0, QLIN_ERR_ALIGNMENT,
+               "K and K+S must be multiples of 32 (16-byte aligned packed rows)");
+  if (rows == 0) return ok();
+  QLIN_REQUIRE(x && g && q && sf, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(x) && aligned16(q) && aligned16(perm), QLIN_ERR_ALIGNMENT,
+               "x, q and perm must be 16-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(g) & 3u) == 0, QLIN_ERR_ALIGNMENT, "g must be 4-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_quant_nvfp4(x, x_dtype, rows, K, perm, S, mode, g, q, sf, stream), "quant_nvfp4 launch");
+}
+
+qlin_status qlin_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,
+                            int64_t T, int64_t N, int64_t K, const float* g_a, const float* g_b, void* out,
+                            qlin_dtype out_dtype, cudaStream_t stream) {
+  QLIN_REQUIRE(T >= 0 && T <= kMaxDim && N >= 0 && N <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG,
+               "bad sizes T=%lld N=%lld K=%lld", (long long)T, (long long)N, (long long)K);
+  QLIN_REQUIRE(K % 64 == 0, QLIN_ERR_INVALID_ARG, "K=%lld is not a multiple of 64", (long long)K);
+  QLIN_REQUIRE(out_dtype == QLIN_F16 || out_dtype == QLIN_BF16, QLIN_ERR_INVALID_ARG, "out_dtype must be F16 or BF16");
+  if (T == 0 || N == 0) return ok();
+  QLIN_REQUIRE(a && sfa && b && sfb && g_a && g_b && out, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(a) && aligned16(b) && aligned16(out), QLIN_ERR_ALIGNMENT,
+               "a, b and out must be 16-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(sfa) & 3u) == 0 && (reinterpret_cast<uintptr_t>(sfb) & 3u) == 0,
+               QLIN_ERR_ALIGNMENT, "sfa and sfb must be 4-byte aligned");
+  QLIN_REQUIRE((N * 2) % 16 == 0, QLIN_ERR_ALIGNMENT, "the out row pitch (2N bytes) must be a multiple of 16");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_nvfp4_gemm(a, sfa, b, sfb, T, N, K, g_a, g_b, out, out_dtype, stream), "nvfp4_gemm launch");
+}
+
+}  // extern "C"

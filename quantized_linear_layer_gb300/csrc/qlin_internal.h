@@ -1,0 +1,60 @@
+// Internal host-side interface between the C ABI layer (qlin_api.cu) and the
+// kernel translation units.  Every launcher enqueues on `stream`, returns the
+// launch status and never synchronizes.  Arguments have already been checked
+// by the ABI layer.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qlin.h"
+
+namespace qlin {
+
+// Device address of the per-device error word (set up once per device).
+int32_t* device_error_word();
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+cudaError_t launch_quant_w4_g128(const void* w, qlin_dtype w_dtype, int64_t N, int64_t K, uint8_t* wq,
+                                 void* scales, uint8_t* zeros, cudaStream_t stream);
+
+cudaError_t launch_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq,
+                              const void* scales, const uint8_t* zeros, void* y, cudaStream_t stream);
+
+cudaError_t launch_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
+                                  float* scale, int32_t* azp, cudaStream_t stream);
+
+cudaError_t launch_int8_row_sum(const int8_t* b, int64_t N, int64_t K, int32_t* out, cudaStream_t stream);
+
+struct W8A8Epilogue {
+  const float* scale_a;
+  bool scale_a_per_row;
+  const float* scale_b;
+  bool scale_b_per_col;
+  const int32_t* azp;      // [T] or null
+  const int32_t* azp_adj;  // [N] or null
+  const void* bias;        // [N] or null
+  qlin_dtype bias_dtype;
+  qlin_dtype out_dtype;    // F16, BF16 or I32 (raw accumulator)
+};
+
+cudaError_t launch_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_t N, int64_t K,
+                             const W8A8Epilogue& epi, void* out, cudaStream_t stream);
+
+cudaError_t launch_nvfp4_global_scale(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, float* g,
+                                      cudaStream_t stream);
+
+cudaError_t launch_arc_perm(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, int32_t* perm,
+                            cudaStream_t stream);
+
+cudaError_t launch_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const int32_t* perm,
+                               int64_t S, qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
+                               cudaStream_t stream);
+
+cudaError_t launch_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,
+                              int64_t T, int64_t N, int64_t K, const float* g_a, const float* g_b, void* out,
+                              qlin_dtype out_dtype, cudaStream_t stream);
+
+}  // namespace qlin

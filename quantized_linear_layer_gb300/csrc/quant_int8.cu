@@ -1,0 +1,240 @@
+// Per-token int8 activation quantization (symmetric absmax or asymmetric with
+// an integer zero-point), the int8 row sum used as the W8A8 zero-point
+// adjustment, and the asymmetric 4-bit group weight quantizer.
+//
+// Symmetric: s = max|x| / 127, q = clamp(rint(x / s), -127, 127)
+//   ("LLM and AIGC quantization: from number formats to W4A4", symmetric
+//   quantization with q_max = 2^(b-1) - 1, per-token dynamic scales).
+// Asymmetric: the row range [min(x,0), max(x,0)] is mapped onto [-128, 127]
+//   with an integer zero-point z so that 0 is exact; q = round(x/s) + z
+//   ("Chapter 9 - Quantization kernels", 9.2: zero-point added on quantize).
+// 4-bit weights: s = fp16(max(max - min, 1e-5) / 15), z = rint(-min / s),
+//   q = clamp(rint(w / s) + z, 0, 15) per 128-element group (the AWQ offline
+//   flow's pseudo_quant on the same page).
+//
+// The rounding decisions are taken in IEEE float32 exactly as written: true
+// division (__fdiv_rn), round-half-to-even (__float2int_rn), and no fused
+// multiply-add anywhere a result feeds a rounding decision.
+#include "device_common.cuh"
+#include "qlin_internal.h"
+
+namespace qlin {
+namespace {
+
+constexpr int kQuantThreads = 256;
+constexpr int kMaxVecPerThread = 4;  // 4 x 8 elements held in registers
+
+template <int DT, bool ASYM>
+__global__ void __launch_bounds__(kQuantThreads) quant_int8_rows_kernel(const void* __restrict__ x, int K,
+                                                                         int8_t* __restrict__ q,
+                                                                         float* __restrict__ scale,
+                                                                         int32_t* __restrict__ azp) {
+  const int64_t row = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nvec = K / 8;
+  const char* xr = static_cast<const char*>(x) + row * (int64_t)K * elem_bytes<DT>();
+  int8_t* qr = q + row * (int64_t)K;
+
+  float v[kMaxVecPerThread][8];
+  // Running absmax (symmetric) or running min / max (asymmetric).  Both start
+  // at 0, which makes the asymmetric range include 0.
+  float s0 = 0.0f;
+  float s1 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kMaxVecPerThread; ++i) {
+    const int idx = tid + i * kQuantThreads;
+    if (idx < nvec) {
+      Vec8Loader<DT>::load(xr + (int64_t)idx * 8 * elem_bytes<DT>(), v[i]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (ASYM) { s0 = fminf(s0, v[i][j]); s1 = fmaxf(s1, v[i][j]); }
+        else s0 = fmaxf(s0, fabsf(v[i][j]));
+      }
+    }
+  }
+  for (int idx = tid + kMaxVecPerThread * kQuantThreads; idx < nvec; idx += kQuantThreads) {
+    float t[8];
+    Vec8Loader<DT>::load(xr + (int64_t)idx * 8 * elem_bytes<DT>(), t);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (ASYM) { s0 = fminf(s0, t[j]); s1 = fmaxf(s1, t[j]); }
+      else s0 = fmaxf(s0, fabsf(t[j]));
+    }
+  }
+
+  // Block reduction (min/max are exact, so the order does not matter).
+  __shared__ float red0[kQuantThreads / 32], red1[kQuantThreads / 32];
+  __shared__ float s_scale;
+  __shared__ int s_zero;
+  if (ASYM) { s0 = warp_min(s0); s1 = warp_max(s1); } else { s0 = warp_max(s0); }
+  if ((tid & 31) == 0) { red0[tid >> 5] = s0; red1[tid >> 5] = s1; }
+  __syncthreads();
+  if (tid == 0) {
+    float a = red0[0], b = red1[0];
+    for (int w = 1; w < kQuantThreads / 32; ++w) {
+      if (ASYM) { a = fminf(a, red0[w]); b = fmaxf(b, red1[w]); } else { a = fmaxf(a, red0[w]); }
+    }
+    if (ASYM) {
+      // a = min(min x, 0), b = max(max x, 0)
+      const float range = fmaxf(__fsub_rn(b, a), 1e-5f);
+      const float s = __fdiv_rn(range, 255.0f);
+      const int z = -128 - __float2int_rn(__fdiv_rn(a, s));
+      s_scale = s;
+      s_zero = z;
+      scale[row] = s;
+      azp[row] = z;
+    } else {
+      const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 127.0f);
+      s_scale = s;
+      s_zero = 0;
+      scale[row] = s;
+    }
+  }
+  __syncthreads();
+  const float s = s_scale;
+  const int z = s_zero;
+
+  auto quant8 = [&](const float* t, int64_t idx) {
+    uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      int r = __float2int_rn(__fdiv_rn(t[j], s));
+      if (ASYM) r = min(max(r + z, -128), 127);
+      else r = min(max(r, -127), 127);
+      const uint32_t byte = static_cast<uint32_t>(r) & 0xffu;
+      if (j < 4) w0 |= byte << (8 * j); else w1 |= byte << (8 * (j - 4));
+    }
+    *reinterpret_cast<uint2*>(qr + idx * 8) = make_uint2(w0, w1);
+  };
+#pragma unroll
+  for (int i = 0; i < kMaxVecPerThread; ++i) {
+    const int idx = tid + i * kQuantThreads;
+    if (idx < nvec) quant8(v[i], idx);
+  }
+  for (int idx = tid + kMaxVecPerThread * kQuantThreads; idx < nvec; idx += kQuantThreads) {
+    float t[8];
+    Vec8Loader<DT>::load(xr + (int64_t)idx * 8 * elem_bytes<DT>(), t);
+    quant8(t, idx);
+  }
+}
+
+// azp_adj[n] = sum_k b[n,k]: one warp per row, 16 bytes per lane per step.
+__global__ void int8_row_sum_kernel(const int8_t* __restrict__ b, int64_t N, int K, int32_t* __restrict__ out) {
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (row >= N) return;
+  const int8_t* br = b + row * (int64_t)K;
+  int acc = 0;
+  for (int off = lane * 16; off < K; off += 32 * 16) {
+    const uint4 u = ldg_v4(br + off);
+    acc = __dp4a(static_cast<int>(u.x), 0x01010101, acc);
+    acc = __dp4a(static_cast<int>(u.y), 0x01010101, acc);
+    acc = __dp4a(static_cast<int>(u.z), 0x01010101, acc);
+    acc = __dp4a(static_cast<int>(u.w), 0x01010101, acc);
+  }
+  acc = warp_sum_int(acc);
+  if (lane == 0) out[row] = acc;
+}
+
+// Asymmetric 4-bit group quantization: one warp per row and pair of
+// 128-element groups; lane l covers 8 consecutive elements, lanes 0-15 the
+// first group and 16-31 the second.
+template <int DT>
+__global__ void quant_w4_g128_kernel(const void* __restrict__ w, int64_t N, int K, uint8_t* __restrict__ wq,
+                                     __half* __restrict__ scales, uint8_t* __restrict__ zeros) {
+  const int G = K / 128;
+  const int pairs = (G + 1) / 2;
+  const int64_t item = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (item >= N * pairs) return;
+  const int64_t row = item / pairs;
+  const int p = static_cast<int>(item % pairs);
+  const int lane = threadIdx.x & 31;
+  const int grp = 2 * p + (lane >> 4);
+  const bool active = grp < G;
+  const int k0 = grp * 128 + (lane & 15) * 8;
+
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float mn = 0.0f, mx = 0.0f;
+  if (active) {
+    Vec8Loader<DT>::load(static_cast<const char*>(w) + (row * (int64_t)K + k0) * elem_bytes<DT>(), v);
+    mn = v[0]; mx = v[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) { mn = fminf(mn, v[j]); mx = fmaxf(mx, v[j]); }
+  }
+  // reduce within each 16-lane half
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  const __half s16 = __float2half_rn(__fdiv_rn(fmaxf(__fsub_rn(mx, mn), 1e-5f), 15.0f));
+  const float s = __half2float(s16);
+  const int z = min(max(__float2int_rn(__fdiv_rn(-mn, s)), 0), 15);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int c = min(max(__float2int_rn(__fdiv_rn(v[j], s)) + z, 0), 15);
+    packed |= static_cast<uint32_t>(c) << (4 * j);
+  }
+  const int z_hi = __shfl_down_sync(0xffffffffu, z, 16);
+  if (active) {
+    *reinterpret_cast<uint32_t*>(wq + row * (int64_t)(K / 2) + k0 / 2) = packed;
+    if ((lane & 15) == 0) scales[row * G + grp] = s16;
+  }
+  if (lane == 0) {
+    const int hi = (2 * p + 1 < G) ? z_hi : 0;
+    zeros[row * (int64_t)pairs + p] = static_cast<uint8_t>(z | (hi << 4));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
+                                  float* scale, int32_t* azp, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>(T)), block(kQuantThreads);
+  const int k = static_cast<int>(K);
+  const bool asym = azp != nullptr;
+  switch (x_dtype) {
+    case QLIN_F16:
+      if (asym) quant_int8_rows_kernel<0, true><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
+      else quant_int8_rows_kernel<0, false><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
+      break;
+    case QLIN_BF16:
+      if (asym) quant_int8_rows_kernel<1, true><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
+      else quant_int8_rows_kernel<1, false><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
+      break;
+    default:
+      if (asym) quant_int8_rows_kernel<2, true><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
+      else quant_int8_rows_kernel<2, false><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
+      break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_int8_row_sum(const int8_t* b, int64_t N, int64_t K, int32_t* out, cudaStream_t stream) {
+  if (N == 0) return cudaSuccess;
+  const int warps = 8;
+  dim3 grid(static_cast<unsigned>((N + warps - 1) / warps)), block(32 * warps);
+  int8_row_sum_kernel<<<grid, block, 0, stream>>>(b, N, static_cast<int>(K), out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_w4_g128(const void* w, qlin_dtype w_dtype, int64_t N, int64_t K, uint8_t* wq,
+                                 void* scales, uint8_t* zeros, cudaStream_t stream) {
+  if (N == 0) return cudaSuccess;
+  const int64_t pairs = (K / 128 + 1) / 2;
+  const int64_t items = N * pairs;
+  const int warps = 8;
+  dim3 grid(static_cast<unsigned>((items + warps - 1) / warps)), block(32 * warps);
+  __half* s = static_cast<__half*>(scales);
+  const int k = static_cast<int>(K);
+  switch (w_dtype) {
+    case QLIN_F16: quant_w4_g128_kernel<0><<<grid, block, 0, stream>>>(w, N, k, wq, s, zeros); break;
+    case QLIN_BF16: quant_w4_g128_kernel<1><<<grid, block, 0, stream>>>(w, N, k, wq, s, zeros); break;
+    default: quant_w4_g128_kernel<2><<<grid, block, 0, stream>>>(w, N, k, wq, s, zeros); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace qlin

@@ -23,3 +23,34 @@ def load_golden(name):
 @pytest.fixture
 def golden():
     return load_golden
+
+
+def assert_within_tolerance(y, ref, what=""):
+    """The floating-point parity bar for fp16 / bf16 outputs against the
+    float64 oracle: max |err| <= 1e-2 (1 + |ref|) elementwise, and relative
+    Frobenius error <= 2e-3."""
+    import numpy as np
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert y.shape == ref.shape, (y.shape, ref.shape)
+    assert np.all(np.isfinite(y)), what + ": non-finite output"
+    err = np.abs(y - ref)
+    bound = 1e-2 * (1.0 + np.abs(ref))
+    worst = np.unravel_index(np.argmax(err - bound), err.shape) if err.size else None
+    assert np.all(err <= bound), "%s: max err %g at %s (ref %g)" % (what, err[worst], worst, ref[worst])
+    nref = np.linalg.norm(ref)
+    if nref > 0:
+        rel = np.linalg.norm(y - ref) / nref
+        assert rel <= 2e-3, "%s: relative Frobenius error %g" % (what, rel)
+
+
+@pytest.fixture(scope="session")
+def qlin_gpu():
+    """The built library on a GB300; skips (never falls back) without a GPU."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_linear_layer_gb300 as q
+    q.build()
+    q.lib()
+    return q

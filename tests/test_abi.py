@@ -1,0 +1,79 @@
+"""The C ABI on the CPU: the library loads, exports every entry point that
+include/qlin.h declares, and rejects bad arguments before touching the GPU."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import quantized_linear_layer_gb300 as q
+from quantized_linear_layer_gb300 import buildlib as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "qlin.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qlin_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def built():
+    qbuild.build()
+    return q.lib()
+
+
+def test_exports_every_declared_symbol(built):
+    names = _declared()
+    assert "qlin_w8a8_gemm" in names and "qlin_nvfp4_gemm" in names
+    out = subprocess.run(["nm", "-D", "--defined-only", qbuild.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\b(qlin_[a-z0-9_]+)\b", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(built, n)
+
+
+def test_status_strings(built):
+    built.qlin_status_string.restype = ctypes.c_char_p
+    assert built.qlin_status_string(0) == b"QLIN_OK"
+    assert built.qlin_status_string(5) == b"QLIN_ERR_TIMEOUT"
+    assert built.qlin_version() >= 100
+
+
+def test_rejects_bad_arguments_without_gpu(built):
+    L = built
+    P = ctypes.c_void_p
+    # W4A16: group 64 is not built; T above 64; K not a multiple of the group
+    assert L.qlin_w4a16_gemm(P(16), 1, 16, 256, P(16), P(16), None, 64, P(16), None) == 3
+    assert L.qlin_w4a16_gemm(P(16), 65, 16, 256, P(16), P(16), None, 128, P(16), None) == 1
+    assert L.qlin_w4a16_gemm(P(16), 1, 16, 200, P(16), P(16), None, 128, P(16), None) == 1
+    assert L.qlin_w4a16_gemm(P(8), 1, 16, 256, P(16), P(16), None, 128, P(16), None) == 2
+    # int8 quant: K not a multiple of 16, bad dtype, misaligned x
+    assert L.qlin_quant_act_int8(P(16), 0, 4, 40, P(16), P(16), None, None) == 2
+    assert L.qlin_quant_act_int8(P(16), 3, 4, 64, P(16), P(16), None, None) == 1
+    assert L.qlin_quant_act_int8(P(24), 0, 4, 64, P(16), P(16), None, None) == 2
+    # W8A8: scale numel, azp without azp_adj, bad out dtype
+    assert L.qlin_w8a8_gemm(P(16), P(16), 4, 8, 64, P(16), 3, P(16), 8, None, None, None, 0, P(16), 0, None) == 1
+    assert L.qlin_w8a8_gemm(P(16), P(16), 4, 8, 64, P(16), 4, P(16), 8, P(16), None, None, 0, P(16), 0, None) == 1
+    assert L.qlin_w8a8_gemm(P(16), P(16), 4, 8, 64, P(16), 4, P(16), 8, None, None, None, 0, P(16), 2, None) == 1
+    # NVFP4: S not a multiple of 16, K+S not a multiple of 32, GEMM K not a multiple of 64
+    assert L.qlin_quant_nvfp4(P(16), 0, 4, 64, None, 8, 0, P(16), P(16), P(16), None) == 1
+    assert L.qlin_quant_nvfp4(P(16), 0, 4, 64, None, 16, 0, P(16), P(16), P(16), None) == 2
+    assert L.qlin_nvfp4_gemm(P(16), P(16), P(16), P(16), 4, 8, 96, P(16), P(16), P(16), 1, None) == 1
+    # perm K limit
+    assert L.qlin_arc_perm(P(16), 0, 4, 32768, P(16), None) == 1
+    msg = L.qlin_last_error_message()
+    assert b"16384" in msg
+
+
+def test_empty_problems_launch_nothing(built):
+    L = built
+    P = ctypes.c_void_p
+    assert L.qlin_w4a16_gemm(None, 0, 16, 256, None, None, None, 128, None, None) == 0
+    assert L.qlin_quant_act_int8(None, 0, 0, 64, None, None, None, None) == 0
+    assert L.qlin_w8a8_gemm(None, None, 0, 8, 64, None, 1, None, 1, None, None, None, 0, None, 0, None) == 0
+    assert L.qlin_nvfp4_gemm(None, None, None, None, 4, 0, 64, None, None, None, 1, None) == 0

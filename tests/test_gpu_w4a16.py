@@ -1,0 +1,94 @@
+"""W4A16 on the GPU against the CPU oracle: the a0 weight quantizer bit for
+bit, and the fused dequant GEMV / skinny GEMM within the fp16 tolerance, on
+the tiny symmetric workload and on the Llama-2-7B-shaped decode layers."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_linear_layer_gb300 import inputs
+from conftest import assert_within_tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _gpu_quant_w4(q, w):
+    n, k = w.shape
+    wq = torch.empty((n, k // 2), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((n, k // 128), dtype=torch.float16, device="cuda")
+    zp = torch.empty((n, (k // 128 + 1) // 2), dtype=torch.uint8, device="cuda")
+    q.qlin_quant_w4_g128(_dev(w), wq, sc, zp)
+    return wq, sc, zp
+
+
+def _gemm(q, x, wq, sc, zp):
+    y = torch.empty((x.shape[0], wq.shape[0]), dtype=torch.float16, device="cuda")
+    q.qlin_w4a16_gemm(x, wq, sc, zp, y)
+    torch.cuda.synchronize()
+    assert q.qlin_get_device_error() == 0
+    return y.cpu().numpy()
+
+
+def test_tiny_symmetric(qlin_gpu):
+    d = inputs.tiny_w4a16(seed=0)
+    ref = oracle.w4a16_reference(d["x"], d["codes"], d["scales"], None)
+    y = _gemm(qlin_gpu, _dev(d["x"]), _dev(oracle.pack_u4(d["codes"])), _dev(d["scales"]), None)
+    assert_within_tolerance(y, ref, "tiny W4A16")
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 8, 9, 16, 24, 33, 64])
+def test_token_counts_ragged_rows(qlin_gpu, T):
+    # N = 200 is not a multiple of the 16-row tile; every code and zero-point occurs
+    d = inputs.w4a16_decode(seed=17, T=T, N=200, K=640)
+    codes, s16, z = oracle.quant_w4_g128(d["w"])
+    ref = oracle.w4a16_reference(d["x"], codes, s16, z)
+    y = _gemm(qlin_gpu, _dev(d["x"]), _dev(oracle.pack_u4(codes)), _dev(s16), _dev(oracle.pack_u4(z)))
+    assert_within_tolerance(y, ref, "W4A16 T=%d" % T)
+
+
+def test_all_codes_and_zero_points_exact(qlin_gpu):
+    """Every (code, zero-point) pair: with one-hot activations the GEMV
+    returns s * (q - z) itself, which is exact in fp16 for these scales."""
+    n, k = 256, 128
+    codes = np.tile(np.arange(16, dtype=np.uint8), (n, k // 16))
+    zeros = (np.arange(n, dtype=np.uint8) % 16).reshape(n, 1)
+    scales = np.full((n, 1), 0.25, dtype=np.float16)
+    wq, sc, zp = _dev(oracle.pack_u4(codes)), _dev(scales), _dev(oracle.pack_u4(zeros))
+    for kk in range(0, 16):
+        x = np.zeros((1, k), dtype=np.float16)
+        x[0, kk] = 1.0
+        y = _gemm(qlin_gpu, _dev(x), wq, sc, zp)
+        expect = 0.25 * (kk - zeros[:, 0].astype(np.float64))
+        assert np.array_equal(y[0].astype(np.float64), expect)
+
+
+def test_weight_quantizer_bit_exact(qlin_gpu):
+    d = inputs.w4a16_decode(seed=3, T=1, N=300, K=1152)   # odd group count (9)
+    w = d["w"].copy()
+    w[5, :128] = 0.0                                        # a flat group: range floor
+    w[7, 128:256] = np.abs(w[7, 128:256])                   # a group that does not straddle 0
+    codes, s16, z = oracle.quant_w4_g128(w)
+    wq, sc, zp = _gpu_quant_w4(qlin_gpu, w)
+    assert np.array_equal(wq.cpu().numpy(), oracle.pack_u4(codes))
+    assert np.array_equal(sc.cpu().numpy().view(np.uint16), s16.view(np.uint16))
+    assert np.array_equal(zp.cpu().numpy(), oracle.pack_u4(z))
+
+
+@pytest.mark.parametrize("N,K", inputs.LLAMA2_7B_LAYERS)
+def test_llama_decode_layers(qlin_gpu, N, K):
+    d = inputs.w4a16_decode(seed=1, T=16, N=N, K=K)
+    codes, s16, z = oracle.quant_w4_g128(d["w"])
+    wq, sc, zp = _gpu_quant_w4(qlin_gpu, d["w"])
+    assert np.array_equal(wq.cpu().numpy(), oracle.pack_u4(codes))
+    assert np.array_equal(sc.cpu().numpy().view(np.uint16), s16.view(np.uint16))
+    assert np.array_equal(zp.cpu().numpy(), oracle.pack_u4(z))
+    for T in (1, 4, 16):
+        x = d["x"][:T]
+        ref = oracle.w4a16_reference(x, codes, s16, z)
+        y = _gemm(qlin_gpu, _dev(x), wq, sc, zp)
+        assert_within_tolerance(y, ref, "W4A16 N=%d K=%d T=%d" % (N, K, T))
