@@ -7,7 +7,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/qlin.h"
+#include "qlin.h"
 
 namespace qlin {
 

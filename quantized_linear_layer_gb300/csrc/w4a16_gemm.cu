@@ -28,12 +28,12 @@
 // the product over a group covers every K index once.
 #include "device_common.cuh"
 #include "qlin_internal.h"
+#include "tc_common.cuh"
 
 namespace qlin {
 namespace {
 
 constexpr int kW4Group = 128;
-constexpr int kW4Batch = 4;  // groups whose weight loads are in flight together
 
 __device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
   __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
@@ -75,22 +75,184 @@ __device__ __forceinline__ void pair_x(uint4 u, uint32_t* out) {
   out[3] = __byte_perm(u.y, u.w, 0x7632);
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most `pending` of this thread's most recent cp.async groups
+// are still in flight (the count must be an immediate, hence the switch).
+__device__ __forceinline__ void cp_async_wait_pending(int pending) {
+  switch (pending) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+  }
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start
+// launching, and wait for the previous one before touching data it writes.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Groups one CTA handles at most; longer rows are split over a cluster.
+constexpr int kW4MaxGroupsPerCta = 32;
+
+// Shared-memory plan of one CTA (16 output rows, W warps, GPW groups per warp,
+// GC groups of K, Tc tokens, C CTAs in the cluster).
+struct W4Smem {
+  int w_off, s_off, z_off, x_off, r_off, c_off, total;
+};
+
+__host__ __device__ inline W4Smem w4_smem_plan(int W, int GPW, int GC, int Tc, int NT, int C) {
+  W4Smem p;
+  p.w_off = 0;                                   // [W][GPW][2 rows][32 lanes] x 16 B
+  p.s_off = p.w_off + W * GPW * 2 * 32 * 16;     // [16 rows][GC] fp16 scales
+  p.z_off = p.s_off + ((16 * GC * 2 + 15) / 16) * 16;   // [16 rows][GC] zero-points, one per byte
+  p.x_off = p.z_off + ((16 * GC + 15) / 16) * 16;       // [Tc][GC*16] activation chunks (16 B)
+  p.r_off = p.x_off + Tc * GC * 16 * 16;                // [W][32][NT*4] fp32 partial sums
+  p.c_off = p.r_off + W * 32 * NT * 4 * 4;              // [C][32][NT*4] cluster partial sums
+  p.total = p.c_off + C * 32 * NT * 4 * 4;
+  return p;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// One cluster of C CTAs per 16 output rows; CTA r of the cluster handles the
+// groups [r*GC, min((r+1)*GC, G)) of K and its warps split those groups
+// (warp w takes groups w, w + W, ...).  Every thread copies its own 16-byte
+// weight slices into shared memory with cp.async at the start, the scales,
+// zero-points and activations of the CTA's K range follow asynchronously, so
+// a CTA has all of its operands in flight at once and nothing of the stream
+// is held in registers.  Partial sums are added across warps through shared
+// memory and across the cluster through distributed shared memory into CTA 0,
+// always in the same order.
 template <int NT>
-__global__ void __launch_bounds__(256) w4a16_mma_kernel(const __half* __restrict__ x, int T, int N, int K,
+__global__ void __launch_bounds__(256) w4a16_mma_kernel(const __half* __restrict__ x, int Tc, int N, int K,
                                                        const uint8_t* __restrict__ wq,
                                                        const __half* __restrict__ scales,
-                                                       const uint8_t* __restrict__ zeros, int zpitch,
-                                                       __half* __restrict__ y) {
-  extern __shared__ float red[];  // [warps][32 lanes][NT * 4]
+                                                       const uint8_t* __restrict__ zeros, int zpitch, int GC,
+                                                       int GPW, __half* __restrict__ y, int ldy) {
+  extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
+  const int W = blockDim.x >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int G = K / kW4Group;
-  const int rA = blockIdx.x * 16 + g, rB = rA + 8;
+  const int C = gridDim.x / ((N + 15) / 16) ;  // CTAs per cluster (grid is C x row blocks)
+  const uint32_t rank = C > 1 ? cluster_rank() : 0;
+  const int gs = rank * GC;
+  const int gn = max(0, min(GC, G - gs));      // groups of this CTA
+  const W4Smem plan = w4_smem_plan(W, GPW, GC, Tc, NT, C);
+  uint4* wbuf = reinterpret_cast<uint4*>(smem + plan.w_off);
+  __half* sbuf = reinterpret_cast<__half*>(smem + plan.s_off);
+  uint8_t* zbuf = smem + plan.z_off;
+  uint4* xbuf = reinterpret_cast<uint4*>(smem + plan.x_off);
+  float* red = reinterpret_cast<float*>(smem + plan.r_off);
+  float* cred = reinterpret_cast<float*>(smem + plan.c_off);
+
+  const int row0 = (blockIdx.x / C) * 16;
+  const int rA = row0 + g, rB = rA + 8;
   // Rows past N read row N-1 (always in bounds); their results are not stored.
   const int rAc = min(rA, N - 1), rBc = min(rB, N - 1);
-  const uint8_t* wA = wq + (int64_t)rAc * (K / 2) + c * 16;
-  const uint8_t* wB = wq + (int64_t)rBc * (K / 2) + c * 16;
+
+  // 1. The weight stream: every group of this warp, both rows, in flight.
+  {
+    const uint8_t* wA = wq + (int64_t)rAc * (K / 2) + gs * (kW4Group / 2) + c * 16;
+    const uint8_t* wB = wq + (int64_t)rBc * (K / 2) + gs * (kW4Group / 2) + c * 16;
+    uint4* mine = wbuf + (size_t)warp * GPW * 64 + lane;
+    for (int i = 0; i < GPW; ++i) {
+      const int grp = warp + i * W;
+      if (grp < gn) {
+        cp_async16(tc::smem_u32(mine + i * 64), wA + grp * (kW4Group / 2));
+        cp_async16(tc::smem_u32(mine + i * 64 + 32), wB + grp * (kW4Group / 2));
+      }
+      cp_async_commit();  // one group per K group, consumed in order below
+    }
+  }
+  // 2. Scales and zero-points of the CTA's rows and groups, into registers
+  //    first (all loads issued before any store waits on one).
+  //    Thread t covers row t / 16 and groups t % 16, t % 16 + 16 (GC <= 32).
+  const int mr = threadIdx.x >> 4, mg = threadIdx.x & 15;
+  const bool meta_row = mr < 16;
+  __half sv[2];
+  uint8_t zv[2];
+  if (meta_row) {
+    const int64_t row = min(row0 + mr, N - 1);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int grp = mg + 16 * j;
+      if (grp < gn) {
+        const int ga = gs + grp;
+        sv[j] = scales[row * G + ga];
+        zv[j] = zeros ? static_cast<uint8_t>((zeros[row * zpitch + (ga >> 1)] >> (4 * (ga & 1))) & 0xF)
+                      : static_cast<uint8_t>(8);
+      }
+    }
+  }
+  pdl_launch_dependents();
+  // 3. Activations (may be produced by the previous kernel in the stream),
+  //    loaded to registers and stored in the pair order of the MMA fragments:
+  //    (x[8m+j], x[8m+j+4]), j = 0..3.
+  pdl_wait();
+  const int XC = gn * 16;  // 16-byte chunks per token in this CTA's K range
+  for (int tok = 0; tok < Tc; ++tok) {
+    const __half* xr = x + (int64_t)tok * K + gs * kW4Group;
+    uint4* xs_row = xbuf + (size_t)tok * GC * 16;
+    constexpr int kXU = 2;
+    for (int m0 = threadIdx.x; m0 < XC; m0 += kXU * blockDim.x) {
+      uint4 u[kXU];
+#pragma unroll
+      for (int j = 0; j < kXU; ++j) {
+        const int m = m0 + j * blockDim.x;
+        if (m < XC) u[j] = ldg_v4(xr + m * 8);
+      }
+#pragma unroll
+      for (int j = 0; j < kXU; ++j) {
+        const int m = m0 + j * blockDim.x;
+        if (m < XC) {
+          uint32_t q[4];
+          pair_x(u[j], q);
+          xs_row[m] = make_uint4(q[0], q[1], q[2], q[3]);
+        }
+      }
+    }
+  }
+  if (meta_row) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int grp = mg + 16 * j;
+      if (grp < gn) {
+        sbuf[mr * GC + grp] = sv[j];
+        zbuf[mr * GC + grp] = zv[j];
+      }
+    }
+  }
+  __syncthreads();
 
   float acc[NT][4];
 #pragma unroll
@@ -98,113 +260,152 @@ __global__ void __launch_bounds__(256) w4a16_mma_kernel(const __half* __restrict
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
 
-  for (int gb = warp * kW4Batch; gb < G; gb += nwarps * kW4Batch) {
-    uint4 qa[kW4Batch], qb[kW4Batch];
+  const uint4* mine = wbuf + (size_t)warp * GPW * 64 + lane;
+  for (int i = 0; i < GPW; ++i) {
+    const int grp = warp + i * W;
+    if (grp >= gn) break;
+    cp_async_wait_pending(GPW - 1 - i);
+    const uint4 qa = mine[i * 64], qb = mine[i * 64 + 32];
+    const uint32_t zA = zbuf[g * GC + grp], zB = zbuf[(g + 8) * GC + grp];
+    const float sA = __half2float(sbuf[g * GC + grp]);
+    const float sB = __half2float(sbuf[(g + 8) * GC + grp]);
+    // half2 constants 1024 + z and -(64 + z), built with integer ops
+    const uint32_t subA = 0x64006400u | (zA << 16) | zA, addA = 0xD400D400u | (zA << 20) | (zA << 4);
+    const uint32_t subB = 0x64006400u | (zB << 16) | zB, addB = 0xD400D400u | (zB << 20) | (zB << 4);
+
+    // A fragments of the 8 MMAs of this group: MMA m uses word m/2 and pairs
+    // 2(m%2), 2(m%2)+1.
+    uint32_t fa[8][4];
+    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
+    const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-    for (int i = 0; i < kW4Batch; ++i) {
-      if (gb + i < G) {
-        qa[i] = ldg_stream_v4(wA + (gb + i) * (kW4Group / 2));
-        qb[i] = ldg_stream_v4(wB + (gb + i) * (kW4Group / 2));
-      }
+    for (int w = 0; w < 4; ++w) {
+      uint32_t pa[4], pb[4];
+      unpack_word(wa[w], subA, addA, pa);
+      unpack_word(wb[w], subB, addB, pb);
+      fa[2 * w][0] = pa[0]; fa[2 * w][1] = pb[0]; fa[2 * w][2] = pa[1]; fa[2 * w][3] = pb[1];
+      fa[2 * w + 1][0] = pa[2]; fa[2 * w + 1][1] = pb[2]; fa[2 * w + 1][2] = pa[3]; fa[2 * w + 1][3] = pb[3];
     }
 #pragma unroll
-    for (int i = 0; i < kW4Batch; ++i) {
-      const int grp = gb + i;
-      if (grp >= G) break;
-      uint32_t zA = 8, zB = 8;
-      if (zeros != nullptr) {
-        zA = (zeros[(int64_t)rAc * zpitch + (grp >> 1)] >> (4 * (grp & 1))) & 0xF;
-        zB = (zeros[(int64_t)rBc * zpitch + (grp >> 1)] >> (4 * (grp & 1))) & 0xF;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int tok = nt * 8 + g;
+      uint4 xp[4];
+      if (tok < Tc) {
+        const uint4* xr = xbuf + (size_t)tok * GC * 16 + grp * 16 + c * 4;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) xp[w] = xr[w];
+      } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) xp[w] = make_uint4(0u, 0u, 0u, 0u);
       }
-      const float sA = __half2float(scales[(int64_t)rAc * G + grp]);
-      const float sB = __half2float(scales[(int64_t)rBc * G + grp]);
-      // half2 constants 1024 + z and -(64 + z), built with integer ops
-      const uint32_t subA = 0x64006400u | (zA << 16) | zA, addA = 0xD400D400u | (zA << 20) | (zA << 4);
-      const uint32_t subB = 0x64006400u | (zB << 16) | zB, addB = 0xD400D400u | (zB << 20) | (zB << 4);
-
-      // A fragments of the 8 MMAs of this group: MMA m uses word m/2 and
-      // pairs 2(m%2), 2(m%2)+1.
-      uint32_t fa[8][4];
-      const uint32_t wa[4] = {qa[i].x, qa[i].y, qa[i].z, qa[i].w};
-      const uint32_t wb[4] = {qb[i].x, qb[i].y, qb[i].z, qb[i].w};
+      // two independent accumulator chains, added at the end of the group
+      float p0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, p1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
-        uint32_t pa[4], pb[4];
-        unpack_word(wa[w], subA, addA, pa);
-        unpack_word(wb[w], subB, addB, pb);
-        fa[2 * w][0] = pa[0]; fa[2 * w][1] = pb[0]; fa[2 * w][2] = pa[1]; fa[2 * w][3] = pb[1];
-        fa[2 * w + 1][0] = pa[2]; fa[2 * w + 1][1] = pb[2]; fa[2 * w + 1][2] = pa[3]; fa[2 * w + 1][3] = pb[3];
+        mma_16816(p0, fa[2 * w], xp[w].x, xp[w].y);
+        mma_16816(p1, fa[2 * w + 1], xp[w].z, xp[w].w);
       }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int tok = nt * 8 + g;
-        uint32_t xp[4][4];  // [word w][pair j]
-        if (tok < T) {
-          const __half* xr = x + (int64_t)tok * K + grp * kW4Group + c * 32;
-#pragma unroll
-          for (int w = 0; w < 4; ++w) pair_x(ldg_v4(xr + 8 * w), xp[w]);
-        } else {
-#pragma unroll
-          for (int w = 0; w < 4; ++w)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) xp[w][j] = 0u;
-        }
-        float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const int w = m >> 1, j0 = 2 * (m & 1);
-          mma_16816(part, fa[m], xp[w][j0], xp[w][j0 + 1]);
-        }
-        acc[nt][0] = fmaf(sA, part[0], acc[nt][0]);
-        acc[nt][1] = fmaf(sA, part[1], acc[nt][1]);
-        acc[nt][2] = fmaf(sB, part[2], acc[nt][2]);
-        acc[nt][3] = fmaf(sB, part[3], acc[nt][3]);
-      }
+      acc[nt][0] = fmaf(sA, p0[0] + p1[0], acc[nt][0]);
+      acc[nt][1] = fmaf(sA, p0[1] + p1[1], acc[nt][1]);
+      acc[nt][2] = fmaf(sB, p0[2] + p1[2], acc[nt][2]);
+      acc[nt][3] = fmaf(sB, p0[3] + p1[3], acc[nt][3]);
     }
   }
 
   // Add the warps' partial sums in a fixed order.
-  float* mine = red + ((size_t)warp * 32 + lane) * (NT * 4);
+  float* slot = red + ((size_t)warp * 32 + lane) * (NT * 4);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) mine[nt * 4 + i] = acc[nt][i];
+    for (int i = 0; i < 4; ++i) slot[nt * 4 + i] = acc[nt][i];
   __syncthreads();
-  if (warp != 0) return;
+  float v[NT][4];
+  if (warp == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[nt][i] = 0.0f;
+      for (int wdx = 0; wdx < W; ++wdx) {
+        const float* p = red + ((size_t)wdx * 32 + lane) * (NT * 4) + nt * 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[nt][i] += p[i];
+      }
+    }
+  }
+  if (C > 1) {
+    // Send this CTA's sums to CTA 0 of the cluster, then CTA 0 adds them in
+    // rank order.
+    if (warp == 0) {
+      const uint32_t dst = map_to_rank(tc::smem_u32(cred + ((size_t)rank * 32 + lane) * (NT * 4)), 0);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) st_cluster_f32(dst + (nt * 4 + i) * 4, v[nt][i]);
+    }
+    cluster_sync_all();
+    if (rank != 0 || warp != 0) return;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[nt][i] = 0.0f;
+      for (int r = 0; r < C; ++r) {
+        const float* p = cred + ((size_t)r * 32 + lane) * (NT * 4) + nt * 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[nt][i] += p[i];
+      }
+    }
+  } else if (warp != 0) {
+    return;
+  }
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int wdx = 0; wdx < nwarps; ++wdx) {
-      const float* p = red + ((size_t)wdx * 32 + lane) * (NT * 4) + nt * 4;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] += p[i];
-    }
     // c0, c1: row g, tokens 2c, 2c+1; c2, c3: row g + 8, same tokens.
     const int t0 = nt * 8 + 2 * c, t1 = t0 + 1;
     if (rA < N) {
-      if (t0 < T) y[(int64_t)t0 * N + rA] = __float2half_rn(v[0]);
-      if (t1 < T) y[(int64_t)t1 * N + rA] = __float2half_rn(v[1]);
+      if (t0 < Tc) y[(int64_t)t0 * ldy + rA] = __float2half_rn(v[nt][0]);
+      if (t1 < Tc) y[(int64_t)t1 * ldy + rA] = __float2half_rn(v[nt][1]);
     }
     if (rB < N) {
-      if (t0 < T) y[(int64_t)t0 * N + rB] = __float2half_rn(v[2]);
-      if (t1 < T) y[(int64_t)t1 * N + rB] = __float2half_rn(v[3]);
+      if (t0 < Tc) y[(int64_t)t0 * ldy + rB] = __float2half_rn(v[nt][2]);
+      if (t1 < Tc) y[(int64_t)t1 * ldy + rB] = __float2half_rn(v[nt][3]);
     }
   }
 }
 
+// Shared memory a launch may use for staged activations.
+constexpr size_t kW4XBudget = 64 * 1024;
+
 template <int NT>
-cudaError_t launch_nt(const void* x, int T, int N, int K, const uint8_t* wq, const void* scales,
-                      const uint8_t* zeros, void* y, cudaStream_t stream) {
+cudaError_t launch_chunk(const __half* x, int Tc, int N, int K, const uint8_t* wq, const __half* scales,
+                         const uint8_t* zeros, __half* y, int ldy, cudaStream_t stream) {
   const int G = K / kW4Group;
-  // Enough warps per CTA to split K; at most 8.
-  int warps = (G + kW4Batch - 1) / kW4Batch;
-  warps = warps < 1 ? 1 : (warps > 8 ? 8 : warps);
-  const size_t smem = (size_t)warps * 32 * NT * 4 * sizeof(float);
-  dim3 grid((N + 15) / 16), block(32 * warps);
-  w4a16_mma_kernel<NT><<<grid, block, smem, stream>>>(
-      static_cast<const __half*>(x), T, N, K, wq, static_cast<const __half*>(scales), zeros, (G + 1) / 2,
-      static_cast<__half*>(y));
-  return cudaGetLastError();
+  const int C = (G + kW4MaxGroupsPerCta - 1) / kW4MaxGroupsPerCta;   // CTAs per cluster
+  const int GC = (G + C - 1) / C;                                     // groups per CTA
+  const int W = 8;  // the scale / zero-point staging below assumes 256 threads
+  const int GPW = (GC + W - 1) / W;
+  const W4Smem plan = w4_smem_plan(W, GPW, GC, Tc, NT, C);
+  cudaError_t e = cudaFuncSetAttribute(w4a16_mma_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.total);
+  if (e != cudaSuccess) return e;
+  if (C > 8) {
+    e = cudaFuncSetAttribute(w4a16_mma_kernel<NT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C * ((N + 15) / 16));
+  cfg.blockDim = dim3(32 * W);
+  cfg.dynamicSmemBytes = plan.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, w4a16_mma_kernel<NT>, x, Tc, N, K, wq, scales, zeros, (G + 1) / 2, GC, GPW, y,
+                            ldy);
 }
 
 }  // namespace
@@ -213,10 +414,24 @@ cudaError_t launch_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, co
                               const void* scales, const uint8_t* zeros, void* y, cudaStream_t stream) {
   if (T == 0 || N == 0) return cudaSuccess;
   const int t = static_cast<int>(T), n = static_cast<int>(N), k = static_cast<int>(K);
-  if (t <= 8) return launch_nt<1>(x, t, n, k, wq, scales, zeros, y, stream);
-  if (t <= 16) return launch_nt<2>(x, t, n, k, wq, scales, zeros, y, stream);
-  if (t <= 32) return launch_nt<4>(x, t, n, k, wq, scales, zeros, y, stream);
-  return launch_nt<8>(x, t, n, k, wq, scales, zeros, y, stream);
+  const __half* xh = static_cast<const __half*>(x);
+  const __half* sh = static_cast<const __half*>(scales);
+  __half* yh = static_cast<__half*>(y);
+  // Tokens per launch: as many as the staging budget allows, at most 16.
+  const int G = k / kW4Group;
+  const int C = (G + kW4MaxGroupsPerCta - 1) / kW4MaxGroupsPerCta;
+  const int GC = (G + C - 1) / C;
+  int tc_max = static_cast<int>(kW4XBudget / ((size_t)GC * kW4Group * 2));
+  tc_max = tc_max < 1 ? 1 : (tc_max > 16 ? 16 : tc_max);
+  for (int t0 = 0; t0 < t; t0 += tc_max) {
+    const int tc = (t - t0) < tc_max ? (t - t0) : tc_max;
+    const __half* xc = xh + (int64_t)t0 * k;
+    __half* yc = yh + (int64_t)t0 * n;
+    cudaError_t e = (tc <= 8) ? launch_chunk<1>(xc, tc, n, k, wq, sh, zeros, yc, n, stream)
+                              : launch_chunk<2>(xc, tc, n, k, wq, sh, zeros, yc, n, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace qlin
