@@ -172,12 +172,12 @@ class Workload:
         q.qlin_arc_perm(self.nv_x, self.nv_perm)
         q.qlin_nvfp4_global_scale(w, self.nv_gw)
         self.nv_qw = torch.empty((N, (K + S) // 2), dtype=torch.uint8, device=dev)
-        self.nv_sfw = torch.empty((N, (K + S) // 16), dtype=torch.uint8, device=dev)
+        self.nv_sfw = torch.empty(q.qlin_nvfp4_sf_bytes(N, K + S, q.QLIN_SF_MMA), dtype=torch.uint8, device=dev)
         q.qlin_quant_nvfp4(w, self.nv_gw, self.nv_qw, self.nv_sfw, perm=self.nv_perm, S=S,
-                           mode=q.QLIN_NVFP4_DUPLICATE)
+                           mode=q.QLIN_NVFP4_DUPLICATE, sf_layout=q.QLIN_SF_MMA)
         del w
         self.nv_qx = torch.empty((T, (K + S) // 2), dtype=torch.uint8, device=dev)
-        self.nv_sfx = torch.empty((T, (K + S) // 16), dtype=torch.uint8, device=dev)
+        self.nv_sfx = torch.empty(q.qlin_nvfp4_sf_bytes(T, K + S, q.QLIN_SF_MMA), dtype=torch.uint8, device=dev)
         self.nv_out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
         torch.cuda.synchronize()
         self.launches = {"w4a16": len(self.w4), "w8a8": 2, "nvfp4": 2}
@@ -192,7 +192,8 @@ class Workload:
         self.q.qlin_w8a8_gemm(self.w8_a, self.w8_b, self.w8_sa, self.w8_sb, self.w8_out, bias=self.w8_bias)
 
     def phase_nvfp4(self):
-        self.q.qlin_quant_nvfp4(self.nv_x, self.nv_gx, self.nv_qx, self.nv_sfx, perm=self.nv_perm, S=NVFP4["S"])
+        self.q.qlin_quant_nvfp4(self.nv_x, self.nv_gx, self.nv_qx, self.nv_sfx, perm=self.nv_perm, S=NVFP4["S"],
+                                sf_layout=self.q.QLIN_SF_MMA)
         self.q.qlin_nvfp4_gemm(self.nv_qx, self.nv_sfx, self.nv_qw, self.nv_sfw, self.nv_gx, self.nv_gw, self.nv_out)
 
     def capture(self):

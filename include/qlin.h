@@ -75,6 +75,16 @@ typedef enum {
   QLIN_NVFP4_DUPLICATE = 1
 } qlin_nvfp4_mode;
 
+typedef enum {
+  /* row-major [rows][K/16], one E4M3 byte per 16-element block */
+  QLIN_SF_ROWS = 0,
+  /* the layout the tensor core reads: rows in tiles of 128, 64-element K
+     blocks in groups of 4 scales; block (rt, kg) is 512 contiguous bytes at
+     ((rt * K/64 + kg) * 512), holding row rt*128 + r, scale 4*kg + j at byte
+     16*(r%32) + 4*(r/32) + j.  Size ceil(rows/128) * K/64 * 512 bytes. */
+  QLIN_SF_MMA = 1
+} qlin_sf_layout;
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* qlin_status_string(qlin_status status);
 
@@ -235,13 +245,25 @@ qlin_status qlin_arc_perm(const void* x, qlin_dtype x_dtype, int64_t rows, int64
  *   S      0 <= S <= K, a multiple of 16
  *   g      float32 [1] device scalar
  *   q      out, uint8 [rows][(K+S)/2]  packed E2M1 codes
- *   sf     out, uint8 [rows][(K+S)/16] E4M3 block scales (row pitch need not
- *          be 16-byte aligned)
- * K must be a multiple of 32 (so packed rows are 16-byte aligned).
+ *   sf     out, E4M3 block scales in sf_layout: QLIN_SF_ROWS [rows][(K+S)/16]
+ *          (row pitch need not be 16-byte aligned), or QLIN_SF_MMA, the
+ *          layout qlin_nvfp4_gemm reads (K+S a multiple of 64; bytes of the
+ *          padding rows are left unwritten)
+ * K and K+S must be multiples of 32 (so packed rows are 16-byte aligned).
  * ---------------------------------------------------------------------- */
 qlin_status qlin_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const int32_t* perm,
                              int64_t S, qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
-                             cudaStream_t stream);
+                             qlin_sf_layout sf_layout, cudaStream_t stream);
+
+/* Bytes of a scale-factor buffer for `rows` rows of K elements in the given
+   layout (-1 if K is not a multiple of 16, or of 64 for QLIN_SF_MMA). */
+int64_t qlin_nvfp4_sf_bytes(int64_t rows, int64_t K, qlin_sf_layout sf_layout);
+
+/* Row-major scales [rows][K/16] -> QLIN_SF_MMA layout (rows past `rows`
+   written as 0).  K a multiple of 64; src 4-byte aligned, dst 16-byte
+   aligned. */
+qlin_status qlin_nvfp4_sf_to_mma(const uint8_t* sf_rows, int64_t rows, int64_t K, uint8_t* sf_mma,
+                                 cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * c2 - NVFP4 block-scaled GEMM
@@ -253,7 +275,8 @@ qlin_status qlin_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, in
  * "NVFP4 quantization and ARCQuant", section 2.2: Y ~ sX_aug QX_aug
  * (sW_aug QW_aug)^T).
  *   a, b      uint8 [T][K/2], [N][K/2]   packed E2M1 codes
- *   sfa, sfb  uint8 [T][K/16], [N][K/16] E4M3 block scales (row-major)
+ *   sfa, sfb  E4M3 block scales of a and b in the QLIN_SF_MMA layout
+ *             (16-byte aligned; qlin_nvfp4_sf_bytes(T or N, K, QLIN_SF_MMA))
  *   g_a, g_b  float32 [1] device scalars
  *   out       [T][N] of out_dtype (BF16 or F16)
  * K must be a multiple of 64 (the tensor-core K step).

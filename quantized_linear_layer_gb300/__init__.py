@@ -18,6 +18,7 @@ from .buildlib import LIB_PATH, build  # noqa: F401
 __all__ = [
     "QlinError", "lib", "build",
     "QLIN_F16", "QLIN_BF16", "QLIN_F32", "QLIN_I32", "QLIN_NVFP4_RESIDUAL", "QLIN_NVFP4_DUPLICATE",
+    "QLIN_SF_ROWS", "QLIN_SF_MMA", "qlin_nvfp4_sf_bytes", "qlin_nvfp4_sf_to_mma",
     "qlin_version", "qlin_get_device_error",
     "qlin_quant_w4_g128", "qlin_w4a16_gemm", "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm",
     "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
@@ -25,6 +26,7 @@ __all__ = [
 
 QLIN_F16, QLIN_BF16, QLIN_F32, QLIN_I32 = 0, 1, 2, 3
 QLIN_NVFP4_RESIDUAL, QLIN_NVFP4_DUPLICATE = 0, 1
+QLIN_SF_ROWS, QLIN_SF_MMA = 0, 1
 
 _STATUS = {0: "QLIN_OK", 1: "QLIN_ERR_INVALID_ARG", 2: "QLIN_ERR_ALIGNMENT", 3: "QLIN_ERR_UNSUPPORTED",
            4: "QLIN_ERR_CUDA", 5: "QLIN_ERR_TIMEOUT"}
@@ -51,7 +53,9 @@ _SIGS = {
     "qlin_w8a8_gemm": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
     "qlin_nvfp4_global_scale": ([_P, _I32, _I64, _I64, _P, _P], _I32),
     "qlin_arc_perm": ([_P, _I32, _I64, _I64, _P, _P], _I32),
-    "qlin_quant_nvfp4": ([_P, _I32, _I64, _I64, _P, _I64, _I32, _P, _P, _P, _P], _I32),
+    "qlin_quant_nvfp4": ([_P, _I32, _I64, _I64, _P, _I64, _I32, _P, _P, _P, _I32, _P], _I32),
+    "qlin_nvfp4_sf_bytes": ([_I64, _I64, _I32], _I64),
+    "qlin_nvfp4_sf_to_mma": ([_P, _I64, _I64, _P, _P], _I32),
     "qlin_nvfp4_gemm": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P], _I32),
 }
 
@@ -198,18 +202,37 @@ def qlin_arc_perm(x, perm, stream=None):
     _check("qlin_arc_perm", lib().qlin_arc_perm(_ptr(x), _dtype_code(x), rows, k, _ptr(perm), _stream(stream)))
 
 
-def qlin_quant_nvfp4(x, g, q, sf, perm=None, S=0, mode=QLIN_NVFP4_RESIDUAL, stream=None):
-    """NVFP4 codes q uint8 [rows][(K+S)/2] and E4M3 scales sf uint8 [rows][(K+S)/16]."""
+def qlin_nvfp4_sf_bytes(rows, K, sf_layout=QLIN_SF_ROWS):
+    """Bytes of an E4M3 scale buffer for rows x K elements in the given layout."""
+    return lib().qlin_nvfp4_sf_bytes(rows, K, sf_layout)
+
+
+def qlin_nvfp4_sf_to_mma(sf_rows, sf_mma, stream=None):
+    """Row-major scales uint8 [rows][K/16] -> the QLIN_SF_MMA layout (1-D uint8)."""
+    torch = _torch()
+    _need(sf_rows, torch.uint8, name="sf_rows"); _need(sf_mma, torch.uint8, name="sf_mma")
+    rows, kb = sf_rows.shape
+    if sf_mma.numel() < qlin_nvfp4_sf_bytes(rows, kb * 16, QLIN_SF_MMA):
+        raise ValueError("sf_mma buffer too small")
+    _check("qlin_nvfp4_sf_to_mma", lib().qlin_nvfp4_sf_to_mma(_ptr(sf_rows), rows, kb * 16, _ptr(sf_mma),
+                                                             _stream(stream)))
+
+
+def qlin_quant_nvfp4(x, g, q, sf, perm=None, S=0, mode=QLIN_NVFP4_RESIDUAL, sf_layout=QLIN_SF_ROWS, stream=None):
+    """NVFP4 codes q uint8 [rows][(K+S)/2] and E4M3 scales sf (uint8 [rows][(K+S)/16]
+    for QLIN_SF_ROWS, or a 1-D buffer of qlin_nvfp4_sf_bytes(rows, K+S, QLIN_SF_MMA))."""
     torch = _torch()
     _need(x, torch.float16, torch.bfloat16, torch.float32, name="x"); _need(g, torch.float32, name="g")
     _need(q, torch.uint8, name="q"); _need(sf, torch.uint8, name="sf"); _need(perm, torch.int32, name="perm")
     rows, k = x.shape
+    if sf.numel() < qlin_nvfp4_sf_bytes(rows, k + S, sf_layout):
+        raise ValueError("sf buffer too small")
     _check("qlin_quant_nvfp4", lib().qlin_quant_nvfp4(_ptr(x), _dtype_code(x), rows, k, _ptr(perm), S, mode, _ptr(g),
-                                                     _ptr(q), _ptr(sf), _stream(stream)))
+                                                     _ptr(q), _ptr(sf), sf_layout, _stream(stream)))
 
 
 def qlin_nvfp4_gemm(a, sfa, b, sfb, g_a, g_b, out, stream=None):
-    """out[T][N] = g_a g_b (dequant(a, sfa) . dequant(b, sfb)^T)."""
+    """out[T][N] = g_a g_b (dequant(a, sfa) . dequant(b, sfb)^T); sfa, sfb in the QLIN_SF_MMA layout."""
     torch = _torch()
     for t_, nm in ((a, "a"), (sfa, "sfa"), (b, "b"), (sfb, "sfb")):
         _need(t_, torch.uint8, name=nm)

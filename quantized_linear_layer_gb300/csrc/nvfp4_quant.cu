@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __r
                                                                   const int32_t* __restrict__ perm, int S,
                                                                   int mode, const float* __restrict__ gp,
                                                                   uint8_t* __restrict__ q,
-                                                                  uint8_t* __restrict__ sf,
+                                                                  uint8_t* __restrict__ sf, int sf_mma,
                                                                   int32_t* __restrict__ err) {
   extern __shared__ __align__(16) unsigned char row_smem[];
   const int64_t row = blockIdx.x;
@@ -95,7 +95,12 @@ __global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __r
   const float g = __ldg(gp);
   const int Kaug = K + S;
   uint8_t* qr = q + row * (int64_t)(Kaug / 2);
-  uint8_t* sfr = sf + row * (int64_t)(Kaug / 16);
+  // Position of the scale of block b of this row in either layout.
+  const int64_t sf_row_base = sf_mma ? ((row >> 7) * (int64_t)(Kaug / 64)) * 512 + 16 * (row & 31) + 4 * ((row & 127) >> 5)
+                                     : row * (int64_t)(Kaug / 16);
+  auto sf_at = [&](int b) -> uint8_t& {
+    return sf_mma ? sf[sf_row_base + (int64_t)(b >> 2) * 512 + (b & 3)] : sf[sf_row_base + b];
+  };
   const int nblk = K / 16;
   const int sblk = S / 16;
   // A channel index outside [0, K) is recorded in the device error word and
@@ -127,11 +132,11 @@ __global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __r
     float d;
     const uint32_t sfc = quant_block16(v, g, packed, &d);
     *reinterpret_cast<uint2*>(qr + b * 8) = make_uint2(packed[0], packed[1]);
-    sfr[b] = static_cast<uint8_t>(sfc);
+    sf_at(b) = static_cast<uint8_t>(sfc);
     if (b < sblk) {
       if (mode == QLIN_NVFP4_DUPLICATE) {
         *reinterpret_cast<uint2*>(qr + (K / 2) + b * 8) = make_uint2(packed[0], packed[1]);
-        sfr[nblk + b] = static_cast<uint8_t>(sfc);
+        sf_at(nblk + b) = static_cast<uint8_t>(sfc);
       } else {
         // residual r = x - e2m1(q) * d, one float32 multiply then one subtract
         float r[16];
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __r
         float rd;
         const uint32_t rsf = quant_block16(r, g, rp, &rd);
         *reinterpret_cast<uint2*>(qr + (K / 2) + b * 8) = make_uint2(rp[0], rp[1]);
-        sfr[nblk + b] = static_cast<uint8_t>(rsf);
+        sf_at(nblk + b) = static_cast<uint8_t>(rsf);
       }
     }
   }
@@ -216,6 +221,19 @@ __global__ void __launch_bounds__(1024) perm_sort_kernel(int32_t* __restrict__ p
   for (int i = threadIdx.x; i < K; i += blockDim.x) perm[i] = static_cast<int32_t>(keys[i] & 0xFFFFFFFFull);
 }
 
+// Row-major scales [rows][K/16] -> the MMA layout: one thread per (padded
+// row, 64-element K block) moves 4 bytes; rows past `rows` are zero.
+__global__ void sf_to_mma_kernel(const uint8_t* __restrict__ src, int rows, int K, uint8_t* __restrict__ dst) {
+  const int KG = K / 64;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t prow = ((int64_t)rows + 127) / 128 * 128;
+  if (i >= prow * KG) return;
+  const int row = static_cast<int>(i / KG), kg = static_cast<int>(i % KG);
+  const uint32_t v = row < rows ? *reinterpret_cast<const uint32_t*>(src + (int64_t)row * (K / 16) + 4 * kg) : 0u;
+  const int64_t off = ((int64_t)(row >> 7) * KG + kg) * 512 + 16 * (row & 31) + 4 * ((row & 127) >> 5);
+  *reinterpret_cast<uint32_t*>(dst + off) = v;
+}
+
 template <typename F>
 cudaError_t dispatch_dtype(qlin_dtype dt, F&& f) {
   switch (dt) {
@@ -229,7 +247,7 @@ cudaError_t dispatch_dtype(qlin_dtype dt, F&& f) {
 
 cudaError_t launch_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const int32_t* perm,
                                int64_t S, qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
-                               cudaStream_t stream) {
+                               qlin_sf_layout sf_layout, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   return dispatch_dtype(x_dtype, [&](auto dt) -> cudaError_t {
     constexpr int DT = decltype(dt)::value;
@@ -240,9 +258,18 @@ cudaError_t launch_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, 
       if (e != cudaSuccess) return e;
     }
     nvfp4_quant_kernel<DT><<<static_cast<unsigned>(rows), kNvThreads, smem, stream>>>(
-        x, static_cast<int>(K), perm, static_cast<int>(S), static_cast<int>(mode), g, q, sf, device_error_word());
+        x, static_cast<int>(K), perm, static_cast<int>(S), static_cast<int>(mode), g, q, sf,
+        sf_layout == QLIN_SF_MMA ? 1 : 0, device_error_word());
     return cudaGetLastError();
   });
+}
+
+cudaError_t launch_nvfp4_sf_to_mma(const uint8_t* src, int64_t rows, int64_t K, uint8_t* dst, cudaStream_t stream) {
+  const int64_t n = (rows + 127) / 128 * 128 * (K / 64);
+  if (n == 0) return cudaSuccess;
+  sf_to_mma_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(src, static_cast<int>(rows),
+                                                                              static_cast<int>(K), dst);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_nvfp4_global_scale(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, float* g,

@@ -282,9 +282,30 @@ qlin_status qlin_arc_perm(const void* x, qlin_dtype x_dtype, int64_t rows, int64
   QLIN_LAUNCH(launch_arc_perm(x, x_dtype, rows, K, perm, stream), "arc_perm launch");
 }
 
+int64_t qlin_nvfp4_sf_bytes(int64_t rows, int64_t K, qlin_sf_layout sf_layout) {
+  if (rows < 0 || K <= 0 || K % 16 != 0) return -1;
+  if (sf_layout == QLIN_SF_ROWS) return rows * (K / 16);
+  if (sf_layout == QLIN_SF_MMA && K % 64 == 0) return (rows + 127) / 128 * (K / 64) * 512;
+  return -1;
+}
+
+qlin_status qlin_nvfp4_sf_to_mma(const uint8_t* sf_rows, int64_t rows, int64_t K, uint8_t* sf_mma,
+                                 cudaStream_t stream) {
+  QLIN_REQUIRE(rows >= 0 && rows <= kMaxDim && K > 0 && K <= kMaxDim && K % 64 == 0, QLIN_ERR_INVALID_ARG,
+               "bad sizes rows=%lld K=%lld (K a multiple of 64)", (long long)rows, (long long)K);
+  if (rows == 0) return ok();
+  QLIN_REQUIRE(sf_rows && sf_mma, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(sf_rows) & 3u) == 0 && aligned16(sf_mma), QLIN_ERR_ALIGNMENT,
+               "sf_rows must be 4-byte and sf_mma 16-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_nvfp4_sf_to_mma(sf_rows, rows, K, sf_mma, stream), "nvfp4_sf_to_mma launch");
+}
+
 qlin_status qlin_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const int32_t* perm,
                              int64_t S, qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
-                             cudaStream_t stream) {
+                             qlin_sf_layout sf_layout, cudaStream_t stream) {
+  QLIN_REQUIRE(sf_layout == QLIN_SF_ROWS || (sf_layout == QLIN_SF_MMA && (K + S) % 64 == 0), QLIN_ERR_INVALID_ARG,
+               "sf_layout must be QLIN_SF_ROWS, or QLIN_SF_MMA with K+S a multiple of 64");
   QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");
   QLIN_REQUIRE(mode == QLIN_NVFP4_RESIDUAL || mode == QLIN_NVFP4_DUPLICATE, QLIN_ERR_INVALID_ARG, "bad mode");
   QLIN_REQUIRE(rows >= 0 && rows <= kMaxDim && K > 0, QLIN_ERR_INVALID_ARG, "bad sizes rows=%lld K=%lld",
@@ -301,7 +322,8 @@ qlin_status qlin_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, in
                "x, q and perm must be 16-byte aligned");
   QLIN_REQUIRE((reinterpret_cast<uintptr_t>(g) & 3u) == 0, QLIN_ERR_ALIGNMENT, "g must be 4-byte aligned");
   QLIN_DEVICE();
-  QLIN_LAUNCH(launch_quant_nvfp4(x, x_dtype, rows, K, perm, S, mode, g, q, sf, stream), "quant_nvfp4 launch");
+  QLIN_LAUNCH(launch_quant_nvfp4(x, x_dtype, rows, K, perm, S, mode, g, q, sf, sf_layout, stream),
+              "quant_nvfp4 launch");
 }
 
 qlin_status qlin_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,
@@ -315,8 +337,8 @@ qlin_status qlin_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t*
   QLIN_REQUIRE(a && sfa && b && sfb && g_a && g_b && out, QLIN_ERR_INVALID_ARG, "null pointer");
   QLIN_REQUIRE(aligned16(a) && aligned16(b) && aligned16(out), QLIN_ERR_ALIGNMENT,
                "a, b and out must be 16-byte aligned");
-  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(sfa) & 3u) == 0 && (reinterpret_cast<uintptr_t>(sfb) & 3u) == 0,
-               QLIN_ERR_ALIGNMENT, "sfa and sfb must be 4-byte aligned");
+  QLIN_REQUIRE(aligned16(sfa) && aligned16(sfb), QLIN_ERR_ALIGNMENT,
+               "sfa and sfb (QLIN_SF_MMA layout) must be 16-byte aligned");
   QLIN_REQUIRE((N * 2) % 16 == 0, QLIN_ERR_ALIGNMENT, "the out row pitch (2N bytes) must be a multiple of 16");
   QLIN_DEVICE();
   QLIN_LAUNCH(launch_nvfp4_gemm(a, sfa, b, sfb, T, N, K, g_a, g_b, out, out_dtype, stream), "nvfp4_gemm launch");

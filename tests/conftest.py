@@ -72,3 +72,18 @@ def qlin_gpu():
     q.build()
     q.lib()
     return q
+
+
+def sf_rows_to_mma(sf):
+    """Row-major E4M3 scales [rows][K/16] -> the documented QLIN_SF_MMA byte
+    layout (a layout restatement for tests; rows padded to 128 with zeros)."""
+    import numpy as np
+    sf = np.asarray(sf, dtype=np.uint8)
+    rows, kb = sf.shape
+    kg = kb // 4
+    rt = (rows + 127) // 128
+    pad = np.zeros((rt * 128, kb), dtype=np.uint8)
+    pad[:rows] = sf
+    # [rt][r1 = r // 32][r0 = r % 32][kg][j] -> block (rt, kg): byte 16*r0 + 4*r1 + j
+    v = pad.reshape(rt, 4, 32, kg, 4)
+    return np.ascontiguousarray(v.transpose(0, 3, 2, 1, 4)).reshape(-1)

@@ -61,8 +61,13 @@ def test_rejects_bad_arguments_without_gpu(built):
     assert L.qlin_w8a8_gemm(P(16), P(16), 4, 8, 64, P(16), 4, P(16), 8, P(16), None, None, 0, P(16), 0, None) == 1
     assert L.qlin_w8a8_gemm(P(16), P(16), 4, 8, 64, P(16), 4, P(16), 8, None, None, None, 0, P(16), 2, None) == 1
     # NVFP4: S not a multiple of 16, K+S not a multiple of 32, GEMM K not a multiple of 64
-    assert L.qlin_quant_nvfp4(P(16), 0, 4, 64, None, 8, 0, P(16), P(16), P(16), None) == 1
-    assert L.qlin_quant_nvfp4(P(16), 0, 4, 64, None, 16, 0, P(16), P(16), P(16), None) == 2
+    assert L.qlin_quant_nvfp4(P(16), 0, 4, 64, None, 8, 0, P(16), P(16), P(16), 0, None) == 1
+    assert L.qlin_quant_nvfp4(P(16), 0, 4, 64, None, 16, 0, P(16), P(16), P(16), 0, None) == 2
+    # the MMA scale layout needs K+S to be a multiple of 64
+    assert L.qlin_quant_nvfp4(P(16), 0, 4, 96, None, 0, 0, P(16), P(16), P(16), 1, None) == 1
+    assert L.qlin_nvfp4_sf_bytes(130, 4224, 1) == 2 * 66 * 512
+    assert L.qlin_nvfp4_sf_bytes(130, 4224, 0) == 130 * 264
+    assert L.qlin_nvfp4_sf_bytes(130, 4208, 1) == -1
     assert L.qlin_nvfp4_gemm(P(16), P(16), P(16), P(16), 4, 8, 96, P(16), P(16), P(16), 1, None) == 1
     # perm K limit
     assert L.qlin_arc_perm(P(16), 0, 4, 32768, P(16), None) == 1

@@ -10,7 +10,7 @@ import torch
 import oracle
 import quantized_linear_layer_gb300 as qmod
 from quantized_linear_layer_gb300 import inputs
-from conftest import assert_within_tolerance
+from conftest import assert_within_tolerance, sf_rows_to_mma
 
 pytestmark = pytest.mark.gpu
 
@@ -21,7 +21,8 @@ def _dev(a):
 
 def _gemm(q, qa, sfa, ga, qb, sfb, gb, out_dtype=torch.bfloat16):
     out = torch.empty((qa.shape[0], qb.shape[0]), dtype=out_dtype, device="cuda")
-    q.qlin_nvfp4_gemm(_dev(oracle.pack_u4(qa)), _dev(sfa), _dev(oracle.pack_u4(qb)), _dev(sfb),
+    q.qlin_nvfp4_gemm(_dev(oracle.pack_u4(qa)), _dev(sf_rows_to_mma(sfa)), _dev(oracle.pack_u4(qb)),
+                      _dev(sf_rows_to_mma(sfb)),
                       _dev(np.array([ga], np.float32)), _dev(np.array([gb], np.float32)), out)
     torch.cuda.synchronize()
     assert q.qlin_get_device_error() == 0
@@ -84,8 +85,15 @@ def test_config5_arcquant(qlin_gpu):
     sfw = torch.empty((N, (K + S) // 16), dtype=torch.uint8, device="cuda")
     qlin_gpu.qlin_quant_nvfp4(xt, gx, qx, sfx, perm=perm, S=S, mode=qmod.QLIN_NVFP4_RESIDUAL)
     qlin_gpu.qlin_quant_nvfp4(wt, gw, qw, sfw, perm=perm, S=S, mode=qmod.QLIN_NVFP4_DUPLICATE)
+    # the GEMM reads the scales in the MMA layout, written directly by the quantizer
+    sfx_m = torch.empty(qlin_gpu.qlin_nvfp4_sf_bytes(T, K + S, qmod.QLIN_SF_MMA), dtype=torch.uint8, device="cuda")
+    sfw_m = torch.empty(qlin_gpu.qlin_nvfp4_sf_bytes(N, K + S, qmod.QLIN_SF_MMA), dtype=torch.uint8, device="cuda")
+    qlin_gpu.qlin_quant_nvfp4(xt, gx, qx, sfx_m, perm=perm, S=S, mode=qmod.QLIN_NVFP4_RESIDUAL,
+                              sf_layout=qmod.QLIN_SF_MMA)
+    qlin_gpu.qlin_quant_nvfp4(wt, gw, qw, sfw_m, perm=perm, S=S, mode=qmod.QLIN_NVFP4_DUPLICATE,
+                              sf_layout=qmod.QLIN_SF_MMA)
     out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
-    qlin_gpu.qlin_nvfp4_gemm(qx, sfx, qw, sfw, gx, gw, out)
+    qlin_gpu.qlin_nvfp4_gemm(qx, sfx_m, qw, sfw_m, gx, gw, out)
     torch.cuda.synchronize()
     assert qlin_gpu.qlin_get_device_error() == 0
     rperm = oracle.arc_perm(x32)
@@ -94,6 +102,8 @@ def test_config5_arcquant(qlin_gpu):
     rqb, rsfb = oracle.arc_quantize_weight(d["w"], rperm, S, rgw)
     assert np.array_equal(qx.cpu().numpy(), oracle.pack_u4(rqa)) and np.array_equal(sfx.cpu().numpy(), rsfa)
     assert np.array_equal(qw.cpu().numpy(), oracle.pack_u4(rqb)) and np.array_equal(sfw.cpu().numpy(), rsfb)
+    assert np.array_equal(sfx_m.cpu().numpy(), sf_rows_to_mma(rsfa))
+    assert np.array_equal(sfw_m.cpu().numpy(), sf_rows_to_mma(rsfb))
     ref = oracle.nvfp4_gemm_reference(rqa, rsfa, rgx, rqb, rsfb, rgw)
     y = out.float().cpu().numpy()
     assert_within_tolerance(y, ref, "config 5")
@@ -103,3 +113,13 @@ def test_config5_arcquant(qlin_gpu):
     wq0, ws0 = oracle.arc_quantize_weight(d["w"], rperm, 0, rgw)
     rtn = oracle.nvfp4_gemm_reference(rq0, rs0, rgx, wq0, ws0, rgw)
     assert np.linalg.norm(y - exact) < np.linalg.norm(rtn - exact)
+
+
+@pytest.mark.parametrize("rows,K", [(128, 256), (130, 4224), (1, 64), (300, 1088)])
+def test_sf_to_mma_conversion(qlin_gpu, rows, K):
+    rng = np.random.default_rng(rows + K)
+    sf = rng.integers(0, 0x7E, size=(rows, K // 16), dtype=np.uint8)
+    out = torch.full((qlin_gpu.qlin_nvfp4_sf_bytes(rows, K, qmod.QLIN_SF_MMA),), 0xAB, dtype=torch.uint8, device="cuda")
+    qlin_gpu.qlin_nvfp4_sf_to_mma(_dev(sf), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), sf_rows_to_mma(sf))

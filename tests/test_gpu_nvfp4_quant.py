@@ -9,6 +9,7 @@ import torch
 import oracle
 import quantized_linear_layer_gb300 as qmod
 from quantized_linear_layer_gb300 import inputs
+from conftest import sf_rows_to_mma
 
 pytestmark = pytest.mark.gpu
 
@@ -134,3 +135,25 @@ def test_config5_activation_and_weight(qlin_gpu):
     wq, wsf = _quant(qlin_gpu, wt, gw_t, perm, S, qmod.QLIN_NVFP4_DUPLICATE)
     rwq, rwsf = oracle.arc_quantize_weight(d["w"], rperm, S, gw)
     assert np.array_equal(wsf, rwsf) and np.array_equal(wq, oracle.pack_u4(rwq))
+
+
+@pytest.mark.parametrize("rows,S,mode", [(130, 128, 0), (128, 64, 1), (7, 0, 0)])
+def test_quant_nvfp4_mma_scale_layout(qlin_gpu, rows, S, mode):
+    d = inputs.nvfp4_arc(seed=6, T=rows, K=1024)
+    xt = torch.from_numpy(d["x"]).cuda()
+    x32 = d["x"].astype(np.float32)
+    g = np.float32(oracle.nvfp4_global_scale(x32))
+    perm = oracle.arc_perm(x32)
+    k_aug = 1024 + S
+    q1 = torch.empty((rows, k_aug // 2), dtype=torch.uint8, device="cuda")
+    sf_m = torch.full((qlin_gpu.qlin_nvfp4_sf_bytes(rows, k_aug, qmod.QLIN_SF_MMA),), 0, dtype=torch.uint8,
+                      device="cuda")
+    qlin_gpu.qlin_quant_nvfp4(xt, torch.tensor([g]).cuda(), q1, sf_m, perm=torch.from_numpy(perm).cuda(), S=S, mode=mode,
+                              sf_layout=qmod.QLIN_SF_MMA)
+    torch.cuda.synchronize()
+    if mode == 0:
+        rq, rsf = oracle.arc_quantize_activation(x32, perm, S, g)
+    else:
+        rq, rsf = oracle.arc_quantize_weight(x32, perm, S, g)
+    assert np.array_equal(q1.cpu().numpy(), oracle.pack_u4(rq))
+    assert np.array_equal(sf_m.cpu().numpy(), sf_rows_to_mma(rsf))
