@@ -10,7 +10,7 @@
 // residual channels are extra K columns of the same GEMM).
 //
 // Persistent kernel: one CTA per SM walks the 128 x 128 output tiles
-// (tile = blockIdx.x, + gridDim.x, ...), 6 warps:
+// (tile = blockIdx.x, + gridDim.x, ...), 7 warps:
 //   warp 0      TMA producer: packed codes of A and B, 128 rows x 128 bytes
 //               (256 elements) per stage, into the 128-byte swizzled K-major
 //               layout the MMA descriptors describe, plus two bulk copies of
@@ -18,10 +18,12 @@
 //               (128-row x 4-block blocks of 512 bytes, byte
 //               16*(r%32) + 4*(r/32) + j for row r, K block j) and land exactly
 //               as tcgen05.cp reads them.
-//   warp 1      TMEM allocation and the MMA issuer: per stage, tcgen05.cp of
-//               the stage's scale factors from shared memory into TMEM, then
+//   warp 1      TMEM allocation and the MMA issuer: per stage,
 //               4 x tcgen05.mma kind::mxf4nvf4.block_scale.scale_vec::4X
 //               (M=128, N=128, K=64) into one of two accumulator buffers.
+//   warp 6      scale-factor copier: tcgen05.cp of each landed stage's scales
+//               into that stage's TMEM slot, handed to the MMA issuer through
+//               an mbarrier so the copies run ahead of the MMAs.
 //   warps 2-5   epilogue: the fp32 accumulator from TMEM, times g_a . g_b,
 //               rounded once to bf16 / fp16; the other accumulator buffer
 //               keeps the MMAs of the next tile going meanwhile.
@@ -42,7 +44,7 @@ constexpr int kBM = 128, kBN = 128;
 constexpr int kBKB = 128;                 // bytes of packed codes per row per stage (256 elements)
 constexpr int kMmaPerStage = 4;           // K = 64 elements each
 constexpr int kStages = 6;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kAccCols = kBN;
 constexpr int kSfColsPerStage = 2 * kMmaPerStage * 4;  // A and B, 4 TMEM columns per MMA
 constexpr int kTmemCols = 512;            // 2 accumulators (256) + scale factors (6 stages x 32)
@@ -52,7 +54,7 @@ constexpr int kSfBytes = 2 * kMmaPerStage * 512;         // 4 KB per stage
 constexpr int kSmemCodes = 0;
 constexpr int kSmemSf = kSmemCodes + kStages * kCodeBytes;          // 192 KB
 constexpr int kSmemBar = kSmemSf + kStages * kSfBytes;              // +24 KB
-constexpr int kNumBars = 2 * kStages + 4 + 1;
+constexpr int kNumBars = 3 * kStages + 4 + 2;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
 constexpr int kSmemTotal = kSmemMisc + 16 + 1024;
 static_assert(kSmemTotal <= 227 * 1024, "shared memory budget");
@@ -99,6 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
   auto acc_full = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
   auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
   const uint32_t mma_done = bar0 + 8u * (2 * kStages + 4);
+  auto sf_ready = [&](int s) { return bar0 + 8u * (2 * kStages + 5 + s); };
+  const uint32_t cp_done = bar0 + 8u * (3 * kStages + 5);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
 
@@ -112,6 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
       tc::mbar_init(acc_empty(b), 4);
     }
     tc::mbar_init(mma_done, 1);
+    for (int s = 0; s < kStages; ++s) tc::mbar_init(sf_ready(s), 1);  // scale-factor copier commit
+    tc::mbar_init(cp_done, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -173,13 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
         const uint32_t d = tmem + buf * kAccCols;
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % kStages;
-          if (!tc::mbar_wait(full(s), (it / kStages) & 1, err, kSiteFull)) { *abort_flag = 1; break; }
+          // codes landed and scale factors copied into TMEM slot s by the copier warp
+          if (!tc::mbar_wait(sf_ready(s), (it / kStages) & 1, err, kSiteFull)) { *abort_flag = 1; break; }
           tc::tc_fence_after();
-          const uint32_t sf_smem = sbase + kSmemSf + s * kSfBytes;
           const uint32_t sf_t = tmem_sf + s * kSfColsPerStage;
-#pragma unroll
-          for (int i = 0; i < 2 * kMmaPerStage; ++i)
-            tc::tmem_cp_32x128b_x4(sf_t + 4 * i, tc::plain_desc(sf_smem + 512 * i));
           const uint32_t a_base = sbase + kSmemCodes + s * kCodeBytes;
           const uint32_t b_base = a_base + kBM * kBKB;
           const int kk_valid = min(kMmaPerStage, (KB - kb * kBKB) / 32);
@@ -199,6 +202,31 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
       if (*abort_flag && issued_any) {
         tc::mma_commit(mma_done);
         tc::mbar_wait(mma_done, 0, err, kSiteDrain);
+      }
+    }
+  } else if (warp == 6) {
+    // ---------------- scale-factor copier ----------------
+    // Copies each stage's scale factors from shared memory into the stage's
+    // TMEM slot as soon as the stage has landed, ahead of the MMA issuer.
+    if (lane == 0) {
+      int it = 0;
+      for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!tc::mbar_wait(full(s), (it / kStages) & 1, err, kSiteFull)) { *abort_flag = 1; break; }
+          tc::tc_fence_after();
+          const uint32_t sf_smem = sbase + kSmemSf + s * kSfBytes;
+          const uint32_t sf_t = tmem_sf + s * kSfColsPerStage;
+#pragma unroll
+          for (int i = 0; i < 2 * kMmaPerStage; ++i)
+            tc::tmem_cp_32x128b_x4(sf_t + 4 * i, tc::plain_desc(sf_smem + 512 * i));
+          tc::mma_commit(sf_ready(s));
+        }
+      }
+      if (*abort_flag && it > 0) {
+        // copies still in flight must land before TMEM is freed
+        tc::mma_commit(cp_done);
+        tc::mbar_wait(cp_done, 0, err, kSiteDrain);
       }
     }
   } else {
