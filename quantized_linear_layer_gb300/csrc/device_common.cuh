@@ -20,6 +20,13 @@ __device__ __forceinline__ void record_device_error(int32_t* err, int32_t code) 
   if (err != nullptr) atomicCAS(err, 0, code);
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start
+// launching, and wait for the previous one before touching data it writes.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 16-byte read-only load that does not allocate in L1 (streamed weights).
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
   uint4 r;

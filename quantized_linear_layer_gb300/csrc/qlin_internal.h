@@ -23,6 +23,12 @@ cudaError_t launch_quant_w4_g128(const void* w, qlin_dtype w_dtype, int64_t N, i
 cudaError_t launch_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq,
                               const void* scales, const uint8_t* zeros, void* y, cudaStream_t stream);
 
+// One-token W4A16 GEMV on the CUDA cores (T == 1, K <= 12288, the CTA's
+// band of scales small enough for its shared-memory plan).
+bool w4a16_gemv_supported(int64_t T, int64_t N, int64_t K);
+cudaError_t launch_w4a16_gemv(const void* x, int64_t N, int64_t K, const uint8_t* wq, const void* scales,
+                              const uint8_t* zeros, void* y, cudaStream_t stream);
+
 cudaError_t launch_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
                                   float* scale, int32_t* azp, cudaStream_t stream);
 

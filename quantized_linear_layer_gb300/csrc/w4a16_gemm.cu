@@ -93,13 +93,6 @@ __device__ __forceinline__ void cp_async_wait_pending(int pending) {
   }
 }
 
-// Programmatic dependent launch: let the next kernel in the stream start
-// launching, and wait for the previous one before touching data it writes.
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Groups one CTA handles at most; longer rows are split over a cluster.
 constexpr int kW4MaxGroupsPerCta = 32;
 
@@ -412,6 +405,7 @@ cudaError_t launch_chunk(const __half* x, int Tc, int N, int K, const uint8_t* w
 cudaError_t launch_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq,
                               const void* scales, const uint8_t* zeros, void* y, cudaStream_t stream) {
   if (T == 0 || N == 0) return cudaSuccess;
+  if (w4a16_gemv_supported(T, N, K)) return launch_w4a16_gemv(x, N, K, wq, scales, zeros, y, stream);
   const int t = static_cast<int>(T), n = static_cast<int>(N), k = static_cast<int>(K);
   const __half* xh = static_cast<const __half*>(x);
   const __half* sh = static_cast<const __half*>(scales);

@@ -1,0 +1,374 @@
+// W4A16 decode GEMV (one token) on the CUDA cores.
+//
+//   y[n] = sum_g s[n,g] . sum_{k in g} x[k] . (q[n,k] - z[n,g])
+//
+// ("Chapter 9 - Quantization kernels", 9.5 dequantize right before the
+// multiply, weights stay 4-bit in HBM and shared memory; 9.6 the magic-number
+// unpack; "LLM and AIGC quantization", W4A16 section.)
+//
+// Why not the tensor core at T = 1.  A warp-level m16n8k16 MMA with the
+// token as the N side spends 7/8 of its work on padding; on this GPU that
+// caps a decode GEMV below the HBM rate.  One token needs one multiply-add
+// per weight, which the CUDA cores' 4-way byte dot product (dp4a) does with
+// far fewer instructions per code than any float unpack.
+//
+// Integer dot products.  Each thread rounds its 32 activations once to fixed
+// point with a per-chunk scale s_x = max|x| / (127 . 2^15) and writes the
+// result in base-256 signed digits, x_fix = 2^16 hi + 2^8 mid + lo, as three
+// byte planes.  Two AND masks turn a word of eight codes into the bytes of its
+// even and odd codes, and one dp4a per plane and parity gives
+// sum (n - z) . plane exactly in int32 (the zero-point enters once per chunk
+// as z . sum(plane)).  The plane sums are combined and scaled by s_g . s_x in
+// fp32.  The two high planes alone represent every x within 2^-15 of the
+// chunk's largest |x|; that is as fine as fp16 for every element above
+// max|x| / 16, and the low plane (error 2^-22 of max|x|) is added only for
+// chunks whose largest |x| exceeds 64 times the mean |x| of the others
+// (activation outliers), decided per warp.
+//
+// Data path for GB300.  One CTA per SM owns a contiguous band of weight rows;
+// the band is contiguous in HBM, so a single elected thread streams it into a
+// ring of shared-memory stages with 1-D bulk copies (no per-thread load
+// instructions).  The ring is filled before the kernel waits on the previous
+// kernel in the stream (programmatic dependent launch): the weights do not
+// depend on it, so one layer's weights stream in while the previous layer is
+// still finishing, and HBM sees no gap at the layer boundary.  The CTA uses
+// less than half of an SM, so the next layer's CTA fits beside it.
+//
+// Work split.  Thread j of a row owns the 32-code chunk j of every row (its
+// 32 activations live in registers for the whole kernel); a row's chunks are
+// spread over the warps of one row group, the CTA's rows over its row groups.
+// Per row a warp adds its lanes' partial sums with shuffles; the warps' sums
+// meet in shared memory and are added in a fixed order at the end.
+#include <algorithm>
+
+#include "device_common.cuh"
+#include "qlin_internal.h"
+#include "tc_common.cuh"
+
+namespace qlin {
+namespace {
+
+constexpr int kGvMaxWarpsPerRow = 12;       // K <= 12 * 32 * 32 = 12288
+constexpr int kGvMaxComputeWarps = 12;
+constexpr int kGvThreadsMax = (kGvMaxComputeWarps + 1) * 32;
+constexpr int kGvCtaBytes = 112 * 1024;     // two CTAs (this layer, the next) fit on one SM
+constexpr int kGvMinStages = 2;
+constexpr int kGvMaxStages = 8;
+constexpr int kGvSiteFull = 1, kGvSiteEmpty = 2, kGvSiteDrain = 3;
+constexpr int kGvRowsPerBatch = 4;          // rows a warp reduces together
+
+struct GvArgs {
+  const __half* x;
+  const uint8_t* wq;
+  const __half* scales;
+  const uint8_t* zeros;
+  __half* y;
+  int32_t* err;
+  int N, K, zpitch;
+  int WPR, RG;                 // warps per row, row groups
+  int R, S, stage_bytes;       // rows per stage, stages
+  int off_sz, off_red, off_bar;
+};
+
+// d = c + sum_i a.byte[i] . b.byte[i], a unsigned bytes, b signed bytes.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// sum_k (n[k] - z) . x_fix[k] over one 32-code chunk (16 bytes), with the NP
+// high byte planes of x_fix.  xp[p][2w] / xp[p][2w + 1] hold plane p's bytes
+// of the even / odd codes of word w; xsum[p] is the sum of plane p.
+template <int NP>
+__device__ __forceinline__ float gv_chunk(uint4 q, const uint32_t (*xp)[8], const int* xsum, int z) {
+  int a0 = 0, a1 = 0, a2 = 0;
+  const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t ev = wd[w] & 0x0F0F0F0Fu, od = (wd[w] >> 4) & 0x0F0F0F0Fu;
+    a0 = dp4a_us(ev, xp[0][2 * w], a0);
+    a1 = dp4a_us(ev, xp[1][2 * w], a1);
+    if (NP == 3) a2 = dp4a_us(ev, xp[2][2 * w], a2);
+    a0 = dp4a_us(od, xp[0][2 * w + 1], a0);
+    a1 = dp4a_us(od, xp[1][2 * w + 1], a1);
+    if (NP == 3) a2 = dp4a_us(od, xp[2][2 * w + 1], a2);
+  }
+  float d = fmaf(static_cast<float>(a0 - z * xsum[0]), 65536.0f, static_cast<float>(a1 - z * xsum[1]) * 256.0f);
+  if (NP == 3) d += static_cast<float>(a2 - z * xsum[2]);
+  return d;
+}
+
+// Rows rg, rg + RG, rg + 2 RG, rg + 3 RG of one stage: the thread's partial
+// sums, computed without branches (indices clamped into the stage, invalid
+// results zeroed) so that the four chunks interleave.
+template <int NP>
+__device__ __forceinline__ void gv_batch(const unsigned char* stg, int rows_i, int row0, int RG, int rg, int row_bytes,
+                                         int G, int jc, bool act, const float2* sz, const uint32_t (*xp)[8],
+                                         const int* xsum, float sx, float* p) {
+#pragma unroll
+  for (int b = 0; b < kGvRowsPerBatch; ++b) {
+    const int rr = rg + RG * b;
+    const int rrc = min(rr, rows_i - 1);
+    const uint4 q = *reinterpret_cast<const uint4*>(stg + rrc * row_bytes + jc * 16);
+    const float2 m = sz[(row0 + rrc) * G + (jc >> 2)];
+    const float c = (m.x * sx) * gv_chunk<NP>(q, xp, xsum, __float_as_int(m.y));
+    p[b] = (act && rr < rows_i) ? c : 0.0f;
+  }
+}
+
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ncw = a.RG * a.WPR;  // compute warps; warp ncw is the producer
+  const int G = a.K >> 7, KC = a.K >> 5, row_bytes = a.K >> 1;
+  const int base = a.N / gridDim.x, extra = a.N % gridDim.x;
+  const int r0 = blockIdx.x * base + min(static_cast<int>(blockIdx.x), extra);
+  const int nrows = base + (static_cast<int>(blockIdx.x) < extra ? 1 : 0);
+  const int nloads = (nrows + a.R - 1) / a.R;
+  const int S = a.S;
+  float2* sz = reinterpret_cast<float2*>(smem + a.off_sz);  // per (row, group): {s, z as int bits}
+  float* red = reinterpret_cast<float*>(smem + a.off_red);
+  const uint32_t ring = tc::smem_u32(smem);
+  const uint32_t bar0 = tc::smem_u32(smem + a.off_bar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + a.off_bar + 16 * S);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(full(s), 1);
+      tc::mbar_init(empty(s), ncw);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  if (warp == ncw) {
+    // ---------------- producer: the CTA's band of weight rows ----------------
+    if (lane == 0) {
+      const uint64_t policy = tc::l2_policy_evict_first();
+      int i = 0;
+      for (; i < nloads; ++i) {
+        const int s = i % S;
+        if (i >= S && !tc::mbar_wait(empty(s), ((i / S) - 1) & 1, a.err, kGvSiteEmpty)) {
+          *abort_flag = 1;
+          break;
+        }
+        if (*abort_flag) break;
+        const int rows_i = min(a.R, nrows - i * a.R);
+        const uint32_t bytes = static_cast<uint32_t>(rows_i * row_bytes);
+        tc::mbar_arrive_expect_tx(full(s), bytes);
+        tc::bulk_load_policy(ring + s * a.stage_bytes, a.wq + static_cast<int64_t>(r0 + i * a.R) * row_bytes, bytes,
+                             full(s), policy);
+      }
+      // The last copy into each stage must have landed before the CTA exits.
+      for (int j = max(0, i - S); j < i; ++j) tc::mbar_wait(full(j % S), (j / S) & 1, a.err, kGvSiteDrain);
+    }
+    return;
+  }
+
+  // ---------------- compute warps ----------------
+  const int nct = ncw * 32;
+  // Scales and zero-points of the band: weights, so read before waiting on
+  // the previous kernel.  Loads are issued in batches so that one batch costs
+  // one memory round trip.
+  {
+    constexpr int kB = 8;
+    const int ne = nrows * G;
+    const __half* sg = a.scales + static_cast<int64_t>(r0) * G;
+    for (int e0 = threadIdx.x; e0 < ne; e0 += kB * nct) {
+      __half sv[kB];
+      uint32_t zv[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int e = e0 + u * nct;
+        zv[u] = 0x88u;
+        if (e < ne) {
+          sv[u] = sg[e];
+          const int r = e / G, g = e - r * G;
+          if (a.zeros) zv[u] = a.zeros[static_cast<int64_t>(r0 + r) * a.zpitch + (g >> 1)] >> ((g & 1) * 4);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int e = e0 + u * nct;
+        if (e < ne) sz[e] = make_float2(__half2float(sv[u]), __int_as_float(static_cast<int>(zv[u] & 0xFu)));
+      }
+    }
+  }
+  const int rg = warp / a.WPR, wr = warp - rg * a.WPR;
+  const int j = wr * 32 + lane;  // this thread's chunk
+  const bool act = j < KC;
+  const int jc = min(j, KC - 1);  // in-bounds chunk for the idle lanes of the last warp
+
+  named_sync(1, nct);  // scales and zero-points are in shared memory
+  pdl_wait();          // the activations may come from the previous kernel
+  uint32_t xp[3][8];         // byte planes hi, mid, lo
+  int xsum[3] = {0, 0, 0};   // plane sums over the chunk
+  float sx = 0.0f;           // x = x_fix . sx
+  bool wide = false;         // chunk needs the low plane
+  if (act) {
+    const uint4* xg = reinterpret_cast<const uint4*>(a.x + j * 32);
+    float xf[32];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint4 u = ldg_v4(xg + w);
+      const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 f = __half22float2(h[t]);
+        xf[8 * w + 2 * t] = f.x;
+        xf[8 * w + 2 * t + 1] = f.y;
+      }
+    }
+    float amax = 0.0f, asum = 0.0f;
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      const float ax = fabsf(xf[t]);
+      amax = fmaxf(amax, ax);
+      asum += ax;
+    }
+    wide = amax > (64.0f / 31.0f) * (asum - amax);
+    sx = amax > 0.0f ? amax * (1.0f / 4161536.0f) : 1.0f;   // 4161536 = 127 . 2^15
+    const float inv = 1.0f / sx;
+    // x_fix + 0x8080: byte 0 ^ 0x80 = lo, byte 1 ^ 0x80 = mid, byte 2 = hi.
+    // x . inv + 1.5 . 2^23 rounds x . inv to an integer (|x . inv| < 2^22).
+    uint32_t vb[32];
+#pragma unroll
+    for (int t = 0; t < 32; ++t) vb[t] = __float_as_uint(fmaf(xf[t], inv, 12582912.0f)) - 0x4B400000u + 0x8080u;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+#pragma unroll
+      for (int par = 0; par < 2; ++par) {
+        const int e = 8 * w + par;  // elements e, e + 2, e + 4, e + 6
+        const uint32_t hi01 = __byte_perm(vb[e], vb[e + 2], 0x0062), hi23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0062);
+        const uint32_t md01 = __byte_perm(vb[e], vb[e + 2], 0x0051), md23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0051);
+        const uint32_t lo01 = __byte_perm(vb[e], vb[e + 2], 0x0040), lo23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0040);
+        xp[0][2 * w + par] = __byte_perm(hi01, hi23, 0x5410);
+        xp[1][2 * w + par] = __byte_perm(md01, md23, 0x5410) ^ 0x80808080u;
+        xp[2][2 * w + par] = __byte_perm(lo01, lo23, 0x5410) ^ 0x80808080u;
+      }
+    }
+#pragma unroll
+    for (int pl = 0; pl < 3; ++pl)
+#pragma unroll
+      for (int w = 0; w < 8; ++w) xsum[pl] = dp4a_us(0x01010101u, xp[pl][w], xsum[pl]);
+  } else {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) xp[0][w] = xp[1][w] = xp[2][w] = 0u;
+  }
+  const bool wide_warp = __any_sync(0xffffffffu, wide);
+
+  const bool b0 = (lane & 1) != 0, b1 = (lane & 2) != 0;
+  for (int i = 0; i < nloads; ++i) {
+    const int s = i % S;
+    bool ok = tc::mbar_wait(full(s), (i / S) & 1, a.err, kGvSiteFull);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) {
+      *abort_flag = 1;
+      break;
+    }
+    const int rows_i = min(a.R, nrows - i * a.R);
+    const unsigned char* stg = smem + s * a.stage_bytes;
+    float p[kGvRowsPerBatch];
+    if (wide_warp)
+      gv_batch<3>(stg, rows_i, i * a.R, a.RG, rg, row_bytes, G, jc, act, sz, xp, xsum, sx, p);
+    else
+      gv_batch<2>(stg, rows_i, i * a.R, a.RG, rg, row_bytes, G, jc, act, sz, xp, xsum, sx, p);
+    // Butterfly: after the xor-1 and xor-2 steps lane l holds row 2 (l & 1) +
+    // ((l >> 1) & 1) summed over its 4-lane group, then over all 32 lanes.
+    float k0 = b0 ? p[2] : p[0], k1 = b0 ? p[3] : p[1];
+    const float s0 = b0 ? p[0] : p[2], s1 = b0 ? p[1] : p[3];
+    k0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    k1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    float k = b1 ? k1 : k0;
+    k += __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
+    k += __shfl_xor_sync(0xffffffffu, k, 4);
+    k += __shfl_xor_sync(0xffffffffu, k, 8);
+    k += __shfl_xor_sync(0xffffffffu, k, 16);
+    if (lane < kGvRowsPerBatch) {
+      const int rr = rg + a.RG * (2 * (lane & 1) + (lane >> 1));
+      if (rr < rows_i) red[(i * a.R + rr) * a.WPR + wr] = k;
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(empty(s));
+  }
+  named_sync(1, nct);
+  if (*abort_flag) return;
+  for (int r = threadIdx.x; r < nrows; r += nct) {
+    float v = 0.0f;
+    for (int w = 0; w < a.WPR; ++w) v += red[r * a.WPR + w];
+    a.y[r0 + r] = __float2half_rn(v);
+  }
+}
+
+// Shared-memory plan of one launch; false when the band's scales do not
+// leave room for a double-buffered ring within the per-CTA budget.
+bool gv_plan(int64_t N, int64_t K, GvArgs& a, int& grid, int& smem) {
+  if (K > static_cast<int64_t>(kGvMaxWarpsPerRow) * 32 * 32 || N <= 0) return false;
+  const int G = static_cast<int>(K / 128), KC = static_cast<int>(K / 32), row_bytes = static_cast<int>(K / 2);
+  a.WPR = (KC + 31) / 32;
+  a.RG = a.WPR >= 8 ? 1 : 8 / a.WPR;
+  grid = static_cast<int>(std::min<int64_t>(sm_count(), (N + a.RG - 1) / a.RG));
+  const int rows_max = static_cast<int>((N + grid - 1) / grid);
+  // A stage holds one batch of rows for every row group.
+  a.R = std::min(kGvRowsPerBatch * a.RG, rows_max);
+  a.stage_bytes = a.R * row_bytes;
+  auto up = [](int v, int m) { return (v + m - 1) / m * m; };
+  const int extras = up(rows_max * G * 8, 16) + up(rows_max * a.WPR * 4, 16) + 16 * kGvMaxStages + 16 + 128;
+  const int loads_max = (rows_max + a.R - 1) / a.R;
+  a.S = std::min({kGvMaxStages, (kGvCtaBytes - extras) / a.stage_bytes, loads_max});
+  if (a.S < std::min(kGvMinStages, loads_max)) return false;
+  a.off_sz = up(a.S * a.stage_bytes, 128);
+  a.off_red = a.off_sz + up(rows_max * G * 8, 16);
+  a.off_bar = a.off_red + up(rows_max * a.WPR * 4, 16);
+  smem = a.off_bar + 16 * a.S + 16;
+  return true;
+}
+
+}  // namespace
+
+bool w4a16_gemv_supported(int64_t T, int64_t N, int64_t K) {
+  GvArgs a = {};
+  int grid = 0, smem = 0;
+  return T == 1 && gv_plan(N, K, a, grid, smem);
+}
+
+cudaError_t launch_w4a16_gemv(const void* x, int64_t N, int64_t K, const uint8_t* wq, const void* scales,
+                              const uint8_t* zeros, void* y, cudaStream_t stream) {
+  if (N == 0) return cudaSuccess;
+  GvArgs a = {};
+  int grid = 0, smem = 0;
+  if (!gv_plan(N, K, a, grid, smem)) return cudaErrorInvalidValue;
+  a.x = static_cast<const __half*>(x);
+  a.wq = wq;
+  a.scales = static_cast<const __half*>(scales);
+  a.zeros = zeros;
+  a.y = static_cast<__half*>(y);
+  a.err = device_error_word();
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.zpitch = static_cast<int>((K / 128 + 1) / 2);
+  cudaError_t e = cudaFuncSetAttribute(w4a16_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3((a.RG * a.WPR + 1) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w4a16_gemv_kernel, a);
+}
+
+}  // namespace qlin

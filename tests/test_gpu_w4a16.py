@@ -92,3 +92,31 @@ def test_llama_decode_layers(qlin_gpu, N, K):
         ref = oracle.w4a16_reference(x, codes, s16, z)
         y = _gemm(qlin_gpu, _dev(x), wq, sc, zp)
         assert_within_tolerance(y, ref, "W4A16 N=%d K=%d T=%d" % (N, K, T))
+
+
+@pytest.mark.parametrize("scale", [1e3, 3e4])
+def test_decode_activation_outliers(qlin_gpu, scale):
+    """Large activation outliers next to ordinary ones in the same 32-element
+    chunk; in half of the rows the outlier channels carry code = zero-point,
+    so those outputs come from the ordinary activations alone."""
+    d = inputs.w4a16_decode(seed=23, T=1, N=512, K=4096)
+    x = d["x"].astype(np.float32)
+    idx = np.random.default_rng(5).choice(4096, 16, replace=False)
+    x[0, idx] *= scale
+    x = np.clip(x, -60000.0, 60000.0).astype(np.float16)
+    codes, s16, z = oracle.quant_w4_g128(d["w"])
+    codes[:256, idx] = z[:256, idx // 128]
+    ref = oracle.w4a16_reference(x, codes, s16, z)
+    y = _gemm(qlin_gpu, _dev(x), _dev(oracle.pack_u4(codes)), _dev(s16), _dev(oracle.pack_u4(z)))
+    assert_within_tolerance(y, ref, "W4A16 outliers x%g" % scale)
+
+
+def test_decode_band_split_shapes(qlin_gpu):
+    """Row counts that split unevenly over the CTAs and K with a partial last
+    warp of 32-code chunks (K = 1408: 44 chunks)."""
+    for (n, k) in ((763, 4096), (1000, 1408), (1, 128), (3, 384)):
+        d = inputs.w4a16_decode(seed=29, T=1, N=n, K=k)
+        codes, s16, z = oracle.quant_w4_g128(d["w"])
+        ref = oracle.w4a16_reference(d["x"], codes, s16, z)
+        y = _gemm(qlin_gpu, _dev(d["x"]), _dev(oracle.pack_u4(codes)), _dev(s16), _dev(oracle.pack_u4(z)))
+        assert_within_tolerance(y, ref, "W4A16 N=%d K=%d" % (n, k))
