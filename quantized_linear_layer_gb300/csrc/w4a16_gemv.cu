@@ -40,6 +40,7 @@
 // Per row a warp adds its lanes' partial sums with shuffles; the warps' sums
 // meet in shared memory and are added in a fixed order at the end.
 #include <algorithm>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "qlin_internal.h"
@@ -77,43 +78,62 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
-// sum_k (n[k] - z) . x_fix[k] over one 32-code chunk (16 bytes), with the NP
-// high byte planes of x_fix.  xp[p][2w] / xp[p][2w + 1] hold plane p's bytes
-// of the even / odd codes of word w; xsum[p] is the sum of plane p.
+// sum_k (n[k] - z) . x_fix[k] over one 32-code chunk (16 bytes).
+// xp[p][2w] / xp[p][2w + 1] hold byte plane p of the even / odd codes of
+// word w.  The even codes are masked to bytes in place (w & 0x0F0F0F0F); the
+// odd ones stay in the high nibble of their byte (w & 0xF0F0F0F0 = 16 n) and
+// get their own accumulators, whose factor 16 is divided out in the fp32
+// combination.  Every partial sum is an exact integer below 2^20.
+//   NP = 2: the two high planes; the zero-point term z . sum(x_fix) (xzf,
+//           rounded to fp32) is subtracted in fp32.
+//   NP = 3: all three planes, the zero-point term subtracted per plane in
+//           int32 (exact), for chunks with activation outliers.
 template <int NP>
-__device__ __forceinline__ float gv_chunk(uint4 q, const uint32_t (*xp)[8], const int* xsum, int z) {
-  int a0 = 0, a1 = 0, a2 = 0;
+__device__ __forceinline__ float gv_chunk(uint4 q, const uint32_t (*xp)[8], const int* xsum, float xzf, int z) {
+  int he = 0, ho = 0, me = 0, mo = 0, le = 0, lo = 0;
   const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    const uint32_t ev = wd[w] & 0x0F0F0F0Fu, od = (wd[w] >> 4) & 0x0F0F0F0Fu;
-    a0 = dp4a_us(ev, xp[0][2 * w], a0);
-    a1 = dp4a_us(ev, xp[1][2 * w], a1);
-    if (NP == 3) a2 = dp4a_us(ev, xp[2][2 * w], a2);
-    a0 = dp4a_us(od, xp[0][2 * w + 1], a0);
-    a1 = dp4a_us(od, xp[1][2 * w + 1], a1);
-    if (NP == 3) a2 = dp4a_us(od, xp[2][2 * w + 1], a2);
+    const uint32_t ev = wd[w] & 0x0F0F0F0Fu, od = wd[w] & 0xF0F0F0F0u;
+    he = dp4a_us(ev, xp[0][2 * w], he);
+    ho = dp4a_us(od, xp[0][2 * w + 1], ho);
+    me = dp4a_us(ev, xp[1][2 * w], me);
+    mo = dp4a_us(od, xp[1][2 * w + 1], mo);
+    if (NP == 3) {
+      le = dp4a_us(ev, xp[2][2 * w], le);
+      lo = dp4a_us(od, xp[2][2 * w + 1], lo);
+    }
   }
-  float d = fmaf(static_cast<float>(a0 - z * xsum[0]), 65536.0f, static_cast<float>(a1 - z * xsum[1]) * 256.0f);
-  if (NP == 3) d += static_cast<float>(a2 - z * xsum[2]);
-  return d;
+  if (NP == 2) {
+    const float d = fmaf(static_cast<float>(he), 65536.0f,
+                         fmaf(static_cast<float>(ho), 4096.0f,
+                              fmaf(static_cast<float>(me), 256.0f, static_cast<float>(mo) * 16.0f)));
+    return fmaf(-static_cast<float>(z), xzf, d);
+  } else {
+    // (odd sums are multiples of 16: the shifts are exact)
+    const int h = he + (ho >> 4) - z * xsum[0];
+    const int m = me + (mo >> 4) - z * xsum[1];
+    const int l = le + (lo >> 4) - z * xsum[2];
+    return fmaf(static_cast<float>(h), 65536.0f, fmaf(static_cast<float>(m), 256.0f, static_cast<float>(l)));
+  }
 }
 
 // Rows rg, rg + RG, rg + 2 RG, rg + 3 RG of one stage: the thread's partial
-// sums, computed without branches (indices clamped into the stage, invalid
-// results zeroed) so that the four chunks interleave.
+// sums.  Row indices past the stage are clamped to its last row (their sums
+// are never stored), so the four chunks run without branches and interleave;
+// idle lanes have zero activations and contribute 0.
 template <int NP>
 __device__ __forceinline__ void gv_batch(const unsigned char* stg, int rows_i, int row0, int RG, int rg, int row_bytes,
-                                         int G, int jc, bool act, const float2* sz, const uint32_t (*xp)[8],
-                                         const int* xsum, float sx, float* p) {
+                                         int G, int jc, const float2* sz, const uint32_t (*xp)[8], const int* xsum,
+                                         float xzf, float sx, float* p) {
+  const unsigned char* cbase = stg + jc * 16;
+  const float2* sbase = sz + row0 * G + (jc >> 2);
 #pragma unroll
   for (int b = 0; b < kGvRowsPerBatch; ++b) {
-    const int rr = rg + RG * b;
-    const int rrc = min(rr, rows_i - 1);
-    const uint4 q = *reinterpret_cast<const uint4*>(stg + rrc * row_bytes + jc * 16);
-    const float2 m = sz[(row0 + rrc) * G + (jc >> 2)];
-    const float c = (m.x * sx) * gv_chunk<NP>(q, xp, xsum, __float_as_int(m.y));
-    p[b] = (act && rr < rows_i) ? c : 0.0f;
+    const int rrc = min(rg + RG * b, rows_i - 1);
+    const uint4 q = *reinterpret_cast<const uint4*>(cbase + rrc * row_bytes);
+    const float2 m = sbase[rrc * G];
+    p[b] = (m.x * sx) * gv_chunk<NP>(q, xp, xsum, xzf, __float_as_int(m.y));
   }
 }
 
@@ -208,8 +228,11 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
   const bool act = j < KC;
   const int jc = min(j, KC - 1);  // in-bounds chunk for the idle lanes of the last warp
 
-  named_sync(1, nct);  // scales and zero-points are in shared memory
-  pdl_wait();          // the activations may come from the previous kernel
+  // The activations may come from the previous kernel: one warp waits for it,
+  // the others block on the named barrier (which also publishes the scales
+  // and zero-points) instead of polling.
+  if (warp == 0) pdl_wait();
+  named_sync(1, nct);
   uint32_t xp[3][8];         // byte planes hi, mid, lo
   int xsum[3] = {0, 0, 0};   // plane sums over the chunk
   float sx = 0.0f;           // x = x_fix . sx
@@ -265,41 +288,62 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
     for (int w = 0; w < 8; ++w) xp[0][w] = xp[1][w] = xp[2][w] = 0u;
   }
   const bool wide_warp = __any_sync(0xffffffffu, wide);
+  // sum(x_fix) of the two high planes (what the two-plane dot products see)
+  const float xzf = fmaf(static_cast<float>(xsum[0]), 65536.0f, static_cast<float>(xsum[1]) * 256.0f);
 
   const bool b0 = (lane & 1) != 0, b1 = (lane & 2) != 0;
-  for (int i = 0; i < nloads; ++i) {
-    const int s = i % S;
-    bool ok = tc::mbar_wait(full(s), (i / S) & 1, a.err, kGvSiteFull);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) {
-      *abort_flag = 1;
-      break;
+  // The consume loop, instantiated once per plane count so that the common
+  // two-plane loop does not keep the low plane live.
+  auto consume = [&](auto np) {
+    constexpr int NP = decltype(np)::value;
+    // The reduction of one batch runs in the same block as the dot products
+    // of the next, so that the shuffles' latency overlaps the dp4a work.
+    float prev[kGvRowsPerBatch] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int prev_row0 = -1, prev_rows = 0;
+    auto reduce_store = [&](const float* v, int row0, int rows) {
+      // Butterfly: after the xor-1 and xor-2 steps lane l holds row
+      // 2 (l & 1) + ((l >> 1) & 1) summed over its 4-lane group, then over
+      // all 32 lanes.
+      float k0 = b0 ? v[2] : v[0], k1 = b0 ? v[3] : v[1];
+      const float s0 = b0 ? v[0] : v[2], s1 = b0 ? v[1] : v[3];
+      k0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+      k1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+      float k = b1 ? k1 : k0;
+      k += __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
+      k += __shfl_xor_sync(0xffffffffu, k, 4);
+      k += __shfl_xor_sync(0xffffffffu, k, 8);
+      k += __shfl_xor_sync(0xffffffffu, k, 16);
+      if (lane < kGvRowsPerBatch) {
+        const int rr = rg + a.RG * (2 * (lane & 1) + (lane >> 1));
+        if (rr < rows) red[(row0 + rr) * a.WPR + wr] = k;
+      }
+    };
+    for (int i = 0; i < nloads; ++i) {
+      const int s = i % S;
+      bool ok = tc::mbar_wait(full(s), (i / S) & 1, a.err, kGvSiteFull);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        *abort_flag = 1;
+        break;
+      }
+      const int rows_i = min(a.R, nrows - i * a.R);
+      float p[kGvRowsPerBatch];
+      gv_batch<NP>(smem + s * a.stage_bytes, rows_i, i * a.R, a.RG, rg, row_bytes, G, jc, sz, xp, xsum, xzf, sx, p);
+      // The stage's codes are in registers: hand it back to the producer.
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(empty(s));
+      if (prev_row0 >= 0) reduce_store(prev, prev_row0, prev_rows);
+#pragma unroll
+      for (int b = 0; b < kGvRowsPerBatch; ++b) prev[b] = p[b];
+      prev_row0 = i * a.R;
+      prev_rows = rows_i;
     }
-    const int rows_i = min(a.R, nrows - i * a.R);
-    const unsigned char* stg = smem + s * a.stage_bytes;
-    float p[kGvRowsPerBatch];
-    if (wide_warp)
-      gv_batch<3>(stg, rows_i, i * a.R, a.RG, rg, row_bytes, G, jc, act, sz, xp, xsum, sx, p);
-    else
-      gv_batch<2>(stg, rows_i, i * a.R, a.RG, rg, row_bytes, G, jc, act, sz, xp, xsum, sx, p);
-    // Butterfly: after the xor-1 and xor-2 steps lane l holds row 2 (l & 1) +
-    // ((l >> 1) & 1) summed over its 4-lane group, then over all 32 lanes.
-    float k0 = b0 ? p[2] : p[0], k1 = b0 ? p[3] : p[1];
-    const float s0 = b0 ? p[0] : p[2], s1 = b0 ? p[1] : p[3];
-    k0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-    k1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-    float k = b1 ? k1 : k0;
-    k += __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
-    k += __shfl_xor_sync(0xffffffffu, k, 4);
-    k += __shfl_xor_sync(0xffffffffu, k, 8);
-    k += __shfl_xor_sync(0xffffffffu, k, 16);
-    if (lane < kGvRowsPerBatch) {
-      const int rr = rg + a.RG * (2 * (lane & 1) + (lane >> 1));
-      if (rr < rows_i) red[(i * a.R + rr) * a.WPR + wr] = k;
-    }
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(empty(s));
-  }
+    if (prev_row0 >= 0) reduce_store(prev, prev_row0, prev_rows);
+  };
+  if (wide_warp)
+    consume(std::integral_constant<int, 3>());
+  else
+    consume(std::integral_constant<int, 2>());
   named_sync(1, nct);
   if (*abort_flag) return;
   for (int r = threadIdx.x; r < nrows; r += nct) {
