@@ -41,7 +41,7 @@ LLAMA_BLOCK = [(4096, 4096)] * 4 + [(11008, 4096)] * 2 + [(4096, 11008)]
 W8A8 = dict(T=2048, K=4096, N=4096)
 NVFP4 = dict(T=2048, K=4096, N=4096, S=128)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "w4a16_decode_stack_traffic.txt")
-W4A16_SOURCE = os.path.join(ROOT, "quantized_linear_layer_gb300", "csrc", "w4a16_gemm.cu")
+W4A16_SOURCE = os.path.join(ROOT, "quantized_linear_layer_gb300", "csrc", "w4a16_gemv.cu")
 
 
 def w4a16_bytes(N, K, T):
@@ -390,7 +390,7 @@ def run_ours(args):
                       "frac_of_fp4_tensor_peak": round(nv_ops / tnv / 1e12 / (peak16 * 6.0), 4)},
         },
         "roofline": {
-            "kernel": "w4a16_mma_kernel (fused dequant GEMV, T=1)",
+            "kernel": "w4a16_gemv_kernel (fused dequant GEMV, T=1)",
             "bound": "hbm",
             "achieved": round(per_launch_bytes / per_launch_s / 1e9, 1),
             "peak": peaks["hbm_gbs"],
