@@ -118,23 +118,39 @@ __device__ __forceinline__ float gv_chunk(uint4 q, const uint32_t (*xp)[8], cons
   }
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float2 lds64f(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+
 // Rows rg, rg + RG, rg + 2 RG, rg + 3 RG of one stage: the thread's partial
 // sums.  Row indices past the stage are clamped to its last row (their sums
 // are never stored), so the four chunks run without branches and interleave;
-// idle lanes have zero activations and contribute 0.
+// idle lanes have zero activations and contribute 0.  Addresses are 32-bit
+// shared-window offsets: cbase = the thread's chunk in the stage, sbase = its
+// group's {scale, zero} of the stage's first row.
 template <int NP>
-__device__ __forceinline__ void gv_batch(const unsigned char* stg, int rows_i, int row0, int RG, int rg, int row_bytes,
-                                         int G, int jc, const float2* sz, const uint32_t (*xp)[8], const int* xsum,
-                                         float xzf, float sx, float* p) {
-  const unsigned char* cbase = stg + jc * 16;
-  const float2* sbase = sz + row0 * G + (jc >> 2);
+__device__ __forceinline__ void gv_batch(uint32_t cbase, uint32_t sbase, int rows_i, int RG, int rg, int row_bytes,
+                                         int G, const uint32_t (*xp)[8], const int* xsum, float xzf, float sx,
+                                         float* p) {
+  uint4 q[kGvRowsPerBatch];
+  float2 m[kGvRowsPerBatch];
 #pragma unroll
   for (int b = 0; b < kGvRowsPerBatch; ++b) {
     const int rrc = min(rg + RG * b, rows_i - 1);
-    const uint4 q = *reinterpret_cast<const uint4*>(cbase + rrc * row_bytes);
-    const float2 m = sbase[rrc * G];
-    p[b] = (m.x * sx) * gv_chunk<NP>(q, xp, xsum, xzf, __float_as_int(m.y));
+    q[b] = lds128(cbase + rrc * row_bytes);
+    m[b] = lds64f(sbase + rrc * G * 8);
   }
+#pragma unroll
+  for (int b = 0; b < kGvRowsPerBatch; ++b)
+    p[b] = (m[b].x * sx) * gv_chunk<NP>(q[b], xp, xsum, xzf, __float_as_int(m[b].y));
 }
 
 __device__ __forceinline__ void named_sync(int id, int threads) {
@@ -292,6 +308,7 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
   const float xzf = fmaf(static_cast<float>(xsum[0]), 65536.0f, static_cast<float>(xsum[1]) * 256.0f);
 
   const bool b0 = (lane & 1) != 0, b1 = (lane & 2) != 0;
+  const uint32_t sz_base = tc::smem_u32(sz + (jc >> 2));  // this thread's group column
   // The consume loop, instantiated once per plane count so that the common
   // two-plane loop does not keep the low plane live.
   auto consume = [&](auto np) {
@@ -328,7 +345,8 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
       }
       const int rows_i = min(a.R, nrows - i * a.R);
       float p[kGvRowsPerBatch];
-      gv_batch<NP>(smem + s * a.stage_bytes, rows_i, i * a.R, a.RG, rg, row_bytes, G, jc, sz, xp, xsum, xzf, sx, p);
+      gv_batch<NP>(ring + s * a.stage_bytes + jc * 16, sz_base + (i * a.R * G) * 8, rows_i, a.RG, rg, row_bytes, G, xp,
+                   xsum, xzf, sx, p);
       // The stage's codes are in registers: hand it back to the producer.
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(empty(s));
