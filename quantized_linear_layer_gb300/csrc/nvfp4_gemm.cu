@@ -294,9 +294,9 @@ cudaError_t launch_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_
   if (T == 0 || N == 0) return cudaSuccess;
   CUtensorMap tmA, tmB;
   cudaError_t st = make_tmap_2d_u8(&tmA, a, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(T), kBKB, kBM,
-                                   /*swizzle128=*/true);
+                                   /*swizzle_bytes=*/128);
   if (st != cudaSuccess) return st;
-  st = make_tmap_2d_u8(&tmB, b, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(N), kBKB, kBN, true);
+  st = make_tmap_2d_u8(&tmB, b, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(N), kBKB, kBN, 128);
   if (st != cudaSuccess) return st;
   st = cudaFuncSetAttribute(nvfp4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
   if (st != cudaSuccess) return st;

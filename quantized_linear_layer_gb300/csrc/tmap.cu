@@ -24,7 +24,7 @@ void resolve_encode() {
 }  // namespace
 
 cudaError_t make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                            uint32_t box_rows, bool swizzle128) {
+                            uint32_t box_rows, int swizzle_bytes) {
   std::call_once(g_encode_once, resolve_encode);
   if (g_encode == nullptr) return g_encode_status != cudaSuccess ? g_encode_status : cudaErrorNotSupported;
   const cuuint64_t dims[2] = {cols, rows};
@@ -33,7 +33,9 @@ cudaError_t make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t cols, u
   const cuuint32_t elem_strides[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
                         elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                        : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

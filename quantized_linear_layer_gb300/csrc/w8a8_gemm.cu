@@ -18,20 +18,32 @@
 // chunk's fp32 accumulator is converted to int32 and added in int32, which
 // gives D^ bit for bit.
 //
-// Kernel structure (one CTA per 128 x 128 output tile, 10 warps):
-//   warp 0      TMA producer: int8 tiles of A and B (128 x 64 bytes each)
-//               into a 4-stage staging ring.
-//   warp 1      TMEM allocation and the MMA issuer: 4 x tcgen05.mma
-//               (M=128, N=128, K=16, fp16 -> fp32) per 64-wide K stage into
-//               one of two 128-column TMEM accumulators (one per K chunk,
-//               double buffered).
-//   warps 2-5   converters: int8 staging -> fp16 operand ring in the 128-byte
-//               swizzled K-major layout the MMA descriptors describe.  The
-//               conversion is a byte permute into the low mantissa of fp16
-//               1024 and one half2 subtract per two codes.
-//   warps 6-9   epilogue: drain each finished chunk accumulator into int32
-//               registers (one output row per thread), then apply the
-//               epilogue and store.
+// Design for GB300.  The int8 -> fp16 widening is the expensive part: done
+// through shared memory it costs a load, a store of twice the bytes and the
+// MMA's read of them.  Here A is widened in registers and written straight
+// into tensor memory (the MMA reads its A operand from TMEM), so only B
+// passes through shared memory as fp16.  The kernel is persistent: one CTA
+// per SM walks 128 x 128 output tiles (groups of 8 row tiles share column
+// tiles for L2 reuse), and the epilogue of a tile overlaps the MMAs of the
+// next through two chunk accumulators.
+//
+//   warp 0       TMA producer: int8 tiles of A (64-byte swizzle) and B
+//                (128 x 64 bytes each) into a 6-stage staging ring.
+//   warp 1       TMEM allocation and the MMA issuer: 4 x tcgen05.mma
+//                (M=N=128, K=16, A from TMEM, B from shared memory) per
+//                64-wide K stage into one of two 128-column accumulators.
+//   warps 2-5    A wideners: lane l of the warp with TMEM lane quadrant q owns
+//                row 32q + l, widens its 64 codes and stores them with one
+//                tcgen05.st into a 4-stage A ring in TMEM.
+//   warps 6-9    B wideners: int8 staging -> fp16 operand ring in the
+//                128-byte swizzled K-major layout the MMA descriptors
+//                describe (4 stages).
+//   warps 10-13  epilogue: lane l of quadrant q owns output row 32q + l; each
+//                finished chunk is converted to int32 and added to a running
+//                int32 total kept in TMEM; after the last chunk of a tile the
+//                epilogue is applied and the row is stored.
+// TMEM columns: [0,256) two chunk accumulators, [256,384) the int32 total,
+// [384,512) the A ring.
 // Every barrier wait is bounded; on expiry the kernel records the site in the
 // device error word, stops issuing work, waits (bounded) for copies and MMAs
 // already in flight, frees TMEM and exits.
@@ -46,25 +58,38 @@ namespace qlin {
 namespace {
 
 constexpr int kBM = 128, kBN = 128, kBK = 64;
-constexpr int kStg = 4;             // int8 staging stages
-constexpr int kOps = 4;             // fp16 operand stages
+constexpr int kStg = 6;             // int8 staging stages (A and B)
+constexpr int kOpsA = 4;            // fp16 A stages in TMEM
+constexpr int kOpsB = 4;            // fp16 B stages in shared memory
 constexpr int kChunkK = 1024;       // exact fp32 accumulation span
 constexpr int kKbPerChunk = kChunkK / kBK;
-constexpr int kTmemCols = 2 * kBN;  // two accumulator buffers
-constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;
+constexpr int kTmemTotal = 2 * kBN;         // int32 running total
+constexpr int kTmemA = kTmemTotal + kBN;    // A ring, 32 columns per stage
+constexpr int kThreads = 14 * 32;
 
 constexpr int kStgBytes = (kBM + kBN) * kBK;            // 16 KB (A then B)
-constexpr int kOpBytes = (kBM + kBN) * kBK * 2;         // 32 KB (A then B, fp16)
+constexpr int kOpBytesB = kBN * kBK * 2;                // 16 KB fp16
 constexpr int kSmemStg = 0;
-constexpr int kSmemOps = kSmemStg + kStg * kStgBytes;                 // 64 KB
-constexpr int kSmemPar = kSmemOps + kOps * kOpBytes;                  // 192 KB
-constexpr int kSmemBar = kSmemPar + 3 * kBN * 4;                      // +1.5 KB
-constexpr int kNumBars = 2 * kStg + 2 * kOps + 2 + 2 + 1;
+constexpr int kSmemOps = kSmemStg + kStg * kStgBytes;   // 96 KB
+constexpr int kSmemPar = kSmemOps + kOpsB * kOpBytesB;  // 160 KB
+constexpr int kSmemBar = kSmemPar + 4 * 3 * kBN * 4;    // + 6 KB (column parameters, one copy per epilogue warp)
+constexpr int kNumBars = 2 * kStg + 2 * kOpsA + 2 * kOpsB + 2 + 2 + 1;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
-constexpr int kSmemTotal = kSmemMisc + 16 + 1024;                     // + alignment slack
+constexpr int kSmemTotal = kSmemMisc + 16 + 1024;       // + alignment slack
 
 // Sites recorded in the device error word when a wait expires.
-enum { kSiteStgEmpty = 1, kSiteStgFull, kSiteOpEmpty, kSiteOpFull, kSiteAccEmpty, kSiteAccFull, kSiteDrain };
+enum {
+  kSiteStgEmpty = 1,
+  kSiteStgFull,
+  kSiteAEmpty,
+  kSiteAFull,
+  kSiteBEmpty,
+  kSiteBFull,
+  kSiteAccEmpty,
+  kSiteAccFull,
+  kSiteDrain
+};
 
 struct EpiArgs {
   const float* scale_a;
@@ -80,11 +105,10 @@ __device__ __forceinline__ uint32_t h2_sub_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-// 16 int8 codes -> 16 exact fp16 values (two 16-byte chunks).
-__device__ __forceinline__ void int8x16_to_f16(uint4 v, uint4& h0, uint4& h1) {
+// 16 int8 codes -> 8 words of exact fp16 pairs (codes 2i, 2i+1 in word i).
+__device__ __forceinline__ void int8x16_to_f16(uint4 v, uint32_t* o) {
   const uint32_t kBias = 0x64806480u;  // fp16 (1152, 1152) = 1024 + 128
-  uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
-  uint32_t o[8];
+  const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     // fp16 with exponent of 1024 and the offset code (code + 128) in the low
@@ -92,8 +116,6 @@ __device__ __forceinline__ void int8x16_to_f16(uint4 v, uint4& h0, uint4& h1) {
     o[2 * i] = h2_sub_u32(__byte_perm(w[i], 0x64646464u, 0x4140), kBias);
     o[2 * i + 1] = h2_sub_u32(__byte_perm(w[i], 0x64646464u, 0x4342), kBias);
   }
-  h0 = make_uint4(o[0], o[1], o[2], o[3]);
-  h1 = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -113,6 +135,19 @@ __device__ __forceinline__ float load_as_float(const void* p, int dtype, int i) 
   return static_cast<const float*>(p)[i];
 }
 
+// Output tile `tile` in the persistent order: groups of 8 row tiles walk the
+// column tiles together, so the B tiles of a column are reused from L2.
+__device__ __forceinline__ void tile_coords(int tile, int mt_count, int nt_count, int& mt, int& nt) {
+  constexpr int kGroup = 8;
+  const int per_group = kGroup * nt_count;
+  const int grp = tile / per_group;
+  const int first_m = grp * kGroup;
+  const int rows = min(kGroup, mt_count - first_m);
+  const int in = tile - grp * per_group;
+  mt = first_m + in % rows;
+  nt = in / rows;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                 const __grid_constant__ CUtensorMap tmB, int T,
                                                                 int N, int K, EpiArgs epi, void* __restrict__ out,
@@ -121,7 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
+  const int mt_count = (T + kBM - 1) / kBM, nt_count = (N + kBN - 1) / kBN;
+  const int tiles = mt_count * nt_count;
+  const int my_tiles = blockIdx.x < tiles ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   const int num_kb = (K + kBK - 1) / kBK;
   const int num_chunks = (num_kb + kKbPerChunk - 1) / kKbPerChunk;
 
@@ -129,21 +166,33 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
   const uint32_t bar0 = sbase + kSmemBar;
   auto stg_full = [&](int s) { return bar0 + 8u * s; };
   auto stg_empty = [&](int s) { return bar0 + 8u * (kStg + s); };
-  auto op_full = [&](int o) { return bar0 + 8u * (2 * kStg + o); };
-  auto op_empty = [&](int o) { return bar0 + 8u * (2 * kStg + kOps + o); };
-  auto acc_full = [&](int b) { return bar0 + 8u * (2 * kStg + 2 * kOps + b); };
-  auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kStg + 2 * kOps + 2 + b); };
-  const uint32_t mma_done = bar0 + 8u * (2 * kStg + 2 * kOps + 4);
+  auto a_full = [&](int o) { return bar0 + 8u * (2 * kStg + o); };
+  auto a_empty = [&](int o) { return bar0 + 8u * (2 * kStg + kOpsA + o); };
+  auto b_full = [&](int o) { return bar0 + 8u * (2 * kStg + 2 * kOpsA + o); };
+  auto b_empty = [&](int o) { return bar0 + 8u * (2 * kStg + 2 * kOpsA + kOpsB + o); };
+  auto acc_full = [&](int b) { return bar0 + 8u * (2 * kStg + 2 * kOpsA + 2 * kOpsB + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kStg + 2 * kOpsA + 2 * kOpsB + 2 + b); };
+  const uint32_t mma_done = bar0 + 8u * (2 * kStg + 2 * kOpsA + 2 * kOpsB + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
-  float* par_sb = reinterpret_cast<float*>(smem + kSmemPar);
-  int32_t* par_adj = reinterpret_cast<int32_t*>(smem + kSmemPar + kBN * 4);
-  float* par_bias = reinterpret_cast<float*>(smem + kSmemPar + 2 * kBN * 4);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStg; ++s) { tc::mbar_init(stg_full(s), 1); tc::mbar_init(stg_empty(s), 4); }
-    for (int o = 0; o < kOps; ++o) { tc::mbar_init(op_full(o), 4); tc::mbar_init(op_empty(o), 1); }
-    for (int b = 0; b < 2; ++b) { tc::mbar_init(acc_full(b), 1); tc::mbar_init(acc_empty(b), 4); }
+    for (int s = 0; s < kStg; ++s) {
+      tc::mbar_init(stg_full(s), 1);
+      tc::mbar_init(stg_empty(s), 8);  // four A and four B widener warps
+    }
+    for (int o = 0; o < kOpsA; ++o) {
+      tc::mbar_init(a_full(o), 4);
+      tc::mbar_init(a_empty(o), 1);
+    }
+    for (int o = 0; o < kOpsB; ++o) {
+      tc::mbar_init(b_full(o), 4);
+      tc::mbar_init(b_empty(o), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(acc_full(b), 1);
+      tc::mbar_init(acc_empty(b), 4);
+    }
     tc::mbar_init(mma_done, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -151,17 +200,6 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
   if (warp == 1) {
     tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
     tc::tmem_relinquish();
-  }
-  if (warp >= 6) {
-    // Per-column epilogue parameters of this tile.
-    const int col = threadIdx.x - 192;  // 0..127
-    const int n = n0 + col;
-    const bool inb = n < N;
-    if (epi.out_dtype != QLIN_I32) {
-      par_sb[col] = inb ? (epi.scale_b_per_col ? epi.scale_b[n] : epi.scale_b[0]) : 0.0f;
-      par_adj[col] = (inb && epi.azp_adj != nullptr) ? epi.azp_adj[n] : 0;
-      par_bias[col] = (inb && epi.bias != nullptr) ? load_as_float(epi.bias, epi.bias_dtype, n) : 0.0f;
-    }
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -173,24 +211,28 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
     if (lane == 0) {
       tc::prefetch_tmap(&tmA);
       tc::prefetch_tmap(&tmB);
-      int issued = 0;
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const int s = kb % kStg;
-        if (kb >= kStg && !tc::mbar_wait(stg_empty(s), ((kb / kStg) - 1) & 1, err, kSiteStgEmpty)) {
-          *abort_flag = 1;
-          break;
+      int it = 0, issued = 0;
+      for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
+        int mt, nt;
+        tile_coords(blockIdx.x + ti * gridDim.x, mt_count, nt_count, mt, nt);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % kStg;
+          if (it >= kStg && !tc::mbar_wait(stg_empty(s), ((it / kStg) - 1) & 1, err, kSiteStgEmpty)) {
+            *abort_flag = 1;
+            break;
+          }
+          if (*abort_flag) break;
+          const uint32_t dst = sbase + kSmemStg + s * kStgBytes;
+          tc::mbar_arrive_expect_tx(stg_full(s), kStgBytes);
+          tc::tma_load_2d(dst, &tmA, kb * kBK, mt * kBM, stg_full(s));
+          tc::tma_load_2d(dst + kBM * kBK, &tmB, kb * kBK, nt * kBN, stg_full(s));
+          issued = it + 1;
         }
-        if (*abort_flag) break;
-        const uint32_t dst = sbase + kSmemStg + s * kStgBytes;
-        tc::mbar_arrive_expect_tx(stg_full(s), kStgBytes);
-        tc::tma_load_2d(dst, &tmA, kb * kBK, m0, stg_full(s));
-        tc::tma_load_2d(dst + kBM * kBK, &tmB, kb * kBK, n0, stg_full(s));
-        issued = kb + 1;
       }
       if (*abort_flag) {
         // Let the copies already issued land before the CTA can exit.
-        for (int kb = (issued > kStg ? issued - kStg : 0); kb < issued; ++kb)
-          tc::mbar_wait(stg_full(kb % kStg), (kb / kStg) & 1, err, kSiteDrain);
+        for (int j = (issued > kStg ? issued - kStg : 0); j < issued; ++j)
+          tc::mbar_wait(stg_full(j % kStg), (j / kStg) & 1, err, kSiteDrain);
       }
     }
   } else if (warp == 1) {
@@ -198,32 +240,38 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_f16(kBM, kBN, 0);  // fp16 x fp16 -> fp32
       bool issued_any = false;
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const int o = kb % kOps;
-        const int chunk = kb / kKbPerChunk, kin = kb % kKbPerChunk;
-        const int buf = chunk & 1;
-        if (kin == 0 && chunk >= 2 &&
-            !tc::mbar_wait(acc_empty(buf), ((chunk / 2) - 1) & 1, err, kSiteAccEmpty)) {
-          *abort_flag = 1;
-          break;
-        }
-        if (!tc::mbar_wait(op_full(o), (kb / kOps) & 1, err, kSiteOpFull)) {
-          *abort_flag = 1;
-          break;
-        }
-        if (*abort_flag) break;
-        tc::tc_fence_after();
-        const uint32_t a_base = sbase + kSmemOps + o * kOpBytes;
-        const uint32_t b_base = a_base + kBM * kBK * 2;
-        const uint32_t d = tmem + buf * kBN;
+      int it = 0, g = 0;  // K stage and chunk counters across tiles
+      for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int kin = kb % kKbPerChunk;
+          const int buf = g & 1;
+          if (kin == 0 && g >= 2 && !tc::mbar_wait(acc_empty(buf), ((g >> 1) - 1) & 1, err, kSiteAccEmpty)) {
+            *abort_flag = 1;
+            break;
+          }
+          const int oa = it % kOpsA, ob = it % kOpsB;
+          if (!tc::mbar_wait(a_full(oa), (it / kOpsA) & 1, err, kSiteAFull) ||
+              !tc::mbar_wait(b_full(ob), (it / kOpsB) & 1, err, kSiteBFull)) {
+            *abort_flag = 1;
+            break;
+          }
+          if (*abort_flag) break;
+          tc::tc_fence_after();
+          const uint32_t b_base = sbase + kSmemOps + ob * kOpBytesB;
+          const uint32_t d = tmem + buf * kBN;
+          const uint32_t a_t = tmem + kTmemA + oa * (kBK / 2);
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k) {
-          tc::mma_f16(d, tc::sw128_kmajor_desc(a_base + 32 * k), tc::sw128_kmajor_desc(b_base + 32 * k), idesc,
-                      (kin > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kBK / 16; ++k) {
+            tc::mma_f16_ta(d, a_t + 8 * k, tc::sw128_kmajor_desc(b_base + 32 * k), idesc, (kin > 0 || k > 0) ? 1u : 0u);
+          }
+          issued_any = true;
+          tc::mma_commit(a_empty(oa));
+          tc::mma_commit(b_empty(ob));
+          if (kin == kKbPerChunk - 1 || kb == num_kb - 1) {
+            tc::mma_commit(acc_full(buf));
+            ++g;
+          }
         }
-        issued_any = true;
-        tc::mma_commit(op_empty(o));
-        if (kin == kKbPerChunk - 1 || kb == num_kb - 1) tc::mma_commit(acc_full(buf));
       }
       if (*abort_flag && issued_any) {
         tc::mma_commit(mma_done);
@@ -231,101 +279,177 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
       }
     }
   } else if (warp < 6) {
-    // ---------------- converters ----------------
-    const int ct = threadIdx.x - 64;  // 0..127
-    for (int kb = 0; kb < num_kb; ++kb) {
-      const int s = kb % kStg, o = kb % kOps;
-      bool ok = tc::mbar_wait(stg_full(s), (kb / kStg) & 1, err, kSiteStgFull);
-      if (ok && kb >= kOps) ok = tc::mbar_wait(op_empty(o), ((kb / kOps) - 1) & 1, err, kSiteOpEmpty);
-      ok = __all_sync(0xffffffffu, ok && !*abort_flag);  // lanes agree and reconverge
-      if (!ok) { *abort_flag = 1; break; }
-      const uint32_t src = sbase + kSmemStg + s * kStgBytes;
-      const uint32_t dst = sbase + kSmemOps + o * kOpBytes;
+    // ---------------- A wideners (int8 staging -> fp16 in TMEM) ----------------
+    const int q = warp & 3;         // TMEM lane quadrant of this warp
+    const int r = q * 32 + lane;    // row of the tile
+    const uint32_t sw = static_cast<uint32_t>((r >> 1) & 3);  // 64-byte swizzle of this row
+    int it = 0;
+    bool ok = true;
+    for (int ti = 0; ti < my_tiles && ok; ++ti) {
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int s = it % kStg, o = it % kOpsA;
+        ok = tc::mbar_wait(stg_full(s), (it / kStg) & 1, err, kSiteStgFull);
+        if (ok && it >= kOpsA) ok = tc::mbar_wait(a_empty(o), ((it / kOpsA) - 1) & 1, err, kSiteAEmpty);
+        ok = __all_sync(0xffffffffu, ok && !*abort_flag);  // lanes agree and reconverge
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t src = sbase + kSmemStg + s * kStgBytes + r * kBK;
+        uint32_t v[32];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int item = ct + 128 * j;          // 1024 16-byte chunks: A rows then B rows
-        const int op = item >> 9;               // 0 = A, 1 = B
-        const int r = (item >> 2) & 127;        // row within the tile
-        const int cc = item & 3;                // 16-byte chunk within the 64-byte row
-        const uint4 v = lds128(src + op * (kBM * kBK) + r * kBK + cc * 16);
-        uint4 h0, h1;
-        int8x16_to_f16(v, h0, h1);
-        const uint32_t rowb = dst + op * (kBM * kBK * 2) + (r >> 3) * 1024 + (r & 7) * 128;
-        sts128(rowb + (((2 * cc) ^ (r & 7)) << 4), h0);
-        sts128(rowb + (((2 * cc + 1) ^ (r & 7)) << 4), h1);
+        for (int c = 0; c < kBK / 16; ++c) int8x16_to_f16(lds128(src + ((c ^ sw) << 4)), v + 8 * c);
+        tc::tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemA + o * (kBK / 2), v);
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(a_full(o));
+          tc::mbar_arrive(stg_empty(s));
+        }
       }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(op_full(o));
-        tc::mbar_arrive(stg_empty(s));
+    }
+  } else if (warp < 10) {
+    // ---------------- B wideners (int8 staging -> fp16 swizzled smem) ----------------
+    const int ct = threadIdx.x - 192;  // 0..127
+    int it = 0;
+    bool ok = true;
+    for (int ti = 0; ti < my_tiles && ok; ++ti) {
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int s = it % kStg, o = it % kOpsB;
+        ok = tc::mbar_wait(stg_full(s), (it / kStg) & 1, err, kSiteStgFull);
+        if (ok && it >= kOpsB) ok = tc::mbar_wait(b_empty(o), ((it / kOpsB) - 1) & 1, err, kSiteBEmpty);
+        ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+        const uint32_t src = sbase + kSmemStg + s * kStgBytes + kBM * kBK;
+        const uint32_t dst = sbase + kSmemOps + o * kOpBytesB;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int item = ct + 128 * j;  // 512 16-byte chunks of the B tile
+          const int rr = item >> 2;       // row within the tile
+          const int cc = item & 3;        // 16-byte chunk within the 64-byte row
+          uint32_t h[8];
+          int8x16_to_f16(lds128(src + rr * kBK + cc * 16), h);
+          const uint32_t rowb = dst + (rr >> 3) * 1024 + (rr & 7) * 128;
+          sts128(rowb + (((2 * cc) ^ (rr & 7)) << 4), make_uint4(h[0], h[1], h[2], h[3]));
+          sts128(rowb + (((2 * cc + 1) ^ (rr & 7)) << 4), make_uint4(h[4], h[5], h[6], h[7]));
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(b_full(o));
+          tc::mbar_arrive(stg_empty(s));
+        }
       }
     }
   } else {
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const int row = m0 + q * 32 + lane;
-    int32_t acc[kBN];
-#pragma unroll
-    for (int i = 0; i < kBN; ++i) acc[i] = 0;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const bool per_tensor_adj = epi.azp == nullptr && epi.azp_adj != nullptr;
+    int g = 0;
     bool ok = true;
-    for (int chunk = 0; chunk < num_chunks; ++chunk) {
-      const int buf = chunk & 1;
-      ok = tc::mbar_wait(acc_full(buf), (chunk / 2) & 1, err, kSiteAccFull);
-      ok = __all_sync(0xffffffffu, ok);  // lanes agree and reconverge before tcgen05.ld
-      if (!ok) { *abort_flag = 1; break; }
-      tc::tc_fence_after();
+    for (int ti = 0; ti < my_tiles && ok; ++ti) {
+      int mt, nt;
+      tile_coords(blockIdx.x + ti * gridDim.x, mt_count, nt_count, mt, nt);
+      const int m0 = mt * kBM, n0 = nt * kBN;
+      const int row = m0 + q * 32 + lane;
+      // Column parameters of this tile, in a copy private to this warp (so no
+      // other warp's progress matters): lane l loads columns l, l+32, l+64, l+96.
+      float* par_sb = reinterpret_cast<float*>(smem + kSmemPar + q * 3 * kBN * 4);
+      int32_t* par_adj = reinterpret_cast<int32_t*>(par_sb + kBN);
+      float* par_bias = par_sb + 2 * kBN;
+      __syncwarp();  // every lane is done with the previous tile's parameters
+      if (epi.out_dtype != QLIN_I32) {
 #pragma unroll
-      for (int cg = 0; cg < kBN / 32; ++cg) {
-        uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + cg * 32, v);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[cg * 32 + i] += __float2int_rn(__uint_as_float(v[i]));
+        for (int j = 0; j < 4; ++j) {
+          const int col = lane + 32 * j, n = n0 + col;
+          const bool inb = n < N;
+          par_sb[col] = inb ? (epi.scale_b_per_col ? epi.scale_b[n] : epi.scale_b[0]) : 0.0f;
+          par_adj[col] = (inb && epi.azp_adj != nullptr) ? epi.azp_adj[n] : 0;
+          par_bias[col] = (inb && epi.bias != nullptr) ? load_as_float(epi.bias, epi.bias_dtype, n) : 0.0f;
+        }
       }
-      tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(acc_empty(buf));
-    }
-    if (ok && row < T) {
-      if (epi.out_dtype == QLIN_I32) {
-        int32_t* o = static_cast<int32_t*>(out) + (int64_t)row * N + n0;
-#pragma unroll
-        for (int c4 = 0; c4 < kBN / 4; ++c4) {
-          if (n0 + c4 * 4 < N)
-            *reinterpret_cast<int4*>(o + c4 * 4) = make_int4(acc[4 * c4], acc[4 * c4 + 1], acc[4 * c4 + 2],
-                                                              acc[4 * c4 + 3]);
+      float sa = 0.0f;
+      int32_t za = 0;
+      if (epi.out_dtype != QLIN_I32 && row < T) {
+        sa = epi.scale_a_per_row ? epi.scale_a[row] : epi.scale_a[0];
+        za = epi.azp != nullptr ? epi.azp[row] : 0;
+      }
+      for (int c = 0; c < num_chunks; ++c, ++g) {
+        const int buf = g & 1;
+        ok = tc::mbar_wait(acc_full(buf), (g >> 1) & 1, err, kSiteAccFull);
+        ok = __all_sync(0xffffffffu, ok);  // lanes agree and reconverge before tcgen05.ld
+        if (!ok) {
+          *abort_flag = 1;
+          break;
         }
-      } else {
-        const float sa = epi.scale_a_per_row ? epi.scale_a[row] : epi.scale_a[0];
-        const int32_t za = epi.azp != nullptr ? epi.azp[row] : 0;
-        const bool per_tensor_adj = epi.azp == nullptr && epi.azp_adj != nullptr;
-        __half* oh = static_cast<__half*>(out) + (int64_t)row * N + n0;
-        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out) + (int64_t)row * N + n0;
+        tc::tc_fence_after();
+        const bool last = c == num_chunks - 1;
+#pragma unroll 1
+        for (int cg = 0; cg < kBN / 32; ++cg) {
+          __syncwarp();  // reconverge after the row-bound branches before the aligned TMEM ops
+          uint32_t va[32], vt[32];
+          tc::tmem_ld_32x32b_x32(lane_base + buf * kBN + cg * 32, va);
+          if (c > 0) tc::tmem_ld_32x32b_x32(lane_base + kTmemTotal + cg * 32, vt);
+          tc::tmem_wait_ld();
+          int32_t acc[32];
 #pragma unroll
-        for (int c8 = 0; c8 < kBN / 8; ++c8) {
-          if (n0 + c8 * 8 >= N) continue;
-          float f[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int col = c8 * 8 + i;
-            // D^ - azp . azp_adj in int32, then one conversion to float
-            const int32_t corr = per_tensor_adj ? par_adj[col] : za * par_adj[col];
-            const float d = __int2float_rn(acc[col] - corr);
-            f[i] = fmaf(sa, d * par_sb[col], par_bias[col]);
+          for (int i = 0; i < 32; ++i)
+            acc[i] = (c > 0 ? static_cast<int32_t>(vt[i]) : 0) + __float2int_rn(__uint_as_float(va[i]));
+          if (!last) {
+            tc::tmem_st_32x32b_x32(lane_base + kTmemTotal + cg * 32, reinterpret_cast<const uint32_t*>(acc));
+            continue;
           }
-          if (epi.out_dtype == QLIN_BF16) {
-            __nv_bfloat162 p[4];
+          if (row >= T) continue;
+          const int nc = n0 + cg * 32;
+          if (epi.out_dtype == QLIN_I32) {
+            int32_t* o = static_cast<int32_t*>(out) + (int64_t)row * N + nc;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) p[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-            *reinterpret_cast<uint4*>(ob + c8 * 8) = *reinterpret_cast<uint4*>(p);
+            for (int c4 = 0; c4 < 8; ++c4)
+              if (nc + c4 * 4 < N)
+                *reinterpret_cast<int4*>(o + c4 * 4) =
+                    make_int4(acc[4 * c4], acc[4 * c4 + 1], acc[4 * c4 + 2], acc[4 * c4 + 3]);
           } else {
-            __half2 p[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) p[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
-            *reinterpret_cast<uint4*>(oh + c8 * 8) = *reinterpret_cast<uint4*>(p);
+            for (int c8 = 0; c8 < 4; ++c8) {
+              if (nc + c8 * 8 >= N) continue;
+              float f[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int col = cg * 32 + c8 * 8 + i;
+                // D^ - azp . azp_adj in int32, then one conversion to float
+                const int32_t corr = per_tensor_adj ? par_adj[col] : za * par_adj[col];
+                const float d = __int2float_rn(acc[c8 * 8 + i] - corr);
+                f[i] = fmaf(sa, d * par_sb[col], par_bias[col]);
+              }
+              uint4 packed;
+              uint32_t* pw = reinterpret_cast<uint32_t*>(&packed);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if (epi.out_dtype == QLIN_BF16) {
+                  __nv_bfloat162 p2 = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+                  pw[i] = *reinterpret_cast<uint32_t*>(&p2);
+                } else {
+                  __half2 p2 = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+                  pw[i] = *reinterpret_cast<uint32_t*>(&p2);
+                }
+              }
+              unsigned char* ob = static_cast<unsigned char*>(out) + ((int64_t)row * N + nc + c8 * 8) * 2;
+              *reinterpret_cast<uint4*>(ob) = packed;
+            }
           }
         }
+        __syncwarp();
+        if (!last) tc::tmem_wait_st();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(acc_empty(buf));
       }
     }
   }
@@ -345,7 +469,8 @@ cudaError_t launch_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_
                              const W8A8Epilogue& e, void* out, cudaStream_t stream) {
   if (T == 0 || N == 0) return cudaSuccess;
   CUtensorMap tmA, tmB;
-  cudaError_t st = make_tmap_2d_u8(&tmA, a, static_cast<uint64_t>(K), static_cast<uint64_t>(T), kBK, kBM);
+  cudaError_t st = make_tmap_2d_u8(&tmA, a, static_cast<uint64_t>(K), static_cast<uint64_t>(T), kBK, kBM,
+                                   /*swizzle_bytes=*/64);
   if (st != cudaSuccess) return st;
   st = make_tmap_2d_u8(&tmB, b, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK, kBN);
   if (st != cudaSuccess) return st;
@@ -361,7 +486,8 @@ cudaError_t launch_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_
   epi.scale_b_per_col = e.scale_b_per_col ? 1 : 0;
   epi.bias_dtype = e.bias_dtype;
   epi.out_dtype = e.out_dtype;
-  dim3 grid(static_cast<unsigned>((N + kBN - 1) / kBN), static_cast<unsigned>((T + kBM - 1) / kBM));
+  const int64_t tiles = ((T + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
   w8a8_gemm_kernel<<<grid, kThreads, kSmemTotal, stream>>>(tmA, tmB, static_cast<int>(T), static_cast<int>(N),
                                                            static_cast<int>(K), epi, out, device_error_word());
   return cudaGetLastError();
