@@ -27,23 +27,29 @@
 // tiles for L2 reuse), and the epilogue of a tile overlaps the MMAs of the
 // next through two chunk accumulators.
 //
-//   warp 0       TMA producer: int8 tiles of A (64-byte swizzle) and B
-//                (128 x 64 bytes each) into a 6-stage staging ring.
-//   warp 1       TMEM allocation and the MMA issuer: 4 x tcgen05.mma
+//   warp 0       TMA producer: int8 tiles of A and B (128 x 128 bytes each,
+//                whole 128-byte lines; A in the 128-byte swizzle) into a
+//                4-stage staging ring.
+//   warp 1       TMEM allocation and the MMA issuer: 8 x tcgen05.mma
 //                (M=N=128, K=16, A from TMEM, B from shared memory) per
-//                64-wide K stage into one of two 128-column accumulators.
-//   warps 2-5    A wideners: lane l of the warp with TMEM lane quadrant q owns
-//                row 32q + l, widens its 64 codes and stores them with one
-//                tcgen05.st into a 4-stage A ring in TMEM.
-//   warps 6-9    B wideners: int8 staging -> fp16 operand ring in the
-//                128-byte swizzled K-major layout the MMA descriptors
-//                describe (4 stages).
-//   warps 10-13  epilogue: lane l of quadrant q owns output row 32q + l; each
+//                128-wide K stage into one of two 128-column accumulators.
+//   warps 2-9    A wideners, two sets of four taking alternate stages: lane l
+//                of the warp with TMEM lane quadrant q owns row 32q + l,
+//                widens its 128 codes and stores them with two tcgen05.st
+//                into a 2-stage A ring in TMEM.
+//   warps 10-17  B wideners, two sets of four taking alternate stages: int8
+//                staging -> fp16 operand ring (2 stages) in the 128-byte
+//                swizzled K-major layout the MMA descriptors describe, two
+//                64-element K blocks per stage.
+//   warps 18-21  epilogue: lane l of quadrant q owns output row 32q + l; each
 //                finished chunk is converted to int32 and added to a running
 //                int32 total kept in TMEM; after the last chunk of a tile the
 //                epilogue is applied and the row is stored.
+// One widener warp needs several times the MMA's time per stage (its loads,
+// conversion, store and barrier round trip are a serial chain), hence two
+// sets.
 // TMEM columns: [0,256) two chunk accumulators, [256,384) the int32 total,
-// [384,512) the A ring.
+// [384,512) the A ring (64 columns per stage).
 // Every barrier wait is bounded; on expiry the kernel records the site in the
 // device error word, stops issuing work, waits (bounded) for copies and MMAs
 // already in flight, frees TMEM and exits.
@@ -57,22 +63,23 @@
 namespace qlin {
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 64;
-constexpr int kStg = 6;             // int8 staging stages (A and B)
-constexpr int kOpsA = 4;            // fp16 A stages in TMEM
-constexpr int kOpsB = 4;            // fp16 B stages in shared memory
+constexpr int kBM = 128, kBN = 128, kBK = 128;
+constexpr int kStg = 4;             // int8 staging stages (A and B)
+constexpr int kOpsA = 2;            // fp16 A stages in TMEM
+constexpr int kOpsB = 2;            // fp16 B stages in shared memory
 constexpr int kChunkK = 1024;       // exact fp32 accumulation span
 constexpr int kKbPerChunk = kChunkK / kBK;
 constexpr int kTmemCols = 512;
 constexpr int kTmemTotal = 2 * kBN;         // int32 running total
-constexpr int kTmemA = kTmemTotal + kBN;    // A ring, 32 columns per stage
-constexpr int kThreads = 14 * 32;
+constexpr int kTmemA = kTmemTotal + kBN;    // A ring, 64 columns per stage
+constexpr int kThreads = 22 * 32;
+constexpr int kWarpA0 = 2, kWarpB0 = 10, kWarpE0 = 18;
 
-constexpr int kStgBytes = (kBM + kBN) * kBK;            // 16 KB (A then B)
-constexpr int kOpBytesB = kBN * kBK * 2;                // 16 KB fp16
+constexpr int kStgBytes = (kBM + kBN) * kBK;            // 32 KB (A then B)
+constexpr int kOpBytesB = kBN * kBK * 2;                // 32 KB fp16 (two 64-element K blocks)
 constexpr int kSmemStg = 0;
-constexpr int kSmemOps = kSmemStg + kStg * kStgBytes;   // 96 KB
-constexpr int kSmemPar = kSmemOps + kOpsB * kOpBytesB;  // 160 KB
+constexpr int kSmemOps = kSmemStg + kStg * kStgBytes;   // 128 KB
+constexpr int kSmemPar = kSmemOps + kOpsB * kOpBytesB;  // 192 KB
 constexpr int kSmemBar = kSmemPar + 4 * 3 * kBN * 4;    // + 6 KB (column parameters, one copy per epilogue warp)
 constexpr int kNumBars = 2 * kStg + 2 * kOpsA + 2 * kOpsB + 2 + 2 + 1;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
@@ -262,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
           const uint32_t a_t = tmem + kTmemA + oa * (kBK / 2);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            tc::mma_f16_ta(d, a_t + 8 * k, tc::sw128_kmajor_desc(b_base + 32 * k), idesc, (kin > 0 || k > 0) ? 1u : 0u);
+            const uint32_t b_k = b_base + (k >> 2) * (kBN * 128) + 32 * (k & 3);  // K block, then 32 B in the atom
+            tc::mma_f16_ta(d, a_t + 8 * k, tc::sw128_kmajor_desc(b_k), idesc, (kin > 0 || k > 0) ? 1u : 0u);
           }
           issued_any = true;
           tc::mma_commit(a_empty(oa));
@@ -278,15 +286,17 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
         tc::mbar_wait(mma_done, 0, err, kSiteDrain);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < kWarpB0) {
     // ---------------- A wideners (int8 staging -> fp16 in TMEM) ----------------
+    const int set = (warp - kWarpA0) >> 2;  // takes the stages with it % 2 == set
     const int q = warp & 3;         // TMEM lane quadrant of this warp
     const int r = q * 32 + lane;    // row of the tile
-    const uint32_t sw = static_cast<uint32_t>((r >> 1) & 3);  // 64-byte swizzle of this row
+    const uint32_t sw = static_cast<uint32_t>(r & 7);  // 128-byte swizzle of this row
     int it = 0;
     bool ok = true;
     for (int ti = 0; ti < my_tiles && ok; ++ti) {
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        if ((it & 1) != set) continue;
         const int s = it % kStg, o = it % kOpsA;
         ok = tc::mbar_wait(stg_full(s), (it / kStg) & 1, err, kSiteStgFull);
         if (ok && it >= kOpsA) ok = tc::mbar_wait(a_empty(o), ((it / kOpsA) - 1) & 1, err, kSiteAEmpty);
@@ -297,10 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
         }
         tc::tc_fence_after();
         const uint32_t src = sbase + kSmemStg + s * kStgBytes + r * kBK;
-        uint32_t v[32];
 #pragma unroll
-        for (int c = 0; c < kBK / 16; ++c) int8x16_to_f16(lds128(src + ((c ^ sw) << 4)), v + 8 * c);
-        tc::tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemA + o * (kBK / 2), v);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) int8x16_to_f16(lds128(src + (((4 * h + c) ^ sw) << 4)), v + 8 * c);
+          tc::tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemA + o * (kBK / 2) + 32 * h, v);
+        }
         tc::tmem_wait_st();
         tc::tc_fence_before();
         __syncwarp();
@@ -310,13 +323,15 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
         }
       }
     }
-  } else if (warp < 10) {
+  } else if (warp < kWarpE0) {
     // ---------------- B wideners (int8 staging -> fp16 swizzled smem) ----------------
-    const int ct = threadIdx.x - 192;  // 0..127
+    const int set = (warp - kWarpB0) >> 2;              // takes the stages with it % 2 == set
+    const int ct = threadIdx.x - (kWarpB0 + 4 * set) * 32;  // 0..127
     int it = 0;
     bool ok = true;
     for (int ti = 0; ti < my_tiles && ok; ++ti) {
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        if ((it & 1) != set) continue;
         const int s = it % kStg, o = it % kOpsB;
         ok = tc::mbar_wait(stg_full(s), (it / kStg) & 1, err, kSiteStgFull);
         if (ok && it >= kOpsB) ok = tc::mbar_wait(b_empty(o), ((it / kOpsB) - 1) & 1, err, kSiteBEmpty);
@@ -328,15 +343,17 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
         const uint32_t src = sbase + kSmemStg + s * kStgBytes + kBM * kBK;
         const uint32_t dst = sbase + kSmemOps + o * kOpBytesB;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int item = ct + 128 * j;  // 512 16-byte chunks of the B tile
-          const int rr = item >> 2;       // row within the tile
-          const int cc = item & 3;        // 16-byte chunk within the 64-byte row
+        for (int j = 0; j < 8; ++j) {
+          const int item = ct + 128 * j;  // 1024 16-byte chunks of the B tile
+          const int rr = item >> 3;       // row within the tile
+          const int cc = item & 7;        // 16-byte chunk within the 128-byte row
           uint32_t h[8];
           int8x16_to_f16(lds128(src + rr * kBK + cc * 16), h);
-          const uint32_t rowb = dst + (rr >> 3) * 1024 + (rr & 7) * 128;
-          sts128(rowb + (((2 * cc) ^ (rr & 7)) << 4), make_uint4(h[0], h[1], h[2], h[3]));
-          sts128(rowb + (((2 * cc + 1) ^ (rr & 7)) << 4), make_uint4(h[4], h[5], h[6], h[7]));
+          // fp16 chunks 2cc, 2cc+1 of the 256-byte row: K block cc / 4, chunk (2cc) % 8 in it
+          const uint32_t rowb = dst + (cc >> 2) * (kBN * 128) + (rr >> 3) * 1024 + (rr & 7) * 128;
+          const int c0 = (2 * cc) & 7;
+          sts128(rowb + ((c0 ^ (rr & 7)) << 4), make_uint4(h[0], h[1], h[2], h[3]));
+          sts128(rowb + (((c0 + 1) ^ (rr & 7)) << 4), make_uint4(h[4], h[5], h[6], h[7]));
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
@@ -392,37 +409,37 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
         tc::tc_fence_after();
         const bool last = c == num_chunks - 1;
 #pragma unroll 1
-        for (int cg = 0; cg < kBN / 32; ++cg) {
+        for (int cg = 0; cg < kBN / 16; ++cg) {
           __syncwarp();  // reconverge after the row-bound branches before the aligned TMEM ops
-          uint32_t va[32], vt[32];
-          tc::tmem_ld_32x32b_x32(lane_base + buf * kBN + cg * 32, va);
-          if (c > 0) tc::tmem_ld_32x32b_x32(lane_base + kTmemTotal + cg * 32, vt);
+          uint32_t va[16], vt[16];
+          tc::tmem_ld_32x32b_x16(lane_base + buf * kBN + cg * 16, va);
+          if (c > 0) tc::tmem_ld_32x32b_x16(lane_base + kTmemTotal + cg * 16, vt);
           tc::tmem_wait_ld();
-          int32_t acc[32];
+          int32_t acc[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < 16; ++i)
             acc[i] = (c > 0 ? static_cast<int32_t>(vt[i]) : 0) + __float2int_rn(__uint_as_float(va[i]));
           if (!last) {
-            tc::tmem_st_32x32b_x32(lane_base + kTmemTotal + cg * 32, reinterpret_cast<const uint32_t*>(acc));
+            tc::tmem_st_32x32b_x16(lane_base + kTmemTotal + cg * 16, reinterpret_cast<const uint32_t*>(acc));
             continue;
           }
           if (row >= T) continue;
-          const int nc = n0 + cg * 32;
+          const int nc = n0 + cg * 16;
           if (epi.out_dtype == QLIN_I32) {
             int32_t* o = static_cast<int32_t*>(out) + (int64_t)row * N + nc;
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
+            for (int c4 = 0; c4 < 4; ++c4)
               if (nc + c4 * 4 < N)
                 *reinterpret_cast<int4*>(o + c4 * 4) =
                     make_int4(acc[4 * c4], acc[4 * c4 + 1], acc[4 * c4 + 2], acc[4 * c4 + 3]);
           } else {
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
+            for (int c8 = 0; c8 < 2; ++c8) {
               if (nc + c8 * 8 >= N) continue;
               float f[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                const int col = cg * 32 + c8 * 8 + i;
+                const int col = cg * 16 + c8 * 8 + i;
                 // D^ - azp . azp_adj in int32, then one conversion to float
                 const int32_t corr = per_tensor_adj ? par_adj[col] : za * par_adj[col];
                 const float d = __int2float_rn(acc[c8 * 8 + i] - corr);
@@ -470,7 +487,7 @@ cudaError_t launch_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_
   if (T == 0 || N == 0) return cudaSuccess;
   CUtensorMap tmA, tmB;
   cudaError_t st = make_tmap_2d_u8(&tmA, a, static_cast<uint64_t>(K), static_cast<uint64_t>(T), kBK, kBM,
-                                   /*swizzle_bytes=*/64);
+                                   /*swizzle_bytes=*/128);
   if (st != cudaSuccess) return st;
   st = make_tmap_2d_u8(&tmB, b, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK, kBN);
   if (st != cudaSuccess) return st;
