@@ -349,11 +349,15 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
           const int cc = item & 7;        // 16-byte chunk within the 128-byte row
           uint32_t h[8];
           int8x16_to_f16(lds128(src + rr * kBK + cc * 16), h);
-          // fp16 chunks 2cc, 2cc+1 of the 256-byte row: K block cc / 4, chunk (2cc) % 8 in it
+          // fp16 chunks 2cc, 2cc+1 of the 256-byte row: K block cc / 4, chunk (2cc) % 8 in it.
+          // Threads cc and cc + 4 hit the same chunk of the two K blocks (same
+          // banks), so the upper half stores its two chunks in the other order.
           const uint32_t rowb = dst + (cc >> 2) * (kBN * 128) + (rr >> 3) * 1024 + (rr & 7) * 128;
           const int c0 = (2 * cc) & 7;
-          sts128(rowb + ((c0 ^ (rr & 7)) << 4), make_uint4(h[0], h[1], h[2], h[3]));
-          sts128(rowb + (((c0 + 1) ^ (rr & 7)) << 4), make_uint4(h[4], h[5], h[6], h[7]));
+          const bool flip = (cc & 4) != 0;
+          const uint4 lo = make_uint4(h[0], h[1], h[2], h[3]), hi = make_uint4(h[4], h[5], h[6], h[7]);
+          sts128(rowb + (((c0 + (flip ? 1 : 0)) ^ (rr & 7)) << 4), flip ? hi : lo);
+          sts128(rowb + (((c0 + (flip ? 0 : 1)) ^ (rr & 7)) << 4), flip ? lo : hi);
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
