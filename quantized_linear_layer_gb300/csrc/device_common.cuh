@@ -20,6 +20,28 @@ __device__ __forceinline__ void record_device_error(int32_t* err, int32_t code) 
   if (err != nullptr) atomicCAS(err, 0, code);
 }
 
+// x / d rounded to nearest even from r = __frcp_rn(d), by one FMA correction
+// step (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", 1990): q0 = x r, e = x - q0 d, q = q0 + e r.  With r
+// the correctly rounded reciprocal this equals __fdiv_rn(x, d) whenever d,
+// r and the quotient are normal numbers; a quotient below the normal range
+// comes out as a tiny number (or zero) with the sign of x.  A zero dividend
+// returns q0 = x r, the correctly signed zero (the correction would add
+// +0 and -0 and lose the sign).  Four operations per element instead of a
+// full division when many elements share d.
+__device__ __forceinline__ float div_by_rcp(float x, float d, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float e = __fmaf_rn(-q0, d, x);
+  const float q = __fmaf_rn(e, r, q0);
+  return x == 0.0f ? q0 : q;
+}
+
+// True when div_by_rcp may replace the division by d (d and 1/d normal).
+__device__ __forceinline__ bool rcp_division_ok(float d, float r) {
+  const float kMinNormal = 1.17549435e-38f, kMaxFinite = 3.40282347e38f;
+  return fabsf(d) >= kMinNormal && fabsf(d) <= kMaxFinite && fabsf(r) >= kMinNormal && fabsf(r) <= kMaxFinite;
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start
 // launching, and wait for the previous one before touching data it writes.
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -13,8 +13,10 @@
 // or a copy of their codes and scales (weights: "copy rather than compute").
 //
 // Every rounding decision is taken in IEEE float32 as written (true division,
-// separate multiply and subtract); the E4M3 and E2M1 encodes use the
-// hardware's round-to-nearest-even saturating conversions.
+// separate multiply and subtract; the 16 divisions of a block by its d go
+// through the correctly rounded reciprocal plus one FMA correction, which
+// gives the same quotients); the E4M3 and E2M1 encodes use the hardware's
+// round-to-nearest-even saturating conversions.
 #include <type_traits>
 
 #include "device_common.cuh"
@@ -63,10 +65,22 @@ __device__ __forceinline__ uint32_t quant_block16(const float* v, float g, uint3
   packed[0] = 0u;
   packed[1] = 0u;
   if (d != 0.0f) {
+    // The 16 quotients share d: x / d through the correctly rounded
+    // reciprocal and one FMA correction (equal to the IEEE quotient wherever
+    // it can change a code: every E2M1 decision lies in the normal range).
+    const float rd = __frcp_rn(d);
+    if (rcp_division_ok(d, rd)) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t byte = f32x2_to_e2m1x2(__fdiv_rn(v[2 * i], d), __fdiv_rn(v[2 * i + 1], d));
-      packed[i >> 2] |= byte << (8 * (i & 3));
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t byte = f32x2_to_e2m1x2(div_by_rcp(v[2 * i], d, rd), div_by_rcp(v[2 * i + 1], d, rd));
+        packed[i >> 2] |= byte << (8 * (i & 3));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t byte = f32x2_to_e2m1x2(__fdiv_rn(v[2 * i], d), __fdiv_rn(v[2 * i + 1], d));
+        packed[i >> 2] |= byte << (8 * (i & 3));
+      }
     }
   }
   *d_out = d;

@@ -93,12 +93,17 @@ __global__ void __launch_bounds__(kQuantThreads) quant_int8_rows_kernel(const vo
   __syncthreads();
   const float s = s_scale;
   const int z = s_zero;
+  // Every element of the row is divided by s: through the correctly rounded
+  // reciprocal and one FMA correction, which gives the IEEE quotient wherever
+  // it can change the rounded code (tiny quotients round to 0 either way).
+  const float rs = __frcp_rn(s);
+  const bool rcp_ok = rcp_division_ok(s, rs);
 
   auto quant8 = [&](const float* t, int64_t idx) {
     uint32_t w0 = 0, w1 = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      int r = __float2int_rn(__fdiv_rn(t[j], s));
+      int r = __float2int_rn(rcp_ok ? div_by_rcp(t[j], s, rs) : __fdiv_rn(t[j], s));
       if (ASYM) r = min(max(r + z, -128), 127);
       else r = min(max(r, -127), 127);
       const uint32_t byte = static_cast<uint32_t>(r) & 0xffu;
