@@ -56,7 +56,6 @@ constexpr int kGvCtaBytes = 112 * 1024;     // two CTAs (this layer, the next) f
 constexpr int kGvMinStages = 2;
 constexpr int kGvMaxStages = 8;
 constexpr int kGvSiteFull = 1, kGvSiteEmpty = 2, kGvSiteDrain = 3;
-constexpr int kGvRowsPerBatch = 4;          // rows a warp reduces together
 
 struct GvArgs {
   const __half* x;
@@ -136,20 +135,20 @@ __device__ __forceinline__ float2 lds64f(uint32_t addr) {
 // idle lanes have zero activations and contribute 0.  Addresses are 32-bit
 // shared-window offsets: cbase = the thread's chunk in the stage, sbase = its
 // group's {scale, zero} of the stage's first row.
-template <int NP>
+template <int NP, int B>
 __device__ __forceinline__ void gv_batch(uint32_t cbase, uint32_t sbase, int rows_i, int RG, int rg, int row_bytes,
                                          int G, const uint32_t (*xp)[8], const int* xsum, float xzf, float sx,
                                          float* p) {
-  uint4 q[kGvRowsPerBatch];
-  float2 m[kGvRowsPerBatch];
+  uint4 q[B];
+  float2 m[B];
 #pragma unroll
-  for (int b = 0; b < kGvRowsPerBatch; ++b) {
+  for (int b = 0; b < B; ++b) {
     const int rrc = min(rg + RG * b, rows_i - 1);
     q[b] = lds128(cbase + rrc * row_bytes);
     m[b] = lds64f(sbase + rrc * G * 8);
   }
 #pragma unroll
-  for (int b = 0; b < kGvRowsPerBatch; ++b)
+  for (int b = 0; b < B; ++b)
     p[b] = (m[b].x * sx) * gv_chunk<NP>(q[b], xp, xsum, xzf, __float_as_int(m[b].y));
 }
 
@@ -157,7 +156,10 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// B rows of each stage per warp and row group (a power of two).
+template <int B>
 __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvArgs a) {
+  constexpr int kGvRowsPerBatch = B;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ncw = a.RG * a.WPR;  // compute warps; warp ncw is the producer
@@ -307,7 +309,6 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
   // sum(x_fix) of the two high planes (what the two-plane dot products see)
   const float xzf = fmaf(static_cast<float>(xsum[0]), 65536.0f, static_cast<float>(xsum[1]) * 256.0f);
 
-  const bool b0 = (lane & 1) != 0, b1 = (lane & 2) != 0;
   const uint32_t sz_base = tc::smem_u32(sz + (jc >> 2));  // this thread's group column
   // The consume loop, instantiated once per plane count so that the common
   // two-plane loop does not keep the low plane live.
@@ -315,23 +316,36 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
     constexpr int NP = decltype(np)::value;
     // The reduction of one batch runs in the same block as the dot products
     // of the next, so that the shuffles' latency overlaps the dp4a work.
-    float prev[kGvRowsPerBatch] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float prev[kGvRowsPerBatch];
+#pragma unroll
+    for (int b = 0; b < kGvRowsPerBatch; ++b) prev[b] = 0.0f;
     int prev_row0 = -1, prev_rows = 0;
     auto reduce_store = [&](const float* v, int row0, int rows) {
-      // Butterfly: after the xor-1 and xor-2 steps lane l holds row
-      // 2 (l & 1) + ((l >> 1) & 1) summed over its 4-lane group, then over
-      // all 32 lanes.
-      float k0 = b0 ? v[2] : v[0], k1 = b0 ? v[3] : v[1];
-      const float s0 = b0 ? v[0] : v[2], s1 = b0 ? v[1] : v[3];
-      k0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-      k1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-      float k = b1 ? k1 : k0;
-      k += __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
-      k += __shfl_xor_sync(0xffffffffu, k, 4);
-      k += __shfl_xor_sync(0xffffffffu, k, 8);
-      k += __shfl_xor_sync(0xffffffffu, k, 16);
+      // Butterfly over the batch: at the step with lane mask m = 1, 2, 4, ...
+      // a lane keeps the half of its values selected by its bit and adds the
+      // partner's copy of that half; after log2(batch) steps lane l holds
+      // row bitrev(l mod batch) summed over its lane group, and the remaining
+      // xor steps sum over all 32 lanes.
+      float w[kGvRowsPerBatch];
+#pragma unroll
+      for (int b = 0; b < kGvRowsPerBatch; ++b) w[b] = v[b];
+      int row_sel = 0;
+#pragma unroll
+      for (int half = kGvRowsPerBatch / 2, m = 1; half >= 1; half >>= 1, m <<= 1) {
+        const bool hi = (lane & m) != 0;
+        row_sel = (row_sel << 1) | (hi ? 1 : 0);
+#pragma unroll
+        for (int j = 0; j < half; ++j) {
+          const float keep = hi ? w[j + half] : w[j];
+          const float send = hi ? w[j] : w[j + half];
+          w[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+      float k = w[0];
+#pragma unroll
+      for (int m = kGvRowsPerBatch; m < 32; m <<= 1) k += __shfl_xor_sync(0xffffffffu, k, m);
       if (lane < kGvRowsPerBatch) {
-        const int rr = rg + a.RG * (2 * (lane & 1) + (lane >> 1));
+        const int rr = rg + a.RG * row_sel;
         if (rr < rows) red[(row0 + rr) * a.WPR + wr] = k;
       }
     };
@@ -345,7 +359,7 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
       }
       const int rows_i = min(a.R, nrows - i * a.R);
       float p[kGvRowsPerBatch];
-      gv_batch<NP>(ring + s * a.stage_bytes + jc * 16, sz_base + (i * a.R * G) * 8, rows_i, a.RG, rg, row_bytes, G, xp,
+      gv_batch<NP, B>(ring + s * a.stage_bytes + jc * 16, sz_base + (i * a.R * G) * 8, rows_i, a.RG, rg, row_bytes, G, xp,
                    xsum, xzf, sx, p);
       // The stage's codes are in registers: hand it back to the producer.
       __syncwarp();
@@ -371,6 +385,8 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
   }
 }
 
+__host__ __device__ constexpr int gv_rows_per_batch(int RG) { return RG >= 2 ? 8 : 4; }
+
 // Shared-memory plan of one launch; false when the band's scales do not
 // leave room for a double-buffered ring within the per-CTA budget.
 bool gv_plan(int64_t N, int64_t K, GvArgs& a, int& grid, int& smem) {
@@ -380,8 +396,9 @@ bool gv_plan(int64_t N, int64_t K, GvArgs& a, int& grid, int& smem) {
   a.RG = a.WPR >= 8 ? 1 : 8 / a.WPR;
   grid = static_cast<int>(std::min<int64_t>(sm_count(), (N + a.RG - 1) / a.RG));
   const int rows_max = static_cast<int>((N + grid - 1) / grid);
-  // A stage holds one batch of rows for every row group.
-  a.R = std::min(kGvRowsPerBatch * a.RG, rows_max);
+  // A stage holds one batch of rows for every row group: 8 rows per warp
+  // when there are several row groups, 4 when one (long rows, large stages).
+  a.R = std::min(gv_rows_per_batch(a.RG) * a.RG, rows_max);
   a.stage_bytes = a.R * row_bytes;
   auto up = [](int v, int m) { return (v + m - 1) / m * m; };
   const int extras = up(rows_max * G * 8, 16) + up(rows_max * a.WPR * 4, 16) + 16 * kGvMaxStages + 16 + 128;
@@ -418,7 +435,9 @@ cudaError_t launch_w4a16_gemv(const void* x, int64_t N, int64_t K, const uint8_t
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
   a.zpitch = static_cast<int>((K / 128 + 1) / 2);
-  cudaError_t e = cudaFuncSetAttribute(w4a16_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const bool b8 = gv_rows_per_batch(a.RG) == 8;
+  cudaError_t e = cudaFuncSetAttribute(b8 ? w4a16_gemv_kernel<8> : w4a16_gemv_kernel<4>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -430,7 +449,7 @@ cudaError_t launch_w4a16_gemv(const void* x, int64_t N, int64_t K, const uint8_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, w4a16_gemv_kernel, a);
+  return b8 ? cudaLaunchKernelEx(&cfg, w4a16_gemv_kernel<8>, a) : cudaLaunchKernelEx(&cfg, w4a16_gemv_kernel<4>, a);
 }
 
 }  // namespace qlin
