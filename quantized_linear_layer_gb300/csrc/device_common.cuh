@@ -65,6 +65,15 @@ __device__ __forceinline__ uint4 ldg_v4(const void* p) {
   return r;
 }
 
+// 16-byte load cached in L2 only.  For data the previous kernel in the stream
+// writes while this one is already resident (programmatic dependent launch):
+// an L1 line filled before that kernel finished could be stale.
+__device__ __forceinline__ uint4 ldg_cg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

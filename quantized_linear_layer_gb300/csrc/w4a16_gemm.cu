@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(256) w4a16_mma_kernel(const __half* __restrict
 #pragma unroll
       for (int j = 0; j < kXU; ++j) {
         const int m = m0 + j * blockDim.x;
-        if (m < XC) u[j] = ldg_v4(xr + m * 8);
+        if (m < XC) u[j] = ldg_cg_v4(xr + m * 8);
       }
 #pragma unroll
       for (int j = 0; j < kXU; ++j) {

@@ -248,19 +248,20 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
 
   // The activations may come from the previous kernel: one warp waits for it,
   // the others block on the named barrier (which also publishes the scales
-  // and zero-points) instead of polling.
+  // and zero-points) instead of polling.  They are read through L2 only: an
+  // L1 line filled while the previous kernel was still running could be stale.
   if (warp == 0) pdl_wait();
   named_sync(1, nct);
   uint32_t xp[3][8];         // byte planes hi, mid, lo
   int xsum[3] = {0, 0, 0};   // plane sums over the chunk
-  float sx = 0.0f;           // x = x_fix . sx
-  bool wide = false;         // chunk needs the low plane
+  float sx = 1.0f;           // x = x_fix . sx
+  float xf[32];
+  float amax = 0.0f, asum = 0.0f;
   if (act) {
     const uint4* xg = reinterpret_cast<const uint4*>(a.x + j * 32);
-    float xf[32];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      const uint4 u = ldg_v4(xg + w);
+      const uint4 u = ldg_cg_v4(xg + w);
       const __half2* h = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -269,14 +270,20 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
         xf[8 * w + 2 * t + 1] = f.y;
       }
     }
-    float amax = 0.0f, asum = 0.0f;
+    // four partial maxima / sums (short dependency chains)
+    float pm[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int t = 0; t < 32; ++t) {
       const float ax = fabsf(xf[t]);
-      amax = fmaxf(amax, ax);
-      asum += ax;
+      pm[t & 3] = fmaxf(pm[t & 3], ax);
+      ps[t & 3] += ax;
     }
-    wide = amax > (64.0f / 31.0f) * (asum - amax);
+    amax = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+    asum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+  }
+  // The low plane is built only in warps holding a chunk with an outlier.
+  const bool wide_warp = __any_sync(0xffffffffu, act && amax > (64.0f / 31.0f) * (asum - amax));
+  if (act) {
     sx = amax > 0.0f ? amax * (1.0f / 4161536.0f) : 1.0f;   // 4161536 = 127 . 2^15
     const float inv = 1.0f / sx;
     // x_fix + 0x8080: byte 0 ^ 0x80 = lo, byte 1 ^ 0x80 = mid, byte 2 = hi.
@@ -291,21 +298,28 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
         const int e = 8 * w + par;  // elements e, e + 2, e + 4, e + 6
         const uint32_t hi01 = __byte_perm(vb[e], vb[e + 2], 0x0062), hi23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0062);
         const uint32_t md01 = __byte_perm(vb[e], vb[e + 2], 0x0051), md23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0051);
-        const uint32_t lo01 = __byte_perm(vb[e], vb[e + 2], 0x0040), lo23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0040);
         xp[0][2 * w + par] = __byte_perm(hi01, hi23, 0x5410);
         xp[1][2 * w + par] = __byte_perm(md01, md23, 0x5410) ^ 0x80808080u;
-        xp[2][2 * w + par] = __byte_perm(lo01, lo23, 0x5410) ^ 0x80808080u;
+        xp[2][2 * w + par] = 0u;
+        if (wide_warp) {
+          const uint32_t lo01 = __byte_perm(vb[e], vb[e + 2], 0x0040), lo23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0040);
+          xp[2][2 * w + par] = __byte_perm(lo01, lo23, 0x5410) ^ 0x80808080u;
+        }
       }
     }
 #pragma unroll
-    for (int pl = 0; pl < 3; ++pl)
+    for (int w = 0; w < 8; ++w) {
+      xsum[0] = dp4a_us(0x01010101u, xp[0][w], xsum[0]);
+      xsum[1] = dp4a_us(0x01010101u, xp[1][w], xsum[1]);
+    }
+    if (wide_warp) {
 #pragma unroll
-      for (int w = 0; w < 8; ++w) xsum[pl] = dp4a_us(0x01010101u, xp[pl][w], xsum[pl]);
+      for (int w = 0; w < 8; ++w) xsum[2] = dp4a_us(0x01010101u, xp[2][w], xsum[2]);
+    }
   } else {
 #pragma unroll
     for (int w = 0; w < 8; ++w) xp[0][w] = xp[1][w] = xp[2][w] = 0u;
   }
-  const bool wide_warp = __any_sync(0xffffffffu, wide);
   // sum(x_fix) of the two high planes (what the two-plane dot products see)
   const float xzf = fmaf(static_cast<float>(xsum[0]), 65536.0f, static_cast<float>(xsum[1]) * 256.0f);
 

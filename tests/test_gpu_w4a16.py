@@ -120,3 +120,29 @@ def test_decode_band_split_shapes(qlin_gpu):
         ref = oracle.w4a16_reference(d["x"], codes, s16, z)
         y = _gemm(qlin_gpu, _dev(d["x"]), _dev(oracle.pack_u4(codes)), _dev(s16), _dev(oracle.pack_u4(z)))
         assert_within_tolerance(y, ref, "W4A16 N=%d K=%d" % (n, k))
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_decode_chain_ping_pong(qlin_gpu, T):
+    """Six layers launched back to back on one stream, each reading the
+    previous layer's output from a ping-pong buffer pair (the kernels overlap
+    through programmatic dependent launch); the oracle runs the same chain,
+    rounding each layer's output to fp16 as the kernels do."""
+    n = 2048
+    layers = []
+    for i in range(6):
+        d = inputs.w4a16_decode(seed=40 + i, T=T, N=n, K=n)
+        codes, s16, z = oracle.quant_w4_g128(d["w"])  # gain about 1 per layer: magnitudes stay O(1)
+        layers.append((codes, s16, z))
+    x0 = inputs.w4a16_decode(seed=39, T=T, N=n, K=n)["x"]
+    bufs = [_dev(x0), torch.empty((T, n), dtype=torch.float16, device="cuda")]
+    dev_w = [(_dev(oracle.pack_u4(c)), _dev(s), _dev(oracle.pack_u4(z))) for (c, s, z) in layers]
+    for i, (wq, sc, zp) in enumerate(dev_w):
+        qlin_gpu.qlin_w4a16_gemm(bufs[i % 2], wq, sc, zp, bufs[(i + 1) % 2])
+    torch.cuda.synchronize()
+    assert qlin_gpu.qlin_get_device_error() == 0
+    y = bufs[len(dev_w) % 2].cpu().numpy()
+    ref = x0
+    for (c, s, z) in layers:
+        ref = oracle.w4a16_reference(ref, c, s, z).astype(np.float16)
+    assert_within_tolerance(y, ref.astype(np.float64), "W4A16 chain T=%d" % T)
