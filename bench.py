@@ -227,6 +227,22 @@ class Workload:
         torch.cuda.synchronize()
 
 
+def max_over_ranks(dist, values, device=None):
+    """Element-wise maximum of a list of floats over all ranks of the process
+    group (the values themselves without one)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_rank, seconds, world):
+    """Weak scaling: every rank processes the same units; the job's rate is
+    all ranks' units over the slowest rank's time."""
+    return units_per_rank * world / seconds
+
+
 def kernel_timed_run(wl, torch, steps, warmup, dist):
     """Device-resident timing: per phase, the average over `steps` of the
     event-measured duration on the phase's stream."""
@@ -358,10 +374,8 @@ def run_ours(args):
     clocks = sampler.stop() if sampler else None
     err = q.qlin_get_device_error()
     # max over ranks of the timed region and of each phase
-    vals = torch.tensor([total] + [phase[n] for n in ("w4a16", "w8a8", "nvfp4")], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    total, tw4, tw8, tnv = vals.tolist()
+    total, tw4, tw8, tnv = max_over_ranks(dist, [total] + [phase[n] for n in ("w4a16", "w8a8", "nvfp4")],
+                                          device="cuda")
     e2e_phase, h2d, d2h = e2e_run(wl, torch, max(3, args.steps // 5), 2)
     if rank != 0:
         if dist is not None:
@@ -369,7 +383,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return
     ms_per_step = total / args.steps * 1e3
-    w4_gbs = wl.w4_bytes / tw4 / 1e9 * world
+    w4_gbs = whole_job_rate(wl.w4_bytes, tw4, world) / 1e9
     w8_ops = 2 * W8A8["T"] * W8A8["N"] * W8A8["K"]
     nv_ops = 2 * NVFP4["T"] * NVFP4["N"] * (NVFP4["K"] + NVFP4["S"])
     peak16 = peaks["bf16_tflops_sustained"]
