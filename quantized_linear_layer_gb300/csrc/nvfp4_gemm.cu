@@ -9,24 +9,37 @@
 // during accumulation; "NVFP4 quantization and ARCQuant", section 2.2: the
 // residual channels are extra K columns of the same GEMM).
 //
-// Persistent kernel: one CTA per SM walks the 128 x 128 output tiles
-// (tile = blockIdx.x, + gridDim.x, ...), 7 warps:
-//   warp 0      TMA producer: packed codes of A and B, 128 rows x 128 bytes
-//               (256 elements) per stage, into the 128-byte swizzled K-major
-//               layout the MMA descriptors describe, plus two bulk copies of
-//               the stage's E4M3 scales, which are stored in the MMA layout
-//               (128-row x 4-block blocks of 512 bytes, byte
-//               16*(r%32) + 4*(r/32) + j for row r, K block j) and land exactly
-//               as tcgen05.cp reads them.
-//   warp 1      TMEM allocation and the MMA issuer: per stage,
-//               4 x tcgen05.mma kind::mxf4nvf4.block_scale.scale_vec::4X
-//               (M=128, N=128, K=64) into one of two accumulator buffers.
-//   warp 6      scale-factor copier: tcgen05.cp of each landed stage's scales
-//               into that stage's TMEM slot, handed to the MMA issuer through
-//               an mbarrier so the copies run ahead of the MMAs.
-//   warps 2-5   epilogue: the fp32 accumulator from TMEM, times g_a . g_b,
-//               rounded once to bf16 / fp16; the other accumulator buffer
-//               keeps the MMAs of the next tile going meanwhile.
+// Persistent kernel: one CTA per SM walks the 128 x 256 output tiles
+// (tile = blockIdx.x, + gridDim.x, ...), 14 warps:
+//   warp 0      TMA producer: packed codes of A (128 rows) and B (256 rows),
+//               128 bytes (256 elements) per row per stage, into the 128-byte
+//               swizzled K-major layout the MMA descriptors describe, plus bulk
+//               copies of the stage's E4M3 scales, which are stored in the MMA
+//               layout (128-row x 4-block blocks of 512 bytes, byte
+//               16*(r%32) + 4*(r/32) + j for row r, K block j); B's 256 rows
+//               are two such blocks.
+//   warps 10-13 scale-factor writers, one per TMEM lane quadrant: lane l of
+//               a block holds, in 16 bytes, the scales of rows l, l+32, l+64,
+//               l+96, which is what every quadrant of the scale TMEM slot holds
+//               at lane l (4 columns per 128 rows).  Each warp reads its 16-byte
+//               pieces of the landed stage with ld.shared and writes the
+//               stage's 48 columns (A: 4 per MMA, B: 8 per MMA, rows 128-255
+//               in the upper 4) into its own quadrant with tcgen05.st.  Written
+//               from registers, the scales stay off the tensor pipe, where
+//               tcgen05.cp copies of the same bytes queue behind the MMAs and
+//               take longer than the MMAs themselves.
+//   warp 1      TMEM allocation and the MMA issuer: per stage, once the four
+//               writers have arrived, 4 x tcgen05.mma
+//               kind::mxf4nvf4.block_scale.scale_vec::4X (M=128, N=256, K=64)
+//               into the 256-column accumulator.  The wide N reads each A tile
+//               once for 256 output columns, which keeps the shared-memory
+//               bytes per multiply-add (TMA writes plus MMA reads) a quarter
+//               below those of a 128 x 128 tile.
+//   warps 2-9   epilogue: warp w reads TMEM lane quadrant w%4, columns
+//               128*((w-2)/4) .. +127, of the finished accumulator, packs them
+//               to bf16 / fp16 pairs in registers (times g_a . g_b, one
+//               rounding) and releases the accumulator before it stores, so
+//               the next tile's MMAs start meanwhile.
 // Every barrier wait is bounded; on expiry the kernel records the site in the
 // device error word, stops issuing work, waits (bounded) for copies and MMAs
 // already in flight, frees TMEM and exits.
@@ -40,25 +53,31 @@
 namespace qlin {
 namespace {
 
-constexpr int kBM = 128, kBN = 128;
+constexpr int kBM = 128, kBN = 256;
 constexpr int kBKB = 128;                 // bytes of packed codes per row per stage (256 elements)
 constexpr int kMmaPerStage = 4;           // K = 64 elements each
-constexpr int kStages = 6;
-constexpr int kThreads = 224;
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kSfWarp0 = 2 + kEpiWarps;   // first of the 4 scale-factor writer warps
+constexpr int kThreads = 32 * (kSfWarp0 + 4);
 constexpr int kAccCols = kBN;
-constexpr int kSfColsPerStage = 2 * kMmaPerStage * 4;  // A and B, 4 TMEM columns per MMA
-constexpr int kTmemCols = 512;            // 2 accumulators (256) + scale factors (6 stages x 32)
+constexpr int kSfaCols = 4;               // TMEM columns of one MMA's A scales (128 rows)
+constexpr int kSfbCols = 4 * kBN / 128;   // TMEM columns of one MMA's B scales (256 rows)
+constexpr int kSfColsPerStage = kMmaPerStage * (kSfaCols + kSfbCols);
+constexpr int kTmemCols = 512;            // accumulator (256) + scale factors (4 stages x 48)
 
-constexpr int kCodeBytes = (kBM + kBN) * kBKB;           // 32 KB per stage
-constexpr int kSfBytes = 2 * kMmaPerStage * 512;         // 4 KB per stage
+constexpr int kSfBlock = 512;                               // one 128-row x 4-block scale block
+constexpr int kCodeBytes = (kBM + kBN) * kBKB;              // 48 KB per stage
+constexpr int kSfBytes = kMmaPerStage * (1 + kBN / 128) * kSfBlock;  // 6 KB per stage
 constexpr int kSmemCodes = 0;
 constexpr int kSmemSf = kSmemCodes + kStages * kCodeBytes;          // 192 KB
 constexpr int kSmemBar = kSmemSf + kStages * kSfBytes;              // +24 KB
-constexpr int kNumBars = 3 * kStages + 4 + 2;
+constexpr int kNumBars = 4 * kStages + 3;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
 constexpr int kSmemTotal = kSmemMisc + 16 + 1024;
 static_assert(kSmemTotal <= 227 * 1024, "shared memory budget");
-static_assert(2 * kAccCols + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+static_assert(kBN % 128 == 0 && kBN <= 256, "B tile is whole 128-row scale blocks");
 
 enum { kSiteEmpty = 1, kSiteFull, kSiteAccFull, kSiteAccEmpty, kSiteDrain };
 
@@ -98,26 +117,24 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
   const uint32_t bar0 = sbase + kSmemBar;
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto acc_full = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-  auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-  const uint32_t mma_done = bar0 + 8u * (2 * kStages + 4);
-  auto sf_ready = [&](int s) { return bar0 + 8u * (2 * kStages + 5 + s); };
-  const uint32_t cp_done = bar0 + 8u * (3 * kStages + 5);
+  auto sf_ready = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
+  auto sf_full = [&](int s) { return bar0 + 8u * (3 * kStages + s); };
+  const uint32_t acc_full = bar0 + 8u * (4 * kStages);
+  const uint32_t acc_empty = bar0 + 8u * (4 * kStages + 1);
+  const uint32_t mma_done = bar0 + 8u * (4 * kStages + 2);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(full(s), 1);        // TMA producer (codes + scale factors)
+      tc::mbar_init(full(s), 1);        // TMA producer: codes
+      tc::mbar_init(sf_full(s), 1);     // TMA producer: scale factors
       tc::mbar_init(empty(s), 1);       // MMA commit
+      tc::mbar_init(sf_ready(s), 4);    // the four scale-factor writer warps
     }
-    for (int b = 0; b < 2; ++b) {
-      tc::mbar_init(acc_full(b), 1);
-      tc::mbar_init(acc_empty(b), 4);
-    }
+    tc::mbar_init(acc_full, 1);
+    tc::mbar_init(acc_empty, kEpiWarps);
     tc::mbar_init(mma_done, 1);
-    for (int s = 0; s < kStages; ++s) tc::mbar_init(sf_ready(s), 1);  // scale-factor copier commit
-    tc::mbar_init(cp_done, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -129,7 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_sf = tmem + 2 * kAccCols;
+  const uint32_t tmem_sf = tmem + kAccCols;
+  const int n128_count = (N + 127) / 128;  // 128-row scale blocks of B
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -140,6 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
       for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
         int mt, nt;
         tile_coords(blockIdx.x + ti * gridDim.x, mt_count, nt_count, mt, nt);
+        const int nb0 = nt * (kBN / 128);                     // first 128-row scale block of the B tile
+        const int nbs = min(kBN / 128, n128_count - nb0);     // scale blocks of the B tile that exist
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % kStages;
           if (it >= kStages && !tc::mbar_wait(empty(s), ((it / kStages) - 1) & 1, err, kSiteEmpty)) {
@@ -150,17 +170,24 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
           const uint32_t sf_dst = sbase + kSmemSf + s * kSfBytes;
           const int kg0 = kb * kMmaPerStage;                  // first 64-element K block of the stage
           const int nkg = min(kMmaPerStage, KG - kg0);        // blocks of this stage that exist
-          tc::mbar_arrive_expect_tx(full(s), kCodeBytes + 2 * nkg * 512);
+          // scales first, on their own barrier: the writer warps put them into
+          // TMEM while the codes are still in flight
+          tc::mbar_arrive_expect_tx(sf_full(s), (1 + nbs) * nkg * kSfBlock);
+          tc::bulk_load(sf_dst, sfa + ((int64_t)mt * KG + kg0) * kSfBlock, nkg * kSfBlock, sf_full(s));
+          for (int h = 0; h < nbs; ++h)
+            tc::bulk_load(sf_dst + (1 + h) * kMmaPerStage * kSfBlock,
+                          sfb + ((int64_t)(nb0 + h) * KG + kg0) * kSfBlock, nkg * kSfBlock, sf_full(s));
+          tc::mbar_arrive_expect_tx(full(s), kCodeBytes);
           tc::tma_load_2d(dst, &tmA, kb * kBKB, mt * kBM, full(s));
           tc::tma_load_2d(dst + kBM * kBKB, &tmB, kb * kBKB, nt * kBN, full(s));
-          tc::bulk_load(sf_dst, sfa + ((int64_t)mt * KG + kg0) * 512, nkg * 512, full(s));
-          tc::bulk_load(sf_dst + kMmaPerStage * 512, sfb + ((int64_t)nt * KG + kg0) * 512, nkg * 512, full(s));
           issued = it + 1;
         }
       }
       if (*abort_flag) {
-        for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+        for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i) {
+          tc::mbar_wait(sf_full(i % kStages), (i / kStages) & 1, err, kSiteDrain);
           tc::mbar_wait(full(i % kStages), (i / kStages) & 1, err, kSiteDrain);
+        }
       }
     }
   } else if (warp == 1) {
@@ -170,17 +197,20 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
       bool issued_any = false;
       int it = 0;
       for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
-        const int buf = ti & 1;
-        if (ti >= 2 && !tc::mbar_wait(acc_empty(buf), ((ti / 2) - 1) & 1, err, kSiteAccEmpty)) {
+        // the epilogue has taken the previous tile's accumulator into registers
+        if (ti >= 1 && !tc::mbar_wait(acc_empty, (ti - 1) & 1, err, kSiteAccEmpty)) {
           *abort_flag = 1;
           break;
         }
         tc::tc_fence_after();
-        const uint32_t d = tmem + buf * kAccCols;
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % kStages;
-          // codes landed and scale factors copied into TMEM slot s by the copier warp
-          if (!tc::mbar_wait(sf_ready(s), (it / kStages) & 1, err, kSiteFull)) { *abort_flag = 1; break; }
+          // scales written into TMEM slot s by the writer warps, codes landed
+          if (!tc::mbar_wait(sf_ready(s), (it / kStages) & 1, err, kSiteFull) ||
+              !tc::mbar_wait(full(s), (it / kStages) & 1, err, kSiteFull)) {
+            *abort_flag = 1;
+            break;
+          }
           tc::tc_fence_after();
           const uint32_t sf_t = tmem_sf + s * kSfColsPerStage;
           const uint32_t a_base = sbase + kSmemCodes + s * kCodeBytes;
@@ -189,91 +219,133 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
 #pragma unroll
           for (int kk = 0; kk < kMmaPerStage; ++kk) {
             if (kk < kk_valid) {
-              tc::mma_nvf4(d, tc::sw128_kmajor_desc(a_base + 32 * kk), tc::sw128_kmajor_desc(b_base + 32 * kk),
-                           idesc, sf_t + 4 * kk, sf_t + 4 * (kMmaPerStage + kk), (kb > 0 || kk > 0) ? 1u : 0u);
+              tc::mma_nvf4(tmem, tc::sw128_kmajor_desc(a_base + 32 * kk), tc::sw128_kmajor_desc(b_base + 32 * kk),
+                           idesc, sf_t + kSfaCols * kk, sf_t + kMmaPerStage * kSfaCols + kSfbCols * kk,
+                           (kb > 0 || kk > 0) ? 1u : 0u);
             }
           }
           issued_any = true;
           tc::mma_commit(empty(s));
         }
         if (*abort_flag) break;
-        tc::mma_commit(acc_full(buf));
+        tc::mma_commit(acc_full);
       }
       if (*abort_flag && issued_any) {
+        // MMAs still in flight must finish before TMEM is freed
         tc::mma_commit(mma_done);
         tc::mbar_wait(mma_done, 0, err, kSiteDrain);
       }
     }
-  } else if (warp == 6) {
-    // ---------------- scale-factor copier ----------------
-    // Copies each stage's scale factors from shared memory into the stage's
-    // TMEM slot as soon as the stage has landed, ahead of the MMA issuer.
-    if (lane == 0) {
-      int it = 0;
-      for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const int s = it % kStages;
-          if (!tc::mbar_wait(full(s), (it / kStages) & 1, err, kSiteFull)) { *abort_flag = 1; break; }
-          tc::tc_fence_after();
-          const uint32_t sf_smem = sbase + kSmemSf + s * kSfBytes;
-          const uint32_t sf_t = tmem_sf + s * kSfColsPerStage;
+  } else if (warp >= kSfWarp0) {
+    // ---------------- scale-factor writers ----------------
+    // Slot layout: A scales of MMA kk in columns 4kk..4kk+3, then B scales of
+    // MMA kk in columns 16+8kk..16+8kk+7 (rows 0-127, then rows 128-255).
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    int it = 0;
+    for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
+      bool ok = true;
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int s = it % kStages;
+        ok = tc::mbar_wait(sf_full(s), (it / kStages) & 1, err, kSiteFull);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) { *abort_flag = 1; break; }
+        tc::tc_fence_after();
+        const uint32_t src = sbase + kSmemSf + s * kSfBytes + 16 * lane;
+        uint32_t v[kSfColsPerStage];
 #pragma unroll
-          for (int i = 0; i < 2 * kMmaPerStage; ++i)
-            tc::tmem_cp_32x128b_x4(sf_t + 4 * i, tc::plain_desc(sf_smem + 512 * i));
-          tc::mma_commit(sf_ready(s));
+        for (int kk = 0; kk < kMmaPerStage; ++kk) {
+          const uint4 w = tc::lds128(src + kSfBlock * kk);
+          v[4 * kk] = w.x; v[4 * kk + 1] = w.y; v[4 * kk + 2] = w.z; v[4 * kk + 3] = w.w;
+#pragma unroll
+          for (int h = 0; h < kBN / 128; ++h) {
+            const uint4 u = tc::lds128(src + ((1 + h) * kMmaPerStage + kk) * kSfBlock);
+            const int c = kMmaPerStage * kSfaCols + kSfbCols * kk + 4 * h;
+            v[c] = u.x; v[c + 1] = u.y; v[c + 2] = u.z; v[c + 3] = u.w;
+          }
         }
+        const uint32_t dst = tmem + lane_base + kAccCols + s * kSfColsPerStage;
+        tc::tmem_st_32x32b_x32(dst, v);
+        tc::tmem_st_32x32b_x16(dst + 32, v + 32);
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(sf_ready(s));
       }
-      if (*abort_flag && it > 0) {
-        // copies still in flight must land before TMEM is freed
-        tc::mma_commit(cp_done);
-        tc::mbar_wait(cp_done, 0, err, kSiteDrain);
-      }
+      if (!ok) break;
     }
   } else {
     // ---------------- epilogue ----------------
-    const int q = warp & 3;  // warps 2-5: TMEM lane quadrants 2, 3, 0, 1
+    const int q = warp & 3;                      // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) / 4;             // column half of the 256-column tile
     const float alpha = __ldg(g_a) * __ldg(g_b);
     for (int ti = 0; ti < my_tiles; ++ti) {
-      const int buf = ti & 1;
-      bool ok = tc::mbar_wait(acc_full(buf), (ti / 2) & 1, err, kSiteAccFull);
+      bool ok = tc::mbar_wait(acc_full, ti & 1, err, kSiteAccFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) { *abort_flag = 1; break; }
       tc::tc_fence_after();
       int mt, nt;
       tile_coords(blockIdx.x + ti * gridDim.x, mt_count, nt_count, mt, nt);
-      const int row = mt * kBM + q * 32 + lane;
-      const int n0 = nt * kBN;
+      const int c0 = nt * kBN + half * 128;      // first output column of this warp
+      uint32_t pk[64];                           // 128 outputs, two per word
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + half * 128;
 #pragma unroll
-      for (int cg = 0; cg < kBN / 32; ++cg) {
+      for (int cg = 0; cg < 4; ++cg) {
         uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kAccCols + cg * 32, v);
+        tc::tmem_ld_32x32b_x32(taddr + cg * 32, v);
         tc::tmem_wait_ld();
-        if (row < T) {
 #pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            const int col = n0 + cg * 32 + c8 * 8;
-            if (col >= N) continue;
-            uint4 pk;
-            uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float f0 = __uint_as_float(v[c8 * 8 + 2 * i]) * alpha;
-              const float f1 = __uint_as_float(v[c8 * 8 + 2 * i + 1]) * alpha;
-              if (out_dtype == QLIN_BF16) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
-                pw[i] = *reinterpret_cast<uint32_t*>(&h);
-              } else {
-                __half2 h = __floats2half2_rn(f0, f1);
-                pw[i] = *reinterpret_cast<uint32_t*>(&h);
-              }
-            }
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (int64_t)row * N + col) = pk;
+        for (int i = 0; i < 16; ++i) {
+          const float f0 = __uint_as_float(v[2 * i]) * alpha;
+          const float f1 = __uint_as_float(v[2 * i + 1]) * alpha;
+          if (out_dtype == QLIN_BF16) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+            pk[16 * cg + i] = *reinterpret_cast<uint32_t*>(&h);
+          } else {
+            __half2 h = __floats2half2_rn(f0, f1);
+            pk[16 * cg + i] = *reinterpret_cast<uint32_t*>(&h);
           }
         }
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(acc_empty(buf));
+      if (lane == 0) tc::mbar_arrive(acc_empty);  // accumulator free for the next tile
+      // 8 x 8 transpose of 16-byte chunks inside each group of 8 lanes
+      // (three xor-butterfly steps): afterwards lane 8g+j holds, in slot e of
+      // column block b, chunk 8b+j of row 8g+e, so each store below writes 128
+      // contiguous bytes of four rows instead of 16 bytes of 32 rows.
+#pragma unroll
+      for (int st = 0; st < 3; ++st) {
+        const bool up = (lane >> st) & 1;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+#pragma unroll
+          for (int e0 = 0; e0 < 8; ++e0) {
+            if (e0 & (1 << st)) continue;
+            const int e1 = e0 | (1 << st);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              uint32_t& x0 = pk[4 * (8 * b + e0) + w];
+              uint32_t& x1 = pk[4 * (8 * b + e1) + w];
+              const uint32_t got = __shfl_xor_sync(0xffffffffu, up ? x0 : x1, 1 << st);
+              if (up) x0 = got; else x1 = got;
+            }
+          }
+        }
+      }
+      const int j = lane & 7;
+      const int row0 = mt * kBM + q * 32 + 8 * (lane >> 3);
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const int col = c0 + 8 * (8 * b + j);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int r = row0 + e;
+          if (r < T && col < N)
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (int64_t)r * N + col) =
+                make_uint4(pk[4 * (8 * b + e)], pk[4 * (8 * b + e) + 1], pk[4 * (8 * b + e) + 2],
+                           pk[4 * (8 * b + e) + 3]);
+        }
+      }
     }
   }
 

@@ -35,7 +35,8 @@ def _rand(rng, rows, k):
     return codes, sf
 
 
-@pytest.mark.parametrize("T,N,K", [(128, 128, 256), (130, 136, 320), (1, 8, 64), (200, 264, 4224), (300, 128, 1088)])
+@pytest.mark.parametrize("T,N,K", [(128, 128, 256), (130, 136, 320), (1, 8, 64), (200, 264, 4224), (300, 128, 1088),
+                                   (129, 384, 192), (1300, 4480, 320)])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
 def test_random_operands(qlin_gpu, T, N, K, out_dtype):
     rng = np.random.default_rng(T + N + K)
@@ -47,11 +48,13 @@ def test_random_operands(qlin_gpu, T, N, K, out_dtype):
     assert_within_tolerance(y, ref, "nvfp4 %dx%dx%d" % (T, N, K), out_dtype=out_dtype)
 
 
-def test_scale_factor_layout(qlin_gpu):
+@pytest.mark.parametrize("T,N", [(128, 128), (128, 256), (256, 384)])
+def test_scale_factor_layout(qlin_gpu, T, N):
     """Every element 1.0 and one non-unit block scale per row of A (and of B)
     at a row- and block-dependent position: any misplaced scale factor shows
-    up as a wrong output."""
-    T, N, K = 128, 128, 512
+    up as a wrong output.  N spans one, two and three 128-row scale blocks of
+    B, so both halves of a 256-column tile are exercised."""
+    K = 512
     qa = np.full((T, K), 2, dtype=np.uint8)           # E2M1 code 2 = 1.0
     qb = np.full((N, K), 2, dtype=np.uint8)
     one = 0x38                                         # E4M3 1.0
