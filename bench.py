@@ -4,8 +4,11 @@
 One step = one pass of every hot-path step over one batch of synthetic input:
   1. W4A16 decode (T = 1) through a Llama-2-7B-shaped linear stack: 32 blocks
      x {q, k, v, o: 4096x4096; gate, up: 11008x4096; down: 4096x11008},
-     224 fused dequant GEMV launches over 3.4 GB of int4 weights (larger than
-     L2, so every step streams the weights from HBM).
+     224 fused dequant GEMVs over 3.4 GB of int4 weights (larger than L2, so
+     every step streams the weights from HBM), launched with the block's
+     dependency structure: q, k, v grouped in one launch on the block input,
+     o on v's output, gate and up grouped on o's output, down on up's output
+     (4 launches per block).
   2. W8A8 symmetric + bias (T=2048, K=4096, N=4096): per-token int8
      quantization of X, then the int8-exact GEMM with the fused epilogue.
   3. NVFP4 + ARCQuant (T=2048, K=4096, N=4096, S=128): NVFP4 quantization of X
@@ -143,12 +146,14 @@ class Workload:
                 zp = torch.empty((N, (K // 128 + 1) // 2), dtype=torch.uint8, device=dev)
                 q.qlin_quant_w4_g128(protos[(N, K)][0], wq, sc, zp)
                 self.w4.append((N, K, wq, sc, zp))
-        # Activations: inside a block every layer reads the previous layer's
-        # output (q -> k -> v -> o on ping-pong buffers, gate and up from o's
-        # output, down from up's output); every block starts again from the
-        # step's input (the path has no normalisation between blocks).
+        # Activations, following a decoder block's dependencies: q, k and v
+        # read the block input; o reads v's output (in place of the attention
+        # output); gate and up read o's output; down reads up's output (in
+        # place of act(gate) * up).  Every block starts again from the step's
+        # input (the path has no normalisation between blocks).
         self.w4_in = protos[(4096, 4096)][1]
-        self.w4_h = [torch.empty((1, 4096), dtype=torch.float16, device=dev) for _ in range(2)]
+        self.w4_qkv = [torch.empty((1, 4096), dtype=torch.float16, device=dev) for _ in range(3)]
+        self.w4_o = torch.empty((1, 4096), dtype=torch.float16, device=dev)
         self.w4_gate = torch.empty((1, 11008), dtype=torch.float16, device=dev)
         self.w4_up = torch.empty((1, 11008), dtype=torch.float16, device=dev)
         self.w4_out = torch.empty((1, 4096), dtype=torch.float16, device=dev)
@@ -187,22 +192,18 @@ class Workload:
         self.nv_sfx = torch.empty(q.qlin_nvfp4_sf_bytes(T, K + S, q.QLIN_SF_MMA), dtype=torch.uint8, device=dev)
         self.nv_out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
         torch.cuda.synchronize()
-        self.launches = {"w4a16": len(self.w4), "w8a8": 2, "nvfp4": 2}
+        self.launches = {"w4a16": 4 * layers, "w8a8": 2, "nvfp4": 2}
 
     # the three phases, as plain launch sequences on the current stream
     def phase_w4a16(self):
-        gemm = self.q.qlin_w4a16_gemm
+        gemm, grouped = self.q.qlin_w4a16_gemm, self.q.qlin_w4a16_gemm_grouped
         per_block = len(LLAMA_BLOCK)
         for b0 in range(0, len(self.w4), per_block):
-            blk = self.w4[b0:b0 + per_block]
-            h = self.w4_in
-            for i in range(4):  # q, k, v, o
-                out = self.w4_h[i % 2]
-                gemm(h, *blk[i][2:], out)
-                h = out
-            gemm(h, *blk[4][2:], self.w4_gate)
-            gemm(h, *blk[5][2:], self.w4_up)
-            gemm(self.w4_up, *blk[6][2:], self.w4_out)
+            q, k, v, o, gate, up, down = self.w4[b0:b0 + per_block]
+            grouped(self.w4_in, [q[2], k[2], v[2]], [q[3], k[3], v[3]], [q[4], k[4], v[4]], self.w4_qkv)
+            gemm(self.w4_qkv[2], *o[2:], self.w4_o)
+            grouped(self.w4_o, [gate[2], up[2]], [gate[3], up[3]], [gate[4], up[4]], [self.w4_gate, self.w4_up])
+            gemm(self.w4_up, *down[2:], self.w4_out)
 
     def phase_w8a8(self):
         self.q.qlin_quant_act_int8(self.w8_x, self.w8_a, self.w8_sa)
@@ -387,8 +388,8 @@ def run_ours(args):
     w8_ops = 2 * W8A8["T"] * W8A8["N"] * W8A8["K"]
     nv_ops = 2 * NVFP4["T"] * NVFP4["N"] * (NVFP4["K"] + NVFP4["S"])
     peak16 = peaks["bf16_tflops_sustained"]
-    per_launch_bytes = wl.w4_bytes / len(wl.w4)
-    per_launch_s = tw4 / len(wl.w4)
+    per_launch_bytes = wl.w4_bytes / wl.launches["w4a16"]
+    per_launch_s = tw4 / wl.launches["w4a16"]
     traffic = recorded_traffic()
     line = {
         "metric": METRIC,
@@ -404,10 +405,12 @@ def run_ours(args):
         "dtype": "u4xf16->f32 | s8(f16-exact)->s32 | e2m1xe4m3->f32",
         "data": "synthetic",
         "config": {
-            "workload": "W4A16 T=1 decode over a Llama-2-7B-shaped linear stack (%d blocks x 7 layers, each layer "
-                        "reading the previous layer's output within a block) + "
+            "workload": "W4A16 T=1 decode over a Llama-2-7B-shaped linear stack (%d blocks x 7 layers with the "
+                        "block's dependencies: q,k,v grouped on the block input, o on v, gate,up grouped on o, "
+                        "down on up; 4 launches per block) + "
                         "W8A8 sym+bias T=2048 K=4096 N=4096 + NVFP4 ARCQuant T=2048 K=4096 N=4096 S=128" % args.layers,
-            "w4a16_launches_per_step": len(wl.w4),
+            "w4a16_launches_per_step": wl.launches["w4a16"],
+            "w4a16_layers_per_step": len(wl.w4),
             "w4a16_weight_bytes_per_step": wl.w4_bytes,
             "l2": "inputs larger than L2: each step streams %.2f GB of W4A16 weights, which also evicts the "
                   "W8A8/NVFP4 operands between steps" % (wl.w4_bytes / 1e9),

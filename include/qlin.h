@@ -146,6 +146,33 @@ qlin_status qlin_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, cons
                             cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * a1, grouped - several W4A16 linears of the same input in one call
+ *
+ * Y_p = X . dequant(W_p)^T for p = 0 .. count-1, every W_p with the same K:
+ * the q, k and v projections of a decoder block, or its gate and up
+ * projections, which all read the same activations.  At T = 1 a single GEMV
+ * launch covers the concatenated rows of all count matrices, so the group
+ * waits once on the kernel that produced X instead of once per matrix; for
+ * T > 1 (or a concatenation too large for one launch's plan) each matrix
+ * runs as qlin_w4a16_gemm.  Each row is computed exactly as in a separate
+ * qlin_w4a16_gemm call, so the results equal count separate calls bit for
+ * bit.
+ *   x       fp16 [T][K]
+ *   count   1 .. QLIN_W4A16_MAX_GROUP
+ *   N       host array [count], rows of each W_p (0 allowed)
+ *   wq, scales, zeros, y
+ *           host arrays [count] of device pointers, each W_p and Y_p laid
+ *           out as in qlin_w4a16_gemm (zeros[p] NULL: symmetric, z = 8)
+ *   group   128
+ * The host arrays are read during the call only.
+ * ---------------------------------------------------------------------- */
+#define QLIN_W4A16_MAX_GROUP 4
+qlin_status qlin_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
+                                    const uint8_t* const* wq, const void* const* scales,
+                                    const uint8_t* const* zeros, int64_t group, void* const* y,
+                                    cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * b1 - per-token int8 activation quantization
  *
  * Symmetric (azp == NULL): s_t = max_k |x| / 127 (s_t = 1 for an all-zero

@@ -20,7 +20,7 @@ __all__ = [
     "QLIN_F16", "QLIN_BF16", "QLIN_F32", "QLIN_I32", "QLIN_NVFP4_RESIDUAL", "QLIN_NVFP4_DUPLICATE",
     "QLIN_SF_ROWS", "QLIN_SF_MMA", "qlin_nvfp4_sf_bytes", "qlin_nvfp4_sf_to_mma",
     "qlin_version", "qlin_get_device_error",
-    "qlin_quant_w4_g128", "qlin_w4a16_gemm", "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm",
+    "qlin_quant_w4_g128", "qlin_w4a16_gemm", "qlin_w4a16_gemm_grouped", "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm",
     "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
 ]
 
@@ -48,6 +48,7 @@ _SIGS = {
     "qlin_get_device_error": ([_P, _P], _I32),
     "qlin_quant_w4_g128": ([_P, _I32, _I64, _I64, _I64, _P, _P, _P, _P], _I32),
     "qlin_w4a16_gemm": ([_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P], _I32),
+    "qlin_w4a16_gemm_grouped": ([_P, _I64, _I64, _I32, _P, _P, _P, _P, _I64, _P, _P], _I32),
     "qlin_quant_act_int8": ([_P, _I32, _I64, _I64, _P, _P, _P, _P], _I32),
     "qlin_int8_row_sum": ([_P, _I64, _I64, _P, _P], _I32),
     "qlin_w8a8_gemm": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
@@ -147,6 +148,27 @@ def qlin_w4a16_gemm(x, wq, scales, zeros, y, group=128, stream=None):
     n = wq.shape[0]
     _check("qlin_w4a16_gemm", lib().qlin_w4a16_gemm(_ptr(x), t, n, k, _ptr(wq), _ptr(scales), _ptr(zeros), group,
                                                    _ptr(y), _stream(stream)))
+
+
+def qlin_w4a16_gemm_grouped(x, wqs, scales, zeros, ys, group=128, stream=None):
+    """ys[p][T][N_p] = x[T][K] . dequant(wqs[p], scales[p], zeros[p])^T for every p, in one call
+    (zeros[p] None = symmetric, z = 8)."""
+    torch = _torch()
+    count = len(wqs)
+    if not (len(scales) == len(zeros) == len(ys) == count):
+        raise ValueError("wqs, scales, zeros and ys must have the same length")
+    _need(x, torch.float16, name="x")
+    for p in range(count):
+        _need(wqs[p], torch.uint8, name="wq"); _need(scales[p], torch.float16, name="scales")
+        _need(zeros[p], torch.uint8, name="zeros"); _need(ys[p], torch.float16, name="y")
+    t, k = x.shape
+    n_arr = (ctypes.c_int64 * count)(*[w.shape[0] for w in wqs])
+    wq_arr = (ctypes.c_void_p * count)(*[w.data_ptr() for w in wqs])
+    s_arr = (ctypes.c_void_p * count)(*[s.data_ptr() for s in scales])
+    z_arr = (ctypes.c_void_p * count)(*[0 if z is None else z.data_ptr() for z in zeros])
+    y_arr = (ctypes.c_void_p * count)(*[y.data_ptr() for y in ys])
+    _check("qlin_w4a16_gemm_grouped", lib().qlin_w4a16_gemm_grouped(
+        _ptr(x), t, k, count, n_arr, wq_arr, s_arr, z_arr, group, y_arr, _stream(stream)))
 
 
 def qlin_quant_act_int8(x, q, scale, azp=None, stream=None):

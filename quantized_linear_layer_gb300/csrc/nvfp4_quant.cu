@@ -54,25 +54,71 @@ __device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
   return __half22float2(h);
 }
 
+// x / d from r = __frcp_rn(d) by one FMA correction step (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", 1990), with the sign taken from x.  Equal to __fdiv_rn(x, d)
+// when d, r and the quotient are normal; a quotient below the normal range
+// comes out as a tiny number or zero with the sign of x (a zero dividend
+// keeps its sign, which the correction's +0 would otherwise drop).
+__device__ __forceinline__ float div_rcp_signed(float x, float d, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float q = __fmaf_rn(__fmaf_rn(-q0, d, x), r, q0);
+  return __int_as_float((__float_as_int(q) & 0x7FFFFFFF) | (__float_as_int(x) & static_cast<int>(0x80000000u)));
+}
+
+constexpr float kMinNormal = 1.17549435e-38f;
+constexpr float kMaxFinite = 3.40282347e38f;
+
+// Per-tensor scale g with its reciprocal, and whether s / g may go through
+// the reciprocal (g and 1/g normal).
+struct GlobalScale {
+  float g, rg;
+  bool fast;
+};
+
+__device__ __forceinline__ GlobalScale make_global_scale(float g) {
+  GlobalScale gs;
+  gs.g = g;
+  gs.rg = __frcp_rn(g);
+  gs.fast = fabsf(g) >= kMinNormal && fabsf(g) <= kMaxFinite && fabsf(gs.rg) >= kMinNormal && fabsf(gs.rg) <= kMaxFinite;
+  return gs;
+}
+
+// (amax / 6) / g with both divisions correctly rounded.  The reciprocal path
+// is taken only where it provably gives the same float (normal operands and
+// quotients); every other case uses the division itself.
+__device__ __forceinline__ float block_scale_value(float amax, const GlobalScale& gs) {
+  if (amax == 0.0f) return 0.0f;
+  const float r6 = 0.166666672f;  // float nearest 1/6
+  const float s1 = (amax >= 6.0f * kMinNormal && amax <= kMaxFinite)
+                       ? __fmaf_rn(__fmaf_rn(-__fmul_rn(amax, r6), 6.0f, amax), r6, __fmul_rn(amax, r6))
+                       : __fdiv_rn(amax, 6.0f);
+  if (gs.fast) {
+    const float s2 = __fmaf_rn(__fmaf_rn(-__fmul_rn(s1, gs.rg), gs.g, s1), gs.rg, __fmul_rn(s1, gs.rg));
+    if (s2 >= kMinNormal && s2 <= kMaxFinite) return s2;
+  }
+  return __fdiv_rn(s1, gs.g);
+}
+
 // Quantize one 16-element block; returns the scale code, writes 8 code bytes.
-__device__ __forceinline__ uint32_t quant_block16(const float* v, float g, uint32_t* packed /*[2]*/, float* d_out) {
+__device__ __forceinline__ uint32_t quant_block16(const float* v, const GlobalScale& gs, uint32_t* packed /*[2]*/,
+                                                  float* d_out) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const float scaled = (amax == 0.0f) ? 0.0f : __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
-  const uint32_t sfc = f32_to_e4m3(scaled);
-  const float d = __fmul_rn(e4m3_to_f32(sfc), g);
+  const uint32_t sfc = f32_to_e4m3(block_scale_value(amax, gs));
+  const float d = __fmul_rn(e4m3_to_f32(sfc), gs.g);
   packed[0] = 0u;
   packed[1] = 0u;
   if (d != 0.0f) {
-    // The 16 quotients share d: x / d through the correctly rounded
-    // reciprocal and one FMA correction (equal to the IEEE quotient wherever
-    // it can change a code: every E2M1 decision lies in the normal range).
+    // The 16 quotients share d.  Through the reciprocal when d and 1/d are
+    // normal and no quotient can overflow (|x r| <= amax r finite): a
+    // quotient below the normal range rounds to a zero code either way.
     const float rd = __frcp_rn(d);
-    if (rcp_division_ok(d, rd)) {
+    if (fabsf(d) >= kMinNormal && rd >= kMinNormal && __fmul_rn(amax, rd) <= 1.0e38f) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint32_t byte = f32x2_to_e2m1x2(div_by_rcp(v[2 * i], d, rd), div_by_rcp(v[2 * i + 1], d, rd));
+        const uint32_t byte = f32x2_to_e2m1x2(div_rcp_signed(v[2 * i], d, rd), div_rcp_signed(v[2 * i + 1], d, rd));
         packed[i >> 2] |= byte << (8 * (i & 3));
       }
     } else {
@@ -87,84 +133,97 @@ __device__ __forceinline__ uint32_t quant_block16(const float* v, float g, uint3
   return sfc;
 }
 
-// One CTA per row: the row is staged in shared memory in its input dtype,
-// then each thread quantizes 16-element blocks of the reordered row.
-template <int DT>
-__global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __restrict__ x, int K,
+// R rows per CTA: the rows are staged in shared memory in their input dtype,
+// then each thread quantizes 16-element blocks of the reordered rows; the
+// block's 16 channel offsets are loaded and checked once for all R rows.
+template <int DT, int R>
+__global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __restrict__ x, int64_t rows, int K,
                                                                   const int32_t* __restrict__ perm, int S,
                                                                   int mode, const float* __restrict__ gp,
                                                                   uint8_t* __restrict__ q,
                                                                   uint8_t* __restrict__ sf, int sf_mma,
                                                                   int32_t* __restrict__ err) {
   extern __shared__ __align__(16) unsigned char row_smem[];
-  const int64_t row = blockIdx.x;
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * R;
+  const int nr = static_cast<int>(min(static_cast<int64_t>(R), rows - row0));
   const int tid = threadIdx.x;
   constexpr int EB = elem_bytes<DT>();
-  const char* xr = static_cast<const char*>(x) + row * (int64_t)K * EB;
   const int row_bytes = K * EB;
-  for (int off = tid * 16; off < row_bytes; off += kNvThreads * 16)
-    *reinterpret_cast<uint4*>(row_smem + off) = ldg_v4(xr + off);
+  {
+    const char* xr = static_cast<const char*>(x) + row0 * row_bytes;
+    for (int off = tid * 16; off < nr * row_bytes; off += kNvThreads * 16)
+      *reinterpret_cast<uint4*>(row_smem + off) = ldg_v4(xr + off);
+  }
   __syncthreads();
 
-  const float g = __ldg(gp);
+  const GlobalScale gs = make_global_scale(__ldg(gp));
   const int Kaug = K + S;
-  uint8_t* qr = q + row * (int64_t)(Kaug / 2);
-  // Position of the scale of block b of this row in either layout.
-  const int64_t sf_row_base = sf_mma ? ((row >> 7) * (int64_t)(Kaug / 64)) * 512 + 16 * (row & 31) + 4 * ((row & 127) >> 5)
-                                     : row * (int64_t)(Kaug / 16);
-  auto sf_at = [&](int b) -> uint8_t& {
-    return sf_mma ? sf[sf_row_base + (int64_t)(b >> 2) * 512 + (b & 3)] : sf[sf_row_base + b];
-  };
   const int nblk = K / 16;
   const int sblk = S / 16;
-  // A channel index outside [0, K) is recorded in the device error word and
-  // read as channel 0, so the shared-memory gather stays in bounds.
-  auto channel = [&](int p) -> int {
-    if (static_cast<unsigned>(p) >= static_cast<unsigned>(K)) {
-      record_device_error(err, kDevErrBadIndex);
-      return 0;
-    }
-    return p;
-  };
   for (int b = tid; b < nblk; b += kNvThreads) {
-    float v[16];
+    // byte offsets of the block's channels in a staged row; a channel index
+    // outside [0, K) is recorded in the device error word and read as K-1,
+    // so the shared-memory gather stays in bounds
+    uint32_t off[16];
     if (perm != nullptr) {
       const int4* pp = reinterpret_cast<const int4*>(perm + b * 16);
+      uint32_t pmax = 0;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int4 p4 = __ldg(pp + i);
-        v[4 * i + 0] = load_elem<DT>(row_smem, channel(p4.x));
-        v[4 * i + 1] = load_elem<DT>(row_smem, channel(p4.y));
-        v[4 * i + 2] = load_elem<DT>(row_smem, channel(p4.z));
-        v[4 * i + 3] = load_elem<DT>(row_smem, channel(p4.w));
+        const uint32_t c[4] = {static_cast<uint32_t>(p4.x), static_cast<uint32_t>(p4.y),
+                               static_cast<uint32_t>(p4.z), static_cast<uint32_t>(p4.w)};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          pmax = max(pmax, c[j]);
+          off[4 * i + j] = min(c[j], static_cast<uint32_t>(K - 1)) * EB;
+        }
       }
+      if (pmax >= static_cast<uint32_t>(K)) record_device_error(err, kDevErrBadIndex);
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = load_elem<DT>(row_smem, b * 16 + i);
+      for (int i = 0; i < 16; ++i) off[i] = (b * 16 + i) * EB;
     }
-    uint32_t packed[2];
-    float d;
-    const uint32_t sfc = quant_block16(v, g, packed, &d);
-    *reinterpret_cast<uint2*>(qr + b * 8) = make_uint2(packed[0], packed[1]);
-    sf_at(b) = static_cast<uint8_t>(sfc);
-    if (b < sblk) {
-      if (mode == QLIN_NVFP4_DUPLICATE) {
-        *reinterpret_cast<uint2*>(qr + (K / 2) + b * 8) = make_uint2(packed[0], packed[1]);
-        sf_at(nblk + b) = static_cast<uint8_t>(sfc);
-      } else {
-        // residual r = x - e2m1(q) * d, one float32 multiply then one subtract
-        float r[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float2 e = e2m1x2_to_f32x2((packed[i >> 2] >> (8 * (i & 3))) & 0xFFu);
-          r[2 * i] = __fsub_rn(v[2 * i], __fmul_rn(e.x, d));
-          r[2 * i + 1] = __fsub_rn(v[2 * i + 1], __fmul_rn(e.y, d));
+    for (int rr = 0; rr < R; ++rr) {
+      if (rr >= nr) break;
+      const int64_t row = row0 + rr;
+      const unsigned char* rs = row_smem + rr * row_bytes;
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = load_elem<DT>(rs + off[i], 0);
+      uint32_t packed[2];
+      float d;
+      const uint32_t sfc = quant_block16(v, gs, packed, &d);
+      uint8_t* qr = q + row * (int64_t)(Kaug / 2);
+      // position of the scale of block j of this row in either layout
+      const int64_t sf_row_base = sf_mma ? ((row >> 7) * (int64_t)(Kaug / 64)) * 512 + 16 * (row & 31) +
+                                               4 * ((row & 127) >> 5)
+                                         : row * (int64_t)(Kaug / 16);
+      auto sf_at = [&](int j) -> uint8_t& {
+        return sf_mma ? sf[sf_row_base + (int64_t)(j >> 2) * 512 + (j & 3)] : sf[sf_row_base + j];
+      };
+      *reinterpret_cast<uint2*>(qr + b * 8) = make_uint2(packed[0], packed[1]);
+      sf_at(b) = static_cast<uint8_t>(sfc);
+      if (b < sblk) {
+        if (mode == QLIN_NVFP4_DUPLICATE) {
+          *reinterpret_cast<uint2*>(qr + (K / 2) + b * 8) = make_uint2(packed[0], packed[1]);
+          sf_at(nblk + b) = static_cast<uint8_t>(sfc);
+        } else {
+          // residual r = x - e2m1(q) * d, one float32 multiply then one subtract
+          float r[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float2 e = e2m1x2_to_f32x2((packed[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+            r[2 * i] = __fsub_rn(v[2 * i], __fmul_rn(e.x, d));
+            r[2 * i + 1] = __fsub_rn(v[2 * i + 1], __fmul_rn(e.y, d));
+          }
+          uint32_t rp[2];
+          float rd;
+          const uint32_t rsf = quant_block16(r, gs, rp, &rd);
+          *reinterpret_cast<uint2*>(qr + (K / 2) + b * 8) = make_uint2(rp[0], rp[1]);
+          sf_at(nblk + b) = static_cast<uint8_t>(rsf);
         }
-        uint32_t rp[2];
-        float rd;
-        const uint32_t rsf = quant_block16(r, g, rp, &rd);
-        *reinterpret_cast<uint2*>(qr + (K / 2) + b * 8) = make_uint2(rp[0], rp[1]);
-        sf_at(nblk + b) = static_cast<uint8_t>(rsf);
       }
     }
   }
@@ -265,16 +324,23 @@ cudaError_t launch_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, 
   if (rows == 0) return cudaSuccess;
   return dispatch_dtype(x_dtype, [&](auto dt) -> cudaError_t {
     constexpr int DT = decltype(dt)::value;
-    const size_t smem = static_cast<size_t>(K) * elem_bytes<DT>();
-    if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(nvfp4_quant_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
-    }
-    nvfp4_quant_kernel<DT><<<static_cast<unsigned>(rows), kNvThreads, smem, stream>>>(
-        x, static_cast<int>(K), perm, static_cast<int>(S), static_cast<int>(mode), g, q, sf,
-        sf_layout == QLIN_SF_MMA ? 1 : 0, device_error_word());
-    return cudaGetLastError();
+    const size_t row_smem = static_cast<size_t>(K) * elem_bytes<DT>();
+    auto launch = [&](auto rows_per_cta) -> cudaError_t {
+      constexpr int R = decltype(rows_per_cta)::value;
+      const size_t smem = row_smem * R;
+      if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(nvfp4_quant_kernel<DT, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+      }
+      nvfp4_quant_kernel<DT, R><<<static_cast<unsigned>((rows + R - 1) / R), kNvThreads, smem, stream>>>(
+          x, rows, static_cast<int>(K), perm, static_cast<int>(S), static_cast<int>(mode), g, q, sf,
+          sf_layout == QLIN_SF_MMA ? 1 : 0, device_error_word());
+      return cudaGetLastError();
+    };
+    // two rows per CTA share the channel offsets while both fit comfortably
+    if (2 * row_smem <= 96 * 1024) return launch(std::integral_constant<int, 2>{});
+    return launch(std::integral_constant<int, 1>{});
   });
 }
 

@@ -189,6 +189,36 @@ qlin_status qlin_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, cons
   QLIN_LAUNCH(launch_w4a16_gemm(x, T, N, K, wq, scales, zeros, y, stream), "w4a16_gemm launch");
 }
 
+qlin_status qlin_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
+                                    const uint8_t* const* wq, const void* const* scales,
+                                    const uint8_t* const* zeros, int64_t group, void* const* y,
+                                    cudaStream_t stream) {
+  QLIN_REQUIRE(group == 128, QLIN_ERR_UNSUPPORTED, "group size %lld (only 128 is built)", (long long)group);
+  QLIN_REQUIRE(count >= 1 && count <= QLIN_W4A16_MAX_GROUP, QLIN_ERR_INVALID_ARG, "count=%d outside [1, %d]", count,
+               QLIN_W4A16_MAX_GROUP);
+  QLIN_REQUIRE(N && wq && scales && zeros && y, QLIN_ERR_INVALID_ARG, "null host array");
+  QLIN_REQUIRE(T >= 0 && T <= 64, QLIN_ERR_INVALID_ARG, "T=%lld outside [0, 64]", (long long)T);
+  QLIN_REQUIRE(K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad K=%lld", (long long)K);
+  QLIN_REQUIRE(K % group == 0, QLIN_ERR_INVALID_ARG, "K=%lld is not a multiple of the group size", (long long)K);
+  int64_t total = 0;
+  for (int p = 0; p < count; ++p) {
+    QLIN_REQUIRE(N[p] >= 0 && N[p] <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad N[%d]=%lld", p, (long long)N[p]);
+    total += N[p];
+  }
+  QLIN_REQUIRE(total <= kMaxDim, QLIN_ERR_INVALID_ARG, "total rows %lld too large", (long long)total);
+  if (T == 0 || total == 0) return ok();
+  QLIN_REQUIRE(x && aligned16(x), x ? QLIN_ERR_ALIGNMENT : QLIN_ERR_INVALID_ARG, "x must be non-null and 16-byte aligned");
+  for (int p = 0; p < count; ++p) {
+    if (N[p] == 0) continue;
+    QLIN_REQUIRE(wq[p] && scales[p] && y[p], QLIN_ERR_INVALID_ARG, "null pointer for matrix %d", p);
+    QLIN_REQUIRE(aligned16(wq[p]), QLIN_ERR_ALIGNMENT, "wq[%d] must be 16-byte aligned", p);
+    QLIN_REQUIRE((reinterpret_cast<uintptr_t>(scales[p]) & 1u) == 0 && (reinterpret_cast<uintptr_t>(y[p]) & 1u) == 0,
+                 QLIN_ERR_ALIGNMENT, "scales[%d] and y[%d] must be 2-byte aligned", p, p);
+  }
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_w4a16_gemm_grouped(x, T, K, count, N, wq, scales, zeros, y, stream), "w4a16_gemm_grouped launch");
+}
+
 qlin_status qlin_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
                                 float* scale, int32_t* azp, cudaStream_t stream) {
   QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");

@@ -28,6 +28,14 @@ cudaError_t launch_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, co
 bool w4a16_gemv_supported(int64_t T, int64_t N, int64_t K);
 cudaError_t launch_w4a16_gemv(const void* x, int64_t N, int64_t K, const uint8_t* wq, const void* scales,
                               const uint8_t* zeros, void* y, cudaStream_t stream);
+// One GEMV launch over the concatenated rows of `count` matrices sharing x
+// (cudaErrorInvalidValue when the concatenation has no launch plan).
+cudaError_t launch_w4a16_gemv_grouped(const void* x, int64_t K, int count, const int64_t* N,
+                                      const uint8_t* const* wq, const void* const* scales,
+                                      const uint8_t* const* zeros, void* const* y, cudaStream_t stream);
+cudaError_t launch_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
+                                      const uint8_t* const* wq, const void* const* scales,
+                                      const uint8_t* const* zeros, void* const* y, cudaStream_t stream);
 
 cudaError_t launch_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
                                   float* scale, int32_t* azp, cudaStream_t stream);

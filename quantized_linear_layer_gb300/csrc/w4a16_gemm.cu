@@ -427,4 +427,19 @@ cudaError_t launch_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, co
   return cudaSuccess;
 }
 
+cudaError_t launch_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
+                                      const uint8_t* const* wq, const void* const* scales,
+                                      const uint8_t* const* zeros, void* const* y, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  int64_t total = 0;
+  for (int p = 0; p < count; ++p) total += N[p];
+  if (total == 0) return cudaSuccess;
+  if (w4a16_gemv_supported(T, total, K)) return launch_w4a16_gemv_grouped(x, K, count, N, wq, scales, zeros, y, stream);
+  for (int p = 0; p < count; ++p) {
+    cudaError_t e = launch_w4a16_gemm(x, T, N[p], K, wq[p], scales[p], zeros[p], y[p], stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace qlin

@@ -39,6 +39,13 @@
 // spread over the warps of one row group, the CTA's rows over its row groups.
 // Per row a warp adds its lanes' partial sums with shuffles; the warps' sums
 // meet in shared memory and are added in a fixed order at the end.
+//
+// Grouped launch.  Several weight matrices applied to the same activations
+// (the q, k and v projections of a decoder block, or gate and up) run as one
+// launch over their concatenated rows: the bands simply continue from one
+// matrix into the next, a stage that straddles a boundary is filled by one
+// bulk copy per matrix, and the matrices share a single wait on the kernel
+// that produced the activations.
 #include <algorithm>
 #include <type_traits>
 
@@ -56,18 +63,23 @@ constexpr int kGvCtaBytes = 112 * 1024;     // two CTAs (this layer, the next) f
 constexpr int kGvMinStages = 2;
 constexpr int kGvMaxStages = 8;
 constexpr int kGvSiteFull = 1, kGvSiteEmpty = 2, kGvSiteDrain = 3;
+constexpr int kGvMaxGroup = QLIN_W4A16_MAX_GROUP;
+constexpr int64_t kMaxGemvRows = int64_t(1) << 30;  // launch rows are ints
 
 struct GvArgs {
   const __half* x;
-  const uint8_t* wq;
-  const __half* scales;
-  const uint8_t* zeros;
-  __half* y;
+  // matrix p covers rows [row_end[p-1], row_end[p]) of the launch
+  const uint8_t* wq[kGvMaxGroup];
+  const __half* scales[kGvMaxGroup];
+  const uint8_t* zeros[kGvMaxGroup];
+  __half* y[kGvMaxGroup];
+  int row_end[kGvMaxGroup];
+  int np;
   int32_t* err;
   int N, K, zpitch;
   int WPR, RG;                 // warps per row, row groups
   int R, S, stage_bytes;       // rows per stage, stages
-  int off_sz, off_red, off_bar;
+  int off_sz, off_red, off_raw_s, off_raw_z, off_bar;
 };
 
 // d = c + sum_i a.byte[i] . b.byte[i], a unsigned bytes, b signed bytes.
@@ -123,9 +135,9 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ float2 lds64f(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 
@@ -134,22 +146,91 @@ __device__ __forceinline__ float2 lds64f(uint32_t addr) {
 // are never stored), so the four chunks run without branches and interleave;
 // idle lanes have zero activations and contribute 0.  Addresses are 32-bit
 // shared-window offsets: cbase = the thread's chunk in the stage, sbase = its
-// group's {scale, zero} of the stage's first row.
+// group's packed {scale, zero} of the stage's first row (fp16 scale bits in
+// the low half, the zero-point in the high half).
 template <int NP, int B>
 __device__ __forceinline__ void gv_batch(uint32_t cbase, uint32_t sbase, int rows_i, int RG, int rg, int row_bytes,
                                          int G, const uint32_t (*xp)[8], const int* xsum, float xzf, float sx,
                                          float* p) {
   uint4 q[B];
-  float2 m[B];
+  uint32_t m[B];
 #pragma unroll
   for (int b = 0; b < B; ++b) {
     const int rrc = min(rg + RG * b, rows_i - 1);
     q[b] = lds128(cbase + rrc * row_bytes);
-    m[b] = lds64f(sbase + rrc * G * 8);
+    m[b] = lds32(sbase + rrc * G * 4);
   }
 #pragma unroll
-  for (int b = 0; b < B; ++b)
-    p[b] = (m[b].x * sx) * gv_chunk<NP>(q[b], xp, xsum, xzf, __float_as_int(m[b].y));
+  for (int b = 0; b < B; ++b) {
+    const float sg = __half2float(__ushort_as_half(static_cast<unsigned short>(m[b] & 0xFFFFu)));
+    p[b] = (sg * sx) * gv_chunk<NP>(q[b], xp, xsum, xzf, static_cast<int>(m[b] >> 16));
+  }
+}
+
+// Matrix of launch row r, and the first launch row of that matrix.
+__device__ __forceinline__ int gv_matrix(const GvArgs& a, int r, int& first) {
+  int p = 0;
+#pragma unroll
+  for (int i = 0; i < kGvMaxGroup - 1; ++i)
+    if (i < a.np - 1 && r >= a.row_end[i]) p = i + 1;
+  first = p > 0 ? a.row_end[p - 1] : 0;
+  return p;
+}
+
+// The band's scales and zero-points are staged raw in shared memory, one
+// bulk copy per matrix segment and array.  A copy starts at the 16-byte
+// boundary below its first byte and ends at the one above its last (the
+// copied window never leaves the 16-byte blocks holding the segment), and
+// each segment's window starts 16-byte aligned in the staging area.
+struct GvSeg {
+  int row0, rows;         // band rows [row0, row0 + rows) (relative to the band)
+  int sc_off, z_off;      // staging offsets of the segment's first scale / zero byte
+  const char* sc_lo;      // copy windows (16-byte aligned)
+  uint32_t sc_bytes;
+  const char* z_lo;
+  uint32_t z_bytes;
+};
+
+// Segment `k` of the band [r0, r0 + nrows), in band order; false past the last.
+__device__ __forceinline__ bool gv_segment(const GvArgs& a, int r0, int nrows, int G, int k, GvSeg& sg) {
+  int done = 0, sc_off = 0, z_off = 0;
+  for (int i = 0; done < nrows; ++i) {
+    const int r = r0 + done;
+    int first;
+    const int p = gv_matrix(a, r, first);
+    const int seg = min(nrows - done, a.row_end[p] - r);
+    const char* sc = reinterpret_cast<const char*>(a.scales[p] + static_cast<int64_t>(r - first) * G);
+    const char* sc_lo = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(sc) & ~uintptr_t(15));
+    const uint32_t sc_bytes = static_cast<uint32_t>(
+        ((reinterpret_cast<uintptr_t>(sc) + static_cast<uintptr_t>(seg) * G * 2 + 15) & ~uintptr_t(15)) -
+        reinterpret_cast<uintptr_t>(sc_lo));
+    const char* z_lo = nullptr;
+    uint32_t z_bytes = 0;
+    int z_delta = 0;
+    if (a.zeros[p]) {
+      const char* z = reinterpret_cast<const char*>(a.zeros[p] + static_cast<int64_t>(r - first) * a.zpitch);
+      z_lo = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(z) & ~uintptr_t(15));
+      z_bytes = static_cast<uint32_t>(
+          ((reinterpret_cast<uintptr_t>(z) + static_cast<uintptr_t>(seg) * a.zpitch + 15) & ~uintptr_t(15)) -
+          reinterpret_cast<uintptr_t>(z_lo));
+      z_delta = static_cast<int>(z - z_lo);
+    }
+    if (i == k) {
+      sg.row0 = done;
+      sg.rows = seg;
+      sg.sc_off = sc_off + static_cast<int>(sc - sc_lo);
+      sg.z_off = a.zeros[p] ? z_off + z_delta : -1;
+      sg.sc_lo = sc_lo;
+      sg.sc_bytes = sc_bytes;
+      sg.z_lo = z_lo;
+      sg.z_bytes = z_bytes;
+      return true;
+    }
+    sc_off += static_cast<int>(sc_bytes);
+    z_off += static_cast<int>(z_bytes);
+    done += seg;
+  }
+  return false;
 }
 
 __device__ __forceinline__ void named_sync(int id, int threads) {
@@ -169,19 +250,21 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
   const int nrows = base + (static_cast<int>(blockIdx.x) < extra ? 1 : 0);
   const int nloads = (nrows + a.R - 1) / a.R;
   const int S = a.S;
-  float2* sz = reinterpret_cast<float2*>(smem + a.off_sz);  // per (row, group): {s, z as int bits}
+  uint32_t* sz = reinterpret_cast<uint32_t*>(smem + a.off_sz);  // per (row, group): fp16 s | z << 16
   float* red = reinterpret_cast<float*>(smem + a.off_red);
   const uint32_t ring = tc::smem_u32(smem);
   const uint32_t bar0 = tc::smem_u32(smem + a.off_bar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + a.off_bar + 16 * S);
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+  const uint32_t meta_full = bar0 + 16u * S + 8u;  // the band's raw scales and zero-points
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(full(s), 1);
       tc::mbar_init(empty(s), ncw);
     }
+    tc::mbar_init(meta_full, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -192,6 +275,22 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
     // ---------------- producer: the CTA's band of weight rows ----------------
     if (lane == 0) {
       const uint64_t policy = tc::l2_policy_evict_first();
+      // scales and zero-points first: the compute warps convert them while
+      // the weight rows stream
+      {
+        uint32_t meta_bytes = 0;
+        GvSeg sg;
+        for (int k = 0; gv_segment(a, r0, nrows, G, k, sg); ++k) meta_bytes += sg.sc_bytes + sg.z_bytes;
+        tc::mbar_arrive_expect_tx(meta_full, meta_bytes);
+        const uint32_t raw_s = tc::smem_u32(smem + a.off_raw_s), raw_z = tc::smem_u32(smem + a.off_raw_z);
+        uint32_t so = 0, zo = 0;
+        for (int k = 0; gv_segment(a, r0, nrows, G, k, sg); ++k) {
+          tc::bulk_load(raw_s + so, sg.sc_lo, sg.sc_bytes, meta_full);
+          so += sg.sc_bytes;
+          if (sg.z_bytes) tc::bulk_load(raw_z + zo, sg.z_lo, sg.z_bytes, meta_full);
+          zo += sg.z_bytes;
+        }
+      }
       int i = 0;
       for (; i < nloads; ++i) {
         const int s = i % S;
@@ -201,43 +300,44 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
         }
         if (*abort_flag) break;
         const int rows_i = min(a.R, nrows - i * a.R);
-        const uint32_t bytes = static_cast<uint32_t>(rows_i * row_bytes);
-        tc::mbar_arrive_expect_tx(full(s), bytes);
-        tc::bulk_load_policy(ring + s * a.stage_bytes, a.wq + static_cast<int64_t>(r0 + i * a.R) * row_bytes, bytes,
-                             full(s), policy);
+        tc::mbar_arrive_expect_tx(full(s), static_cast<uint32_t>(rows_i * row_bytes));
+        // one bulk copy per matrix the stage's rows fall in
+        for (int done = 0; done < rows_i;) {
+          const int r = r0 + i * a.R + done;
+          int first;
+          const int p = gv_matrix(a, r, first);
+          const int seg = min(rows_i - done, a.row_end[p] - r);
+          tc::bulk_load_policy(ring + s * a.stage_bytes + done * row_bytes,
+                               a.wq[p] + static_cast<int64_t>(r - first) * row_bytes,
+                               static_cast<uint32_t>(seg * row_bytes), full(s), policy);
+          done += seg;
+        }
       }
       // The last copy into each stage must have landed before the CTA exits.
       for (int j = max(0, i - S); j < i; ++j) tc::mbar_wait(full(j % S), (j / S) & 1, a.err, kGvSiteDrain);
+      tc::mbar_wait(meta_full, 0, a.err, kGvSiteDrain);
     }
     return;
   }
 
   // ---------------- compute warps ----------------
   const int nct = ncw * 32;
-  // Scales and zero-points of the band: weights, so read before waiting on
-  // the previous kernel.  Loads are issued in batches so that one batch costs
-  // one memory round trip.
+  // Scales and zero-points of the band (weights, so converted before waiting
+  // on the previous kernel) from their raw staging copies into packed pairs.
   {
-    constexpr int kB = 8;
-    const int ne = nrows * G;
-    const __half* sg = a.scales + static_cast<int64_t>(r0) * G;
-    for (int e0 = threadIdx.x; e0 < ne; e0 += kB * nct) {
-      __half sv[kB];
-      uint32_t zv[kB];
-#pragma unroll
-      for (int u = 0; u < kB; ++u) {
-        const int e = e0 + u * nct;
-        zv[u] = 0x88u;
-        if (e < ne) {
-          sv[u] = sg[e];
-          const int r = e / G, g = e - r * G;
-          if (a.zeros) zv[u] = a.zeros[static_cast<int64_t>(r0 + r) * a.zpitch + (g >> 1)] >> ((g & 1) * 4);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kB; ++u) {
-        const int e = e0 + u * nct;
-        if (e < ne) sz[e] = make_float2(__half2float(sv[u]), __int_as_float(static_cast<int>(zv[u] & 0xFu)));
+    bool ok = tc::mbar_wait(meta_full, 0, a.err, kGvSiteFull);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) *abort_flag = 1;
+    const unsigned char* raw_s = smem + a.off_raw_s;
+    const unsigned char* raw_z = smem + a.off_raw_z;
+    GvSeg sg;
+    for (int k = 0; ok && gv_segment(a, r0, nrows, G, k, sg); ++k) {
+      const int ne = sg.rows * G;
+      for (int e = threadIdx.x; e < ne; e += nct) {
+        const int r = e / G, g = e - r * G;
+        const uint32_t sv = *reinterpret_cast<const unsigned short*>(raw_s + sg.sc_off + 2 * e);
+        const uint32_t zv = sg.z_off >= 0 ? (raw_z[sg.z_off + r * a.zpitch + (g >> 1)] >> ((g & 1) * 4)) & 0xFu : 8u;
+        sz[(sg.row0 + r) * G + g] = sv | (zv << 16);
       }
     }
   }
@@ -373,7 +473,7 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
       }
       const int rows_i = min(a.R, nrows - i * a.R);
       float p[kGvRowsPerBatch];
-      gv_batch<NP, B>(ring + s * a.stage_bytes + jc * 16, sz_base + (i * a.R * G) * 8, rows_i, a.RG, rg, row_bytes, G, xp,
+      gv_batch<NP, B>(ring + s * a.stage_bytes + jc * 16, sz_base + (i * a.R * G) * 4, rows_i, a.RG, rg, row_bytes, G, xp,
                    xsum, xzf, sx, p);
       // The stage's codes are in registers: hand it back to the producer.
       __syncwarp();
@@ -395,7 +495,9 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
   for (int r = threadIdx.x; r < nrows; r += nct) {
     float v = 0.0f;
     for (int w = 0; w < a.WPR; ++w) v += red[r * a.WPR + w];
-    a.y[r0 + r] = __float2half_rn(v);
+    int first;
+    const int p = gv_matrix(a, r0 + r, first);
+    a.y[p][r0 + r - first] = __float2half_rn(v);
   }
 }
 
@@ -415,13 +517,20 @@ bool gv_plan(int64_t N, int64_t K, GvArgs& a, int& grid, int& smem) {
   a.R = std::min(gv_rows_per_batch(a.RG) * a.RG, rows_max);
   a.stage_bytes = a.R * row_bytes;
   auto up = [](int v, int m) { return (v + m - 1) / m * m; };
-  const int extras = up(rows_max * G * 8, 16) + up(rows_max * a.WPR * 4, 16) + 16 * kGvMaxStages + 16 + 128;
+  const int zpitch = (G + 1) / 2;
+  // raw staging: the band's bytes plus up to 32 bytes of alignment window per segment
+  const int raw_s_bytes = up(rows_max * G * 2, 16) + 32 * kGvMaxGroup;
+  const int raw_z_bytes = up(rows_max * zpitch, 16) + 32 * kGvMaxGroup;
+  const int extras = up(rows_max * G * 4, 16) + up(rows_max * a.WPR * 4, 16) + raw_s_bytes + raw_z_bytes +
+                     16 * kGvMaxStages + 16 + 128;
   const int loads_max = (rows_max + a.R - 1) / a.R;
   a.S = std::min({kGvMaxStages, (kGvCtaBytes - extras) / a.stage_bytes, loads_max});
   if (a.S < std::min(kGvMinStages, loads_max)) return false;
   a.off_sz = up(a.S * a.stage_bytes, 128);
-  a.off_red = a.off_sz + up(rows_max * G * 8, 16);
-  a.off_bar = a.off_red + up(rows_max * a.WPR * 4, 16);
+  a.off_red = a.off_sz + up(rows_max * G * 4, 16);
+  a.off_raw_s = a.off_red + up(rows_max * a.WPR * 4, 16);
+  a.off_raw_z = a.off_raw_s + raw_s_bytes;
+  a.off_bar = a.off_raw_z + raw_z_bytes;
   smem = a.off_bar + 16 * a.S + 16;
   return true;
 }
@@ -431,22 +540,33 @@ bool gv_plan(int64_t N, int64_t K, GvArgs& a, int& grid, int& smem) {
 bool w4a16_gemv_supported(int64_t T, int64_t N, int64_t K) {
   GvArgs a = {};
   int grid = 0, smem = 0;
-  return T == 1 && gv_plan(N, K, a, grid, smem);
+  return T == 1 && N <= kMaxGemvRows && gv_plan(N, K, a, grid, smem);
 }
 
-cudaError_t launch_w4a16_gemv(const void* x, int64_t N, int64_t K, const uint8_t* wq, const void* scales,
-                              const uint8_t* zeros, void* y, cudaStream_t stream) {
-  if (N == 0) return cudaSuccess;
+cudaError_t launch_w4a16_gemv_grouped(const void* x, int64_t K, int count, const int64_t* N,
+                                      const uint8_t* const* wq, const void* const* scales,
+                                      const uint8_t* const* zeros, void* const* y, cudaStream_t stream) {
+  if (count < 1 || count > kGvMaxGroup) return cudaErrorInvalidValue;
   GvArgs a = {};
+  int64_t total = 0;
+  a.np = 0;
+  for (int p = 0; p < count; ++p) {
+    if (N[p] == 0) continue;  // an empty matrix takes no rows
+    total += N[p];
+    a.wq[a.np] = wq[p];
+    a.scales[a.np] = static_cast<const __half*>(scales[p]);
+    a.zeros[a.np] = zeros[p];
+    a.y[a.np] = static_cast<__half*>(y[p]);
+    a.row_end[a.np] = static_cast<int>(total);
+    ++a.np;
+  }
+  if (total == 0) return cudaSuccess;
+  if (total > kMaxGemvRows) return cudaErrorInvalidValue;
   int grid = 0, smem = 0;
-  if (!gv_plan(N, K, a, grid, smem)) return cudaErrorInvalidValue;
+  if (!gv_plan(total, K, a, grid, smem)) return cudaErrorInvalidValue;
   a.x = static_cast<const __half*>(x);
-  a.wq = wq;
-  a.scales = static_cast<const __half*>(scales);
-  a.zeros = zeros;
-  a.y = static_cast<__half*>(y);
   a.err = device_error_word();
-  a.N = static_cast<int>(N);
+  a.N = static_cast<int>(total);
   a.K = static_cast<int>(K);
   a.zpitch = static_cast<int>((K / 128 + 1) / 2);
   const bool b8 = gv_rows_per_batch(a.RG) == 8;
@@ -464,6 +584,12 @@ cudaError_t launch_w4a16_gemv(const void* x, int64_t N, int64_t K, const uint8_t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return b8 ? cudaLaunchKernelEx(&cfg, w4a16_gemv_kernel<8>, a) : cudaLaunchKernelEx(&cfg, w4a16_gemv_kernel<4>, a);
+}
+
+cudaError_t launch_w4a16_gemv(const void* x, int64_t N, int64_t K, const uint8_t* wq, const void* scales,
+                              const uint8_t* zeros, void* y, cudaStream_t stream) {
+  if (N == 0) return cudaSuccess;
+  return launch_w4a16_gemv_grouped(x, K, 1, &N, &wq, &scales, &zeros, &y, stream);
 }
 
 }  // namespace qlin

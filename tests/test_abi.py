@@ -69,6 +69,16 @@ def test_rejects_bad_arguments_without_gpu(built):
     assert L.qlin_nvfp4_sf_bytes(130, 4224, 0) == 130 * 264
     assert L.qlin_nvfp4_sf_bytes(130, 4208, 1) == -1
     assert L.qlin_nvfp4_gemm(P(16), P(16), P(16), P(16), 4, 8, 96, P(16), P(16), P(16), 1, None) == 1
+    # grouped W4A16: count outside [1, 4], null host arrays, K not a multiple of the group
+    n2 = (ctypes.c_int64 * 2)(16, 16)
+    ptrs = (ctypes.c_void_p * 2)(16, 16)
+    assert L.qlin_w4a16_gemm_grouped(P(16), 1, 256, 0, n2, ptrs, ptrs, ptrs, 128, ptrs, None) == 1
+    assert L.qlin_w4a16_gemm_grouped(P(16), 1, 256, 5, n2, ptrs, ptrs, ptrs, 128, ptrs, None) == 1
+    assert L.qlin_w4a16_gemm_grouped(P(16), 1, 256, 2, None, ptrs, ptrs, ptrs, 128, ptrs, None) == 1
+    assert L.qlin_w4a16_gemm_grouped(P(16), 1, 200, 2, n2, ptrs, ptrs, ptrs, 128, ptrs, None) == 1
+    assert L.qlin_w4a16_gemm_grouped(P(16), 1, 256, 2, n2, ptrs, ptrs, ptrs, 64, ptrs, None) == 3
+    bad = (ctypes.c_void_p * 2)(16, 24)
+    assert L.qlin_w4a16_gemm_grouped(P(16), 1, 256, 2, n2, bad, ptrs, ptrs, 128, ptrs, None) == 2
     # perm K limit
     assert L.qlin_arc_perm(P(16), 0, 4, 32768, P(16), None) == 1
     msg = L.qlin_last_error_message()
@@ -79,6 +89,9 @@ def test_empty_problems_launch_nothing(built):
     L = built
     P = ctypes.c_void_p
     assert L.qlin_w4a16_gemm(None, 0, 16, 256, None, None, None, 128, None, None) == 0
+    n0 = (ctypes.c_int64 * 2)(0, 0)
+    nul = (ctypes.c_void_p * 2)(None, None)
+    assert L.qlin_w4a16_gemm_grouped(None, 1, 256, 2, n0, nul, nul, nul, 128, nul, None) == 0
     assert L.qlin_quant_act_int8(None, 0, 0, 64, None, None, None, None) == 0
     assert L.qlin_w8a8_gemm(None, None, 0, 8, 64, None, 1, None, 1, None, None, None, 0, None, 0, None) == 0
     assert L.qlin_nvfp4_gemm(None, None, None, None, 4, 0, 64, None, None, None, 1, None) == 0

@@ -114,6 +114,35 @@ def test_quant_nvfp4_edge_values(qlin_gpu):
         assert np.array_equal(gq, oracle.pack_u4(rq)), g
 
 
+@pytest.mark.parametrize("g", [1e-12, 1e-40, 5e-39, 1e20, 3e38])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_quant_nvfp4_extreme_global_scale(qlin_gpu, g, mode):
+    """Per-tensor scales far from the tensor's own: block scales saturating at
+    448 with element quotients that overflow float32 (g = 1e-12 against
+    values near 1e30), subnormal g and subnormal block divisors, and huge g
+    that sends block scales to zero or to the subnormal E4M3 range.  Every
+    code must still equal the one true float32 division gives."""
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((9, 512)).astype(np.float32)
+    x[0] *= np.float32(1e30)
+    x[1] *= np.float32(1e-30)
+    x[2] *= np.float32(3e37)
+    x[3, :16] = 0.0
+    x[3, 16] = -0.0
+    x[4] *= np.float32(1e-39)
+    xt = torch.from_numpy(x).cuda()
+    g32 = np.float32(g)
+    perm = oracle.arc_perm(x)
+    gq, gsf = _quant(qlin_gpu, xt, torch.tensor([g32]).cuda(), torch.from_numpy(perm).cuda(), 64, mode)
+    with np.errstate(over="ignore", divide="ignore", invalid="ignore", under="ignore"):
+        if mode == 0:
+            rq, rsf = oracle.arc_quantize_activation(x, perm, 64, g32)
+        else:
+            rq, rsf = oracle.arc_quantize_weight(x, perm, 64, g32)
+    assert np.array_equal(gsf, rsf)
+    assert np.array_equal(gq, oracle.pack_u4(rq))
+
+
 def test_config5_activation_and_weight(qlin_gpu):
     d = inputs.nvfp4_arc(seed=4)
     S = d["S"]

@@ -146,3 +146,92 @@ def test_decode_chain_ping_pong(qlin_gpu, T):
     for (c, s, z) in layers:
         ref = oracle.w4a16_reference(ref, c, s, z).astype(np.float16)
     assert_within_tolerance(y, ref.astype(np.float64), "W4A16 chain T=%d" % T)
+
+
+def _quantized(seed, n, k):
+    d = inputs.w4a16_decode(seed=seed, T=1, N=n, K=k)
+    codes, s16, z = oracle.quant_w4_g128(d["w"])
+    return codes, s16, z
+
+
+@pytest.mark.parametrize("T,shapes", [(1, ((4096, 4096), (1024, 4096), (1024, 4096))),
+                                      (1, ((763, 1408), (8, 1408), (5, 1408), (1000, 1408))),
+                                      (1, ((0, 512), (300, 512), (1, 512))),
+                                      (4, ((256, 1024), (100, 1024)))])
+def test_grouped_equals_separate(qlin_gpu, T, shapes):
+    """One grouped call over matrices of different heights (a GQA-like q/k/v
+    set, ragged heights whose boundaries fall inside a shared-memory stage,
+    an empty matrix) gives every output bit for bit equal to a separate
+    qlin_w4a16_gemm call, and within tolerance of the oracle; one matrix is
+    symmetric (no zero-points)."""
+    k = shapes[0][1]
+    x = inputs.w4a16_decode(seed=60, T=T, N=8, K=k)["x"]
+    xt = _dev(x)
+    mats = [_quantized(61 + i, n, k) for i, (n, _) in enumerate(shapes)]
+    wqs = [_dev(oracle.pack_u4(c)) for (c, _, _) in mats]
+    scs = [_dev(s) for (_, s, _) in mats]
+    zps = [_dev(oracle.pack_u4(z)) for (_, _, z) in mats]
+    zps[-1] = None
+    ys = [torch.empty((T, n), dtype=torch.float16, device="cuda") for (n, _) in shapes]
+    qlin_gpu.qlin_w4a16_gemm_grouped(xt, wqs, scs, zps, ys)
+    torch.cuda.synchronize()
+    assert qlin_gpu.qlin_get_device_error() == 0
+    for i, (n, _) in enumerate(shapes):
+        if n == 0:
+            continue
+        sep = torch.empty((T, n), dtype=torch.float16, device="cuda")
+        qlin_gpu.qlin_w4a16_gemm(xt, wqs[i], scs[i], zps[i], sep)
+        torch.cuda.synchronize()
+        assert torch.equal(ys[i], sep), "matrix %d" % i
+        codes, s16, z = mats[i]
+        if zps[i] is None:
+            z = np.full_like(z, 8)
+        ref = oracle.w4a16_reference(x, codes, s16, z)
+        assert_within_tolerance(ys[i].cpu().numpy(), ref, "grouped matrix %d (N=%d)" % (i, n))
+
+
+def test_grouped_decoder_block_chain(qlin_gpu):
+    """Two decoder blocks at decode (T = 1) with the block's dependency
+    structure: q, k, v in one grouped call on h; o on v; gate and up in one
+    grouped call on o's output; down on up; the next block starts from down's
+    output.  The kernels overlap through programmatic dependent launch; the
+    oracle runs the same chain, rounding every output to fp16."""
+    hid, inter = 1024, 2816
+    blocks = []
+    seed = 80
+    for _ in range(2):
+        blk = {}
+        for name, (n, k) in (("q", (hid, hid)), ("k", (hid, hid)), ("v", (hid, hid)), ("o", (hid, hid)),
+                             ("gate", (inter, hid)), ("up", (inter, hid)), ("down", (hid, inter))):
+            blk[name] = _quantized(seed, n, k)
+            seed += 1
+        blocks.append(blk)
+    x0 = inputs.w4a16_decode(seed=79, T=1, N=8, K=hid)["x"]
+    dev = [{n: (_dev(oracle.pack_u4(c)), _dev(s), _dev(oracle.pack_u4(z))) for n, (c, s, z) in b.items()}
+           for b in blocks]
+    h = _dev(x0)
+    out = {}
+    for b in dev:
+        out = {n: torch.empty((1, b[n][0].shape[0]), dtype=torch.float16, device="cuda") for n in b}
+        qlin_gpu.qlin_w4a16_gemm_grouped(h, [b[n][0] for n in "qkv"], [b[n][1] for n in "qkv"],
+                                         [b[n][2] for n in "qkv"], [out[n] for n in "qkv"])
+        qlin_gpu.qlin_w4a16_gemm(out["v"], *b["o"], out["o"])
+        qlin_gpu.qlin_w4a16_gemm_grouped(out["o"], [b[n][0] for n in ("gate", "up")], [b[n][1] for n in ("gate", "up")],
+                                         [b[n][2] for n in ("gate", "up")], [out[n] for n in ("gate", "up")])
+        qlin_gpu.qlin_w4a16_gemm(out["up"], *b["down"], out["down"])
+        h = out["down"]
+    torch.cuda.synchronize()
+    assert qlin_gpu.qlin_get_device_error() == 0
+    ref = x0
+    refs = {}
+    for blk in blocks:
+        refs = {}
+        for n in "qkv":
+            refs[n] = oracle.w4a16_reference(ref, *blk[n]).astype(np.float16)
+        refs["o"] = oracle.w4a16_reference(refs["v"], *blk["o"]).astype(np.float16)
+        for n in ("gate", "up"):
+            refs[n] = oracle.w4a16_reference(refs["o"], *blk[n]).astype(np.float16)
+        refs["down"] = oracle.w4a16_reference(refs["up"], *blk["down"]).astype(np.float16)
+        ref = refs["down"]
+    for n in ("q", "k", "gate", "down"):
+        assert_within_tolerance(out[n].cpu().numpy(), refs[n].astype(np.float64), "block chain %s" % n)
