@@ -127,7 +127,7 @@ class Workload:
     """Device-resident inputs, weights and outputs of one step, and the three
     captured phases."""
 
-    def __init__(self, q, torch, layers):
+    def __init__(self, q, torch, layers, w4_path="launches"):
         from quantized_linear_layer_gb300 import inputs
         self.q, self.torch = q, torch
         dev = torch.device("cuda")
@@ -192,18 +192,37 @@ class Workload:
         self.nv_sfx = torch.empty(q.qlin_nvfp4_sf_bytes(T, K + S, q.QLIN_SF_MMA), dtype=torch.uint8, device=dev)
         self.nv_out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
         torch.cuda.synchronize()
-        self.launches = {"w4a16": 4 * layers, "w8a8": 2, "nvfp4": 2}
+        self.w4_path = w4_path
+        self.w4_seq_steps = self.w4a16_steps()
+        self.w4_ws = torch.zeros(q.qlin_w4a16_sequence_workspace_bytes(len(self.w4_seq_steps)), dtype=torch.uint8,
+                                 device=dev)
+        # kernel launches per phase (the sequence: a workspace memset and one launch per 128 steps)
+        n_seq = (len(self.w4_seq_steps) + 127) // 128
+        self.launches = {"w4a16": n_seq if w4_path == "sequence" else 4 * layers, "w8a8": 2, "nvfp4": 2}
 
     # the three phases, as plain launch sequences on the current stream
-    def phase_w4a16(self):
-        gemm, grouped = self.q.qlin_w4a16_gemm, self.q.qlin_w4a16_gemm_grouped
+    def w4a16_steps(self):
+        """The decode stack as steps with the block's dependencies."""
+        steps = []
         per_block = len(LLAMA_BLOCK)
         for b0 in range(0, len(self.w4), per_block):
             q, k, v, o, gate, up, down = self.w4[b0:b0 + per_block]
-            grouped(self.w4_in, [q[2], k[2], v[2]], [q[3], k[3], v[3]], [q[4], k[4], v[4]], self.w4_qkv)
-            gemm(self.w4_qkv[2], *o[2:], self.w4_o)
-            grouped(self.w4_o, [gate[2], up[2]], [gate[3], up[3]], [gate[4], up[4]], [self.w4_gate, self.w4_up])
-            gemm(self.w4_up, *down[2:], self.w4_out)
+            steps.append((self.w4_in, [q[2], k[2], v[2]], [q[3], k[3], v[3]], [q[4], k[4], v[4]], self.w4_qkv))
+            steps.append((self.w4_qkv[2], [o[2]], [o[3]], [o[4]], [self.w4_o]))
+            steps.append((self.w4_o, [gate[2], up[2]], [gate[3], up[3]], [gate[4], up[4]], [self.w4_gate, self.w4_up]))
+            steps.append((self.w4_up, [down[2]], [down[3]], [down[4]], [self.w4_out]))
+        return steps
+
+    def phase_w4a16(self):
+        if self.w4_path == "sequence":
+            # one persistent launch for the whole stack
+            self.q.qlin_w4a16_gemv_sequence(self.w4_seq_steps, self.w4_ws)
+            return
+        for (x, wqs, scs, zps, ys) in self.w4_seq_steps:
+            if len(wqs) == 1:
+                self.q.qlin_w4a16_gemm(x, wqs[0], scs[0], zps[0], ys[0])
+            else:
+                self.q.qlin_w4a16_gemm_grouped(x, wqs, scs, zps, ys)
 
     def phase_w8a8(self):
         self.q.qlin_quant_act_int8(self.w8_x, self.w8_a, self.w8_sa)
@@ -365,7 +384,7 @@ def run_ours(args):
     q.build()
     q.lib()
     peaks = load_peaks()
-    wl = Workload(q, torch, args.layers)
+    wl = Workload(q, torch, args.layers, args.w4a16_path)
     wl.capture()
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
@@ -407,8 +426,11 @@ def run_ours(args):
         "config": {
             "workload": "W4A16 T=1 decode over a Llama-2-7B-shaped linear stack (%d blocks x 7 layers with the "
                         "block's dependencies: q,k,v grouped on the block input, o on v, gate,up grouped on o, "
-                        "down on up; 4 launches per block) + "
-                        "W8A8 sym+bias T=2048 K=4096 N=4096 + NVFP4 ARCQuant T=2048 K=4096 N=4096 S=128" % args.layers,
+                        "down on up; 4 steps per block, %s) + "
+                        "W8A8 sym+bias T=2048 K=4096 N=4096 + NVFP4 ARCQuant T=2048 K=4096 N=4096 S=128" %
+                        (args.layers, "one persistent launch per 128 steps" if args.w4a16_path == "sequence"
+                         else "one launch per step"),
+            "w4a16_path": args.w4a16_path,
             "w4a16_launches_per_step": wl.launches["w4a16"],
             "w4a16_layers_per_step": len(wl.w4),
             "w4a16_weight_bytes_per_step": wl.w4_bytes,
@@ -425,7 +447,8 @@ def run_ours(args):
                       "frac_of_fp4_tensor_peak": round(nv_ops / tnv / 1e12 / (peak16 * 6.0), 4)},
         },
         "roofline": {
-            "kernel": "w4a16_gemv_kernel (fused dequant GEMV, T=1)",
+            "kernel": ("w4a16_seq_kernel (persistent fused dequant GEMV sequence, T=1)" if args.w4a16_path == "sequence"
+                       else "w4a16_gemv_kernel (fused dequant GEMV, T=1)"),
             "bound": "hbm",
             "achieved": round(per_launch_bytes / per_launch_s / 1e9, 1),
             "peak": peaks["hbm_gbs"],
@@ -496,6 +519,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=32, help="transformer blocks in the W4A16 decode stack")
+    ap.add_argument("--w4a16-path", choices=["sequence", "launches"], default="launches",
+                    help="decode stack as one launch per step (grouped where layers share an input), or as one "
+                         "persistent launch")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="length of the bounded oracle sample")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps

@@ -173,6 +173,58 @@ qlin_status qlin_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int cou
                                     cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * a1, sequence - a chain of W4A16 decode steps in one persistent launch
+ *
+ * Runs steps[0], steps[1], ... in order at T = 1, each step a grouped W4A16
+ * linear (as qlin_w4a16_gemm_grouped) whose input may be an output of any
+ * earlier step: the layers of a decoder at decode time.  One cooperative
+ * launch keeps exactly one CTA on every SM; each CTA streams its share of
+ * every step's weights into shared memory ahead of time, and a grid-wide
+ * barrier in global memory separates the steps.  Every output equals the one
+ * qlin_w4a16_gemm gives for the same step bit for bit.
+ *   steps      host array [nsteps] (read during the call only):
+ *                x        fp16 [K] device pointer, the step's input
+ *                K        a multiple of 128, at most 12288
+ *                count    1 .. QLIN_W4A16_MAX_GROUP matrices reading x
+ *                N[p], wq[p], scales[p], zeros[p], y[p]
+ *                         as in qlin_w4a16_gemm_grouped; a step's outputs
+ *                         must not overlap its own x or one another (the
+ *                         barrier between steps orders everything else: a
+ *                         later step may overwrite what an earlier one read
+ *                         or wrote)
+ *   workspace  device memory of qlin_w4a16_sequence_workspace_bytes(nsteps)
+ *              bytes, 4-byte aligned, owned by the caller (the grid
+ *              barrier's counters); it must not be used by another
+ *              sequence call in flight at the same time
+ * The call enqueues a memset of the workspace and one launch per 128 steps
+ * on `stream`.  Returns QLIN_ERR_UNSUPPORTED when the device cannot hold one
+ * CTA per SM for the launch.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  const void* x;
+  int64_t K;
+  int count;
+  int64_t N[QLIN_W4A16_MAX_GROUP];
+  const uint8_t* wq[QLIN_W4A16_MAX_GROUP];
+  const void* scales[QLIN_W4A16_MAX_GROUP];
+  const uint8_t* zeros[QLIN_W4A16_MAX_GROUP];
+  void* y[QLIN_W4A16_MAX_GROUP];
+} qlin_w4a16_step;
+
+int64_t qlin_w4a16_sequence_workspace_bytes(int64_t nsteps);
+qlin_status qlin_w4a16_gemv_sequence(const qlin_w4a16_step* steps, int nsteps, int64_t group, void* workspace,
+                                     cudaStream_t stream);
+
+/* The same without a caller workspace: the barrier counters live in a
+   static device array of the library (no allocation by the caller or the
+   library).  Only one such call may be in flight on a device at a time:
+   calls on one stream are safe; calls on concurrent streams, or in CUDA
+   graphs replayed concurrently, must use qlin_w4a16_gemv_sequence with their
+   own workspaces. */
+qlin_status qlin_w4a16_gemv_sequence_noalloc(const qlin_w4a16_step* steps, int nsteps, int64_t group,
+                                             cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * b1 - per-token int8 activation quantization
  *
  * Symmetric (azp == NULL): s_t = max_k |x| / 127 (s_t = 1 for an all-zero

@@ -20,7 +20,9 @@ __all__ = [
     "QLIN_F16", "QLIN_BF16", "QLIN_F32", "QLIN_I32", "QLIN_NVFP4_RESIDUAL", "QLIN_NVFP4_DUPLICATE",
     "QLIN_SF_ROWS", "QLIN_SF_MMA", "qlin_nvfp4_sf_bytes", "qlin_nvfp4_sf_to_mma",
     "qlin_version", "qlin_get_device_error",
-    "qlin_quant_w4_g128", "qlin_w4a16_gemm", "qlin_w4a16_gemm_grouped", "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm",
+    "qlin_quant_w4_g128", "qlin_w4a16_gemm", "qlin_w4a16_gemm_grouped", "qlin_w4a16_step",
+    "qlin_w4a16_sequence_workspace_bytes", "qlin_w4a16_gemv_sequence", "qlin_w4a16_gemv_sequence_noalloc",
+    "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm",
     "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
 ]
 
@@ -49,6 +51,9 @@ _SIGS = {
     "qlin_quant_w4_g128": ([_P, _I32, _I64, _I64, _I64, _P, _P, _P, _P], _I32),
     "qlin_w4a16_gemm": ([_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P], _I32),
     "qlin_w4a16_gemm_grouped": ([_P, _I64, _I64, _I32, _P, _P, _P, _P, _I64, _P, _P], _I32),
+    "qlin_w4a16_sequence_workspace_bytes": ([_I64], _I64),
+    "qlin_w4a16_gemv_sequence": ([_P, _I32, _I64, _P, _P], _I32),
+    "qlin_w4a16_gemv_sequence_noalloc": ([_P, _I32, _I64, _P], _I32),
     "qlin_quant_act_int8": ([_P, _I32, _I64, _I64, _P, _P, _P, _P], _I32),
     "qlin_int8_row_sum": ([_P, _I64, _I64, _P, _P], _I32),
     "qlin_w8a8_gemm": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
@@ -169,6 +174,66 @@ def qlin_w4a16_gemm_grouped(x, wqs, scales, zeros, ys, group=128, stream=None):
     y_arr = (ctypes.c_void_p * count)(*[y.data_ptr() for y in ys])
     _check("qlin_w4a16_gemm_grouped", lib().qlin_w4a16_gemm_grouped(
         _ptr(x), t, k, count, n_arr, wq_arr, s_arr, z_arr, group, y_arr, _stream(stream)))
+
+
+_MAXG = 4  # QLIN_W4A16_MAX_GROUP
+
+
+class qlin_w4a16_step(ctypes.Structure):
+    """One step of qlin_w4a16_gemv_sequence (the C struct of the same name)."""
+    _fields_ = [("x", ctypes.c_void_p), ("K", ctypes.c_int64), ("count", ctypes.c_int),
+                ("N", ctypes.c_int64 * _MAXG), ("wq", ctypes.c_void_p * _MAXG), ("scales", ctypes.c_void_p * _MAXG),
+                ("zeros", ctypes.c_void_p * _MAXG), ("y", ctypes.c_void_p * _MAXG)]
+
+
+def qlin_w4a16_sequence_workspace_bytes(nsteps):
+    return lib().qlin_w4a16_sequence_workspace_bytes(nsteps)
+
+
+def _w4a16_steps(steps):
+    torch = _torch()
+    arr = (qlin_w4a16_step * max(1, len(steps)))()
+    for i, (x, wqs, scales, zeros, ys) in enumerate(steps):
+        _need(x, torch.float16, name="x")
+        count = len(wqs)
+        if not (1 <= count <= _MAXG and len(scales) == len(zeros) == len(ys) == count):
+            raise ValueError("step %d: 1..%d matrices with matching lists expected" % (i, _MAXG))
+        st = arr[i]
+        st.x = x.data_ptr()
+        st.K = x.shape[-1]
+        st.count = count
+        for p in range(count):
+            _need(wqs[p], torch.uint8, name="wq"); _need(scales[p], torch.float16, name="scales")
+            _need(zeros[p], torch.uint8, name="zeros"); _need(ys[p], torch.float16, name="y")
+            st.N[p] = wqs[p].shape[0]
+            st.wq[p] = wqs[p].data_ptr()
+            st.scales[p] = scales[p].data_ptr()
+            st.zeros[p] = 0 if zeros[p] is None else zeros[p].data_ptr()
+            st.y[p] = ys[p].data_ptr()
+    return arr
+
+
+def qlin_w4a16_gemv_sequence(steps, workspace, group=128, stream=None):
+    """Run decode steps in order in one persistent launch (T = 1).
+
+    steps: list of (x, wqs, scales, zeros, ys) with x fp16 [1][K] (or [K]) and per-matrix lists as in
+    qlin_w4a16_gemm_grouped; workspace: uint8 CUDA tensor of qlin_w4a16_sequence_workspace_bytes(len(steps))
+    bytes or more."""
+    torch = _torch()
+    _need(workspace, torch.uint8, name="workspace")
+    arr = _w4a16_steps(steps)
+    need = qlin_w4a16_sequence_workspace_bytes(len(steps))
+    if workspace.numel() < need:
+        raise ValueError("workspace has %d bytes, %d needed" % (workspace.numel(), need))
+    _check("qlin_w4a16_gemv_sequence", lib().qlin_w4a16_gemv_sequence(
+        ctypes.cast(arr, ctypes.c_void_p), len(steps), group, _ptr(workspace), _stream(stream)))
+
+
+def qlin_w4a16_gemv_sequence_noalloc(steps, group=128, stream=None):
+    """qlin_w4a16_gemv_sequence with the library's own barrier counters (one call in flight per device)."""
+    arr = _w4a16_steps(steps)
+    _check("qlin_w4a16_gemv_sequence_noalloc", lib().qlin_w4a16_gemv_sequence_noalloc(
+        ctypes.cast(arr, ctypes.c_void_p), len(steps), group, _stream(stream)))
 
 
 def qlin_quant_act_int8(x, q, scale, azp=None, stream=None):

@@ -219,6 +219,54 @@ qlin_status qlin_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int cou
   QLIN_LAUNCH(launch_w4a16_gemm_grouped(x, T, K, count, N, wq, scales, zeros, y, stream), "w4a16_gemm_grouped launch");
 }
 
+int64_t qlin_w4a16_sequence_workspace_bytes(int64_t nsteps) {
+  return nsteps < 0 ? -1 : w4a16_sequence_workspace_bytes(nsteps);
+}
+
+qlin_status qlin_w4a16_gemv_sequence(const qlin_w4a16_step* steps, int nsteps, int64_t group, void* workspace,
+                                     cudaStream_t stream) {
+  QLIN_REQUIRE(group == 128, QLIN_ERR_UNSUPPORTED, "group size %lld (only 128 is built)", (long long)group);
+  QLIN_REQUIRE(nsteps >= 0, QLIN_ERR_INVALID_ARG, "nsteps=%d", nsteps);
+  if (nsteps == 0) return ok();
+  QLIN_REQUIRE(steps != nullptr, QLIN_ERR_INVALID_ARG, "null steps");
+  QLIN_REQUIRE(workspace != nullptr, QLIN_ERR_INVALID_ARG, "null workspace");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 3u) == 0, QLIN_ERR_ALIGNMENT, "workspace must be 4-byte aligned");
+  for (int s = 0; s < nsteps; ++s) {
+    const qlin_w4a16_step& st = steps[s];
+    QLIN_REQUIRE(st.count >= 1 && st.count <= QLIN_W4A16_MAX_GROUP, QLIN_ERR_INVALID_ARG,
+                 "step %d: count=%d outside [1, %d]", s, st.count, QLIN_W4A16_MAX_GROUP);
+    QLIN_REQUIRE(st.K > 0 && st.K % group == 0, QLIN_ERR_INVALID_ARG, "step %d: K=%lld is not a positive multiple of %lld",
+                 s, (long long)st.K, (long long)group);
+    QLIN_REQUIRE(w4a16_sequence_supported(st.K), QLIN_ERR_UNSUPPORTED, "step %d: K=%lld above 12288", s,
+                 (long long)st.K);
+    QLIN_REQUIRE(st.x && aligned16(st.x), st.x ? QLIN_ERR_ALIGNMENT : QLIN_ERR_INVALID_ARG,
+                 "step %d: x must be non-null and 16-byte aligned", s);
+    for (int p = 0; p < st.count; ++p) {
+      QLIN_REQUIRE(st.N[p] >= 0 && st.N[p] < (int64_t(1) << 30), QLIN_ERR_INVALID_ARG, "step %d: bad N[%d]=%lld", s, p,
+                   (long long)st.N[p]);
+      if (st.N[p] == 0) continue;
+      QLIN_REQUIRE(st.wq[p] && st.scales[p] && st.y[p], QLIN_ERR_INVALID_ARG, "step %d: null pointer for matrix %d", s, p);
+      QLIN_REQUIRE(aligned16(st.wq[p]), QLIN_ERR_ALIGNMENT, "step %d: wq[%d] must be 16-byte aligned", s, p);
+      QLIN_REQUIRE((reinterpret_cast<uintptr_t>(st.scales[p]) & 1u) == 0 && (reinterpret_cast<uintptr_t>(st.y[p]) & 1u) == 0,
+                   QLIN_ERR_ALIGNMENT, "step %d: scales[%d] and y[%d] must be 2-byte aligned", s, p, p);
+    }
+  }
+  QLIN_DEVICE();
+  const cudaError_t e = launch_w4a16_sequence(steps, nsteps, static_cast<unsigned int*>(workspace), stream);
+  if (e == cudaErrorInvalidValue || e == cudaErrorCooperativeLaunchTooLarge)
+    return fail(QLIN_ERR_UNSUPPORTED, "no launch plan with one CTA per SM for this sequence (%s)", cudaGetErrorString(e));
+  QLIN_LAUNCH(e, "w4a16_gemv_sequence launch");
+}
+
+qlin_status qlin_w4a16_gemv_sequence_noalloc(const qlin_w4a16_step* steps, int nsteps, int64_t group,
+                                             cudaStream_t stream) {
+  if (nsteps == 0) return qlin_w4a16_gemv_sequence(steps, nsteps, group, reinterpret_cast<void*>(16), stream);
+  QLIN_DEVICE();
+  unsigned int* ws = w4a16_sequence_static_workspace();
+  QLIN_REQUIRE(ws != nullptr, QLIN_ERR_CUDA, "device counters unavailable");
+  return qlin_w4a16_gemv_sequence(steps, nsteps, group, ws, stream);
+}
+
 qlin_status qlin_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
                                 float* scale, int32_t* azp, cudaStream_t stream) {
   QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");

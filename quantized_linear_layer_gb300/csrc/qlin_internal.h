@@ -33,6 +33,16 @@ cudaError_t launch_w4a16_gemv(const void* x, int64_t N, int64_t K, const uint8_t
 cudaError_t launch_w4a16_gemv_grouped(const void* x, int64_t K, int count, const int64_t* N,
                                       const uint8_t* const* wq, const void* const* scales,
                                       const uint8_t* const* zeros, void* const* y, cudaStream_t stream);
+using W4A16SeqStep = qlin_w4a16_step;
+int64_t w4a16_sequence_workspace_bytes(int64_t nsteps);
+bool w4a16_sequence_supported(int64_t K);
+// The steps in order in persistent cooperative launches (up to 128 steps
+// each); workspace holds one arrival counter per step.
+cudaError_t launch_w4a16_sequence(const W4A16SeqStep* steps, int nsteps, unsigned int* workspace,
+                                  cudaStream_t stream);
+// Device address of the library's own counters (enough for every launch of
+// a sequence: each launch takes at most 128 steps and zeroes them first).
+unsigned int* w4a16_sequence_static_workspace();
 cudaError_t launch_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
                                       const uint8_t* const* wq, const void* const* scales,
                                       const uint8_t* const* zeros, void* const* y, cudaStream_t stream);

@@ -79,6 +79,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
   return true;
 }
 
+// Bounded wait that sleeps `ns` nanoseconds between polls: for threads with
+// nothing else to do (a producer waiting for a free slot), so that they do
+// not take issue slots from the warps that compute.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, int32_t* err, int site, unsigned ns) {
+  if (mbar_test(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_test(bar, parity)) {
+    __nanosleep(ns);
+    if (clock64() - t0 > kWaitTimeoutCycles) {
+      record_device_error(err, kDevErrTimeoutBase + site);
+      return false;
+    }
+  }
+  return true;
+}
+
 // 2-D TMA tile load into shared memory, completing `bytes` on the mbarrier.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(

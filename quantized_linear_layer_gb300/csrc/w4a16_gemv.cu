@@ -52,9 +52,12 @@
 #include "device_common.cuh"
 #include "qlin_internal.h"
 #include "tc_common.cuh"
+#include "w4a16_gemv_common.cuh"
 
 namespace qlin {
 namespace {
+
+using namespace gv;
 
 constexpr int kGvMaxWarpsPerRow = 12;       // K <= 12 * 32 * 32 = 12288
 constexpr int kGvMaxComputeWarps = 12;
@@ -81,91 +84,6 @@ struct GvArgs {
   int R, S, stage_bytes;       // rows per stage, stages
   int off_sz, off_red, off_raw_s, off_raw_z, off_bar;
 };
-
-// d = c + sum_i a.byte[i] . b.byte[i], a unsigned bytes, b signed bytes.
-__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
-  int d;
-  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-// sum_k (n[k] - z) . x_fix[k] over one 32-code chunk (16 bytes).
-// xp[p][2w] / xp[p][2w + 1] hold byte plane p of the even / odd codes of
-// word w.  The even codes are masked to bytes in place (w & 0x0F0F0F0F); the
-// odd ones stay in the high nibble of their byte (w & 0xF0F0F0F0 = 16 n) and
-// get their own accumulators, whose factor 16 is divided out in the fp32
-// combination.  Every partial sum is an exact integer below 2^20.
-//   NP = 2: the two high planes; the zero-point term z . sum(x_fix) (xzf,
-//           rounded to fp32) is subtracted in fp32.
-//   NP = 3: all three planes, the zero-point term subtracted per plane in
-//           int32 (exact), for chunks with activation outliers.
-template <int NP>
-__device__ __forceinline__ float gv_chunk(uint4 q, const uint32_t (*xp)[8], const int* xsum, float xzf, int z) {
-  int he = 0, ho = 0, me = 0, mo = 0, le = 0, lo = 0;
-  const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const uint32_t ev = wd[w] & 0x0F0F0F0Fu, od = wd[w] & 0xF0F0F0F0u;
-    he = dp4a_us(ev, xp[0][2 * w], he);
-    ho = dp4a_us(od, xp[0][2 * w + 1], ho);
-    me = dp4a_us(ev, xp[1][2 * w], me);
-    mo = dp4a_us(od, xp[1][2 * w + 1], mo);
-    if (NP == 3) {
-      le = dp4a_us(ev, xp[2][2 * w], le);
-      lo = dp4a_us(od, xp[2][2 * w + 1], lo);
-    }
-  }
-  if (NP == 2) {
-    const float d = fmaf(static_cast<float>(he), 65536.0f,
-                         fmaf(static_cast<float>(ho), 4096.0f,
-                              fmaf(static_cast<float>(me), 256.0f, static_cast<float>(mo) * 16.0f)));
-    return fmaf(-static_cast<float>(z), xzf, d);
-  } else {
-    // (odd sums are multiples of 16: the shifts are exact)
-    const int h = he + (ho >> 4) - z * xsum[0];
-    const int m = me + (mo >> 4) - z * xsum[1];
-    const int l = le + (lo >> 4) - z * xsum[2];
-    return fmaf(static_cast<float>(h), 65536.0f, fmaf(static_cast<float>(m), 256.0f, static_cast<float>(l)));
-  }
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
-// Rows rg, rg + RG, rg + 2 RG, rg + 3 RG of one stage: the thread's partial
-// sums.  Row indices past the stage are clamped to its last row (their sums
-// are never stored), so the four chunks run without branches and interleave;
-// idle lanes have zero activations and contribute 0.  Addresses are 32-bit
-// shared-window offsets: cbase = the thread's chunk in the stage, sbase = its
-// group's packed {scale, zero} of the stage's first row (fp16 scale bits in
-// the low half, the zero-point in the high half).
-template <int NP, int B>
-__device__ __forceinline__ void gv_batch(uint32_t cbase, uint32_t sbase, int rows_i, int RG, int rg, int row_bytes,
-                                         int G, const uint32_t (*xp)[8], const int* xsum, float xzf, float sx,
-                                         float* p) {
-  uint4 q[B];
-  uint32_t m[B];
-#pragma unroll
-  for (int b = 0; b < B; ++b) {
-    const int rrc = min(rg + RG * b, rows_i - 1);
-    q[b] = lds128(cbase + rrc * row_bytes);
-    m[b] = lds32(sbase + rrc * G * 4);
-  }
-#pragma unroll
-  for (int b = 0; b < B; ++b) {
-    const float sg = __half2float(__ushort_as_half(static_cast<unsigned short>(m[b] & 0xFFFFu)));
-    p[b] = (sg * sx) * gv_chunk<NP>(q[b], xp, xsum, xzf, static_cast<int>(m[b] >> 16));
-  }
-}
 
 // Matrix of launch row r, and the first launch row of that matrix.
 __device__ __forceinline__ int gv_matrix(const GvArgs& a, int r, int& first) {
@@ -233,9 +151,6 @@ __device__ __forceinline__ bool gv_segment(const GvArgs& a, int r0, int nrows, i
   return false;
 }
 
-__device__ __forceinline__ void named_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
 
 // B rows of each stage per warp and row group (a power of two).
 template <int B>
@@ -294,7 +209,7 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
       int i = 0;
       for (; i < nloads; ++i) {
         const int s = i % S;
-        if (i >= S && !tc::mbar_wait(empty(s), ((i / S) - 1) & 1, a.err, kGvSiteEmpty)) {
+        if (i >= S && !tc::mbar_wait_sleep(empty(s), ((i / S) - 1) & 1, a.err, kGvSiteEmpty, 128)) {
           *abort_flag = 1;
           break;
         }
@@ -352,76 +267,11 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
   // L1 line filled while the previous kernel was still running could be stale.
   if (warp == 0) pdl_wait();
   named_sync(1, nct);
-  uint32_t xp[3][8];         // byte planes hi, mid, lo
-  int xsum[3] = {0, 0, 0};   // plane sums over the chunk
-  float sx = 1.0f;           // x = x_fix . sx
-  float xf[32];
-  float amax = 0.0f, asum = 0.0f;
-  if (act) {
-    const uint4* xg = reinterpret_cast<const uint4*>(a.x + j * 32);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const uint4 u = ldg_cg_v4(xg + w);
-      const __half2* h = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float2 f = __half22float2(h[t]);
-        xf[8 * w + 2 * t] = f.x;
-        xf[8 * w + 2 * t + 1] = f.y;
-      }
-    }
-    // four partial maxima / sums (short dependency chains)
-    float pm[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const float ax = fabsf(xf[t]);
-      pm[t & 3] = fmaxf(pm[t & 3], ax);
-      ps[t & 3] += ax;
-    }
-    amax = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
-    asum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-  }
-  // The low plane is built only in warps holding a chunk with an outlier.
-  const bool wide_warp = __any_sync(0xffffffffu, act && amax > (64.0f / 31.0f) * (asum - amax));
-  if (act) {
-    sx = amax > 0.0f ? amax * (1.0f / 4161536.0f) : 1.0f;   // 4161536 = 127 . 2^15
-    const float inv = 1.0f / sx;
-    // x_fix + 0x8080: byte 0 ^ 0x80 = lo, byte 1 ^ 0x80 = mid, byte 2 = hi.
-    // x . inv + 1.5 . 2^23 rounds x . inv to an integer (|x . inv| < 2^22).
-    uint32_t vb[32];
-#pragma unroll
-    for (int t = 0; t < 32; ++t) vb[t] = __float_as_uint(fmaf(xf[t], inv, 12582912.0f)) - 0x4B400000u + 0x8080u;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-#pragma unroll
-      for (int par = 0; par < 2; ++par) {
-        const int e = 8 * w + par;  // elements e, e + 2, e + 4, e + 6
-        const uint32_t hi01 = __byte_perm(vb[e], vb[e + 2], 0x0062), hi23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0062);
-        const uint32_t md01 = __byte_perm(vb[e], vb[e + 2], 0x0051), md23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0051);
-        xp[0][2 * w + par] = __byte_perm(hi01, hi23, 0x5410);
-        xp[1][2 * w + par] = __byte_perm(md01, md23, 0x5410) ^ 0x80808080u;
-        xp[2][2 * w + par] = 0u;
-        if (wide_warp) {
-          const uint32_t lo01 = __byte_perm(vb[e], vb[e + 2], 0x0040), lo23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0040);
-          xp[2][2 * w + par] = __byte_perm(lo01, lo23, 0x5410) ^ 0x80808080u;
-        }
-      }
-    }
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      xsum[0] = dp4a_us(0x01010101u, xp[0][w], xsum[0]);
-      xsum[1] = dp4a_us(0x01010101u, xp[1][w], xsum[1]);
-    }
-    if (wide_warp) {
-#pragma unroll
-      for (int w = 0; w < 8; ++w) xsum[2] = dp4a_us(0x01010101u, xp[2][w], xsum[2]);
-    }
-  } else {
-#pragma unroll
-    for (int w = 0; w < 8; ++w) xp[0][w] = xp[1][w] = xp[2][w] = 0u;
-  }
-  // sum(x_fix) of the two high planes (what the two-plane dot products see)
-  const float xzf = fmaf(static_cast<float>(xsum[0]), 65536.0f, static_cast<float>(xsum[1]) * 256.0f);
+  GvX X;
+  const bool wide_warp = gv_load_x(a.x, j, act, X);
+  const uint32_t (*xp)[8] = X.xp;
+  const int* xsum = X.xsum;
+  const float sx = X.sx, xzf = X.xzf;
 
   const uint32_t sz_base = tc::smem_u32(sz + (jc >> 2));  // this thread's group column
   // The consume loop, instantiated once per plane count so that the common
@@ -435,37 +285,17 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
     for (int b = 0; b < kGvRowsPerBatch; ++b) prev[b] = 0.0f;
     int prev_row0 = -1, prev_rows = 0;
     auto reduce_store = [&](const float* v, int row0, int rows) {
-      // Butterfly over the batch: at the step with lane mask m = 1, 2, 4, ...
-      // a lane keeps the half of its values selected by its bit and adds the
-      // partner's copy of that half; after log2(batch) steps lane l holds
-      // row bitrev(l mod batch) summed over its lane group, and the remaining
-      // xor steps sum over all 32 lanes.
-      float w[kGvRowsPerBatch];
-#pragma unroll
-      for (int b = 0; b < kGvRowsPerBatch; ++b) w[b] = v[b];
-      int row_sel = 0;
-#pragma unroll
-      for (int half = kGvRowsPerBatch / 2, m = 1; half >= 1; half >>= 1, m <<= 1) {
-        const bool hi = (lane & m) != 0;
-        row_sel = (row_sel << 1) | (hi ? 1 : 0);
-#pragma unroll
-        for (int j = 0; j < half; ++j) {
-          const float keep = hi ? w[j + half] : w[j];
-          const float send = hi ? w[j] : w[j + half];
-          w[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-        }
-      }
-      float k = w[0];
-#pragma unroll
-      for (int m = kGvRowsPerBatch; m < 32; m <<= 1) k += __shfl_xor_sync(0xffffffffu, k, m);
+      float k;
+      const int row_sel = gv_reduce_batch<kGvRowsPerBatch>(v, lane, k);
       if (lane < kGvRowsPerBatch) {
         const int rr = rg + a.RG * row_sel;
         if (rr < rows) red[(row0 + rr) * a.WPR + wr] = k;
       }
     };
+    int s = 0;            // ring position and phase of stage i, kept
+    uint32_t phase = 0;   // incrementally (no division by S in the loop)
     for (int i = 0; i < nloads; ++i) {
-      const int s = i % S;
-      bool ok = tc::mbar_wait(full(s), (i / S) & 1, a.err, kGvSiteFull);
+      bool ok = tc::mbar_wait(full(s), phase, a.err, kGvSiteFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         *abort_flag = 1;
@@ -478,6 +308,10 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
       // The stage's codes are in registers: hand it back to the producer.
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(empty(s));
+      if (++s == S) {
+        s = 0;
+        phase ^= 1u;
+      }
       if (prev_row0 >= 0) reduce_store(prev, prev_row0, prev_rows);
 #pragma unroll
       for (int b = 0; b < kGvRowsPerBatch; ++b) prev[b] = p[b];

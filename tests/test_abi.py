@@ -79,6 +79,28 @@ def test_rejects_bad_arguments_without_gpu(built):
     assert L.qlin_w4a16_gemm_grouped(P(16), 1, 256, 2, n2, ptrs, ptrs, ptrs, 64, ptrs, None) == 3
     bad = (ctypes.c_void_p * 2)(16, 24)
     assert L.qlin_w4a16_gemm_grouped(P(16), 1, 256, 2, n2, bad, ptrs, ptrs, 128, ptrs, None) == 2
+    # W4A16 sequence: workspace size, bad K, null workspace, bad group
+    assert L.qlin_w4a16_sequence_workspace_bytes(128) == 512
+    assert L.qlin_w4a16_sequence_workspace_bytes(-1) == -1
+
+    class Step(ctypes.Structure):
+        _fields_ = [("x", ctypes.c_void_p), ("K", ctypes.c_int64), ("count", ctypes.c_int),
+                    ("N", ctypes.c_int64 * 4), ("wq", ctypes.c_void_p * 4), ("scales", ctypes.c_void_p * 4),
+                    ("zeros", ctypes.c_void_p * 4), ("y", ctypes.c_void_p * 4)]
+    assert ctypes.sizeof(Step) == 184
+    st = (Step * 1)()
+    st[0].x, st[0].K, st[0].count = 16, 200, 1
+    st[0].N[0], st[0].wq[0], st[0].scales[0], st[0].y[0] = 16, 16, 16, 16
+    sp = ctypes.cast(st, ctypes.c_void_p)
+    assert L.qlin_w4a16_gemv_sequence(sp, 1, 128, P(16), None) == 1      # K not a multiple of 128
+    st[0].K = 256
+    assert L.qlin_w4a16_gemv_sequence(sp, 1, 128, None, None) == 1       # null workspace
+    assert L.qlin_w4a16_gemv_sequence(sp, 1, 64, P(16), None) == 3       # group 64 not built
+    st[0].K = 12416
+    assert L.qlin_w4a16_gemv_sequence(sp, 1, 128, P(16), None) == 3      # K above 12288
+    st[0].K, st[0].count = 256, 5
+    assert L.qlin_w4a16_gemv_sequence(sp, 1, 128, P(16), None) == 1      # count above 4
+    assert L.qlin_w4a16_gemv_sequence(None, 0, 128, None, None) == 0     # empty sequence
     # perm K limit
     assert L.qlin_arc_perm(P(16), 0, 4, 32768, P(16), None) == 1
     msg = L.qlin_last_error_message()

@@ -235,3 +235,157 @@ def test_grouped_decoder_block_chain(qlin_gpu):
         ref = refs["down"]
     for n in ("q", "k", "gate", "down"):
         assert_within_tolerance(out[n].cpu().numpy(), refs[n].astype(np.float64), "block chain %s" % n)
+
+
+def _dev_mats(mats, symmetric_last=False):
+    wqs = [_dev(oracle.pack_u4(c)) for (c, _, _) in mats]
+    scs = [_dev(s) for (_, s, _) in mats]
+    zps = [_dev(oracle.pack_u4(z)) for (_, _, z) in mats]
+    if symmetric_last:
+        zps[-1] = None
+    return wqs, scs, zps
+
+
+def _run_sequence(q, steps):
+    ws = torch.zeros(q.qlin_w4a16_sequence_workspace_bytes(len(steps)), dtype=torch.uint8, device="cuda")
+    q.qlin_w4a16_gemv_sequence(steps, ws)
+    torch.cuda.synchronize()
+    assert q.qlin_get_device_error() == 0
+
+
+@pytest.mark.parametrize("hid,inter", [(1024, 2816), (4096, 11008)])
+def test_sequence_decoder_blocks_equal_single_launches(qlin_gpu, hid, inter):
+    """Two decoder blocks as one persistent sequence (q,k,v grouped on the
+    block input; o on v; gate,up grouped on o; down on up; the second block
+    on the first block's output): every output equals the per-launch path on
+    the same inputs bit for bit, and the oracle within tolerance.  The first
+    block's v projection is symmetric (no zero-points)."""
+    seed = 100
+    blocks = []
+    for _ in range(2):
+        blk = {}
+        for name, (n, k) in (("q", (hid, hid)), ("k", (hid // 4, hid)), ("v", (hid // 4, hid)), ("o", (hid, hid // 4)),
+                             ("gate", (inter, hid)), ("up", (inter, hid)), ("down", (hid, inter))):
+            blk[name] = _quantized(seed, n, k)
+            seed += 1
+        blocks.append(blk)
+    x0 = inputs.w4a16_decode(seed=99, T=1, N=8, K=hid)["x"]
+    xt = _dev(x0)
+    devs = []
+    for bi, blk in enumerate(blocks):
+        d = {}
+        for name in blk:
+            wq, sc, zp = _dev_mats([blk[name]], symmetric_last=(bi == 0 and name == "v"))
+            d[name] = (wq[0], sc[0], zp[0])
+        devs.append(d)
+
+    def outputs():
+        return [{n: torch.full((1, blocks[0][n][0].shape[0]), float("nan"), dtype=torch.float16, device="cuda")
+                 for n in blocks[0]} for _ in blocks]
+
+    seq_out, ref_out = outputs(), outputs()
+    steps = []
+    h = xt
+    for d, o in zip(devs, seq_out):
+        steps.append((h, [d[n][0] for n in "qkv"], [d[n][1] for n in "qkv"], [d[n][2] for n in "qkv"],
+                      [o[n] for n in "qkv"]))
+        steps.append((o["v"], [d["o"][0]], [d["o"][1]], [d["o"][2]], [o["o"]]))
+        steps.append((o["o"], [d[n][0] for n in ("gate", "up")], [d[n][1] for n in ("gate", "up")],
+                      [d[n][2] for n in ("gate", "up")], [o[n] for n in ("gate", "up")]))
+        steps.append((o["up"], [d["down"][0]], [d["down"][1]], [d["down"][2]], [o["down"]]))
+        h = o["down"]
+    _run_sequence(qlin_gpu, steps)
+    h = xt
+    for d, o in zip(devs, ref_out):
+        for n in "qkv":
+            qlin_gpu.qlin_w4a16_gemm(h, *d[n], o[n])
+        qlin_gpu.qlin_w4a16_gemm(o["v"], *d["o"], o["o"])
+        for n in ("gate", "up"):
+            qlin_gpu.qlin_w4a16_gemm(o["o"], *d[n], o[n])
+        qlin_gpu.qlin_w4a16_gemm(o["up"], *d["down"], o["down"])
+        h = o["down"]
+    torch.cuda.synchronize()
+    for bi in range(2):
+        for n in blocks[0]:
+            assert torch.equal(seq_out[bi][n], ref_out[bi][n]), "block %d %s" % (bi, n)
+    # the oracle on the first block's q and down projections
+    codes, s16, z = blocks[0]["q"]
+    assert_within_tolerance(seq_out[0]["q"].cpu().numpy(), oracle.w4a16_reference(x0, codes, s16, z), "sequence q")
+    codes, s16, z = blocks[0]["down"]
+    up = seq_out[0]["up"].cpu().numpy()
+    assert_within_tolerance(seq_out[0]["down"].cpu().numpy(), oracle.w4a16_reference(up, codes, s16, z),
+                            "sequence down")
+
+
+def test_sequence_many_small_steps(qlin_gpu):
+    """130 chained steps (more than one launch holds) on two ping-pong buffers,
+    with ragged heights and K values whose scale rows are not 16-byte aligned
+    (K = 1408: 11 groups); equal to per-launch results bit for bit."""
+    rng = np.random.default_rng(7)
+    n_steps = 130
+    width = 1408
+    mats = []
+    for i in range(n_steps):
+        mats.append(_quantized(200 + i, width, width))
+    dev = [_dev_mats([m]) for m in mats]
+    x0 = inputs.w4a16_decode(seed=198, T=1, N=8, K=width)["x"]
+    bufs = [_dev(x0), torch.empty((1, width), dtype=torch.float16, device="cuda")]
+    ref_bufs = [_dev(x0), torch.empty((1, width), dtype=torch.float16, device="cuda")]
+    steps = []
+    for i, (wq, sc, zp) in enumerate(dev):
+        steps.append((bufs[i % 2], wq, sc, zp, [bufs[(i + 1) % 2]]))
+    _run_sequence(qlin_gpu, steps)
+    for i, (wq, sc, zp) in enumerate(dev):
+        qlin_gpu.qlin_w4a16_gemm(ref_bufs[i % 2], wq[0], sc[0], zp[0], ref_bufs[(i + 1) % 2])
+    torch.cuda.synchronize()
+    assert torch.equal(bufs[n_steps % 2], ref_bufs[n_steps % 2])
+    assert torch.isfinite(bufs[n_steps % 2].float()).all()
+
+
+def test_sequence_ragged_groups_and_outliers(qlin_gpu):
+    """Grouped steps with ragged and tiny heights (763, 5, 1000 rows; an empty
+    matrix) and activation outliers (the three-plane path) in the input."""
+    k = 4096
+    mats = [_quantized(300 + i, n, k) for i, n in enumerate((763, 5, 0, 1000))]
+    wqs, scs, zps = _dev_mats([m for m in mats])
+    x = inputs.w4a16_decode(seed=301, T=1, N=8, K=k)["x"].astype(np.float32)
+    x[0, 17] *= 3e3
+    x[0, 2049] *= -1e3
+    x = x.astype(np.float16)
+    xt = _dev(x)
+    ys = [torch.empty((1, max(n, 1) if n else 0), dtype=torch.float16, device="cuda") for n in (763, 5, 0, 1000)]
+    _run_sequence(qlin_gpu, [(xt, wqs, scs, zps, ys)])
+    for i, n in enumerate((763, 5, 0, 1000)):
+        if n == 0:
+            continue
+        ref = torch.empty((1, n), dtype=torch.float16, device="cuda")
+        qlin_gpu.qlin_w4a16_gemm(xt, wqs[i], scs[i], zps[i], ref)
+        torch.cuda.synchronize()
+        assert torch.equal(ys[i], ref), i
+        codes, s16, z = mats[i]
+        assert_within_tolerance(ys[i].cpu().numpy(), oracle.w4a16_reference(x, codes, s16, z), "ragged %d" % n)
+
+
+def test_sequence_noalloc_equals_workspace(qlin_gpu):
+    """The no-allocation entry point (the library's own barrier counters) gives
+    the same outputs as a caller workspace, call after call (each call zeroes
+    the counters it uses), including a sequence longer than one launch."""
+    width = 1408
+    mats = [_quantized(400 + i, width, width) for i in range(140)]
+    dev = [_dev_mats([m]) for m in mats]
+    x0 = _dev(inputs.w4a16_decode(seed=399, T=1, N=8, K=width)["x"])
+
+    def run(noalloc):
+        bufs = [x0.clone(), torch.empty((1, width), dtype=torch.float16, device="cuda")]
+        steps = [(bufs[i % 2], wq, sc, zp, [bufs[(i + 1) % 2]]) for i, (wq, sc, zp) in enumerate(dev)]
+        if noalloc:
+            qlin_gpu.qlin_w4a16_gemv_sequence_noalloc(steps)
+        else:
+            _run_sequence(qlin_gpu, steps)
+        torch.cuda.synchronize()
+        assert qlin_gpu.qlin_get_device_error() == 0
+        return bufs[len(dev) % 2].clone()
+
+    ref = run(False)
+    for _ in range(2):
+        assert torch.equal(run(True), ref)
