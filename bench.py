@@ -44,7 +44,8 @@ LLAMA_BLOCK = [(4096, 4096)] * 4 + [(11008, 4096)] * 2 + [(4096, 11008)]
 W8A8 = dict(T=2048, K=4096, N=4096)
 NVFP4 = dict(T=2048, K=4096, N=4096, S=128)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "w4a16_decode_stack_traffic.txt")
-W4A16_SOURCE = os.path.join(ROOT, "quantized_linear_layer_gb300", "csrc", "w4a16_gemv.cu")
+W4A16_SOURCES = [os.path.join(ROOT, "quantized_linear_layer_gb300", "csrc", f)
+                 for f in ("w4a16_gemv.cu", "w4a16_gemv_common.cuh")]
 
 
 def w4a16_bytes(N, K, T):
@@ -331,6 +332,14 @@ def e2e_run(wl, torch, steps, warmup):
     return phase, h2d, d2h
 
 
+def w4a16_source_sha():
+    """sha256 of the per-launch decode GEMV's source (kernel file + shared device code)."""
+    h = hashlib.sha256()
+    for f in W4A16_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
 def recorded_traffic():
     """Per-launch DRAM traffic of the W4A16 GEMV from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -341,7 +350,7 @@ def recorded_traffic():
     b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     if not m or not b:
         return None
-    cur = hashlib.sha256(open(W4A16_SOURCE, "rb").read()).hexdigest()
+    cur = w4a16_source_sha()
     return float(b.group(1)) if m.group(1) == cur else None
 
 
