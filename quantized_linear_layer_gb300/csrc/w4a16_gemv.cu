@@ -47,6 +47,8 @@
 // bulk copy per matrix, and the matrices share a single wait on the kernel
 // that produced the activations.
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 #include <type_traits>
 
 #include "device_common.cuh"
@@ -63,6 +65,7 @@ constexpr int kGvMaxWarpsPerRow = 12;       // K <= 12 * 32 * 32 = 12288
 constexpr int kGvMaxComputeWarps = 12;
 constexpr int kGvThreadsMax = (kGvMaxComputeWarps + 1) * 32;
 constexpr int kGvCtaBytes = 112 * 1024;     // two CTAs (this layer, the next) fit on one SM
+constexpr int kGvMaxRegs = 72;              // registers per thread (fixed: the launch plan counts them)
 constexpr int kGvMinStages = 2;
 constexpr int kGvMaxStages = 8;
 constexpr int kGvSiteFull = 1, kGvSiteEmpty = 2, kGvSiteDrain = 3;
@@ -152,9 +155,10 @@ __device__ __forceinline__ bool gv_segment(const GvArgs& a, int r0, int nrows, i
 }
 
 
-// B rows of each stage per warp and row group (a power of two).
+// B rows of each stage per warp and row group (a power of two).  Warps past
+// the producer (ballast of the alternate launch shape) leave at once.
 template <int B>
-__global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvArgs a) {
+__global__ void __maxnreg__(kGvMaxRegs) w4a16_gemv_kernel(const GvArgs a) {
   constexpr int kGvRowsPerBatch = B;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -185,6 +189,7 @@ __global__ void __launch_bounds__(kGvThreadsMax, 2) w4a16_gemv_kernel(const GvAr
   }
   __syncthreads();
   pdl_launch_dependents();
+  if (warp > ncw) return;
 
   if (warp == ncw) {
     // ---------------- producer: the CTA's band of weight rows ----------------
@@ -369,6 +374,65 @@ bool gv_plan(int64_t N, int64_t K, GvArgs& a, int& grid, int& smem) {
   return true;
 }
 
+// Launch shapes of consecutive GEMVs.  With programmatic dependent launch the
+// next layer's CTAs take whatever SM slots free up while the current layer
+// runs, and the block scheduler then puts two CTAs of one layer on some SMs
+// and none on others, layer after layer (measured: 100 of 152 SMs per layer).
+// Launches alternate between two shapes of the same kernel instead: shape A
+// asks for more than half of an SM's shared memory, so two A CTAs never share
+// an SM; shape B carries idle ballast warps so that two B CTAs would need
+// more than an SM's registers; one A and one B fit together.  Each layer
+// therefore lands one CTA per SM, beside one CTA of its neighbour.  The
+// shapes come from the device's limits and the kernel's register count; when
+// they cannot be met every launch keeps the plain shape.
+void gv_alternate_shape(const void* fn, int threads, int plan_smem, int& threads_out, int& smem_out) {
+  threads_out = threads;
+  smem_out = plan_smem;
+  static std::atomic<unsigned> parity{0};
+  struct Shape {
+    const void* fn = nullptr;
+    bool ok = false;
+    int regs_per_warp = 0, rf = 0, sm_smem = 0, reserved = 0, block_smem = 0;
+  };
+  static Shape shapes[4];
+  static std::mutex mu;
+  Shape shape;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    int k = 0;
+    while (k < 4 && shapes[k].fn != nullptr && shapes[k].fn != fn) ++k;
+    if (k == 4) return;  // (never: two kernel instances)
+    if (shapes[k].fn == nullptr) {
+      Shape& sh = shapes[k];
+      sh.fn = fn;
+      int dev = 0;
+      cudaFuncAttributes fa = {};
+      if (cudaGetDevice(&dev) == cudaSuccess && cudaFuncGetAttributes(&fa, fn) == cudaSuccess) {
+        cudaDeviceGetAttribute(&sh.rf, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+        cudaDeviceGetAttribute(&sh.sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        cudaDeviceGetAttribute(&sh.reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        cudaDeviceGetAttribute(&sh.block_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        sh.regs_per_warp = 32 * ((fa.numRegs + 7) / 8 * 8);
+        sh.ok = fa.numRegs <= kGvMaxRegs && sh.rf > 0 && sh.sm_smem > 0;
+      }
+    }
+    shape = shapes[k];
+  }
+  if (!shape.ok) return;
+  const int warps_a = threads / 32;
+  int warps_b = warps_a + 1;
+  while (2 * warps_b * shape.regs_per_warp <= shape.rf) ++warps_b;
+  const int smem_a = std::max(plan_smem, shape.sm_smem / 2 - shape.reserved + 16);
+  const bool fits = (warps_a + warps_b) * shape.regs_per_warp <= shape.rf && warps_b * 32 <= 1024 &&
+                    smem_a <= shape.block_smem && smem_a + plan_smem + 2 * shape.reserved <= shape.sm_smem;
+  if (!fits) return;
+  if ((parity.fetch_add(1, std::memory_order_relaxed) & 1u) == 0) {
+    smem_out = smem_a;              // shape A: more than half the shared memory
+  } else {
+    threads_out = warps_b * 32;     // shape B: more than half the registers
+  }
+}
+
 }  // namespace
 
 bool w4a16_gemv_supported(int64_t T, int64_t N, int64_t K) {
@@ -404,13 +468,17 @@ cudaError_t launch_w4a16_gemv_grouped(const void* x, int64_t K, int count, const
   a.K = static_cast<int>(K);
   a.zpitch = static_cast<int>((K / 128 + 1) / 2);
   const bool b8 = gv_rows_per_batch(a.RG) == 8;
-  cudaError_t e = cudaFuncSetAttribute(b8 ? w4a16_gemv_kernel<8> : w4a16_gemv_kernel<4>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const void* fn = b8 ? reinterpret_cast<const void*>(w4a16_gemv_kernel<8>)
+                      : reinterpret_cast<const void*>(w4a16_gemv_kernel<4>);
+  int threads = (a.RG * a.WPR + 1) * 32;
+  int dyn = smem;
+  gv_alternate_shape(fn, threads, smem, threads, dyn);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3((a.RG * a.WPR + 1) * 32);
-  cfg.dynamicSmemBytes = smem;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = dyn;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -186,3 +186,30 @@ def test_quant_nvfp4_mma_scale_layout(qlin_gpu, rows, S, mode):
         rq, rsf = oracle.arc_quantize_weight(x32, perm, S, g)
     assert np.array_equal(q1.cpu().numpy(), oracle.pack_u4(rq))
     assert np.array_equal(sf_m.cpu().numpy(), sf_rows_to_mma(rsf))
+
+
+@pytest.mark.parametrize("rows,K,dtype,S,with_perm", [(5, 40960, "f32", 0, False), (7, 16384, "f16", 128, True),
+                                                     (601, 1024, "bf16", 64, True)])
+def test_quant_nvfp4_row_staging(qlin_gpu, rows, K, dtype, S, with_perm):
+    """Rows staged through one buffer (160 KB fp32 rows), two buffers of one row
+    (64 KB rows), and two buffers of two rows over many items per CTA (601
+    rows: an odd last item)."""
+    rng = np.random.default_rng(rows + K)
+    x = rng.standard_normal((rows, K)).astype(np.float32)
+    if dtype == "f16":
+        xt = torch.from_numpy(x.astype(np.float16)).cuda()
+    elif dtype == "bf16":
+        xt = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    else:
+        xt = torch.from_numpy(x).cuda()
+    x32 = xt.float().cpu().numpy()
+    g = np.float32(oracle.nvfp4_global_scale(x32))
+    perm = oracle.arc_perm(x32) if with_perm else None
+    gq, gsf = _quant(qlin_gpu, xt, torch.tensor([g]).cuda(),
+                     None if perm is None else torch.from_numpy(perm).cuda(), S, 0)
+    if perm is None:
+        rq, rsf = oracle.nvfp4_quantize(x32, g)
+    else:
+        rq, rsf = oracle.arc_quantize_activation(x32, perm, S, g)
+    assert np.array_equal(gsf, rsf)
+    assert np.array_equal(gq, oracle.pack_u4(rq))
