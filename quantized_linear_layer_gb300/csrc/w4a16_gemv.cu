@@ -475,6 +475,10 @@ cudaError_t launch_w4a16_gemv_grouped(const void* x, int64_t K, int count, const
   gv_alternate_shape(fn, threads, smem, threads, dyn);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
+  // the largest shared-memory carveout, so that the SM can hold this CTA and
+  // the neighbouring layer's whatever launch shape reached it first
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(threads);
