@@ -66,6 +66,7 @@ constexpr int kGvMaxComputeWarps = 12;
 constexpr int kGvThreadsMax = (kGvMaxComputeWarps + 1) * 32;
 constexpr int kGvCtaBytes = 112 * 1024;     // two CTAs (this layer, the next) fit on one SM
 constexpr int kGvMaxRegs = 72;              // registers per thread (fixed: the launch plan counts them)
+constexpr int kGvL2Ahead = 2;               // stages of L2 prefetch ahead of the copy into the ring
 constexpr int kGvMinStages = 2;
 constexpr int kGvMaxStages = 8;
 constexpr int kGvSiteFull = 1, kGvSiteEmpty = 2, kGvSiteDrain = 3;
@@ -220,6 +221,20 @@ __global__ void __maxnreg__(kGvMaxRegs) w4a16_gemv_kernel(const GvArgs a) {
         }
         if (*abort_flag) break;
         const int rows_i = min(a.R, nrows - i * a.R);
+        // the rows kGvL2Ahead stages ahead, into L2 only: more bytes in
+        // flight than the ring holds, so the copy into the ring later hits L2
+        const int ia = i + kGvL2Ahead;
+        if (ia < nloads) {
+          const int rl = r0 + ia * a.R, nl = min(a.R, nrows - ia * a.R);
+          for (int done = 0; done < nl;) {
+            int first;
+            const int p = gv_matrix(a, rl + done, first);
+            const int seg = min(nl - done, a.row_end[p] - (rl + done));
+            tc::bulk_prefetch_l2(a.wq[p] + static_cast<int64_t>(rl + done - first) * row_bytes,
+                                 static_cast<uint32_t>(seg * row_bytes));
+            done += seg;
+          }
+        }
         tc::mbar_arrive_expect_tx(full(s), static_cast<uint32_t>(rows_i * row_bytes));
         // one bulk copy per matrix the stage's rows fall in
         for (int done = 0; done < rows_i;) {
@@ -344,11 +359,11 @@ __host__ __device__ constexpr int gv_rows_per_batch(int RG) { return RG >= 2 ? 8
 
 // Shared-memory plan of one launch; false when the band's scales do not
 // leave room for a double-buffered ring within the per-CTA budget.
-bool gv_plan(int64_t N, int64_t K, GvArgs& a, int& grid, int& smem) {
+bool gv_plan(int64_t N, int64_t K, GvArgs& a, int& grid, int& smem, int warps = 8) {
   if (K > static_cast<int64_t>(kGvMaxWarpsPerRow) * 32 * 32 || N <= 0) return false;
   const int G = static_cast<int>(K / 128), KC = static_cast<int>(K / 32), row_bytes = static_cast<int>(K / 2);
   a.WPR = (KC + 31) / 32;
-  a.RG = a.WPR >= 8 ? 1 : 8 / a.WPR;
+  a.RG = a.WPR >= warps ? 1 : warps / a.WPR;
   grid = static_cast<int>(std::min<int64_t>(sm_count(), (N + a.RG - 1) / a.RG));
   const int rows_max = static_cast<int>((N + grid - 1) / grid);
   // A stage holds one batch of rows for every row group: 8 rows per warp
@@ -378,59 +393,51 @@ bool gv_plan(int64_t N, int64_t K, GvArgs& a, int& grid, int& smem) {
 // next layer's CTAs take whatever SM slots free up while the current layer
 // runs, and the block scheduler then puts two CTAs of one layer on some SMs
 // and none on others, layer after layer (measured: 100 of 152 SMs per layer).
-// Launches alternate between two shapes of the same kernel instead: shape A
-// asks for more than half of an SM's shared memory, so two A CTAs never share
-// an SM; shape B carries idle ballast warps so that two B CTAs would need
-// more than an SM's registers; one A and one B fit together.  Each layer
-// therefore lands one CTA per SM, beside one CTA of its neighbour.  The
-// shapes come from the device's limits and the kernel's register count; when
-// they cannot be met every launch keeps the plain shape.
-void gv_alternate_shape(const void* fn, int threads, int plan_smem, int& threads_out, int& smem_out) {
-  threads_out = threads;
-  smem_out = plan_smem;
-  static std::atomic<unsigned> parity{0};
-  struct Shape {
-    const void* fn = nullptr;
-    bool ok = false;
-    int regs_per_warp = 0, rf = 0, sm_smem = 0, reserved = 0, block_smem = 0;
-  };
-  static Shape shapes[4];
-  static std::mutex mu;
-  Shape shape;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    int k = 0;
-    while (k < 4 && shapes[k].fn != nullptr && shapes[k].fn != fn) ++k;
-    if (k == 4) return;  // (never: two kernel instances)
-    if (shapes[k].fn == nullptr) {
-      Shape& sh = shapes[k];
-      sh.fn = fn;
-      int dev = 0;
-      cudaFuncAttributes fa = {};
-      if (cudaGetDevice(&dev) == cudaSuccess && cudaFuncGetAttributes(&fa, fn) == cudaSuccess) {
-        cudaDeviceGetAttribute(&sh.rf, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
-        cudaDeviceGetAttribute(&sh.sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-        cudaDeviceGetAttribute(&sh.reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
-        cudaDeviceGetAttribute(&sh.block_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        sh.regs_per_warp = 32 * ((fa.numRegs + 7) / 8 * 8);
-        sh.ok = fa.numRegs <= kGvMaxRegs && sh.rf > 0 && sh.sm_smem > 0;
-      }
-    }
-    shape = shapes[k];
-  }
-  if (!shape.ok) return;
-  const int warps_a = threads / 32;
-  int warps_b = warps_a + 1;
-  while (2 * warps_b * shape.regs_per_warp <= shape.rf) ++warps_b;
-  const int smem_a = std::max(plan_smem, shape.sm_smem / 2 - shape.reserved + 16);
-  const bool fits = (warps_a + warps_b) * shape.regs_per_warp <= shape.rf && warps_b * 32 <= 1024 &&
-                    smem_a <= shape.block_smem && smem_a + plan_smem + 2 * shape.reserved <= shape.sm_smem;
-  if (!fits) return;
-  if ((parity.fetch_add(1, std::memory_order_relaxed) & 1u) == 0) {
-    smem_out = smem_a;              // shape A: more than half the shared memory
-  } else {
-    threads_out = warps_b * 32;     // shape B: more than half the registers
-  }
+// Launches alternate between two shapes of the same kernel instead: shape R
+// holds more than half of an SM's registers (idle ballast warps on top of the
+// working ones), shape S more than half of its shared memory; two CTAs of one
+// shape never share an SM, one of each does.  Each layer therefore lands one
+// CTA per SM, beside one CTA of its neighbour.  (Twelve working warps in
+// shape R instead of ballast measured the same.)
+// The shapes come from the device's limits and the kernel's register count;
+// when they cannot be met every launch keeps the plain shape.
+struct GvShapeInfo {
+  bool ok = false;
+  int regs_per_warp = 0, rf = 0, sm_smem = 0, reserved = 0, block_smem = 0;
+};
+
+const GvShapeInfo& gv_shape_info() {
+  static GvShapeInfo info;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    cudaFuncAttributes f8 = {}, f4 = {};
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&f8, reinterpret_cast<const void*>(w4a16_gemv_kernel<8>)) != cudaSuccess ||
+        cudaFuncGetAttributes(&f4, reinterpret_cast<const void*>(w4a16_gemv_kernel<4>)) != cudaSuccess)
+      return;
+    const int regs = std::max(f8.numRegs, f4.numRegs);
+    cudaDeviceGetAttribute(&info.rf, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&info.sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&info.reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    cudaDeviceGetAttribute(&info.block_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    info.regs_per_warp = 32 * ((regs + 7) / 8 * 8);
+    info.ok = regs <= kGvMaxRegs && info.rf > 0 && info.sm_smem > 0 &&
+              kGvCtaBytes + info.reserved <= info.sm_smem / 2;
+  });
+  return info;
+}
+
+// The shared memory of a shape-S CTA: more than half of the SM's.
+int gv_smem_shape_s(const GvShapeInfo& si) { return si.sm_smem / 2 - si.reserved + 16; }
+
+// The warps of a shape-R CTA with `warps` working warps: enough to hold more
+// than half of the SM's registers; 0 when that leaves no room for the largest
+// shape-S CTA (kGvMaxComputeWarps + 1 warps) beside it.
+int gv_warps_shape_r(const GvShapeInfo& si, int warps) {
+  int w = warps;
+  while (2 * w * si.regs_per_warp <= si.rf) ++w;
+  return (w + kGvMaxComputeWarps + 1) * si.regs_per_warp <= si.rf ? w : 0;
 }
 
 }  // namespace
@@ -460,6 +467,10 @@ cudaError_t launch_w4a16_gemv_grouped(const void* x, int64_t K, int count, const
   }
   if (total == 0) return cudaSuccess;
   if (total > kMaxGemvRows) return cudaErrorInvalidValue;
+  // launch shape: 0 plain, 1 register-heavy, 2 shared-memory-heavy
+  static std::atomic<unsigned> parity{0};
+  const GvShapeInfo& si = gv_shape_info();
+  int shape = si.ok ? 1 + static_cast<int>(parity.fetch_add(1, std::memory_order_relaxed) & 1u) : 0;
   int grid = 0, smem = 0;
   if (!gv_plan(total, K, a, grid, smem)) return cudaErrorInvalidValue;
   a.x = static_cast<const __half*>(x);
@@ -472,7 +483,13 @@ cudaError_t launch_w4a16_gemv_grouped(const void* x, int64_t K, int count, const
                       : reinterpret_cast<const void*>(w4a16_gemv_kernel<4>);
   int threads = (a.RG * a.WPR + 1) * 32;
   int dyn = smem;
-  gv_alternate_shape(fn, threads, smem, threads, dyn);
+  if (shape == 1) {
+    const int w = gv_warps_shape_r(si, threads / 32);
+    if (w > 0) threads = w * 32;
+  } else if (shape == 2) {
+    dyn = std::max(smem, gv_smem_shape_s(si));
+    if (dyn > si.block_smem) dyn = smem;
+  }
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
   // the largest shared-memory carveout, so that the SM can hold this CTA and
