@@ -43,6 +43,13 @@ cudaError_t launch_w4a16_sequence(const W4A16SeqStep* steps, int nsteps, unsigne
 // Device address of the library's own counters (enough for every launch of
 // a sequence: each launch takes at most 128 steps and zeroes them first).
 unsigned int* w4a16_sequence_static_workspace();
+// Streamed tensor-core W4A16 for up to 16 tokens over the concatenated rows
+// of `count` matrices sharing x (false / cudaErrorInvalidValue when the
+// shape has no launch plan).
+bool w4a16_skinny_supported(int64_t T, int64_t N, int64_t K);
+cudaError_t launch_w4a16_skinny_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
+                                        const uint8_t* const* wq, const void* const* scales,
+                                        const uint8_t* const* zeros, void* const* y, cudaStream_t stream);
 cudaError_t launch_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
                                       const uint8_t* const* wq, const void* const* scales,
                                       const uint8_t* const* zeros, void* const* y, cudaStream_t stream);

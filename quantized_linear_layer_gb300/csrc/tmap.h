@@ -19,4 +19,11 @@ namespace qlin {
 cudaError_t make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                             uint32_t box_rows, int swizzle_bytes = 0);
 
+// Tiled tensor map over a row-major matrix of `rows` rows of `cols8` 8-byte
+// elements (row pitch cols8 * 8 bytes, a multiple of 16), loading boxes of
+// box_rows x box_cols8 elements (box_cols8 <= 256) into plain dense rows;
+// out-of-range parts of a box are filled with zeros.
+cudaError_t make_tmap_2d_u64(CUtensorMap* map, const void* base, uint64_t cols8, uint64_t rows, uint32_t box_cols8,
+                             uint32_t box_rows);
+
 }  // namespace qlin

@@ -19,61 +19,18 @@
 // scale is applied once per group in fp32.  Warps of a CTA split K; their
 // partial sums are added in a fixed order through shared memory.
 //
-// Fragment mapping.  Thread (g, c) = (lane / 4, lane % 4) loads 16 bytes (32
-// codes) of rows g and g + 8 at K offset 32c within a group.  Each 32-bit word
-// holds eight consecutive codes k .. k+7; the unpack yields the half2 pairs
-// (k, k+4), (k+1, k+5), (k+2, k+6), (k+3, k+7).  These pairs are assigned to
-// the MMA's logical K slots (2c, 2c+1) and (2c+8, 2c+9); the activation
-// fragment of the same thread is built with exactly the same assignment, so
-// the product over a group covers every K index once.
+// The fragment mapping and the unpack are in w4a16_mma_common.cuh.
 #include "device_common.cuh"
 #include "qlin_internal.h"
 #include "tc_common.cuh"
+#include "w4a16_mma_common.cuh"
 
 namespace qlin {
 namespace {
 
+using namespace w4mma;
+
 constexpr int kW4Group = 128;
-
-__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
-  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
-__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
-  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b),
-                      *reinterpret_cast<__half2*>(&c));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
-__device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Exact fp16 (q - z) pairs from one word of eight codes.
-//   out[0] = (k, k+4), out[1] = (k+1, k+5), out[2] = (k+2, k+6), out[3] = (k+3, k+7)
-// 0x6400 is fp16 1024: OR-ing a nibble n into its low mantissa bits gives
-// 1024 + n, and 1024 + 16n for the nibble one position higher.
-__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t sub, uint32_t add, uint32_t* out) {
-  const uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u, kEx = 0x64006400u, kSixteenth = 0x2C002C00u;
-  out[0] = h2_sub((w & kLo) | kEx, sub);                 // (1024 + n) - (1024 + z)
-  out[1] = h2_fma((w & kHi) | kEx, kSixteenth, add);     // (1024 + 16n) / 16 - (64 + z)
-  const uint32_t w8 = w >> 8;
-  out[2] = h2_sub((w8 & kLo) | kEx, sub);
-  out[3] = h2_fma((w8 & kHi) | kEx, kSixteenth, add);
-}
-
-// Activation pairs (x[k+j], x[k+j+4]) for j = 0..3 from eight consecutive fp16.
-__device__ __forceinline__ void pair_x(uint4 u, uint32_t* out) {
-  out[0] = __byte_perm(u.x, u.z, 0x5410);
-  out[1] = __byte_perm(u.x, u.z, 0x7632);
-  out[2] = __byte_perm(u.y, u.w, 0x5410);
-  out[3] = __byte_perm(u.y, u.w, 0x7632);
-}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -112,27 +69,6 @@ __host__ __device__ inline W4Smem w4_smem_plan(int W, int GPW, int GC, int Tc, i
   p.c_off = p.r_off + W * 32 * NT * 4 * 4;              // [C][32][NT*4] cluster partial sums
   p.total = p.c_off + C * 32 * NT * 4 * 4;
   return p;
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // One cluster of C CTAs per 16 output rows; CTA r of the cluster handles the
@@ -400,12 +336,10 @@ cudaError_t launch_chunk(const __half* x, int Tc, int N, int K, const uint8_t* w
                             ldy);
 }
 
-}  // namespace
-
-cudaError_t launch_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq,
-                              const void* scales, const uint8_t* zeros, void* y, cudaStream_t stream) {
-  if (T == 0 || N == 0) return cudaSuccess;
-  if (w4a16_gemv_supported(T, N, K)) return launch_w4a16_gemv(x, N, K, wq, scales, zeros, y, stream);
+// The fallback for shapes without a skinny plan: one launch per chunk of
+// tokens that the activation staging budget allows.
+cudaError_t launch_w4a16_mma(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq, const void* scales,
+                             const uint8_t* zeros, void* y, cudaStream_t stream) {
   const int t = static_cast<int>(T), n = static_cast<int>(N), k = static_cast<int>(K);
   const __half* xh = static_cast<const __half*>(x);
   const __half* sh = static_cast<const __half*>(scales);
@@ -427,19 +361,46 @@ cudaError_t launch_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, co
   return cudaSuccess;
 }
 
+}  // namespace
+
+// Dispatch: one token on the CUDA-core GEMV, up to 16 tokens per launch on
+// the streamed tensor-core skinny kernel (more tokens in chunks of 16, each
+// chunk one pass over the weights), and the staged kernel above for shapes
+// the skinny kernel has no plan for.
 cudaError_t launch_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
                                       const uint8_t* const* wq, const void* const* scales,
                                       const uint8_t* const* zeros, void* const* y, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
+  if (count < 1 || count > QLIN_W4A16_MAX_GROUP) return cudaErrorInvalidValue;
   int64_t total = 0;
   for (int p = 0; p < count; ++p) total += N[p];
   if (total == 0) return cudaSuccess;
   if (w4a16_gemv_supported(T, total, K)) return launch_w4a16_gemv_grouped(x, K, count, N, wq, scales, zeros, y, stream);
+  constexpr int64_t kChunk = 16;
+  const int64_t first = T < kChunk ? T : kChunk, last = T % kChunk;
+  if (w4a16_skinny_supported(first, total, K) && (last == 0 || w4a16_skinny_supported(last, total, K))) {
+    for (int64_t t0 = 0; t0 < T; t0 += kChunk) {
+      const int64_t tc = T - t0 < kChunk ? T - t0 : kChunk;
+      void* yc[QLIN_W4A16_MAX_GROUP];
+      for (int p = 0; p < count; ++p) yc[p] = static_cast<__half*>(y[p]) + t0 * N[p];
+      cudaError_t e = launch_w4a16_skinny_grouped(static_cast<const __half*>(x) + t0 * K, tc, K, count, N, wq, scales,
+                                                  zeros, yc, stream);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   for (int p = 0; p < count; ++p) {
-    cudaError_t e = launch_w4a16_gemm(x, T, N[p], K, wq[p], scales[p], zeros[p], y[p], stream);
+    if (N[p] == 0) continue;
+    cudaError_t e = launch_w4a16_mma(x, T, N[p], K, wq[p], scales[p], zeros[p], y[p], stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq,
+                              const void* scales, const uint8_t* zeros, void* y, cudaStream_t stream) {
+  if (T == 0 || N == 0) return cudaSuccess;
+  return launch_w4a16_gemm_grouped(x, T, K, 1, &N, &wq, &scales, &zeros, &y, stream);
 }
 
 }  // namespace qlin

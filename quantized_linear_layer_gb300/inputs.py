@@ -11,6 +11,10 @@ Workloads (default seeds 0..4):
   w4a16_decode    T in {1,4,16}; (N,K) in {(4096,4096),(11008,4096),
                   (4096,11008)} (Llama-2-7B-shaped layers): X ~ N(0,1) fp16,
                   W ~ N(0, 0.02) fp32 (quantized g128 asymmetric by the path).
+  w4a16_packed_random  already-packed uint4 g128 weights for shapes too large
+                  to draw and quantize in fp32: every byte ~ U{0..255} (two
+                  codes), fp16 scales ~ U[0.005, 0.02], packed zero-points
+                  ~ U{0..255}; X ~ N(0,1) fp16.
   w8a8_sym_bias   T=2048, K=4096, N=4096: X ~ N(0,1) with 1% of channels
                   (41, seeded choice) scaled x20, fp16; W ~ N(0, 0.02) fp32;
                   bias ~ N(0, 0.1) fp16.
@@ -35,6 +39,15 @@ def tiny_w4a16(seed=0, T=1, N=256, K=512):
     codes = rng.integers(0, 16, size=(N, K), dtype=np.uint8)
     scales = rng.uniform(0.005, 0.02, size=(N, K // 128)).astype(np.float16)
     return {"x": x, "codes": codes, "scales": scales, "zeros": None}
+
+
+def w4a16_packed_random(seed, T, N, K):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, K), dtype=np.float32).astype(np.float16)
+    wq = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    scales = rng.uniform(0.005, 0.02, size=(N, K // 128)).astype(np.float16)
+    zeros = rng.integers(0, 256, size=(N, (K // 128 + 1) // 2), dtype=np.uint8)
+    return {"x": x, "wq": wq, "scales": scales, "zeros": zeros}
 
 
 def w4a16_decode(seed=1, T=1, N=4096, K=4096):

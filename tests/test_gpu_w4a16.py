@@ -389,3 +389,68 @@ def test_sequence_noalloc_equals_workspace(qlin_gpu):
     ref = run(False)
     for _ in range(2):
         assert torch.equal(run(True), ref)
+
+
+# ---- the streamed tensor-core path for a few tokens (T <= 16 per launch) ----
+
+@pytest.mark.parametrize("T,N,K", [
+    (7, 5000, 128),      # one group per row: every CTA owns full rows
+    (3, 77, 1152),       # bands shorter than a stage, odd group count
+    (9, 1000, 3584),     # two token tiles (one padded token), 14 warps of two groups
+    (6, 1500, 4480),     # K split over two CTAs, ragged group count (35)
+    (2, 2000, 8192),     # two CTAs, 16 warps of two groups
+    (16, 300, 4096),     # two CTAs, two token tiles, bands of one stage
+    (4, 300, 8448),      # K split over four CTAs (66 groups)
+    (12, 640, 7296),     # four CTAs, two token tiles with padded tokens
+    (16, 600, 11008),    # four CTAs on the down-projection K
+])
+def test_skinny_splits_against_oracle(qlin_gpu, T, N, K):
+    d = inputs.w4a16_decode(seed=500 + T, T=T, N=N, K=K)
+    codes, s16, z = oracle.quant_w4_g128(d["w"])
+    ref = oracle.w4a16_reference(d["x"], codes, s16, z)
+    y = _gemm(qlin_gpu, _dev(d["x"]), _dev(oracle.pack_u4(codes)), _dev(s16), _dev(oracle.pack_u4(z)))
+    assert_within_tolerance(y, ref, "W4A16 skinny T=%d N=%d K=%d" % (T, N, K))
+
+
+@pytest.mark.parametrize("T,N,K", [(16, 65536, 4096), (4, 90000, 4096)])
+def test_skinny_several_bands_sampled_rows(qlin_gpu, T, N, K):
+    """Large N: each cluster processes several bands of rows in turn (the
+    receive buffers alternate between bands), or one CTA owns a band of
+    hundreds of rows.  The oracle checks a sample of rows that covers both
+    ends; a second run must give the same bits."""
+    d = inputs.w4a16_packed_random(seed=700 + T, T=T, N=N, K=K)
+    xt, wq, sc, zp = _dev(d["x"]), _dev(d["wq"]), _dev(d["scales"]), _dev(d["zeros"])
+    y = _gemm(qlin_gpu, xt, wq, sc, zp)
+    y2 = _gemm(qlin_gpu, xt, wq, sc, zp)
+    assert np.array_equal(y.view(np.uint16), y2.view(np.uint16))
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([np.arange(0, 40), np.arange(N - 40, N),
+                                     rng.choice(N, size=600, replace=False)]))
+    ref = oracle.w4a16_reference_packed(d["x"], d["wq"][rows], d["scales"][rows], d["zeros"][rows])
+    assert_within_tolerance(y[:, rows], ref, "W4A16 T=%d N=%d sampled rows" % (T, N))
+
+
+@pytest.mark.parametrize("T", [2, 9, 16, 33])
+def test_skinny_grouped_equals_separate(qlin_gpu, T):
+    """Grouped calls over matrices whose boundaries fall inside a 16-row
+    stage give the same bits as one call per matrix (the K split depends
+    only on T and K), and match the oracle."""
+    shapes = ((763, 1408), (8, 1408), (5, 1408), (1000, 1408))
+    k = shapes[0][1]
+    x = inputs.w4a16_decode(seed=800 + T, T=T, N=8, K=k)["x"]
+    xt = _dev(x)
+    mats = [_quantized(801 + i, n, k) for i, (n, _) in enumerate(shapes)]
+    wqs = [_dev(oracle.pack_u4(c)) for (c, _, _) in mats]
+    scs = [_dev(s) for (_, s, _) in mats]
+    zps = [_dev(oracle.pack_u4(z)) for (_, _, z) in mats]
+    ys = [torch.empty((T, n), dtype=torch.float16, device="cuda") for (n, _) in shapes]
+    qlin_gpu.qlin_w4a16_gemm_grouped(xt, wqs, scs, zps, ys)
+    torch.cuda.synchronize()
+    assert qlin_gpu.qlin_get_device_error() == 0
+    for i, (n, _) in enumerate(shapes):
+        sep = torch.empty((T, n), dtype=torch.float16, device="cuda")
+        qlin_gpu.qlin_w4a16_gemm(xt, wqs[i], scs[i], zps[i], sep)
+        torch.cuda.synchronize()
+        assert torch.equal(ys[i], sep), "matrix %d" % i
+        ref = oracle.w4a16_reference(x, *mats[i])
+        assert_within_tolerance(ys[i].cpu().numpy(), ref, "grouped T=%d matrix %d" % (T, i))
