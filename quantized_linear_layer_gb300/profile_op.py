@@ -1,0 +1,127 @@
+"""Runs one operation of the library a few times on seeded synthetic inputs,
+so that a profiler can capture it in isolation, e.g.
+
+    ncu --set full --clock-control none -k regex:w4a16_skinny -s 2 -c 1 -o prof \\
+        python -m quantized_linear_layer_gb300.profile_op w4a16 --T 4 --N 11008 --K 4096
+
+Operations (sizes as flags):
+  w4a16        qlin_w4a16_gemm, X [T][K] fp16, weights N x K (uint4 g128)
+  w4a16_group  qlin_w4a16_gemm_grouped over --groups matrices of N x K each
+  int8_quant   qlin_quant_act_int8, X [T][K] fp16, symmetric
+  w8a8         qlin_w8a8_gemm, A [T][K] int8, B [N][K] int8, per-token / per-channel scales, bf16 out
+  nvfp4_quant  qlin_quant_nvfp4, X [T][K] fp16 with S residual channels, MMA scale layout
+  nvfp4_gemm   qlin_nvfp4_gemm, A [T][K] and B [N][K] NVFP4 (made by the quantizer), bf16 out
+
+Every launch reads its own copy of the weights (--copies of them, rotated), so
+that weight streams come from HBM as they do in a model; the launches run
+back to back on one stream, then the device error word is checked.
+"""
+
+import argparse
+import sys
+
+
+def _setup(args, q, torch):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(args.seed)
+    T, N, K = args.T, args.N, args.K
+    copies = max(1, args.copies)
+
+    def randn(shape, dtype):
+        return torch.randn(shape, device="cuda", generator=g).to(dtype)
+
+    if args.op in ("w4a16", "w4a16_group"):
+        nm = 1 if args.op == "w4a16" else args.groups
+        mats = []
+        for _ in range(copies):
+            blk = []
+            for _m in range(nm):
+                wq = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda", generator=g)
+                sc = (torch.rand((N, K // 128), device="cuda", generator=g) * 0.015 + 0.005).half()
+                zp = torch.randint(0, 256, (N, (K // 128 + 1) // 2), dtype=torch.uint8, device="cuda", generator=g)
+                blk.append((wq, sc, zp))
+            mats.append(blk)
+        x = randn((T, K), torch.float16)
+        ys = [torch.empty((T, N), dtype=torch.float16, device="cuda") for _ in range(nm)]
+
+        def run(i):
+            blk = mats[i % copies]
+            if args.op == "w4a16":
+                q.qlin_w4a16_gemm(x, *blk[0], ys[0])
+            else:
+                q.qlin_w4a16_gemm_grouped(x, [b[0] for b in blk], [b[1] for b in blk], [b[2] for b in blk], ys)
+        return run
+
+    if args.op == "int8_quant":
+        xs = [randn((T, K), torch.float16) for _ in range(copies)]
+        qa = torch.empty((T, K), dtype=torch.int8, device="cuda")
+        sa = torch.empty(T, dtype=torch.float32, device="cuda")
+        return lambda i: q.qlin_quant_act_int8(xs[i % copies], qa, sa)
+
+    if args.op == "w8a8":
+        a = torch.randint(-127, 128, (T, K), dtype=torch.int8, device="cuda", generator=g)
+        sa = torch.rand(T, device="cuda", generator=g) * 0.01 + 0.001
+        bs = [torch.randint(-127, 128, (N, K), dtype=torch.int8, device="cuda", generator=g) for _ in range(copies)]
+        sb = torch.rand(N, device="cuda", generator=g) * 0.01 + 0.001
+        out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+        return lambda i: q.qlin_w8a8_gemm(a, bs[i % copies], sa, sb, out)
+
+    if args.op in ("nvfp4_quant", "nvfp4_gemm"):
+        S = args.S
+        Kin = K if args.op == "nvfp4_quant" else K - S
+        gx = torch.empty(1, dtype=torch.float32, device="cuda")
+        perm = torch.randperm(Kin, generator=torch.Generator().manual_seed(args.seed)).to(torch.int32).cuda()
+
+        def quantize(rows, x):
+            qc = torch.empty((rows, (Kin + S) // 2), dtype=torch.uint8, device="cuda")
+            sf = torch.empty(q.qlin_nvfp4_sf_bytes(rows, Kin + S, q.QLIN_SF_MMA), dtype=torch.uint8, device="cuda")
+            gg = torch.empty(1, dtype=torch.float32, device="cuda")
+            q.qlin_nvfp4_global_scale(x, gg)
+            q.qlin_quant_nvfp4(x, gg, qc, sf, perm=perm, S=S, sf_layout=q.QLIN_SF_MMA)
+            return qc, sf, gg
+
+        if args.op == "nvfp4_quant":
+            xs = [randn((T, Kin), torch.float16) for _ in range(copies)]
+            q.qlin_nvfp4_global_scale(xs[0], gx)
+            qc = torch.empty((T, (Kin + S) // 2), dtype=torch.uint8, device="cuda")
+            sf = torch.empty(q.qlin_nvfp4_sf_bytes(T, Kin + S, q.QLIN_SF_MMA), dtype=torch.uint8, device="cuda")
+            return lambda i: q.qlin_quant_nvfp4(xs[i % copies], gx, qc, sf, perm=perm, S=S,
+                                                sf_layout=q.QLIN_SF_MMA)
+        qa, sfa, ga = quantize(T, randn((T, Kin), torch.float16))
+        ws = [quantize(N, randn((N, Kin), torch.float16) * 0.02) for _ in range(copies)]
+        out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+        return lambda i: q.qlin_nvfp4_gemm(qa, sfa, ws[i % copies][0], ws[i % copies][1], ga, ws[i % copies][2], out)
+
+    raise ValueError(args.op)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("op", choices=["w4a16", "w4a16_group", "int8_quant", "w8a8", "nvfp4_quant", "nvfp4_gemm"])
+    ap.add_argument("--T", type=int, default=1)
+    ap.add_argument("--N", type=int, default=4096)
+    ap.add_argument("--K", type=int, default=4096)
+    ap.add_argument("--S", type=int, default=128, help="NVFP4 residual channels (K includes them for nvfp4_gemm)")
+    ap.add_argument("--groups", type=int, default=3, help="matrices per w4a16_group launch")
+    ap.add_argument("--copies", type=int, default=4, help="weight copies rotated over the launches")
+    ap.add_argument("--reps", type=int, default=4, help="launches")
+    ap.add_argument("--seed", type=int, default=0)
+    args = ap.parse_args(argv)
+
+    import torch
+    import quantized_linear_layer_gb300 as q
+    q.build()
+    run = _setup(args, q, torch)
+    for i in range(args.reps):
+        run(i)
+    torch.cuda.synchronize()
+    err = q.qlin_get_device_error()
+    if err != 0:
+        print("device error word %#x" % err, file=sys.stderr)
+        return 1
+    print("%s: %d launches ok" % (args.op, args.reps))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
