@@ -154,6 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
     if (lane == 0) {
       tc::prefetch_tmap(&tmA);
       tc::prefetch_tmap(&tmB);
+      // the operands may come from the previous kernel in the stream
+      // (programmatic dependent launch: this grid may start before it ends)
+      pdl_wait();
       int it = 0, issued = 0;
       for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
         int mt, nt;
@@ -277,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
     // ---------------- epilogue ----------------
     const int q = warp & 3;                      // TMEM lane quadrant this warp may access
     const int half = (warp - 2) / 4;             // column half of the 256-column tile
+    pdl_wait();  // the global scales may come from the previous kernel
     const float alpha = __ldg(g_a) * __ldg(g_b);
     for (int ti = 0; ti < my_tiles; ++ti) {
       bool ok = tc::mbar_wait(acc_full, ti & 1, err, kSiteAccFull);
@@ -374,10 +378,20 @@ cudaError_t launch_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_
   if (st != cudaSuccess) return st;
   const int64_t tiles = ((T + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-  nvfp4_gemm_kernel<<<grid, kThreads, kSmemTotal, stream>>>(tmA, tmB, sfa, sfb, static_cast<int>(T),
-                                                            static_cast<int>(N), static_cast<int>(K), g_a, g_b, out,
-                                                            static_cast<int>(out_dtype), device_error_word());
-  return cudaGetLastError();
+  // programmatic dependent launch: the prologue (barriers, TMEM, tensor maps)
+  // overlaps the end of the previous kernel (the activation quantizer)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemTotal;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, tmA, tmB, sfa, sfb, static_cast<int>(T), static_cast<int>(N),
+                            static_cast<int>(K), g_a, g_b, out, static_cast<int>(out_dtype), device_error_word());
 }
 
 }  // namespace qlin

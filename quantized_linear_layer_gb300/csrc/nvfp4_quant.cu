@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __r
                                                                   uint8_t* __restrict__ sf, int sf_mma,
                                                                   int32_t* __restrict__ err) {
   extern __shared__ __align__(16) unsigned char row_smem[];
+  pdl_launch_dependents();  // the GEMM that reads the codes may start setting up
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * R;
   const int nr = static_cast<int>(min(static_cast<int64_t>(R), rows - row0));
   const int tid = threadIdx.x;

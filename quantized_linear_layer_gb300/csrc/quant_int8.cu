@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(kQuantThreads) quant_int8_rows_kernel(const vo
                                                                          int8_t* __restrict__ q,
                                                                          float* __restrict__ scale,
                                                                          int32_t* __restrict__ azp) {
+  pdl_launch_dependents();  // the GEMM that reads the codes may start setting up
   const int64_t row = blockIdx.x;
   const int tid = threadIdx.x;
   const int nvec = K / 8;

@@ -218,6 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
     if (lane == 0) {
       tc::prefetch_tmap(&tmA);
       tc::prefetch_tmap(&tmB);
+      // the operands may come from the previous kernel in the stream
+      // (programmatic dependent launch: this grid may start before it ends)
+      pdl_wait();
       int it = 0, issued = 0;
       for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
         int mt, nt;
@@ -371,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    pdl_wait();  // the scales and zero-points may come from the previous kernel
     const bool per_tensor_adj = epi.azp == nullptr && epi.azp_adj != nullptr;
     int g = 0;
     bool ok = true;
@@ -509,9 +513,20 @@ cudaError_t launch_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_
   epi.out_dtype = e.out_dtype;
   const int64_t tiles = ((T + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-  w8a8_gemm_kernel<<<grid, kThreads, kSmemTotal, stream>>>(tmA, tmB, static_cast<int>(T), static_cast<int>(N),
-                                                           static_cast<int>(K), epi, out, device_error_word());
-  return cudaGetLastError();
+  // programmatic dependent launch: the prologue (barriers, TMEM, tensor maps)
+  // overlaps the end of the previous kernel (the activation quantizer)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemTotal;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w8a8_gemm_kernel, tmA, tmB, static_cast<int>(T), static_cast<int>(N),
+                            static_cast<int>(K), epi, out, device_error_word());
 }
 
 }  // namespace qlin
