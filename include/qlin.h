@@ -364,6 +364,45 @@ qlin_status qlin_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t*
                             int64_t T, int64_t N, int64_t K, const float* g_a, const float* g_b, void* out,
                             qlin_dtype out_dtype, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * next 1 - FP8 W8A8: per-row E4M3 quantization
+ *
+ * Per row r (a token of the activations, or an output channel of the
+ * weights): s_r = max_k |x[r,k]| / 448 in float32 (s_r = 1 for an all-zero
+ * row), q[r,k] = E4M3(x[r,k] / s_r) with x / s_r an IEEE float32 division
+ * and the E4M3-FN encode rounding to nearest, ties to even, saturating at
+ * 448 ("LLM and AIGC quantization", "W4A4, FP8 and block-scaled formats": x/s
+ * is converted to E4M3 instead of rounded to INT8, activations per token and
+ * weights per channel; "FP8: robustness from dynamic range": the per-tensor
+ * example [0.6, -45.0, 1.1, -0.8] -> 6, -448, 11, -8).
+ *   x      [rows][K] of x_dtype (16-byte aligned; K a multiple of 8)
+ *   q      out, uint8 [rows][K]: E4M3-FN codes (sign in bit 7)
+ *   scale  out, float32 [rows]
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_quant_fp8(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, uint8_t* q, float* scale,
+                           cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * next 1 - FP8 W8A8 GEMM on the tcgen05 tensor cores (kind::f8f6f4)
+ *
+ * out[t,n] = s_a[t] . s_b[n] . sum_k dec(a[t,k]) . dec(b[n,k]) + bias[n]
+ * with E4M3 operands, fp32 accumulation in the tensor core and the two scales
+ * and the bias applied once in the epilogue, in float32, one final rounding
+ * ("LLM and AIGC quantization", "W4A4, FP8 and block-scaled formats": the
+ * FP8 tensor core multiplies, FP32 accumulates, the epilogue multiplies by
+ * both scales).
+ *   a        uint8 [T][K]  E4M3 codes of the activations (per-token scales)
+ *   b        uint8 [N][K]  E4M3 codes of the weights (per-channel scales)
+ *   scale_a  float32 [T];  scale_b float32 [N]
+ *   bias     [N] of bias_dtype (F16, BF16 or F32), or NULL for 0
+ *   out      [T][N] of out_dtype (F16 or BF16)
+ * a and b 16-byte aligned; K a multiple of 16 (rows of whole 16-byte
+ * pieces); codes 0x7F / 0xFF (NaN) are not valid inputs.
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_fp8_gemm(const uint8_t* a, const uint8_t* b, int64_t T, int64_t N, int64_t K, const float* scale_a,
+                          const float* scale_b, const void* bias, qlin_dtype bias_dtype, void* out,
+                          qlin_dtype out_dtype, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -49,6 +49,8 @@ from .quant import (  # noqa: F401
     quant_int8_sym,
     quant_int8_asym,
     quant_w4_g128,
+    quant_fp8_rows,
+    quant_fp8_tensor,
     nvfp4_global_scale,
     nvfp4_quantize,
     nvfp4_dequantize,
@@ -63,4 +65,5 @@ from .gemm import (  # noqa: F401
     azp_adj_from_weight,
     w8a8_epilogue,
     nvfp4_gemm_reference,
+    fp8_gemm_reference,
 )

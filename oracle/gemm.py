@@ -9,6 +9,9 @@ matrix product.  Integer GEMMs are exact.
 * w4a16_reference - Y = X . (s (q - z))^T with one scale and zero-point per
   group of consecutive K elements ("Chapter 9 - Quantization kernels",
   section 9.5 dequant-fused GEMM; "LLM and AIGC quantization", section W4A16).
+* fp8_gemm_reference - FP8 W8A8: E4M3 operands decoded exactly, one
+  product, then s_a[t] . s_b[n] (+ bias) ("LLM and AIGC quantization",
+  "W4A4, FP8 and block-scaled formats", the FP8 W8A8 item).
 * int8_gemm_exact - D^ = A^ . B^^T with int32 accumulation ("LLM and AIGC
   quantization", W8A8 section: a single product is at most 127^2 = 16129 and
   a K = 4096 sum reaches 6.6e7, so the accumulator must be int32).
@@ -28,7 +31,7 @@ permutation invariance and S = 0 of the augmented GEMM).
 
 import numpy as np
 
-from .formats import unpack_u4
+from .formats import e4m3_decode, unpack_u4
 from .quant import nvfp4_dequantize
 
 
@@ -105,3 +108,18 @@ def nvfp4_gemm_reference(qa, sfa, ga, qb, sfb, gb):
     a = nvfp4_dequantize(qa, sfa, ga)
     b = nvfp4_dequantize(qb, sfb, gb)
     return a @ b.T
+
+
+def fp8_gemm_reference(qa, sa, qb, sb, bias=None):
+    """float64 Y [T][N] = sa[t] . sb[n] . sum_k dec(qa[t,k]) . dec(qb[n,k]) (+ bias[n])
+    for E4M3 codes qa [T][K], qb [N][K] and float32 scales sa [T], sb [N]
+    ("LLM and AIGC quantization", "W4A4, FP8 and block-scaled formats": FP8
+    products accumulated in high precision, both scales applied after the
+    sum).  The decoded products have at most 8 significant bits and the sums
+    stay within 53, so the float64 contraction is exact."""
+    a = e4m3_decode(qa)
+    b = e4m3_decode(qb)
+    y = (a @ b.T) * np.asarray(sa, dtype=np.float64)[:, None] * np.asarray(sb, dtype=np.float64)[None, :]
+    if bias is not None:
+        y = y + np.asarray(bias, dtype=np.float64)[None, :]
+    return y

@@ -27,6 +27,12 @@ Functions and the passages they follow:
   decoded scale and rounded to the nearest E2M1 value ("LLM and AIGC
   quantization", "Block-scaled formats", the 16-element NVFP4 example), with
   a per-tensor fp32 second-level scale.
+* quant_fp8_rows / quant_fp8_tensor - FP8 W8A8: x / s converted to E4M3
+  instead of rounded to an integer, s = max|x| / 448 per token (activations)
+  or per output channel (weights), or one scale per tensor ("LLM and AIGC
+  quantization", "W4A4, FP8 and block-scaled formats": the FP8 W8A8 item;
+  "FP8: robustness from dynamic range": the per-tensor worked example
+  [0.6, -45.0, 1.1, -0.8] -> 6, -448, 11, -8).
 * arc_perm / arc_quantize_activation / arc_quantize_weight - ARCQuant
   residual-channel augmentation ("NVFP4 quantization and ARCQuant",
   sections 2.1 and 2.2): reorder channels by magnitude, quantize, re-quantize
@@ -48,6 +54,11 @@ notes):
   land in E4M3 range (the pages' example sets it to 1); a block whose decoded
   scale d = dec(s) * g is 0 gets all-zero codes; the residual of the ARCQuant
   channels uses the same g as the main part.
+* quant_fp8_*: the scale maps the largest magnitude onto the largest finite
+  E4M3 value, s = max|x| / 448 (the pages print the codes of their example,
+  which this scale reproduces, not the formula); an all-zero row or tensor
+  uses s = 1; x / s is a float32 division, then the E4M3 encode (nearest,
+  ties to even, saturating).
 * arc_perm: calibration statistic = max over rows of |X| per channel, taken
   on X itself; channels sorted by descending statistic, ties by ascending
   channel index.
@@ -218,3 +229,24 @@ def arc_quantize_weight(w, perm, s_res, g):
         return q, sf
     return (np.concatenate([q, q[:, :s_res]], axis=1),
             np.concatenate([sf, sf[:, : s_res // 16]], axis=1))
+
+
+def quant_fp8_rows(x):
+    """Per-row FP8 E4M3.  x: float32 [rows][K] -> (codes uint8 [rows][K], s float32 [rows]).
+
+    s = max|x| / 448 in float32 (1 for an all-zero row); codes = E4M3(x / s)
+    with x / s a float32 division.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x).max(axis=1)
+    s = (a / F32(448.0)).astype(np.float32)
+    s = np.where(a == 0, F32(1.0), s).astype(np.float32)
+    return e4m3_encode(x / s[:, None]), s
+
+
+def quant_fp8_tensor(x):
+    """Per-tensor FP8 E4M3: one scale max|x| / 448 for the whole array."""
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x).max() if x.size else F32(0.0)
+    s = F32(1.0) if a == 0 else F32(a / F32(448.0))
+    return e4m3_encode(x / s), s

@@ -63,6 +63,8 @@ _SIGS = {
     "qlin_nvfp4_sf_bytes": ([_I64, _I64, _I32], _I64),
     "qlin_nvfp4_sf_to_mma": ([_P, _I64, _I64, _P, _P], _I32),
     "qlin_nvfp4_gemm": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P], _I32),
+    "qlin_quant_fp8": ([_P, _I32, _I64, _I64, _P, _P, _P], _I32),
+    "qlin_fp8_gemm": ([_P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
 }
 
 _lib = None
@@ -330,3 +332,29 @@ def qlin_nvfp4_gemm(a, sfa, b, sfb, g_a, g_b, out, stream=None):
     n = b.shape[0]
     _check("qlin_nvfp4_gemm", lib().qlin_nvfp4_gemm(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), t, n, k, _ptr(g_a),
                                                    _ptr(g_b), _ptr(out), _dtype_code(out), _stream(stream)))
+
+
+def qlin_quant_fp8(x, q, scale, stream=None):
+    """Per-row FP8 E4M3 quantization of x [rows][K]: q uint8 [rows][K] (E4M3-FN
+    codes), scale float32 [rows] = max|x| / 448 per row."""
+    torch = _torch()
+    _need(x, torch.float16, torch.bfloat16, torch.float32, name="x"); _need(q, torch.uint8, name="q")
+    _need(scale, torch.float32, name="scale")
+    rows, k = x.shape
+    _check("qlin_quant_fp8", lib().qlin_quant_fp8(_ptr(x), _dtype_code(x), rows, k, _ptr(q), _ptr(scale),
+                                                 _stream(stream)))
+
+
+def qlin_fp8_gemm(a, b, scale_a, scale_b, out, bias=None, stream=None):
+    """out [T][N] = scale_a[t] scale_b[n] (dec(a) . dec(b)^T) + bias for E4M3 codes
+    a uint8 [T][K], b uint8 [N][K]; out fp16 or bf16."""
+    torch = _torch()
+    _need(a, torch.uint8, name="a"); _need(b, torch.uint8, name="b")
+    _need(scale_a, torch.float32, name="scale_a"); _need(scale_b, torch.float32, name="scale_b")
+    _need(bias, torch.float16, torch.bfloat16, torch.float32, name="bias")
+    _need(out, torch.float16, torch.bfloat16, name="out")
+    t, k = a.shape
+    n = b.shape[0]
+    bias_dt = QLIN_F16 if bias is None else _dtype_code(bias)
+    _check("qlin_fp8_gemm", lib().qlin_fp8_gemm(_ptr(a), _ptr(b), t, n, k, _ptr(scale_a), _ptr(scale_b), _ptr(bias),
+                                               bias_dt, _ptr(out), _dtype_code(out), _stream(stream)))

@@ -422,4 +422,40 @@ qlin_status qlin_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t*
   QLIN_LAUNCH(launch_nvfp4_gemm(a, sfa, b, sfb, T, N, K, g_a, g_b, out, out_dtype, stream), "nvfp4_gemm launch");
 }
 
+qlin_status qlin_quant_fp8(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, uint8_t* q, float* scale,
+                           cudaStream_t stream) {
+  QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");
+  QLIN_REQUIRE(rows >= 0 && rows <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG,
+               "bad sizes rows=%lld K=%lld", (long long)rows, (long long)K);
+  QLIN_REQUIRE(K % 16 == 0, QLIN_ERR_ALIGNMENT, "K=%lld is not a multiple of 16", (long long)K);
+  if (rows == 0) return ok();
+  QLIN_REQUIRE(x && q && scale, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(x) && aligned16(q), QLIN_ERR_ALIGNMENT, "x and q must be 16-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(scale) & 3u) == 0, QLIN_ERR_ALIGNMENT, "scale must be 4-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_quant_fp8(x, x_dtype, rows, K, q, scale, stream), "quant_fp8 launch");
+}
+
+qlin_status qlin_fp8_gemm(const uint8_t* a, const uint8_t* b, int64_t T, int64_t N, int64_t K, const float* scale_a,
+                          const float* scale_b, const void* bias, qlin_dtype bias_dtype, void* out,
+                          qlin_dtype out_dtype, cudaStream_t stream) {
+  QLIN_REQUIRE(T >= 0 && T <= kMaxDim && N >= 0 && N <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG,
+               "bad sizes T=%lld N=%lld K=%lld", (long long)T, (long long)N, (long long)K);
+  QLIN_REQUIRE(K % 16 == 0, QLIN_ERR_ALIGNMENT, "K=%lld is not a multiple of 16", (long long)K);
+  QLIN_REQUIRE(out_dtype == QLIN_F16 || out_dtype == QLIN_BF16, QLIN_ERR_INVALID_ARG, "out_dtype must be F16 or BF16");
+  QLIN_REQUIRE(bias == nullptr || is_float_dtype(bias_dtype), QLIN_ERR_INVALID_ARG,
+               "bias_dtype must be F16, BF16 or F32");
+  if (T == 0 || N == 0) return ok();
+  QLIN_REQUIRE(a && b && scale_a && scale_b && out, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(a) && aligned16(b) && aligned16(out), QLIN_ERR_ALIGNMENT,
+               "a, b and out must be 16-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(scale_a) & 3u) == 0 && (reinterpret_cast<uintptr_t>(scale_b) & 3u) == 0,
+               QLIN_ERR_ALIGNMENT, "scale_a and scale_b must be 4-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(bias) & 3u) == 0, QLIN_ERR_ALIGNMENT, "bias must be 4-byte aligned");
+  QLIN_REQUIRE((N * 2) % 16 == 0, QLIN_ERR_ALIGNMENT, "the out row pitch (2N bytes) must be a multiple of 16");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_fp8_gemm(a, b, T, N, K, scale_a, scale_b, bias, bias_dtype, out, out_dtype, stream),
+              "fp8_gemm launch");
+}
+
 }  // extern "C"

@@ -1,6 +1,7 @@
 // Per-token int8 activation quantization (symmetric absmax or asymmetric with
 // an integer zero-point), the int8 row sum used as the W8A8 zero-point
-// adjustment, and the asymmetric 4-bit group weight quantizer.
+// adjustment, the asymmetric 4-bit group weight quantizer, and the per-row
+// FP8 E4M3 quantizer of FP8 W8A8.
 //
 // Symmetric: s = max|x| / 127, q = clamp(rint(x / s), -127, 127)
 //   ("LLM and AIGC quantization: from number formats to W4A4", symmetric
@@ -8,6 +9,12 @@
 // Asymmetric: the row range [min(x,0), max(x,0)] is mapped onto [-128, 127]
 //   with an integer zero-point z so that 0 is exact; q = round(x/s) + z
 //   ("Chapter 9 - Quantization kernels", 9.2: zero-point added on quantize).
+// FP8 E4M3, per token or per output channel: s = max|x| / 448 (1 for an
+//   all-zero row), q = E4M3(x / s), nearest, ties to even, saturating
+//   ("LLM and AIGC quantization", "W4A4, FP8 and block-scaled formats": x/s
+//   converted to E4M3 instead of rounded to INT8; "FP8: robustness from
+//   dynamic range": the per-tensor example [0.6, -45.0, 1.1, -0.8] -> 6, -448,
+//   11, -8, whose printed quotients this scale reproduces).
 // 4-bit weights: s = fp16(max(max - min, 1e-5) / 15), z = rint(-min / s),
 //   q = clamp(rint(w / s) + z, 0, 15) per 128-element group (the AWQ offline
 //   flow's pseudo_quant on the same page).
@@ -124,6 +131,91 @@ __global__ void __launch_bounds__(kQuantThreads) quant_int8_rows_kernel(const vo
   }
 }
 
+// Two floats -> two E4M3-FN codes in one 16-bit word, `lo` in bits 0-7
+// (hardware round-to-nearest-even, saturating at 448).
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// One CTA per row, the same shape as the int8 quantizer: 16-byte loads kept
+// in registers, block absmax, then IEEE division and the E4M3 encode.
+template <int DT>
+__global__ void __launch_bounds__(kQuantThreads) quant_fp8_rows_kernel(const void* __restrict__ x, int K,
+                                                                      uint8_t* __restrict__ q,
+                                                                      float* __restrict__ scale) {
+  pdl_launch_dependents();  // the GEMM that reads the codes may start setting up
+  const int64_t row = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nvec = K / 8;
+  const char* xr = static_cast<const char*>(x) + row * (int64_t)K * elem_bytes<DT>();
+  uint8_t* qr = q + row * (int64_t)K;
+
+  float v[kMaxVecPerThread][8];
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kMaxVecPerThread; ++i) {
+    const int idx = tid + i * kQuantThreads;
+    if (idx < nvec) {
+      Vec8Loader<DT>::load(xr + (int64_t)idx * 8 * elem_bytes<DT>(), v[i]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[i][j]));
+    }
+  }
+  for (int idx = tid + kMaxVecPerThread * kQuantThreads; idx < nvec; idx += kQuantThreads) {
+    float t[8];
+    Vec8Loader<DT>::load(xr + (int64_t)idx * 8 * elem_bytes<DT>(), t);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(t[j]));
+  }
+  __shared__ float red[kQuantThreads / 32];
+  __shared__ float s_scale;
+  m = warp_max(m);
+  if ((tid & 31) == 0) red[tid >> 5] = m;
+  __syncthreads();
+  if (tid == 0) {
+    float a = red[0];
+    for (int w = 1; w < kQuantThreads / 32; ++w) a = fmaxf(a, red[w]);
+    const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+    s_scale = s;
+    scale[row] = s;
+  }
+  __syncthreads();
+  const float s = s_scale;
+  // x / s through the correctly rounded reciprocal and one FMA correction
+  // (the IEEE quotient wherever it can change the code; quotients below the
+  // normal range encode to a signed zero either way)
+  const float rs = __frcp_rn(s);
+  const bool rcp_ok = rcp_division_ok(s, rs);
+  auto quant8 = [&](const float* t, int64_t idx) {
+    uint32_t w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float a0 = t[4 * h + 2 * j], a1 = t[4 * h + 2 * j + 1];
+        const uint32_t pair = f32x2_to_e4m3x2(rcp_ok ? div_by_rcp(a0, s, rs) : __fdiv_rn(a0, s),
+                                              rcp_ok ? div_by_rcp(a1, s, rs) : __fdiv_rn(a1, s));
+        if (j == 0) lo = pair; else hi = pair;
+      }
+      w[h] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint2*>(qr + idx * 8) = make_uint2(w[0], w[1]);
+  };
+#pragma unroll
+  for (int i = 0; i < kMaxVecPerThread; ++i) {
+    const int idx = tid + i * kQuantThreads;
+    if (idx < nvec) quant8(v[i], idx);
+  }
+  for (int idx = tid + kMaxVecPerThread * kQuantThreads; idx < nvec; idx += kQuantThreads) {
+    float t[8];
+    Vec8Loader<DT>::load(xr + (int64_t)idx * 8 * elem_bytes<DT>(), t);
+    quant8(t, idx);
+  }
+}
+
 // azp_adj[n] = sum_k b[n,k]: one warp per row, 16 bytes per lane per step.
 __global__ void int8_row_sum_kernel(const int8_t* __restrict__ b, int64_t N, int K, int32_t* __restrict__ out) {
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
@@ -214,6 +306,19 @@ cudaError_t launch_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, 
       if (asym) quant_int8_rows_kernel<2, true><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
       else quant_int8_rows_kernel<2, false><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
       break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_fp8(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, uint8_t* q, float* scale,
+                             cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>(rows)), block(kQuantThreads);
+  const int k = static_cast<int>(K);
+  switch (x_dtype) {
+    case QLIN_F16: quant_fp8_rows_kernel<0><<<grid, block, 0, stream>>>(x, k, q, scale); break;
+    case QLIN_BF16: quant_fp8_rows_kernel<1><<<grid, block, 0, stream>>>(x, k, q, scale); break;
+    default: quant_fp8_rows_kernel<2><<<grid, block, 0, stream>>>(x, k, q, scale); break;
   }
   return cudaGetLastError();
 }

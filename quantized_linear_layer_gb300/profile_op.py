@@ -11,6 +11,8 @@ Operations (sizes as flags):
   w8a8         qlin_w8a8_gemm, A [T][K] int8, B [N][K] int8, per-token / per-channel scales, bf16 out
   nvfp4_quant  qlin_quant_nvfp4, X [T][K] fp16 with S residual channels, MMA scale layout
   nvfp4_gemm   qlin_nvfp4_gemm, A [T][K] and B [N][K] NVFP4 (made by the quantizer), bf16 out
+  fp8_quant    qlin_quant_fp8, X [T][K] fp16, per-row E4M3
+  fp8_gemm     qlin_fp8_gemm, A [T][K] and B [N][K] E4M3 (made by the quantizer), bias, bf16 out
 
 Every launch reads its own copy of the weights (--copies of them, rotated), so
 that weight streams come from HBM as they do in a model; the launches run
@@ -92,12 +94,32 @@ def _setup(args, q, torch):
         out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
         return lambda i: q.qlin_nvfp4_gemm(qa, sfa, ws[i % copies][0], ws[i % copies][1], ga, ws[i % copies][2], out)
 
+    if args.op == "fp8_quant":
+        xs = [randn((T, K), torch.float16) for _ in range(copies)]
+        qc = torch.empty((T, K), dtype=torch.uint8, device="cuda")
+        sc = torch.empty(T, dtype=torch.float32, device="cuda")
+        return lambda i: q.qlin_quant_fp8(xs[i % copies], qc, sc)
+
+    if args.op == "fp8_gemm":
+        def quantize(rows, x):
+            qc = torch.empty((rows, K), dtype=torch.uint8, device="cuda")
+            sc = torch.empty(rows, dtype=torch.float32, device="cuda")
+            q.qlin_quant_fp8(x, qc, sc)
+            return qc, sc
+
+        qa, sa = quantize(T, randn((T, K), torch.float16))
+        ws = [quantize(N, randn((N, K), torch.float16) * 0.02) for _ in range(copies)]
+        bias = randn((N,), torch.float16)
+        out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+        return lambda i: q.qlin_fp8_gemm(qa, ws[i % copies][0], sa, ws[i % copies][1], out, bias=bias)
+
     raise ValueError(args.op)
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("op", choices=["w4a16", "w4a16_group", "int8_quant", "w8a8", "nvfp4_quant", "nvfp4_gemm"])
+    ap.add_argument("op", choices=["w4a16", "w4a16_group", "int8_quant", "w8a8", "nvfp4_quant", "nvfp4_gemm",
+                                   "fp8_quant", "fp8_gemm"])
     ap.add_argument("--T", type=int, default=1)
     ap.add_argument("--N", type=int, default=4096)
     ap.add_argument("--K", type=int, default=4096)

@@ -101,6 +101,16 @@ def test_rejects_bad_arguments_without_gpu(built):
     st[0].K, st[0].count = 256, 5
     assert L.qlin_w4a16_gemv_sequence(sp, 1, 128, P(16), None) == 1      # count above 4
     assert L.qlin_w4a16_gemv_sequence(None, 0, 128, None, None) == 0     # empty sequence
+    # FP8: K not a multiple of 16, bad dtype, misaligned x; GEMM out dtype, bias dtype,
+    # misaligned b, out row pitch (N = 12: 24 bytes)
+    assert L.qlin_quant_fp8(P(16), 0, 4, 40, P(16), P(16), None) == 2
+    assert L.qlin_quant_fp8(P(16), 3, 4, 64, P(16), P(16), None) == 1
+    assert L.qlin_quant_fp8(P(24), 0, 4, 64, P(16), P(16), None) == 2
+    assert L.qlin_fp8_gemm(P(16), P(16), 4, 8, 64, P(16), P(16), None, 0, P(16), 2, None) == 1
+    assert L.qlin_fp8_gemm(P(16), P(16), 4, 8, 64, P(16), P(16), P(16), 3, P(16), 0, None) == 1
+    assert L.qlin_fp8_gemm(P(16), P(24), 4, 8, 64, P(16), P(16), None, 0, P(16), 0, None) == 2
+    assert L.qlin_fp8_gemm(P(16), P(16), 4, 12, 64, P(16), P(16), None, 0, P(16), 0, None) == 2
+    assert L.qlin_fp8_gemm(P(16), P(16), 4, 8, 72, P(16), P(16), None, 0, P(16), 0, None) == 2
     # perm K limit
     assert L.qlin_arc_perm(P(16), 0, 4, 32768, P(16), None) == 1
     msg = L.qlin_last_error_message()
@@ -117,3 +127,5 @@ def test_empty_problems_launch_nothing(built):
     assert L.qlin_quant_act_int8(None, 0, 0, 64, None, None, None, None) == 0
     assert L.qlin_w8a8_gemm(None, None, 0, 8, 64, None, 1, None, 1, None, None, None, 0, None, 0, None) == 0
     assert L.qlin_nvfp4_gemm(None, None, None, None, 4, 0, 64, None, None, None, 1, None) == 0
+    assert L.qlin_quant_fp8(None, 0, 0, 64, None, None, None) == 0
+    assert L.qlin_fp8_gemm(None, None, 0, 8, 64, None, None, None, 0, None, 0, None) == 0

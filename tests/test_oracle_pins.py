@@ -537,6 +537,87 @@ def test_nvfp4_gemm_brute_force():
 # Planted mistakes: each must make at least one pin fail
 # --------------------------------------------------------------------------
 
+
+# ---- FP8 W8A8 (E4M3 per tensor / per token / per channel) ----
+
+def _e4m3_value(code):
+    """E4M3-FN value from the bit fields (S.EEEE.MMM, bias 7), written out here
+    independently of the oracle's table."""
+    code = int(code)
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 7
+    return sign * ((m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7))
+
+
+def pin_fp8_per_tensor_example():
+    g = load_golden("fp8_w8a8_example.json")
+    x = np.array(g["x"], dtype=np.float32)
+    q, s = oracle.quant_fp8_tensor(x)
+    dec = oracle.e4m3_decode(q)
+    quot = x.astype(np.float64) / np.float64(s)
+    # the printed quotients (two decimals) and their printed E4M3 roundings
+    for printed, code in g["printed_roundings"]:
+        i = int(np.argmin(np.abs(quot - printed)))
+        assert abs(quot[i] - printed) <= 0.005, (quot[i], printed)
+        assert dec[i] == code
+    # every element within half of the printed spacing of its interval; the
+    # largest magnitude lands on the E4M3 maximum
+    for lo, hi, step in g["printed_spacing"]:
+        inside = (np.abs(quot) >= lo) & (np.abs(quot) <= hi)
+        assert np.all(np.abs(dec[inside] - quot[inside]) <= step / 2 + 1e-9)
+    assert np.max(np.abs(dec)) == g["e4m3_max"]
+    assert np.all(np.sign(dec) == np.sign(x))
+
+
+def test_fp8_per_tensor_example():
+    pin_fp8_per_tensor_example()
+
+
+def pin_fp8_rows_properties():
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((64, 256)) * np.exp(rng.uniform(-6, 6, size=(64, 1)))).astype(np.float32)
+    x[3] = 0.0
+    x[5, 7] = 300.0
+    q, s = oracle.quant_fp8_rows(x)
+    dec = oracle.e4m3_decode(q)
+    assert s[3] == 1.0 and np.all(dec[3] == 0)
+    nz = np.abs(x).max(axis=1) > 0
+    assert np.all(np.abs(dec[nz]).max(axis=1) == 448.0)
+    # three mantissa bits: at most 1/16 relative error in the normal range
+    quot = np.abs(x.astype(np.float64) / s[:, None])
+    normal = quot >= 2.0 ** -6
+    err = np.abs(dec * s[:, None].astype(np.float64) - x)
+    assert np.all(err[normal] <= np.abs(x[normal]) / 16 * (1 + 1e-6))
+    for r in (0, 5, 40):
+        q1, s1 = oracle.quant_fp8_tensor(x[r])
+        assert s1 == s[r] and np.array_equal(q1, q[r])
+
+
+def test_fp8_rows_properties():
+    pin_fp8_rows_properties()
+
+
+def pin_fp8_gemm_brute_force():
+    rng = np.random.default_rng(12)
+    T, N, K = 3, 4, 37
+    qa = rng.integers(0, 256, size=(T, K)).astype(np.uint8)
+    qb = rng.integers(0, 256, size=(N, K)).astype(np.uint8)
+    qa[(qa & 0x7F) == 0x7F] = 0x10
+    qb[(qb & 0x7F) == 0x7F] = 0x91
+    sa = rng.uniform(0.01, 1.0, size=T).astype(np.float32)
+    sb = rng.uniform(0.01, 1.0, size=N).astype(np.float32)
+    bias = rng.standard_normal(N).astype(np.float32)
+    y = oracle.fp8_gemm_reference(qa, sa, qb, sb, bias)
+    for t in range(T):
+        for n in range(N):
+            acc = sum(_e4m3_value(qa[t, k]) * _e4m3_value(qb[n, k]) for k in range(K))
+            want = acc * float(sa[t]) * float(sb[n]) + float(bias[n])
+            assert abs(y[t, n] - want) <= 1e-12 * (1 + abs(want)), (t, n, y[t, n], want)
+
+
+def test_fp8_gemm_brute_force():
+    pin_fp8_gemm_brute_force()
+
 def _mut_e2m1_ties_odd(monkeypatch):
     orig = ofmt._nearest_code
 
@@ -604,8 +685,27 @@ def _mut_sym_qmax(monkeypatch):
     return pin_granularity
 
 
+def _mut_fp8_scale_447(monkeypatch):
+    def bad(x):
+        x = np.asarray(x, dtype=np.float32)
+        a = np.abs(x).max()
+        s = np.float32(1.0) if a == 0 else np.float32(a / np.float32(447.0))
+        return oracle.e4m3_encode(x / s), s
+
+    monkeypatch.setattr(oracle, "quant_fp8_tensor", bad)
+    return pin_fp8_per_tensor_example
+
+
+def _mut_fp8_scales_swapped(monkeypatch):
+    orig = ogemm.fp8_gemm_reference
+    monkeypatch.setattr(oracle, "fp8_gemm_reference",
+                        lambda qa, sa, qb, sb, bias=None: orig(qa, np.resize(sb, sa.shape), qb, np.resize(sa, sb.shape), bias))
+    return pin_fp8_gemm_brute_force
+
+
 MUTATIONS = [_mut_e2m1_ties_odd, _mut_azp_sign, _mut_azp_adj_axis, _mut_residual_sign,
-             _mut_w8a8_transposed, _mut_w4_zero_dropped, _mut_nvfp4_scale_not_decoded, _mut_sym_qmax]
+             _mut_w8a8_transposed, _mut_w4_zero_dropped, _mut_nvfp4_scale_not_decoded, _mut_sym_qmax,
+             _mut_fp8_scale_447, _mut_fp8_scales_swapped]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
