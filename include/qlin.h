@@ -85,6 +85,11 @@ typedef enum {
   QLIN_SF_MMA = 1
 } qlin_sf_layout;
 
+typedef enum {
+  QLIN_QFMT_INT8 = 0,     /* symmetric int8, codes in [-127, 127], s = max|y| / 127 */
+  QLIN_QFMT_FP8_E4M3 = 1  /* E4M3-FN codes, s = max|y| / 448 */
+} qlin_qfmt;
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* qlin_status_string(qlin_status status);
 
@@ -402,6 +407,33 @@ qlin_status qlin_quant_fp8(const void* x, qlin_dtype x_dtype, int64_t rows, int6
 qlin_status qlin_fp8_gemm(const uint8_t* a, const uint8_t* b, int64_t T, int64_t N, int64_t K, const float* scale_a,
                           const float* scale_b, const void* bias, qlin_dtype bias_dtype, void* out,
                           qlin_dtype out_dtype, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * next 2 - RMSNorm fused with the per-token quantizer
+ *
+ * Per row: y = (x . inv) . gamma with inv = 1 / sqrt(mean(x^2) + eps) (one
+ * square root and one division per row; a row whose mean(x^2) + eps is 0
+ * normalizes to 0), then the per-token
+ * quantization of y in `fmt` (int8: s = max|y| / 127, q = clamp(rint(y / s),
+ * -127, 127); E4M3: s = max|y| / 448, q = E4M3(y / s); s = 1 for an all-zero
+ * y), with y kept in float32 and the row read once ("Chapter 9 -
+ * Quantization kernels", practical notes: the per-row max and quantization
+ * fused into the upstream operator; "LLM and AIGC quantization", "Static and
+ * dynamic quantization": the per-token reduction is usually fused into the
+ * preceding RMSNorm).  Every step is one IEEE float32 operation; the mean of
+ * squares is summed in a fixed order so that the result is reproducible: the
+ * row's 8-element chunks c are dealt to 256 partial sums (chunk c to partial
+ * c mod 256), each adds the squares of its chunks in ascending order, element
+ * by element, and the partials meet in a binary tree (i += i + h, h = 128 ...
+ * 1).
+ *   x      [rows][K] of x_dtype (16-byte aligned; K a multiple of 16)
+ *   gamma  [K] of x_dtype (16-byte aligned)
+ *   eps    the RMSNorm epsilon (>= 0)
+ *   q      out, [rows][K] bytes: int8 codes or E4M3-FN codes (16-byte aligned)
+ *   scale  out, float32 [rows]
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_rmsnorm_quant(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const void* gamma,
+                               float eps, qlin_qfmt fmt, void* q, float* scale, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -51,6 +51,9 @@ from .quant import (  # noqa: F401
     quant_w4_g128,
     quant_fp8_rows,
     quant_fp8_tensor,
+    rmsnorm_rows,
+    rmsnorm_quant_int8,
+    rmsnorm_quant_fp8,
     nvfp4_global_scale,
     nvfp4_quantize,
     nvfp4_dequantize,

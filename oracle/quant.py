@@ -33,6 +33,15 @@ Functions and the passages they follow:
   quantization", "W4A4, FP8 and block-scaled formats": the FP8 W8A8 item;
   "FP8: robustness from dynamic range": the per-tensor worked example
   [0.6, -45.0, 1.1, -0.8] -> 6, -448, 11, -8).
+* rmsnorm_rows / rmsnorm_quant_int8 / rmsnorm_quant_fp8 - RMSNorm with the
+  per-token quantization fused into it ("Chapter 9 - Quantization kernels",
+  practical notes: the per-row max and the quantization fused into the
+  upstream operator, vLLM's rms_norm_dynamic_per_token_quant; "LLM and AIGC
+  quantization", "Static and dynamic quantization": the per-token reduction
+  is usually fused into the preceding RMSNorm; "SmoothQuant" inference
+  configuration: the RMSNorm kernel emits per-token quantized output).  The
+  normalized row is y = (x . (1 / sqrt(mean(x^2) + eps))) . gamma, quantized
+  per token by quant_int8_sym or quant_fp8_rows without being rounded first.
 * arc_perm / arc_quantize_activation / arc_quantize_weight - ARCQuant
   residual-channel augmentation ("NVFP4 quantization and ARCQuant",
   sections 2.1 and 2.2): reorder channels by magnitude, quantize, re-quantize
@@ -59,6 +68,19 @@ notes):
   which this scale reproduces, not the formula); an all-zero row or tensor
   uses s = 1; x / s is a float32 division, then the E4M3 encode (nearest,
   ties to even, saturating).
+* rmsnorm_*: RMSNorm is y = (x . inv) . gamma with inv = 1 / sqrt(mean(x^2)
+  + eps), every step a separate float32 operation (square, add, divide by K,
+  add eps, square root, divide 1 by it once per row, then two multiplies per
+  element); the pages fix neither the formula nor eps (it is an argument).
+  A row whose mean(x^2) + eps is 0 (eps = 0 and every square 0 or below the
+  float32 range) normalizes to 0.  The mean of squares is a float32 sum in a
+  fixed order that is part of the operation's definition (so its result is
+  reproducible bit for bit): the row's 8-element chunks c are dealt to 256
+  partial sums, chunk c to partial c mod 256; each partial adds the squares
+  of its chunks in ascending order, element by element; the 256 partials are
+  then added in a binary tree, partial i + partial i + h for h = 128, 64, ...,
+  1.  The normalized values are quantized as they are, never rounded to the
+  input dtype first.
 * arc_perm: calibration statistic = max over rows of |X| per channel, taken
   on X itself; channels sorted by descending statistic, ties by ascending
   channel index.
@@ -250,3 +272,46 @@ def quant_fp8_tensor(x):
     a = np.abs(x).max() if x.size else F32(0.0)
     s = F32(1.0) if a == 0 else F32(a / F32(448.0))
     return e4m3_encode(x / s), s
+
+
+RMS_PARTIALS = 256   # partial sums of the mean of squares (the fixed reduction order)
+RMS_CHUNK = 8        # consecutive elements per chunk
+
+
+def rmsnorm_rows(x, gamma, eps):
+    """y = (x . (1 / sqrt(mean(x^2) + eps))) . gamma per row, float32, in the fixed
+    reduction order stated above.  x: float32 [rows][K] (K a multiple of 8),
+    gamma: float32 [K] -> y float32 [rows][K]."""
+    x = np.asarray(x, dtype=np.float32)
+    g = np.asarray(gamma, dtype=np.float32)
+    rows, k = x.shape
+    nchunk = k // RMS_CHUNK
+    per = -(-nchunk // RMS_PARTIALS)
+    sq = (x * x).astype(np.float32)
+    # chunk c of the row is element-block [8c, 8c + 8); partial p holds chunks
+    # p, p + 256, p + 512, ... in that order
+    padded = np.zeros((rows, per * RMS_PARTIALS * RMS_CHUNK), dtype=np.float32)
+    padded[:, :k] = sq
+    blocks = padded.reshape(rows, per, RMS_PARTIALS, RMS_CHUNK).transpose(0, 2, 1, 3).reshape(rows, RMS_PARTIALS, -1)
+    part = np.zeros((rows, RMS_PARTIALS), dtype=np.float32)
+    for j in range(blocks.shape[2]):          # one float32 add at a time, in order
+        part = (part + blocks[:, :, j]).astype(np.float32)
+    h = RMS_PARTIALS // 2
+    while h >= 1:
+        part[:, :h] = (part[:, :h] + part[:, h:2 * h]).astype(np.float32)
+        h //= 2
+    ms = (part[:, 0] / np.float32(k)).astype(np.float32)
+    r = np.sqrt((ms + np.float32(eps)).astype(np.float32)).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        inv = np.where(r == 0, np.float32(0.0), np.float32(1.0) / r).astype(np.float32)
+    return ((x * inv[:, None]).astype(np.float32) * g[None, :]).astype(np.float32)
+
+
+def rmsnorm_quant_int8(x, gamma, eps):
+    """RMSNorm fused with per-token symmetric int8: (q int8, s float32 [rows])."""
+    return quant_int8_sym(rmsnorm_rows(x, gamma, eps))
+
+
+def rmsnorm_quant_fp8(x, gamma, eps):
+    """RMSNorm fused with per-token FP8 E4M3: (codes uint8, s float32 [rows])."""
+    return quant_fp8_rows(rmsnorm_rows(x, gamma, eps))

@@ -24,11 +24,13 @@ __all__ = [
     "qlin_w4a16_sequence_workspace_bytes", "qlin_w4a16_gemv_sequence", "qlin_w4a16_gemv_sequence_noalloc",
     "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm",
     "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
+    "QLIN_QFMT_INT8", "QLIN_QFMT_FP8_E4M3", "qlin_quant_fp8", "qlin_fp8_gemm", "qlin_rmsnorm_quant",
 ]
 
 QLIN_F16, QLIN_BF16, QLIN_F32, QLIN_I32 = 0, 1, 2, 3
 QLIN_NVFP4_RESIDUAL, QLIN_NVFP4_DUPLICATE = 0, 1
 QLIN_SF_ROWS, QLIN_SF_MMA = 0, 1
+QLIN_QFMT_INT8, QLIN_QFMT_FP8_E4M3 = 0, 1
 
 _STATUS = {0: "QLIN_OK", 1: "QLIN_ERR_INVALID_ARG", 2: "QLIN_ERR_ALIGNMENT", 3: "QLIN_ERR_UNSUPPORTED",
            4: "QLIN_ERR_CUDA", 5: "QLIN_ERR_TIMEOUT"}
@@ -65,6 +67,7 @@ _SIGS = {
     "qlin_nvfp4_gemm": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P], _I32),
     "qlin_quant_fp8": ([_P, _I32, _I64, _I64, _P, _P, _P], _I32),
     "qlin_fp8_gemm": ([_P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
+    "qlin_rmsnorm_quant": ([_P, _I32, _I64, _I64, _P, ctypes.c_float, _I32, _P, _P, _P], _I32),
 }
 
 _lib = None
@@ -358,3 +361,17 @@ def qlin_fp8_gemm(a, b, scale_a, scale_b, out, bias=None, stream=None):
     bias_dt = QLIN_F16 if bias is None else _dtype_code(bias)
     _check("qlin_fp8_gemm", lib().qlin_fp8_gemm(_ptr(a), _ptr(b), t, n, k, _ptr(scale_a), _ptr(scale_b), _ptr(bias),
                                                bias_dt, _ptr(out), _dtype_code(out), _stream(stream)))
+
+
+def qlin_rmsnorm_quant(x, gamma, eps, q, scale, fmt=QLIN_QFMT_INT8, stream=None):
+    """y = (x . (1 / sqrt(mean(x^2) + eps))) . gamma per row of x [rows][K], quantized
+    per token: q int8 (QLIN_QFMT_INT8) or uint8 E4M3 codes (QLIN_QFMT_FP8_E4M3)
+    [rows][K], scale float32 [rows]."""
+    torch = _torch()
+    _need(x, torch.float16, torch.bfloat16, torch.float32, name="x")
+    _need(gamma, x.dtype, name="gamma")
+    _need(q, torch.int8 if fmt == QLIN_QFMT_INT8 else torch.uint8, name="q")
+    _need(scale, torch.float32, name="scale")
+    rows, k = x.shape
+    _check("qlin_rmsnorm_quant", lib().qlin_rmsnorm_quant(_ptr(x), _dtype_code(x), rows, k, _ptr(gamma), float(eps),
+                                                         fmt, _ptr(q), _ptr(scale), _stream(stream)))

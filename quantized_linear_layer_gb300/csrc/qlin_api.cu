@@ -458,4 +458,22 @@ qlin_status qlin_fp8_gemm(const uint8_t* a, const uint8_t* b, int64_t T, int64_t
               "fp8_gemm launch");
 }
 
+qlin_status qlin_rmsnorm_quant(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const void* gamma,
+                               float eps, qlin_qfmt fmt, void* q, float* scale, cudaStream_t stream) {
+  QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");
+  QLIN_REQUIRE(fmt == QLIN_QFMT_INT8 || fmt == QLIN_QFMT_FP8_E4M3, QLIN_ERR_INVALID_ARG, "unknown output format %d",
+               static_cast<int>(fmt));
+  QLIN_REQUIRE(eps >= 0.0f && eps <= 3.4e38f, QLIN_ERR_INVALID_ARG, "eps must be a finite number >= 0");
+  QLIN_REQUIRE(rows >= 0 && rows <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG,
+               "bad sizes rows=%lld K=%lld", (long long)rows, (long long)K);
+  QLIN_REQUIRE(K % 16 == 0, QLIN_ERR_ALIGNMENT, "K=%lld is not a multiple of 16", (long long)K);
+  if (rows == 0) return ok();
+  QLIN_REQUIRE(x && gamma && q && scale, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(x) && aligned16(gamma) && aligned16(q), QLIN_ERR_ALIGNMENT,
+               "x, gamma and q must be 16-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(scale) & 3u) == 0, QLIN_ERR_ALIGNMENT, "scale must be 4-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_rmsnorm_quant(x, x_dtype, rows, K, gamma, eps, fmt, q, scale, stream), "rmsnorm_quant launch");
+}
+
 }  // extern "C"

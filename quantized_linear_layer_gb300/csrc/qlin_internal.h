@@ -93,6 +93,9 @@ cudaError_t launch_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_
 cudaError_t launch_quant_fp8(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, uint8_t* q, float* scale,
                              cudaStream_t stream);
 
+cudaError_t launch_rmsnorm_quant(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const void* gamma,
+                                 float eps, qlin_qfmt fmt, void* q, float* scale, cudaStream_t stream);
+
 cudaError_t launch_fp8_gemm(const uint8_t* a, const uint8_t* b, int64_t T, int64_t N, int64_t K, const float* scale_a,
                             const float* scale_b, const void* bias, qlin_dtype bias_dtype, void* out,
                             qlin_dtype out_dtype, cudaStream_t stream);

@@ -216,6 +216,150 @@ __global__ void __launch_bounds__(kQuantThreads) quant_fp8_rows_kernel(const voi
   }
 }
 
+// RMSNorm fused with the per-token quantizers ("Chapter 9 - Quantization
+// kernels", practical notes: the per-row max and the quantization fused into
+// the upstream operator; "LLM and AIGC quantization", "Static and dynamic
+// quantization": the per-token reduction is usually fused into the
+// preceding RMSNorm): y = (x / sqrt(mean(x^2) + eps)) . gamma, then the
+// symmetric int8 (FMT 0) or the E4M3 (FMT 1) quantization of y, without
+// rounding y to the input dtype.  The row is read once.  y is computed as
+// (x . inv) . gamma with inv = 1 / sqrt(mean(x^2) + eps) (one correctly
+// rounded square root and division per row); a row whose mean(x^2) + eps is
+// 0 normalizes to 0.
+// The mean of squares is a float32 sum in a fixed order, part of the
+// operation's definition so that its result is reproducible: thread t owns
+// the 8-element chunks t, t + 256, ... and adds their squares in that order,
+// element by element (separate multiply and add, never contracted), and the
+// 256 partial sums meet in a binary tree (partial i += partial i + h, h =
+// 128 ... 1; the steps below 32 are the same additions done with shuffles
+// inside warp 0).
+template <int DT, int FMT>
+__global__ void __launch_bounds__(kQuantThreads) rmsnorm_quant_kernel(const void* __restrict__ x,
+                                                                     const void* __restrict__ gamma, int K,
+                                                                     float eps, void* __restrict__ q,
+                                                                     float* __restrict__ scale) {
+  static_assert(kQuantThreads == 256, "the reduction order is defined over 256 partial sums");
+  pdl_launch_dependents();  // the GEMM that reads the codes may start setting up
+  const int64_t row = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nvec = K / 8;
+  constexpr int EB = elem_bytes<DT>();
+  const char* xr = static_cast<const char*>(x) + row * (int64_t)K * EB;
+  const char* gr = static_cast<const char*>(gamma);
+
+  float v[kMaxVecPerThread][8];
+  float part = 0.0f;
+  auto add_squares = [&](const float* t) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) part = __fadd_rn(part, __fmul_rn(t[j], t[j]));
+  };
+#pragma unroll
+  for (int i = 0; i < kMaxVecPerThread; ++i) {
+    const int c = tid + i * kQuantThreads;
+    if (c < nvec) {
+      Vec8Loader<DT>::load(xr + (int64_t)c * 8 * EB, v[i]);
+      add_squares(v[i]);
+    }
+  }
+  for (int c = tid + kMaxVecPerThread * kQuantThreads; c < nvec; c += kQuantThreads) {
+    float t[8];
+    Vec8Loader<DT>::load(xr + (int64_t)c * 8 * EB, t);
+    add_squares(t);
+  }
+  __shared__ float red[kQuantThreads];
+  __shared__ float s_scale, s_inv;
+  red[tid] = part;
+  __syncthreads();
+  for (int h = kQuantThreads / 2; h >= 32; h >>= 1) {
+    if (tid < h) red[tid] = __fadd_rn(red[tid], red[tid + h]);
+    __syncthreads();
+  }
+  if (tid < 32) {
+    float p = red[tid];
+#pragma unroll
+    for (int h = 16; h >= 1; h >>= 1) p = __fadd_rn(p, __shfl_down_sync(0xffffffffu, p, h));
+    if (tid == 0) {
+      const float ms = __fdiv_rn(p, static_cast<float>(K));
+      const float r = __fsqrt_rn(__fadd_rn(ms, eps));
+      s_inv = r == 0.0f ? 0.0f : __fdiv_rn(1.0f, r);
+    }
+  }
+  __syncthreads();
+  const float inv = s_inv;
+  // y = (x . inv) . gamma
+  auto normalize = [&](float* t, int c) {
+    float gv[8];
+    Vec8Loader<DT>::load(gr + (int64_t)c * 8 * EB, gv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = __fmul_rn(__fmul_rn(t[j], inv), gv[j]);
+  };
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kMaxVecPerThread; ++i) {
+    const int c = tid + i * kQuantThreads;
+    if (c < nvec) {
+      normalize(v[i], c);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[i][j]));
+    }
+  }
+  for (int c = tid + kMaxVecPerThread * kQuantThreads; c < nvec; c += kQuantThreads) {
+    float t[8];
+    Vec8Loader<DT>::load(xr + (int64_t)c * 8 * EB, t);
+    normalize(t, c);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(t[j]));
+  }
+  // max is exact, so this reduction's order does not matter
+  m = warp_max(m);
+  __syncthreads();  // every thread is done with the tree's red[]
+  if ((tid & 31) == 0) red[tid >> 5] = m;
+  __syncthreads();
+  if (tid == 0) {
+    float a = red[0];
+    for (int w = 1; w < kQuantThreads / 32; ++w) a = fmaxf(a, red[w]);
+    const float sv = (a == 0.0f) ? 1.0f : __fdiv_rn(a, FMT == 0 ? 127.0f : 448.0f);
+    s_scale = sv;
+    scale[row] = sv;
+  }
+  __syncthreads();
+  const float s = s_scale;
+  const float rs = __frcp_rn(s);
+  const bool srcp_ok = rcp_division_ok(s, rs);
+  auto quant8 = [&](const float* t, int c) {
+    uint32_t w0 = 0, w1 = 0;
+    if (FMT == 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        int qi = __float2int_rn(srcp_ok ? div_by_rcp(t[j], s, rs) : __fdiv_rn(t[j], s));
+        qi = min(max(qi, -127), 127);
+        const uint32_t byte = static_cast<uint32_t>(qi) & 0xffu;
+        if (j < 4) w0 |= byte << (8 * j); else w1 |= byte << (8 * (j - 4));
+      }
+    } else {
+      uint32_t pr[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        pr[j] = f32x2_to_e4m3x2(srcp_ok ? div_by_rcp(t[2 * j], s, rs) : __fdiv_rn(t[2 * j], s),
+                                srcp_ok ? div_by_rcp(t[2 * j + 1], s, rs) : __fdiv_rn(t[2 * j + 1], s));
+      w0 = pr[0] | (pr[1] << 16);
+      w1 = pr[2] | (pr[3] << 16);
+    }
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(q) + row * (int64_t)K + (int64_t)c * 8) = make_uint2(w0, w1);
+  };
+#pragma unroll
+  for (int i = 0; i < kMaxVecPerThread; ++i) {
+    const int c = tid + i * kQuantThreads;
+    if (c < nvec) quant8(v[i], c);
+  }
+  for (int c = tid + kMaxVecPerThread * kQuantThreads; c < nvec; c += kQuantThreads) {
+    float t[8];
+    Vec8Loader<DT>::load(xr + (int64_t)c * 8 * EB, t);
+    normalize(t, c);
+    quant8(t, c);
+  }
+}
+
 // azp_adj[n] = sum_k b[n,k]: one warp per row, 16 bytes per lane per step.
 __global__ void int8_row_sum_kernel(const int8_t* __restrict__ b, int64_t N, int K, int32_t* __restrict__ out) {
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
@@ -319,6 +463,29 @@ cudaError_t launch_quant_fp8(const void* x, qlin_dtype x_dtype, int64_t rows, in
     case QLIN_F16: quant_fp8_rows_kernel<0><<<grid, block, 0, stream>>>(x, k, q, scale); break;
     case QLIN_BF16: quant_fp8_rows_kernel<1><<<grid, block, 0, stream>>>(x, k, q, scale); break;
     default: quant_fp8_rows_kernel<2><<<grid, block, 0, stream>>>(x, k, q, scale); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_quant(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const void* gamma,
+                                 float eps, qlin_qfmt fmt, void* q, float* scale, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>(rows)), block(kQuantThreads);
+  const int k = static_cast<int>(K);
+  const bool fp8 = fmt == QLIN_QFMT_FP8_E4M3;
+  switch (x_dtype) {
+    case QLIN_F16:
+      if (fp8) rmsnorm_quant_kernel<0, 1><<<grid, block, 0, stream>>>(x, gamma, k, eps, q, scale);
+      else rmsnorm_quant_kernel<0, 0><<<grid, block, 0, stream>>>(x, gamma, k, eps, q, scale);
+      break;
+    case QLIN_BF16:
+      if (fp8) rmsnorm_quant_kernel<1, 1><<<grid, block, 0, stream>>>(x, gamma, k, eps, q, scale);
+      else rmsnorm_quant_kernel<1, 0><<<grid, block, 0, stream>>>(x, gamma, k, eps, q, scale);
+      break;
+    default:
+      if (fp8) rmsnorm_quant_kernel<2, 1><<<grid, block, 0, stream>>>(x, gamma, k, eps, q, scale);
+      else rmsnorm_quant_kernel<2, 0><<<grid, block, 0, stream>>>(x, gamma, k, eps, q, scale);
+      break;
   }
   return cudaGetLastError();
 }

@@ -111,6 +111,13 @@ def test_rejects_bad_arguments_without_gpu(built):
     assert L.qlin_fp8_gemm(P(16), P(24), 4, 8, 64, P(16), P(16), None, 0, P(16), 0, None) == 2
     assert L.qlin_fp8_gemm(P(16), P(16), 4, 12, 64, P(16), P(16), None, 0, P(16), 0, None) == 2
     assert L.qlin_fp8_gemm(P(16), P(16), 4, 8, 72, P(16), P(16), None, 0, P(16), 0, None) == 2
+    # fused RMSNorm + quant: unknown format, negative eps, K not a multiple of 16, misaligned gamma
+    F = ctypes.c_float
+    assert L.qlin_rmsnorm_quant(P(16), 0, 4, 64, P(16), F(1e-6), 2, P(16), P(16), None) == 1
+    assert L.qlin_rmsnorm_quant(P(16), 0, 4, 64, P(16), F(-1.0), 0, P(16), P(16), None) == 1
+    assert L.qlin_rmsnorm_quant(P(16), 0, 4, 40, P(16), F(1e-6), 0, P(16), P(16), None) == 2
+    assert L.qlin_rmsnorm_quant(P(16), 0, 4, 64, P(24), F(1e-6), 1, P(16), P(16), None) == 2
+    assert L.qlin_rmsnorm_quant(None, 0, 0, 64, None, F(1e-6), 0, None, None, None) == 0
     # perm K limit
     assert L.qlin_arc_perm(P(16), 0, 4, 32768, P(16), None) == 1
     msg = L.qlin_last_error_message()

@@ -1,0 +1,49 @@
+"""RMSNorm fused with the per-token quantizers on the GPU against the CPU
+oracle: codes and scales bit for bit, int8 and E4M3 outputs, 16-bit and
+float32 inputs, rows held in registers and rows read twice."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_linear_layer_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(seed, rows, k):
+    d = inputs.w8a8_sym_bias(seed=seed, T=rows, K=k, N=16)
+    x = d["x"].astype(np.float32)
+    x[1] = 0.0                 # all-zero row: y = 0, scale 1
+    x[2] = 0.5                 # constant row
+    x[3, 7] = 3000.0           # one outlier channel
+    x[4] *= np.float32(1e-4)   # small magnitudes (the mean of squares near eps)
+    return x
+
+
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("k,eps", [(4096, 1e-6), (8256, 1e-5), (16, 0.0), (4160, 1e-6)])
+def test_rmsnorm_quant_bit_exact(qlin_gpu, fmt, dtype, k, eps):
+    rng = np.random.default_rng(k + 3)
+    x = _rows(41, 48, k)
+    g = rng.uniform(0.5, 1.5, size=k).astype(np.float32)
+    xt = torch.from_numpy(x).to(dtype).cuda()
+    gt = torch.from_numpy(g).to(dtype).cuda()
+    q_fmt = qlin_gpu.QLIN_QFMT_INT8 if fmt == "int8" else qlin_gpu.QLIN_QFMT_FP8_E4M3
+    q = torch.empty((48, k), dtype=torch.int8 if fmt == "int8" else torch.uint8, device="cuda")
+    s = torch.empty(48, dtype=torch.float32, device="cuda")
+    qlin_gpu.qlin_rmsnorm_quant(xt, gt, eps, q, s, fmt=q_fmt)
+    torch.cuda.synchronize()
+    assert qlin_gpu.qlin_get_device_error() == 0
+    xo, go = xt.float().cpu().numpy(), gt.float().cpu().numpy()
+    if fmt == "int8":
+        rq, rs = oracle.rmsnorm_quant_int8(xo, go, eps)
+    else:
+        rq, rs = oracle.rmsnorm_quant_fp8(xo, go, eps)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32)), \
+        "scales differ in rows %s" % np.nonzero(s.cpu().numpy() != rs)[0][:5].tolist()
+    got = q.cpu().numpy().view(np.uint8)
+    bad = np.argwhere(got != rq.view(np.uint8))
+    assert bad.size == 0, "first mismatches (row, col): %s" % bad[:5].tolist()

@@ -618,6 +618,67 @@ def pin_fp8_gemm_brute_force():
 def test_fp8_gemm_brute_force():
     pin_fp8_gemm_brute_force()
 
+
+# ---- RMSNorm fused with the per-token quantizers ----
+
+def pin_rmsnorm_formula():
+    rng = np.random.default_rng(13)
+    for k, eps in ((4096, 1e-6), (4160, 1e-5), (16, 0.0), (8, 1e-3)):
+        x = (rng.standard_normal((5, k)) * np.exp(rng.uniform(-4, 4, size=(5, 1)))).astype(np.float32)
+        g = rng.uniform(0.25, 2.0, size=k).astype(np.float32)
+        y = oracle.rmsnorm_rows(x, g, eps)
+        x64 = x.astype(np.float64)
+        ref = x64 / np.sqrt((x64 ** 2).mean(axis=1, keepdims=True) + eps) * g.astype(np.float64)
+        # a handful of float32 roundings plus the float32 sum of squares
+        tol = 8 * 2.0 ** -24 + k * 2.0 ** -24
+        assert np.all(np.abs(y - ref) <= tol * np.abs(ref) + 1e-30), k
+
+
+def test_rmsnorm_formula():
+    pin_rmsnorm_formula()
+
+
+def test_rmsnorm_power_of_two_invariance():
+    """With eps = 0, x and 2^j x normalize to the same bits (every step scales
+    exactly), so the fused quantizers give the same codes."""
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal((4, 1024)).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, size=1024).astype(np.float32)
+    y = oracle.rmsnorm_rows(x, g, 0.0)
+    for j in (-20, -3, 5, 30):
+        assert np.array_equal(oracle.rmsnorm_rows(x * np.float32(2.0 ** j), g, 0.0), y)
+    q1, s1 = oracle.rmsnorm_quant_int8(x, g, 0.0)
+    q2, s2 = oracle.rmsnorm_quant_int8(x * np.float32(8.0), g, 0.0)
+    assert np.array_equal(q1, q2) and np.array_equal(s1, s2)
+
+
+def test_rmsnorm_constant_row():
+    """A constant row 0.5 with gamma = 1 and eps = 0 normalizes to exactly 1
+    (mean of squares 0.25, root 0.5, inverse 2): int8 codes 127 with s = 1/127,
+    FP8 codes 448; a zero row with eps = 0 normalizes to 0 (codes 0, s = 1)."""
+    x = np.full((2, 4096), 0.5, dtype=np.float32)
+    x[1] = 0.0
+    g = np.ones(4096, dtype=np.float32)
+    y = oracle.rmsnorm_rows(x, g, 0.0)
+    assert np.all(y[0] == 1.0) and np.all(y[1] == 0.0)
+    q, s = oracle.rmsnorm_quant_int8(x, g, 0.0)
+    assert np.all(q[0] == 127) and s[0] == np.float32(1.0) / np.float32(127.0) and np.all(q[1] == 0) and s[1] == 1.0
+    c, sf = oracle.rmsnorm_quant_fp8(x, g, 0.0)
+    assert np.all(oracle.e4m3_decode(c[0]) == 448.0) and np.all(oracle.e4m3_decode(c[1]) == 0.0)
+
+
+def test_rmsnorm_sum_order_bound():
+    """The fixed-order float32 mean of squares stays within K . 2^-24 of the
+    exact mean (a bound any summation order meets)."""
+    rng = np.random.default_rng(15)
+    x = rng.standard_normal((8, 8192)).astype(np.float32)
+    g = np.ones(8192, dtype=np.float32)
+    y = oracle.rmsnorm_rows(x, g, 0.0)
+    x64 = x.astype(np.float64)
+    r_exact = np.sqrt((x64 ** 2).mean(axis=1))
+    r_implied = np.median(x64 / y.astype(np.float64), axis=1)
+    assert np.all(np.abs(r_implied - r_exact) <= 8192 * 2.0 ** -24 * r_exact)
+
 def _mut_e2m1_ties_odd(monkeypatch):
     orig = ofmt._nearest_code
 
@@ -703,9 +764,21 @@ def _mut_fp8_scales_swapped(monkeypatch):
     return pin_fp8_gemm_brute_force
 
 
+def _mut_rmsnorm_mean_k_minus_1(monkeypatch):
+    def bad(x, gamma, eps):
+        x = np.asarray(x, dtype=np.float32)
+        k = x.shape[1]
+        ms = ((x * x).sum(axis=1, dtype=np.float32) / np.float32(k - 1)).astype(np.float32)
+        inv = (np.float32(1.0) / np.sqrt(ms + np.float32(eps))).astype(np.float32)
+        return ((x * inv[:, None]) * np.asarray(gamma, dtype=np.float32)).astype(np.float32)
+
+    monkeypatch.setattr(oracle, "rmsnorm_rows", bad)
+    return pin_rmsnorm_formula
+
+
 MUTATIONS = [_mut_e2m1_ties_odd, _mut_azp_sign, _mut_azp_adj_axis, _mut_residual_sign,
              _mut_w8a8_transposed, _mut_w4_zero_dropped, _mut_nvfp4_scale_not_decoded, _mut_sym_qmax,
-             _mut_fp8_scale_447, _mut_fp8_scales_swapped]
+             _mut_fp8_scale_447, _mut_fp8_scales_swapped, _mut_rmsnorm_mean_k_minus_1]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
