@@ -435,6 +435,27 @@ qlin_status qlin_fp8_gemm(const uint8_t* a, const uint8_t* b, int64_t T, int64_t
 qlin_status qlin_rmsnorm_quant(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const void* gamma,
                                float eps, qlin_qfmt fmt, void* q, float* scale, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * next 2 - RMSNorm fused with the NVFP4 / ARCQuant quantizer
+ *
+ * Per row, y = (x . inv) . gamma exactly as qlin_rmsnorm_quant defines it
+ * (the same fixed order of the mean of squares, the same float32 steps),
+ * then qlin_quant_nvfp4 of y: the reordered channels ys = y[:, perm], the
+ * 16-element blocks with E4M3 scales over the per-tensor g, and the S
+ * residual (or duplicated) channels; y stays in float32 and x is read once.
+ * g and perm are calibrated on y (the normalized activations the GEMM
+ * consumes), e.g. with qlin_nvfp4_global_scale / qlin_arc_perm on a
+ * calibration batch of y.
+ *   x, perm, S, mode, g, q, sf, sf_layout  as in qlin_quant_nvfp4
+ *   gamma  [K] of x_dtype (16-byte aligned)
+ *   eps    the RMSNorm epsilon (>= 0)
+ * Rows of up to 96 KB (K <= 49152 for 16-bit x, 24576 for F32): a row and
+ * gamma are both staged in shared memory (QLIN_ERR_UNSUPPORTED above).
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_rmsnorm_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const void* gamma,
+                                     float eps, const int32_t* perm, int64_t S, qlin_nvfp4_mode mode, const float* g,
+                                     uint8_t* q, uint8_t* sf, qlin_sf_layout sf_layout, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

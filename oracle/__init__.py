@@ -54,6 +54,7 @@ from .quant import (  # noqa: F401
     rmsnorm_rows,
     rmsnorm_quant_int8,
     rmsnorm_quant_fp8,
+    rmsnorm_arc_quantize_activation,
     nvfp4_global_scale,
     nvfp4_quantize,
     nvfp4_dequantize,

@@ -315,3 +315,11 @@ def rmsnorm_quant_int8(x, gamma, eps):
 def rmsnorm_quant_fp8(x, gamma, eps):
     """RMSNorm fused with per-token FP8 E4M3: (codes uint8, s float32 [rows])."""
     return quant_fp8_rows(rmsnorm_rows(x, gamma, eps))
+
+
+def rmsnorm_arc_quantize_activation(x, gamma, eps, perm, s_res, g):
+    """RMSNorm fused with the ARCQuant NVFP4 activation quantizer: the float32
+    RMSNorm output y of rmsnorm_rows (gamma applied at each channel's own
+    position), then arc_quantize_activation(y, perm, S, g).  g and perm belong
+    to y, the activations the GEMM consumes."""
+    return arc_quantize_activation(rmsnorm_rows(x, gamma, eps), perm, s_res, g)

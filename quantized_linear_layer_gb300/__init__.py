@@ -25,6 +25,7 @@ __all__ = [
     "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm",
     "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
     "QLIN_QFMT_INT8", "QLIN_QFMT_FP8_E4M3", "qlin_quant_fp8", "qlin_fp8_gemm", "qlin_rmsnorm_quant",
+    "qlin_rmsnorm_quant_nvfp4",
 ]
 
 QLIN_F16, QLIN_BF16, QLIN_F32, QLIN_I32 = 0, 1, 2, 3
@@ -68,6 +69,8 @@ _SIGS = {
     "qlin_quant_fp8": ([_P, _I32, _I64, _I64, _P, _P, _P], _I32),
     "qlin_fp8_gemm": ([_P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
     "qlin_rmsnorm_quant": ([_P, _I32, _I64, _I64, _P, ctypes.c_float, _I32, _P, _P, _P], _I32),
+    "qlin_rmsnorm_quant_nvfp4": ([_P, _I32, _I64, _I64, _P, ctypes.c_float, _P, _I64, _I32, _P, _P, _P, _I32, _P],
+                                 _I32),
 }
 
 _lib = None
@@ -375,3 +378,19 @@ def qlin_rmsnorm_quant(x, gamma, eps, q, scale, fmt=QLIN_QFMT_INT8, stream=None)
     rows, k = x.shape
     _check("qlin_rmsnorm_quant", lib().qlin_rmsnorm_quant(_ptr(x), _dtype_code(x), rows, k, _ptr(gamma), float(eps),
                                                          fmt, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def qlin_rmsnorm_quant_nvfp4(x, gamma, eps, g, q, sf, perm=None, S=0, mode=QLIN_NVFP4_RESIDUAL,
+                             sf_layout=QLIN_SF_ROWS, stream=None):
+    """y = (x . (1 / sqrt(mean(x^2) + eps))) . gamma per row of x [rows][K], then the
+    NVFP4 quantization of y as qlin_quant_nvfp4 does it (g and perm calibrated on y)."""
+    torch = _torch()
+    _need(x, torch.float16, torch.bfloat16, torch.float32, name="x")
+    _need(gamma, x.dtype, name="gamma"); _need(g, torch.float32, name="g")
+    _need(q, torch.uint8, name="q"); _need(sf, torch.uint8, name="sf"); _need(perm, torch.int32, name="perm")
+    rows, k = x.shape
+    if sf.numel() < qlin_nvfp4_sf_bytes(rows, k + S, sf_layout):
+        raise ValueError("sf buffer too small")
+    _check("qlin_rmsnorm_quant_nvfp4",
+           lib().qlin_rmsnorm_quant_nvfp4(_ptr(x), _dtype_code(x), rows, k, _ptr(gamma), float(eps), _ptr(perm), S,
+                                          mode, _ptr(g), _ptr(q), _ptr(sf), sf_layout, _stream(stream)))

@@ -133,29 +133,112 @@ __device__ __forceinline__ uint32_t quant_block16(const float* v, const GlobalSc
   return sfc;
 }
 
+// Eight consecutive staged elements (16 or 32 bytes of shared memory) as float32.
+template <int DT>
+__device__ __forceinline__ void smem_chunk8(const unsigned char* p, float* v) {
+  if constexpr (DT == 2) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 c = *reinterpret_cast<const float4*>(p + 16);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+  } else {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f;
+      if constexpr (DT == 0) f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+}
+
+// 1 / sqrt(mean(x^2) + eps) of each of the nr staged rows into inv[] (0 where
+// the root is 0), every thread of the CTA taking part: the float32 mean of
+// squares in the fixed order of the fused RMSNorm quantizers (thread t adds
+// the squares of the row's 8-element chunks t, t + 256, ... in order, then a
+// binary tree over the 256 partial sums, its last five steps by shuffles in
+// warp 0).  The rows' trees run side by side.
+template <int DT, int R>
+__device__ void staged_rows_inv_rms(const unsigned char* rows_smem, int row_bytes, int nr, int K, float eps,
+                                    float (*red)[kNvThreads], float* inv) {
+  constexpr int EB = elem_bytes<DT>();
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int rr = 0; rr < R; ++rr) {
+    float part = 0.0f;
+    if (rr < nr) {
+      const unsigned char* rs = rows_smem + rr * row_bytes;
+      for (int c = tid; c * 8 < K; c += kNvThreads) {
+        float v[8];
+        smem_chunk8<DT>(rs + c * 8 * EB, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part = __fadd_rn(part, __fmul_rn(v[i], v[i]));
+      }
+    }
+    red[rr][tid] = part;
+  }
+  __syncthreads();
+  for (int h = kNvThreads / 2; h >= 32; h >>= 1) {
+    if (tid < h) {
+#pragma unroll
+      for (int rr = 0; rr < R; ++rr) red[rr][tid] = __fadd_rn(red[rr][tid], red[rr][tid + h]);
+    }
+    __syncthreads();
+  }
+  if (tid < 32) {
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+      float p = red[rr][tid];
+#pragma unroll
+      for (int h = 16; h >= 1; h >>= 1) p = __fadd_rn(p, __shfl_down_sync(0xffffffffu, p, h));
+      if (tid == 0) {
+        const float r = __fsqrt_rn(__fadd_rn(__fdiv_rn(p, static_cast<float>(K)), eps));
+        inv[rr] = r == 0.0f ? 0.0f : __fdiv_rn(1.0f, r);
+      }
+    }
+  }
+  __syncthreads();
+}
+
 // R rows per CTA: the rows are staged in shared memory in their input dtype,
 // then each thread quantizes 16-element blocks of the reordered rows; the
 // block's 16 channel offsets are loaded and checked once for all R rows.
-template <int DT, int R>
+// NORM: RMSNorm fused in front (gamma staged after the rows, in its own
+// order, and gathered with the same offsets as the row elements).
+template <int DT, int R, bool NORM>
 __global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __restrict__ x, int64_t rows, int K,
                                                                   const int32_t* __restrict__ perm, int S,
                                                                   int mode, const float* __restrict__ gp,
                                                                   uint8_t* __restrict__ q,
                                                                   uint8_t* __restrict__ sf, int sf_mma,
+                                                                  const void* __restrict__ gamma, float eps,
                                                                   int32_t* __restrict__ err) {
   extern __shared__ __align__(16) unsigned char row_smem[];
+  static_assert(kNvThreads == 256, "the fused RMSNorm's reduction order is defined over 256 partial sums");
   pdl_launch_dependents();  // the GEMM that reads the codes may start setting up
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * R;
   const int nr = static_cast<int>(min(static_cast<int64_t>(R), rows - row0));
   const int tid = threadIdx.x;
   constexpr int EB = elem_bytes<DT>();
   const int row_bytes = K * EB;
+  unsigned char* gamma_smem = row_smem + R * row_bytes;
   {
     const char* xr = static_cast<const char*>(x) + row0 * row_bytes;
     for (int off = tid * 16; off < nr * row_bytes; off += kNvThreads * 16)
       *reinterpret_cast<uint4*>(row_smem + off) = ldg_v4(xr + off);
+    if constexpr (NORM) {
+      for (int off = tid * 16; off < row_bytes; off += kNvThreads * 16)
+        *reinterpret_cast<uint4*>(gamma_smem + off) = ldg_v4(static_cast<const char*>(gamma) + off);
+    }
   }
   __syncthreads();
+  // fused RMSNorm: each staged row's 1 / rms
+  __shared__ float red[NORM ? R : 1][kNvThreads];
+  __shared__ float inv_rms[R];
+  if constexpr (NORM) staged_rows_inv_rms<DT, R>(row_smem, row_bytes, nr, K, eps, red, inv_rms);
 
   const GlobalScale gs = make_global_scale(__ldg(gp));
   const int Kaug = K + S;
@@ -185,6 +268,12 @@ __global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __r
 #pragma unroll
       for (int i = 0; i < 16; ++i) off[i] = (b * 16 + i) * EB;
     }
+    // fused RMSNorm: the block's gamma at the channels' original positions
+    float gv[16];
+    if constexpr (NORM) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) gv[i] = load_elem<DT>(gamma_smem + off[i], 0);
+    }
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {
       if (rr >= nr) break;
@@ -193,6 +282,11 @@ __global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __r
       float v[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] = load_elem<DT>(rs + off[i], 0);
+      if constexpr (NORM) {
+        const float inv = inv_rms[rr];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(__fmul_rn(v[i], inv), gv[i]);
+      }
       uint32_t packed[2];
       float d;
       const uint32_t sfc = quant_block16(v, gs, packed, &d);
@@ -321,27 +415,34 @@ cudaError_t dispatch_dtype(qlin_dtype dt, F&& f) {
 
 cudaError_t launch_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const int32_t* perm,
                                int64_t S, qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
-                               qlin_sf_layout sf_layout, cudaStream_t stream) {
+                               qlin_sf_layout sf_layout, const void* gamma, float eps, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   return dispatch_dtype(x_dtype, [&](auto dt) -> cudaError_t {
     constexpr int DT = decltype(dt)::value;
     const size_t row_smem = static_cast<size_t>(K) * elem_bytes<DT>();
-    auto launch = [&](auto rows_per_cta) -> cudaError_t {
+    auto launch = [&](auto rows_per_cta, auto norm) -> cudaError_t {
       constexpr int R = decltype(rows_per_cta)::value;
-      const size_t smem = row_smem * R;
-      if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(nvfp4_quant_kernel<DT, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      constexpr bool NORM = decltype(norm)::value;
+      const size_t smem = row_smem * (R + (NORM ? 1 : 0));
+      auto kern = nvfp4_quant_kernel<DT, R, NORM>;
+      // the opt-in covers dynamic plus static shared memory above the 48 KB default
+      if (smem + 4 * 1024 > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
       }
-      nvfp4_quant_kernel<DT, R><<<static_cast<unsigned>((rows + R - 1) / R), kNvThreads, smem, stream>>>(
+      kern<<<static_cast<unsigned>((rows + R - 1) / R), kNvThreads, smem, stream>>>(
           x, rows, static_cast<int>(K), perm, static_cast<int>(S), static_cast<int>(mode), g, q, sf,
-          sf_layout == QLIN_SF_MMA ? 1 : 0, device_error_word());
+          sf_layout == QLIN_SF_MMA ? 1 : 0, gamma, eps, device_error_word());
       return cudaGetLastError();
     };
-    // two rows per CTA share the channel offsets while both fit comfortably
-    if (2 * row_smem <= 96 * 1024) return launch(std::integral_constant<int, 2>{});
-    return launch(std::integral_constant<int, 1>{});
+    // two rows per CTA share the channel offsets (and gamma) while both fit comfortably
+    const bool two = 2 * row_smem <= 96 * 1024;
+    if (gamma != nullptr)
+      return two ? launch(std::integral_constant<int, 2>{}, std::true_type{})
+                 : launch(std::integral_constant<int, 1>{}, std::true_type{});
+    return two ? launch(std::integral_constant<int, 2>{}, std::false_type{})
+               : launch(std::integral_constant<int, 1>{}, std::false_type{});
   });
 }
 

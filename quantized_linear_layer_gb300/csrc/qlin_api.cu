@@ -379,16 +379,20 @@ qlin_status qlin_nvfp4_sf_to_mma(const uint8_t* sf_rows, int64_t rows, int64_t K
   QLIN_LAUNCH(launch_nvfp4_sf_to_mma(sf_rows, rows, K, sf_mma, stream), "nvfp4_sf_to_mma launch");
 }
 
-qlin_status qlin_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const int32_t* perm,
-                             int64_t S, qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
-                             qlin_sf_layout sf_layout, cudaStream_t stream) {
+// Argument checks shared by the NVFP4 quantizer and its fused RMSNorm form
+// (gamma != nullptr), then the launch.
+static qlin_status quant_nvfp4_checked(const char* name, const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K,
+                                       const void* gamma, float eps, const int32_t* perm, int64_t S,
+                                       qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
+                                       qlin_sf_layout sf_layout, cudaStream_t stream) {
   QLIN_REQUIRE(sf_layout == QLIN_SF_ROWS || (sf_layout == QLIN_SF_MMA && (K + S) % 64 == 0), QLIN_ERR_INVALID_ARG,
                "sf_layout must be QLIN_SF_ROWS, or QLIN_SF_MMA with K+S a multiple of 64");
   QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");
   QLIN_REQUIRE(mode == QLIN_NVFP4_RESIDUAL || mode == QLIN_NVFP4_DUPLICATE, QLIN_ERR_INVALID_ARG, "bad mode");
+  QLIN_REQUIRE(eps >= 0.0f && eps <= 3.4e38f, QLIN_ERR_INVALID_ARG, "eps must be a finite number >= 0");
   QLIN_REQUIRE(rows >= 0 && rows <= kMaxDim && K > 0, QLIN_ERR_INVALID_ARG, "bad sizes rows=%lld K=%lld",
                (long long)rows, (long long)K);
-  QLIN_REQUIRE(K * dtype_bytes(x_dtype) <= 160 * 1024, QLIN_ERR_UNSUPPORTED,
+  QLIN_REQUIRE(K * dtype_bytes(x_dtype) <= (gamma ? 96 : 160) * 1024, QLIN_ERR_UNSUPPORTED,
                "a row of %lld elements does not fit the shared-memory staging buffer", (long long)K);
   QLIN_REQUIRE(S >= 0 && S <= K && S % 16 == 0, QLIN_ERR_INVALID_ARG, "S=%lld must be a multiple of 16 in [0, K]",
                (long long)S);
@@ -399,9 +403,24 @@ qlin_status qlin_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, in
   QLIN_REQUIRE(aligned16(x) && aligned16(q) && aligned16(perm), QLIN_ERR_ALIGNMENT,
                "x, q and perm must be 16-byte aligned");
   QLIN_REQUIRE((reinterpret_cast<uintptr_t>(g) & 3u) == 0, QLIN_ERR_ALIGNMENT, "g must be 4-byte aligned");
+  QLIN_REQUIRE(aligned16(gamma), QLIN_ERR_ALIGNMENT, "gamma must be 16-byte aligned");
   QLIN_DEVICE();
-  QLIN_LAUNCH(launch_quant_nvfp4(x, x_dtype, rows, K, perm, S, mode, g, q, sf, sf_layout, stream),
-              "quant_nvfp4 launch");
+  QLIN_LAUNCH(launch_quant_nvfp4(x, x_dtype, rows, K, perm, S, mode, g, q, sf, sf_layout, gamma, eps, stream), name);
+}
+
+qlin_status qlin_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const int32_t* perm,
+                             int64_t S, qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
+                             qlin_sf_layout sf_layout, cudaStream_t stream) {
+  return quant_nvfp4_checked("quant_nvfp4 launch", x, x_dtype, rows, K, nullptr, 0.0f, perm, S, mode, g, q, sf,
+                             sf_layout, stream);
+}
+
+qlin_status qlin_rmsnorm_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const void* gamma,
+                                     float eps, const int32_t* perm, int64_t S, qlin_nvfp4_mode mode, const float* g,
+                                     uint8_t* q, uint8_t* sf, qlin_sf_layout sf_layout, cudaStream_t stream) {
+  QLIN_REQUIRE(rows == 0 || gamma != nullptr, QLIN_ERR_INVALID_ARG, "null gamma");
+  return quant_nvfp4_checked("rmsnorm_quant_nvfp4 launch", x, x_dtype, rows, K, gamma, eps, perm, S, mode, g, q, sf,
+                             sf_layout, stream);
 }
 
 qlin_status qlin_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,

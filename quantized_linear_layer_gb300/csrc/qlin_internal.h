@@ -82,7 +82,7 @@ cudaError_t launch_arc_perm(const void* x, qlin_dtype x_dtype, int64_t rows, int
 
 cudaError_t launch_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const int32_t* perm,
                                int64_t S, qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
-                               qlin_sf_layout sf_layout, cudaStream_t stream);
+                               qlin_sf_layout sf_layout, const void* gamma, float eps, cudaStream_t stream);
 
 cudaError_t launch_nvfp4_sf_to_mma(const uint8_t* src, int64_t rows, int64_t K, uint8_t* dst, cudaStream_t stream);
 

@@ -11,6 +11,8 @@ Operations (sizes as flags):
   w8a8         qlin_w8a8_gemm, A [T][K] int8, B [N][K] int8, per-token / per-channel scales, bf16 out
   nvfp4_quant  qlin_quant_nvfp4, X [T][K] fp16 with S residual channels, MMA scale layout
   nvfp4_gemm   qlin_nvfp4_gemm, A [T][K] and B [N][K] NVFP4 (made by the quantizer), bf16 out
+  rmsnorm_nvfp4  qlin_rmsnorm_quant_nvfp4, X [T][K] fp16, gamma [K], S residual channels, MMA scale layout
+  rmsnorm_int8   qlin_rmsnorm_quant, X [T][K] fp16, gamma [K], per-token int8
   fp8_quant    qlin_quant_fp8, X [T][K] fp16, per-row E4M3
   fp8_gemm     qlin_fp8_gemm, A [T][K] and B [N][K] E4M3 (made by the quantizer), bias, bf16 out
 
@@ -94,6 +96,21 @@ def _setup(args, q, torch):
         out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
         return lambda i: q.qlin_nvfp4_gemm(qa, sfa, ws[i % copies][0], ws[i % copies][1], ga, ws[i % copies][2], out)
 
+    if args.op in ("rmsnorm_nvfp4", "rmsnorm_int8"):
+        xs = [randn((T, K), torch.float16) for _ in range(copies)]
+        gam = (torch.rand(K, device="cuda", generator=g) + 0.5).half()
+        if args.op == "rmsnorm_int8":
+            qc = torch.empty((T, K), dtype=torch.int8, device="cuda")
+            sc = torch.empty(T, dtype=torch.float32, device="cuda")
+            return lambda i: q.qlin_rmsnorm_quant(xs[i % copies], gam, 1e-6, qc, sc)
+        S = args.S
+        perm = torch.randperm(K, generator=torch.Generator().manual_seed(args.seed)).to(torch.int32).cuda()
+        gx = torch.full((1,), 6.0 / 2688.0, dtype=torch.float32, device="cuda")
+        qc = torch.empty((T, (K + S) // 2), dtype=torch.uint8, device="cuda")
+        sf = torch.empty(q.qlin_nvfp4_sf_bytes(T, K + S, q.QLIN_SF_MMA), dtype=torch.uint8, device="cuda")
+        return lambda i: q.qlin_rmsnorm_quant_nvfp4(xs[i % copies], gam, 1e-6, gx, qc, sf, perm=perm, S=S,
+                                                    sf_layout=q.QLIN_SF_MMA)
+
     if args.op == "fp8_quant":
         xs = [randn((T, K), torch.float16) for _ in range(copies)]
         qc = torch.empty((T, K), dtype=torch.uint8, device="cuda")
@@ -119,7 +136,7 @@ def _setup(args, q, torch):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("op", choices=["w4a16", "w4a16_group", "int8_quant", "w8a8", "nvfp4_quant", "nvfp4_gemm",
-                                   "fp8_quant", "fp8_gemm"])
+                                   "fp8_quant", "fp8_gemm", "rmsnorm_nvfp4", "rmsnorm_int8"])
     ap.add_argument("--T", type=int, default=1)
     ap.add_argument("--N", type=int, default=4096)
     ap.add_argument("--K", type=int, default=4096)

@@ -118,6 +118,15 @@ def test_rejects_bad_arguments_without_gpu(built):
     assert L.qlin_rmsnorm_quant(P(16), 0, 4, 40, P(16), F(1e-6), 0, P(16), P(16), None) == 2
     assert L.qlin_rmsnorm_quant(P(16), 0, 4, 64, P(24), F(1e-6), 1, P(16), P(16), None) == 2
     assert L.qlin_rmsnorm_quant(None, 0, 0, 64, None, F(1e-6), 0, None, None, None) == 0
+    # fused RMSNorm + NVFP4: null gamma, negative eps, misaligned gamma, S not a multiple
+    # of 16, a row above 96 KB; an empty problem needs no pointers
+    assert L.qlin_rmsnorm_quant_nvfp4(P(16), 0, 4, 64, None, F(1e-6), None, 0, 0, P(16), P(16), P(16), 0, None) == 1
+    assert L.qlin_rmsnorm_quant_nvfp4(P(16), 0, 4, 64, P(16), F(-1.0), None, 0, 0, P(16), P(16), P(16), 0, None) == 1
+    assert L.qlin_rmsnorm_quant_nvfp4(P(16), 0, 4, 64, P(24), F(1e-6), None, 0, 0, P(16), P(16), P(16), 0, None) == 2
+    assert L.qlin_rmsnorm_quant_nvfp4(P(16), 2, 4, 24608, P(16), F(1e-6), None, 0, 0, P(16), P(16), P(16), 0,
+                                      None) == 3
+    assert L.qlin_rmsnorm_quant_nvfp4(P(16), 0, 4, 64, P(16), F(1e-6), None, 8, 0, P(16), P(16), P(16), 0, None) == 1
+    assert L.qlin_rmsnorm_quant_nvfp4(None, 0, 0, 64, None, F(1e-6), None, 0, 0, None, None, None, 0, None) == 0
     # perm K limit
     assert L.qlin_arc_perm(P(16), 0, 4, 32768, P(16), None) == 1
     msg = L.qlin_last_error_message()

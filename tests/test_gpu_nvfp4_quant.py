@@ -191,9 +191,8 @@ def test_quant_nvfp4_mma_scale_layout(qlin_gpu, rows, S, mode):
 @pytest.mark.parametrize("rows,K,dtype,S,with_perm", [(5, 40960, "f32", 0, False), (7, 16384, "f16", 128, True),
                                                      (601, 1024, "bf16", 64, True)])
 def test_quant_nvfp4_row_staging(qlin_gpu, rows, K, dtype, S, with_perm):
-    """Rows staged through one buffer (160 KB fp32 rows), two buffers of one row
-    (64 KB rows), and two buffers of two rows over many items per CTA (601
-    rows: an odd last item)."""
+    """One staged row per CTA (160 KB fp32 rows), two per CTA (32 KB fp16 rows),
+    and 601 rows of two per CTA (an odd last CTA)."""
     rng = np.random.default_rng(rows + K)
     x = rng.standard_normal((rows, K)).astype(np.float32)
     if dtype == "f16":

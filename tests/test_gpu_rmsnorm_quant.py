@@ -1,6 +1,7 @@
 """RMSNorm fused with the per-token quantizers on the GPU against the CPU
 oracle: codes and scales bit for bit, int8 and E4M3 outputs, 16-bit and
-float32 inputs, rows held in registers and rows read twice."""
+float32 inputs, rows held in registers and rows read twice; and the NVFP4 /
+ARCQuant form (codes and block scales bit for bit)."""
 
 import numpy as np
 import pytest
@@ -8,6 +9,7 @@ import torch
 
 import oracle
 from quantized_linear_layer_gb300 import inputs
+from conftest import sf_rows_to_mma
 
 pytestmark = pytest.mark.gpu
 
@@ -47,3 +49,43 @@ def test_rmsnorm_quant_bit_exact(qlin_gpu, fmt, dtype, k, eps):
     got = q.cpu().numpy().view(np.uint8)
     bad = np.argwhere(got != rq.view(np.uint8))
     assert bad.size == 0, "first mismatches (row, col): %s" % bad[:5].tolist()
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("k,eps,S,mode,layout", [
+    (4096, 1e-6, 128, 0, "rows"),
+    (8192, 1e-5, 256, 0, "mma"),
+    (1024, 0.0, 0, 0, "rows"),         # eps = 0 with an all-zero row; no residual channels
+    (4160, 1e-6, 64, 1, "mma"),        # duplicated (weight-side) columns
+])
+def test_rmsnorm_quant_nvfp4_bit_exact(qlin_gpu, dtype, k, eps, S, mode, layout):
+    """RMSNorm fused with the NVFP4 / ARCQuant quantizer: codes and block scales
+    bit for bit, g and perm calibrated by the oracle on the normalized rows;
+    47 rows (an odd last pair of staged rows)."""
+    rows = 47
+    rng = np.random.default_rng(k + S)
+    x = _rows(43, rows, k)
+    gam = rng.uniform(0.5, 1.5, size=k).astype(np.float32)
+    gam[5] = 6.0                                    # one strong channel of gamma
+    xt = torch.from_numpy(x).to(dtype).cuda()
+    gt = torch.from_numpy(gam).to(dtype).cuda()
+    xo, go = xt.float().cpu().numpy(), gt.float().cpu().numpy()
+    y = oracle.rmsnorm_rows(xo, go, eps)
+    g = np.float32(oracle.nvfp4_global_scale(y))
+    perm = oracle.arc_perm(y)
+    sf_layout = qlin_gpu.QLIN_SF_ROWS if layout == "rows" else qlin_gpu.QLIN_SF_MMA
+    q = torch.empty((rows, (k + S) // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(qlin_gpu.qlin_nvfp4_sf_bytes(rows, k + S, sf_layout), dtype=torch.uint8, device="cuda")
+    qlin_gpu.qlin_rmsnorm_quant_nvfp4(xt, gt, eps, torch.tensor([g]).cuda(), q, sf,
+                                      perm=torch.from_numpy(perm).cuda(), S=S, mode=mode, sf_layout=sf_layout)
+    torch.cuda.synchronize()
+    assert qlin_gpu.qlin_get_device_error() == 0
+    if mode == 0:
+        rq, rsf = oracle.rmsnorm_arc_quantize_activation(xo, go, eps, perm, S, g)
+    else:
+        rq, rsf = oracle.arc_quantize_weight(y, perm, S, g)
+    want_sf = rsf.reshape(-1) if layout == "rows" else sf_rows_to_mma(rsf)
+    assert np.array_equal(sf.cpu().numpy(), want_sf)
+    got = q.cpu().numpy()
+    bad = np.argwhere(got != oracle.pack_u4(rq))
+    assert bad.size == 0, "first mismatches (row, byte): %s" % bad[:5].tolist()

@@ -679,6 +679,30 @@ def test_rmsnorm_sum_order_bound():
     r_implied = np.median(x64 / y.astype(np.float64), axis=1)
     assert np.all(np.abs(r_implied - r_exact) <= 8192 * 2.0 ** -24 * r_exact)
 
+def pin_rmsnorm_arc_unit_rms():
+    """Rows of +-1 with eps = 0 have mean of squares exactly 1, so the RMSNorm
+    output is x . gamma exactly; the fused NVFP4 quantizer must then equal the
+    plain quantizer of the reordered values x[i, perm[j]] . gamma[perm[j]],
+    built here element by element (gamma travels with its channel)."""
+    rng = np.random.default_rng(16)
+    rows, k, s_res = 6, 256, 32
+    x = np.where(rng.random((rows, k)) < 0.5, -1.0, 1.0).astype(np.float32)
+    gamma = rng.uniform(0.1, 4.0, size=k).astype(np.float32)
+    perm = rng.permutation(k).astype(np.int32)
+    ys = np.empty((rows, k), dtype=np.float32)
+    for i in range(rows):
+        for j in range(k):
+            ys[i, j] = x[i, perm[j]] * gamma[perm[j]]
+    g = np.float32(oracle.nvfp4_global_scale(ys))
+    q, sf = oracle.rmsnorm_arc_quantize_activation(x, gamma, 0.0, perm, s_res, g)
+    rq, rsf = oracle.arc_quantize_activation(ys, None, s_res, g)
+    assert np.array_equal(q, rq) and np.array_equal(sf, rsf)
+
+
+def test_rmsnorm_arc_unit_rms():
+    pin_rmsnorm_arc_unit_rms()
+
+
 def _mut_e2m1_ties_odd(monkeypatch):
     orig = ofmt._nearest_code
 
@@ -776,9 +800,19 @@ def _mut_rmsnorm_mean_k_minus_1(monkeypatch):
     return pin_rmsnorm_formula
 
 
+def _mut_rmsnorm_arc_gamma_reordered(monkeypatch):
+    def bad(x, gamma, eps, perm, s_res, g):
+        y = oquant.rmsnorm_rows(x, np.ones_like(gamma), eps)[:, perm] * np.asarray(gamma, dtype=np.float32)
+        return oquant.arc_quantize_activation(y.astype(np.float32), None, s_res, g)
+
+    monkeypatch.setattr(oracle, "rmsnorm_arc_quantize_activation", bad)
+    return pin_rmsnorm_arc_unit_rms
+
+
 MUTATIONS = [_mut_e2m1_ties_odd, _mut_azp_sign, _mut_azp_adj_axis, _mut_residual_sign,
              _mut_w8a8_transposed, _mut_w4_zero_dropped, _mut_nvfp4_scale_not_decoded, _mut_sym_qmax,
-             _mut_fp8_scale_447, _mut_fp8_scales_swapped, _mut_rmsnorm_mean_k_minus_1]
+             _mut_fp8_scale_447, _mut_fp8_scales_swapped, _mut_rmsnorm_mean_k_minus_1,
+             _mut_rmsnorm_arc_gamma_reordered]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
