@@ -62,6 +62,15 @@ from .quant import (  # noqa: F401
     arc_quantize_activation,
     arc_quantize_weight,
 )
+from .mx import (  # noqa: F401
+    MX_BLOCK,
+    MX_EMAX,
+    mx_block_exponent,
+    mx_quantize,
+    mx_dequantize,
+    mx_gemm_reference,
+    e8m0_decode,
+)
 from .gemm import (  # noqa: F401
     w4a16_reference,
     w4a16_reference_packed,

@@ -17,6 +17,7 @@ import oracle
 from oracle import formats as ofmt
 from oracle import gemm as ogemm
 from oracle import quant as oquant
+from oracle import mx as oquant_mx
 from conftest import load_golden
 
 F32 = np.float32
@@ -703,6 +704,107 @@ def test_rmsnorm_arc_unit_rms():
     pin_rmsnorm_arc_unit_rms()
 
 
+# ---- MX block-scaled formats (MXFP8, MXFP4) ----
+
+def _pad32(v):
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, :len(v)] = np.asarray(v, dtype=np.float32)
+    return x
+
+
+def pin_mx_page_examples():
+    g = load_golden("mx_examples.json")
+    assert oracle.MX_EMAX["e4m3"] == g["emax"]["e4m3"] and oracle.MX_EMAX["e2m1"] == g["emax"]["e2m1"]
+    # MXFP4: scale 2^(floor(log2 2.4) - 2) = 0.5; 2.4 / 0.5 = 4.8 -> 4 -> 2.0, error 0.4
+    x = _pad32(g["mxfp4_block"])
+    q, sf = oracle.mx_quantize(x, "e2m1")
+    assert oracle.e8m0_decode(sf)[0, 0] == g["mxfp4_scale_printed"]
+    deq = oracle.mx_dequantize(q, sf, "e2m1")[0]
+    i = int(np.argmax(np.abs(x[0])))
+    m = g["mxfp4_max"]
+    assert x[0, i] == np.float32(m["x"]) and oracle.e2m1_decode(q[0, i]) == m["value"]
+    assert deq[i] == m["dequant_printed"] and abs(abs(deq[i] - x[0, i]) - m["error_printed"]) < 1e-6
+    # MXFP8 of the eight weights: the printed MSE (three significant digits)
+    w = _pad32(g["mxfp8_weights"])
+    q8, sf8 = oracle.mx_quantize(w, "e4m3")
+    err = oracle.mx_dequantize(q8, sf8, "e4m3")[0, :8] - w[0, :8].astype(np.float64)
+    assert abs(np.mean(err ** 2) - g["mxfp8_mse_printed"]) <= 0.005e-3
+
+
+def test_mx_page_examples():
+    pin_mx_page_examples()
+
+
+def test_mx_scaled_max_range():
+    """The block maximum over its scale lies in [2^e_max, 2^(e_max+1)) wherever
+    the exponent is not clamped; the scale is a power of two; every element's
+    code is the nearest value of the element format to x / scale."""
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((6, 256)) * np.exp(rng.uniform(-20, 20, size=(6, 1)))).astype(np.float32)
+    for fmt, top in (("e4m3", 448.0), ("e2m1", 6.0)):
+        q, sf = oracle.mx_quantize(x, fmt)
+        scale = oracle.e8m0_decode(sf)
+        amax = np.abs(x.reshape(6, 8, 32)).max(axis=2).astype(np.float64)
+        r = amax / scale
+        emax = oracle.MX_EMAX[fmt]
+        assert np.all((r >= 2.0 ** emax) & (r < 2.0 ** (emax + 1)))
+        dec = oracle.e4m3_decode(q) if fmt == "e4m3" else oracle.e2m1_decode(q)
+        y = x.astype(np.float64) / np.repeat(scale, 32, axis=1)
+        table = oracle.e4m3_finite_magnitudes() if fmt == "e4m3" else np.array([0, .5, 1, 1.5, 2, 3, 4, 6.])
+        best = np.abs(np.abs(np.minimum(np.abs(y), top))[..., None] - table).min(axis=-1)
+        assert np.all(np.abs(np.abs(dec) - np.minimum(np.abs(y), top)) == best)
+
+
+def test_mx_power_of_two_invariance_and_edges():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((3, 64)).astype(np.float32)
+    for fmt in ("e4m3", "e2m1"):
+        q, sf = oracle.mx_quantize(x, fmt)
+        for j in (-30, -1, 7, 40):
+            q2, sf2 = oracle.mx_quantize(x * np.float32(2.0 ** j), fmt)
+            assert np.array_equal(q2, q) and np.array_equal(sf2.astype(int), sf.astype(int) + j)
+        z = np.zeros((1, 32), dtype=np.float32)
+        qz, sfz = oracle.mx_quantize(z, fmt)
+        assert sfz[0, 0] == 0 and not np.any(qz)
+        big = np.full((1, 32), 3.0e38, dtype=np.float32)             # floor(log2) = 127: unclamped
+        _, sfb = oracle.mx_quantize(big, fmt)
+        assert int(sfb[0, 0]) == 127 + 127 - oracle.MX_EMAX[fmt]
+        tiny = np.full((1, 32), 1e-45, dtype=np.float32)             # subnormal: exponent clamped to -127
+        _, sft = oracle.mx_quantize(tiny, fmt)
+        assert sft[0, 0] == 0
+
+
+def pin_mx_gemm_brute_force():
+    rng = np.random.default_rng(23)
+    T, N, K = 2, 3, 64
+    e2m1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for fmt in ("e4m3", "e2m1"):
+        hi = 256 if fmt == "e4m3" else 16
+        qa = rng.integers(0, hi, size=(T, K)).astype(np.uint8)
+        qb = rng.integers(0, hi, size=(N, K)).astype(np.uint8)
+        if fmt == "e4m3":
+            qa[(qa & 0x7F) == 0x7F] = 0x21
+            qb[(qb & 0x7F) == 0x7F] = 0xA2
+        sfa = rng.integers(100, 150, size=(T, K // 32)).astype(np.uint8)
+        sfb = rng.integers(100, 150, size=(N, K // 32)).astype(np.uint8)
+        y = oracle.mx_gemm_reference(qa, sfa, qb, sfb, fmt)
+
+        def val(code):
+            if fmt == "e4m3":
+                return _e4m3_value(code)
+            return (-1.0 if code & 8 else 1.0) * e2m1[code & 7]
+
+        for t in range(T):
+            for n in range(N):
+                want = sum(val(qa[t, k]) * 2.0 ** (int(sfa[t, k // 32]) - 127) *
+                           val(qb[n, k]) * 2.0 ** (int(sfb[n, k // 32]) - 127) for k in range(K))
+                assert abs(y[t, n] - want) <= 1e-12 * (1 + abs(want)), (fmt, t, n)
+
+
+def test_mx_gemm_brute_force():
+    pin_mx_gemm_brute_force()
+
+
 def _mut_e2m1_ties_odd(monkeypatch):
     orig = ofmt._nearest_code
 
@@ -809,10 +911,22 @@ def _mut_rmsnorm_arc_gamma_reordered(monkeypatch):
     return pin_rmsnorm_arc_unit_rms
 
 
+def _mut_mx_emax_e4m3_7(monkeypatch):
+    monkeypatch.setitem(oquant_mx.MX_EMAX, "e4m3", 7)
+    return pin_mx_page_examples
+
+
+def _mut_mx_scales_swapped(monkeypatch):
+    orig = oquant_mx.mx_gemm_reference
+    monkeypatch.setattr(oracle, "mx_gemm_reference",
+                        lambda qa, sfa, qb, sfb, fmt: orig(qa, np.resize(sfb, sfa.shape), qb, np.resize(sfa, sfb.shape), fmt))
+    return pin_mx_gemm_brute_force
+
+
 MUTATIONS = [_mut_e2m1_ties_odd, _mut_azp_sign, _mut_azp_adj_axis, _mut_residual_sign,
              _mut_w8a8_transposed, _mut_w4_zero_dropped, _mut_nvfp4_scale_not_decoded, _mut_sym_qmax,
              _mut_fp8_scale_447, _mut_fp8_scales_swapped, _mut_rmsnorm_mean_k_minus_1,
-             _mut_rmsnorm_arc_gamma_reordered]
+             _mut_rmsnorm_arc_gamma_reordered, _mut_mx_emax_e4m3_7, _mut_mx_scales_swapped]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
