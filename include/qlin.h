@@ -90,6 +90,12 @@ typedef enum {
   QLIN_QFMT_FP8_E4M3 = 1  /* E4M3-FN codes, s = max|y| / 448 */
 } qlin_qfmt;
 
+/* MX element formats (one E8M0 scale per 32 elements along K). */
+typedef enum {
+  QLIN_MX_FP8_E4M3 = 0,  /* MXFP8: E4M3-FN elements, one byte each */
+  QLIN_MX_FP4_E2M1 = 1   /* MXFP4: E2M1 elements, two per byte (element 2i in the low nibble) */
+} qlin_mx_fmt;
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* qlin_status_string(qlin_status status);
 
@@ -452,6 +458,39 @@ qlin_status qlin_rmsnorm_quant(const void* x, qlin_dtype x_dtype, int64_t rows, 
  * Rows of up to 96 KB (K <= 49152 for 16-bit x, 24576 for F32): a row and
  * gamma are both staged in shared memory (QLIN_ERR_UNSUPPORTED above).
  * ---------------------------------------------------------------------- */
+/* ------------------------------------------------------------------------
+ * next 1 - MX block-scaled formats: MXFP8 and MXFP4
+ *
+ * qlin_quant_mx, per row, per block of 32 consecutive elements ("LLM and
+ * AIGC quantization", block-scaled formats: the E8M0 scale is the power of
+ * two 2^(floor(log2 absmax) - e_max), e_max = 8 for E4M3 and 2 for E2M1):
+ *   e  = floor(log2 max|x|) - e_max, clamped to [-127, 127]; -127 for a zero
+ *        block
+ *   sf = e + 127 (the E8M0 code);  q = E4M3 / E2M1(x . 2^-e)  (float32
+ *        multiply; round-to-nearest-even, saturating at 448 / 6, sign kept)
+ *   x     [rows][K] of x_dtype (F16, BF16 or F32), 16-byte aligned
+ *   q     out: MXFP8 uint8 [rows][K]; MXFP4 uint8 [rows][K/2] (16-byte aligned)
+ *   sf    out: E8M0 codes in sf_layout: QLIN_SF_ROWS [rows][K/32], or
+ *         QLIN_SF_MMA, the layout qlin_mx_gemm reads: 512-byte blocks of 128
+ *         rows x 4 scales, block (r/128, j/4) at ((r/128) . ceil(K/128) +
+ *         j/4) . 512, byte 16 (r%32) + 4 ((r%128)/32) + j%4 for row r, scale
+ *         j (bytes of padding rows and of a last partial group are left
+ *         unwritten)
+ * K a multiple of 32.
+ *
+ * qlin_mx_gemm: out[t][n] = sum_k dec(a)[t,k] 2^(sfa[t,k/32]-127) .
+ * dec(b)[n,k] 2^(sfb[n,k/32]-127), fp32 accumulation on the block-scaled
+ * tensor cores (the MMA applies both blocks' scales), one rounding to out.
+ *   a [T][K] / b [N][K] codes as qlin_quant_mx writes them; sfa, sfb in
+ *   QLIN_SF_MMA (16-byte aligned); out [T][N] F16 or BF16, N a multiple of 8.
+ *   K a multiple of 32 (MXFP8) or 64 (MXFP4).
+ * ---------------------------------------------------------------------- */
+int64_t qlin_mx_sf_bytes(int64_t rows, int64_t K, qlin_sf_layout sf_layout);
+qlin_status qlin_quant_mx(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, qlin_mx_fmt fmt, uint8_t* q,
+                          uint8_t* sf, qlin_sf_layout sf_layout, cudaStream_t stream);
+qlin_status qlin_mx_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb, int64_t T,
+                         int64_t N, int64_t K, qlin_mx_fmt fmt, void* out, qlin_dtype out_dtype, cudaStream_t stream);
+
 qlin_status qlin_rmsnorm_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const void* gamma,
                                      float eps, const int32_t* perm, int64_t S, qlin_nvfp4_mode mode, const float* g,
                                      uint8_t* q, uint8_t* sf, qlin_sf_layout sf_layout, cudaStream_t stream);

@@ -25,13 +25,15 @@ __all__ = [
     "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm",
     "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
     "QLIN_QFMT_INT8", "QLIN_QFMT_FP8_E4M3", "qlin_quant_fp8", "qlin_fp8_gemm", "qlin_rmsnorm_quant",
-    "qlin_rmsnorm_quant_nvfp4",
+    "qlin_rmsnorm_quant_nvfp4", "QLIN_MX_FP8_E4M3", "QLIN_MX_FP4_E2M1", "qlin_mx_sf_bytes", "qlin_quant_mx",
+    "qlin_mx_gemm",
 ]
 
 QLIN_F16, QLIN_BF16, QLIN_F32, QLIN_I32 = 0, 1, 2, 3
 QLIN_NVFP4_RESIDUAL, QLIN_NVFP4_DUPLICATE = 0, 1
 QLIN_SF_ROWS, QLIN_SF_MMA = 0, 1
 QLIN_QFMT_INT8, QLIN_QFMT_FP8_E4M3 = 0, 1
+QLIN_MX_FP8_E4M3, QLIN_MX_FP4_E2M1 = 0, 1
 
 _STATUS = {0: "QLIN_OK", 1: "QLIN_ERR_INVALID_ARG", 2: "QLIN_ERR_ALIGNMENT", 3: "QLIN_ERR_UNSUPPORTED",
            4: "QLIN_ERR_CUDA", 5: "QLIN_ERR_TIMEOUT"}
@@ -64,6 +66,9 @@ _SIGS = {
     "qlin_arc_perm": ([_P, _I32, _I64, _I64, _P, _P], _I32),
     "qlin_quant_nvfp4": ([_P, _I32, _I64, _I64, _P, _I64, _I32, _P, _P, _P, _I32, _P], _I32),
     "qlin_nvfp4_sf_bytes": ([_I64, _I64, _I32], _I64),
+    "qlin_mx_sf_bytes": ([_I64, _I64, _I32], _I64),
+    "qlin_quant_mx": ([_P, _I32, _I64, _I64, _I32, _P, _P, _I32, _P], _I32),
+    "qlin_mx_gemm": ([_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _I32, _P], _I32),
     "qlin_nvfp4_sf_to_mma": ([_P, _I64, _I64, _P, _P], _I32),
     "qlin_nvfp4_gemm": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I32, _P], _I32),
     "qlin_quant_fp8": ([_P, _I32, _I64, _I64, _P, _P, _P], _I32),
@@ -394,3 +399,42 @@ def qlin_rmsnorm_quant_nvfp4(x, gamma, eps, g, q, sf, perm=None, S=0, mode=QLIN_
     _check("qlin_rmsnorm_quant_nvfp4",
            lib().qlin_rmsnorm_quant_nvfp4(_ptr(x), _dtype_code(x), rows, k, _ptr(gamma), float(eps), _ptr(perm), S,
                                           mode, _ptr(g), _ptr(q), _ptr(sf), sf_layout, _stream(stream)))
+
+
+def qlin_mx_sf_bytes(rows, K, sf_layout=QLIN_SF_ROWS):
+    """Bytes of an MX (E8M0) scale buffer for `rows` rows of K elements, -1 if K % 32."""
+    return lib().qlin_mx_sf_bytes(rows, K, sf_layout)
+
+
+def qlin_quant_mx(x, q, sf, fmt=QLIN_MX_FP8_E4M3, sf_layout=QLIN_SF_ROWS, stream=None):
+    """MXFP8 / MXFP4 quantization of x [rows][K]: q uint8 [rows][K] (E4M3) or
+    [rows][K/2] (packed E2M1), sf uint8 E8M0 scales (one per 32 elements) in sf_layout."""
+    torch = _torch()
+    _need(x, torch.float16, torch.bfloat16, torch.float32, name="x")
+    _need(q, torch.uint8, name="q"); _need(sf, torch.uint8, name="sf")
+    rows, k = x.shape
+    if q.numel() < rows * (k if fmt == QLIN_MX_FP8_E4M3 else k // 2):
+        raise ValueError("q buffer too small")
+    if sf.numel() < qlin_mx_sf_bytes(rows, k, sf_layout):
+        raise ValueError("sf buffer too small")
+    _check("qlin_quant_mx", lib().qlin_quant_mx(_ptr(x), _dtype_code(x), rows, k, fmt, _ptr(q), _ptr(sf), sf_layout,
+                                               _stream(stream)))
+
+
+def qlin_mx_gemm(a, sfa, b, sfb, out, fmt=QLIN_MX_FP8_E4M3, stream=None):
+    """out[T][N] = dequant(a, sfa) . dequant(b, sfb)^T for MX codes a [T][..], b [N][..]
+    and E8M0 scales in the QLIN_SF_MMA layout; out fp16 or bf16."""
+    torch = _torch()
+    for t_, nm in ((a, "a"), (sfa, "sfa"), (b, "b"), (sfb, "sfb")):
+        _need(t_, torch.uint8, name=nm)
+    _need(out, torch.bfloat16, torch.float16, name="out")
+    t, n = a.shape[0], b.shape[0]
+    k = a.shape[1] * (1 if fmt == QLIN_MX_FP8_E4M3 else 2)
+    if b.shape[1] != a.shape[1]:
+        raise ValueError("a and b must have the same K")
+    if sfa.numel() < qlin_mx_sf_bytes(t, k, QLIN_SF_MMA) or sfb.numel() < qlin_mx_sf_bytes(n, k, QLIN_SF_MMA):
+        raise ValueError("scale buffers too small for the QLIN_SF_MMA layout")
+    if out.shape[0] != t or out.shape[1] != n:
+        raise ValueError("out must be [T][N]")
+    _check("qlin_mx_gemm", lib().qlin_mx_gemm(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), t, n, k, fmt, _ptr(out),
+                                             _dtype_code(out), _stream(stream)))

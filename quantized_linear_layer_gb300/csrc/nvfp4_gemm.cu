@@ -81,6 +81,56 @@ static_assert(kBN % 128 == 0 && kBN <= 256, "B tile is whole 128-row scale block
 
 enum { kSiteEmpty = 1, kSiteFull, kSiteAccFull, kSiteAccEmpty, kSiteDrain };
 
+// The block-scaled formats of this kernel.  A stage always holds 128 code
+// bytes per row (4 MMAs of 32 bytes along K), and a 512-byte scale block holds
+// 4 scales per row for 128 rows; one scale block covers 1 MMA (NVFP4, 4
+// scales of 16 elements per K = 64), 2 MMAs (MXFP4, 2 scales of 32 per
+// K = 64) or 4 MMAs (MXFP8, 1 scale of 32 per K = 32).  The MMA's scale-data
+// ID (instruction descriptor bits 4-5 for B, 29-30 for A) selects the bytes
+// of the 32-bit TMEM word that belong to it.
+enum { kFmtNvf4 = 0, kFmtMxf4 = 1, kFmtMxf8 = 2 };
+
+template <int F>
+struct BsFormat {
+  static constexpr int kElemsPerByte = F == kFmtMxf8 ? 1 : 2;
+  static constexpr int kScaleK = F == kFmtNvf4 ? 16 : 32;             // elements per scale
+  static constexpr int kMmaPerSfBlock = F == kFmtNvf4 ? 1 : (F == kFmtMxf4 ? 2 : 4);
+  static constexpr int kSfBlocksPerStage = kMmaPerStage / kMmaPerSfBlock;
+};
+
+// Instruction descriptor: E2M1 x E2M1 with E4M3 scales (NVFP4), E2M1 x E2M1
+// with E8M0 scales (MXFP4), E4M3 x E4M3 with E8M0 scales (MXFP8), fp32
+// accumulator, K-major A and B, M = 128, N = n.
+template <int F>
+__host__ __device__ constexpr uint32_t idesc_bs(int m, int n, uint32_t sf_id) {
+  const uint32_t elems = F == kFmtMxf8 ? 0u : (1u << 7) | (1u << 10);
+  const uint32_t e8m0 = F == kFmtNvf4 ? 0u : (1u << 23);
+  return elems | e8m0 | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24) |
+         (sf_id << 4) | (sf_id << 29);
+}
+
+template <int F>
+__device__ __forceinline__ void mma_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  if constexpr (F == kFmtNvf4) {
+    tc::mma_nvf4(d_tmem, a_desc, b_desc, idesc, sfa_tmem, sfb_tmem, accumulate);
+  } else if constexpr (F == kFmtMxf4) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p; }" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+  } else {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p; }" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+  }
+}
+
 // Tile order: groups of 8 M tiles walk all N tiles, so CTAs working at the
 // same time share operand tiles in L2.
 __device__ __forceinline__ void tile_coords(int tile, int mt_count, int nt_count, int& mt, int& nt) {
@@ -94,7 +144,8 @@ __device__ __forceinline__ void tile_coords(int tile, int mt_count, int nt_count
   nt = in / rows;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+template <int F>
+__global__ void __launch_bounds__(kThreads, 1) block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                  const __grid_constant__ CUtensorMap tmB,
                                                                  const uint8_t* __restrict__ sfa,
                                                                  const uint8_t* __restrict__ sfb, int T, int N,
@@ -106,8 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KB = K / 2;                       // packed bytes per row
-  const int KG = K / 64;                      // 64-element K blocks (one MMA each)
+  using Fmt = BsFormat<F>;
+  const int KB = K / Fmt::kElemsPerByte;      // code bytes per row
+  const int KG = (K / Fmt::kScaleK + 3) / 4;  // 4-scale groups per row (512-byte scale blocks per 128 rows)
   const int num_kb = (KB + kBKB - 1) / kBKB;  // stages per tile
   const int mt_count = (T + kBM - 1) / kBM, nt_count = (N + kBN - 1) / kBN;
   const int num_tiles = mt_count * nt_count;
@@ -171,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
           }
           const uint32_t dst = sbase + kSmemCodes + s * kCodeBytes;
           const uint32_t sf_dst = sbase + kSmemSf + s * kSfBytes;
-          const int kg0 = kb * kMmaPerStage;                  // first 64-element K block of the stage
-          const int nkg = min(kMmaPerStage, KG - kg0);        // blocks of this stage that exist
+          const int kg0 = kb * Fmt::kSfBlocksPerStage;        // first scale group of the stage
+          const int nkg = min(Fmt::kSfBlocksPerStage, KG - kg0);  // groups of this stage that exist
           // scales first, on their own barrier: the writer warps put them into
           // TMEM while the codes are still in flight
           tc::mbar_arrive_expect_tx(sf_full(s), (1 + nbs) * nkg * kSfBlock);
@@ -196,7 +248,6 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = tc::idesc_nvf4(kBM, kBN);
       bool issued_any = false;
       int it = 0;
       for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
@@ -222,9 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
 #pragma unroll
           for (int kk = 0; kk < kMmaPerStage; ++kk) {
             if (kk < kk_valid) {
-              tc::mma_nvf4(tmem, tc::sw128_kmajor_desc(a_base + 32 * kk), tc::sw128_kmajor_desc(b_base + 32 * kk),
-                           idesc, sf_t + kSfaCols * kk, sf_t + kMmaPerStage * kSfaCols + kSfbCols * kk,
-                           (kb > 0 || kk > 0) ? 1u : 0u);
+              constexpr int mpb = Fmt::kMmaPerSfBlock;
+              const int blk = kk / mpb;                       // the stage's scale block of this MMA
+              const uint32_t sf_id = static_cast<uint32_t>((kk % mpb) * (4 / mpb));
+              mma_bs<F>(tmem, tc::sw128_kmajor_desc(a_base + 32 * kk), tc::sw128_kmajor_desc(b_base + 32 * kk),
+                        idesc_bs<F>(kBM, kBN, sf_id), sf_t + kSfaCols * blk,
+                        sf_t + kMmaPerStage * kSfaCols + kSfbCols * blk, (kb > 0 || kk > 0) ? 1u : 0u);
             }
           }
           issued_any = true;
@@ -241,8 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
     }
   } else if (warp >= kSfWarp0) {
     // ---------------- scale-factor writers ----------------
-    // Slot layout: A scales of MMA kk in columns 4kk..4kk+3, then B scales of
-    // MMA kk in columns 16+8kk..16+8kk+7 (rows 0-127, then rows 128-255).
+    // Slot layout: A scale block j in columns 4j..4j+3, then B scale block j
+    // in columns 16+8j..16+8j+7 (rows 0-127, then rows 128-255).  The MX
+    // formats use the first 2 (MXFP4) or 1 (MXFP8) blocks; the rest are zero.
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int it = 0;
     for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
@@ -257,6 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
         uint32_t v[kSfColsPerStage];
 #pragma unroll
         for (int kk = 0; kk < kMmaPerStage; ++kk) {
+          if (kk >= BsFormat<F>::kSfBlocksPerStage) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[4 * kk + c] = 0u;
+#pragma unroll
+            for (int c = 0; c < 4 * (kBN / 128); ++c) v[kMmaPerStage * kSfaCols + kSfbCols * kk + c] = 0u;
+            continue;
+          }
           const uint4 w = tc::lds128(src + kSfBlock * kk);
           v[4 * kk] = w.x; v[4 * kk + 1] = w.y; v[4 * kk + 2] = w.z; v[4 * kk + 3] = w.w;
 #pragma unroll
@@ -281,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
     const int q = warp & 3;                      // TMEM lane quadrant this warp may access
     const int half = (warp - 2) / 4;             // column half of the 256-column tile
     pdl_wait();  // the global scales may come from the previous kernel
-    const float alpha = __ldg(g_a) * __ldg(g_b);
+    const float alpha = g_a != nullptr ? __ldg(g_a) * __ldg(g_b) : 1.0f;  // MX formats: no per-tensor scales
     for (int ti = 0; ti < my_tiles; ++ti) {
       bool ok = tc::mbar_wait(acc_full, ti & 1, err, kSiteAccFull);
       ok = __all_sync(0xffffffffu, ok);
@@ -362,19 +424,18 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_gemm_kernel(const __grid_co
   }
 }
 
-}  // namespace
-
-cudaError_t launch_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,
-                              int64_t T, int64_t N, int64_t K, const float* g_a, const float* g_b, void* out,
-                              qlin_dtype out_dtype, cudaStream_t stream) {
+template <int F>
+cudaError_t launch_block_scaled_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,
+                                     int64_t T, int64_t N, int64_t K, const float* g_a, const float* g_b, void* out,
+                                     qlin_dtype out_dtype, cudaStream_t stream) {
   if (T == 0 || N == 0) return cudaSuccess;
+  const uint64_t row_bytes = static_cast<uint64_t>(K / BsFormat<F>::kElemsPerByte);
   CUtensorMap tmA, tmB;
-  cudaError_t st = make_tmap_2d_u8(&tmA, a, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(T), kBKB, kBM,
-                                   /*swizzle_bytes=*/128);
+  cudaError_t st = make_tmap_2d_u8(&tmA, a, row_bytes, static_cast<uint64_t>(T), kBKB, kBM, /*swizzle_bytes=*/128);
   if (st != cudaSuccess) return st;
-  st = make_tmap_2d_u8(&tmB, b, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(N), kBKB, kBN, 128);
+  st = make_tmap_2d_u8(&tmB, b, row_bytes, static_cast<uint64_t>(N), kBKB, kBN, 128);
   if (st != cudaSuccess) return st;
-  st = cudaFuncSetAttribute(nvfp4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
+  st = cudaFuncSetAttribute(block_scaled_gemm_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
   if (st != cudaSuccess) return st;
   const int64_t tiles = ((T + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
@@ -390,8 +451,25 @@ cudaError_t launch_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, tmA, tmB, sfa, sfb, static_cast<int>(T), static_cast<int>(N),
-                            static_cast<int>(K), g_a, g_b, out, static_cast<int>(out_dtype), device_error_word());
+  return cudaLaunchKernelEx(&cfg, block_scaled_gemm_kernel<F>, tmA, tmB, sfa, sfb, static_cast<int>(T),
+                            static_cast<int>(N), static_cast<int>(K), g_a, g_b, out, static_cast<int>(out_dtype),
+                            device_error_word());
+}
+
+}  // namespace
+
+cudaError_t launch_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,
+                              int64_t T, int64_t N, int64_t K, const float* g_a, const float* g_b, void* out,
+                              qlin_dtype out_dtype, cudaStream_t stream) {
+  return launch_block_scaled_gemm<kFmtNvf4>(a, sfa, b, sfb, T, N, K, g_a, g_b, out, out_dtype, stream);
+}
+
+cudaError_t launch_mx_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb, int64_t T,
+                           int64_t N, int64_t K, qlin_mx_fmt fmt, void* out, qlin_dtype out_dtype,
+                           cudaStream_t stream) {
+  if (fmt == QLIN_MX_FP8_E4M3)
+    return launch_block_scaled_gemm<kFmtMxf8>(a, sfa, b, sfb, T, N, K, nullptr, nullptr, out, out_dtype, stream);
+  return launch_block_scaled_gemm<kFmtMxf4>(a, sfa, b, sfb, T, N, K, nullptr, nullptr, out, out_dtype, stream);
 }
 
 }  // namespace qlin

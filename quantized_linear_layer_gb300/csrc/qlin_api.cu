@@ -441,6 +441,48 @@ qlin_status qlin_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t*
   QLIN_LAUNCH(launch_nvfp4_gemm(a, sfa, b, sfb, T, N, K, g_a, g_b, out, out_dtype, stream), "nvfp4_gemm launch");
 }
 
+int64_t qlin_mx_sf_bytes(int64_t rows, int64_t K, qlin_sf_layout sf_layout) {
+  if (rows < 0 || K <= 0 || K % 32 != 0) return -1;
+  if (sf_layout == QLIN_SF_ROWS) return rows * (K / 32);
+  if (sf_layout == QLIN_SF_MMA) return (rows + 127) / 128 * ((K + 127) / 128) * 512;
+  return -1;
+}
+
+qlin_status qlin_quant_mx(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, qlin_mx_fmt fmt, uint8_t* q,
+                          uint8_t* sf, qlin_sf_layout sf_layout, cudaStream_t stream) {
+  QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");
+  QLIN_REQUIRE(fmt == QLIN_MX_FP8_E4M3 || fmt == QLIN_MX_FP4_E2M1, QLIN_ERR_INVALID_ARG, "unknown MX format %d",
+               static_cast<int>(fmt));
+  QLIN_REQUIRE(sf_layout == QLIN_SF_ROWS || sf_layout == QLIN_SF_MMA, QLIN_ERR_INVALID_ARG, "unknown sf_layout");
+  QLIN_REQUIRE(rows >= 0 && rows <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG,
+               "bad sizes rows=%lld K=%lld", (long long)rows, (long long)K);
+  QLIN_REQUIRE(K % 32 == 0, QLIN_ERR_INVALID_ARG, "K=%lld is not a multiple of 32", (long long)K);
+  if (rows == 0) return ok();
+  QLIN_REQUIRE(x && q && sf, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(x) && aligned16(q), QLIN_ERR_ALIGNMENT, "x and q must be 16-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_quant_mx(x, x_dtype, rows, K, fmt, q, sf, sf_layout, stream), "quant_mx launch");
+}
+
+qlin_status qlin_mx_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb, int64_t T,
+                         int64_t N, int64_t K, qlin_mx_fmt fmt, void* out, qlin_dtype out_dtype, cudaStream_t stream) {
+  QLIN_REQUIRE(fmt == QLIN_MX_FP8_E4M3 || fmt == QLIN_MX_FP4_E2M1, QLIN_ERR_INVALID_ARG, "unknown MX format %d",
+               static_cast<int>(fmt));
+  QLIN_REQUIRE(T >= 0 && T <= kMaxDim && N >= 0 && N <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG,
+               "bad sizes T=%lld N=%lld K=%lld", (long long)T, (long long)N, (long long)K);
+  const int64_t kmul = fmt == QLIN_MX_FP8_E4M3 ? 32 : 64;
+  QLIN_REQUIRE(K % kmul == 0, QLIN_ERR_INVALID_ARG, "K=%lld is not a multiple of %lld", (long long)K,
+               (long long)kmul);
+  QLIN_REQUIRE(out_dtype == QLIN_F16 || out_dtype == QLIN_BF16, QLIN_ERR_INVALID_ARG, "out_dtype must be F16 or BF16");
+  if (T == 0 || N == 0) return ok();
+  QLIN_REQUIRE(a && sfa && b && sfb && out, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(a) && aligned16(b) && aligned16(out) && aligned16(sfa) && aligned16(sfb), QLIN_ERR_ALIGNMENT,
+               "a, b, sfa, sfb and out must be 16-byte aligned");
+  QLIN_REQUIRE((N * 2) % 16 == 0, QLIN_ERR_ALIGNMENT, "the out row pitch (2N bytes) must be a multiple of 16");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_mx_gemm(a, sfa, b, sfb, T, N, K, fmt, out, out_dtype, stream), "mx_gemm launch");
+}
+
 qlin_status qlin_quant_fp8(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, uint8_t* q, float* scale,
                            cudaStream_t stream) {
   QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");

@@ -90,6 +90,11 @@ cudaError_t launch_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_
                               int64_t T, int64_t N, int64_t K, const float* g_a, const float* g_b, void* out,
                               qlin_dtype out_dtype, cudaStream_t stream);
 
+cudaError_t launch_quant_mx(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, qlin_mx_fmt fmt, uint8_t* q,
+                            uint8_t* sf, qlin_sf_layout sf_layout, cudaStream_t stream);
+cudaError_t launch_mx_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb, int64_t T,
+                           int64_t N, int64_t K, qlin_mx_fmt fmt, void* out, qlin_dtype out_dtype,
+                           cudaStream_t stream);
 cudaError_t launch_quant_fp8(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, uint8_t* q, float* scale,
                              cudaStream_t stream);
 

@@ -127,6 +127,18 @@ def test_rejects_bad_arguments_without_gpu(built):
                                       None) == 3
     assert L.qlin_rmsnorm_quant_nvfp4(P(16), 0, 4, 64, P(16), F(1e-6), None, 8, 0, P(16), P(16), P(16), 0, None) == 1
     assert L.qlin_rmsnorm_quant_nvfp4(None, 0, 0, 64, None, F(1e-6), None, 0, 0, None, None, None, 0, None) == 0
+    # MX: unknown format, K not a multiple of 32, misaligned x; GEMM: MXFP4 K not a
+    # multiple of 64, F32 out, out row pitch (N = 12); empty problems; scale sizes
+    assert L.qlin_quant_mx(P(16), 0, 4, 64, 2, P(16), P(16), 0, None) == 1
+    assert L.qlin_quant_mx(P(16), 0, 4, 48, 0, P(16), P(16), 0, None) == 1
+    assert L.qlin_quant_mx(P(24), 0, 4, 64, 1, P(16), P(16), 1, None) == 2
+    assert L.qlin_quant_mx(None, 0, 0, 64, 0, None, None, 0, None) == 0
+    assert L.qlin_mx_gemm(P(16), P(16), P(16), P(16), 4, 8, 96, 1, P(16), 0, None) == 1
+    assert L.qlin_mx_gemm(P(16), P(16), P(16), P(16), 4, 8, 96, 0, P(16), 2, None) == 1
+    assert L.qlin_mx_gemm(P(16), P(16), P(16), P(16), 4, 12, 96, 0, P(16), 0, None) == 2
+    assert L.qlin_mx_gemm(None, None, None, None, 0, 8, 96, 0, None, 0, None) == 0
+    assert L.qlin_mx_sf_bytes(130, 160, 1) == 2 * 2 * 512 and L.qlin_mx_sf_bytes(3, 96, 0) == 9
+    assert L.qlin_mx_sf_bytes(3, 100, 0) == -1
     # perm K limit
     assert L.qlin_arc_perm(P(16), 0, 4, 32768, P(16), None) == 1
     msg = L.qlin_last_error_message()
