@@ -11,6 +11,8 @@ Operations (sizes as flags):
   w8a8         qlin_w8a8_gemm, A [T][K] int8, B [N][K] int8, per-token / per-channel scales, bf16 out
   nvfp4_quant  qlin_quant_nvfp4, X [T][K] fp16 with S residual channels, MMA scale layout
   nvfp4_gemm   qlin_nvfp4_gemm, A [T][K] and B [N][K] NVFP4 (made by the quantizer), bf16 out
+  mxfp8_quant / mxfp4_quant  qlin_quant_mx, X [T][K] fp16, MMA scale layout
+  mxfp8_gemm / mxfp4_gemm    qlin_mx_gemm, A [T][K] and B [N][K] (made by the quantizer), bf16 out
   rmsnorm_nvfp4  qlin_rmsnorm_quant_nvfp4, X [T][K] fp16, gamma [K], S residual channels, MMA scale layout
   rmsnorm_int8   qlin_rmsnorm_quant, X [T][K] fp16, gamma [K], per-token int8
   fp8_quant    qlin_quant_fp8, X [T][K] fp16, per-row E4M3
@@ -96,6 +98,25 @@ def _setup(args, q, torch):
         out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
         return lambda i: q.qlin_nvfp4_gemm(qa, sfa, ws[i % copies][0], ws[i % copies][1], ga, ws[i % copies][2], out)
 
+    if args.op in ("mxfp8_quant", "mxfp4_quant", "mxfp8_gemm", "mxfp4_gemm"):
+        fmt = q.QLIN_MX_FP8_E4M3 if args.op.startswith("mxfp8") else q.QLIN_MX_FP4_E2M1
+        cb = 1 if fmt == q.QLIN_MX_FP8_E4M3 else 2
+
+        def mxq(rows, x):
+            qc = torch.empty((rows, K // cb), dtype=torch.uint8, device="cuda")
+            sf = torch.zeros(q.qlin_mx_sf_bytes(rows, K, q.QLIN_SF_MMA), dtype=torch.uint8, device="cuda")
+            q.qlin_quant_mx(x, qc, sf, fmt=fmt, sf_layout=q.QLIN_SF_MMA)
+            return qc, sf
+
+        if args.op.endswith("quant"):
+            xs = [randn((T, K), torch.float16) for _ in range(copies)]
+            qc, sf = mxq(T, xs[0])
+            return lambda i: q.qlin_quant_mx(xs[i % copies], qc, sf, fmt=fmt, sf_layout=q.QLIN_SF_MMA)
+        qa, sfa = mxq(T, randn((T, K), torch.float16))
+        ws = [mxq(N, randn((N, K), torch.float16) * 0.02) for _ in range(copies)]
+        out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+        return lambda i: q.qlin_mx_gemm(qa, sfa, ws[i % copies][0], ws[i % copies][1], out, fmt=fmt)
+
     if args.op in ("rmsnorm_nvfp4", "rmsnorm_int8"):
         xs = [randn((T, K), torch.float16) for _ in range(copies)]
         gam = (torch.rand(K, device="cuda", generator=g) + 0.5).half()
@@ -136,7 +157,8 @@ def _setup(args, q, torch):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("op", choices=["w4a16", "w4a16_group", "int8_quant", "w8a8", "nvfp4_quant", "nvfp4_gemm",
-                                   "fp8_quant", "fp8_gemm", "rmsnorm_nvfp4", "rmsnorm_int8"])
+                                   "fp8_quant", "fp8_gemm", "rmsnorm_nvfp4", "rmsnorm_int8", "mxfp8_quant",
+                                   "mxfp4_quant", "mxfp8_gemm", "mxfp4_gemm"])
     ap.add_argument("--T", type=int, default=1)
     ap.add_argument("--N", type=int, default=4096)
     ap.add_argument("--K", type=int, default=4096)
