@@ -150,7 +150,11 @@ qlin_status qlin_quant_w4_g128(const void* w, qlin_dtype w_dtype, int64_t N, int
  *           the symmetric zero-point 8 for every group
  *   group   128
  *   y       out, fp16 [T][N]
- * 1 <= T <= 64 (decode / skinny shapes), K a multiple of `group`.
+ * K a multiple of `group`; any T >= 0.  Up to 64 tokens run the decode /
+ * skinny kernels above.  More tokens (prefill) run a tcgen05 GEMM
+ * ("LLM and AIGC quantization", W4A16: dequantize next to the tensor cores,
+ * fp16 multiply, fp32 accumulate).  That GEMM rounds each weight once to
+ * fp16, (q - z) . s with (q - z) exact, before the fp32 accumulation.
  * ---------------------------------------------------------------------- */
 qlin_status qlin_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq,
                             const void* scales, const uint8_t* zeros, int64_t group, void* y,

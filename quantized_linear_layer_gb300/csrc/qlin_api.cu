@@ -176,7 +176,7 @@ qlin_status qlin_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, cons
                             const void* scales, const uint8_t* zeros, int64_t group, void* y,
                             cudaStream_t stream) {
   QLIN_REQUIRE(group == 128, QLIN_ERR_UNSUPPORTED, "group size %lld (only 128 is built)", (long long)group);
-  QLIN_REQUIRE(T >= 0 && T <= 64, QLIN_ERR_INVALID_ARG, "T=%lld outside [0, 64]", (long long)T);
+  QLIN_REQUIRE(T >= 0 && T <= kMaxDim, QLIN_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
   QLIN_REQUIRE(N >= 0 && N <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad sizes N=%lld K=%lld",
                (long long)N, (long long)K);
   QLIN_REQUIRE(K % group == 0, QLIN_ERR_INVALID_ARG, "K=%lld is not a multiple of the group size", (long long)K);
@@ -197,7 +197,7 @@ qlin_status qlin_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int cou
   QLIN_REQUIRE(count >= 1 && count <= QLIN_W4A16_MAX_GROUP, QLIN_ERR_INVALID_ARG, "count=%d outside [1, %d]", count,
                QLIN_W4A16_MAX_GROUP);
   QLIN_REQUIRE(N && wq && scales && zeros && y, QLIN_ERR_INVALID_ARG, "null host array");
-  QLIN_REQUIRE(T >= 0 && T <= 64, QLIN_ERR_INVALID_ARG, "T=%lld outside [0, 64]", (long long)T);
+  QLIN_REQUIRE(T >= 0 && T <= kMaxDim, QLIN_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
   QLIN_REQUIRE(K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad K=%lld", (long long)K);
   QLIN_REQUIRE(K % group == 0, QLIN_ERR_INVALID_ARG, "K=%lld is not a multiple of the group size", (long long)K);
   int64_t total = 0;

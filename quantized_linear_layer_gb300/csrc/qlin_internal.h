@@ -50,6 +50,10 @@ bool w4a16_skinny_supported(int64_t T, int64_t N, int64_t K);
 cudaError_t launch_w4a16_skinny_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
                                         const uint8_t* const* wq, const void* const* scales,
                                         const uint8_t* const* zeros, void* const* y, cudaStream_t stream);
+// W4A16 for many tokens (prefill) on the tcgen05 tensor cores.
+bool w4a16_prefill_supported(int64_t T, int64_t N, int64_t K);
+cudaError_t launch_w4a16_prefill(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq,
+                                 const void* scales, const uint8_t* zeros, void* y, cudaStream_t stream);
 cudaError_t launch_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
                                       const uint8_t* const* wq, const void* const* scales,
                                       const uint8_t* const* zeros, void* const* y, cudaStream_t stream);

@@ -367,6 +367,12 @@ cudaError_t launch_w4a16_mma(const void* x, int64_t T, int64_t N, int64_t K, con
 // the streamed tensor-core skinny kernel (more tokens in chunks of 16, each
 // chunk one pass over the weights), and the staged kernel above for shapes
 // the skinny kernel has no plan for.
+// Above this many tokens the tensor-core prefill GEMM runs instead of the
+// skinny kernel (16 tokens per launch, the weights read once per launch):
+// measured on the Llama-2-7B shapes, the skinny launches win up to 32 tokens,
+// the prefill GEMM from 48 on.
+constexpr int64_t kW4a16PrefillMinT = 32;
+
 cudaError_t launch_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
                                       const uint8_t* const* wq, const void* const* scales,
                                       const uint8_t* const* zeros, void* const* y, cudaStream_t stream) {
@@ -376,6 +382,19 @@ cudaError_t launch_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int c
   for (int p = 0; p < count; ++p) total += N[p];
   if (total == 0) return cudaSuccess;
   if (w4a16_gemv_supported(T, total, K)) return launch_w4a16_gemv_grouped(x, K, count, N, wq, scales, zeros, y, stream);
+  // many tokens: one tensor-core GEMM per matrix, weights dequantized on chip
+  if (T > kW4a16PrefillMinT) {
+    bool all = true;
+    for (int p = 0; p < count; ++p) all = all && (N[p] == 0 || w4a16_prefill_supported(T, N[p], K));
+    if (all) {
+      for (int p = 0; p < count; ++p) {
+        if (N[p] == 0) continue;
+        cudaError_t e = launch_w4a16_prefill(x, T, N[p], K, wq[p], scales[p], zeros[p], y[p], stream);
+        if (e != cudaSuccess) return e;
+      }
+      return cudaSuccess;
+    }
+  }
   constexpr int64_t kChunk = 16;
   const int64_t first = T < kChunk ? T : kChunk, last = T % kChunk;
   if (w4a16_skinny_supported(first, total, K) && (last == 0 || w4a16_skinny_supported(last, total, K))) {

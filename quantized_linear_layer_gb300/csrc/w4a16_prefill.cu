@@ -1,0 +1,389 @@
+// W4A16 beyond decode (prefill, many tokens): Y = X . W^T with uint4 g128
+// weights dequantized on the fly, on the tcgen05 tensor cores.
+//
+//   Y[t, n] = sum_k X[t, k] . ((q[n, k] - z[n, k / 128]) . s[n, k / 128])
+//
+// ("LLM and AIGC quantization: from number formats to W4A4", W4A16: the
+// weights stay 4-bit in memory and are dequantized to fp16 next to the
+// tensor cores, which multiply in fp16 and accumulate in fp32.)  Each weight
+// is rounded once to fp16 after its scale, (q - z) . s, with (q - z) exact.
+//
+// Design for GB300.  The weight tile is the MMA's A operand and is read from
+// tensor memory: dequantized in registers and written with tcgen05.st, so
+// only the packed codes (half a byte per weight) pass through shared memory.
+// The activations are the B operand, copied by TMA straight into the
+// 128-byte swizzled K-major layout the MMA reads.  One CTA per SM walks
+// 128 (weight rows) x 128 (tokens) output tiles; a K stage of 128 is one
+// quantization group, so each row needs one scale and one zero-point per
+// stage.  Two accumulators let a tile's epilogue run under the next tile's
+// MMAs.
+//
+//   warp 0       TMA producer: per stage the activation tile (128 tokens x
+//                128 K, two 64-element K blocks, 32 KB) and the packed codes
+//                (128 rows x 64 bytes in the 64-byte swizzle, 8 KB) into a
+//                4-stage ring.
+//   warp 1       TMEM allocation and the MMA issuer: 8 x tcgen05.mma
+//                kind::f16 (M = 128, N = 128, K = 16, A from TMEM) per stage
+//                into one of two 128-column fp32 accumulators.
+//   warps 2-13   dequantizers, three sets of four taking every third stage: lane
+//                l of the warp with TMEM lane quadrant q owns weight row
+//                32q + l, turns its 128 codes of the stage into 64 fp16 pairs
+//                and stores them into a 3-stage A ring in TMEM (64 columns
+//                per stage); the scale and zero-point of its next stage are
+//                loaded while it works on the current one.
+//   warps 14-17  epilogue: lane l of quadrant q owns weight row 32q + l and
+//                writes its 128 tokens, 32 at a time.
+// TMEM columns: [0, 256) the two accumulators, [256, 448) the A ring.
+// Every barrier wait is bounded; on expiry the kernel records the site in the
+// device error word, stops issuing work, waits (bounded) for copies and MMAs
+// already in flight, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "device_common.cuh"
+#include "qlin_internal.h"
+#include "tc_common.cuh"
+#include "tmap.h"
+
+namespace qlin {
+namespace {
+
+constexpr int kPfBM = 128;                          // weight rows per tile (MMA M)
+constexpr int kPfBN = 128;                          // tokens per tile (MMA N)
+constexpr int kPfBK = 128;                          // K per stage: one quantization group
+constexpr int kPfStg = 4;                           // shared-memory stages
+constexpr int kPfOpsA = 3;                          // TMEM stages of dequantized weights
+constexpr int kPfTmemCols = 512;
+constexpr int kPfTmemA = 2 * kPfBN;                 // A ring after the two accumulators
+constexpr int kPfSets = 3;                          // dequantizer sets of four warps
+constexpr int kPfWarpA0 = 2, kPfWarpE0 = kPfWarpA0 + 4 * kPfSets;
+constexpr int kPfThreads = (kPfWarpE0 + 4) * 32;
+constexpr int kPfXBytes = kPfBN * kPfBK * 2;        // 32 KB of fp16 activations
+constexpr int kPfWBytes = kPfBM * kPfBK / 2;        // 8 KB of packed codes
+constexpr int kPfStgBytes = kPfXBytes + kPfWBytes;  // 40 KB (a multiple of 1024)
+constexpr int kPfSmemBar = kPfStg * kPfStgBytes;
+constexpr int kPfNumBars = 2 * kPfStg + 2 * kPfOpsA + 5;
+constexpr int kPfSmemMisc = kPfSmemBar + kPfNumBars * 8;
+constexpr int kPfSmemTotal = kPfSmemMisc + 16 + 1024;  // + alignment slack
+static_assert(kPfSmemTotal <= 227 * 1024, "shared memory budget");
+static_assert(kPfTmemA + kPfOpsA * (kPfBK / 2) <= kPfTmemCols, "TMEM budget");
+static_assert(kPfStgBytes % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled tiles");
+
+enum { kPfSiteStgEmpty = 1, kPfSiteStgFull, kPfSiteAEmpty, kPfSiteAFull, kPfSiteAccEmpty, kPfSiteAccFull,
+       kPfSiteDrain };
+
+// Eight codes of one word (element k + i in bits 4i .. 4i+3) -> four words of
+// fp16 pairs ((k, k+1), (k+2, k+3), ...), each (q - z) . s rounded once.
+// Byte j of the word holds the pair; one byte permute copies it into both
+// halves and one mask leaves the low nibble in the low half's mantissa and
+// the high nibble four bits up in the high half's, under fp16 1024 (0x6400):
+// 1024 + q and 1024 + 16 q, both exact.  One fma with (1, 1/16) and
+// (-(1024 + z), -(64 + z)) gives q - z in both halves, exactly; one multiply
+// by s rounds.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t mul, uint32_t add, __half2 s2, uint32_t* out) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t t = __byte_perm(w, 0u, 0x4040u + 0x0101u * j);
+    const uint32_t v = (t & 0x00F0000Fu) | 0x64006400u;
+    const __half2 d = __hfma2(*reinterpret_cast<const __half2*>(&v), *reinterpret_cast<const __half2*>(&mul),
+                              *reinterpret_cast<const __half2*>(&add));
+    const __half2 r = __hmul2(d, s2);
+    out[j] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
+// Output tile `tile` in the persistent order: groups of 8 weight-row tiles
+// walk the token tiles together (operand tiles shared through L2).
+__device__ __forceinline__ void pf_tile_coords(int tile, int mt_count, int nt_count, int& mt, int& nt) {
+  constexpr int kGroup = 8;
+  const int per_group = kGroup * nt_count;
+  const int grp = tile / per_group;
+  const int first_m = grp * kGroup;
+  const int rows = min(kGroup, mt_count - first_m);
+  const int in = tile - grp * per_group;
+  mt = first_m + in % rows;
+  nt = in / rows;
+}
+
+__global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                      const __grid_constant__ CUtensorMap tmW,
+                                                                      const __half* __restrict__ scales,
+                                                                      const uint8_t* __restrict__ zeros, int T,
+                                                                      int N, int K, __half* __restrict__ y,
+                                                                      int32_t* __restrict__ err) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt_count = (N + kPfBM - 1) / kPfBM, nt_count = (T + kPfBN - 1) / kPfBN;
+  const int tiles = mt_count * nt_count;
+  const int my_tiles = blockIdx.x < tiles ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int num_kb = K / kPfBK;
+  const int G = K / 128, zpitch = (G + 1) / 2;
+
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t bar0 = sbase + kPfSmemBar;
+  auto stg_full = [&](int s) { return bar0 + 8u * s; };
+  auto stg_empty = [&](int s) { return bar0 + 8u * (kPfStg + s); };
+  auto a_full = [&](int o) { return bar0 + 8u * (2 * kPfStg + o); };
+  auto a_empty = [&](int o) { return bar0 + 8u * (2 * kPfStg + kPfOpsA + o); };
+  auto acc_full = [&](int b) { return bar0 + 8u * (2 * kPfStg + 2 * kPfOpsA + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kPfStg + 2 * kPfOpsA + 2 + b); };
+  const uint32_t mma_done = bar0 + 8u * (2 * kPfStg + 2 * kPfOpsA + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPfSmemMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kPfSmemMisc + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPfStg; ++s) {
+      tc::mbar_init(stg_full(s), 1);
+      tc::mbar_init(stg_empty(s), 1 + 4);  // the MMA commit and the stage's four dequantizer warps
+    }
+    for (int o = 0; o < kPfOpsA; ++o) {
+      tc::mbar_init(a_full(o), 4);
+      tc::mbar_init(a_empty(o), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(acc_full(b), 1);
+      tc::mbar_init(acc_empty(b), 4);  // the four epilogue warps
+    }
+    tc::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), kPfTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tc::prefetch_tmap(&tmX);
+      tc::prefetch_tmap(&tmW);
+      pdl_wait();  // the activations may come from the previous kernel in the stream
+      int it = 0, issued = 0;
+      for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
+        int mt, nt;
+        pf_tile_coords(blockIdx.x + ti * gridDim.x, mt_count, nt_count, mt, nt);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % kPfStg;
+          if (it >= kPfStg && !tc::mbar_wait(stg_empty(s), ((it / kPfStg) - 1) & 1, err, kPfSiteStgEmpty)) {
+            *abort_flag = 1;
+            break;
+          }
+          if (*abort_flag) break;
+          const uint32_t dst = sbase + s * kPfStgBytes;
+          tc::mbar_arrive_expect_tx(stg_full(s), kPfStgBytes);
+          tc::tma_load_2d(dst, &tmX, kb * kPfBK * 2, nt * kPfBN, stg_full(s));
+          tc::tma_load_2d(dst + kPfXBytes / 2, &tmX, kb * kPfBK * 2 + 128, nt * kPfBN, stg_full(s));
+          tc::tma_load_2d(dst + kPfXBytes, &tmW, kb * kPfBK / 2, mt * kPfBM, stg_full(s));
+          issued = it + 1;
+        }
+      }
+      if (*abort_flag) {
+        for (int j = (issued > kPfStg ? issued - kPfStg : 0); j < issued; ++j)
+          tc::mbar_wait(stg_full(j % kPfStg), (j / kPfStg) & 1, err, kPfSiteDrain);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_f16(kPfBM, kPfBN, 0);  // fp16 x fp16 -> fp32
+      bool issued_any = false;
+      int it = 0;
+      for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
+        const int buf = ti & 1;
+        // the epilogue has written out the tile that last used this accumulator
+        if (ti >= 2 && !tc::mbar_wait(acc_empty(buf), ((ti >> 1) - 1) & 1, err, kPfSiteAccEmpty)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc::tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % kPfStg, o = it % kPfOpsA;
+          if (!tc::mbar_wait(a_full(o), (it / kPfOpsA) & 1, err, kPfSiteAFull) ||
+              !tc::mbar_wait(stg_full(s), (it / kPfStg) & 1, err, kPfSiteStgFull)) {
+            *abort_flag = 1;
+            break;
+          }
+          if (*abort_flag) break;
+          tc::tc_fence_after();
+          const uint32_t xb = sbase + s * kPfStgBytes;
+          const uint32_t a_t = tmem + kPfTmemA + o * (kPfBK / 2);
+#pragma unroll
+          for (int k = 0; k < kPfBK / 16; ++k) {
+            const uint32_t b_k = xb + (k >> 2) * (kPfBN * 128) + 32 * (k & 3);  // K block, then 32 B in the atom
+            tc::mma_f16_ta(tmem + buf * kPfBN, a_t + 8 * k, tc::sw128_kmajor_desc(b_k), idesc,
+                           (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          issued_any = true;
+          tc::mma_commit(a_empty(o));
+          tc::mma_commit(stg_empty(s));
+        }
+        if (*abort_flag) break;
+        tc::mma_commit(acc_full(buf));
+      }
+      if (*abort_flag && issued_any) {
+        tc::mma_commit(mma_done);
+        tc::mbar_wait(mma_done, 0, err, kPfSiteDrain);
+      }
+    }
+  } else if (warp < kPfWarpE0) {
+    // ---------------- dequantizers (codes -> fp16 weights in TMEM) ----------------
+    const int set = (warp - kPfWarpA0) >> 2;  // takes the stages with it % kPfSets == set
+    const int q = warp & 3;                   // TMEM lane quadrant of this warp
+    const int r = q * 32 + lane;              // weight row of the tile
+    pdl_wait();                               // scales and zero-points, like every input
+    // Stage i of this CTA is K block i % num_kb of its tile i / num_kb.  The
+    // scale and zero-point of the set's next stage are loaded while the
+    // current stage is dequantized, so their latency stays off the chain.
+    const int total = my_tiles * num_kb;
+    auto load_sz = [&](int i, __half& sc, uint32_t& z) {
+      sc = __ushort_as_half(0);  // rows past N dequantize to 0
+      z = 0;
+      if (i >= total) return;
+      int mt, nt;
+      pf_tile_coords(blockIdx.x + (i / num_kb) * gridDim.x, mt_count, nt_count, mt, nt);
+      const int n = mt * kPfBM + r, kb = i % num_kb;
+      if (n < N) {
+        sc = scales[static_cast<int64_t>(n) * G + kb];
+        z = zeros != nullptr ? (zeros[static_cast<int64_t>(n) * zpitch + (kb >> 1)] >> (4 * (kb & 1))) & 0xFu : 8u;
+      }
+    };
+    __half sc_next;
+    uint32_t z_next;
+    load_sz(set, sc_next, z_next);
+    for (int it = set; it < total; it += kPfSets) {
+      const __half sc = sc_next;
+      const uint32_t z = z_next;
+      load_sz(it + kPfSets, sc_next, z_next);
+      const int s = it % kPfStg, o = it % kPfOpsA;
+      bool ok = tc::mbar_wait(stg_full(s), (it / kPfStg) & 1, err, kPfSiteStgFull);
+      if (ok && it >= kPfOpsA) ok = tc::mbar_wait(a_empty(o), ((it / kPfOpsA) - 1) & 1, err, kPfSiteAEmpty);
+      ok = __all_sync(0xffffffffu, ok && !*abort_flag);  // lanes agree and reconverge
+      if (!ok) {
+        *abort_flag = 1;
+        break;
+      }
+      tc::tc_fence_after();
+      {
+        const uint32_t mul = 0x2C003C00u;                          // (1, 1/16)
+        const uint32_t add = 0xD400E400u | (z << 20) | z;          // (-(1024 + z), -(64 + z))
+        const __half2 s2 = __half2half2(sc);
+        // the codes arrive in the 64-byte swizzle: 16-byte chunk c of row r sits
+        // at chunk c ^ ((r / 2) % 4), so the eight rows of a quarter warp hit
+        // distinct banks
+        const uint32_t src = sbase + s * kPfStgBytes + kPfXBytes + r * (kPfBK / 2);
+        const int swz = (r >> 1) & 3;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint4 u = tc::lds128(src + (((2 * h + c) ^ swz) << 4));
+            dequant_word(u.x, mul, add, s2, v + 16 * c);
+            dequant_word(u.y, mul, add, s2, v + 16 * c + 4);
+            dequant_word(u.z, mul, add, s2, v + 16 * c + 8);
+            dequant_word(u.w, mul, add, s2, v + 16 * c + 12);
+          }
+          tc::tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + kPfTmemA + o * (kPfBK / 2) + 32 * h,
+                                 v);
+        }
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(a_full(o));
+          tc::mbar_arrive(stg_empty(s));
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    for (int ti = 0; ti < my_tiles; ++ti) {
+      const int buf = ti & 1;
+      bool ok = tc::mbar_wait(acc_full(buf), (ti >> 1) & 1, err, kPfSiteAccFull);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        *abort_flag = 1;
+        break;
+      }
+      tc::tc_fence_after();
+      int mt, nt;
+      pf_tile_coords(blockIdx.x + ti * gridDim.x, mt_count, nt_count, mt, nt);
+      // Y[t][n]: the warp's 32 lanes hold 32 consecutive n of each token t, so
+      // every store instruction writes 64 contiguous bytes
+      const int n = mt * kPfBM + q * 32 + lane;
+      unsigned short* yr = reinterpret_cast<unsigned short*>(y) + n;
+#pragma unroll 1
+      for (int cg = 0; cg < kPfBN / 32; ++cg) {
+        __syncwarp();  // reconverge after the bound checks before the aligned TMEM load
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(lane_base + buf * kPfBN + cg * 32, v);
+        tc::tmem_wait_ld();
+        const int t0 = nt * kPfBN + cg * 32;
+        if (n < N) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int t = t0 + i;
+            if (t < T) yr[static_cast<int64_t>(t) * N] = __half_as_ushort(__float2half_rn(__uint_as_float(v[i])));
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(acc_empty(buf));
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kPfTmemCols);
+  }
+}
+
+}  // namespace
+
+bool w4a16_prefill_supported(int64_t T, int64_t N, int64_t K) {
+  return T >= 1 && N >= 1 && K >= kPfBK && K % kPfBK == 0 && T <= (1 << 30) && N <= (1 << 30);
+}
+
+cudaError_t launch_w4a16_prefill(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq,
+                                 const void* scales, const uint8_t* zeros, void* y, cudaStream_t stream) {
+  if (T == 0 || N == 0) return cudaSuccess;
+  CUtensorMap tmX, tmW;
+  cudaError_t st = make_tmap_2d_u8(&tmX, x, static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(T), 128, kPfBN,
+                                   /*swizzle_bytes=*/128);
+  if (st != cudaSuccess) return st;
+  st = make_tmap_2d_u8(&tmW, wq, static_cast<uint64_t>(K) / 2, static_cast<uint64_t>(N), kPfBK / 2, kPfBM,
+                       /*swizzle_bytes=*/64);
+  if (st != cudaSuccess) return st;
+  st = cudaFuncSetAttribute(w4a16_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemTotal);
+  if (st != cudaSuccess) return st;
+  const int64_t tiles = ((N + kPfBM - 1) / kPfBM) * ((T + kPfBN - 1) / kPfBN);
+  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPfThreads);
+  cfg.dynamicSmemBytes = kPfSmemTotal;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w4a16_prefill_kernel, tmX, tmW, static_cast<const __half*>(scales), zeros,
+                            static_cast<int>(T), static_cast<int>(N), static_cast<int>(K), static_cast<__half*>(y),
+                            device_error_word());
+}
+
+}  // namespace qlin

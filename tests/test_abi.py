@@ -47,9 +47,9 @@ def test_status_strings(built):
 def test_rejects_bad_arguments_without_gpu(built):
     L = built
     P = ctypes.c_void_p
-    # W4A16: group 64 is not built; T above 64; K not a multiple of the group
+    # W4A16: group 64 is not built; T out of range; K not a multiple of the group
     assert L.qlin_w4a16_gemm(P(16), 1, 16, 256, P(16), P(16), None, 64, P(16), None) == 3
-    assert L.qlin_w4a16_gemm(P(16), 65, 16, 256, P(16), P(16), None, 128, P(16), None) == 1
+    assert L.qlin_w4a16_gemm(P(16), 1 << 31, 16, 256, P(16), P(16), None, 128, P(16), None) == 1
     assert L.qlin_w4a16_gemm(P(16), 1, 16, 200, P(16), P(16), None, 128, P(16), None) == 1
     assert L.qlin_w4a16_gemm(P(8), 1, 16, 256, P(16), P(16), None, 128, P(16), None) == 2
     # int8 quant: K not a multiple of 16, bad dtype, misaligned x
