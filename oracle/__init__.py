@@ -74,6 +74,8 @@ from .mx import (  # noqa: F401
 from .gemm import (  # noqa: F401
     w4a16_reference,
     w4a16_reference_packed,
+    w4a16_act_order_reference,
+    act_order_perm,
     int8_gemm_exact,
     azp_adj_from_weight,
     w8a8_epilogue,

@@ -57,6 +57,33 @@ def w4a16_reference_packed(x, wq, scales, zeros_packed, group=128):
     return w4a16_reference(x, codes, scales, zeros, group)
 
 
+def w4a16_act_order_reference(x, codes, scales, zeros, g_idx, group=128):
+    """W4A16 with act-order ("LLM and AIGC quantization", GPTQ engineering
+    details: desc_act quantizes the columns in descending diag(H) order, so
+    g_idx records each input channel's group and the scale reads are no longer
+    contiguous): column k is dequantized with the scale and zero-point of
+    group g_idx[k].  float64 Y [T][N]; codes uint8 [N][K], scales fp16 [N][G],
+    zeros uint8 [N][G] or None (8), g_idx int [K] in [0, G)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    g_idx = np.asarray(g_idx, dtype=np.int64)
+    n, k = codes.shape
+    s = np.asarray(scales).astype(np.float64)[:, g_idx]                    # [N][K]
+    z = np.full((n, k), 8.0) if zeros is None else np.asarray(zeros).astype(np.float64)[:, g_idx]
+    w = (codes.astype(np.float64) - z) * s
+    return np.asarray(x).astype(np.float64) @ w.T
+
+
+def act_order_perm(g_idx, group=128):
+    """The column order that makes every group contiguous: a stable sort of the
+    columns by g_idx (column perm[j] goes to position j).  Each group must hold
+    exactly `group` columns, as GPTQ's act-order assigns them."""
+    g_idx = np.asarray(g_idx, dtype=np.int64)
+    counts = np.bincount(g_idx, minlength=len(g_idx) // group)
+    if len(g_idx) % group or np.any(counts != group):
+        raise ValueError("every group must hold exactly `group` columns")
+    return np.argsort(g_idx, kind="stable").astype(np.int32)
+
+
 def int8_gemm_exact(a, b):
     """Exact D^ = A^ B^^T for int8 A^ [T][K], B^ [N][K] -> int64 [T][N].
 

@@ -704,6 +704,51 @@ def test_rmsnorm_arc_unit_rms():
     pin_rmsnorm_arc_unit_rms()
 
 
+# ---- W4A16 act-order (g_idx) ----
+
+def _act_order_case(seed, n=6, k=512, t=3):
+    rng = np.random.default_rng(seed)
+    g = k // 128
+    g_idx = rng.permutation(np.repeat(np.arange(g), 128))          # every group 128 columns, scattered
+    codes = rng.integers(0, 16, size=(n, k)).astype(np.uint8)
+    scales = rng.uniform(0.001, 0.02, size=(n, g)).astype(np.float16)
+    zeros = rng.integers(0, 16, size=(n, g)).astype(np.uint8)
+    x = rng.standard_normal((t, k)).astype(np.float16)
+    return x, codes, scales, zeros, g_idx
+
+
+def pin_act_order():
+    x, codes, scales, zeros, g_idx = _act_order_case(31)
+    y = oracle.w4a16_act_order_reference(x, codes, scales, zeros, g_idx)
+    # contiguous groups: the plain g128 definition (pinned by brute force above)
+    plain = np.arange(512) // 128
+    assert np.allclose(oracle.w4a16_act_order_reference(x, codes, scales, zeros, plain),
+                       oracle.w4a16_reference(x, codes, scales, zeros), rtol=0, atol=1e-12)
+    # brute force, one column at a time
+    t, n = 1, 4
+    want = sum(float(x[t, k]) * (int(codes[n, k]) - int(zeros[n, g_idx[k]])) * float(scales[n, g_idx[k]])
+               for k in range(512))
+    assert abs(y[t, n] - want) <= 1e-12 * (1 + abs(want))
+    # sorting the columns by group (the same permutation on x, the codes and
+    # g_idx) leaves Y unchanged and makes the groups contiguous
+    perm = oracle.act_order_perm(g_idx)
+    assert np.array_equal(g_idx[perm], plain)
+    assert np.all(np.diff(perm[g_idx[perm] == 2]) > 0)                 # stable inside a group
+    y2 = oracle.w4a16_reference(x[:, perm], codes[:, perm], scales, zeros)
+    assert np.allclose(y, y2, rtol=1e-12, atol=1e-12)
+
+
+def test_act_order():
+    pin_act_order()
+
+
+def test_act_order_perm_rejects_uneven_groups():
+    g_idx = np.repeat(np.arange(4), 128)
+    g_idx[0] = 1
+    with pytest.raises(ValueError):
+        oracle.act_order_perm(g_idx)
+
+
 # ---- MX block-scaled formats (MXFP8, MXFP4) ----
 
 def _pad32(v):
@@ -911,6 +956,12 @@ def _mut_rmsnorm_arc_gamma_reordered(monkeypatch):
     return pin_rmsnorm_arc_unit_rms
 
 
+def _mut_act_order_ignores_g_idx(monkeypatch):
+    monkeypatch.setattr(oracle, "w4a16_act_order_reference",
+                        lambda x, c, s, z, g_idx, group=128: ogemm.w4a16_reference(x, c, s, z, group))
+    return pin_act_order
+
+
 def _mut_mx_emax_e4m3_7(monkeypatch):
     monkeypatch.setitem(oquant_mx.MX_EMAX, "e4m3", 7)
     return pin_mx_page_examples
@@ -926,7 +977,8 @@ def _mut_mx_scales_swapped(monkeypatch):
 MUTATIONS = [_mut_e2m1_ties_odd, _mut_azp_sign, _mut_azp_adj_axis, _mut_residual_sign,
              _mut_w8a8_transposed, _mut_w4_zero_dropped, _mut_nvfp4_scale_not_decoded, _mut_sym_qmax,
              _mut_fp8_scale_447, _mut_fp8_scales_swapped, _mut_rmsnorm_mean_k_minus_1,
-             _mut_rmsnorm_arc_gamma_reordered, _mut_mx_emax_e4m3_7, _mut_mx_scales_swapped]
+             _mut_rmsnorm_arc_gamma_reordered, _mut_mx_emax_e4m3_7, _mut_mx_scales_swapped,
+             _mut_act_order_ignores_g_idx]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
