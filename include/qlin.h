@@ -188,6 +188,37 @@ qlin_status qlin_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int cou
                                     cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * next 3 - W4A16 with act-order (g_idx)
+ *
+ * With act-order ("LLM and AIGC quantization", GPTQ engineering details:
+ * desc_act quantizes the columns in descending diag(H) order, and g_idx
+ * records each input channel's group), column k of the weights uses the
+ * scale and zero-point of group g_idx[k]:
+ *   Y[t,n] = sum_k X[t,k] . (q[n,k] - z[n, g_idx[k]]) . s[n, g_idx[k]]
+ *
+ * qlin_w4a16_act_order_prepare (offline, once per weight):
+ *   perm[j]       = the j-th column in group order (a stable sort by g_idx:
+ *                   group 0's columns in ascending order, then group 1's ...)
+ *   wq_sorted     = the codes with their columns in that order
+ *   g_idx   int32 [K], each group in [0, K/group) holding exactly `group`
+ *           columns (otherwise the device error word records a nonzero
+ *           code: see qlin_get_device_error)
+ *   wq      uint8 [N][K/2] packed codes in the original column order
+ *   perm    out, int32 [K] (16-byte aligned); wq_sorted out, uint8 [N][K/2]
+ *   scales / zeros stay as they are ([N][K/group], now per contiguous group).
+ * qlin_w4a16_gemm_act_order (run time): x_work[t][j] = x[t][perm[j]] (one
+ *   gather kernel), then qlin_w4a16_gemm(x_work, wq_sorted, scales, zeros);
+ *   the sums are the same terms in another order.
+ *   x, x_work  fp16 [T][K] (16-byte aligned; x_work is a caller workspace)
+ *   other arguments as in qlin_w4a16_gemm; group 128.
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_w4a16_act_order_prepare(const int32_t* g_idx, int64_t K, int64_t group, const uint8_t* wq,
+                                         int64_t N, int32_t* perm, uint8_t* wq_sorted, cudaStream_t stream);
+qlin_status qlin_w4a16_gemm_act_order(const void* x, int64_t T, int64_t N, int64_t K, const int32_t* perm,
+                                      const uint8_t* wq_sorted, const void* scales, const uint8_t* zeros,
+                                      int64_t group, void* x_work, void* y, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * a1, sequence - a chain of W4A16 decode steps in one persistent launch
  *
  * Runs steps[0], steps[1], ... in order at T = 1, each step a grouped W4A16

@@ -26,7 +26,7 @@ __all__ = [
     "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
     "QLIN_QFMT_INT8", "QLIN_QFMT_FP8_E4M3", "qlin_quant_fp8", "qlin_fp8_gemm", "qlin_rmsnorm_quant",
     "qlin_rmsnorm_quant_nvfp4", "QLIN_MX_FP8_E4M3", "QLIN_MX_FP4_E2M1", "qlin_mx_sf_bytes", "qlin_quant_mx",
-    "qlin_mx_gemm",
+    "qlin_mx_gemm", "qlin_w4a16_act_order_prepare", "qlin_w4a16_gemm_act_order",
 ]
 
 QLIN_F16, QLIN_BF16, QLIN_F32, QLIN_I32 = 0, 1, 2, 3
@@ -67,6 +67,8 @@ _SIGS = {
     "qlin_quant_nvfp4": ([_P, _I32, _I64, _I64, _P, _I64, _I32, _P, _P, _P, _I32, _P], _I32),
     "qlin_nvfp4_sf_bytes": ([_I64, _I64, _I32], _I64),
     "qlin_mx_sf_bytes": ([_I64, _I64, _I32], _I64),
+    "qlin_w4a16_act_order_prepare": ([_P, _I64, _I64, _P, _I64, _P, _P, _P], _I32),
+    "qlin_w4a16_gemm_act_order": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _I64, _P, _P, _P], _I32),
     "qlin_quant_mx": ([_P, _I32, _I64, _I64, _I32, _P, _P, _I32, _P], _I32),
     "qlin_mx_gemm": ([_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _I32, _P], _I32),
     "qlin_nvfp4_sf_to_mma": ([_P, _I64, _I64, _P, _P], _I32),
@@ -438,3 +440,38 @@ def qlin_mx_gemm(a, sfa, b, sfb, out, fmt=QLIN_MX_FP8_E4M3, stream=None):
         raise ValueError("out must be [T][N]")
     _check("qlin_mx_gemm", lib().qlin_mx_gemm(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), t, n, k, fmt, _ptr(out),
                                              _dtype_code(out), _stream(stream)))
+
+
+def qlin_w4a16_act_order_prepare(g_idx, wq, perm, wq_sorted, group=128, stream=None):
+    """Offline act-order preparation: perm int32 [K] (the columns in group order)
+    and wq_sorted uint8 [N][K/2] (the packed codes in that order) from g_idx
+    int32 [K] and wq uint8 [N][K/2]."""
+    torch = _torch()
+    _need(g_idx, torch.int32, name="g_idx"); _need(wq, torch.uint8, name="wq")
+    _need(perm, torch.int32, name="perm"); _need(wq_sorted, torch.uint8, name="wq_sorted")
+    k = g_idx.numel()
+    n = wq.shape[0]
+    if perm.numel() != k or tuple(wq_sorted.shape) != tuple(wq.shape) or wq.shape[1] * 2 != k:
+        raise ValueError("shape mismatch between g_idx, wq, perm and wq_sorted")
+    _check("qlin_w4a16_act_order_prepare",
+           lib().qlin_w4a16_act_order_prepare(_ptr(g_idx), k, group, _ptr(wq), n, _ptr(perm), _ptr(wq_sorted),
+                                              _stream(stream)))
+
+
+def qlin_w4a16_gemm_act_order(x, perm, wq_sorted, scales, zeros, y, x_work=None, group=128, stream=None):
+    """y [T][N] = x . dequant(W)^T for act-order weights prepared by
+    qlin_w4a16_act_order_prepare; x_work fp16 [T][K] workspace (allocated here if None)."""
+    torch = _torch()
+    _need(x, torch.float16, name="x"); _need(perm, torch.int32, name="perm")
+    _need(wq_sorted, torch.uint8, name="wq_sorted"); _need(scales, torch.float16, name="scales")
+    _need(zeros, torch.uint8, name="zeros"); _need(y, torch.float16, name="y")
+    if x_work is None:
+        x_work = torch.empty_like(x)
+    _need(x_work, torch.float16, name="x_work")
+    t, k = x.shape
+    n = wq_sorted.shape[0]
+    if x_work.shape != x.shape or perm.numel() != k or wq_sorted.shape[1] * 2 != k or tuple(y.shape) != (t, n):
+        raise ValueError("shape mismatch")
+    _check("qlin_w4a16_gemm_act_order",
+           lib().qlin_w4a16_gemm_act_order(_ptr(x), t, n, k, _ptr(perm), _ptr(wq_sorted), _ptr(scales), _ptr(zeros),
+                                           group, _ptr(x_work), _ptr(y), _stream(stream)))

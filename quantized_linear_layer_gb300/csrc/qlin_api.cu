@@ -219,6 +219,42 @@ qlin_status qlin_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int cou
   QLIN_LAUNCH(launch_w4a16_gemm_grouped(x, T, K, count, N, wq, scales, zeros, y, stream), "w4a16_gemm_grouped launch");
 }
 
+qlin_status qlin_w4a16_act_order_prepare(const int32_t* g_idx, int64_t K, int64_t group, const uint8_t* wq,
+                                         int64_t N, int32_t* perm, uint8_t* wq_sorted, cudaStream_t stream) {
+  QLIN_REQUIRE(group == 128, QLIN_ERR_UNSUPPORTED, "group size %lld (only 128 is built)", (long long)group);
+  QLIN_REQUIRE(K > 0 && K <= kMaxDim && K % group == 0, QLIN_ERR_INVALID_ARG, "K=%lld is not a positive multiple of %lld",
+               (long long)K, (long long)group);
+  QLIN_REQUIRE(N >= 0 && N <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad N=%lld", (long long)N);
+  QLIN_REQUIRE(g_idx && perm && (N == 0 || (wq && wq_sorted)), QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(wq != wq_sorted || N == 0, QLIN_ERR_INVALID_ARG, "wq_sorted must not alias wq");
+  QLIN_REQUIRE(aligned16(perm), QLIN_ERR_ALIGNMENT, "perm must be 16-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(g_idx) & 3u) == 0, QLIN_ERR_ALIGNMENT, "g_idx must be 4-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_w4a16_act_order_prepare(g_idx, K, group, wq, N, perm, wq_sorted, stream),
+              "w4a16_act_order_prepare launch");
+}
+
+qlin_status qlin_w4a16_gemm_act_order(const void* x, int64_t T, int64_t N, int64_t K, const int32_t* perm,
+                                      const uint8_t* wq_sorted, const void* scales, const uint8_t* zeros,
+                                      int64_t group, void* x_work, void* y, cudaStream_t stream) {
+  QLIN_REQUIRE(group == 128, QLIN_ERR_UNSUPPORTED, "group size %lld (only 128 is built)", (long long)group);
+  QLIN_REQUIRE(T >= 0 && T <= kMaxDim, QLIN_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
+  QLIN_REQUIRE(N >= 0 && N <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad sizes N=%lld K=%lld",
+               (long long)N, (long long)K);
+  QLIN_REQUIRE(K % group == 0, QLIN_ERR_INVALID_ARG, "K=%lld is not a multiple of the group size", (long long)K);
+  if (T == 0 || N == 0) return ok();
+  QLIN_REQUIRE(x && perm && wq_sorted && scales && x_work && y, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(x_work != x, QLIN_ERR_INVALID_ARG, "x_work must not alias x");
+  QLIN_REQUIRE(aligned16(x) && aligned16(wq_sorted) && aligned16(perm) && aligned16(x_work), QLIN_ERR_ALIGNMENT,
+               "x, perm, wq_sorted and x_work must be 16-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(scales) & 1u) == 0 && (reinterpret_cast<uintptr_t>(y) & 1u) == 0,
+               QLIN_ERR_ALIGNMENT, "scales and y must be 2-byte aligned");
+  QLIN_DEVICE();
+  cudaError_t e = launch_x_permute(x, T, K, perm, x_work, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "x_permute launch");
+  QLIN_LAUNCH(launch_w4a16_gemm(x_work, T, N, K, wq_sorted, scales, zeros, y, stream), "w4a16_gemm launch");
+}
+
 int64_t qlin_w4a16_sequence_workspace_bytes(int64_t nsteps) {
   return nsteps < 0 ? -1 : w4a16_sequence_workspace_bytes(nsteps);
 }

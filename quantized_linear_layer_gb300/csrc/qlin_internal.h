@@ -50,6 +50,11 @@ bool w4a16_skinny_supported(int64_t T, int64_t N, int64_t K);
 cudaError_t launch_w4a16_skinny_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
                                         const uint8_t* const* wq, const void* const* scales,
                                         const uint8_t* const* zeros, void* const* y, cudaStream_t stream);
+// W4A16 act-order: group-sorted column order and codes (offline), activation gather.
+cudaError_t launch_w4a16_act_order_prepare(const int32_t* g_idx, int64_t K, int64_t group, const uint8_t* wq,
+                                           int64_t N, int32_t* perm, uint8_t* wq_sorted, cudaStream_t stream);
+cudaError_t launch_x_permute(const void* x, int64_t T, int64_t K, const int32_t* perm, void* out,
+                             cudaStream_t stream);
 // W4A16 for many tokens (prefill) on the tcgen05 tensor cores.
 bool w4a16_prefill_supported(int64_t T, int64_t N, int64_t K);
 cudaError_t launch_w4a16_prefill(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq,

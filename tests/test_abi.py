@@ -127,6 +127,16 @@ def test_rejects_bad_arguments_without_gpu(built):
                                       None) == 3
     assert L.qlin_rmsnorm_quant_nvfp4(P(16), 0, 4, 64, P(16), F(1e-6), None, 8, 0, P(16), P(16), P(16), 0, None) == 1
     assert L.qlin_rmsnorm_quant_nvfp4(None, 0, 0, 64, None, F(1e-6), None, 0, 0, None, None, None, 0, None) == 0
+    # act-order: group 64 not built, K not a multiple of 128, misaligned perm, wq_sorted
+    # aliasing wq; GEMM: x_work missing or aliasing x, misaligned x_work; empty problems
+    assert L.qlin_w4a16_act_order_prepare(P(16), 256, 64, P(16), 4, P(16), P(32), None) == 3
+    assert L.qlin_w4a16_act_order_prepare(P(16), 200, 128, P(16), 4, P(16), P(32), None) == 1
+    assert L.qlin_w4a16_act_order_prepare(P(16), 256, 128, P(16), 4, P(24), P(32), None) == 2
+    assert L.qlin_w4a16_act_order_prepare(P(16), 256, 128, P(16), 4, P(16), P(16), None) == 1
+    assert L.qlin_w4a16_gemm_act_order(P(16), 2, 8, 256, P(16), P(16), P(16), None, 128, None, P(16), None) == 1
+    assert L.qlin_w4a16_gemm_act_order(P(16), 2, 8, 256, P(16), P(16), P(16), None, 128, P(16), P(16), None) == 1
+    assert L.qlin_w4a16_gemm_act_order(P(16), 2, 8, 256, P(16), P(16), P(16), None, 128, P(40), P(16), None) == 2
+    assert L.qlin_w4a16_gemm_act_order(None, 0, 8, 256, None, None, None, None, 128, None, None, None) == 0
     # MX: unknown format, K not a multiple of 32, misaligned x; GEMM: MXFP4 K not a
     # multiple of 64, F32 out, out row pitch (N = 12); empty problems; scale sizes
     assert L.qlin_quant_mx(P(16), 0, 4, 64, 2, P(16), P(16), 0, None) == 1
