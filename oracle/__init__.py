@@ -71,6 +71,14 @@ from .mx import (  # noqa: F401
     mx_gemm_reference,
     e8m0_decode,
 )
+from .hadamard import (  # noqa: F401
+    fwht_rows,
+    regular_rows,
+    hadamard_rotate,
+    hadamard_scale,
+    sylvester_matrix,
+    regular_matrix,
+)
 from .gemm import (  # noqa: F401
     w4a16_reference,
     w4a16_reference_packed,

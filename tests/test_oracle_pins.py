@@ -18,6 +18,7 @@ from oracle import formats as ofmt
 from oracle import gemm as ogemm
 from oracle import quant as oquant
 from oracle import mx as oquant_mx
+from oracle import hadamard as oquant_had
 from conftest import load_golden
 
 F32 = np.float32
@@ -749,6 +750,57 @@ def test_act_order_perm_rejects_uneven_groups():
         oracle.act_order_perm(g_idx)
 
 
+# ---- online Hadamard rotation ----
+
+def _sylvester_by_recursion(n):
+    """H_n written out from its element formula: (-1)^popcount(i & j)."""
+    i = np.arange(n)
+    return np.array([[(-1.0) ** bin(a & b).count("1") for b in i] for a in i])
+
+
+def pin_hadamard_dense():
+    rng = np.random.default_rng(41)
+    for kind, sizes in (("sylvester", (2, 8, 64, 256, 1024)), ("regular", (4, 16, 64, 256))):
+        for n in sizes:
+            x = rng.standard_normal((3, 2 * n)).astype(np.float32)
+            y = oracle.hadamard_rotate(x, n, kind)
+            if kind == "sylvester":
+                h = _sylvester_by_recursion(n) if n <= 64 else oracle.sylvester_matrix(n)
+            else:
+                h = oracle.regular_matrix(n)
+            ref = (x.astype(np.float64).reshape(-1, n) @ h / np.sqrt(n)).reshape(x.shape)
+            bound = (np.log2(n) + 2) * 2.0 ** -24 * np.sqrt(n) * np.abs(x).max()
+            assert np.max(np.abs(y - ref)) <= bound, (kind, n)
+
+
+def test_hadamard_dense():
+    pin_hadamard_dense()
+
+
+def test_hadamard_matrices():
+    """The Sylvester matrix equals the element formula; both matrices are
+    orthogonal up to n; the regular one has all column sums +-sqrt(n), so a row
+    of ones rotates to exactly +-1 (every intermediate is an integer)."""
+    assert np.array_equal(oracle.sylvester_matrix(32), _sylvester_by_recursion(32))
+    for n in (4, 16, 64, 256):
+        h = oracle.regular_matrix(n)
+        assert np.array_equal(h @ h.T, n * np.eye(n)) and np.array_equal(h, h.T)
+        assert np.array_equal(np.abs(h.sum(axis=0)), np.full(n, np.sqrt(n)))
+        y = oracle.hadamard_rotate(np.ones((1, n), dtype=np.float32), n, "regular")
+        assert np.array_equal(np.abs(y), np.ones((1, n), dtype=np.float32))
+
+
+def test_hadamard_involution_and_signs():
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal((4, 512)).astype(np.float32)
+    for kind, n in (("sylvester", 512), ("sylvester", 128), ("regular", 256)):
+        y = oracle.hadamard_rotate(oracle.hadamard_rotate(x, n, kind), n, kind)
+        assert np.max(np.abs(y - x)) <= 2 * (np.log2(n) + 2) * 2.0 ** -24 * np.sqrt(n) * np.abs(x).max()
+    signs = np.where(rng.random(512) < 0.5, -1.0, 1.0).astype(np.float32)
+    assert np.array_equal(oracle.hadamard_rotate(x, 256, "regular", signs),
+                          oracle.hadamard_rotate(x, 256, "regular") * signs)
+
+
 # ---- MX block-scaled formats (MXFP8, MXFP4) ----
 
 def _pad32(v):
@@ -962,6 +1014,16 @@ def _mut_act_order_ignores_g_idx(monkeypatch):
     return pin_act_order
 
 
+def _mut_hadamard_stage_sign(monkeypatch):
+    orig = oquant_had.fwht_rows
+
+    def bad(x, n):
+        y = orig(x, n)
+        return np.concatenate([y[:, 1:2], y[:, :1], y[:, 2:]], axis=1)   # two outputs swapped
+    monkeypatch.setattr(oquant_had, "fwht_rows", bad)
+    return pin_hadamard_dense
+
+
 def _mut_mx_emax_e4m3_7(monkeypatch):
     monkeypatch.setitem(oquant_mx.MX_EMAX, "e4m3", 7)
     return pin_mx_page_examples
@@ -978,7 +1040,7 @@ MUTATIONS = [_mut_e2m1_ties_odd, _mut_azp_sign, _mut_azp_adj_axis, _mut_residual
              _mut_w8a8_transposed, _mut_w4_zero_dropped, _mut_nvfp4_scale_not_decoded, _mut_sym_qmax,
              _mut_fp8_scale_447, _mut_fp8_scales_swapped, _mut_rmsnorm_mean_k_minus_1,
              _mut_rmsnorm_arc_gamma_reordered, _mut_mx_emax_e4m3_7, _mut_mx_scales_swapped,
-             _mut_act_order_ignores_g_idx]
+             _mut_act_order_ignores_g_idx, _mut_hadamard_stage_sign]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
