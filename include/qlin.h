@@ -90,6 +90,12 @@ typedef enum {
   QLIN_QFMT_FP8_E4M3 = 1  /* E4M3-FN codes, s = max|y| / 448 */
 } qlin_qfmt;
 
+/* Online Hadamard rotations (qlin_hadamard). */
+typedef enum {
+  QLIN_HADAMARD_SYLVESTER = 0,  /* fast Walsh-Hadamard butterflies, n a power of two */
+  QLIN_HADAMARD_REGULAR = 1     /* Kronecker power of the 4 x 4 regular Hadamard H4, n a power of four */
+} qlin_hadamard_kind;
+
 /* MX element formats (one E8M0 scale per 32 elements along K). */
 typedef enum {
   QLIN_MX_FP8_E4M3 = 0,  /* MXFP8: E4M3-FN elements, one byte each */
@@ -525,6 +531,33 @@ qlin_status qlin_quant_mx(const void* x, qlin_dtype x_dtype, int64_t rows, int64
                           uint8_t* sf, qlin_sf_layout sf_layout, cudaStream_t stream);
 qlin_status qlin_mx_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb, int64_t T,
                          int64_t N, int64_t K, qlin_mx_fmt fmt, void* out, qlin_dtype out_dtype, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * next 4 - online Hadamard rotation of the activations before 4-bit
+ * quantization
+ *
+ * Every group of n consecutive elements of each row is rotated:
+ *   QLIN_HADAMARD_SYLVESTER ("LLM and AIGC quantization", QuaRot: the fast
+ *     Walsh-Hadamard transform, log2(n) butterfly stages mapping the pair
+ *     (a, b) at distance h to (a + b, a - b)), stages h = 1, 2, ..., n/2;
+ *     n a power of two, 2 <= n <= 8192;
+ *   QLIN_HADAMARD_REGULAR (ConvRot: each group of N0 times the regular
+ *     Hadamard, the Kronecker power of H4 = [[1,1,1,-1],[1,1,-1,1],
+ *     [1,-1,1,1],[-1,1,1,1]]), radix-4 stages at strides 1, 4, 16, ...,
+ *     each quad becoming y_i = s - 2 x_(3-i), s = (x0 + x1) + (x2 + x3);
+ *     n in {4, 16, 64, 256};
+ * then times c = float32(1/sqrt(n)), times signs[k] (QuaRot's diag(+-1))
+ * when signs is not NULL, rounded once to the input dtype.  Every step is one
+ * float32 operation in the order given, so the result is reproducible bit
+ * for bit.  The weights take the same rotation offline (W . Q), which leaves
+ * X . W^T unchanged.
+ *   x      [rows][K] of dtype (F16, BF16 or F32), 16-byte aligned
+ *   signs  int8 [K] of +1 / -1 (8-byte aligned), or NULL
+ *   y      out, [rows][K] of dtype, 16-byte aligned (y == x allowed)
+ * K a multiple of n and of 8.
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_hadamard(const void* x, qlin_dtype dtype, int64_t rows, int64_t K, qlin_hadamard_kind kind,
+                          int64_t n, const int8_t* signs, void* y, cudaStream_t stream);
 
 qlin_status qlin_rmsnorm_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const void* gamma,
                                      float eps, const int32_t* perm, int64_t S, qlin_nvfp4_mode mode, const float* g,

@@ -26,7 +26,8 @@ __all__ = [
     "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
     "QLIN_QFMT_INT8", "QLIN_QFMT_FP8_E4M3", "qlin_quant_fp8", "qlin_fp8_gemm", "qlin_rmsnorm_quant",
     "qlin_rmsnorm_quant_nvfp4", "QLIN_MX_FP8_E4M3", "QLIN_MX_FP4_E2M1", "qlin_mx_sf_bytes", "qlin_quant_mx",
-    "qlin_mx_gemm", "qlin_w4a16_act_order_prepare", "qlin_w4a16_gemm_act_order",
+    "qlin_mx_gemm", "QLIN_HADAMARD_SYLVESTER", "QLIN_HADAMARD_REGULAR", "qlin_hadamard",
+    "qlin_w4a16_act_order_prepare", "qlin_w4a16_gemm_act_order",
 ]
 
 QLIN_F16, QLIN_BF16, QLIN_F32, QLIN_I32 = 0, 1, 2, 3
@@ -34,6 +35,7 @@ QLIN_NVFP4_RESIDUAL, QLIN_NVFP4_DUPLICATE = 0, 1
 QLIN_SF_ROWS, QLIN_SF_MMA = 0, 1
 QLIN_QFMT_INT8, QLIN_QFMT_FP8_E4M3 = 0, 1
 QLIN_MX_FP8_E4M3, QLIN_MX_FP4_E2M1 = 0, 1
+QLIN_HADAMARD_SYLVESTER, QLIN_HADAMARD_REGULAR = 0, 1
 
 _STATUS = {0: "QLIN_OK", 1: "QLIN_ERR_INVALID_ARG", 2: "QLIN_ERR_ALIGNMENT", 3: "QLIN_ERR_UNSUPPORTED",
            4: "QLIN_ERR_CUDA", 5: "QLIN_ERR_TIMEOUT"}
@@ -67,6 +69,7 @@ _SIGS = {
     "qlin_quant_nvfp4": ([_P, _I32, _I64, _I64, _P, _I64, _I32, _P, _P, _P, _I32, _P], _I32),
     "qlin_nvfp4_sf_bytes": ([_I64, _I64, _I32], _I64),
     "qlin_mx_sf_bytes": ([_I64, _I64, _I32], _I64),
+    "qlin_hadamard": ([_P, _I32, _I64, _I64, _I32, _I64, _P, _P, _P], _I32),
     "qlin_w4a16_act_order_prepare": ([_P, _I64, _I64, _P, _I64, _P, _P, _P], _I32),
     "qlin_w4a16_gemm_act_order": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _I64, _P, _P, _P], _I32),
     "qlin_quant_mx": ([_P, _I32, _I64, _I64, _I32, _P, _P, _I32, _P], _I32),
@@ -475,3 +478,21 @@ def qlin_w4a16_gemm_act_order(x, perm, wq_sorted, scales, zeros, y, x_work=None,
     _check("qlin_w4a16_gemm_act_order",
            lib().qlin_w4a16_gemm_act_order(_ptr(x), t, n, k, _ptr(perm), _ptr(wq_sorted), _ptr(scales), _ptr(zeros),
                                            group, _ptr(x_work), _ptr(y), _stream(stream)))
+
+
+def qlin_hadamard(x, n, y=None, kind=QLIN_HADAMARD_SYLVESTER, signs=None, stream=None):
+    """Rotates every group of n consecutive elements of the rows of x [rows][K]
+    (Sylvester fast Walsh-Hadamard or the regular Hadamard of order 4^k), scaled by
+    1/sqrt(n) and multiplied by signs (int8 [K] of +-1) if given; y defaults to a new
+    tensor (y = x rotates in place)."""
+    torch = _torch()
+    _need(x, torch.float16, torch.bfloat16, torch.float32, name="x"); _need(signs, torch.int8, name="signs")
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, x.dtype, name="y")
+    rows, k = x.shape
+    if y.shape != x.shape or (signs is not None and signs.numel() != k):
+        raise ValueError("shape mismatch")
+    _check("qlin_hadamard", lib().qlin_hadamard(_ptr(x), _dtype_code(x), rows, k, kind, n, _ptr(signs), _ptr(y),
+                                               _stream(stream)))
+    return y

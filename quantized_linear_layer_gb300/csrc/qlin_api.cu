@@ -477,6 +477,28 @@ qlin_status qlin_nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t*
   QLIN_LAUNCH(launch_nvfp4_gemm(a, sfa, b, sfb, T, N, K, g_a, g_b, out, out_dtype, stream), "nvfp4_gemm launch");
 }
 
+qlin_status qlin_hadamard(const void* x, qlin_dtype dtype, int64_t rows, int64_t K, qlin_hadamard_kind kind,
+                          int64_t n, const int8_t* signs, void* y, cudaStream_t stream) {
+  QLIN_REQUIRE(is_float_dtype(dtype), QLIN_ERR_INVALID_ARG, "dtype must be F16, BF16 or F32");
+  QLIN_REQUIRE(kind == QLIN_HADAMARD_SYLVESTER || kind == QLIN_HADAMARD_REGULAR, QLIN_ERR_INVALID_ARG,
+               "unknown Hadamard kind %d", static_cast<int>(kind));
+  const bool pow2 = n >= 2 && (n & (n - 1)) == 0;
+  QLIN_REQUIRE(kind != QLIN_HADAMARD_SYLVESTER || (pow2 && n <= 8192), QLIN_ERR_INVALID_ARG,
+               "n=%lld: the Sylvester transform takes a power of two in [2, 8192]", (long long)n);
+  QLIN_REQUIRE(kind != QLIN_HADAMARD_REGULAR || n == 4 || n == 16 || n == 64 || n == 256, QLIN_ERR_INVALID_ARG,
+               "n=%lld: the regular transform takes 4, 16, 64 or 256", (long long)n);
+  QLIN_REQUIRE(rows >= 0 && rows <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG,
+               "bad sizes rows=%lld K=%lld", (long long)rows, (long long)K);
+  QLIN_REQUIRE(K % n == 0 && K % 8 == 0, QLIN_ERR_INVALID_ARG, "K=%lld must be a multiple of n=%lld and of 8",
+               (long long)K, (long long)n);
+  if (rows == 0) return ok();
+  QLIN_REQUIRE(x && y, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(x) && aligned16(y), QLIN_ERR_ALIGNMENT, "x and y must be 16-byte aligned");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(signs) & 7u) == 0, QLIN_ERR_ALIGNMENT, "signs must be 8-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_hadamard(x, dtype, rows, K, kind, n, signs, y, stream), "hadamard launch");
+}
+
 int64_t qlin_mx_sf_bytes(int64_t rows, int64_t K, qlin_sf_layout sf_layout) {
   if (rows < 0 || K <= 0 || K % 32 != 0) return -1;
   if (sf_layout == QLIN_SF_ROWS) return rows * (K / 32);

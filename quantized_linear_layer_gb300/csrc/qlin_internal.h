@@ -50,6 +50,8 @@ bool w4a16_skinny_supported(int64_t T, int64_t N, int64_t K);
 cudaError_t launch_w4a16_skinny_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
                                         const uint8_t* const* wq, const void* const* scales,
                                         const uint8_t* const* zeros, void* const* y, cudaStream_t stream);
+cudaError_t launch_hadamard(const void* x, qlin_dtype dtype, int64_t rows, int64_t K, qlin_hadamard_kind kind,
+                            int64_t n, const int8_t* signs, void* y, cudaStream_t stream);
 // W4A16 act-order: group-sorted column order and codes (offline), activation gather.
 cudaError_t launch_w4a16_act_order_prepare(const int32_t* g_idx, int64_t K, int64_t group, const uint8_t* wq,
                                            int64_t N, int32_t* perm, uint8_t* wq_sorted, cudaStream_t stream);

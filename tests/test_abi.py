@@ -127,6 +127,15 @@ def test_rejects_bad_arguments_without_gpu(built):
                                       None) == 3
     assert L.qlin_rmsnorm_quant_nvfp4(P(16), 0, 4, 64, P(16), F(1e-6), None, 8, 0, P(16), P(16), P(16), 0, None) == 1
     assert L.qlin_rmsnorm_quant_nvfp4(None, 0, 0, 64, None, F(1e-6), None, 0, 0, None, None, None, 0, None) == 0
+    # Hadamard: unknown kind, n not a power of two, regular n = 8, n above 8192, K not a
+    # multiple of n, misaligned signs; an empty problem
+    assert L.qlin_hadamard(P(16), 0, 4, 256, 2, 256, None, P(16), None) == 1
+    assert L.qlin_hadamard(P(16), 0, 4, 384, 0, 48, None, P(16), None) == 1
+    assert L.qlin_hadamard(P(16), 0, 4, 256, 1, 8, None, P(16), None) == 1
+    assert L.qlin_hadamard(P(16), 0, 4, 16384, 0, 16384, None, P(16), None) == 1
+    assert L.qlin_hadamard(P(16), 0, 4, 320, 0, 256, None, P(16), None) == 1
+    assert L.qlin_hadamard(P(16), 0, 4, 256, 0, 256, P(12), P(16), None) == 2
+    assert L.qlin_hadamard(None, 0, 0, 256, 0, 256, None, None, None) == 0
     # act-order: group 64 not built, K not a multiple of 128, misaligned perm, wq_sorted
     # aliasing wq; GEMM: x_work missing or aliasing x, misaligned x_work; empty problems
     assert L.qlin_w4a16_act_order_prepare(P(16), 256, 64, P(16), 4, P(16), P(32), None) == 3
