@@ -13,27 +13,28 @@
 // only the packed codes (half a byte per weight) pass through shared memory.
 // The activations are the B operand, copied by TMA straight into the
 // 128-byte swizzled K-major layout the MMA reads.  One CTA per SM walks
-// 128 (weight rows) x 128 (tokens) output tiles; a K stage of 128 is one
+// 128 (weight rows) x 256 (tokens) output tiles; a K stage of 128 is one
 // quantization group, so each row needs one scale and one zero-point per
-// stage.  Two accumulators let a tile's epilogue run under the next tile's
-// MMAs.
+// stage.  N = 256: with 128 x 128 tiles the same kernel ran its kind::f16
+// MMAs at about half the rate (0.40-0.48 of the bf16 peak against 0.65-0.77).
 //
-//   warp 0       TMA producer: per stage the activation tile (128 tokens x
-//                128 K, two 64-element K blocks, 32 KB) and the packed codes
+//   warp 0       TMA producer: per stage the activation tile (256 tokens x
+//                128 K, two 64-element K blocks, 64 KB) and the packed codes
 //                (128 rows x 64 bytes in the 64-byte swizzle, 8 KB) into a
-//                4-stage ring.
+//                3-stage ring.
 //   warp 1       TMEM allocation and the MMA issuer: 8 x tcgen05.mma
-//                kind::f16 (M = 128, N = 128, K = 16, A from TMEM) per stage
-//                into one of two 128-column fp32 accumulators.
-//   warps 2-13   dequantizers, three sets of four taking every third stage: lane
+//                kind::f16 (M = 128, N = 256, K = 16, A from TMEM) per stage
+//                into one 256-column fp32 accumulator.
+//   warps 2-9    dequantizers, two sets of four taking alternate stages: lane
 //                l of the warp with TMEM lane quadrant q owns weight row
 //                32q + l, turns its 128 codes of the stage into 64 fp16 pairs
 //                and stores them into a 3-stage A ring in TMEM (64 columns
 //                per stage); the scale and zero-point of its next stage are
 //                loaded while it works on the current one.
-//   warps 14-17  epilogue: lane l of quadrant q owns weight row 32q + l and
-//                writes its 128 tokens, 32 at a time.
-// TMEM columns: [0, 256) the two accumulators, [256, 448) the A ring.
+//   warps 10-17  epilogue: two warps per lane quadrant; lane l of quadrant q
+//                owns weight row 32q + l and writes its 128 tokens of the
+//                tile, 32 at a time, then frees the accumulator.
+// TMEM columns: [0, 256) the accumulator, [256, 448) the A ring.
 // Every barrier wait is bounded; on expiry the kernel records the site in the
 // device error word, stops issuing work, waits (bounded) for copies and MMAs
 // already in flight, frees TMEM and exits.
@@ -49,18 +50,19 @@ namespace qlin {
 namespace {
 
 constexpr int kPfBM = 128;                          // weight rows per tile (MMA M)
-constexpr int kPfBN = 128;                          // tokens per tile (MMA N)
+constexpr int kPfBN = 256;                          // tokens per tile (MMA N)
 constexpr int kPfBK = 128;                          // K per stage: one quantization group
-constexpr int kPfStg = 4;                           // shared-memory stages
+constexpr int kPfStg = 3;                           // shared-memory stages
 constexpr int kPfOpsA = 3;                          // TMEM stages of dequantized weights
 constexpr int kPfTmemCols = 512;
-constexpr int kPfTmemA = 2 * kPfBN;                 // A ring after the two accumulators
-constexpr int kPfSets = 3;                          // dequantizer sets of four warps
+constexpr int kPfTmemA = kPfBN;                     // A ring after the accumulator
+constexpr int kPfSets = 2;                          // dequantizer sets of four warps
 constexpr int kPfWarpA0 = 2, kPfWarpE0 = kPfWarpA0 + 4 * kPfSets;
-constexpr int kPfThreads = (kPfWarpE0 + 4) * 32;
-constexpr int kPfXBytes = kPfBN * kPfBK * 2;        // 32 KB of fp16 activations
+constexpr int kPfEpiWarps = 8;                      // two per TMEM lane quadrant
+constexpr int kPfThreads = (kPfWarpE0 + kPfEpiWarps) * 32;
+constexpr int kPfXBytes = kPfBN * kPfBK * 2;        // 64 KB of fp16 activations
 constexpr int kPfWBytes = kPfBM * kPfBK / 2;        // 8 KB of packed codes
-constexpr int kPfStgBytes = kPfXBytes + kPfWBytes;  // 40 KB (a multiple of 1024)
+constexpr int kPfStgBytes = kPfXBytes + kPfWBytes;  // 72 KB (a multiple of 1024)
 constexpr int kPfSmemBar = kPfStg * kPfStgBytes;
 constexpr int kPfNumBars = 2 * kPfStg + 2 * kPfOpsA + 5;
 constexpr int kPfSmemMisc = kPfSmemBar + kPfNumBars * 8;
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(acc_full(b), 1);
-      tc::mbar_init(acc_empty(b), 4);  // the four epilogue warps
+      tc::mbar_init(acc_empty(b), kPfEpiWarps);
     }
     tc::mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -196,9 +198,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
       bool issued_any = false;
       int it = 0;
       for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
-        const int buf = ti & 1;
-        // the epilogue has written out the tile that last used this accumulator
-        if (ti >= 2 && !tc::mbar_wait(acc_empty(buf), ((ti >> 1) - 1) & 1, err, kPfSiteAccEmpty)) {
+        const int buf = 0;
+        // the epilogue has written out the previous tile
+        if (ti >= 1 && !tc::mbar_wait(acc_empty(buf), (ti - 1) & 1, err, kPfSiteAccEmpty)) {
           *abort_flag = 1;
           break;
         }
@@ -304,11 +306,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
     }
   } else {
     // ---------------- epilogue ----------------
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const int q = warp & 3;                    // TMEM lane quadrant this warp may access
+    const int half = (warp - kPfWarpE0) >> 2;  // 128-token half of the tile
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + half * 128;
     for (int ti = 0; ti < my_tiles; ++ti) {
-      const int buf = ti & 1;
-      bool ok = tc::mbar_wait(acc_full(buf), (ti >> 1) & 1, err, kPfSiteAccFull);
+      const int buf = 0;
+      bool ok = tc::mbar_wait(acc_full(buf), ti & 1, err, kPfSiteAccFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         *abort_flag = 1;
@@ -322,12 +325,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
       const int n = mt * kPfBM + q * 32 + lane;
       unsigned short* yr = reinterpret_cast<unsigned short*>(y) + n;
 #pragma unroll 1
-      for (int cg = 0; cg < kPfBN / 32; ++cg) {
+      for (int cg = 0; cg < 4; ++cg) {
         __syncwarp();  // reconverge after the bound checks before the aligned TMEM load
         uint32_t v[32];
         tc::tmem_ld_32x32b_x32(lane_base + buf * kPfBN + cg * 32, v);
         tc::tmem_wait_ld();
-        const int t0 = nt * kPfBN + cg * 32;
+        const int t0 = nt * kPfBN + half * 128 + cg * 32;
         if (n < N) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
