@@ -216,7 +216,8 @@ qlin_status qlin_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int cou
  *   gather kernel), then qlin_w4a16_gemm(x_work, wq_sorted, scales, zeros);
  *   the sums are the same terms in another order.
  *   x, x_work  fp16 [T][K] (16-byte aligned; x_work is a caller workspace)
- *   other arguments as in qlin_w4a16_gemm; group 128.
+ *   other arguments as in qlin_w4a16_gemm; group 128; K <= 98304 (a row is
+ *   staged in shared memory for the gather, QLIN_ERR_UNSUPPORTED above).
  * ---------------------------------------------------------------------- */
 qlin_status qlin_w4a16_act_order_prepare(const int32_t* g_idx, int64_t K, int64_t group, const uint8_t* wq,
                                          int64_t N, int32_t* perm, uint8_t* wq_sorted, cudaStream_t stream);

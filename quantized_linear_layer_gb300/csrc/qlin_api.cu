@@ -242,6 +242,8 @@ qlin_status qlin_w4a16_gemm_act_order(const void* x, int64_t T, int64_t N, int64
   QLIN_REQUIRE(N >= 0 && N <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad sizes N=%lld K=%lld",
                (long long)N, (long long)K);
   QLIN_REQUIRE(K % group == 0, QLIN_ERR_INVALID_ARG, "K=%lld is not a multiple of the group size", (long long)K);
+  QLIN_REQUIRE(K <= 98304, QLIN_ERR_UNSUPPORTED, "K=%lld: the gathered row must fit shared memory (K <= 98304)",
+               (long long)K);
   if (T == 0 || N == 0) return ok();
   QLIN_REQUIRE(x && perm && wq_sorted && scales && x_work && y, QLIN_ERR_INVALID_ARG, "null pointer");
   QLIN_REQUIRE(x_work != x, QLIN_ERR_INVALID_ARG, "x_work must not alias x");

@@ -67,27 +67,29 @@ __global__ void w4_permute_k_kernel(const uint8_t* __restrict__ wq, int64_t nbyt
   }
 }
 
-// x'[t][j] = x[t][perm[j]], eight outputs (one 16-byte store) per thread.
-__global__ void __launch_bounds__(kAoThreads) x_permute_kernel(const __half* __restrict__ x, int64_t nvec, int K,
+// x'[t][j] = x[t][perm[j]]: one CTA per row at a time; the row is copied into
+// shared memory with 16-byte loads (coalesced), then each thread gathers
+// eight elements from it and writes them with one 16-byte store.
+__global__ void __launch_bounds__(kAoThreads) x_permute_kernel(const __half* __restrict__ x, int64_t T, int K,
                                                                 const int32_t* __restrict__ perm,
                                                                 __half* __restrict__ out, int32_t* __restrict__ err) {
-  const int vpr = K / 8;
-  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec;
-       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t t = v / vpr;
-    const int j0 = static_cast<int>(v - t * vpr) * 8;
-    const int4 p0 = __ldg(reinterpret_cast<const int4*>(perm + j0));
-    const int4 p1 = __ldg(reinterpret_cast<const int4*>(perm + j0 + 4));
-    const int32_t cols[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-    const unsigned short* xr = reinterpret_cast<const unsigned short*>(x) + t * K;
-    uint32_t w[4];
+  extern __shared__ __align__(16) unsigned short row[];
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * K);
+    for (int i = threadIdx.x; i < K / 8; i += kAoThreads) reinterpret_cast<uint4*>(row)[i] = __ldg(src + i);
+    __syncthreads();
+    for (int j0 = threadIdx.x * 8; j0 < K; j0 += kAoThreads * 8) {
+      const int4 p0 = __ldg(reinterpret_cast<const int4*>(perm + j0));
+      const int4 p1 = __ldg(reinterpret_cast<const int4*>(perm + j0 + 4));
+      const int32_t cols[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = __ldg(xr + checked_col(cols[2 * i], K, err));
-      const uint32_t hi = __ldg(xr + checked_col(cols[2 * i + 1], K, err));
-      w[i] = lo | (hi << 16);
+      for (int i = 0; i < 4; ++i)
+        w[i] = static_cast<uint32_t>(row[checked_col(cols[2 * i], K, err)]) |
+               (static_cast<uint32_t>(row[checked_col(cols[2 * i + 1], K, err)]) << 16);
+      *reinterpret_cast<uint4*>(out + t * K + j0) = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    *reinterpret_cast<uint4*>(out + t * K + j0) = make_uint4(w[0], w[1], w[2], w[3]);
+    __syncthreads();  // the row buffer is refilled for the next row
   }
 }
 
@@ -114,11 +116,17 @@ cudaError_t launch_w4a16_act_order_prepare(const int32_t* g_idx, int64_t K, int6
 
 cudaError_t launch_x_permute(const void* x, int64_t T, int64_t K, const int32_t* perm, void* out,
                              cudaStream_t stream) {
-  const int64_t nvec = T * (K / 8);
-  if (nvec == 0) return cudaSuccess;
-  x_permute_kernel<<<grid_for(nvec), kAoThreads, 0, stream>>>(static_cast<const __half*>(x), nvec,
-                                                              static_cast<int>(K), perm,
-                                                              static_cast<__half*>(out), device_error_word());
+  if (T == 0) return cudaSuccess;
+  const size_t smem = static_cast<size_t>(K) * 2;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(x_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  const unsigned grid = static_cast<unsigned>(T < cap ? T : cap);
+  x_permute_kernel<<<grid, kAoThreads, smem, stream>>>(static_cast<const __half*>(x), T, static_cast<int>(K), perm,
+                                                       static_cast<__half*>(out), device_error_word());
   return cudaGetLastError();
 }
 

@@ -13,6 +13,8 @@ Operations (sizes as flags):
   nvfp4_gemm   qlin_nvfp4_gemm, A [T][K] and B [N][K] NVFP4 (made by the quantizer), bf16 out
   mxfp8_quant / mxfp4_quant  qlin_quant_mx, X [T][K] fp16, MMA scale layout
   mxfp8_gemm / mxfp4_gemm    qlin_mx_gemm, A [T][K] and B [N][K] (made by the quantizer), bf16 out
+  hadamard       qlin_hadamard, X [T][K] fp16, groups of --n (--kind 0 Sylvester, 1 regular), random signs
+  w4a16_act_order  qlin_w4a16_gemm_act_order, X [T][K] fp16, act-order weights N x K (gather + GEMM)
   rmsnorm_nvfp4  qlin_rmsnorm_quant_nvfp4, X [T][K] fp16, gamma [K], S residual channels, MMA scale layout
   rmsnorm_int8   qlin_rmsnorm_quant, X [T][K] fp16, gamma [K], per-token int8
   fp8_quant    qlin_quant_fp8, X [T][K] fp16, per-row E4M3
@@ -117,6 +119,29 @@ def _setup(args, q, torch):
         out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
         return lambda i: q.qlin_mx_gemm(qa, sfa, ws[i % copies][0], ws[i % copies][1], out, fmt=fmt)
 
+    if args.op == "hadamard":
+        xs = [randn((T, K), torch.float16) for _ in range(copies)]
+        ys = torch.empty_like(xs[0])
+        signs = (torch.randint(0, 2, (K,), device="cuda", generator=g) * 2 - 1).to(torch.int8)
+        return lambda i: q.qlin_hadamard(xs[i % copies], args.n, y=ys, kind=args.kind, signs=signs)
+
+    if args.op == "w4a16_act_order":
+        G = K // 128
+        g_idx = torch.randperm(K, device="cuda", generator=g).to(torch.int32) // 128   # each group 128 columns
+        x = randn((T, K), torch.float16)
+        mats = []
+        for _ in range(copies):
+            wq = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda", generator=g)
+            perm = torch.empty(K, dtype=torch.int32, device="cuda")
+            wq_sorted = torch.empty_like(wq)
+            q.qlin_w4a16_act_order_prepare(g_idx, wq, perm, wq_sorted)
+            sc = (torch.rand((N, G), device="cuda", generator=g) * 0.015 + 0.005).half()
+            zp = torch.randint(0, 256, (N, (G + 1) // 2), dtype=torch.uint8, device="cuda", generator=g)
+            mats.append((perm, wq_sorted, sc, zp))
+        x_work = torch.empty_like(x)
+        y = torch.empty((T, N), dtype=torch.float16, device="cuda")
+        return lambda i: q.qlin_w4a16_gemm_act_order(x, *mats[i % copies], y, x_work=x_work)
+
     if args.op in ("rmsnorm_nvfp4", "rmsnorm_int8"):
         xs = [randn((T, K), torch.float16) for _ in range(copies)]
         gam = (torch.rand(K, device="cuda", generator=g) + 0.5).half()
@@ -158,7 +183,9 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("op", choices=["w4a16", "w4a16_group", "int8_quant", "w8a8", "nvfp4_quant", "nvfp4_gemm",
                                    "fp8_quant", "fp8_gemm", "rmsnorm_nvfp4", "rmsnorm_int8", "mxfp8_quant",
-                                   "mxfp4_quant", "mxfp8_gemm", "mxfp4_gemm"])
+                                   "mxfp4_quant", "mxfp8_gemm", "mxfp4_gemm", "hadamard", "w4a16_act_order"])
+    ap.add_argument("--n", type=int, default=256, help="Hadamard group size")
+    ap.add_argument("--kind", type=int, default=0, help="Hadamard kind: 0 Sylvester, 1 regular")
     ap.add_argument("--T", type=int, default=1)
     ap.add_argument("--N", type=int, default=4096)
     ap.add_argument("--K", type=int, default=4096)
