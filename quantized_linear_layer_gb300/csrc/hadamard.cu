@@ -34,9 +34,26 @@ namespace {
 
 constexpr int kHdThreads = 256;
 
+// Eight elements as float32 through the coherent path (not the read-only
+// one: the rotation may run in place).
 template <int DT>
 __device__ __forceinline__ void load8(const void* p, float* v) {
-  Vec8Loader<DT>::load(p, v);
+  if constexpr (DT == 2) {
+    const float4 a = static_cast<const float4*>(p)[0], b = static_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 u = *static_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f;
+      if constexpr (DT == 0) f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
 }
 
 template <int DT>
@@ -161,9 +178,11 @@ __device__ __forceinline__ void scale_and_sign(float* v, float c, const int8_t* 
 // same iterations (the shuffles need the whole warp), and a group is all in
 // range or all out (K is a multiple of n).
 template <int DT, int KIND>
-__global__ void __launch_bounds__(kHdThreads) hadamard_warp_kernel(const void* __restrict__ x, int64_t nvec, int K,
+__global__ void __launch_bounds__(kHdThreads) hadamard_warp_kernel(const void* x, int64_t nvec, int K,
                                                                   int n, float c, const int8_t* __restrict__ signs,
-                                                                  void* __restrict__ y) {
+                                                                  void* y) {
+  // x and y may be the same rows (in place): every element is read by the
+  // thread that later writes it, before the write
   constexpr int EB = DT == 2 ? 4 : 2;
   const int lane = threadIdx.x & 31;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kHdThreads;
@@ -194,9 +213,9 @@ __global__ void __launch_bounds__(kHdThreads) hadamard_warp_kernel(const void* _
 // stages h >= 256 through shared memory (each thread keeps its own 8 values
 // in registers and reads the 8 partners).
 template <int DT>
-__global__ void __launch_bounds__(1024) hadamard_cta_kernel(const void* __restrict__ x, int64_t groups, int K, int n,
+__global__ void __launch_bounds__(1024) hadamard_cta_kernel(const void* x, int64_t groups, int K, int n,
                                                             float c, const int8_t* __restrict__ signs,
-                                                            void* __restrict__ y) {
+                                                            void* y) {
   extern __shared__ __align__(16) float buf[];
   constexpr int EB = DT == 2 ? 4 : 2;
   const int tid = threadIdx.x, lane = tid & 31;
