@@ -45,6 +45,7 @@
 #include "qlin_internal.h"
 #include "tc_common.cuh"
 #include "tmap.h"
+#include "w4a16_mma_common.cuh"
 
 namespace qlin {
 namespace {
@@ -64,7 +65,7 @@ constexpr int kPfXBytes = kPfBN * kPfBK * 2;        // 64 KB of fp16 activations
 constexpr int kPfWBytes = kPfBM * kPfBK / 2;        // 8 KB of packed codes
 constexpr int kPfStgBytes = kPfXBytes + kPfWBytes;  // 72 KB (a multiple of 1024)
 constexpr int kPfSmemBar = kPfStg * kPfStgBytes;
-constexpr int kPfNumBars = 2 * kPfStg + 2 * kPfOpsA + 5;
+constexpr int kPfNumBars = 2 * kPfStg + 2 * kPfOpsA + 7;
 constexpr int kPfSmemMisc = kPfSmemBar + kPfNumBars * 8;
 constexpr int kPfSmemTotal = kPfSmemMisc + 16 + 1024;  // + alignment slack
 static_assert(kPfSmemTotal <= 227 * 1024, "shared memory budget");
@@ -72,7 +73,16 @@ static_assert(kPfTmemA + kPfOpsA * (kPfBK / 2) <= kPfTmemCols, "TMEM budget");
 static_assert(kPfStgBytes % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled tiles");
 
 enum { kPfSiteStgEmpty = 1, kPfSiteStgFull, kPfSiteAEmpty, kPfSiteAFull, kPfSiteAccEmpty, kPfSiteAccFull,
-       kPfSiteDrain };
+       kPfSiteDrain, kPfSiteRedReady, kPfSiteRedData };
+
+// A bounded wait (about a second) on a local mbarrier that a CTA of the
+// cluster arrives on with release semantics.
+__device__ __forceinline__ bool pf_wait_cluster(uint32_t bar, uint32_t parity, int32_t* err, int site) {
+  for (int i = 0; i < 1000; ++i)
+    if (w4mma::mbar_try_wait_cluster(bar, parity)) return true;
+  record_device_error(err, kDevErrTimeoutBase + site);
+  return false;
+}
 
 // Eight codes of one word (element k + i in bits 4i .. 4i+3) -> four words of
 // fp16 pairs ((k, k+1), (k+2, k+3), ...), each (q - z) . s rounded once.
@@ -112,15 +122,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
                                                                       const __half* __restrict__ scales,
                                                                       const uint8_t* __restrict__ zeros, int T,
                                                                       int N, int K, __half* __restrict__ y,
-                                                                      int32_t* __restrict__ err) {
+                                                                      int split, int32_t* __restrict__ err) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt_count = (N + kPfBM - 1) / kPfBM, nt_count = (T + kPfBN - 1) / kPfBN;
   const int tiles = mt_count * nt_count;
-  const int my_tiles = blockIdx.x < tiles ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  // split == 2: a cluster of two CTAs shares one tile, each taking half of K
+  // (rank 0 the first half); rank 1's accumulator is added to rank 0's through
+  // distributed shared memory before the store.  Otherwise CTAs are
+  // persistent over the tiles.
+  const uint32_t rank = split == 2 ? w4mma::cluster_rank() : 0u;
+  const int tile0 = split == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tstride = split == 2 ? tiles : static_cast<int>(gridDim.x);
+  const int my_tiles = tile0 < tiles ? (split == 2 ? 1 : (tiles - tile0 + tstride - 1) / tstride) : 0;
   const int num_kb = K / kPfBK;
+  const int kb_begin = (split == 2 && rank == 1) ? num_kb / 2 : 0;
+  const int kb_count = split == 2 ? (rank == 1 ? num_kb - num_kb / 2 : num_kb / 2) : num_kb;
   const int G = K / 128, zpitch = (G + 1) / 2;
 
   const uint32_t sbase = tc::smem_u32(smem);
@@ -132,6 +151,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
   auto acc_full = [&](int b) { return bar0 + 8u * (2 * kPfStg + 2 * kPfOpsA + b); };
   auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kPfStg + 2 * kPfOpsA + 2 + b); };
   const uint32_t mma_done = bar0 + 8u * (2 * kPfStg + 2 * kPfOpsA + 4);
+  const uint32_t red_ready = mma_done + 8u;  // (rank 1) rank 0's stage buffers are free
+  const uint32_t red_data = mma_done + 16u;  // (rank 0) rank 1's accumulator has landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPfSmemMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kPfSmemMisc + 4);
 
@@ -149,6 +170,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
       tc::mbar_init(acc_empty(b), kPfEpiWarps);
     }
     tc::mbar_init(mma_done, 1);
+    tc::mbar_init(red_ready, kPfEpiWarps * 32);
+    tc::mbar_init(red_data, kPfEpiWarps * 32);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -160,6 +183,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (split == 2) w4mma::cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -170,8 +194,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
       int it = 0, issued = 0;
       for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
         int mt, nt;
-        pf_tile_coords(blockIdx.x + ti * gridDim.x, mt_count, nt_count, mt, nt);
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        pf_tile_coords(tile0 + ti * tstride, mt_count, nt_count, mt, nt);
+        for (int kbi = 0; kbi < kb_count; ++kbi, ++it) {
+          const int kb = kb_begin + kbi;
           const int s = it % kPfStg;
           if (it >= kPfStg && !tc::mbar_wait(stg_empty(s), ((it / kPfStg) - 1) & 1, err, kPfSiteStgEmpty)) {
             *abort_flag = 1;
@@ -205,7 +230,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
           break;
         }
         tc::tc_fence_after();
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        for (int kbi = 0; kbi < kb_count; ++kbi, ++it) {
           const int s = it % kPfStg, o = it % kPfOpsA;
           if (!tc::mbar_wait(a_full(o), (it / kPfOpsA) & 1, err, kPfSiteAFull) ||
               !tc::mbar_wait(stg_full(s), (it / kPfStg) & 1, err, kPfSiteStgFull)) {
@@ -220,7 +245,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
           for (int k = 0; k < kPfBK / 16; ++k) {
             const uint32_t b_k = xb + (k >> 2) * (kPfBN * 128) + 32 * (k & 3);  // K block, then 32 B in the atom
             tc::mma_f16_ta(tmem + buf * kPfBN, a_t + 8 * k, tc::sw128_kmajor_desc(b_k), idesc,
-                           (kb > 0 || k > 0) ? 1u : 0u);
+                           (kbi > 0 || k > 0) ? 1u : 0u);
           }
           issued_any = true;
           tc::mma_commit(a_empty(o));
@@ -240,17 +265,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
     const int q = warp & 3;                   // TMEM lane quadrant of this warp
     const int r = q * 32 + lane;              // weight row of the tile
     pdl_wait();                               // scales and zero-points, like every input
-    // Stage i of this CTA is K block i % num_kb of its tile i / num_kb.  The
+    // Stage i of this CTA is K block kb_begin + i % kb_count of its tile
+    // i / kb_count (kb_count = num_kb unless the tile is split).  The
     // scale and zero-point of the set's next stage are loaded while the
     // current stage is dequantized, so their latency stays off the chain.
-    const int total = my_tiles * num_kb;
+    const int total = my_tiles * kb_count;
     auto load_sz = [&](int i, __half& sc, uint32_t& z) {
       sc = __ushort_as_half(0);  // rows past N dequantize to 0
       z = 0;
       if (i >= total) return;
       int mt, nt;
-      pf_tile_coords(blockIdx.x + (i / num_kb) * gridDim.x, mt_count, nt_count, mt, nt);
-      const int n = mt * kPfBM + r, kb = i % num_kb;
+      pf_tile_coords(tile0 + (i / kb_count) * tstride, mt_count, nt_count, mt, nt);
+      const int n = mt * kPfBM + r, kb = kb_begin + i % kb_count;
       if (n < N) {
         sc = scales[static_cast<int64_t>(n) * G + kb];
         z = zeros != nullptr ? (zeros[static_cast<int64_t>(n) * zpitch + (kb >> 1)] >> (4 * (kb & 1))) & 0xFu : 8u;
@@ -319,23 +345,67 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
       }
       tc::tc_fence_after();
       int mt, nt;
-      pf_tile_coords(blockIdx.x + ti * gridDim.x, mt_count, nt_count, mt, nt);
-      // Y[t][n]: the warp's 32 lanes hold 32 consecutive n of each token t, so
-      // every store instruction writes 64 contiguous bytes
-      const int n = mt * kPfBM + q * 32 + lane;
-      unsigned short* yr = reinterpret_cast<unsigned short*>(y) + n;
+      pf_tile_coords(tile0 + ti * tstride, mt_count, nt_count, mt, nt);
+      const int row = q * 32 + lane;  // weight row within the tile
+      // the partner's accumulator in rank 0's stage area: row r's 64 chunks of
+      // 16 bytes, chunk c at position c ^ (r % 32) (fewer bank conflicts)
+      auto red_off = [&](int chunk) { return static_cast<uint32_t>((row * 64 + (chunk ^ (row & 31))) * 16); };
+      if (split == 2 && rank == 1) {
+        // push this half-K accumulator to rank 0 once its stage buffers are free
+        bool go = pf_wait_cluster(red_ready, 0, err, kPfSiteRedReady);
+        go = __all_sync(0xffffffffu, go);
+        if (go) {
+          const uint32_t remote = w4mma::map_to_rank(sbase, 0);
 #pragma unroll 1
-      for (int cg = 0; cg < 4; ++cg) {
-        __syncwarp();  // reconverge after the bound checks before the aligned TMEM load
-        uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(lane_base + buf * kPfBN + cg * 32, v);
-        tc::tmem_wait_ld();
-        const int t0 = nt * kPfBN + half * 128 + cg * 32;
-        if (n < N) {
+          for (int cg = 0; cg < 4; ++cg) {
+            __syncwarp();
+            uint32_t v[32];
+            tc::tmem_ld_32x32b_x32(lane_base + buf * kPfBN + cg * 32, v);
+            tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int t = t0 + i;
-            if (t < T) yr[static_cast<int64_t>(t) * N] = __half_as_ushort(__float2half_rn(__uint_as_float(v[i])));
+            for (int c4 = 0; c4 < 8; ++c4)
+              w4mma::st_cluster_v4(remote + red_off(half * 32 + cg * 8 + c4),
+                                   make_float4(__uint_as_float(v[4 * c4]), __uint_as_float(v[4 * c4 + 1]),
+                                               __uint_as_float(v[4 * c4 + 2]), __uint_as_float(v[4 * c4 + 3])));
+          }
+          w4mma::mbar_arrive_cluster(w4mma::map_to_rank(red_data, 0));
+        }
+      } else {
+        bool partner = false;
+        if (split == 2) {
+          // rank 0: every MMA of this CTA is done, so its stage buffers may take
+          // rank 1's accumulator
+          w4mma::mbar_arrive_cluster(w4mma::map_to_rank(red_ready, 1));
+          partner = pf_wait_cluster(red_data, 0, err, kPfSiteRedData);
+          partner = __all_sync(0xffffffffu, partner);
+        }
+        // Y[t][n]: the warp's 32 lanes hold 32 consecutive n of each token t, so
+        // every store instruction writes 64 contiguous bytes
+        const int n = mt * kPfBM + row;
+        unsigned short* yr = reinterpret_cast<unsigned short*>(y) + n;
+#pragma unroll 1
+        for (int cg = 0; cg < 4; ++cg) {
+          __syncwarp();  // reconverge after the bound checks before the aligned TMEM load
+          uint32_t v[32];
+          tc::tmem_ld_32x32b_x32(lane_base + buf * kPfBN + cg * 32, v);
+          tc::tmem_wait_ld();
+          if (partner) {  // first half of K plus second half, in that order
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const uint4 p4 = tc::lds128(sbase + red_off(half * 32 + cg * 8 + c4));
+              v[4 * c4] = __float_as_uint(__fadd_rn(__uint_as_float(v[4 * c4]), __uint_as_float(p4.x)));
+              v[4 * c4 + 1] = __float_as_uint(__fadd_rn(__uint_as_float(v[4 * c4 + 1]), __uint_as_float(p4.y)));
+              v[4 * c4 + 2] = __float_as_uint(__fadd_rn(__uint_as_float(v[4 * c4 + 2]), __uint_as_float(p4.z)));
+              v[4 * c4 + 3] = __float_as_uint(__fadd_rn(__uint_as_float(v[4 * c4 + 3]), __uint_as_float(p4.w)));
+            }
+          }
+          const int t0 = nt * kPfBN + half * 128 + cg * 32;
+          if (n < N) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int t = t0 + i;
+              if (t < T) yr[static_cast<int64_t>(t) * N] = __half_as_ushort(__float2half_rn(__uint_as_float(v[i])));
+            }
           }
         }
       }
@@ -347,6 +417,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
 
   tc::tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair leaves while the other may still touch its shared
+  // memory (every wait above is bounded, so all threads get here)
+  if (split == 2) w4mma::cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc::tc_fence_after();
@@ -373,20 +446,27 @@ cudaError_t launch_w4a16_prefill(const void* x, int64_t T, int64_t N, int64_t K,
   st = cudaFuncSetAttribute(w4a16_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemTotal);
   if (st != cudaSuccess) return st;
   const int64_t tiles = ((N + kPfBM - 1) / kPfBM) * ((T + kPfBN - 1) / kPfBN);
-  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  // few tiles (few tokens): two CTAs per tile, each half of K, so that twice
+  // as many SMs stream the weights
+  const int split = (2 * tiles <= sm_count() && K / kPfBK >= 2) ? 2 : 1;
+  const int grid = split == 2 ? static_cast<int>(2 * tiles) : static_cast<int>(tiles < sm_count() ? tiles : sm_count());
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kPfThreads);
   cfg.dynamicSmemBytes = kPfSmemTotal;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = split;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = split == 2 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, w4a16_prefill_kernel, tmX, tmW, static_cast<const __half*>(scales), zeros,
                             static_cast<int>(T), static_cast<int>(N), static_cast<int>(K), static_cast<__half*>(y),
-                            device_error_word());
+                            split, device_error_word());
 }
 
 }  // namespace qlin
