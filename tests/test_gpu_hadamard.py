@@ -59,3 +59,14 @@ def test_hadamard_in_place(qlin_gpu):
     qlin_gpu.qlin_hadamard(xt, 1024, y=xt)
     torch.cuda.synchronize()
     assert torch.equal(xt.cpu().view(torch.int16), want.view(torch.int16))
+
+
+@pytest.mark.parametrize("kind,n,rows,k", [("sylvester", 8, 1, 8), ("regular", 4, 3, 8), ("sylvester", 8192, 2, 8192)])
+def test_hadamard_small_and_largest(qlin_gpu, kind, n, rows, k):
+    x = np.random.default_rng(n + k).standard_normal((rows, k)).astype(np.float32)
+    xt = torch.from_numpy(x).cuda()
+    code = qlin_gpu.QLIN_HADAMARD_SYLVESTER if kind == "sylvester" else qlin_gpu.QLIN_HADAMARD_REGULAR
+    y = qlin_gpu.qlin_hadamard(xt, n, kind=code)
+    torch.cuda.synchronize()
+    want = oracle.hadamard_rotate(x, n, kind)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), want.view(np.uint32))

@@ -126,3 +126,21 @@ def test_mx_pipeline_sampled_rows(qlin_gpu, fmt):
     oqb, osb = oracle.mx_quantize(w.astype(np.float32), ofmt)
     ref = oracle.mx_gemm_reference(oqa, osa, oqb, osb, ofmt)
     assert_within_tolerance(out.float().cpu().numpy()[rows], ref, "%s pipeline (sampled rows)" % fmt)
+
+
+@pytest.mark.parametrize("fmt,T,N,K", [("mxfp8", 1, 8, 32), ("mxfp4", 3, 16, 64), ("mxfp8", 130, 264, 96)])
+def test_mx_gemm_smallest_k(qlin_gpu, fmt, T, N, K):
+    """One MMA of K (a single scale block for MXFP8, two for MXFP4), and a K of
+    three MXFP8 MMAs whose scale group is partial."""
+    ofmt, code = FMTS[fmt]
+    rng = np.random.default_rng(K + T)
+    qa, sfa = _random_operands(rng, T, K, ofmt)
+    qb, sfb = _random_operands(rng, N, K, ofmt)
+    out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    qlin_gpu.qlin_mx_gemm(_dev(_codes_bytes(qa, ofmt)), _dev(_mx_sf_mma(sfa)), _dev(_codes_bytes(qb, ofmt)),
+                          _dev(_mx_sf_mma(sfb)), out, fmt=code)
+    torch.cuda.synchronize()
+    assert qlin_gpu.qlin_get_device_error() == 0
+    ref = oracle.mx_gemm_reference(qa, sfa, qb, sfb, ofmt)
+    assert_within_tolerance(out.float().cpu().numpy(), ref, "%s GEMM %dx%dx%d" % (fmt, T, N, K),
+                            out_dtype=torch.bfloat16)

@@ -96,3 +96,16 @@ def test_prefill_llama_layers_sampled_rows(qlin_gpu, N, K):
                                      np.random.default_rng(N).choice(T, 24, replace=False)]))
     ref = oracle.w4a16_reference(d["x"][rows], codes, s16, z)
     assert_within_tolerance(y[rows], ref, "W4A16 prefill %dx%dx%d (sampled rows)" % (T, N, K))
+
+
+@pytest.mark.parametrize("T,N,K", [
+    (33, 8, 128),       # the smallest prefill: one tile, one K stage (no split)
+    (257, 128, 256),    # two token tiles, two K stages: the CTA pair splits K one stage each
+    (64, 256, 384),     # an odd stage count split 1 + 2
+])
+def test_prefill_edge_shapes(qlin_gpu, T, N, K):
+    d = inputs.w4a16_decode(seed=T * 3 + K, T=T, N=N, K=K)
+    codes, s16, z = oracle.quant_w4_g128(d["w"])
+    ref = oracle.w4a16_reference(d["x"], codes, s16, z)
+    y = _gemm(qlin_gpu, _dev(d["x"]), _dev(oracle.pack_u4(codes)), _dev(s16), _dev(oracle.pack_u4(z)))
+    assert_within_tolerance(y, ref, "W4A16 prefill edge T=%d N=%d K=%d" % (T, N, K))
