@@ -74,6 +74,9 @@ __global__ void __launch_bounds__(kAoThreads) x_permute_kernel(const __half* __r
                                                                 const int32_t* __restrict__ perm,
                                                                 __half* __restrict__ out, int32_t* __restrict__ err) {
   extern __shared__ __align__(16) unsigned short row[];
+  // the GEMM that follows may start streaming its weights meanwhile (it waits
+  // for this grid before it reads the gathered activations)
+  pdl_launch_dependents();
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     const uint4* src = reinterpret_cast<const uint4*>(x + t * K);
     for (int i = threadIdx.x; i < K / 8; i += kAoThreads) reinterpret_cast<uint4*>(row)[i] = __ldg(src + i);
