@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(kHdThreads) hadamard_warp_kernel(const void* x
                                                                   void* y) {
   // x and y may be the same rows (in place): every element is read by the
   // thread that later writes it, before the write
+  pdl_launch_dependents();  // the quantizer that reads the rotated rows may start setting up
   constexpr int EB = DT == 2 ? 4 : 2;
   const int lane = threadIdx.x & 31;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kHdThreads;
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(1024) hadamard_cta_kernel(const void* x, int64
                                                             float c, const int8_t* __restrict__ signs,
                                                             void* y) {
   extern __shared__ __align__(16) float buf[];
+  pdl_launch_dependents();
   constexpr int EB = DT == 2 ? 4 : 2;
   const int tid = threadIdx.x, lane = tid & 31;
   for (int64_t g = blockIdx.x; g < groups; g += gridDim.x) {

@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) w4a16_prefill_kernel(const __gr
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
+  pdl_launch_dependents();  // the next layer may start setting up (it waits for this grid before reading Y)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt_count = (N + kPfBM - 1) / kPfBM, nt_count = (T + kPfBN - 1) / kPfBN;
   const int tiles = mt_count * nt_count;
