@@ -35,6 +35,10 @@
 //                owns weight row 32q + l and writes its 128 tokens of the
 //                tile, 32 at a time, then frees the accumulator.
 // TMEM columns: [0, 256) the accumulator, [256, 448) the A ring.
+// Few tiles (few tokens): a cluster of two CTAs shares each tile, each taking
+// half of K; rank 1 pushes its accumulator into rank 0's free stage buffers
+// through distributed shared memory and rank 0 adds the halves before the
+// store.
 // Every barrier wait is bounded; on expiry the kernel records the site in the
 // device error word, stops issuing work, waits (bounded) for copies and MMAs
 // already in flight, frees TMEM and exits.
