@@ -268,12 +268,34 @@ int64_t qlin_w4a16_sequence_workspace_bytes(int64_t nsteps);
 qlin_status qlin_w4a16_gemv_sequence(const qlin_w4a16_step* steps, int nsteps, int64_t group, void* workspace,
                                      cudaStream_t stream);
 
-/* The same without a caller workspace: the barrier counters live in a
-   static device array of the library (no allocation by the caller or the
-   library).  Only one such call may be in flight on a device at a time:
-   calls on one stream are safe; calls on concurrent streams, or in CUDA
-   graphs replayed concurrently, must use qlin_w4a16_gemv_sequence with their
-   own workspaces. */
+/* The same sequence without any device memory from the caller.  The pages
+   have no counterpart of this entry point; it exists for callers that cannot
+   allocate device memory on the path that runs the decoder: an inference
+   runtime that loads this library as a plugin and gives it no allocator or
+   workspace, or a serving engine that reserved nearly all of HBM for weights
+   and KV cache at start-up and lets nothing else call cudaMalloc (which may
+   also synchronize the device, a stall a per-token loop cannot take).
+   The grid barrier's counters live in a fixed array of 128 four-byte words
+   inside the library (a static device variable, 512 bytes, which every GPU
+   that loads the library holds until the process exits).
+   - No allocation: the call makes no cudaMalloc or cudaFree and no other
+     allocating call, on the device or on the host.
+   - Size limit: every launch takes at most 128 steps, the array's size; a
+     longer sequence runs as several launches on `stream`, one after another,
+     each of which first zeroes (memset on `stream`) the counters it uses.
+     So any nsteps is accepted, and no counter state carries over from an
+     earlier call.
+   - Set-up: the first call with a device current looks up the array's
+     device address for that device (cudaGetSymbolAddress) and keeps it;
+     make that first call before any stream capture begins.  A failed lookup
+     returns QLIN_ERR_CUDA.
+   - Sharing: all calls on a device share the one array.  Calls issued on
+     one stream run one after another and are safe; two calls whose kernels
+     can overlap on the GPU (different streams, or concurrently replayed
+     graphs) race on the counters and give wrong results or a timeout in the
+     device error word.  Such callers must use qlin_w4a16_gemv_sequence with
+     a workspace each.
+   Outputs equal qlin_w4a16_gemv_sequence's bit for bit. */
 qlin_status qlin_w4a16_gemv_sequence_noalloc(const qlin_w4a16_step* steps, int nsteps, int64_t group,
                                              cudaStream_t stream);
 

@@ -300,8 +300,9 @@ qlin_status qlin_w4a16_gemv_sequence_noalloc(const qlin_w4a16_step* steps, int n
                                              cudaStream_t stream) {
   if (nsteps == 0) return qlin_w4a16_gemv_sequence(steps, nsteps, group, reinterpret_cast<void*>(16), stream);
   QLIN_DEVICE();
-  unsigned int* ws = w4a16_sequence_static_workspace();
-  QLIN_REQUIRE(ws != nullptr, QLIN_ERR_CUDA, "device counters unavailable");
+  unsigned int* ws = nullptr;
+  const cudaError_t e = w4a16_sequence_static_workspace(&ws);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(sequence counters)");
   return qlin_w4a16_gemv_sequence(steps, nsteps, group, ws, stream);
 }
 

@@ -40,9 +40,11 @@ bool w4a16_sequence_supported(int64_t K);
 // each); workspace holds one arrival counter per step.
 cudaError_t launch_w4a16_sequence(const W4A16SeqStep* steps, int nsteps, unsigned int* workspace,
                                   cudaStream_t stream);
-// Device address of the library's own counters (enough for every launch of
-// a sequence: each launch takes at most 128 steps and zeroes them first).
-unsigned int* w4a16_sequence_static_workspace();
+// Device address of the library's own counters on the current device (enough
+// for every launch of a sequence: each launch takes at most 128 steps and
+// zeroes them first).  The address is looked up once per device, on the
+// first call with that device current.
+cudaError_t w4a16_sequence_static_workspace(unsigned int** out);
 // Streamed tensor-core W4A16 for up to 16 tokens over the concatenated rows
 // of `count` matrices sharing x (false / cudaErrorInvalidValue when the
 // shape has no launch plan).

@@ -31,6 +31,8 @@
 // Every wait is bounded: on expiry the kernel records the site in the device
 // error word and stops, and every other CTA's bounded waits end the same way.
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 
 #include "device_common.cuh"
 #include "qlin_internal.h"
@@ -423,23 +425,66 @@ __global__ void __launch_bounds__(kSqThreads, 1) w4a16_seq_kernel(const __grid_c
 // at the same time.
 static __device__ __align__(256) unsigned int g_seq_counters[kSqMaxSteps];
 
+constexpr int kSqMaxDevices = 64;
+std::mutex g_seq_mutex;
+unsigned int* g_seq_counter_addr[kSqMaxDevices] = {};  // device address of g_seq_counters, per device
+std::atomic<int> g_seq_smem_set[kSqMaxDevices];         // largest dynamic shared memory granted, per device
+
+// The launch arguments are built in a per-thread host buffer (about 22 KB),
+// so a launch allocates nothing on the host either; cudaLaunchKernelEx copies
+// them before it returns.
+thread_local SqArgs t_sq_args;
+
 }  // namespace
 
-unsigned int* w4a16_sequence_static_workspace() {
-  void* p = nullptr;
-  return cudaGetSymbolAddress(&p, g_seq_counters) == cudaSuccess ? static_cast<unsigned int*>(p) : nullptr;
+cudaError_t w4a16_sequence_static_workspace(unsigned int** out) {
+  *out = nullptr;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kSqMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_seq_mutex);
+  if (g_seq_counter_addr[dev] == nullptr) {
+    // In host code g_seq_counters names a host-side stand-in, not device
+    // memory: the kernel must be given the address the runtime reports for
+    // this device.
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_seq_counters);
+    if (e != cudaSuccess) return e;
+    g_seq_counter_addr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_seq_counter_addr[dev];
+  return cudaSuccess;
 }
 
 int64_t w4a16_sequence_workspace_bytes(int64_t nsteps) { return (nsteps * 4 + 255) / 256 * 256; }
 
 bool w4a16_sequence_supported(int64_t K) { return K > 0 && K % 128 == 0 && K <= 12288; }
 
+// Raises the kernel's dynamic shared-memory limit on the current device when
+// a launch needs more than any earlier one did (one attribute call per new
+// maximum instead of one per launch).
+static cudaError_t sq_allow_smem(int smem) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kSqMaxDevices)
+    return cudaFuncSetAttribute(w4a16_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (g_seq_smem_set[dev].load(std::memory_order_acquire) >= smem) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(g_seq_mutex);
+  if (g_seq_smem_set[dev].load(std::memory_order_relaxed) >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(w4a16_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) g_seq_smem_set[dev].store(smem, std::memory_order_release);
+  return e;
+}
+
 cudaError_t launch_w4a16_sequence(const W4A16SeqStep* steps, int nsteps, unsigned int* workspace,
                                   cudaStream_t stream) {
   const int grid = sm_count();
   for (int s0 = 0; s0 < nsteps; s0 += kSqMaxSteps) {
     const int ns = std::min(kSqMaxSteps, nsteps - s0);
-    SqArgs* a = new SqArgs();
+    SqArgs* a = &t_sq_args;
+    *a = SqArgs{};
     int slot = 0, red_floats = 0, kmax = 0;
     for (int s = 0; s < ns; ++s) {
       const W4A16SeqStep& in = steps[s0 + s];
@@ -471,10 +516,7 @@ cudaError_t launch_w4a16_sequence(const W4A16SeqStep* steps, int nsteps, unsigne
     const int red_bytes = (red_floats * 4 + 15) / 16 * 16;
     const int x_bytes = kmax * 2;  // a multiple of 256
     const int S = std::min(kSqMaxSlots, (kSqSmemMax - red_bytes - x_bytes - 24 * kSqMaxSlots - 16) / a->slot_bytes);
-    if (S < 2) {
-      delete a;
-      return cudaErrorInvalidValue;
-    }
+    if (S < 2) return cudaErrorInvalidValue;
     a->S = S;
     a->off_red = S * a->slot_bytes;
     a->off_x = a->off_red + red_bytes;
@@ -483,8 +525,7 @@ cudaError_t launch_w4a16_sequence(const W4A16SeqStep* steps, int nsteps, unsigne
     a->grid_bar = workspace;
     a->err = device_error_word();
     cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned int) * ns, stream);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(w4a16_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = sq_allow_smem(smem);
     if (e == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(grid);
@@ -498,7 +539,6 @@ cudaError_t launch_w4a16_sequence(const W4A16SeqStep* steps, int nsteps, unsigne
       cfg.numAttrs = 1;
       e = cudaLaunchKernelEx(&cfg, w4a16_seq_kernel, *a);
     }
-    delete a;
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

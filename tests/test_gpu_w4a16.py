@@ -366,31 +366,6 @@ def test_sequence_ragged_groups_and_outliers(qlin_gpu):
         assert_within_tolerance(ys[i].cpu().numpy(), oracle.w4a16_reference(x, codes, s16, z), "ragged %d" % n)
 
 
-def test_sequence_noalloc_equals_workspace(qlin_gpu):
-    """The no-allocation entry point (the library's own barrier counters) gives
-    the same outputs as a caller workspace, call after call (each call zeroes
-    the counters it uses), including a sequence longer than one launch."""
-    width = 1408
-    mats = [_quantized(400 + i, width, width) for i in range(140)]
-    dev = [_dev_mats([m]) for m in mats]
-    x0 = _dev(inputs.w4a16_decode(seed=399, T=1, N=8, K=width)["x"])
-
-    def run(noalloc):
-        bufs = [x0.clone(), torch.empty((1, width), dtype=torch.float16, device="cuda")]
-        steps = [(bufs[i % 2], wq, sc, zp, [bufs[(i + 1) % 2]]) for i, (wq, sc, zp) in enumerate(dev)]
-        if noalloc:
-            qlin_gpu.qlin_w4a16_gemv_sequence_noalloc(steps)
-        else:
-            _run_sequence(qlin_gpu, steps)
-        torch.cuda.synchronize()
-        assert qlin_gpu.qlin_get_device_error() == 0
-        return bufs[len(dev) % 2].clone()
-
-    ref = run(False)
-    for _ in range(2):
-        assert torch.equal(run(True), ref)
-
-
 # ---- the streamed tensor-core path for a few tokens (T <= 16 per launch) ----
 
 @pytest.mark.parametrize("T,N,K", [
