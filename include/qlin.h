@@ -490,12 +490,10 @@ qlin_status qlin_fp8_gemm(const uint8_t* a, const uint8_t* b, int64_t T, int64_t
  * Quantization kernels", practical notes: the per-row max and quantization
  * fused into the upstream operator; "LLM and AIGC quantization", "Static and
  * dynamic quantization": the per-token reduction is usually fused into the
- * preceding RMSNorm).  Every step is one IEEE float32 operation; the mean of
- * squares is summed in a fixed order so that the result is reproducible: the
- * row's 8-element chunks c are dealt to 256 partial sums (chunk c to partial
- * c mod 256), each adds the squares of its chunks in ascending order, element
- * by element, and the partials meet in a binary tree (i += i + h, h = 128 ...
- * 1).
+ * preceding RMSNorm).  The mean of squares is the exact sum of the row's
+ * squares rounded once to float32 (nearest, ties to even), divided by K in
+ * float32: no order of additions is implied, and the result is the same for
+ * any number of threads.  Every other step is one IEEE float32 operation.
  *   x      [rows][K] of x_dtype (16-byte aligned; K a multiple of 16)
  *   gamma  [K] of x_dtype (16-byte aligned)
  *   eps    the RMSNorm epsilon (>= 0)
@@ -509,7 +507,7 @@ qlin_status qlin_rmsnorm_quant(const void* x, qlin_dtype x_dtype, int64_t rows, 
  * next 2 - RMSNorm fused with the NVFP4 / ARCQuant quantizer
  *
  * Per row, y = (x . inv) . gamma exactly as qlin_rmsnorm_quant defines it
- * (the same fixed order of the mean of squares, the same float32 steps),
+ * (the same exactly rounded mean of squares, the same float32 steps),
  * then qlin_quant_nvfp4 of y: the reordered channels ys = y[:, perm], the
  * 16-element blocks with E4M3 scales over the per-tensor g, and the S
  * residual (or duplicated) channels; y stays in float32 and x is read once.
@@ -559,21 +557,21 @@ qlin_status qlin_mx_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
  * next 4 - online Hadamard rotation of the activations before 4-bit
  * quantization
  *
- * Every group of n consecutive elements of each row is rotated:
- *   QLIN_HADAMARD_SYLVESTER ("LLM and AIGC quantization", QuaRot: the fast
- *     Walsh-Hadamard transform, log2(n) butterfly stages mapping the pair
- *     (a, b) at distance h to (a + b, a - b)), stages h = 1, 2, ..., n/2;
- *     n a power of two, 2 <= n <= 8192;
+ * Every group of n consecutive elements of each row is multiplied by the
+ * normalized Hadamard matrix H_n / sqrt(n), then by signs[k] (QuaRot's
+ * diag(+-1)) when signs is not NULL, and rounded once to the input dtype:
+ *   QLIN_HADAMARD_SYLVESTER ("LLM and AIGC quantization", QuaRot: the
+ *     Sylvester matrix, applied as the fast Walsh-Hadamard transform,
+ *     log2(n) butterfly stages mapping the pair (a, b) at distance h to
+ *     (a + b, a - b)); n a power of two, 2 <= n <= 8192;
  *   QLIN_HADAMARD_REGULAR (ConvRot: each group of N0 times the regular
  *     Hadamard, the Kronecker power of H4 = [[1,1,1,-1],[1,1,-1,1],
- *     [1,-1,1,1],[-1,1,1,1]]), radix-4 stages at strides 1, 4, 16, ...,
- *     each quad becoming y_i = s - 2 x_(3-i), s = (x0 + x1) + (x2 + x3);
- *     n in {4, 16, 64, 256};
- * then times c = float32(1/sqrt(n)), times signs[k] (QuaRot's diag(+-1))
- * when signs is not NULL, rounded once to the input dtype.  Every step is one
- * float32 operation in the order given, so the result is reproducible bit
- * for bit.  The weights take the same rotation offline (W . Q), which leaves
- * X . W^T unchanged.
+ *     [1,-1,1,1],[-1,1,1,1]], applied as radix-4 stages); n in {4, 16, 64,
+ *     256}.
+ * The stages run in float32; the result is within float32 rounding of the
+ * exact rotation (before the final rounding to the input dtype) and the same
+ * on every run.  The weights take the same rotation offline (W . Q), which
+ * leaves X . W^T unchanged.
  *   x      [rows][K] of dtype (F16, BF16 or F32), 16-byte aligned
  *   signs  int8 [K] of +1 / -1 (8-byte aligned), or NULL
  *   y      out, [rows][K] of dtype, 16-byte aligned (y == x allowed)

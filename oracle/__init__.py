@@ -51,6 +51,7 @@ from .quant import (  # noqa: F401
     quant_w4_g128,
     quant_fp8_rows,
     quant_fp8_tensor,
+    sum_squares_f32,
     rmsnorm_rows,
     rmsnorm_quant_int8,
     rmsnorm_quant_fp8,
@@ -72,10 +73,7 @@ from .mx import (  # noqa: F401
     e8m0_decode,
 )
 from .hadamard import (  # noqa: F401
-    fwht_rows,
-    regular_rows,
     hadamard_rotate,
-    hadamard_scale,
     sylvester_matrix,
     regular_matrix,
 )

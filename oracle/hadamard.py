@@ -1,94 +1,42 @@
 """Online Hadamard rotation of activations before 4-bit quantization (oracle
 side).  TEST INFRASTRUCTURE ONLY - see the package docstring.
 
-Two transforms, each applied to every group of n consecutive elements of a
-row along K:
+Every group of n consecutive elements of a row along K is multiplied by the
+normalized Hadamard matrix of order n, and the result optionally by a +-1
+sign per column:
 
-* Sylvester / fast Walsh-Hadamard ("LLM and AIGC quantization", QuaRot: the
-  randomized Hadamard Q = H . diag(+-1); the fast transform is log2(n)
-  butterfly stages, stage h mapping the pair (a, b) at distance h to
-  (a + b, a - b)).  The stages run in the order h = 1, 2, 4, ..., n/2.
-* Regular Hadamard of order n = 4^k ("LLM and AIGC quantization", ConvRot:
-  K is cut into groups of N0 (default 256) and every group is multiplied by
-  the same regular Hadamard, the k-fold Kronecker power of the 4 x 4 matrix
-  H4 = [[1,1,1,-1],[1,1,-1,1],[1,-1,1,1],[-1,1,1,1]], whose column sums are
-  +-sqrt(n); the group rotation is the block-diagonal diag(H, ..., H) and stays
-  orthogonal).  Computed as k radix-4 stages at strides 1, 4, 16, ...; every
-  quad (x0, x1, x2, x3) at one stride becomes y_i = s - 2 x_(3-i) with
-  s = (x0 + x1) + (x2 + x3) (H4 = J - 2 . antidiag).
+    y[g] = x[g] . H_n / sqrt(n),   then   y[:, k] = y[:, k] . signs[k]
 
-Both are then scaled by c = the float32 nearest 1/sqrt(n) (exactly 2^-k/2 for
-even powers of two), and optionally multiplied by per-column signs
-(diag(+-1) of QuaRot's Q = H . diag(+-1), column k of the row).  Every step
-is one float32 operation in the order written; the result is rounded once
-to the output type.  This fixed order is part of the operation's
-definition (the pages give the butterflies, not an order of roundings).
+computed in float64 from the matrix itself (one matrix product per group
+size), so the only rounding is float64's.  Two matrices:
 
-Pins: tests/test_oracle_pins.py (dense products with the matrices built from
-their definitions in float64, the regular matrix's +-1 response to a row of
-ones, orthogonality: applying a transform twice gives back x).
+* Sylvester H_n, n a power of two ("LLM and AIGC quantization", QuaRot
+  section: the Sylvester construction H_2n = [[H_n, H_n], [H_n, -H_n]], the
+  randomized Q = H . diag(+-1); the worked example rotates an 8-element
+  token by H_8 / sqrt(8)).
+* Regular H_n, n = 4^k ("LLM and AIGC quantization", ConvRot section: K is
+  cut into groups of N0 and every group is multiplied by the same regular
+  Hadamard, built from the 4 x 4 regular matrix H4 by Kronecker products;
+  every row and column sums to +-sqrt(n)).
+
+Readings: the signs multiply the rotated columns (Q = H . diag(+-1) applied
+as x . Q); a rotation of n = 8192 is computed with one Sylvester doubling
+step, [a, b] . [[H, H], [H, -H]] = [a H + b H, a H - b H], so that no dense
+matrix above 4096 x 4096 is built.
+
+Pins: tests/test_oracle_pins.py (the pages' two worked examples, matrices
+built two independent ways, orthogonality, column sums, involution).
 """
 import numpy as np
 
-F32 = np.float32
 H4 = np.array([[1, 1, 1, -1], [1, 1, -1, 1], [1, -1, 1, 1], [-1, 1, 1, 1]], dtype=np.float64)
+_DENSE_MAX = 4096
 
 
 def _is_pow(n, base):
     while n > 1 and n % base == 0:
         n //= base
     return n == 1
-
-
-def hadamard_scale(n):
-    """c = float32(1 / sqrt(n))."""
-    return F32(1.0 / np.sqrt(float(n)))
-
-
-def fwht_rows(x, n):
-    """Sylvester butterflies on every n-group of the rows of x (float32), unscaled."""
-    x = np.asarray(x, dtype=F32)
-    rows, k = x.shape
-    if not _is_pow(n, 2) or n < 2 or k % n:
-        raise ValueError("n must be a power of two dividing K")
-    y = x.reshape(rows * (k // n), n).copy()
-    h = 1
-    while h < n:
-        v = y.reshape(-1, n // (2 * h), 2, h)
-        a = v[:, :, 0, :].copy()
-        b = v[:, :, 1, :].copy()
-        v[:, :, 0, :] = (a + b).astype(F32)
-        v[:, :, 1, :] = (a - b).astype(F32)
-        h *= 2
-    return y.reshape(rows, k)
-
-
-def regular_rows(x, n):
-    """Radix-4 regular-Hadamard stages on every n-group of the rows (float32), unscaled."""
-    x = np.asarray(x, dtype=F32)
-    rows, k = x.shape
-    if not _is_pow(n, 4) or n < 4 or k % n:
-        raise ValueError("n must be a power of four dividing K")
-    y = x.reshape(rows * (k // n), n).copy()
-    d = 1
-    while d < n:
-        v = y.reshape(-1, n // (4 * d), 4, d)
-        q = [v[:, :, i, :].copy() for i in range(4)]
-        s = ((q[0] + q[1]).astype(F32) + (q[2] + q[3]).astype(F32)).astype(F32)
-        for i in range(4):
-            v[:, :, i, :] = (s - F32(2.0) * q[3 - i]).astype(F32)
-        d *= 4
-    return y.reshape(rows, k)
-
-
-def hadamard_rotate(x, n, kind="sylvester", signs=None):
-    """The rotation as the kernels compute it: float32 transform, times
-    c = float32(1/sqrt(n)), times signs[k] (+-1 per column, or None).  float32 out."""
-    t = fwht_rows(x, n) if kind == "sylvester" else regular_rows(x, n)
-    y = (t * hadamard_scale(n)).astype(F32)
-    if signs is not None:
-        y = (y * np.asarray(signs, dtype=F32)[None, :]).astype(F32)
-    return y
 
 
 def sylvester_matrix(n):
@@ -100,8 +48,39 @@ def sylvester_matrix(n):
 
 
 def regular_matrix(n):
-    """The k-fold Kronecker power of H4, float64, unnormalized."""
+    """The Kronecker power of H4 of order n = 4^k, float64, unnormalized."""
     h = np.ones((1, 1))
     while h.shape[0] < n:
         h = np.kron(h, H4)
     return h
+
+
+def _rotate_groups(g, n, kind):
+    """g: float64 [m][n] -> g . H_n (unnormalized)."""
+    if kind == "sylvester" and n > _DENSE_MAX:
+        a = _rotate_groups(g[:, : n // 2], n // 2, kind)
+        b = _rotate_groups(g[:, n // 2:], n // 2, kind)
+        return np.concatenate([a + b, a - b], axis=1)
+    h = sylvester_matrix(n) if kind == "sylvester" else regular_matrix(n)
+    return g @ h
+
+
+def hadamard_rotate(x, n, kind="sylvester", signs=None):
+    """x [rows][K] (K a multiple of n) -> float64 [rows][K]: every n-group
+    times H_n / sqrt(n), then times signs[k] per column (or no signs)."""
+    x = np.asarray(x, dtype=np.float64)
+    rows, k = x.shape
+    if kind == "sylvester":
+        if n < 2 or not _is_pow(n, 2):
+            raise ValueError("n must be a power of two")
+    elif kind == "regular":
+        if n < 4 or not _is_pow(n, 4):
+            raise ValueError("n must be a power of four")
+    else:
+        raise ValueError("kind must be 'sylvester' or 'regular'")
+    if k % n:
+        raise ValueError("n must divide K")
+    y = (_rotate_groups(x.reshape(rows * (k // n), n), n, kind) / np.sqrt(float(n))).reshape(rows, k)
+    if signs is not None:
+        y = y * np.asarray(signs, dtype=np.float64)[None, :]
+    return y

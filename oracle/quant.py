@@ -69,18 +69,17 @@ notes):
   uses s = 1; x / s is a float32 division, then the E4M3 encode (nearest,
   ties to even, saturating).
 * rmsnorm_*: RMSNorm is y = (x . inv) . gamma with inv = 1 / sqrt(mean(x^2)
-  + eps), every step a separate float32 operation (square, add, divide by K,
-  add eps, square root, divide 1 by it once per row, then two multiplies per
-  element); the pages fix neither the formula nor eps (it is an argument).
-  A row whose mean(x^2) + eps is 0 (eps = 0 and every square 0 or below the
-  float32 range) normalizes to 0.  The mean of squares is a float32 sum in a
-  fixed order that is part of the operation's definition (so its result is
-  reproducible bit for bit): the row's 8-element chunks c are dealt to 256
-  partial sums, chunk c to partial c mod 256; each partial adds the squares
-  of its chunks in ascending order, element by element; the 256 partials are
-  then added in a binary tree, partial i + partial i + h for h = 128, 64, ...,
-  1.  The normalized values are quantized as they are, never rounded to the
-  input dtype first.
+  + eps); the pages fix neither the formula nor eps (it is an argument).
+  The mean of squares is the exact sum of the row's squares (exact
+  rational arithmetic; every float32 square is exact in it) rounded once
+  to float32, round to nearest, ties to even, then one float32 division by
+  K: the pages fix no order of summation, and this is the one result that
+  no order of float32 additions can change.  The remaining steps are
+  separate float32 operations (add eps, square root, divide 1 by it once
+  per row, then two multiplies per element).  A row whose mean(x^2) + eps
+  is 0 (eps = 0 and every square 0 or rounding to 0) normalizes to 0.  The
+  normalized values are quantized as they are, never rounded to the input
+  dtype first.
 * arc_perm: calibration statistic = max over rows of |X| per channel, taken
   on X itself; channels sorted by descending statistic, ties by ascending
   channel index.
@@ -274,37 +273,69 @@ def quant_fp8_tensor(x):
     return e4m3_encode(x / s), s
 
 
-RMS_PARTIALS = 256   # partial sums of the mean of squares (the fixed reduction order)
-RMS_CHUNK = 8        # consecutive elements per chunk
+def _f32_fields(x):
+    """(m, p) per float32 element, with x = m . 2^(p/2 - 149) exactly: m the
+    integer significand (implicit bit included), p = 2 max(E, 1) - 2 for the
+    exponent field E, so that x^2 = m^2 . 2^(p - 298)."""
+    bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.int64)
+    e = (bits >> 23) & 0xFF
+    man = bits & 0x7FFFFF
+    m = np.where(e > 0, man | 0x800000, man)
+    return m, 2 * np.maximum(e, 1) - 2
+
+
+def _round_to_f32(n):
+    """The float32 nearest to n . 2^-298 (n a non-negative Python integer),
+    ties to even, +inf past the largest finite float32."""
+    if n == 0:
+        return np.float32(0.0)
+    lead = n.bit_length() - 1               # position of the leading bit
+    ulp = max(lead - 23, 149)               # 24 significant bits, nothing below 2^-149
+    q, r = divmod(n, 1 << ulp)
+    half = 1 << (ulp - 1)
+    if r > half or (r == half and q & 1):
+        q += 1
+    if ulp - 298 + q.bit_length() - 1 > 127:
+        return np.float32(np.inf)
+    return np.float32(float(q) * 2.0 ** (ulp - 298))   # q <= 2^24: exact in float64 and float32
+
+
+def sum_squares_f32(x):
+    """Per row: the exact sum of the squares of the float32 values, rounded
+    once to float32 (nearest, ties to even).  A NaN element gives NaN, an
+    infinite one +inf.  x: float32 [rows][K] -> float32 [rows]."""
+    x = np.asarray(x, dtype=np.float32)
+    out = np.empty(x.shape[0], dtype=np.float32)
+    for i, row in enumerate(x):
+        if np.isnan(row).any():
+            out[i] = np.float32(np.nan)
+            continue
+        if np.isinf(row).any():
+            out[i] = np.float32(np.inf)
+            continue
+        m, p = _f32_fields(row)
+        n = 0
+        for pos in np.unique(p):                        # squares sharing an exponent: one integer sum
+            sq = [int(v) * int(v) for v in m[p == pos]]
+            n += sum(sq) << int(pos)
+        out[i] = _round_to_f32(n)
+    return out
 
 
 def rmsnorm_rows(x, gamma, eps):
-    """y = (x . (1 / sqrt(mean(x^2) + eps))) . gamma per row, float32, in the fixed
-    reduction order stated above.  x: float32 [rows][K] (K a multiple of 8),
-    gamma: float32 [K] -> y float32 [rows][K]."""
+    """y = (x . (1 / sqrt(mean(x^2) + eps))) . gamma per row in float32, the mean
+    of squares being sum_squares_f32(x) / K.  x: float32 [rows][K], gamma:
+    float32 [K] -> y float32 [rows][K]."""
     x = np.asarray(x, dtype=np.float32)
     g = np.asarray(gamma, dtype=np.float32)
-    rows, k = x.shape
-    nchunk = k // RMS_CHUNK
-    per = -(-nchunk // RMS_PARTIALS)
-    sq = (x * x).astype(np.float32)
-    # chunk c of the row is element-block [8c, 8c + 8); partial p holds chunks
-    # p, p + 256, p + 512, ... in that order
-    padded = np.zeros((rows, per * RMS_PARTIALS * RMS_CHUNK), dtype=np.float32)
-    padded[:, :k] = sq
-    blocks = padded.reshape(rows, per, RMS_PARTIALS, RMS_CHUNK).transpose(0, 2, 1, 3).reshape(rows, RMS_PARTIALS, -1)
-    part = np.zeros((rows, RMS_PARTIALS), dtype=np.float32)
-    for j in range(blocks.shape[2]):          # one float32 add at a time, in order
-        part = (part + blocks[:, :, j]).astype(np.float32)
-    h = RMS_PARTIALS // 2
-    while h >= 1:
-        part[:, :h] = (part[:, :h] + part[:, h:2 * h]).astype(np.float32)
-        h //= 2
-    ms = (part[:, 0] / np.float32(k)).astype(np.float32)
-    r = np.sqrt((ms + np.float32(eps)).astype(np.float32)).astype(np.float32)
+    k = x.shape[1]
+    with np.errstate(over="ignore", invalid="ignore"):
+        ms = (sum_squares_f32(x) / np.float32(k)).astype(np.float32)
+        r = np.sqrt((ms + np.float32(eps)).astype(np.float32)).astype(np.float32)
     with np.errstate(divide="ignore"):
         inv = np.where(r == 0, np.float32(0.0), np.float32(1.0) / r).astype(np.float32)
-    return ((x * inv[:, None]).astype(np.float32) * g[None, :]).astype(np.float32)
+    with np.errstate(invalid="ignore"):
+        return ((x * inv[:, None]).astype(np.float32) * g[None, :]).astype(np.float32)
 
 
 def rmsnorm_quant_int8(x, gamma, eps):

@@ -1,16 +1,19 @@
 // Online Hadamard rotation of activation rows before 4-bit quantization.
 //
-// Every group of n consecutive elements of a row is transformed:
-//   Sylvester (QuaRot's fast Walsh-Hadamard transform, "LLM and AIGC
-//     quantization": log2(n) butterfly stages, stage h maps the pair (a, b)
-//     at distance h to (a + b, a - b)), stages h = 1, 2, 4, ..., n/2;
-//   regular (ConvRot's grouped rotation by the Kronecker power of
-//     H4 = [[1,1,1,-1],[1,1,-1,1],[1,-1,1,1],[-1,1,1,1]], n = 4^k), radix-4
-//     stages at strides 1, 4, 16, ...: each quad (x0, x1, x2, x3) becomes
-//     y_i = s - 2 x_(3-i) with s = (x0 + x1) + (x2 + x3);
-// then y = t . c with c = float32(1/sqrt(n)), times signs[k] (+-1 per column,
-// QuaRot's diag(+-1)) if given, rounded once to the output type.  Every step
-// is one float32 operation in this order, which fixes the result bit for bit.
+// The operation: every group of n consecutive elements of a row times the
+// normalized Hadamard matrix H_n / sqrt(n), then times signs[k] (+-1 per
+// column, QuaRot's diag(+-1)) if given, rounded once to the output type.
+//   Sylvester H_n ("LLM and AIGC quantization", QuaRot section): computed
+//     by the fast Walsh-Hadamard transform, log2(n) butterfly stages, stage
+//     h mapping the pair (a, b) at distance h to (a + b, a - b);
+//   regular H_n, n = 4^k (ConvRot section: the Kronecker power of
+//     H4 = [[1,1,1,-1],[1,1,-1,1],[1,-1,1,1],[-1,1,1,1]]): computed by
+//     radix-4 stages at strides 1, 4, 16, ..., each quad (x0, x1, x2, x3)
+//     becoming y_i = s - 2 x_(3-i) with s = (x0 + x1) + (x2 + x3) (H4 is the
+//     all-ones matrix minus twice the anti-diagonal).
+// The stages run in float32, then one multiply by c = float32(1/sqrt(n)) and
+// the signs; the result is within float32 rounding of the exact rotation and
+// the same on every run.
 //
 // HBM-bound (read and write the rows once; a few float32 operations per
 // element and stage), so no tensor cores: the pages' ConvRot multiplies by the
@@ -20,6 +23,10 @@
 // (Sylvester up to n = 256, the regular transform up to 256), and Sylvester
 // stages beyond 256 elements through shared memory, one CTA of n/8 threads
 // per group.
+//
+// The kernels do not trigger a programmatic dependent launch: the quantizers
+// that read the rotated rows are launched without it and read x at their
+// start.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -183,7 +190,6 @@ __global__ void __launch_bounds__(kHdThreads) hadamard_warp_kernel(const void* x
                                                                   void* y) {
   // x and y may be the same rows (in place): every element is read by the
   // thread that later writes it, before the write
-  pdl_launch_dependents();  // the quantizer that reads the rotated rows may start setting up
   constexpr int EB = DT == 2 ? 4 : 2;
   const int lane = threadIdx.x & 31;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kHdThreads;
@@ -218,7 +224,6 @@ __global__ void __launch_bounds__(1024) hadamard_cta_kernel(const void* x, int64
                                                             float c, const int8_t* __restrict__ signs,
                                                             void* y) {
   extern __shared__ __align__(16) float buf[];
-  pdl_launch_dependents();
   constexpr int EB = DT == 2 ? 4 : 2;
   const int tid = threadIdx.x, lane = tid & 31;
   for (int64_t g = blockIdx.x; g < groups; g += gridDim.x) {

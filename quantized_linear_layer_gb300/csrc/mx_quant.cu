@@ -102,6 +102,9 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const void* __rest
 
 }  // namespace
 
+// Launched without the programmatic-serialization attribute: the kernel reads
+// x at its start, with no griddepcontrol.wait before it, so it must not
+// overlap the kernel that writes x.
 cudaError_t launch_quant_mx(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, qlin_mx_fmt fmt, uint8_t* q,
                             uint8_t* sf, qlin_sf_layout sf_layout, cudaStream_t stream) {
   const int64_t nvec = rows * (K / 8);

@@ -20,6 +20,7 @@
 #include <type_traits>
 
 #include "device_common.cuh"
+#include "exact_sumsq.cuh"
 #include "qlin_internal.h"
 
 namespace qlin {
@@ -156,48 +157,34 @@ __device__ __forceinline__ void smem_chunk8(const unsigned char* p, float* v) {
 }
 
 // 1 / sqrt(mean(x^2) + eps) of each of the nr staged rows into inv[] (0 where
-// the root is 0), every thread of the CTA taking part: the float32 mean of
-// squares in the fixed order of the fused RMSNorm quantizers (thread t adds
-// the squares of the row's 8-element chunks t, t + 256, ... in order, then a
-// binary tree over the 256 partial sums, its last five steps by shuffles in
-// warp 0).  The rows' trees run side by side.
+// the root is 0), every thread of the CTA taking part: the mean of squares is
+// the exact sum of the row's squares rounded once to float32, divided by K
+// (the definition of the fused RMSNorm quantizers; exact_sum_squares_cta).
 template <int DT, int R>
 __device__ void staged_rows_inv_rms(const unsigned char* rows_smem, int row_bytes, int nr, int K, float eps,
-                                    float (*red)[kNvThreads], float* inv) {
+                                    ExactSqScratch<kNvThreads / 32>& sq, float* inv) {
   constexpr int EB = elem_bytes<DT>();
   const int tid = threadIdx.x;
 #pragma unroll
   for (int rr = 0; rr < R; ++rr) {
-    float part = 0.0f;
-    if (rr < nr) {
-      const unsigned char* rs = rows_smem + rr * row_bytes;
+    if (rr >= nr) break;  // uniform over the CTA
+    const unsigned char* rs = rows_smem + rr * row_bytes;
+    auto for_each = [&](auto f) {
       for (int c = tid; c * 8 < K; c += kNvThreads) {
         float v[8];
         smem_chunk8<DT>(rs + c * 8 * EB, v);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) part = __fadd_rn(part, __fmul_rn(v[i], v[i]));
+        for (int i = 0; i < 8; ++i) f(v[i]);
       }
-    }
-    red[rr][tid] = part;
-  }
-  __syncthreads();
-  for (int h = kNvThreads / 2; h >= 32; h >>= 1) {
-    if (tid < h) {
-#pragma unroll
-      for (int rr = 0; rr < R; ++rr) red[rr][tid] = __fadd_rn(red[rr][tid], red[rr][tid + h]);
-    }
-    __syncthreads();
-  }
-  if (tid < 32) {
-#pragma unroll
-    for (int rr = 0; rr < R; ++rr) {
-      float p = red[rr][tid];
-#pragma unroll
-      for (int h = 16; h >= 1; h >>= 1) p = __fadd_rn(p, __shfl_down_sync(0xffffffffu, p, h));
-      if (tid == 0) {
-        const float r = __fsqrt_rn(__fadd_rn(__fdiv_rn(p, static_cast<float>(K)), eps));
-        inv[rr] = r == 0.0f ? 0.0f : __fdiv_rn(1.0f, r);
-      }
+    };
+    float sumsq;
+    if constexpr (DT == 0)
+      sumsq = exact_sum_squares_f16_cta<kNvThreads / 32>(for_each, sq);
+    else
+      sumsq = exact_sum_squares_cta<kNvThreads / 32, DT == 1 ? 32 : 0>(for_each, sq);
+    if (tid == 0) {
+      const float r = __fsqrt_rn(__fadd_rn(__fdiv_rn(sumsq, static_cast<float>(K)), eps));
+      inv[rr] = r == 0.0f ? 0.0f : __fdiv_rn(1.0f, r);
     }
   }
   __syncthreads();
@@ -217,7 +204,6 @@ __global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __r
                                                                   const void* __restrict__ gamma, float eps,
                                                                   int32_t* __restrict__ err) {
   extern __shared__ __align__(16) unsigned char row_smem[];
-  static_assert(kNvThreads == 256, "the fused RMSNorm's reduction order is defined over 256 partial sums");
   pdl_launch_dependents();  // the GEMM that reads the codes may start setting up
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * R;
   const int nr = static_cast<int>(min(static_cast<int64_t>(R), rows - row0));
@@ -236,9 +222,11 @@ __global__ void __launch_bounds__(kNvThreads) nvfp4_quant_kernel(const void* __r
   }
   __syncthreads();
   // fused RMSNorm: each staged row's 1 / rms
-  __shared__ float red[NORM ? R : 1][kNvThreads];
   __shared__ float inv_rms[R];
-  if constexpr (NORM) staged_rows_inv_rms<DT, R>(row_smem, row_bytes, nr, K, eps, red, inv_rms);
+  if constexpr (NORM) {
+    __shared__ ExactSqScratch<kNvThreads / 32> sq;
+    staged_rows_inv_rms<DT, R>(row_smem, row_bytes, nr, K, eps, sq, inv_rms);
+  }
 
   const GlobalScale gs = make_global_scale(__ldg(gp));
   const int Kaug = K + S;
@@ -413,6 +401,9 @@ cudaError_t dispatch_dtype(qlin_dtype dt, F&& f) {
 
 }  // namespace
 
+// Launched without the programmatic-serialization attribute: the kernel reads
+// x at its start, with no griddepcontrol.wait before it, so it must not
+// overlap the kernel that writes x.
 cudaError_t launch_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const int32_t* perm,
                                int64_t S, qlin_nvfp4_mode mode, const float* g, uint8_t* q, uint8_t* sf,
                                qlin_sf_layout sf_layout, const void* gamma, float eps, cudaStream_t stream) {

@@ -23,6 +23,7 @@
 // division (__fdiv_rn), round-half-to-even (__float2int_rn), and no fused
 // multiply-add anywhere a result feeds a rounding decision.
 #include "device_common.cuh"
+#include "exact_sumsq.cuh"
 #include "qlin_internal.h"
 
 namespace qlin {
@@ -226,19 +227,14 @@ __global__ void __launch_bounds__(kQuantThreads) quant_fp8_rows_kernel(const voi
 // (x . inv) . gamma with inv = 1 / sqrt(mean(x^2) + eps) (one correctly
 // rounded square root and division per row); a row whose mean(x^2) + eps is
 // 0 normalizes to 0.
-// The mean of squares is a float32 sum in a fixed order, part of the
-// operation's definition so that its result is reproducible: thread t owns
-// the 8-element chunks t, t + 256, ... and adds their squares in that order,
-// element by element (separate multiply and add, never contracted), and the
-// 256 partial sums meet in a binary tree (partial i += partial i + h, h =
-// 128 ... 1; the steps below 32 are the same additions done with shuffles
-// inside warp 0).
+// The mean of squares is the exact sum of the row's squares rounded once to
+// float32 (exact_sum_squares_cta), divided by K in float32: the result does
+// not depend on the number of threads or on the order of the additions.
 template <int DT, int FMT>
 __global__ void __launch_bounds__(kQuantThreads) rmsnorm_quant_kernel(const void* __restrict__ x,
                                                                      const void* __restrict__ gamma, int K,
                                                                      float eps, void* __restrict__ q,
                                                                      float* __restrict__ scale) {
-  static_assert(kQuantThreads == 256, "the reduction order is defined over 256 partial sums");
   pdl_launch_dependents();  // the GEMM that reads the codes may start setting up
   const int64_t row = blockIdx.x;
   const int tid = threadIdx.x;
@@ -248,43 +244,40 @@ __global__ void __launch_bounds__(kQuantThreads) rmsnorm_quant_kernel(const void
   const char* gr = static_cast<const char*>(gamma);
 
   float v[kMaxVecPerThread][8];
-  float part = 0.0f;
-  auto add_squares = [&](const float* t) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) part = __fadd_rn(part, __fmul_rn(t[j], t[j]));
-  };
 #pragma unroll
   for (int i = 0; i < kMaxVecPerThread; ++i) {
     const int c = tid + i * kQuantThreads;
-    if (c < nvec) {
-      Vec8Loader<DT>::load(xr + (int64_t)c * 8 * EB, v[i]);
-      add_squares(v[i]);
-    }
+    if (c < nvec) Vec8Loader<DT>::load(xr + (int64_t)c * 8 * EB, v[i]);
   }
-  for (int c = tid + kMaxVecPerThread * kQuantThreads; c < nvec; c += kQuantThreads) {
-    float t[8];
-    Vec8Loader<DT>::load(xr + (int64_t)c * 8 * EB, t);
-    add_squares(t);
-  }
-  __shared__ float red[kQuantThreads];
-  __shared__ float s_scale, s_inv;
-  red[tid] = part;
-  __syncthreads();
-  for (int h = kQuantThreads / 2; h >= 32; h >>= 1) {
-    if (tid < h) red[tid] = __fadd_rn(red[tid], red[tid + h]);
-    __syncthreads();
-  }
-  if (tid < 32) {
-    float p = red[tid];
+  // every element of this thread's share: the chunks held in registers, then
+  // (rows longer than the registers hold) the rest read again
+  auto for_each = [&](auto f) {
 #pragma unroll
-    for (int h = 16; h >= 1; h >>= 1) p = __fadd_rn(p, __shfl_down_sync(0xffffffffu, p, h));
-    if (tid == 0) {
-      const float ms = __fdiv_rn(p, static_cast<float>(K));
-      const float r = __fsqrt_rn(__fadd_rn(ms, eps));
-      s_inv = r == 0.0f ? 0.0f : __fdiv_rn(1.0f, r);
+    for (int i = 0; i < kMaxVecPerThread; ++i) {
+      const int c = tid + i * kQuantThreads;
+      if (c < nvec) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f(v[i][j]);
+      }
     }
-  }
-  __syncthreads();
+    for (int c = tid + kMaxVecPerThread * kQuantThreads; c < nvec; c += kQuantThreads) {
+      float t[8];
+      Vec8Loader<DT>::load(xr + (int64_t)c * 8 * EB, t);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f(t[j]);
+    }
+  };
+  __shared__ ExactSqScratch<kQuantThreads / 32> sq;
+  __shared__ float red[kQuantThreads / 32];
+  __shared__ float s_scale;
+  float sumsq;
+  if constexpr (DT == 0)
+    sumsq = exact_sum_squares_f16_cta<kQuantThreads / 32>(for_each, sq);
+  else
+    sumsq = exact_sum_squares_cta<kQuantThreads / 32, DT == 1 ? 32 : 0>(for_each, sq);
+  const float ms = __fdiv_rn(sumsq, static_cast<float>(K));
+  const float r = __fsqrt_rn(__fadd_rn(ms, eps));
+  const float s_inv = r == 0.0f ? 0.0f : __fdiv_rn(1.0f, r);
   const float inv = s_inv;
   // y = (x . inv) . gamma
   auto normalize = [&](float* t, int c) {
@@ -312,7 +305,6 @@ __global__ void __launch_bounds__(kQuantThreads) rmsnorm_quant_kernel(const void
   }
   // max is exact, so this reduction's order does not matter
   m = warp_max(m);
-  __syncthreads();  // every thread is done with the tree's red[]
   if ((tid & 31) == 0) red[tid >> 5] = m;
   __syncthreads();
   if (tid == 0) {
@@ -431,6 +423,9 @@ __global__ void quant_w4_g128_kernel(const void* __restrict__ w, int64_t N, int 
 
 }  // namespace
 
+// Launched without the programmatic-serialization attribute: the kernel reads
+// x at its start, with no griddepcontrol.wait before it, so it must not
+// overlap the kernel that writes x.
 cudaError_t launch_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
                                   float* scale, int32_t* azp, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
@@ -454,6 +449,9 @@ cudaError_t launch_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, 
   return cudaGetLastError();
 }
 
+// Launched without the programmatic-serialization attribute: the kernel reads
+// x at its start, with no griddepcontrol.wait before it, so it must not
+// overlap the kernel that writes x.
 cudaError_t launch_quant_fp8(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, uint8_t* q, float* scale,
                              cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
@@ -467,6 +465,9 @@ cudaError_t launch_quant_fp8(const void* x, qlin_dtype x_dtype, int64_t rows, in
   return cudaGetLastError();
 }
 
+// Launched without the programmatic-serialization attribute: the kernel reads
+// x at its start, with no griddepcontrol.wait before it, so it must not
+// overlap the kernel that writes x.
 cudaError_t launch_rmsnorm_quant(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, const void* gamma,
                                  float eps, qlin_qfmt fmt, void* q, float* scale, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;

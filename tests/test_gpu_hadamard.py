@@ -1,13 +1,17 @@
-"""Online Hadamard rotation on the GPU against the CPU oracle, bit for bit:
-the Sylvester fast Walsh-Hadamard transform (groups of 2 .. 4096, warp-level
-and through shared memory) and the regular Hadamard of order 4^k, with and
-without column signs, fp16 / bf16 / fp32 rows, in place."""
+"""Online Hadamard rotation on the GPU against the CPU oracle's float64
+definition, every n-group of a row times H_n / sqrt(n) and then the column
+signs: the Sylvester transform (groups of 2 .. 8192, warp-level and through
+shared memory) and the regular Hadamard of order 4^k, fp16 / bf16 / fp32
+rows, in place and out of place.  Outputs are compared within the fp
+tolerance (max |err| <= 1e-2 (1 + |ref|), relative Frobenius <= 2e-3)
+against the exact rotation of the same input values."""
 
 import numpy as np
 import pytest
 import torch
 
 import oracle
+from conftest import assert_within_tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -17,6 +21,7 @@ def _rows(seed, rows, k):
     x = (rng.standard_normal((rows, k)) * np.exp(rng.uniform(-3, 3, size=(rows, 1)))).astype(np.float32)
     x[1] = 0.0
     x[2, ::7] *= 100.0           # outlier channels, the case the rotation is for
+    x[3] = 2.5                   # a constant row (a row outlier)
     return x
 
 
@@ -24,9 +29,8 @@ def _signs(seed, k):
     return np.where(np.random.default_rng(seed).random(k) < 0.5, -1, 1).astype(np.int8)
 
 
-def _expected(x32, n, kind, signs, dtype):
-    y = oracle.hadamard_rotate(x32, n, kind, None if signs is None else signs.astype(np.float32))
-    return torch.from_numpy(y).to(dtype)   # one round-to-nearest-even to the output type
+def _code(q, kind):
+    return q.QLIN_HADAMARD_SYLVESTER if kind == "sylvester" else q.QLIN_HADAMARD_REGULAR
 
 
 CASES = [("sylvester", 2, 64), ("sylvester", 8, 1024), ("sylvester", 64, 4160), ("sylvester", 256, 4096),
@@ -36,37 +40,50 @@ CASES = [("sylvester", 2, 64), ("sylvester", 8, 1024), ("sylvester", 64, 4160), 
 
 @pytest.mark.parametrize("kind,n,k", CASES)
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
-def test_hadamard_bit_exact(qlin_gpu, kind, n, k, dtype):
+def test_hadamard_within_tolerance(qlin_gpu, kind, n, k, dtype):
     rows = 37
-    x = _rows(n + k, rows, k)
-    xt = torch.from_numpy(x).to(dtype).cuda()
+    xt = torch.from_numpy(_rows(n + k, rows, k)).to(dtype).cuda()
     signs = _signs(k, k) if n % 2 == 0 and (n // 2) % 2 == 0 else None
-    code = qlin_gpu.QLIN_HADAMARD_SYLVESTER if kind == "sylvester" else qlin_gpu.QLIN_HADAMARD_REGULAR
-    y = qlin_gpu.qlin_hadamard(xt, n, kind=code, signs=None if signs is None else torch.from_numpy(signs).cuda())
+    y = qlin_gpu.qlin_hadamard(xt, n, kind=_code(qlin_gpu, kind),
+                               signs=None if signs is None else torch.from_numpy(signs).cuda())
     torch.cuda.synchronize()
-    want = _expected(xt.float().cpu().numpy(), n, kind, signs, dtype)
-    got = y.cpu()
-    same = (got.view(torch.int16 if dtype != torch.float32 else torch.int32) ==
-            want.view(torch.int16 if dtype != torch.float32 else torch.int32))
-    bad = torch.nonzero(~same)
-    assert bad.numel() == 0, "first mismatches (row, col): %s" % bad[:5].tolist()
+    assert qlin_gpu.qlin_get_device_error() == 0
+    ref = oracle.hadamard_rotate(xt.double().cpu().numpy(), n, kind, signs)
+    assert_within_tolerance(y.double().cpu().numpy(), ref, "%s n=%d %s" % (kind, n, dtype))
 
 
 def test_hadamard_in_place(qlin_gpu):
-    x = _rows(3, 16, 2048)
-    xt = torch.from_numpy(x).half().cuda()
-    want = _expected(xt.float().cpu().numpy(), 1024, "sylvester", None, torch.float16)
-    qlin_gpu.qlin_hadamard(xt, 1024, y=xt)
+    """Rotating a buffer onto itself gives what the out-of-place call gives."""
+    x = torch.from_numpy(_rows(3, 16, 2048)).half().cuda()
+    ref = oracle.hadamard_rotate(x.double().cpu().numpy(), 1024, "sylvester")
+    out = qlin_gpu.qlin_hadamard(x, 1024)
     torch.cuda.synchronize()
-    assert torch.equal(xt.cpu().view(torch.int16), want.view(torch.int16))
+    qlin_gpu.qlin_hadamard(x, 1024, y=x)
+    torch.cuda.synchronize()
+    assert torch.equal(x.cpu().view(torch.int16), out.cpu().view(torch.int16))
+    assert_within_tolerance(x.double().cpu().numpy(), ref, "in place")
 
 
-@pytest.mark.parametrize("kind,n,rows,k", [("sylvester", 8, 1, 8), ("regular", 4, 3, 8), ("sylvester", 8192, 2, 8192)])
+@pytest.mark.parametrize("kind,n,rows,k", [("sylvester", 8, 1, 8), ("regular", 4, 3, 8), ("sylvester", 8192, 2, 8192),
+                                           ("regular", 256, 1, 256)])
 def test_hadamard_small_and_largest(qlin_gpu, kind, n, rows, k):
-    x = np.random.default_rng(n + k).standard_normal((rows, k)).astype(np.float32)
-    xt = torch.from_numpy(x).cuda()
-    code = qlin_gpu.QLIN_HADAMARD_SYLVESTER if kind == "sylvester" else qlin_gpu.QLIN_HADAMARD_REGULAR
-    y = qlin_gpu.qlin_hadamard(xt, n, kind=code)
+    x = torch.from_numpy(np.random.default_rng(n + k).standard_normal((rows, k)).astype(np.float32)).cuda()
+    y = qlin_gpu.qlin_hadamard(x, n, kind=_code(qlin_gpu, kind))
     torch.cuda.synchronize()
-    want = oracle.hadamard_rotate(x, n, kind)
-    assert np.array_equal(y.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    ref = oracle.hadamard_rotate(x.double().cpu().numpy(), n, kind)
+    # float32 rows: the float32 butterflies stay within (log2 n + 2) roundings
+    # of 2^-24 times sqrt(n) max|x| of the exact rotation
+    bound = (np.log2(n) + 2) * 2.0 ** -24 * np.sqrt(n) * np.abs(x.cpu().numpy()).max()
+    assert np.max(np.abs(y.double().cpu().numpy() - ref)) <= bound
+    assert_within_tolerance(y.double().cpu().numpy(), ref, "%s n=%d" % (kind, n))
+
+
+def test_hadamard_page_example_on_gpu(qlin_gpu):
+    """The page's 8-element token rotated by H_8 / sqrt(8) (QuaRot section),
+    in float32, to the printed three decimals."""
+    from conftest import load_golden
+    ex = load_golden("hadamard_examples.json")["sylvester_h8"]
+    x = torch.tensor([ex["x"]], dtype=torch.float32).cuda()
+    y = qlin_gpu.qlin_hadamard(x, 8)
+    torch.cuda.synchronize()
+    assert np.all(np.abs(y.cpu().numpy()[0] - np.array(ex["xH_printed"])) <= 1e-3)

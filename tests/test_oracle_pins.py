@@ -164,6 +164,35 @@ def test_int8_asym_properties():
     assert np.all(np.abs(deq - x) <= s[:, None].astype(np.float64) * (0.5 + 2e-5))
 
 
+def pin_zero_point_added_after_rounding():
+    """Chapter 9, section 9.2 writes x_int = round(x / s) + z: the integer
+    zero-point is added after rounding (AWQ's pseudo_quant on the LLM
+    quantization page does the same: (w / s).round().add(z)).  The order
+    matters on a tie with an odd zero-point.
+
+    int8, per token: the row range [-17/16, 14.875] gives s = (255/16) / 255
+    = 1/16 exactly and z = -128 - round(-17) = -111; x = 5/32 is x / s = 2.5,
+    so round(2.5) + z = 2 - 111 = -109 (rounding 2.5 - 111 instead gives
+    -108).  The range ends map to -128 and 127, and 0 to z.
+
+    4-bit weights, per group of 128: the range [-5/16, 10/16] gives s = 1/16
+    (exact in fp16) and z = round(5) = 5; w = 5/32 is w / s = 2.5, so the code
+    is 2 + 5 = 7 (not round(7.5) = 8)."""
+    x = np.array([[-17 / 16, 14.875, 5 / 32, 0.0]], dtype=np.float32)
+    q, sc, z = oracle.quant_int8_asym(x)
+    assert sc[0] == np.float32(1 / 16) and z[0] == -111
+    assert q.tolist() == [[-128, 127, -109, -111]]
+    w = np.zeros((1, 128), dtype=np.float32)
+    w[0, :3] = [-5 / 16, 10 / 16, 5 / 32]
+    codes, s16, zw = oracle.quant_w4_g128(w)
+    assert s16[0, 0] == np.float16(1 / 16) and zw[0, 0] == 5
+    assert codes[0, :4].tolist() == [0, 15, 7, 5]
+
+
+def test_zero_point_added_after_rounding():
+    pin_zero_point_added_after_rounding()
+
+
 def test_w4_g128_properties():
     rng = np.random.default_rng(13)
     w = (rng.standard_normal((8, 512)) * 0.02).astype(np.float32)
@@ -631,8 +660,8 @@ def pin_rmsnorm_formula():
         y = oracle.rmsnorm_rows(x, g, eps)
         x64 = x.astype(np.float64)
         ref = x64 / np.sqrt((x64 ** 2).mean(axis=1, keepdims=True) + eps) * g.astype(np.float64)
-        # a handful of float32 roundings plus the float32 sum of squares
-        tol = 8 * 2.0 ** -24 + k * 2.0 ** -24
+        # a handful of float32 roundings (the sum of squares is rounded once)
+        tol = 8 * 2.0 ** -24
         assert np.all(np.abs(y - ref) <= tol * np.abs(ref) + 1e-30), k
 
 
@@ -669,17 +698,54 @@ def test_rmsnorm_constant_row():
     assert np.all(oracle.e4m3_decode(c[0]) == 448.0) and np.all(oracle.e4m3_decode(c[1]) == 0.0)
 
 
-def test_rmsnorm_sum_order_bound():
-    """The fixed-order float32 mean of squares stays within K . 2^-24 of the
-    exact mean (a bound any summation order meets)."""
+def pin_sum_squares_exact():
+    """The mean of squares starts from the exact sum of squares rounded once to
+    float32 (nearest, ties to even).  Values worked out by hand:
+    [1, 2^-12] sums to 1 + 2^-24, halfway between 1 and 1 + 2^-23, and rounds
+    to the even 1; adding 2^-40 puts it above halfway, so it rounds up to
+    1 + 2^-23 (a float32 sum from the left gives 1 in both cases); 3^2 + 4^2
+    = 25; (2^-75)^2 = 2^-150 is half the smallest subnormal and rounds to 0,
+    (1.5 . 2^-75)^2 = 1.125 . 2^-149 rounds to 2^-149; 2^64 squared is 2^128,
+    past the float32 range: +inf; 2^63 twice gives 2^127."""
+    rows = [([1.0, 2.0 ** -12], 1.0),
+            ([1.0, 2.0 ** -12, 2.0 ** -40], 1.0 + 2.0 ** -23),
+            ([3.0, 4.0], 25.0),
+            ([2.0 ** -75], 0.0),
+            ([1.5 * 2.0 ** -75], 2.0 ** -149),
+            ([2.0 ** 64], np.inf),
+            ([2.0 ** 63, 2.0 ** 63], 2.0 ** 127),
+            ([0.0, -0.0], 0.0)]
+    for vals, want in rows:
+        x = np.zeros((1, 8), dtype=np.float32)
+        x[0, :len(vals)] = vals
+        got = oracle.sum_squares_f32(x)[0]
+        assert got == np.float32(want), (vals, got, want)
+        # the order of the elements does not matter
+        assert oracle.sum_squares_f32(x[:, ::-1])[0] == got
+    assert np.isnan(oracle.sum_squares_f32(np.array([[1.0, np.nan]], dtype=np.float32))[0])
+    assert oracle.sum_squares_f32(np.array([[1.0, -np.inf]], dtype=np.float32))[0] == np.inf
+
+
+def test_sum_squares_exact():
+    pin_sum_squares_exact()
+
+
+def test_sum_squares_against_fsum():
+    """math.fsum returns the exact sum correctly rounded to float64 (Shewchuk's
+    method); rounding that to float32 gives the same float32 unless the exact
+    sum sits within 2^-53 of a float32 midpoint, which these rows do not.
+    Any order of the rows' elements gives the same bits."""
+    import math
     rng = np.random.default_rng(15)
-    x = rng.standard_normal((8, 8192)).astype(np.float32)
-    g = np.ones(8192, dtype=np.float32)
-    y = oracle.rmsnorm_rows(x, g, 0.0)
-    x64 = x.astype(np.float64)
-    r_exact = np.sqrt((x64 ** 2).mean(axis=1))
-    r_implied = np.median(x64 / y.astype(np.float64), axis=1)
-    assert np.all(np.abs(r_implied - r_exact) <= 8192 * 2.0 ** -24 * r_exact)
+    x = (rng.standard_normal((24, 4160)) * np.exp(rng.uniform(-8, 8, size=(24, 1)))).astype(np.float16)
+    x = x.astype(np.float32)
+    x[3, :7] = 3000.0
+    got = oracle.sum_squares_f32(x)
+    for i in range(x.shape[0]):
+        assert got[i] == np.float32(math.fsum(float(v) * float(v) for v in x[i])), i
+    perm = rng.permutation(x.shape[1])
+    assert np.array_equal(oracle.sum_squares_f32(x[:, perm]), got)
+
 
 def pin_rmsnorm_arc_unit_rms():
     """Rows of +-1 with eps = 0 have mean of squares exactly 1, so the RMSNorm
@@ -752,25 +818,61 @@ def test_act_order_perm_rejects_uneven_groups():
 
 # ---- online Hadamard rotation ----
 
-def _sylvester_by_recursion(n):
+def _sylvester_by_formula(n):
     """H_n written out from its element formula: (-1)^popcount(i & j)."""
     i = np.arange(n)
     return np.array([[(-1.0) ** bin(a & b).count("1") for b in i] for a in i])
 
 
+def _regular_by_formula(n):
+    """The Kronecker power of H4 element by element: the product over the
+    base-4 digits (i_d, j_d) of the indices of H4[i_d][j_d]."""
+    h4 = [[1, 1, 1, -1], [1, 1, -1, 1], [1, -1, 1, 1], [-1, 1, 1, 1]]
+    out = np.ones((n, n))
+    for a in range(n):
+        for b in range(n):
+            v, i, j = 1, a, b
+            while i or j:            # leading digit pairs (0, 0) contribute H4[0][0] = 1
+                v *= h4[i % 4][j % 4]
+                i //= 4
+                j //= 4
+            out[a, b] = v
+    return out
+
+
+def pin_hadamard_page_examples():
+    g = load_golden("hadamard_examples.json")
+    ex = g["sylvester_h8"]
+    xh = oracle.hadamard_rotate(np.array([ex["x"]]), 8, "sylvester")[0]
+    wh = oracle.hadamard_rotate(np.array([ex["w"]]), 8, "sylvester")[0]
+    assert np.all(np.abs(xh - ex["xH_printed"]) <= 1e-3)
+    assert np.all(np.abs(wh - ex["wH_printed"]) <= 1e-3)
+    # orthogonal: the dot product is unchanged
+    assert abs(float(xh @ wh) - ex["dot_printed"]) <= 5e-4
+    assert abs(float(np.dot(ex["x"], ex["w"])) - ex["dot_printed"]) <= 5e-4
+    r = g["regular_h4"]
+    y = oracle.hadamard_rotate(np.array([r["x"]]), 4, "regular")[0]
+    assert abs(y[0] - r["y0_printed"]) <= 1e-12
+    assert abs(y[0] - float(np.dot(r["x"], r["first_column"])) / 2.0) <= 1e-12
+
+
+def test_hadamard_page_examples():
+    pin_hadamard_page_examples()
+
+
 def pin_hadamard_dense():
+    """Every group times the matrix built from its element formula, over sqrt(n),
+    to float64 rounding; the signs multiply the rotated columns."""
     rng = np.random.default_rng(41)
-    for kind, sizes in (("sylvester", (2, 8, 64, 256, 1024)), ("regular", (4, 16, 64, 256))):
+    for kind, sizes in (("sylvester", (2, 8, 64, 256)), ("regular", (4, 16, 64))):
         for n in sizes:
-            x = rng.standard_normal((3, 2 * n)).astype(np.float32)
+            x = rng.standard_normal((3, 2 * n))
+            h = _sylvester_by_formula(n) if kind == "sylvester" else _regular_by_formula(n)
+            ref = (x.reshape(-1, n) @ h / np.sqrt(n)).reshape(x.shape)
             y = oracle.hadamard_rotate(x, n, kind)
-            if kind == "sylvester":
-                h = _sylvester_by_recursion(n) if n <= 64 else oracle.sylvester_matrix(n)
-            else:
-                h = oracle.regular_matrix(n)
-            ref = (x.astype(np.float64).reshape(-1, n) @ h / np.sqrt(n)).reshape(x.shape)
-            bound = (np.log2(n) + 2) * 2.0 ** -24 * np.sqrt(n) * np.abs(x).max()
-            assert np.max(np.abs(y - ref)) <= bound, (kind, n)
+            assert np.max(np.abs(y - ref)) <= 1e-12 * np.sqrt(n) * np.abs(x).max(), (kind, n)
+            signs = np.where(rng.random(2 * n) < 0.5, -1.0, 1.0)
+            assert np.array_equal(oracle.hadamard_rotate(x, n, kind, signs), y * signs)
 
 
 def test_hadamard_dense():
@@ -778,27 +880,41 @@ def test_hadamard_dense():
 
 
 def test_hadamard_matrices():
-    """The Sylvester matrix equals the element formula; both matrices are
-    orthogonal up to n; the regular one has all column sums +-sqrt(n), so a row
-    of ones rotates to exactly +-1 (every intermediate is an integer)."""
-    assert np.array_equal(oracle.sylvester_matrix(32), _sylvester_by_recursion(32))
+    """The doubling equals the element formula; both matrices are symmetric and
+    orthogonal; the regular one has every column sum +-sqrt(n), so a row of
+    ones rotates to +-1 ("every channel is +-c")."""
+    assert np.array_equal(oracle.sylvester_matrix(32), _sylvester_by_formula(32))
+    assert np.array_equal(oracle.regular_matrix(64), _regular_by_formula(64))
     for n in (4, 16, 64, 256):
         h = oracle.regular_matrix(n)
         assert np.array_equal(h @ h.T, n * np.eye(n)) and np.array_equal(h, h.T)
         assert np.array_equal(np.abs(h.sum(axis=0)), np.full(n, np.sqrt(n)))
-        y = oracle.hadamard_rotate(np.ones((1, n), dtype=np.float32), n, "regular")
-        assert np.array_equal(np.abs(y), np.ones((1, n), dtype=np.float32))
+        y = oracle.hadamard_rotate(np.ones((1, n)), n, "regular")
+        assert np.allclose(np.abs(y), 1.0, rtol=0, atol=1e-12)
+    h = oracle.sylvester_matrix(256)
+    assert np.array_equal(h @ h.T, 256 * np.eye(256))
+    # Sylvester: the first column sums to n, the others to 0 (a constant row
+    # lands entirely in the first channel)
+    y = oracle.hadamard_rotate(np.full((1, 16), 3.0), 16, "sylvester")[0]
+    assert abs(y[0] - 12.0) <= 1e-12 and np.all(np.abs(y[1:]) <= 1e-12)
 
 
-def test_hadamard_involution_and_signs():
+def test_hadamard_involution_and_doubling():
     rng = np.random.default_rng(42)
-    x = rng.standard_normal((4, 512)).astype(np.float32)
-    for kind, n in (("sylvester", 512), ("sylvester", 128), ("regular", 256)):
+    x = rng.standard_normal((4, 8192))
+    for kind, n in (("sylvester", 8192), ("sylvester", 128), ("regular", 256)):
         y = oracle.hadamard_rotate(oracle.hadamard_rotate(x, n, kind), n, kind)
-        assert np.max(np.abs(y - x)) <= 2 * (np.log2(n) + 2) * 2.0 ** -24 * np.sqrt(n) * np.abs(x).max()
-    signs = np.where(rng.random(512) < 0.5, -1.0, 1.0).astype(np.float32)
-    assert np.array_equal(oracle.hadamard_rotate(x, 256, "regular", signs),
-                          oracle.hadamard_rotate(x, 256, "regular") * signs)
+        assert np.max(np.abs(y - x)) <= 1e-11 * np.abs(x).max()
+
+
+def test_hadamard_doubling_step_equals_dense(monkeypatch):
+    """The one doubling step used above 4096 x 4096, checked at a small order
+    by lowering the dense limit: the result equals the dense product."""
+    rng = np.random.default_rng(43)
+    x = rng.standard_normal((3, 128))
+    dense = oracle.hadamard_rotate(x, 64, "sylvester")
+    monkeypatch.setattr(oquant_had, "_DENSE_MAX", 8)
+    assert np.allclose(oracle.hadamard_rotate(x, 64, "sylvester"), dense, rtol=0, atol=1e-12)
 
 
 # ---- MX block-scaled formats (MXFP8, MXFP4) ----
@@ -1014,14 +1130,56 @@ def _mut_act_order_ignores_g_idx(monkeypatch):
     return pin_act_order
 
 
-def _mut_hadamard_stage_sign(monkeypatch):
-    orig = oquant_had.fwht_rows
+def _mut_hadamard_outputs_swapped(monkeypatch):
+    orig = oquant_had._rotate_groups
 
-    def bad(x, n):
-        y = orig(x, n)
+    def bad(g, n, kind):
+        y = orig(g, n, kind)
         return np.concatenate([y[:, 1:2], y[:, :1], y[:, 2:]], axis=1)   # two outputs swapped
-    monkeypatch.setattr(oquant_had, "fwht_rows", bad)
+    monkeypatch.setattr(oquant_had, "_rotate_groups", bad)
     return pin_hadamard_dense
+
+
+def _mut_asym_add_then_round(monkeypatch):
+    def bad(x):
+        x = np.asarray(x, dtype=np.float32)
+        mn = np.minimum(x.min(axis=1), F32(0.0))
+        mx = np.maximum(x.max(axis=1), F32(0.0))
+        s = (np.maximum(mx - mn, F32(1e-5)) / F32(255.0)).astype(np.float32)
+        z = (-128 - np.rint(mn / s).astype(np.int64)).astype(np.int32)
+        q = np.clip(np.rint((x / s[:, None]).astype(np.float64) + z[:, None]), -128, 127).astype(np.int8)
+        return q, s, z
+
+    monkeypatch.setattr(oracle, "quant_int8_asym", bad)
+    return pin_zero_point_added_after_rounding
+
+
+def _mut_w4_add_then_round(monkeypatch):
+    def bad(w, group=128):
+        w = np.asarray(w, dtype=np.float32)
+        n, k = w.shape
+        g = w.reshape(n, k // group, group)
+        s16 = (np.maximum(g.max(axis=2) - g.min(axis=2), F32(1e-5)) / F32(15.0)).astype(np.float16)
+        s = s16.astype(np.float32)
+        z = np.clip(np.rint(-g.min(axis=2) / s), 0, 15)
+        q = np.clip(np.rint((g / s[:, :, None]).astype(np.float64) + z[:, :, None]), 0, 15)
+        return q.reshape(n, k).astype(np.uint8), s16, z.astype(np.uint8)
+
+    monkeypatch.setattr(oracle, "quant_w4_g128", bad)
+    return pin_zero_point_added_after_rounding
+
+
+def _mut_sum_squares_float32_left_to_right(monkeypatch):
+    def bad(x):
+        x = np.asarray(x, dtype=np.float32)
+        out = np.zeros(x.shape[0], dtype=np.float32)
+        for j in range(x.shape[1]):
+            with np.errstate(over="ignore", invalid="ignore"):
+                out = (out + (x[:, j] * x[:, j]).astype(np.float32)).astype(np.float32)
+        return out
+
+    monkeypatch.setattr(oracle, "sum_squares_f32", bad)
+    return pin_sum_squares_exact
 
 
 def _mut_mx_emax_e4m3_7(monkeypatch):
@@ -1040,7 +1198,8 @@ MUTATIONS = [_mut_e2m1_ties_odd, _mut_azp_sign, _mut_azp_adj_axis, _mut_residual
              _mut_w8a8_transposed, _mut_w4_zero_dropped, _mut_nvfp4_scale_not_decoded, _mut_sym_qmax,
              _mut_fp8_scale_447, _mut_fp8_scales_swapped, _mut_rmsnorm_mean_k_minus_1,
              _mut_rmsnorm_arc_gamma_reordered, _mut_mx_emax_e4m3_7, _mut_mx_scales_swapped,
-             _mut_act_order_ignores_g_idx, _mut_hadamard_stage_sign]
+             _mut_act_order_ignores_g_idx, _mut_hadamard_outputs_swapped,
+             _mut_asym_add_then_round, _mut_w4_add_then_round, _mut_sum_squares_float32_left_to_right]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
