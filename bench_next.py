@@ -3,7 +3,7 @@ quantizers, the W4A16 prefill GEMM and act-order, the Hadamard rotation) on
 seeded synthetic inputs and prints one JSON line per operation with its rate
 against the roofline that bounds it:
 
-    python -m quantized_linear_layer_gb300.bench_next [--only NAME ...]
+    python bench_next.py [--only NAME ...]
 
 Each operation is captured in a CUDA graph of 10 launches over rotating
 inputs (weights rotate over three copies, so weight streams come from HBM),
@@ -19,7 +19,7 @@ import json
 import os
 import sys
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 
 
 def _peaks():
@@ -109,11 +109,11 @@ def _rows(q, torch):
     rows.append(("mxfp8", "MXFP8 quantize + block-scaled GEMM, T=2048 N=K=4096, bf16 out", mx(q.QLIN_MX_FP8_E4M3)))
     rows.append(("mxfp4", "MXFP4 quantize + block-scaled GEMM, T=2048 N=K=4096, bf16 out", mx(q.QLIN_MX_FP4_E2M1)))
 
-    def rmsnorm(kind):
+    def rmsnorm(kind, dtype=torch.float16):
         def setup():
             T, K, S = 2048, 4096, 128
-            xs = [randn(T, K) for _ in range(4)]
-            gam = (torch.rand(K, device=dev, generator=g) + 0.5).half()
+            xs = [randn(T, K).to(dtype) for _ in range(4)]
+            gam = (torch.rand(K, device=dev, generator=g) + 0.5).to(dtype)
             it = [0]
             if kind == "nvfp4":
                 perm = torch.randperm(K, device=dev, generator=g).to(torch.int32)
@@ -137,6 +137,7 @@ def _rows(q, torch):
         return setup
     for kind in ("int8", "fp8", "nvfp4"):
         rows.append(("rmsnorm_" + kind, "RMSNorm fused with the %s quantizer, 2048 x 4096 fp16" % kind, rmsnorm(kind)))
+    rows.append(("rmsnorm_int8_bf16", "RMSNorm fused with the int8 quantizer, 2048 x 4096 bf16", rmsnorm("int8", torch.bfloat16)))
 
     def w4(N, K, T, act_order=False):
         def setup():

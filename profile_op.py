@@ -2,7 +2,7 @@
 so that a profiler can capture it in isolation, e.g.
 
     ncu --set full --clock-control none -k regex:w4a16_skinny -s 2 -c 1 -o prof \\
-        python -m quantized_linear_layer_gb300.profile_op w4a16 --T 4 --N 11008 --K 4096
+        python profile_op.py w4a16 --T 4 --N 11008 --K 4096
 
 Operations (sizes as flags):
   w4a16        qlin_w4a16_gemm, X [T][K] fp16, weights N x K (uint4 g128)
