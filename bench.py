@@ -24,9 +24,10 @@ per-tensor scale and channel order are calibrated once on X at set-up.
 224 GEMVs / time of that phase); every configuration's rate, its roofline
 fraction and the CPU oracle's rate on the same configuration are in
 `paths`.  Each phase is a captured CUDA graph, timed with CUDA events on its
-stream.  `e2e` calls the public binding once per layer per step (no graph),
-with each phase's input copied from pinned host memory and its output read
-back inside the timed region.
+stream.  `e2e` calls the public binding without graphs (the decode stacks
+through qlin_w4a16_chain, the C ABI's host work for every layer on the
+clock), with each phase's input copied from pinned host memory and its output
+read back inside the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -149,7 +150,7 @@ class Workload:
     """Device-resident inputs, weights and outputs of one step, and the
     captured phases."""
 
-    def __init__(self, q, torch, layers, w4_path="launches"):
+    def __init__(self, q, torch, layers, w4_path="chain"):
         from quantized_linear_layer_gb300 import inputs
         self.q, self.torch = q, torch
         dev = torch.device("cuda")
@@ -269,6 +270,10 @@ class Workload:
         if T == 1 and self.w4_path == "sequence":
             # one persistent launch for the whole stack
             self.q.qlin_w4a16_gemv_sequence(self.w4_steps[1], self.w4_ws)
+            return
+        if self.w4_path == "chain":
+            # one call for the whole stack, a launch per step
+            self.q.qlin_w4a16_chain(self.w4_steps[T])
             return
         for (x, wqs, scs, zps, ys) in self.w4_steps[T]:
             if len(wqs) == 1:
@@ -596,10 +601,11 @@ def run_ours(args):
         "config": {
             "workload": "W4A16 decode at T=1, 4 and 16 over a Llama-2-7B-shaped linear stack (%d blocks x 7 layers "
                         "with the block's dependencies: q,k,v grouped on the block input, o on v, gate,up grouped "
-                        "on o, down on up; 4 launches per block%s) + W8A8 sym+bias T=2048 K=4096 N=4096 + W8A8 "
+                        "on o, down on up; 4 launches per block; %s) + W8A8 sym+bias T=2048 K=4096 N=4096 + W8A8 "
                         "azp per-token T=4096 K=4096 N=14336 + NVFP4 ARCQuant T=2048 K=4096 N=4096 S=128" %
-                        (args.layers, "; T=1 as one persistent launch per 128 steps" if args.w4a16_path == "sequence"
-                         else ""),
+                        (args.layers, {"sequence": "T=1 as one persistent launch per 128 steps",
+                                       "chain": "one qlin_w4a16_chain call per stack",
+                                       "launches": "one grouped call per step"}[args.w4a16_path]),
             "w4a16_path": args.w4a16_path,
             "w4a16_layers_per_step": len(wl.w4),
             "w4a16_weight_bytes_per_pass": wl.w4_bytes[1],
@@ -618,8 +624,9 @@ def run_ours(args):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "ms_per_step": round(sum(e2e_phase.values()) * 1e3, 4),
-            "how": "public binding called once per layer per step, no CUDA graph; each phase's input copied from "
-                   "pinned host memory and its output read back inside the timed region",
+            "how": "public binding without CUDA graphs (the W4A16 stacks through one qlin_w4a16_chain call each, "
+                   "the other phases one call per kernel step); each phase's input copied from pinned host memory "
+                   "and its output read back inside the timed region",
         },
         "gpu_launches": sum(wl.launches.values()) * args.steps,
         "clocks": clocks,
@@ -675,9 +682,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=32, help="transformer blocks in the W4A16 decode stack")
-    ap.add_argument("--w4a16-path", choices=["sequence", "launches"], default="launches",
-                    help="decode stack as one launch per step (grouped where layers share an input), or as one "
-                         "persistent launch")
+    ap.add_argument("--w4a16-path", choices=["chain", "launches", "sequence"], default="chain",
+                    help="decode stacks as one qlin_w4a16_chain call (a launch per step), as one grouped call per "
+                         "step, or (T=1) as one persistent launch")
     ap.add_argument("--cpu-seconds", type=float, default=4.0, help="length of each bounded oracle sample")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps

@@ -264,6 +264,26 @@ typedef struct {
   void* y[QLIN_W4A16_MAX_GROUP];
 } qlin_w4a16_step;
 
+/* ------------------------------------------------------------------------
+ * a1, chain - a decoder's W4A16 linears in one call, one launch per step
+ *
+ * Runs steps[0], steps[1], ... in order on `stream` at T tokens, each step
+ * exactly as qlin_w4a16_gemm_grouped(steps[s].x, T, ...) (so the outputs equal
+ * those calls bit for bit): the chain of dependent linears a decoder runs per
+ * token ("Chapter 9 - Quantization kernels", 9.1: decode reads every weight
+ * once per token).  Every step is checked before anything is launched, and
+ * the launches follow one another with programmatic dependent launch as in
+ * separate calls; one call instead of one per layer keeps the host's share of
+ * a decode step small.
+ *   steps   host array [nsteps] (read during the call only), as for
+ *           qlin_w4a16_gemv_sequence; x of step s is fp16 [T][K_s] and each
+ *           y[p] fp16 [T][N_p]; a step may read what an earlier step wrote
+ *   T       tokens, 0 .. 2^31-1
+ *   group   128
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_w4a16_chain(const qlin_w4a16_step* steps, int nsteps, int64_t T, int64_t group,
+                             cudaStream_t stream);
+
 int64_t qlin_w4a16_sequence_workspace_bytes(int64_t nsteps);
 qlin_status qlin_w4a16_gemv_sequence(const qlin_w4a16_step* steps, int nsteps, int64_t group, void* workspace,
                                      cudaStream_t stream);

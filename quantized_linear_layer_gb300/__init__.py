@@ -22,6 +22,7 @@ __all__ = [
     "qlin_version", "qlin_get_device_error",
     "qlin_quant_w4_g128", "qlin_w4a16_gemm", "qlin_w4a16_gemm_grouped", "qlin_w4a16_step",
     "qlin_w4a16_sequence_workspace_bytes", "qlin_w4a16_gemv_sequence", "qlin_w4a16_gemv_sequence_noalloc",
+    "qlin_w4a16_chain",
     "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm",
     "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
     "QLIN_QFMT_INT8", "QLIN_QFMT_FP8_E4M3", "qlin_quant_fp8", "qlin_fp8_gemm", "qlin_rmsnorm_quant",
@@ -61,6 +62,7 @@ _SIGS = {
     "qlin_w4a16_sequence_workspace_bytes": ([_I64], _I64),
     "qlin_w4a16_gemv_sequence": ([_P, _I32, _I64, _P, _P], _I32),
     "qlin_w4a16_gemv_sequence_noalloc": ([_P, _I32, _I64, _P], _I32),
+    "qlin_w4a16_chain": ([_P, _I32, _I64, _I64, _P], _I32),
     "qlin_quant_act_int8": ([_P, _I32, _I64, _I64, _P, _P, _P, _P], _I32),
     "qlin_int8_row_sum": ([_P, _I64, _I64, _P, _P], _I32),
     "qlin_w8a8_gemm": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
@@ -252,6 +254,22 @@ def qlin_w4a16_gemv_sequence_noalloc(steps, group=128, stream=None):
     arr = _w4a16_steps(steps)
     _check("qlin_w4a16_gemv_sequence_noalloc", lib().qlin_w4a16_gemv_sequence_noalloc(
         ctypes.cast(arr, ctypes.c_void_p), len(steps), group, _stream(stream)))
+
+
+def qlin_w4a16_chain(steps, group=128, stream=None):
+    """Run W4A16 steps in order at T = x.shape[0] tokens in one call, one launch per step.
+
+    steps: list of (x, wqs, scales, zeros, ys) with x fp16 [T][K] and per-matrix lists as in
+    qlin_w4a16_gemm_grouped (ys[p] fp16 [T][N_p])."""
+    if not steps:
+        return
+    t = steps[0][0].shape[0]
+    for i, st in enumerate(steps):
+        if st[0].dim() != 2 or st[0].shape[0] != t or any(y.shape[0] != t for y in st[4]):
+            raise ValueError("step %d: every x and y must be [T][...] with the same T" % i)
+    arr = _w4a16_steps(steps)
+    _check("qlin_w4a16_chain", lib().qlin_w4a16_chain(ctypes.cast(arr, ctypes.c_void_p), len(steps), t, group,
+                                                     _stream(stream)))
 
 
 def qlin_quant_act_int8(x, q, scale, azp=None, stream=None):

@@ -189,34 +189,81 @@ qlin_status qlin_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, cons
   QLIN_LAUNCH(launch_w4a16_gemm(x, T, N, K, wq, scales, zeros, y, stream), "w4a16_gemm launch");
 }
 
+}  // extern "C"
+
+namespace {
+
+// The checks of one grouped W4A16 call (T tokens, `count` matrices of K
+// columns); `what` names the call or step in the message.
+qlin_status check_w4a16_group(const char* what, const void* x, int64_t T, int64_t K, int count, const int64_t* N,
+                              const uint8_t* const* wq, const void* const* scales, const void* const* y,
+                              int64_t group, int64_t* total_out) {
+  QLIN_REQUIRE(group == 128, QLIN_ERR_UNSUPPORTED, "group size %lld (only 128 is built)", (long long)group);
+  QLIN_REQUIRE(count >= 1 && count <= QLIN_W4A16_MAX_GROUP, QLIN_ERR_INVALID_ARG, "%s: count=%d outside [1, %d]", what,
+               count, QLIN_W4A16_MAX_GROUP);
+  QLIN_REQUIRE(T >= 0 && T <= kMaxDim, QLIN_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
+  QLIN_REQUIRE(K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG, "%s: bad K=%lld", what, (long long)K);
+  QLIN_REQUIRE(K % group == 0, QLIN_ERR_INVALID_ARG, "%s: K=%lld is not a multiple of the group size", what,
+               (long long)K);
+  int64_t total = 0;
+  for (int p = 0; p < count; ++p) {
+    QLIN_REQUIRE(N[p] >= 0 && N[p] <= kMaxDim, QLIN_ERR_INVALID_ARG, "%s: bad N[%d]=%lld", what, p, (long long)N[p]);
+    total += N[p];
+  }
+  QLIN_REQUIRE(total <= kMaxDim, QLIN_ERR_INVALID_ARG, "%s: total rows %lld too large", what, (long long)total);
+  *total_out = total;
+  if (T == 0 || total == 0) return QLIN_OK;
+  QLIN_REQUIRE(x && aligned16(x), x ? QLIN_ERR_ALIGNMENT : QLIN_ERR_INVALID_ARG,
+               "%s: x must be non-null and 16-byte aligned", what);
+  for (int p = 0; p < count; ++p) {
+    if (N[p] == 0) continue;
+    QLIN_REQUIRE(wq[p] && scales[p] && y[p], QLIN_ERR_INVALID_ARG, "%s: null pointer for matrix %d", what, p);
+    QLIN_REQUIRE(aligned16(wq[p]), QLIN_ERR_ALIGNMENT, "%s: wq[%d] must be 16-byte aligned", what, p);
+    QLIN_REQUIRE((reinterpret_cast<uintptr_t>(scales[p]) & 1u) == 0 && (reinterpret_cast<uintptr_t>(y[p]) & 1u) == 0,
+                 QLIN_ERR_ALIGNMENT, "%s: scales[%d] and y[%d] must be 2-byte aligned", what, p, p);
+  }
+  return QLIN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 qlin_status qlin_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
                                     const uint8_t* const* wq, const void* const* scales,
                                     const uint8_t* const* zeros, int64_t group, void* const* y,
                                     cudaStream_t stream) {
-  QLIN_REQUIRE(group == 128, QLIN_ERR_UNSUPPORTED, "group size %lld (only 128 is built)", (long long)group);
-  QLIN_REQUIRE(count >= 1 && count <= QLIN_W4A16_MAX_GROUP, QLIN_ERR_INVALID_ARG, "count=%d outside [1, %d]", count,
-               QLIN_W4A16_MAX_GROUP);
   QLIN_REQUIRE(N && wq && scales && zeros && y, QLIN_ERR_INVALID_ARG, "null host array");
-  QLIN_REQUIRE(T >= 0 && T <= kMaxDim, QLIN_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
-  QLIN_REQUIRE(K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad K=%lld", (long long)K);
-  QLIN_REQUIRE(K % group == 0, QLIN_ERR_INVALID_ARG, "K=%lld is not a multiple of the group size", (long long)K);
   int64_t total = 0;
-  for (int p = 0; p < count; ++p) {
-    QLIN_REQUIRE(N[p] >= 0 && N[p] <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad N[%d]=%lld", p, (long long)N[p]);
-    total += N[p];
-  }
-  QLIN_REQUIRE(total <= kMaxDim, QLIN_ERR_INVALID_ARG, "total rows %lld too large", (long long)total);
+  const qlin_status st = check_w4a16_group("w4a16_gemm_grouped", x, T, K, count, N, wq, scales, y, group, &total);
+  if (st != QLIN_OK) return st;
   if (T == 0 || total == 0) return ok();
-  QLIN_REQUIRE(x && aligned16(x), x ? QLIN_ERR_ALIGNMENT : QLIN_ERR_INVALID_ARG, "x must be non-null and 16-byte aligned");
-  for (int p = 0; p < count; ++p) {
-    if (N[p] == 0) continue;
-    QLIN_REQUIRE(wq[p] && scales[p] && y[p], QLIN_ERR_INVALID_ARG, "null pointer for matrix %d", p);
-    QLIN_REQUIRE(aligned16(wq[p]), QLIN_ERR_ALIGNMENT, "wq[%d] must be 16-byte aligned", p);
-    QLIN_REQUIRE((reinterpret_cast<uintptr_t>(scales[p]) & 1u) == 0 && (reinterpret_cast<uintptr_t>(y[p]) & 1u) == 0,
-                 QLIN_ERR_ALIGNMENT, "scales[%d] and y[%d] must be 2-byte aligned", p, p);
-  }
   QLIN_DEVICE();
   QLIN_LAUNCH(launch_w4a16_gemm_grouped(x, T, K, count, N, wq, scales, zeros, y, stream), "w4a16_gemm_grouped launch");
+}
+
+qlin_status qlin_w4a16_chain(const qlin_w4a16_step* steps, int nsteps, int64_t T, int64_t group,
+                             cudaStream_t stream) {
+  QLIN_REQUIRE(nsteps >= 0, QLIN_ERR_INVALID_ARG, "nsteps=%d", nsteps);
+  if (nsteps == 0 || T == 0) return ok();
+  QLIN_REQUIRE(steps != nullptr, QLIN_ERR_INVALID_ARG, "null steps");
+  char what[32];
+  for (int s = 0; s < nsteps; ++s) {
+    const qlin_w4a16_step& st = steps[s];
+    snprintf(what, sizeof(what), "step %d", s);
+    int64_t total = 0;
+    const qlin_status r = check_w4a16_group(what, st.x, T, st.K, st.count, st.N, st.wq, st.scales, st.y, group,
+                                            &total);
+    if (r != QLIN_OK) return r;
+  }
+  QLIN_DEVICE();
+  for (int s = 0; s < nsteps; ++s) {
+    const qlin_w4a16_step& st = steps[s];
+    const cudaError_t e = launch_w4a16_gemm_grouped(st.x, T, st.K, st.count, st.N, st.wq, st.scales, st.zeros,
+                                                    st.y, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "w4a16_chain launch");
+  }
+  return ok();
 }
 
 qlin_status qlin_w4a16_act_order_prepare(const int32_t* g_idx, int64_t K, int64_t group, const uint8_t* wq,

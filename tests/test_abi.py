@@ -176,3 +176,24 @@ def test_empty_problems_launch_nothing(built):
     assert L.qlin_nvfp4_gemm(None, None, None, None, 4, 0, 64, None, None, None, 1, None) == 0
     assert L.qlin_quant_fp8(None, 0, 0, 64, None, None, None) == 0
     assert L.qlin_fp8_gemm(None, None, 0, 8, 64, None, None, None, 0, None, 0, None) == 0
+
+
+def test_chain_checks_every_step_before_launching(built):
+    """qlin_w4a16_chain rejects a bad step anywhere in the chain on the host,
+    before any launch (no GPU is touched here)."""
+    L = built
+    steps = (q.qlin_w4a16_step * 2)()
+    for st in steps:
+        st.x, st.K, st.count = 16, 256, 1
+        st.N[0], st.wq[0], st.scales[0], st.y[0] = 8, 32, 64, 96
+    arr = ctypes.cast(steps, ctypes.c_void_p)
+    assert L.qlin_w4a16_chain(arr, 2, 1, 64, None) == 3            # group 64 is not built
+    steps[1].x = 24                                                 # step 1: x not 16-byte aligned
+    assert L.qlin_w4a16_chain(arr, 2, 1, 128, None) == 2
+    assert b"step 1" in L.qlin_last_error_message()
+    steps[1].x, steps[1].count = 16, 0                              # step 1: no matrix
+    assert L.qlin_w4a16_chain(arr, 2, 1, 128, None) == 1
+    steps[1].count, steps[1].K = 1, 200                             # K not a multiple of 128
+    assert L.qlin_w4a16_chain(arr, 2, 4, 128, None) == 1
+    assert L.qlin_w4a16_chain(arr, 0, 4, 128, None) == 0            # nothing to do
+    assert L.qlin_w4a16_chain(None, 2, 4, 128, None) == 1

@@ -317,6 +317,66 @@ def test_sequence_decoder_blocks_equal_single_launches(qlin_gpu, hid, inter):
                             "sequence down")
 
 
+@pytest.mark.parametrize("T,hid,inter", [(1, 1024, 2816), (4, 1024, 2816), (16, 1024, 2816), (20, 512, 1408),
+                                          (4, 4096, 11008)])
+def test_chain_equals_grouped_calls(qlin_gpu, T, hid, inter):
+    """qlin_w4a16_chain (one call, a launch per step) over two decoder blocks
+    gives every output of the same grouped calls made one by one, bit for
+    bit, and the oracle within tolerance; T = 20 runs as a 16-token and a
+    4-token launch per step.  The first block's v projection is symmetric (no
+    zero-points)."""
+    seed = 700 + T
+    blocks = []
+    for _ in range(2):
+        blk = {}
+        for name, (n, k) in (("q", (hid, hid)), ("k", (hid // 4, hid)), ("v", (hid // 4, hid)), ("o", (hid, hid // 4)),
+                             ("gate", (inter, hid)), ("up", (inter, hid)), ("down", (hid, inter))):
+            blk[name] = _quantized(seed, n, k)
+            seed += 1
+        blocks.append(blk)
+    x0 = inputs.w4a16_decode(seed=98, T=T, N=8, K=hid)["x"]
+    xt = _dev(x0)
+    devs = []
+    for bi, blk in enumerate(blocks):
+        d = {}
+        for name in blk:
+            wq, sc, zp = _dev_mats([blk[name]], symmetric_last=(bi == 0 and name == "v"))
+            d[name] = (wq[0], sc[0], zp[0])
+        devs.append(d)
+
+    def run(chain):
+        outs = [{n: torch.full((T, blocks[0][n][0].shape[0]), float("nan"), dtype=torch.float16, device="cuda")
+                 for n in blocks[0]} for _ in blocks]
+        steps = []
+        h = xt
+        for d, o in zip(devs, outs):
+            steps.append((h, [d[n][0] for n in "qkv"], [d[n][1] for n in "qkv"], [d[n][2] for n in "qkv"],
+                          [o[n] for n in "qkv"]))
+            steps.append((o["v"], [d["o"][0]], [d["o"][1]], [d["o"][2]], [o["o"]]))
+            steps.append((o["o"], [d[n][0] for n in ("gate", "up")], [d[n][1] for n in ("gate", "up")],
+                          [d[n][2] for n in ("gate", "up")], [o[n] for n in ("gate", "up")]))
+            steps.append((o["up"], [d["down"][0]], [d["down"][1]], [d["down"][2]], [o["down"]]))
+            h = o["down"]
+        if chain:
+            qlin_gpu.qlin_w4a16_chain(steps)
+        else:
+            for (x, wqs, scs, zps, ys) in steps:
+                qlin_gpu.qlin_w4a16_gemm_grouped(x, wqs, scs, zps, ys)
+        torch.cuda.synchronize()
+        assert qlin_gpu.qlin_get_device_error() == 0
+        return outs
+
+    got, ref = run(True), run(False)
+    for bi in range(2):
+        for n in blocks[0]:
+            assert torch.equal(got[bi][n], ref[bi][n]), "block %d %s" % (bi, n)
+    codes, s16, z = blocks[0]["q"]
+    assert_within_tolerance(got[0]["q"].cpu().numpy(), oracle.w4a16_reference(x0, codes, s16, z), "chain q")
+    codes, s16, z = blocks[1]["down"]
+    up = got[1]["up"].cpu().numpy()
+    assert_within_tolerance(got[1]["down"].cpu().numpy(), oracle.w4a16_reference(up, codes, s16, z), "chain down")
+
+
 def test_sequence_many_small_steps(qlin_gpu):
     """130 chained steps (more than one launch holds) on two ping-pong buffers,
     with ragged heights and K values whose scale rows are not 16-byte aligned
