@@ -11,7 +11,10 @@ at every configuration the workload defines:
      one launch on the block input, o on v's output, gate and up grouped on
      o's output, down on up's output (4 launches per block).
   2. W8A8 symmetric + bias (T=2048, K=4096, N=4096): per-token int8
-     quantization of X, then the int8-exact GEMM with the fused epilogue.
+     quantization of X, then the int8-exact GEMM with the fused epilogue
+     (the weight codes stored as exact fp16 values by default, which GB300's
+     16-bit tensor cores read without widening them; --w8a8-weights i8 keeps
+     them int8).
   3. W8A8 asymmetric per token with azp (T=4096, K=4096, N=14336, fp16 out):
      per-token asymmetric int8 quantization of X, then the GEMM with the
      s_a s_b (D - azp azp_adj) + bias epilogue.
@@ -150,9 +153,10 @@ class Workload:
     """Device-resident inputs, weights and outputs of one step, and the
     captured phases."""
 
-    def __init__(self, q, torch, layers, w4_path="chain"):
+    def __init__(self, q, torch, layers, w4_path="chain", w8_weights="f16"):
         from quantized_linear_layer_gb300 import inputs
         self.q, self.torch = q, torch
+        self.w8_weights = w8_weights
         dev = torch.device("cuda")
         self.stream = torch.cuda.Stream()
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
@@ -194,6 +198,10 @@ class Workload:
         q.qlin_quant_act_int8(w, self.w8_b, self.w8_sb)
         del w
         self.w8_bias = t(d["bias"])
+        # the weight codes also as exact fp16 values (offline): the GEMM then
+        # reads B without widening it on chip
+        self.w8_b16 = torch.empty((N, K), dtype=torch.float16, device=dev)
+        q.qlin_int8_to_f16(self.w8_b, self.w8_b16)
         self.w8_a = torch.empty((T, K), dtype=torch.int8, device=dev)
         self.w8_sa = torch.empty(T, dtype=torch.float32, device=dev)
         self.w8_out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
@@ -209,6 +217,8 @@ class Workload:
         self.az_adj = torch.empty(N, dtype=torch.int32, device=dev)
         q.qlin_int8_row_sum(self.az_b, self.az_adj)
         self.az_bias = t(d["bias"])
+        self.az_b16 = torch.empty((N, K), dtype=torch.float16, device=dev)
+        q.qlin_int8_to_f16(self.az_b, self.az_b16)
         self.az_a = torch.empty((T, K), dtype=torch.int8, device=dev)
         self.az_sa = torch.empty(T, dtype=torch.float32, device=dev)
         self.az_zp = torch.empty(T, dtype=torch.int32, device=dev)
@@ -283,12 +293,16 @@ class Workload:
 
     def phase_w8a8(self):
         self.q.qlin_quant_act_int8(self.w8_x, self.w8_a, self.w8_sa)
-        self.q.qlin_w8a8_gemm(self.w8_a, self.w8_b, self.w8_sa, self.w8_sb, self.w8_out, bias=self.w8_bias)
+        if self.w8_weights == "f16":
+            self.q.qlin_w8a8_gemm_f16b(self.w8_a, self.w8_b16, self.w8_sa, self.w8_sb, self.w8_out, bias=self.w8_bias)
+        else:
+            self.q.qlin_w8a8_gemm(self.w8_a, self.w8_b, self.w8_sa, self.w8_sb, self.w8_out, bias=self.w8_bias)
 
     def phase_w8a8_azp(self):
         self.q.qlin_quant_act_int8(self.az_x, self.az_a, self.az_sa, self.az_zp)
-        self.q.qlin_w8a8_gemm(self.az_a, self.az_b, self.az_sa, self.az_sb, self.az_out, azp=self.az_zp,
-                              azp_adj=self.az_adj, bias=self.az_bias)
+        gemm = self.q.qlin_w8a8_gemm_f16b if self.w8_weights == "f16" else self.q.qlin_w8a8_gemm
+        gemm(self.az_a, self.az_b16 if self.w8_weights == "f16" else self.az_b, self.az_sa, self.az_sb, self.az_out,
+             azp=self.az_zp, azp_adj=self.az_adj, bias=self.az_bias)
 
     def phase_nvfp4(self):
         self.q.qlin_quant_nvfp4(self.nv_x, self.nv_gx, self.nv_qx, self.nv_sfx, perm=self.nv_perm, S=NVFP4["S"],
@@ -516,7 +530,7 @@ def run_ours(args):
     q.build()
     q.lib()
     peaks = load_peaks()
-    wl = Workload(q, torch, args.layers, args.w4a16_path)
+    wl = Workload(q, torch, args.layers, args.w4a16_path, args.w8a8_weights)
     wl.capture()
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
@@ -553,7 +567,8 @@ def run_ours(args):
         paths[n] = {"ms": round(phase[n] * 1e3, 4), "TOPS_incl_quant": round(tops, 1),
                     "frac_of_16bit_peak_burst": round(tops / p16, 4),
                     "frac_of_16bit_peak_sustained": round(tops / p16s, 4),
-                    "kernel": KERNEL_OF[n] + " (int8 codes as exact fp16 on the 16-bit tensor cores)",
+                    "kernel": KERNEL_OF[n] + (" (weight codes stored as exact fp16, activations int8 widened on chip)"
+                                              if args.w8a8_weights == "f16" else " (int8 weights widened on chip)"),
                     "e2e_ms": round(e2e_phase[n] * 1e3, 4), "host_enqueue_ms": round(e2e_host[n] * 1e3, 4)}
     tops = ops["nvfp4"] / phase["nvfp4"] / 1e12
     paths["nvfp4"] = {"ms": round(phase["nvfp4"] * 1e3, 4), "TOPS_incl_quant": round(tops, 1),
@@ -607,6 +622,7 @@ def run_ours(args):
                                        "chain": "one qlin_w4a16_chain call per stack",
                                        "launches": "one grouped call per step"}[args.w4a16_path]),
             "w4a16_path": args.w4a16_path,
+            "w8a8_weights": args.w8a8_weights,
             "w4a16_layers_per_step": len(wl.w4),
             "w4a16_weight_bytes_per_pass": wl.w4_bytes[1],
             "l2": "inputs larger than L2: each W4A16 pass streams %.2f GB of weights, which also evicts the "
@@ -685,6 +701,8 @@ def main():
     ap.add_argument("--w4a16-path", choices=["chain", "launches", "sequence"], default="chain",
                     help="decode stacks as one qlin_w4a16_chain call (a launch per step), as one grouped call per "
                          "step, or (T=1) as one persistent launch")
+    ap.add_argument("--w8a8-weights", choices=["f16", "i8"], default="f16",
+                    help="W8A8 weight codes stored as exact fp16 values (qlin_w8a8_gemm_f16b) or as int8")
     ap.add_argument("--cpu-seconds", type=float, default=4.0, help="length of each bounded oracle sample")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps

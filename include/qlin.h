@@ -376,15 +376,40 @@ qlin_status qlin_int8_row_sum(const int8_t* b, int64_t N, int64_t K, int32_t* az
  *   out        [T][N] of out_dtype: F16 or BF16; or I32, which writes the raw
  *              accumulator D^ and ignores the epilogue arguments (test hook)
  * K must be a multiple of 16.  GB300 has no int8 tensor-core MMA: the
- * contraction runs on the bf16 tensor cores on exact bf16 copies of the int8
- * codes, in K chunks whose partial sums are exact in fp32, converted to int32
- * and added in int32, so D^ is bit-exact.
+ * contraction runs on the 16-bit tensor cores on exact fp16 copies of the
+ * int8 codes, in K chunks whose partial sums are exact in fp32, converted to
+ * int32 and added in int32, so D^ is bit-exact.
  * ---------------------------------------------------------------------- */
 qlin_status qlin_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_t N, int64_t K,
                            const float* scale_a, int64_t scale_a_numel, const float* scale_b,
                            int64_t scale_b_numel, const int32_t* azp, const int32_t* azp_adj,
                            const void* bias, qlin_dtype bias_dtype, void* out, qlin_dtype out_dtype,
                            cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * a0 + b2 + b3 - the same W8A8 GEMM with the int8 weight codes stored as
+ * exact fp16 values
+ *
+ * Because GB300's tensor cores have no int8 MMA, qlin_w8a8_gemm widens both
+ * operands to fp16 on chip, and widening the weights through shared memory
+ * on every tile is what bounds that kernel.  The weights are static, so they
+ * can be widened once at load time instead: qlin_int8_to_f16 writes every
+ * int8 code as the fp16 number of the same value (exact: |code| <= 128), and
+ * qlin_w8a8_gemm_f16b reads B in that form straight into the MMA's operand
+ * layout.  The arithmetic is unchanged: D^, and every output, equal those of
+ * qlin_w8a8_gemm on the int8 codes bit for bit.  The trade is twice the
+ * weight bytes in memory (2 N K instead of N K) for a faster GEMM where it
+ * is bound by the tensor cores (many tokens); the activations stay int8.
+ *   qlin_int8_to_f16:   src int8 [count] -> dst fp16 [count] (16-byte aligned)
+ *   qlin_w8a8_gemm_f16b: as qlin_w8a8_gemm, with b16 fp16 [N][K] holding
+ *                        the codes (16-byte aligned)
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_int8_to_f16(const int8_t* src, int64_t count, void* dst, cudaStream_t stream);
+qlin_status qlin_w8a8_gemm_f16b(const int8_t* a, const void* b16, int64_t T, int64_t N, int64_t K,
+                                const float* scale_a, int64_t scale_a_numel, const float* scale_b,
+                                int64_t scale_b_numel, const int32_t* azp, const int32_t* azp_adj,
+                                const void* bias, qlin_dtype bias_dtype, void* out, qlin_dtype out_dtype,
+                                cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * c0 - NVFP4 calibration helpers (offline / set-up)

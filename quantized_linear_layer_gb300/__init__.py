@@ -23,7 +23,7 @@ __all__ = [
     "qlin_quant_w4_g128", "qlin_w4a16_gemm", "qlin_w4a16_gemm_grouped", "qlin_w4a16_step",
     "qlin_w4a16_sequence_workspace_bytes", "qlin_w4a16_gemv_sequence", "qlin_w4a16_gemv_sequence_noalloc",
     "qlin_w4a16_chain",
-    "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm",
+    "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm", "qlin_int8_to_f16", "qlin_w8a8_gemm_f16b",
     "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
     "QLIN_QFMT_INT8", "QLIN_QFMT_FP8_E4M3", "qlin_quant_fp8", "qlin_fp8_gemm", "qlin_rmsnorm_quant",
     "qlin_rmsnorm_quant_nvfp4", "QLIN_MX_FP8_E4M3", "QLIN_MX_FP4_E2M1", "qlin_mx_sf_bytes", "qlin_quant_mx",
@@ -66,6 +66,8 @@ _SIGS = {
     "qlin_quant_act_int8": ([_P, _I32, _I64, _I64, _P, _P, _P, _P], _I32),
     "qlin_int8_row_sum": ([_P, _I64, _I64, _P, _P], _I32),
     "qlin_w8a8_gemm": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
+    "qlin_w8a8_gemm_f16b": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
+    "qlin_int8_to_f16": ([_P, _I64, _P, _P], _I32),
     "qlin_nvfp4_global_scale": ([_P, _I32, _I64, _I64, _P, _P], _I32),
     "qlin_arc_perm": ([_P, _I32, _I64, _I64, _P, _P], _I32),
     "qlin_quant_nvfp4": ([_P, _I32, _I64, _I64, _P, _I64, _I32, _P, _P, _P, _I32, _P], _I32),
@@ -306,6 +308,33 @@ def qlin_w8a8_gemm(a, b, scale_a, scale_b, out, azp=None, azp_adj=None, bias=Non
     _check("qlin_w8a8_gemm", lib().qlin_w8a8_gemm(_ptr(a), _ptr(b), t, n, k, _ptr(scale_a), sa_n, _ptr(scale_b), sb_n,
                                                  _ptr(azp), _ptr(azp_adj), _ptr(bias), bias_dt, _ptr(out),
                                                  _dtype_code(out), _stream(stream)))
+
+
+def qlin_int8_to_f16(src, dst, stream=None):
+    """dst = the int8 codes of src as exact fp16 values (the same number of elements)."""
+    torch = _torch()
+    _need(src, torch.int8, name="src"); _need(dst, torch.float16, name="dst")
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst must have the same number of elements")
+    _check("qlin_int8_to_f16", lib().qlin_int8_to_f16(_ptr(src), src.numel(), _ptr(dst), _stream(stream)))
+
+
+def qlin_w8a8_gemm_f16b(a, b16, scale_a, scale_b, out, azp=None, azp_adj=None, bias=None, stream=None):
+    """qlin_w8a8_gemm with the weight codes as exact fp16 values b16 [N][K] (qlin_int8_to_f16)."""
+    torch = _torch()
+    _need(a, torch.int8, name="a"); _need(b16, torch.float16, name="b16")
+    _need(scale_a, torch.float32, name="scale_a"); _need(scale_b, torch.float32, name="scale_b")
+    _need(azp, torch.int32, name="azp"); _need(azp_adj, torch.int32, name="azp_adj")
+    _need(bias, torch.float16, torch.bfloat16, torch.float32, name="bias")
+    _need(out, torch.float16, torch.bfloat16, torch.int32, name="out")
+    t, k = a.shape
+    n = b16.shape[0]
+    sa_n = 0 if scale_a is None else scale_a.numel()
+    sb_n = 0 if scale_b is None else scale_b.numel()
+    bias_dt = QLIN_F16 if bias is None else _dtype_code(bias)
+    _check("qlin_w8a8_gemm_f16b", lib().qlin_w8a8_gemm_f16b(_ptr(a), _ptr(b16), t, n, k, _ptr(scale_a), sa_n,
+                                                           _ptr(scale_b), sb_n, _ptr(azp), _ptr(azp_adj), _ptr(bias),
+                                                           bias_dt, _ptr(out), _dtype_code(out), _stream(stream)))
 
 
 def qlin_nvfp4_global_scale(x, g, stream=None):

@@ -380,7 +380,11 @@ qlin_status qlin_int8_row_sum(const int8_t* b, int64_t N, int64_t K, int32_t* az
   QLIN_LAUNCH(launch_int8_row_sum(b, N, K, azp_adj, stream), "int8_row_sum launch");
 }
 
-qlin_status qlin_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_t N, int64_t K,
+}  // extern "C"
+
+namespace {
+
+qlin_status w8a8_gemm_checked(const int8_t* a, const void* b, bool b_f16, int64_t T, int64_t N, int64_t K,
                            const float* scale_a, int64_t scale_a_numel, const float* scale_b,
                            int64_t scale_b_numel, const int32_t* azp, const int32_t* azp_adj,
                            const void* bias, qlin_dtype bias_dtype, void* out, qlin_dtype out_dtype,
@@ -419,7 +423,38 @@ qlin_status qlin_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_t 
   epi.bias = raw ? nullptr : bias;
   epi.bias_dtype = bias_dtype;
   epi.out_dtype = out_dtype;
-  QLIN_LAUNCH(launch_w8a8_gemm(a, b, T, N, K, epi, out, stream), "w8a8_gemm launch");
+  QLIN_LAUNCH(launch_w8a8_gemm(a, b, b_f16, T, N, K, epi, out, stream), "w8a8_gemm launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+qlin_status qlin_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_t N, int64_t K,
+                           const float* scale_a, int64_t scale_a_numel, const float* scale_b,
+                           int64_t scale_b_numel, const int32_t* azp, const int32_t* azp_adj,
+                           const void* bias, qlin_dtype bias_dtype, void* out, qlin_dtype out_dtype,
+                           cudaStream_t stream) {
+  return w8a8_gemm_checked(a, b, false, T, N, K, scale_a, scale_a_numel, scale_b, scale_b_numel, azp, azp_adj, bias,
+                           bias_dtype, out, out_dtype, stream);
+}
+
+qlin_status qlin_w8a8_gemm_f16b(const int8_t* a, const void* b16, int64_t T, int64_t N, int64_t K,
+                                const float* scale_a, int64_t scale_a_numel, const float* scale_b,
+                                int64_t scale_b_numel, const int32_t* azp, const int32_t* azp_adj,
+                                const void* bias, qlin_dtype bias_dtype, void* out, qlin_dtype out_dtype,
+                                cudaStream_t stream) {
+  return w8a8_gemm_checked(a, b16, true, T, N, K, scale_a, scale_a_numel, scale_b, scale_b_numel, azp, azp_adj, bias,
+                           bias_dtype, out, out_dtype, stream);
+}
+
+qlin_status qlin_int8_to_f16(const int8_t* src, int64_t count, void* dst, cudaStream_t stream) {
+  QLIN_REQUIRE(count >= 0 && count <= (int64_t(1) << 40), QLIN_ERR_INVALID_ARG, "bad count=%lld", (long long)count);
+  if (count == 0) return ok();
+  QLIN_REQUIRE(src && dst, QLIN_ERR_INVALID_ARG, "null pointer");
+  QLIN_REQUIRE(aligned16(src) && aligned16(dst), QLIN_ERR_ALIGNMENT, "src and dst must be 16-byte aligned");
+  QLIN_DEVICE();
+  QLIN_LAUNCH(launch_int8_to_f16(src, count, dst, stream), "int8_to_f16 launch");
 }
 
 qlin_status qlin_nvfp4_global_scale(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, float* g,

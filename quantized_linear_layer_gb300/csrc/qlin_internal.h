@@ -84,8 +84,12 @@ struct W8A8Epilogue {
   qlin_dtype out_dtype;    // F16, BF16 or I32 (raw accumulator)
 };
 
-cudaError_t launch_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_t N, int64_t K,
+// b: int8 [N][K], or (b_f16) the same codes as exact fp16 values [N][K].
+cudaError_t launch_w8a8_gemm(const int8_t* a, const void* b, bool b_f16, int64_t T, int64_t N, int64_t K,
                              const W8A8Epilogue& epi, void* out, cudaStream_t stream);
+
+// dst[i] = fp16(src[i]) for int8 src (exact).
+cudaError_t launch_int8_to_f16(const int8_t* src, int64_t count, void* dst, cudaStream_t stream);
 
 cudaError_t launch_nvfp4_global_scale(const void* x, qlin_dtype x_dtype, int64_t rows, int64_t K, float* g,
                                       cudaStream_t stream);

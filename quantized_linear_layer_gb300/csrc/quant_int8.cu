@@ -22,6 +22,8 @@
 // The rounding decisions are taken in IEEE float32 exactly as written: true
 // division (__fdiv_rn), round-half-to-even (__float2int_rn), and no fused
 // multiply-add anywhere a result feeds a rounding decision.
+#include <algorithm>
+
 #include "device_common.cuh"
 #include "exact_sumsq.cuh"
 #include "qlin_internal.h"
@@ -352,6 +354,32 @@ __global__ void __launch_bounds__(kQuantThreads) rmsnorm_quant_kernel(const void
   }
 }
 
+// Exact fp16 copies of int8 codes: 16 codes per thread (one 16-byte load,
+// two 16-byte stores), grid-stride; the last count % 16 codes one by one.
+__global__ void int8_to_f16_kernel(const int8_t* __restrict__ src, int64_t count, __half* __restrict__ dst) {
+  const int64_t nvec = count / 16;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+    const uint4 u = ldg_v4(src + v * 16);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 lo = __halves2half2(__short2half_rn(static_cast<int8_t>(w[i] & 0xFF)),
+                                        __short2half_rn(static_cast<int8_t>((w[i] >> 8) & 0xFF)));
+      const __half2 hi = __halves2half2(__short2half_rn(static_cast<int8_t>((w[i] >> 16) & 0xFF)),
+                                        __short2half_rn(static_cast<int8_t>(w[i] >> 24)));
+      h[2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
+      h[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+    }
+    uint4* d = reinterpret_cast<uint4*>(dst + v * 16);
+    d[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    d[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+  if (blockIdx.x == 0)
+    for (int64_t i = nvec * 16 + threadIdx.x; i < count; i += blockDim.x) dst[i] = __short2half_rn(src[i]);
+}
+
 // azp_adj[n] = sum_k b[n,k]: one warp per row, 16 bytes per lane per step.
 __global__ void int8_row_sum_kernel(const int8_t* __restrict__ b, int64_t N, int K, int32_t* __restrict__ out) {
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
@@ -488,6 +516,14 @@ cudaError_t launch_rmsnorm_quant(const void* x, qlin_dtype x_dtype, int64_t rows
       else rmsnorm_quant_kernel<2, 0><<<grid, block, 0, stream>>>(x, gamma, k, eps, q, scale);
       break;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_int8_to_f16(const int8_t* src, int64_t count, void* dst, cudaStream_t stream) {
+  if (count == 0) return cudaSuccess;
+  const int64_t nvec = count / 16;
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((nvec + 255) / 256, 8 * sm_count()));
+  int8_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, count, static_cast<__half*>(dst));
   return cudaGetLastError();
 }
 

@@ -64,26 +64,37 @@ namespace qlin {
 namespace {
 
 constexpr int kBM = 128, kBN = 128, kBK = 128;
-constexpr int kStg = 4;             // int8 staging stages (A and B)
+constexpr int kStg = 4;             // staging stages (A int8, and B: int8 or fp16 codes)
 constexpr int kOpsA = 2;            // fp16 A stages in TMEM
-constexpr int kOpsB = 2;            // fp16 B stages in shared memory
+constexpr int kOpsB = 2;            // fp16 B stages in shared memory (int8 B only)
 constexpr int kChunkK = 1024;       // exact fp32 accumulation span
 constexpr int kKbPerChunk = kChunkK / kBK;
 constexpr int kTmemCols = 512;
 constexpr int kTmemTotal = 2 * kBN;         // int32 running total
 constexpr int kTmemA = kTmemTotal + kBN;    // A ring, 64 columns per stage
-constexpr int kThreads = 22 * 32;
-constexpr int kWarpA0 = 2, kWarpB0 = 10, kWarpE0 = 18;
+constexpr int kWarpA0 = 2, kWarpB0 = 10;
 
-constexpr int kStgBytes = (kBM + kBN) * kBK;            // 32 KB (A then B)
-constexpr int kOpBytesB = kBN * kBK * 2;                // 32 KB fp16 (two 64-element K blocks)
-constexpr int kSmemStg = 0;
-constexpr int kSmemOps = kSmemStg + kStg * kStgBytes;   // 128 KB
-constexpr int kSmemPar = kSmemOps + kOpsB * kOpBytesB;  // 192 KB
-constexpr int kSmemBar = kSmemPar + 4 * 3 * kBN * 4;    // + 6 KB (column parameters, one copy per epilogue warp)
-constexpr int kNumBars = 2 * kStg + 2 * kOpsA + 2 * kOpsB + 2 + 2 + 1;
-constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
-constexpr int kSmemTotal = kSmemMisc + 16 + 1024;       // + alignment slack
+// Shared-memory plan of the two forms.  int8 B: 4 staging stages of the int8
+// tiles (A then B, 32 KB) and a 2-stage ring of widened fp16 B (32 KB each).
+// fp16-coded B: 4 stages of the int8 A tile (16 KB) followed by the fp16 B
+// tile (32 KB, two 64-element K blocks in the 128-byte swizzle), which the
+// MMA reads where TMA put it.
+template <bool B16>
+struct W8Plan {
+  static constexpr int kWarpE0 = B16 ? kWarpB0 : kWarpB0 + 8;
+  static constexpr int kThreads = (kWarpE0 + 4) * 32;
+  static constexpr int kStgBytes = B16 ? kBM * kBK + kBN * kBK * 2 : (kBM + kBN) * kBK;
+  static constexpr int kOpBytesB = kBN * kBK * 2;
+  static constexpr int kSmemStg = 0;
+  static constexpr int kSmemOps = kSmemStg + kStg * kStgBytes;
+  static constexpr int kSmemPar = kSmemOps + (B16 ? 0 : kOpsB * kOpBytesB);
+  static constexpr int kSmemBar = kSmemPar + 4 * 3 * kBN * 4;  // column parameters, one copy per epilogue warp
+  static constexpr int kNumBars = 2 * kStg + 2 * kOpsA + 2 * kOpsB + 2 + 2 + 1;
+  static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
+  static constexpr int kSmemTotal = kSmemMisc + 16 + 1024;  // + alignment slack
+  static_assert(kSmemTotal <= 227 * 1024, "shared memory budget");
+  static_assert(kStgBytes % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled tiles");
+};
 
 // Sites recorded in the device error word when a wait expires.
 enum {
@@ -155,10 +166,16 @@ __device__ __forceinline__ void tile_coords(int tile, int mt_count, int nt_count
   nt = in / rows;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+// B16: B holds the int8 weight codes as exact fp16 values (no widening on
+// chip); otherwise B is int8 and widened by warps 10-17.
+template <bool B16>
+__global__ void __launch_bounds__(W8Plan<B16>::kThreads, 1) w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                 const __grid_constant__ CUtensorMap tmB, int T,
                                                                 int N, int K, EpiArgs epi, void* __restrict__ out,
                                                                 int32_t* __restrict__ err) {
+  using P = W8Plan<B16>;
+  constexpr int kStgBytes = P::kStgBytes, kOpBytesB = P::kOpBytesB, kSmemStg = P::kSmemStg, kSmemOps = P::kSmemOps,
+                kSmemPar = P::kSmemPar, kSmemBar = P::kSmemBar, kSmemMisc = P::kSmemMisc, kWarpE0 = P::kWarpE0;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
@@ -186,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStg; ++s) {
       tc::mbar_init(stg_full(s), 1);
-      tc::mbar_init(stg_empty(s), 8);  // four A and four B widener warps
+      tc::mbar_init(stg_empty(s), B16 ? 4 + 1 : 8);  // four A wideners and (fp16 B) the MMA commit, or four B wideners
     }
     for (int o = 0; o < kOpsA; ++o) {
       tc::mbar_init(a_full(o), 4);
@@ -235,7 +252,14 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
           const uint32_t dst = sbase + kSmemStg + s * kStgBytes;
           tc::mbar_arrive_expect_tx(stg_full(s), kStgBytes);
           tc::tma_load_2d(dst, &tmA, kb * kBK, mt * kBM, stg_full(s));
-          tc::tma_load_2d(dst + kBM * kBK, &tmB, kb * kBK, nt * kBN, stg_full(s));
+          if (B16) {
+            // the fp16 codes of the stage's 128 K: two 64-element blocks (128
+            // bytes per row each), the layout the MMA descriptors describe
+            tc::tma_load_2d(dst + kBM * kBK, &tmB, kb * kBK * 2, nt * kBN, stg_full(s));
+            tc::tma_load_2d(dst + kBM * kBK + kBN * 128, &tmB, kb * kBK * 2 + 128, nt * kBN, stg_full(s));
+          } else {
+            tc::tma_load_2d(dst + kBM * kBK, &tmB, kb * kBK, nt * kBN, stg_full(s));
+          }
           issued = it + 1;
         }
       }
@@ -259,15 +283,16 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
             *abort_flag = 1;
             break;
           }
-          const int oa = it % kOpsA, ob = it % kOpsB;
+          const int oa = it % kOpsA, ob = it % kOpsB, s = it % kStg;
           if (!tc::mbar_wait(a_full(oa), (it / kOpsA) & 1, err, kSiteAFull) ||
-              !tc::mbar_wait(b_full(ob), (it / kOpsB) & 1, err, kSiteBFull)) {
+              !(B16 ? tc::mbar_wait(stg_full(s), (it / kStg) & 1, err, kSiteStgFull)
+                    : tc::mbar_wait(b_full(ob), (it / kOpsB) & 1, err, kSiteBFull))) {
             *abort_flag = 1;
             break;
           }
           if (*abort_flag) break;
           tc::tc_fence_after();
-          const uint32_t b_base = sbase + kSmemOps + ob * kOpBytesB;
+          const uint32_t b_base = B16 ? sbase + kSmemStg + s * kStgBytes + kBM * kBK : sbase + kSmemOps + ob * kOpBytesB;
           const uint32_t d = tmem + buf * kBN;
           const uint32_t a_t = tmem + kTmemA + oa * (kBK / 2);
 #pragma unroll
@@ -277,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
           }
           issued_any = true;
           tc::mma_commit(a_empty(oa));
-          tc::mma_commit(b_empty(ob));
+          tc::mma_commit(B16 ? stg_empty(s) : b_empty(ob));
           if (kin == kKbPerChunk - 1 || kb == num_kb - 1) {
             tc::mma_commit(acc_full(buf));
             ++g;
@@ -326,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
         }
       }
     }
-  } else if (warp < kWarpE0) {
+  } else if (!B16 && warp < kWarpE0) {
     // ---------------- B wideners (int8 staging -> fp16 swizzled smem) ----------------
     const int set = (warp - kWarpB0) >> 2;              // takes the stages with it % 2 == set
     const int ct = threadIdx.x - (kWarpB0 + 4 * set) * 32;  // 0..127
@@ -490,16 +515,21 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_gemm_kernel(const __grid_con
 
 }  // namespace
 
-cudaError_t launch_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_t N, int64_t K,
+cudaError_t launch_w8a8_gemm(const int8_t* a, const void* b, bool b_f16, int64_t T, int64_t N, int64_t K,
                              const W8A8Epilogue& e, void* out, cudaStream_t stream) {
   if (T == 0 || N == 0) return cudaSuccess;
   CUtensorMap tmA, tmB;
   cudaError_t st = make_tmap_2d_u8(&tmA, a, static_cast<uint64_t>(K), static_cast<uint64_t>(T), kBK, kBM,
                                    /*swizzle_bytes=*/128);
   if (st != cudaSuccess) return st;
-  st = make_tmap_2d_u8(&tmB, b, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK, kBN);
+  st = b_f16 ? make_tmap_2d_u8(&tmB, b, static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N), 128, kBN,
+                               /*swizzle_bytes=*/128)
+             : make_tmap_2d_u8(&tmB, b, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK, kBN);
   if (st != cudaSuccess) return st;
-  st = cudaFuncSetAttribute(w8a8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
+  const void* fn = b_f16 ? reinterpret_cast<const void*>(w8a8_gemm_kernel<true>)
+                         : reinterpret_cast<const void*>(w8a8_gemm_kernel<false>);
+  const int smem = b_f16 ? W8Plan<true>::kSmemTotal : W8Plan<false>::kSmemTotal;
+  st = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (st != cudaSuccess) return st;
   EpiArgs epi;
   epi.scale_a = e.scale_a;
@@ -517,16 +547,18 @@ cudaError_t launch_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_
   // overlaps the end of the previous kernel (the activation quantizer)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemTotal;
+  cfg.blockDim = dim3(b_f16 ? W8Plan<true>::kThreads : W8Plan<false>::kThreads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, w8a8_gemm_kernel, tmA, tmB, static_cast<int>(T), static_cast<int>(N),
-                            static_cast<int>(K), epi, out, device_error_word());
+  const int Ti = static_cast<int>(T), Ni = static_cast<int>(N), Ki = static_cast<int>(K);
+  int32_t* err = device_error_word();
+  return b_f16 ? cudaLaunchKernelEx(&cfg, w8a8_gemm_kernel<true>, tmA, tmB, Ti, Ni, Ki, epi, out, err)
+               : cudaLaunchKernelEx(&cfg, w8a8_gemm_kernel<false>, tmA, tmB, Ti, Ni, Ki, epi, out, err);
 }
 
 }  // namespace qlin

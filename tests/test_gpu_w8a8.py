@@ -1,7 +1,9 @@
 """W8A8 on the GPU against the CPU oracle: the int32 accumulator bit for bit
 (including adversarial extremes that bring each exact fp32 chunk to its
 2^24 bound), the four fused epilogues within the bf16/fp16 tolerance, and
-the two full-size workloads through the device quantizers."""
+the two full-size workloads through the device quantizers.  Every GEMM test
+runs with the weights as int8 codes (qlin_w8a8_gemm) and as the same codes
+in fp16 (qlin_int8_to_f16 + qlin_w8a8_gemm_f16b)."""
 
 import numpy as np
 import pytest
@@ -18,25 +20,50 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def _raw(q, a, b):
+BFORMS = ["i8", "f16"]
+
+
+def _gemm(q, bform, a, b, sa, sb, out, **kw):
+    """qlin_w8a8_gemm on int8 weights b, or qlin_w8a8_gemm_f16b on their
+    exact fp16 copy made by qlin_int8_to_f16."""
+    if bform == "i8":
+        q.qlin_w8a8_gemm(a, b, sa, sb, out, **kw)
+    else:
+        b16 = torch.empty(b.shape, dtype=torch.float16, device="cuda")
+        q.qlin_int8_to_f16(b, b16)
+        q.qlin_w8a8_gemm_f16b(a, b16, sa, sb, out, **kw)
+
+
+def _raw(q, a, b, bform="i8"):
     out = torch.empty((a.shape[0], b.shape[0]), dtype=torch.int32, device="cuda")
-    q.qlin_w8a8_gemm(_dev(a), _dev(b), None, None, out)
+    _gemm(q, bform, _dev(a), _dev(b), None, None, out)
     torch.cuda.synchronize()
     assert q.qlin_get_device_error() == 0
     return out.cpu().numpy()
 
 
+def test_int8_to_f16_exact(qlin_gpu):
+    """Every code, in a count that is not a multiple of 16."""
+    src = np.tile(np.arange(-128, 128, dtype=np.int16).astype(np.int8), 5)[:1277]
+    dst = torch.empty(src.shape, dtype=torch.float16, device="cuda")
+    qlin_gpu.qlin_int8_to_f16(_dev(src), dst)
+    torch.cuda.synchronize()
+    assert np.array_equal(dst.cpu().numpy().astype(np.float64), src.astype(np.float64))
+
+
+@pytest.mark.parametrize("bform", BFORMS)
 @pytest.mark.parametrize("T,N,K", [(128, 128, 64), (200, 136, 1040), (1, 8, 16), (130, 264, 2064),
                                    (257, 384, 4096), (64, 1000, 3072)])
-def test_accumulator_bit_exact(qlin_gpu, T, N, K):
+def test_accumulator_bit_exact(qlin_gpu, T, N, K, bform):
     rng = np.random.default_rng(T * 7 + N + K)
     a = rng.integers(-128, 128, size=(T, K), dtype=np.int8)
     b = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
-    assert np.array_equal(_raw(qlin_gpu, a, b), oracle.int8_gemm_exact(a, b))
+    assert np.array_equal(_raw(qlin_gpu, a, b, bform), oracle.int8_gemm_exact(a, b))
 
 
+@pytest.mark.parametrize("bform", BFORMS)
 @pytest.mark.parametrize("K", [1024, 2048, 4096, 5120])
-def test_accumulator_extremes(qlin_gpu, K):
+def test_accumulator_extremes(qlin_gpu, K, bform):
     """All-extreme codes drive every 1024-wide fp32 chunk to +-1024*128*127."""
     T, N = 128, 128
     a = np.full((T, K), -128, dtype=np.int8)
@@ -46,7 +73,7 @@ def test_accumulator_extremes(qlin_gpu, K):
     b[1::2] = -127
     b[5] = -128
     b[7, ::3] = 0
-    got = _raw(qlin_gpu, a, b)
+    got = _raw(qlin_gpu, a, b, bform)
     ref = oracle.int8_gemm_exact(a, b)
     assert np.array_equal(got, ref)
     assert np.abs(ref).max() >= (K // 1024) * 1024 * 127 * 127
@@ -58,9 +85,10 @@ def _epilogue_case(rng, T, N, K):
     return x, w
 
 
+@pytest.mark.parametrize("bform", BFORMS)
 @pytest.mark.parametrize("form", ["scaled", "bias", "azp_tensor", "azp_token", "azp_token_nobias", "scalar_scales"])
 @pytest.mark.parametrize("out_dtype", ["bf16", "f16"])
-def test_epilogues(qlin_gpu, form, out_dtype):
+def test_epilogues(qlin_gpu, form, out_dtype, bform):
     rng = np.random.default_rng(5)
     T, N, K = 193, 264, 1552
     x, w = _epilogue_case(rng, T, N, K)
@@ -98,10 +126,10 @@ def test_epilogues(qlin_gpu, form, out_dtype):
         ref = oracle.w8a8_epilogue(d, sa, sb)
     tdt = torch.bfloat16 if out_dtype == "bf16" else torch.float16
     out = torch.empty((T, N), dtype=tdt, device="cuda")
-    qlin_gpu.qlin_w8a8_gemm(_dev(aq), _dev(bq), _dev(sa), _dev(sb), out, **kw)
+    _gemm(qlin_gpu, bform, _dev(aq), _dev(bq), _dev(sa), _dev(sb), out, **kw)
     torch.cuda.synchronize()
     assert qlin_gpu.qlin_get_device_error() == 0
-    assert_within_tolerance(out.float().cpu().numpy(), ref, "W8A8 %s %s" % (form, out_dtype))
+    assert_within_tolerance(out.float().cpu().numpy(), ref, "W8A8 %s %s %s" % (form, out_dtype, bform))
 
 
 def _device_quant(q, x_np, asym):
@@ -114,7 +142,8 @@ def _device_quant(q, x_np, asym):
     return aq, sa, za
 
 
-def test_config3_symmetric_bias_bf16(qlin_gpu):
+@pytest.mark.parametrize("bform", BFORMS)
+def test_config3_symmetric_bias_bf16(qlin_gpu, bform):
     d = inputs.w8a8_sym_bias(seed=2)
     x32 = d["x"].astype(np.float32)
     aq, sa, _ = _device_quant(qlin_gpu, d["x"], asym=False)
@@ -124,17 +153,18 @@ def test_config3_symmetric_bias_bf16(qlin_gpu):
     assert np.array_equal(aq.cpu().numpy(), raq) and np.array_equal(bq.cpu().numpy(), rbq)
     dh = oracle.int8_gemm_exact(raq, rbq)
     raw = torch.empty((2048, 4096), dtype=torch.int32, device="cuda")
-    qlin_gpu.qlin_w8a8_gemm(aq, bq, None, None, raw)
+    _gemm(qlin_gpu, bform, aq, bq, None, None, raw)
     assert np.array_equal(raw.cpu().numpy(), dh)
     out = torch.empty((2048, 4096), dtype=torch.bfloat16, device="cuda")
-    qlin_gpu.qlin_w8a8_gemm(aq, bq, sa, sb, out, bias=_dev(d["bias"]))
+    _gemm(qlin_gpu, bform, aq, bq, sa, sb, out, bias=_dev(d["bias"]))
     torch.cuda.synchronize()
     assert qlin_gpu.qlin_get_device_error() == 0
     ref = oracle.w8a8_epilogue(dh, rsa, rsb, bias=d["bias"])
     assert_within_tolerance(out.float().cpu().numpy(), ref, "config 3")
 
 
-def test_config4_azp_per_token_f16(qlin_gpu):
+@pytest.mark.parametrize("bform", BFORMS)
+def test_config4_azp_per_token_f16(qlin_gpu, bform):
     d = inputs.w8a8_azp_token(seed=3)
     x32 = d["x"].astype(np.float32)
     aq, sa, za = _device_quant(qlin_gpu, d["x"], asym=True)
@@ -150,11 +180,11 @@ def test_config4_azp_per_token_f16(qlin_gpu):
     dh = oracle.int8_gemm_exact(raq, rbq)
     for bias in (d["bias"], None):
         out = torch.empty((4096, 14336), dtype=torch.float16, device="cuda")
-        qlin_gpu.qlin_w8a8_gemm(aq, bq, sa, sb, out, azp=za, azp_adj=adj, bias=None if bias is None else _dev(bias))
+        _gemm(qlin_gpu, bform, aq, bq, sa, sb, out, azp=za, azp_adj=adj, bias=None if bias is None else _dev(bias))
         torch.cuda.synchronize()
         assert qlin_gpu.qlin_get_device_error() == 0
         ref = oracle.w8a8_epilogue(dh, rsa, rsb, azp=rza, azp_adj=radj, bias=bias)
         assert_within_tolerance(out.float().cpu().numpy(), ref, "config 4 bias=%s" % (bias is not None))
     raw = torch.empty((4096, 14336), dtype=torch.int32, device="cuda")
-    qlin_gpu.qlin_w8a8_gemm(aq, bq, None, None, raw)
+    _gemm(qlin_gpu, bform, aq, bq, None, None, raw)
     assert np.array_equal(raw.cpu().numpy(), dh)
