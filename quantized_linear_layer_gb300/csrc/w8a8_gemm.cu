@@ -45,6 +45,11 @@
 //                finished chunk is converted to int32 and added to a running
 //                int32 total kept in TMEM; after the last chunk of a tile the
 //                epilogue is applied and the row is stored.
+// With the weight codes given as exact fp16 values (qlin_w8a8_gemm_f16b) TMA
+// writes each B tile straight into the swizzled operand layout next to its A
+// tile (48 KB stages), there are no B wideners, and warps 10-17 are the
+// epilogue: two per lane quadrant, each draining half of the columns, so that
+// a chunk's drain stays shorter than the next chunk's MMAs.
 // One widener warp needs several times the MMA's time per stage (its loads,
 // conversion, store and barrier round trip are a serial chain), hence two
 // sets.
@@ -82,13 +87,17 @@ constexpr int kWarpA0 = 2, kWarpB0 = 10;
 template <bool B16>
 struct W8Plan {
   static constexpr int kWarpE0 = B16 ? kWarpB0 : kWarpB0 + 8;
-  static constexpr int kThreads = (kWarpE0 + 4) * 32;
+  // epilogue warps: with fp16-coded B the eight warps that would widen B
+  // drain the accumulator instead, two per TMEM lane quadrant, each taking
+  // half of the tile's columns
+  static constexpr int kEpiWarps = B16 ? 8 : 4;
+  static constexpr int kThreads = (kWarpE0 + kEpiWarps) * 32;
   static constexpr int kStgBytes = B16 ? kBM * kBK + kBN * kBK * 2 : (kBM + kBN) * kBK;
   static constexpr int kOpBytesB = kBN * kBK * 2;
   static constexpr int kSmemStg = 0;
   static constexpr int kSmemOps = kSmemStg + kStg * kStgBytes;
   static constexpr int kSmemPar = kSmemOps + (B16 ? 0 : kOpsB * kOpBytesB);
-  static constexpr int kSmemBar = kSmemPar + 4 * 3 * kBN * 4;  // column parameters, one copy per epilogue warp
+  static constexpr int kSmemBar = kSmemPar + kEpiWarps * 3 * kBN * 4;  // column parameters, one copy per epilogue warp
   static constexpr int kNumBars = 2 * kStg + 2 * kOpsA + 2 * kOpsB + 2 + 2 + 1;
   static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
   static constexpr int kSmemTotal = kSmemMisc + 16 + 1024;  // + alignment slack
@@ -175,7 +184,8 @@ __global__ void __launch_bounds__(W8Plan<B16>::kThreads, 1) w8a8_gemm_kernel(con
                                                                 int32_t* __restrict__ err) {
   using P = W8Plan<B16>;
   constexpr int kStgBytes = P::kStgBytes, kOpBytesB = P::kOpBytesB, kSmemStg = P::kSmemStg, kSmemOps = P::kSmemOps,
-                kSmemPar = P::kSmemPar, kSmemBar = P::kSmemBar, kSmemMisc = P::kSmemMisc, kWarpE0 = P::kWarpE0;
+                kSmemPar = P::kSmemPar, kSmemBar = P::kSmemBar, kSmemMisc = P::kSmemMisc, kWarpE0 = P::kWarpE0,
+                kEpiWarps = P::kEpiWarps;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
@@ -215,7 +225,7 @@ __global__ void __launch_bounds__(W8Plan<B16>::kThreads, 1) w8a8_gemm_kernel(con
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(acc_full(b), 1);
-      tc::mbar_init(acc_empty(b), 4);
+      tc::mbar_init(acc_empty(b), kEpiWarps);
     }
     tc::mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -398,6 +408,9 @@ __global__ void __launch_bounds__(W8Plan<B16>::kThreads, 1) w8a8_gemm_kernel(con
   } else {
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int ew = warp - kWarpE0;
+    constexpr int kCols = kBN / (kEpiWarps / 4);  // columns of the tile this warp drains
+    const int col0 = (ew >> 2) * kCols;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     pdl_wait();  // the scales and zero-points may come from the previous kernel
     const bool per_tensor_adj = epi.azp == nullptr && epi.azp_adj != nullptr;
@@ -410,7 +423,7 @@ __global__ void __launch_bounds__(W8Plan<B16>::kThreads, 1) w8a8_gemm_kernel(con
       const int row = m0 + q * 32 + lane;
       // Column parameters of this tile, in a copy private to this warp (so no
       // other warp's progress matters): lane l loads columns l, l+32, l+64, l+96.
-      float* par_sb = reinterpret_cast<float*>(smem + kSmemPar + q * 3 * kBN * 4);
+      float* par_sb = reinterpret_cast<float*>(smem + kSmemPar + ew * 3 * kBN * 4);
       int32_t* par_adj = reinterpret_cast<int32_t*>(par_sb + kBN);
       float* par_bias = par_sb + 2 * kBN;
       __syncwarp();  // every lane is done with the previous tile's parameters
@@ -442,7 +455,7 @@ __global__ void __launch_bounds__(W8Plan<B16>::kThreads, 1) w8a8_gemm_kernel(con
         tc::tc_fence_after();
         const bool last = c == num_chunks - 1;
 #pragma unroll 1
-        for (int cg = 0; cg < kBN / 16; ++cg) {
+        for (int cg = col0 / 16; cg < (col0 + kCols) / 16; ++cg) {
           __syncwarp();  // reconverge after the row-bound branches before the aligned TMEM ops
           uint32_t va[16], vt[16];
           tc::tmem_ld_32x32b_x16(lane_base + buf * kBN + cg * 16, va);
