@@ -11,10 +11,12 @@ at every configuration the workload defines:
      one launch on the block input, o on v's output, gate and up grouped on
      o's output, down on up's output (4 launches per block).
   2. W8A8 symmetric + bias (T=2048, K=4096, N=4096): per-token int8
-     quantization of X, then the int8-exact GEMM with the fused epilogue
-     (the weight codes stored as exact fp16 values by default, which GB300's
-     16-bit tensor cores read without widening them; --w8a8-weights i8 keeps
-     them int8).
+     quantization of X, then the int8-exact GEMM with the fused epilogue.
+     By default both operands' codes are stored as exact fp16 values (the
+     quantizer writes the activation codes in that form, the weights are
+     converted once at set-up), which GB300's 16-bit tensor cores read
+     without widening them; --w8a8-form f16b keeps the activation codes int8
+     and --w8a8-form i8 both.
   3. W8A8 asymmetric per token with azp (T=4096, K=4096, N=14336, fp16 out):
      per-token asymmetric int8 quantization of X, then the GEMM with the
      s_a s_b (D - azp azp_adj) + bias epilogue.
@@ -58,7 +60,7 @@ W8A8_AZP = dict(T=4096, K=4096, N=14336)
 NVFP4 = dict(T=2048, K=4096, N=4096, S=128)
 PATHS = ["w4a16_t1", "w4a16_t4", "w4a16_t16", "w8a8_sym", "w8a8_azp", "nvfp4"]
 KERNEL_OF = {"w4a16_t1": "w4a16_gemv_kernel", "w4a16_t4": "w4a16_skinny_kernel", "w4a16_t16": "w4a16_skinny_kernel",
-             "w8a8_sym": "w8a8_gemm_kernel", "w8a8_azp": "w8a8_gemm_kernel",
+             "w8a8_sym": None, "w8a8_azp": None,
              "nvfp4": "block_scaled_gemm_kernel<NVFP4>"}
 CSRC = os.path.join(ROOT, "quantized_linear_layer_gb300", "csrc")
 # ncu DRAM-traffic summaries, each valid for the kernel sources it names
@@ -71,6 +73,10 @@ TRAFFIC = {
 # fp4 block-scaled MMA rate relative to the 16-bit rate: nominal (13.5 / 2.25
 # PFLOP/s) and the rate measured with back-to-back tcgen05 MMAs on this GPU
 FP4_RATIO_NOMINAL, FP4_RATIO_MEASURED = 6.0, 4.0
+# the W8A8 GEMM kernel of each operand form
+W8A8_KERNEL = {"f16": "w8a8_f16_gemm_kernel (activation and weight codes stored as exact fp16)",
+               "f16b": "w8a8_gemm_kernel<true> (weight codes stored as exact fp16, activations widened on chip)",
+               "i8": "w8a8_gemm_kernel<false> (int8 codes widened on chip)"}
 
 
 def w4a16_bytes(N, K, T):
@@ -153,10 +159,10 @@ class Workload:
     """Device-resident inputs, weights and outputs of one step, and the
     captured phases."""
 
-    def __init__(self, q, torch, layers, w4_path="chain", w8_weights="f16"):
+    def __init__(self, q, torch, layers, w4_path="chain", w8_form="f16"):
         from quantized_linear_layer_gb300 import inputs
         self.q, self.torch = q, torch
-        self.w8_weights = w8_weights
+        self.w8_form = w8_form
         dev = torch.device("cuda")
         self.stream = torch.cuda.Stream()
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
@@ -203,6 +209,7 @@ class Workload:
         self.w8_b16 = torch.empty((N, K), dtype=torch.float16, device=dev)
         q.qlin_int8_to_f16(self.w8_b, self.w8_b16)
         self.w8_a = torch.empty((T, K), dtype=torch.int8, device=dev)
+        self.w8_a16 = torch.empty((T, K), dtype=torch.float16, device=dev)
         self.w8_sa = torch.empty(T, dtype=torch.float32, device=dev)
         self.w8_out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
         # 3. W8A8 asymmetric per token with azp (azp_adj precomputed offline)
@@ -220,6 +227,7 @@ class Workload:
         self.az_b16 = torch.empty((N, K), dtype=torch.float16, device=dev)
         q.qlin_int8_to_f16(self.az_b, self.az_b16)
         self.az_a = torch.empty((T, K), dtype=torch.int8, device=dev)
+        self.az_a16 = torch.empty((T, K), dtype=torch.float16, device=dev)
         self.az_sa = torch.empty(T, dtype=torch.float32, device=dev)
         self.az_zp = torch.empty(T, dtype=torch.int32, device=dev)
         self.az_out = torch.empty((T, N), dtype=torch.float16, device=dev)
@@ -292,17 +300,29 @@ class Workload:
                 self.q.qlin_w4a16_gemm_grouped(x, wqs, scs, zps, ys)
 
     def phase_w8a8(self):
-        self.q.qlin_quant_act_int8(self.w8_x, self.w8_a, self.w8_sa)
-        if self.w8_weights == "f16":
-            self.q.qlin_w8a8_gemm_f16b(self.w8_a, self.w8_b16, self.w8_sa, self.w8_sb, self.w8_out, bias=self.w8_bias)
+        q = self.q
+        if self.w8_form == "f16":
+            q.qlin_quant_act_int8_f16(self.w8_x, self.w8_a16, self.w8_sa)
+            q.qlin_w8a8_gemm_f16(self.w8_a16, self.w8_b16, self.w8_sa, self.w8_sb, self.w8_out, bias=self.w8_bias)
+            return
+        q.qlin_quant_act_int8(self.w8_x, self.w8_a, self.w8_sa)
+        if self.w8_form == "f16b":
+            q.qlin_w8a8_gemm_f16b(self.w8_a, self.w8_b16, self.w8_sa, self.w8_sb, self.w8_out, bias=self.w8_bias)
         else:
-            self.q.qlin_w8a8_gemm(self.w8_a, self.w8_b, self.w8_sa, self.w8_sb, self.w8_out, bias=self.w8_bias)
+            q.qlin_w8a8_gemm(self.w8_a, self.w8_b, self.w8_sa, self.w8_sb, self.w8_out, bias=self.w8_bias)
 
     def phase_w8a8_azp(self):
-        self.q.qlin_quant_act_int8(self.az_x, self.az_a, self.az_sa, self.az_zp)
-        gemm = self.q.qlin_w8a8_gemm_f16b if self.w8_weights == "f16" else self.q.qlin_w8a8_gemm
-        gemm(self.az_a, self.az_b16 if self.w8_weights == "f16" else self.az_b, self.az_sa, self.az_sb, self.az_out,
-             azp=self.az_zp, azp_adj=self.az_adj, bias=self.az_bias)
+        q = self.q
+        kw = dict(azp=self.az_zp, azp_adj=self.az_adj, bias=self.az_bias)
+        if self.w8_form == "f16":
+            q.qlin_quant_act_int8_f16(self.az_x, self.az_a16, self.az_sa, self.az_zp)
+            q.qlin_w8a8_gemm_f16(self.az_a16, self.az_b16, self.az_sa, self.az_sb, self.az_out, **kw)
+            return
+        q.qlin_quant_act_int8(self.az_x, self.az_a, self.az_sa, self.az_zp)
+        if self.w8_form == "f16b":
+            q.qlin_w8a8_gemm_f16b(self.az_a, self.az_b16, self.az_sa, self.az_sb, self.az_out, **kw)
+        else:
+            q.qlin_w8a8_gemm(self.az_a, self.az_b, self.az_sa, self.az_sb, self.az_out, **kw)
 
     def phase_nvfp4(self):
         self.q.qlin_quant_nvfp4(self.nv_x, self.nv_gx, self.nv_qx, self.nv_sfx, perm=self.nv_perm, S=NVFP4["S"],
@@ -530,7 +550,7 @@ def run_ours(args):
     q.build()
     q.lib()
     peaks = load_peaks()
-    wl = Workload(q, torch, args.layers, args.w4a16_path, args.w8a8_weights)
+    wl = Workload(q, torch, args.layers, args.w4a16_path, args.w8a8_form)
     wl.capture()
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
@@ -567,8 +587,7 @@ def run_ours(args):
         paths[n] = {"ms": round(phase[n] * 1e3, 4), "TOPS_incl_quant": round(tops, 1),
                     "frac_of_16bit_peak_burst": round(tops / p16, 4),
                     "frac_of_16bit_peak_sustained": round(tops / p16s, 4),
-                    "kernel": KERNEL_OF[n] + (" (weight codes stored as exact fp16, activations int8 widened on chip)"
-                                              if args.w8a8_weights == "f16" else " (int8 weights widened on chip)"),
+                    "kernel": W8A8_KERNEL[args.w8a8_form],
                     "e2e_ms": round(e2e_phase[n] * 1e3, 4), "host_enqueue_ms": round(e2e_host[n] * 1e3, 4)}
     tops = ops["nvfp4"] / phase["nvfp4"] / 1e12
     paths["nvfp4"] = {"ms": round(phase["nvfp4"] * 1e3, 4), "TOPS_incl_quant": round(tops, 1),
@@ -593,7 +612,7 @@ def run_ours(args):
         achieved = ops[dom] / phase[dom] / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4)}
-    kern = KERNEL_OF[dom]
+    kern = KERNEL_OF[dom] or W8A8_KERNEL[args.w8a8_form].split(" ")[0]
     if dom == "w4a16_t1" and args.w4a16_path == "sequence":
         kern = "w4a16_seq_kernel"
     roof.update({"kernel": kern, "phase": dom, "share_of_step": round(phase[dom] / sum(phase.values()), 4),
@@ -622,7 +641,7 @@ def run_ours(args):
                                        "chain": "one qlin_w4a16_chain call per stack",
                                        "launches": "one grouped call per step"}[args.w4a16_path]),
             "w4a16_path": args.w4a16_path,
-            "w8a8_weights": args.w8a8_weights,
+            "w8a8_form": args.w8a8_form,
             "w4a16_layers_per_step": len(wl.w4),
             "w4a16_weight_bytes_per_pass": wl.w4_bytes[1],
             "l2": "inputs larger than L2: each W4A16 pass streams %.2f GB of weights, which also evicts the "
@@ -701,8 +720,9 @@ def main():
     ap.add_argument("--w4a16-path", choices=["chain", "launches", "sequence"], default="chain",
                     help="decode stacks as one qlin_w4a16_chain call (a launch per step), as one grouped call per "
                          "step, or (T=1) as one persistent launch")
-    ap.add_argument("--w8a8-weights", choices=["f16", "i8"], default="f16",
-                    help="W8A8 weight codes stored as exact fp16 values (qlin_w8a8_gemm_f16b) or as int8")
+    ap.add_argument("--w8a8-form", choices=["f16", "f16b", "i8"], default="f16",
+                    help="W8A8 operand codes: both as exact fp16 values (qlin_quant_act_int8_f16 + "
+                         "qlin_w8a8_gemm_f16), the weights only (qlin_w8a8_gemm_f16b), or int8 (qlin_w8a8_gemm)")
     ap.add_argument("--cpu-seconds", type=float, default=4.0, help="length of each bounded oracle sample")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps

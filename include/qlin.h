@@ -412,6 +412,30 @@ qlin_status qlin_w8a8_gemm_f16b(const int8_t* a, const void* b16, int64_t T, int
                                 cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * b1 + b2 + b3 - per-token int8 quantization and the W8A8 GEMM with both
+ * operands' codes stored as exact fp16 values
+ *
+ * The same arithmetic again, with the activation codes in the fp16 form as
+ * well: qlin_quant_act_int8_f16 computes exactly the codes, scales and
+ * zero-points of qlin_quant_act_int8 and writes each code as the fp16
+ * number of the same value; qlin_w8a8_gemm_f16 then runs the GEMM with both
+ * tiles read by TMA straight into the MMA's operand layout (no widening on
+ * chip, 128 x 256 output tiles).  D^ and every output equal those of
+ * qlin_w8a8_gemm on the int8 codes bit for bit.  The trade is 2 T K bytes of
+ * activation codes instead of T K (written once, read from L2 by the tiles).
+ *   qlin_quant_act_int8_f16: as qlin_quant_act_int8, q16 out fp16 [T][K]
+ *                            (16-byte aligned)
+ *   qlin_w8a8_gemm_f16:      as qlin_w8a8_gemm, with a16 fp16 [T][K] and b16
+ *                            fp16 [N][K] holding the codes (16-byte aligned)
+ * ---------------------------------------------------------------------- */
+qlin_status qlin_quant_act_int8_f16(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, void* q16,
+                                    float* scale, int32_t* azp, cudaStream_t stream);
+qlin_status qlin_w8a8_gemm_f16(const void* a16, const void* b16, int64_t T, int64_t N, int64_t K,
+                               const float* scale_a, int64_t scale_a_numel, const float* scale_b,
+                               int64_t scale_b_numel, const int32_t* azp, const int32_t* azp_adj, const void* bias,
+                               qlin_dtype bias_dtype, void* out, qlin_dtype out_dtype, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * c0 - NVFP4 calibration helpers (offline / set-up)
  *
  * qlin_nvfp4_global_scale: g = max |x| / (6 . 448) over the whole tensor, the

@@ -10,6 +10,8 @@ Operations (sizes as flags):
   int8_quant   qlin_quant_act_int8, X [T][K] fp16, symmetric
   w8a8         qlin_w8a8_gemm, A [T][K] int8, B [N][K] int8, per-token / per-channel scales, bf16 out
   w8a8_f16b    qlin_w8a8_gemm_f16b, the same with B as exact fp16 codes
+  w8a8_f16     qlin_w8a8_gemm_f16, the same with A and B as exact fp16 codes
+  int8_quant_f16  qlin_quant_act_int8_f16, X [T][K] fp16, symmetric, codes written as fp16
   nvfp4_quant  qlin_quant_nvfp4, X [T][K] fp16 with S residual channels, MMA scale layout
   nvfp4_gemm   qlin_nvfp4_gemm, A [T][K] and B [N][K] NVFP4 (made by the quantizer), bf16 out
   mxfp8_quant / mxfp4_quant  qlin_quant_mx, X [T][K] fp16, MMA scale layout
@@ -67,7 +69,13 @@ def _setup(args, q, torch):
         sa = torch.empty(T, dtype=torch.float32, device="cuda")
         return lambda i: q.qlin_quant_act_int8(xs[i % copies], qa, sa)
 
-    if args.op in ("w8a8", "w8a8_f16b"):
+    if args.op == "int8_quant_f16":
+        xs = [randn((T, K), torch.float16) for _ in range(copies)]
+        qa = torch.empty((T, K), dtype=torch.float16, device="cuda")
+        sa = torch.empty(T, dtype=torch.float32, device="cuda")
+        return lambda i: q.qlin_quant_act_int8_f16(xs[i % copies], qa, sa)
+
+    if args.op in ("w8a8", "w8a8_f16b", "w8a8_f16"):
         a = torch.randint(-127, 128, (T, K), dtype=torch.int8, device="cuda", generator=g)
         sa = torch.rand(T, device="cuda", generator=g) * 0.01 + 0.001
         bs = [torch.randint(-127, 128, (N, K), dtype=torch.int8, device="cuda", generator=g) for _ in range(copies)]
@@ -78,7 +86,11 @@ def _setup(args, q, torch):
         b16s = [torch.empty((N, K), dtype=torch.float16, device="cuda") for _ in range(copies)]
         for b, b16 in zip(bs, b16s):
             q.qlin_int8_to_f16(b, b16)
-        return lambda i: q.qlin_w8a8_gemm_f16b(a, b16s[i % copies], sa, sb, out)
+        if args.op == "w8a8_f16b":
+            return lambda i: q.qlin_w8a8_gemm_f16b(a, b16s[i % copies], sa, sb, out)
+        a16 = torch.empty((T, K), dtype=torch.float16, device="cuda")
+        q.qlin_int8_to_f16(a, a16)
+        return lambda i: q.qlin_w8a8_gemm_f16(a16, b16s[i % copies], sa, sb, out)
 
     if args.op in ("nvfp4_quant", "nvfp4_gemm"):
         S = args.S
@@ -187,7 +199,8 @@ def _setup(args, q, torch):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("op", choices=["w4a16", "w4a16_group", "int8_quant", "w8a8", "w8a8_f16b", "nvfp4_quant", "nvfp4_gemm",
+    ap.add_argument("op", choices=["w4a16", "w4a16_group", "int8_quant", "w8a8", "w8a8_f16b", "w8a8_f16", "int8_quant_f16",
+                                   "nvfp4_quant", "nvfp4_gemm",
                                    "fp8_quant", "fp8_gemm", "rmsnorm_nvfp4", "rmsnorm_int8", "mxfp8_quant",
                                    "mxfp4_quant", "mxfp8_gemm", "mxfp4_gemm", "hadamard", "w4a16_act_order"])
     ap.add_argument("--n", type=int, default=256, help="Hadamard group size")

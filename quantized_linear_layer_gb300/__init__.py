@@ -24,6 +24,7 @@ __all__ = [
     "qlin_w4a16_sequence_workspace_bytes", "qlin_w4a16_gemv_sequence", "qlin_w4a16_gemv_sequence_noalloc",
     "qlin_w4a16_chain",
     "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm", "qlin_int8_to_f16", "qlin_w8a8_gemm_f16b",
+    "qlin_quant_act_int8_f16", "qlin_w8a8_gemm_f16",
     "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
     "QLIN_QFMT_INT8", "QLIN_QFMT_FP8_E4M3", "qlin_quant_fp8", "qlin_fp8_gemm", "qlin_rmsnorm_quant",
     "qlin_rmsnorm_quant_nvfp4", "QLIN_MX_FP8_E4M3", "QLIN_MX_FP4_E2M1", "qlin_mx_sf_bytes", "qlin_quant_mx",
@@ -68,6 +69,8 @@ _SIGS = {
     "qlin_w8a8_gemm": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
     "qlin_w8a8_gemm_f16b": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
     "qlin_int8_to_f16": ([_P, _I64, _P, _P], _I32),
+    "qlin_quant_act_int8_f16": ([_P, _I32, _I64, _I64, _P, _P, _P, _P], _I32),
+    "qlin_w8a8_gemm_f16": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
     "qlin_nvfp4_global_scale": ([_P, _I32, _I64, _I64, _P, _P], _I32),
     "qlin_arc_perm": ([_P, _I32, _I64, _I64, _P, _P], _I32),
     "qlin_quant_nvfp4": ([_P, _I32, _I64, _I64, _P, _I64, _I32, _P, _P, _P, _I32, _P], _I32),
@@ -284,6 +287,16 @@ def qlin_quant_act_int8(x, q, scale, azp=None, stream=None):
                                                            _ptr(azp), _stream(stream)))
 
 
+def qlin_quant_act_int8_f16(x, q16, scale, azp=None, stream=None):
+    """qlin_quant_act_int8 writing each code as the fp16 number of the same value, q16 [T][K]."""
+    torch = _torch()
+    _need(x, torch.float16, torch.bfloat16, torch.float32, name="x"); _need(q16, torch.float16, name="q16")
+    _need(scale, torch.float32, name="scale"); _need(azp, torch.int32, name="azp")
+    t, k = x.shape
+    _check("qlin_quant_act_int8_f16", lib().qlin_quant_act_int8_f16(_ptr(x), _dtype_code(x), t, k, _ptr(q16),
+                                                                   _ptr(scale), _ptr(azp), _stream(stream)))
+
+
 def qlin_int8_row_sum(b, azp_adj, stream=None):
     """azp_adj[n] = sum_k b[n, k] for int8 b [N][K]."""
     torch = _torch()
@@ -335,6 +348,25 @@ def qlin_w8a8_gemm_f16b(a, b16, scale_a, scale_b, out, azp=None, azp_adj=None, b
     _check("qlin_w8a8_gemm_f16b", lib().qlin_w8a8_gemm_f16b(_ptr(a), _ptr(b16), t, n, k, _ptr(scale_a), sa_n,
                                                            _ptr(scale_b), sb_n, _ptr(azp), _ptr(azp_adj), _ptr(bias),
                                                            bias_dt, _ptr(out), _dtype_code(out), _stream(stream)))
+
+
+def qlin_w8a8_gemm_f16(a16, b16, scale_a, scale_b, out, azp=None, azp_adj=None, bias=None, stream=None):
+    """qlin_w8a8_gemm with both operands' codes as exact fp16 values: a16 [T][K]
+    (qlin_quant_act_int8_f16) and b16 [N][K] (qlin_int8_to_f16)."""
+    torch = _torch()
+    _need(a16, torch.float16, name="a16"); _need(b16, torch.float16, name="b16")
+    _need(scale_a, torch.float32, name="scale_a"); _need(scale_b, torch.float32, name="scale_b")
+    _need(azp, torch.int32, name="azp"); _need(azp_adj, torch.int32, name="azp_adj")
+    _need(bias, torch.float16, torch.bfloat16, torch.float32, name="bias")
+    _need(out, torch.float16, torch.bfloat16, torch.int32, name="out")
+    t, k = a16.shape
+    n = b16.shape[0]
+    sa_n = 0 if scale_a is None else scale_a.numel()
+    sb_n = 0 if scale_b is None else scale_b.numel()
+    bias_dt = QLIN_F16 if bias is None else _dtype_code(bias)
+    _check("qlin_w8a8_gemm_f16", lib().qlin_w8a8_gemm_f16(_ptr(a16), _ptr(b16), t, n, k, _ptr(scale_a), sa_n,
+                                                         _ptr(scale_b), sb_n, _ptr(azp), _ptr(azp_adj), _ptr(bias),
+                                                         bias_dt, _ptr(out), _dtype_code(out), _stream(stream)))
 
 
 def qlin_nvfp4_global_scale(x, g, stream=None):

@@ -353,8 +353,8 @@ qlin_status qlin_w4a16_gemv_sequence_noalloc(const qlin_w4a16_step* steps, int n
   return qlin_w4a16_gemv_sequence(steps, nsteps, group, ws, stream);
 }
 
-qlin_status qlin_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
-                                float* scale, int32_t* azp, cudaStream_t stream) {
+static qlin_status quant_act_int8_checked(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, void* q,
+                                          bool f16_codes, float* scale, int32_t* azp, cudaStream_t stream) {
   QLIN_REQUIRE(is_float_dtype(x_dtype), QLIN_ERR_INVALID_ARG, "x_dtype must be F16, BF16 or F32");
   QLIN_REQUIRE(T >= 0 && T <= kMaxDim && K > 0 && K <= kMaxDim, QLIN_ERR_INVALID_ARG, "bad sizes T=%lld K=%lld",
                (long long)T, (long long)K);
@@ -365,7 +365,17 @@ qlin_status qlin_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, in
   QLIN_REQUIRE((reinterpret_cast<uintptr_t>(scale) & 3u) == 0 && (reinterpret_cast<uintptr_t>(azp) & 3u) == 0,
                QLIN_ERR_ALIGNMENT, "scale and azp must be 4-byte aligned");
   QLIN_DEVICE();
-  QLIN_LAUNCH(launch_quant_act_int8(x, x_dtype, T, K, q, scale, azp, stream), "quant_act_int8 launch");
+  QLIN_LAUNCH(launch_quant_act_int8(x, x_dtype, T, K, q, f16_codes, scale, azp, stream), "quant_act_int8 launch");
+}
+
+qlin_status qlin_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
+                                float* scale, int32_t* azp, cudaStream_t stream) {
+  return quant_act_int8_checked(x, x_dtype, T, K, q, false, scale, azp, stream);
+}
+
+qlin_status qlin_quant_act_int8_f16(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, void* q16,
+                                    float* scale, int32_t* azp, cudaStream_t stream) {
+  return quant_act_int8_checked(x, x_dtype, T, K, q16, true, scale, azp, stream);
 }
 
 qlin_status qlin_int8_row_sum(const int8_t* b, int64_t N, int64_t K, int32_t* azp_adj, cudaStream_t stream) {
@@ -384,7 +394,11 @@ qlin_status qlin_int8_row_sum(const int8_t* b, int64_t N, int64_t K, int32_t* az
 
 namespace {
 
-qlin_status w8a8_gemm_checked(const int8_t* a, const void* b, bool b_f16, int64_t T, int64_t N, int64_t K,
+// Operand forms of the W8A8 GEMM: int8 codes, or the same codes as exact
+// fp16 values for B only or for both operands.
+enum W8A8Form { kW8I8, kW8F16B, kW8F16 };
+
+qlin_status w8a8_gemm_checked(const void* a, const void* b, W8A8Form form, int64_t T, int64_t N, int64_t K,
                            const float* scale_a, int64_t scale_a_numel, const float* scale_b,
                            int64_t scale_b_numel, const int32_t* azp, const int32_t* azp_adj,
                            const void* bias, qlin_dtype bias_dtype, void* out, qlin_dtype out_dtype,
@@ -423,7 +437,11 @@ qlin_status w8a8_gemm_checked(const int8_t* a, const void* b, bool b_f16, int64_
   epi.bias = raw ? nullptr : bias;
   epi.bias_dtype = bias_dtype;
   epi.out_dtype = out_dtype;
-  QLIN_LAUNCH(launch_w8a8_gemm(a, b, b_f16, T, N, K, epi, out, stream), "w8a8_gemm launch");
+  if (form == kW8F16) {
+    QLIN_LAUNCH(launch_w8a8_gemm_f16(a, b, T, N, K, epi, out, stream), "w8a8_gemm_f16 launch");
+  }
+  QLIN_LAUNCH(launch_w8a8_gemm(static_cast<const int8_t*>(a), b, form == kW8F16B, T, N, K, epi, out, stream),
+              "w8a8_gemm launch");
 }
 
 }  // namespace
@@ -435,7 +453,7 @@ qlin_status qlin_w8a8_gemm(const int8_t* a, const int8_t* b, int64_t T, int64_t 
                            int64_t scale_b_numel, const int32_t* azp, const int32_t* azp_adj,
                            const void* bias, qlin_dtype bias_dtype, void* out, qlin_dtype out_dtype,
                            cudaStream_t stream) {
-  return w8a8_gemm_checked(a, b, false, T, N, K, scale_a, scale_a_numel, scale_b, scale_b_numel, azp, azp_adj, bias,
+  return w8a8_gemm_checked(a, b, kW8I8, T, N, K, scale_a, scale_a_numel, scale_b, scale_b_numel, azp, azp_adj, bias,
                            bias_dtype, out, out_dtype, stream);
 }
 
@@ -444,8 +462,16 @@ qlin_status qlin_w8a8_gemm_f16b(const int8_t* a, const void* b16, int64_t T, int
                                 int64_t scale_b_numel, const int32_t* azp, const int32_t* azp_adj,
                                 const void* bias, qlin_dtype bias_dtype, void* out, qlin_dtype out_dtype,
                                 cudaStream_t stream) {
-  return w8a8_gemm_checked(a, b16, true, T, N, K, scale_a, scale_a_numel, scale_b, scale_b_numel, azp, azp_adj, bias,
+  return w8a8_gemm_checked(a, b16, kW8F16B, T, N, K, scale_a, scale_a_numel, scale_b, scale_b_numel, azp, azp_adj, bias,
                            bias_dtype, out, out_dtype, stream);
+}
+
+qlin_status qlin_w8a8_gemm_f16(const void* a16, const void* b16, int64_t T, int64_t N, int64_t K,
+                               const float* scale_a, int64_t scale_a_numel, const float* scale_b,
+                               int64_t scale_b_numel, const int32_t* azp, const int32_t* azp_adj, const void* bias,
+                               qlin_dtype bias_dtype, void* out, qlin_dtype out_dtype, cudaStream_t stream) {
+  return w8a8_gemm_checked(a16, b16, kW8F16, T, N, K, scale_a, scale_a_numel, scale_b, scale_b_numel, azp, azp_adj,
+                           bias, bias_dtype, out, out_dtype, stream);
 }
 
 qlin_status qlin_int8_to_f16(const int8_t* src, int64_t count, void* dst, cudaStream_t stream) {

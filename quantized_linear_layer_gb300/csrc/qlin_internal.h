@@ -67,7 +67,8 @@ cudaError_t launch_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int c
                                       const uint8_t* const* wq, const void* const* scales,
                                       const uint8_t* const* zeros, void* const* y, cudaStream_t stream);
 
-cudaError_t launch_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
+// q: int8 [T][K], or (f16_codes) the same codes as exact fp16 values [T][K].
+cudaError_t launch_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, void* q, bool f16_codes,
                                   float* scale, int32_t* azp, cudaStream_t stream);
 
 cudaError_t launch_int8_row_sum(const int8_t* b, int64_t N, int64_t K, int32_t* out, cudaStream_t stream);
@@ -87,6 +88,10 @@ struct W8A8Epilogue {
 // b: int8 [N][K], or (b_f16) the same codes as exact fp16 values [N][K].
 cudaError_t launch_w8a8_gemm(const int8_t* a, const void* b, bool b_f16, int64_t T, int64_t N, int64_t K,
                              const W8A8Epilogue& epi, void* out, cudaStream_t stream);
+
+// Both operands as exact fp16 codes: a16 fp16 [T][K], b16 fp16 [N][K].
+cudaError_t launch_w8a8_gemm_f16(const void* a16, const void* b16, int64_t T, int64_t N, int64_t K,
+                                 const W8A8Epilogue& epi, void* out, cudaStream_t stream);
 
 // dst[i] = fp16(src[i]) for int8 src (exact).
 cudaError_t launch_int8_to_f16(const int8_t* src, int64_t count, void* dst, cudaStream_t stream);

@@ -34,9 +34,11 @@ namespace {
 constexpr int kQuantThreads = 256;
 constexpr int kMaxVecPerThread = 4;  // 4 x 8 elements held in registers
 
-template <int DT, bool ASYM>
+// F16: the codes are written as the fp16 numbers of the same values (exact,
+// |q| <= 128), the operand form of the W8A8 GEMM that widens nothing on chip.
+template <int DT, bool ASYM, bool F16>
 __global__ void __launch_bounds__(kQuantThreads) quant_int8_rows_kernel(const void* __restrict__ x, int K,
-                                                                         int8_t* __restrict__ q,
+                                                                         void* __restrict__ q,
                                                                          float* __restrict__ scale,
                                                                          int32_t* __restrict__ azp) {
   pdl_launch_dependents();  // the GEMM that reads the codes may start setting up
@@ -44,7 +46,7 @@ __global__ void __launch_bounds__(kQuantThreads) quant_int8_rows_kernel(const vo
   const int tid = threadIdx.x;
   const int nvec = K / 8;
   const char* xr = static_cast<const char*>(x) + row * (int64_t)K * elem_bytes<DT>();
-  int8_t* qr = q + row * (int64_t)K;
+  unsigned char* qr = static_cast<unsigned char*>(q) + row * (int64_t)K * (F16 ? 2 : 1);
 
   float v[kMaxVecPerThread][8];
   // Running absmax (symmetric) or running min / max (asymmetric).  Both start
@@ -111,16 +113,30 @@ __global__ void __launch_bounds__(kQuantThreads) quant_int8_rows_kernel(const vo
   const bool rcp_ok = rcp_division_ok(s, rs);
 
   auto quant8 = [&](const float* t, int64_t idx) {
-    uint32_t w0 = 0, w1 = 0;
+    int r[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      int r = __float2int_rn(rcp_ok ? div_by_rcp(t[j], s, rs) : __fdiv_rn(t[j], s));
-      if (ASYM) r = min(max(r + z, -128), 127);
-      else r = min(max(r, -127), 127);
-      const uint32_t byte = static_cast<uint32_t>(r) & 0xffu;
-      if (j < 4) w0 |= byte << (8 * j); else w1 |= byte << (8 * (j - 4));
+      r[j] = __float2int_rn(rcp_ok ? div_by_rcp(t[j], s, rs) : __fdiv_rn(t[j], s));
+      if (ASYM) r[j] = min(max(r[j] + z, -128), 127);
+      else r[j] = min(max(r[j], -127), 127);
     }
-    *reinterpret_cast<uint2*>(qr + idx * 8) = make_uint2(w0, w1);
+    if (F16) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half2 h = __halves2half2(__int2half_rn(r[2 * j]), __int2half_rn(r[2 * j + 1]));
+        w[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(qr + idx * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t byte = static_cast<uint32_t>(r[j]) & 0xffu;
+        if (j < 4) w0 |= byte << (8 * j); else w1 |= byte << (8 * (j - 4));
+      }
+      *reinterpret_cast<uint2*>(qr + idx * 8) = make_uint2(w0, w1);
+    }
   };
 #pragma unroll
   for (int i = 0; i < kMaxVecPerThread; ++i) {
@@ -454,26 +470,35 @@ __global__ void quant_w4_g128_kernel(const void* __restrict__ w, int64_t N, int 
 // Launched without the programmatic-serialization attribute: the kernel reads
 // x at its start, with no griddepcontrol.wait before it, so it must not
 // overlap the kernel that writes x.
-cudaError_t launch_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, int8_t* q,
-                                  float* scale, int32_t* azp, cudaStream_t stream) {
-  if (T == 0) return cudaSuccess;
+namespace {
+template <bool F16>
+void quant_act_int8_dispatch(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, void* q, float* scale,
+                             int32_t* azp, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(T)), block(kQuantThreads);
   const int k = static_cast<int>(K);
   const bool asym = azp != nullptr;
   switch (x_dtype) {
     case QLIN_F16:
-      if (asym) quant_int8_rows_kernel<0, true><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
-      else quant_int8_rows_kernel<0, false><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
+      if (asym) quant_int8_rows_kernel<0, true, F16><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
+      else quant_int8_rows_kernel<0, false, F16><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
       break;
     case QLIN_BF16:
-      if (asym) quant_int8_rows_kernel<1, true><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
-      else quant_int8_rows_kernel<1, false><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
+      if (asym) quant_int8_rows_kernel<1, true, F16><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
+      else quant_int8_rows_kernel<1, false, F16><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
       break;
     default:
-      if (asym) quant_int8_rows_kernel<2, true><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
-      else quant_int8_rows_kernel<2, false><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
+      if (asym) quant_int8_rows_kernel<2, true, F16><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
+      else quant_int8_rows_kernel<2, false, F16><<<grid, block, 0, stream>>>(x, k, q, scale, azp);
       break;
   }
+}
+}  // namespace
+
+cudaError_t launch_quant_act_int8(const void* x, qlin_dtype x_dtype, int64_t T, int64_t K, void* q, bool f16_codes,
+                                  float* scale, int32_t* azp, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  if (f16_codes) quant_act_int8_dispatch<true>(x, x_dtype, T, K, q, scale, azp, stream);
+  else quant_act_int8_dispatch<false>(x, x_dtype, T, K, q, scale, azp, stream);
   return cudaGetLastError();
 }
 

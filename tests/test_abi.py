@@ -60,6 +60,12 @@ def test_rejects_bad_arguments_without_gpu(built):
     assert L.qlin_w8a8_gemm(P(16), P(16), 4, 8, 64, P(16), 3, P(16), 8, None, None, None, 0, P(16), 0, None) == 1
     assert L.qlin_w8a8_gemm(P(16), P(16), 4, 8, 64, P(16), 4, P(16), 8, P(16), None, None, 0, P(16), 0, None) == 1
     assert L.qlin_w8a8_gemm(P(16), P(16), 4, 8, 64, P(16), 4, P(16), 8, None, None, None, 0, P(16), 2, None) == 1
+    # the fp16-code forms take the same checks, and their own alignment
+    assert L.qlin_quant_act_int8_f16(P(16), 0, 4, 40, P(16), P(16), None, None) == 2
+    assert L.qlin_quant_act_int8_f16(P(16), 0, 4, 64, P(24), P(16), None, None) == 2
+    assert L.qlin_w8a8_gemm_f16(P(16), P(16), 4, 8, 64, P(16), 3, P(16), 8, None, None, None, 0, P(16), 0, None) == 1
+    assert L.qlin_w8a8_gemm_f16(P(16), P(16), 4, 8, 40, P(16), 4, P(16), 8, None, None, None, 0, P(16), 0, None) == 2
+    assert L.qlin_w8a8_gemm_f16(P(24), P(16), 4, 8, 64, P(16), 4, P(16), 8, None, None, None, 0, P(16), 0, None) == 2
     # NVFP4: S not a multiple of 16, K+S not a multiple of 32, GEMM K not a multiple of 64
     assert L.qlin_quant_nvfp4(P(16), 0, 4, 64, None, 8, 0, P(16), P(16), P(16), 0, None) == 1
     assert L.qlin_quant_nvfp4(P(16), 0, 4, 64, None, 16, 0, P(16), P(16), P(16), 0, None) == 2
@@ -173,6 +179,8 @@ def test_empty_problems_launch_nothing(built):
     assert L.qlin_w4a16_gemm_grouped(None, 1, 256, 2, n0, nul, nul, nul, 128, nul, None) == 0
     assert L.qlin_quant_act_int8(None, 0, 0, 64, None, None, None, None) == 0
     assert L.qlin_w8a8_gemm(None, None, 0, 8, 64, None, 1, None, 1, None, None, None, 0, None, 0, None) == 0
+    assert L.qlin_w8a8_gemm_f16(None, None, 0, 8, 64, None, 1, None, 1, None, None, None, 0, None, 0, None) == 0
+    assert L.qlin_quant_act_int8_f16(None, 0, 0, 64, None, None, None, None) == 0
     assert L.qlin_nvfp4_gemm(None, None, None, None, 4, 0, 64, None, None, None, 1, None) == 0
     assert L.qlin_quant_fp8(None, 0, 0, 64, None, None, None) == 0
     assert L.qlin_fp8_gemm(None, None, 0, 8, 64, None, None, None, 0, None, 0, None) == 0

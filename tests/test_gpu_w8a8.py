@@ -2,8 +2,10 @@
 (including adversarial extremes that bring each exact fp32 chunk to its
 2^24 bound), the four fused epilogues within the bf16/fp16 tolerance, and
 the two full-size workloads through the device quantizers.  Every GEMM test
-runs with the weights as int8 codes (qlin_w8a8_gemm) and as the same codes
-in fp16 (qlin_int8_to_f16 + qlin_w8a8_gemm_f16b)."""
+runs with the weights as int8 codes (qlin_w8a8_gemm), as the same codes in
+fp16 (qlin_int8_to_f16 + qlin_w8a8_gemm_f16b), and with both operands' codes
+in fp16 (qlin_w8a8_gemm_f16; on the full-size workloads the activation codes
+come from qlin_quant_act_int8_f16)."""
 
 import numpy as np
 import pytest
@@ -20,18 +22,26 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-BFORMS = ["i8", "f16"]
+BFORMS = ["i8", "f16", "f16ab"]
 
 
-def _gemm(q, bform, a, b, sa, sb, out, **kw):
-    """qlin_w8a8_gemm on int8 weights b, or qlin_w8a8_gemm_f16b on their
-    exact fp16 copy made by qlin_int8_to_f16."""
+def _f16(q, codes):
+    c16 = torch.empty(codes.shape, dtype=torch.float16, device="cuda")
+    q.qlin_int8_to_f16(codes, c16)
+    return c16
+
+
+def _gemm(q, bform, a, b, sa, sb, out, a16=None, **kw):
+    """qlin_w8a8_gemm on int8 codes; qlin_w8a8_gemm_f16b on the weights'
+    exact fp16 copy (qlin_int8_to_f16); or qlin_w8a8_gemm_f16 on fp16 copies
+    of both (a16: the activation codes already in fp16, e.g. from
+    qlin_quant_act_int8_f16)."""
     if bform == "i8":
         q.qlin_w8a8_gemm(a, b, sa, sb, out, **kw)
+    elif bform == "f16":
+        q.qlin_w8a8_gemm_f16b(a, _f16(q, b), sa, sb, out, **kw)
     else:
-        b16 = torch.empty(b.shape, dtype=torch.float16, device="cuda")
-        q.qlin_int8_to_f16(b, b16)
-        q.qlin_w8a8_gemm_f16b(a, b16, sa, sb, out, **kw)
+        q.qlin_w8a8_gemm_f16(_f16(q, a) if a16 is None else a16, _f16(q, b), sa, sb, out, **kw)
 
 
 def _raw(q, a, b, bform="i8"):
@@ -142,21 +152,39 @@ def _device_quant(q, x_np, asym):
     return aq, sa, za
 
 
+def _device_quant_f16(q, x_np, asym, aq, sa, za):
+    """qlin_quant_act_int8_f16 on the same rows: its codes, scales and
+    zero-points must equal qlin_quant_act_int8's exactly."""
+    xt = _dev(x_np)
+    t, k = x_np.shape
+    a16 = torch.empty((t, k), dtype=torch.float16, device="cuda")
+    sa16 = torch.empty(t, dtype=torch.float32, device="cuda")
+    za16 = torch.empty(t, dtype=torch.int32, device="cuda") if asym else None
+    q.qlin_quant_act_int8_f16(xt, a16, sa16, za16)
+    torch.cuda.synchronize()
+    assert torch.equal(a16.float(), aq.float())
+    assert torch.equal(sa16, sa)
+    if asym:
+        assert torch.equal(za16, za)
+    return a16
+
+
 @pytest.mark.parametrize("bform", BFORMS)
 def test_config3_symmetric_bias_bf16(qlin_gpu, bform):
     d = inputs.w8a8_sym_bias(seed=2)
     x32 = d["x"].astype(np.float32)
     aq, sa, _ = _device_quant(qlin_gpu, d["x"], asym=False)
     bq, sb, _ = _device_quant(qlin_gpu, d["w"], asym=False)
+    a16 = _device_quant_f16(qlin_gpu, d["x"], False, aq, sa, None) if bform == "f16ab" else None
     raq, rsa = oracle.quant_int8_sym(x32)
     rbq, rsb = oracle.quant_int8_sym(d["w"])
     assert np.array_equal(aq.cpu().numpy(), raq) and np.array_equal(bq.cpu().numpy(), rbq)
     dh = oracle.int8_gemm_exact(raq, rbq)
     raw = torch.empty((2048, 4096), dtype=torch.int32, device="cuda")
-    _gemm(qlin_gpu, bform, aq, bq, None, None, raw)
+    _gemm(qlin_gpu, bform, aq, bq, None, None, raw, a16=a16)
     assert np.array_equal(raw.cpu().numpy(), dh)
     out = torch.empty((2048, 4096), dtype=torch.bfloat16, device="cuda")
-    _gemm(qlin_gpu, bform, aq, bq, sa, sb, out, bias=_dev(d["bias"]))
+    _gemm(qlin_gpu, bform, aq, bq, sa, sb, out, a16=a16, bias=_dev(d["bias"]))
     torch.cuda.synchronize()
     assert qlin_gpu.qlin_get_device_error() == 0
     ref = oracle.w8a8_epilogue(dh, rsa, rsb, bias=d["bias"])
@@ -169,6 +197,7 @@ def test_config4_azp_per_token_f16(qlin_gpu, bform):
     x32 = d["x"].astype(np.float32)
     aq, sa, za = _device_quant(qlin_gpu, d["x"], asym=True)
     bq, sb, _ = _device_quant(qlin_gpu, d["w"], asym=False)
+    a16 = _device_quant_f16(qlin_gpu, d["x"], True, aq, sa, za) if bform == "f16ab" else None
     adj = torch.empty(d["w"].shape[0], dtype=torch.int32, device="cuda")
     qlin_gpu.qlin_int8_row_sum(bq, adj)
     raq, rsa, rza = oracle.quant_int8_asym(x32)
@@ -180,11 +209,38 @@ def test_config4_azp_per_token_f16(qlin_gpu, bform):
     dh = oracle.int8_gemm_exact(raq, rbq)
     for bias in (d["bias"], None):
         out = torch.empty((4096, 14336), dtype=torch.float16, device="cuda")
-        _gemm(qlin_gpu, bform, aq, bq, sa, sb, out, azp=za, azp_adj=adj, bias=None if bias is None else _dev(bias))
+        _gemm(qlin_gpu, bform, aq, bq, sa, sb, out, a16=a16, azp=za, azp_adj=adj,
+              bias=None if bias is None else _dev(bias))
         torch.cuda.synchronize()
         assert qlin_gpu.qlin_get_device_error() == 0
         ref = oracle.w8a8_epilogue(dh, rsa, rsb, azp=rza, azp_adj=radj, bias=bias)
         assert_within_tolerance(out.float().cpu().numpy(), ref, "config 4 bias=%s" % (bias is not None))
     raw = torch.empty((4096, 14336), dtype=torch.int32, device="cuda")
-    _gemm(qlin_gpu, bform, aq, bq, None, None, raw)
+    _gemm(qlin_gpu, bform, aq, bq, None, None, raw, a16=a16)
     assert np.array_equal(raw.cpu().numpy(), dh)
+
+
+@pytest.mark.parametrize("T,N,K", [(193, 264, 1552), (1, 8, 16), (300, 520, 3088), (128, 256, 1024)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
+def test_operand_forms_agree_bit_for_bit(qlin_gpu, T, N, K, out_dtype):
+    """The three operand forms compute the same D^ and apply the same
+    epilogue in the same order: their outputs are equal bit for bit (the
+    per-token zero-point form, with bias, on ragged tiles)."""
+    rng = np.random.default_rng(T + N + K)
+    x, w = _epilogue_case(rng, T, N, K)
+    aq, sa, za = oracle.quant_int8_asym(x + 0.5)
+    bq, sb = oracle.quant_int8_sym(w)
+    adj = oracle.azp_adj_from_weight(bq)
+    bias = (rng.standard_normal(N) * 0.1).astype(np.float32)
+    outs = []
+    for bform in BFORMS:
+        out = torch.empty((T, N), dtype=out_dtype, device="cuda")
+        _gemm(qlin_gpu, bform, _dev(aq), _dev(bq), _dev(sa), _dev(sb), out, azp=_dev(za), azp_adj=_dev(adj),
+              bias=_dev(bias))
+        torch.cuda.synchronize()
+        assert qlin_gpu.qlin_get_device_error() == 0
+        outs.append(out.cpu())
+    ref = oracle.w8a8_epilogue(oracle.int8_gemm_exact(aq, bq), sa, sb, azp=za, azp_adj=adj, bias=bias)
+    assert_within_tolerance(outs[0].float().numpy(), ref, "W8A8 forms %dx%dx%d" % (T, N, K))
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
