@@ -34,8 +34,10 @@
 // turns its codes of the 16 rows into exact fp16 (q - z) A fragments and runs
 // the m16n8k16 MMAs, accumulating each group in fp32 before scaling it by
 // s[n,g], then writes its partial sums into a slot of a reduction ring and
-// moves on.  Warp W + 1 (the reducer) adds the warps' sums of each stage in
-// warp order; with a cluster it sends them into the shared memory of the
+// moves on (one row of token sums per float2 store, tokens contiguous).  Warp
+// W + 1 (the reducer) adds the warps' sums of each stage, four tokens per
+// load, the even and the odd warps each in warp order and then the two
+// chains; with a cluster it sends them into the shared memory of the
 // rank that owns the stage (stage i: rank i mod C), and once the band is
 // done every rank adds the C sums of its stages in rank order.  So every
 // output element is the same sum in the same order on every run, and no CTA
@@ -60,7 +62,10 @@ constexpr int kSkTile = 16;           // rows per stage: one MMA tile
 // compute warps (plus the producer and the reducer): 16 with one token tile
 // (576 threads, 113 registers each), 14 with two (512 threads, 128 registers)
 __host__ __device__ constexpr int sk_max_warps(int NT) { return NT == 1 ? 16 : 14; }
-constexpr int kSkRedPitch = 20;       // floats per (warp, token) row of a reduction slot
+// Floats per (warp, row) of a reduction slot: the row's NT x 8 token sums,
+// padded so that the compute warps' float2 stores hit distinct banks within
+// each half warp.
+__host__ __device__ constexpr int sk_red_pitch(int NT) { return NT == 1 ? 8 : 24; }
 constexpr int kSkMinStages = 2, kSkMaxStages = 8;
 constexpr int kSkSiteFull = 1, kSkSiteEmpty = 2, kSkSiteDrain = 3, kSkSiteReady = 4, kSkSiteMeta = 5,
               kSkSiteRedFull = 6, kSkSiteRedEmpty = 7;
@@ -220,6 +225,9 @@ __global__ void __launch_bounds__((sk_max_warps(NT) + 2) * 32, 1) w4a16_skinny_k
   auto red_full = [&](int r) { return bar0 + 8u * (2 * S + r); };
   auto red_empty = [&](int r) { return bar0 + 8u * (2 * S + RS + r); };
   const uint32_t meta_full = bar0 + 8u * (2 * S + 2 * RS), meta_empty = meta_full + 8u, ready = meta_full + 16u;
+  // with a cluster: the last band's sums have all arrived and the compute
+  // warps may help add them (the reducer arrives)
+  const uint32_t final_go = meta_full + 32u;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + a.off_bar + 8 * (2 * S + 2 * RS) + 24);
   // A failed wait stops every later wait of the CTA (they return at once);
   // every arrive still happens, so no barrier count goes wrong.
@@ -242,12 +250,52 @@ __global__ void __launch_bounds__((sk_max_warps(NT) + 2) * 32, 1) w4a16_skinny_k
     tc::mbar_init(meta_full, 1);
     tc::mbar_init(meta_empty, W);
     tc::mbar_init(ready, C);
+    tc::mbar_init(final_go, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
   __syncthreads();
   if (C > 1) cluster_sync_all();  // every CTA's barriers exist before any remote arrive
   pdl_launch_dependents();
+
+  // With a cluster, once every rank's sums of band u (the CTA's kbb-th) have
+  // landed: this rank adds the C sums of each of its stages in rank order and
+  // stores them.  Worker `worker` of `nworkers` takes every nworkers-th of the
+  // rank's stages (the outputs do not depend on the split).
+  auto owner_sums = [&](int kbb, int u, int worker, int nworkers) {
+    int ur0, un;
+    sk_band(a, u, ur0, un);
+    const int Tp = (a.T + 3) & ~3, nq = Tp >> 2;
+    const int bufo = ((kbb & 1) % a.recv_bufs) * (C * a.slots * kSkTile * Tp);
+    const float4* rf = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(smem + a.off_recv) + bufo);
+    for (int cur = 0, i = 0; cur < un; ++i) {
+      int p, mfirst;
+      const int rows_i = sk_stage(a, ur0, un, cur, p, mfirst);
+      if (i % C == rank && (i / C) % nworkers == worker) {
+        const int off = kSkTile - rows_i, slot = i / C;
+        const int np = a.row_end[p] - mfirst;
+        __half* yp = a.y[p] + (ur0 + cur - off - mfirst);
+        for (int e = lane; e < kSkTile * nq; e += 32) {
+          const int rr = e & 15, tq = e >> 4;
+          if (rr >= off) {
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            for (int q = 0; q < C; ++q) {
+              const float4 w4 = rf[((q * a.slots + slot) * kSkTile + rr) * nq + tq];
+              v.x += w4.x;
+              v.y += w4.y;
+              v.z += w4.z;
+              v.w += w4.w;
+            }
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (4 * tq + j < a.T) yp[static_cast<int64_t>(4 * tq + j) * np + rr] = __float2half_rn(vv[j]);
+          }
+        }
+      }
+      cur += rows_i;
+    }
+  };
 
   if (warp == W) {
     // ---------------- producer: the band's scales, then its weight stages ----------------
@@ -303,7 +351,8 @@ __global__ void __launch_bounds__((sk_max_warps(NT) + 2) * 32, 1) w4a16_skinny_k
     return;
   }
 
-  const int red_slot = W * NT * 8 * kSkRedPitch;  // floats per reduction slot
+  constexpr int kRedPitch = sk_red_pitch(NT);
+  const int red_slot = W * kSkTile * kRedPitch;  // floats per reduction slot: [warp][row][token]
 
   if (warp == W + 1) {
     // ---------------- reducer: the warps' sums of each stage, in warp order ----------------
@@ -332,14 +381,22 @@ __global__ void __launch_bounds__((sk_max_warps(NT) + 2) * 32, 1) w4a16_skinny_k
         for (int e = lane; e < kSkTile * nq; e += 32) {
           const int rr = e & 15, t0 = (e >> 4) * 4;
           if (rr >= off) {
-            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            for (int w = 0; w < W; ++w) {
-              const float* pw = rb + (w * NT * 8 + t0) * kSkRedPitch + rr;
-              v.x += pw[0];
-              v.y += pw[kSkRedPitch];
-              v.z += pw[2 * kSkRedPitch];
-              v.w += pw[3 * kSkRedPitch];
+            // four tokens per load; even and odd warps in two chains, then
+            // added (a fixed order)
+            float4 v0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), v1 = v0;
+            const float* pr = rb + rr * kRedPitch + t0;
+            int w = 0;
+            for (; w + 1 < W; w += 2) {
+              const float4 a0 = *reinterpret_cast<const float4*>(pr + w * kSkTile * kRedPitch);
+              const float4 a1 = *reinterpret_cast<const float4*>(pr + (w + 1) * kSkTile * kRedPitch);
+              v0.x += a0.x; v0.y += a0.y; v0.z += a0.z; v0.w += a0.w;
+              v1.x += a1.x; v1.y += a1.y; v1.z += a1.z; v1.w += a1.w;
             }
+            if (w < W) {
+              const float4 a0 = *reinterpret_cast<const float4*>(pr + w * kSkTile * kRedPitch);
+              v0.x += a0.x; v0.y += a0.y; v0.z += a0.z; v0.w += a0.w;
+            }
+            const float4 v = make_float4(v0.x + v1.x, v0.y + v1.y, v0.z + v1.z, v0.w + v1.w);
             if (C == 1) {
               const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -365,38 +422,16 @@ __global__ void __launch_bounds__((sk_max_warps(NT) + 2) * 32, 1) w4a16_skinny_k
         __syncwarp();
         if (lane == 0)
           for (int q = 0; q < C; ++q) mbar_arrive_cluster(map_to_rank(ready, q));
-        const bool ok = sk_wait_cluster(ready, kb & 1, a.err, kSkSiteReady);
-        if (__all_sync(0xffffffffu, ok)) {
-          const float4* rf = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(smem + a.off_recv) + bufo);
-          for (int cur = 0, i = 0; cur < un; ++i) {
-            int p, mfirst;
-            const int rows_i = sk_stage(a, ur0, un, cur, p, mfirst);
-            if (i % C == rank) {
-              const int off = kSkTile - rows_i, slot = i / C;
-              const int np = a.row_end[p] - mfirst;
-              __half* yp = a.y[p] + (ur0 + cur - off - mfirst);
-              for (int e = lane; e < kSkTile * nq; e += 32) {
-                const int rr = e & 15, tq = e >> 4;
-                if (rr >= off) {
-                  float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                  for (int q = 0; q < C; ++q) {
-                    const float4 w4 = rf[((q * a.slots + slot) * kSkTile + rr) * nq + tq];
-                    v.x += w4.x;
-                    v.y += w4.y;
-                    v.z += w4.z;
-                    v.w += w4.w;
-                  }
-                  const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                  for (int j = 0; j < 4; ++j)
-                    if (4 * tq + j < a.T) yp[static_cast<int64_t>(4 * tq + j) * np + rr] = __float2half_rn(vv[j]);
-                }
-              }
-            }
-            cur += rows_i;
-          }
-        } else if (lane == 0) {
-          *abort_flag = 1;
+        const bool ok = __all_sync(0xffffffffu, sk_wait_cluster(ready, kb & 1, a.err, kSkSiteReady));
+        if (!ok && lane == 0) *abort_flag = 1;
+        if (u + a.NC >= a.NU) {
+          // the CTA's last band: the compute warps, done with their stages,
+          // take a share of the additions
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(final_go);
+          if (ok) owner_sums(kb, u, W, W + 1);
+        } else if (ok) {
+          owner_sums(kb, u, 0, 1);
         }
       }
     }
@@ -513,14 +548,12 @@ __global__ void __launch_bounds__((sk_max_warps(NT) + 2) * 32, 1) w4a16_skinny_k
       }
       // this warp's sums of the stage into a free reduction slot
       if (it >= RS) wait(red_empty(r), rph ^ 1u, kSkSiteRedEmpty);
-      float* rw = red + r * red_slot + warp * NT * 8 * kSkRedPitch;
+      float* rw = red + r * red_slot + warp * kSkTile * kRedPitch;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int t0 = nt * 8 + 2 * c;
-        rw[t0 * kSkRedPitch + g] = acc[nt][0];
-        rw[(t0 + 1) * kSkRedPitch + g] = acc[nt][1];
-        rw[t0 * kSkRedPitch + g + 8] = acc[nt][2];
-        rw[(t0 + 1) * kSkRedPitch + g + 8] = acc[nt][3];
+        *reinterpret_cast<float2*>(rw + g * kRedPitch + t0) = make_float2(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<float2*>(rw + (g + 8) * kRedPitch + t0) = make_float2(acc[nt][2], acc[nt][3]);
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(red_full(r));
@@ -533,6 +566,11 @@ __global__ void __launch_bounds__((sk_max_warps(NT) + 2) * 32, 1) w4a16_skinny_k
     // the band's staged scales are no longer read by this warp
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(meta_empty);
+  }
+  if (C > 1 && kb > 0) {
+    // help add the last band's sums once they have all arrived
+    const bool go = __all_sync(0xffffffffu, tc::mbar_wait(final_go, 0, a.err, kSkSiteReady));
+    if (go && !*abort_flag) owner_sums(kb - 1, cl + (kb - 1) * a.NC, warp, W + 1);
   }
 }
 
@@ -631,7 +669,7 @@ bool sk_layout(int64_t T, int64_t N, int64_t K, int C, int GPW, const SkDevice& 
   p.stage_bytes = kSkTile * p.pitch;
   auto up = [](int v, int m) { return (v + m - 1) / m * m; };
   p.RS = p.NT == 1 ? 4 : 2;
-  const int red_bytes = p.RS * p.W * p.NT * 8 * kSkRedPitch * 4;
+  const int red_bytes = p.RS * p.W * kSkTile * sk_red_pitch(p.NT) * 4;
   // bands: as few as fit the per-CTA budget of staged scales and received sums
   const int per_row = G * 2 + zpitch + (C > 1 ? 2 * (static_cast<int>(T) + 3) / 4 * 16 : 0);
   const int64_t rows_cl = (N + p.NC - 1) / p.NC;
@@ -647,7 +685,7 @@ bool sk_layout(int64_t T, int64_t N, int64_t K, int C, int GPW, const SkDevice& 
   const int raw_z_bytes = up(p.Umax * zpitch, 16) + 32 * kSkMaxGroup;
   const int Tp = (static_cast<int>(T) + 3) & ~3;
   const int recv_bytes = C > 1 ? p.recv_bufs * C * p.slots * kSkTile * Tp * 4 : 0;
-  const int bar_bytes = 8 * (2 * kSkMaxStages + 2 * p.RS) + 32;
+  const int bar_bytes = 8 * (2 * kSkMaxStages + 2 * p.RS) + 40;
   const int fixed = raw_s_bytes + raw_z_bytes + red_bytes + up(recv_bytes, 16) + 64 + bar_bytes + 128;
   const int cap = d.block_smem;
   const int bands_per_cl = static_cast<int>((p.NU + p.NC - 1) / p.NC);
@@ -660,7 +698,7 @@ bool sk_layout(int64_t T, int64_t N, int64_t K, int C, int GPW, const SkDevice& 
   p.off_recv = p.off_red + red_bytes;
   p.off_seg = up(p.off_recv + recv_bytes, 16);
   p.off_bar = p.off_seg + 64;
-  p.smem = p.off_bar + 8 * (2 * p.S + 2 * p.RS) + 32;
+  p.smem = p.off_bar + 8 * (2 * p.S + 2 * p.RS) + 40;
   // more than half of the SM, so that no two CTAs share one
   p.smem = std::max(p.smem, d.sm_smem / 2 - d.reserved + 16);
   if (p.smem > cap) return false;
