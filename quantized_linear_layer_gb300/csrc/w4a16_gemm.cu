@@ -206,11 +206,12 @@ __global__ void __launch_bounds__(256) w4a16_mma_kernel(const __half* __restrict
     uint32_t fa[8][4];
     const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
     const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
+    const UnpackConsts uk = unpack_consts();
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       uint32_t pa[4], pb[4];
-      unpack_word(wa[w], subA, addA, pa);
-      unpack_word(wb[w], subB, addB, pb);
+      unpack_word(wa[w], subA, addA, uk, pa);
+      unpack_word(wb[w], subB, addB, uk, pb);
       fa[2 * w][0] = pa[0]; fa[2 * w][1] = pb[0]; fa[2 * w][2] = pa[1]; fa[2 * w][3] = pb[1];
       fa[2 * w + 1][0] = pa[2]; fa[2 * w + 1][1] = pb[2]; fa[2 * w + 1][2] = pa[3]; fa[2 * w + 1][3] = pb[3];
     }

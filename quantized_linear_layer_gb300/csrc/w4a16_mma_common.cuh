@@ -44,17 +44,40 @@ __device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, uint32_t 
 __device__ __forceinline__ uint32_t zp_sub(uint32_t z) { return 0x64006400u | (z << 16) | z; }
 __device__ __forceinline__ uint32_t zp_add(uint32_t z) { return 0xD400D400u | (z << 20) | (z << 4); }
 
+// (a & b) | c in one three-input logic operation (lookup table 0xEA).  The
+// mask and the fp16 exponent are passed in registers: with two immediates
+// the compiler splits the operation in two.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// The unpack constants, kept in registers by the caller across a loop.
+struct UnpackConsts {
+  uint32_t lo, hi, ex;
+};
+__device__ __forceinline__ UnpackConsts unpack_consts() {
+  UnpackConsts k;
+  // opaque to constant folding, so that each stays one register
+  asm("mov.b32 %0, 0x000F000F;" : "=r"(k.lo));
+  asm("mov.b32 %0, 0x00F000F0;" : "=r"(k.hi));
+  asm("mov.b32 %0, 0x64006400;" : "=r"(k.ex));
+  return k;
+}
+
 // Exact fp16 (q - z) pairs from one word of eight codes.
 //   out[0] = (k, k+4), out[1] = (k+1, k+5), out[2] = (k+2, k+6), out[3] = (k+3, k+7)
 // 0x6400 is fp16 1024: OR-ing a nibble n into its low mantissa bits gives
 // 1024 + n, and 1024 + 16n for the nibble one position higher.
-__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t sub, uint32_t add, uint32_t* out) {
-  const uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u, kEx = 0x64006400u, kSixteenth = 0x2C002C00u;
-  out[0] = h2_sub((w & kLo) | kEx, sub);                 // (1024 + n) - (1024 + z)
-  out[1] = h2_fma((w & kHi) | kEx, kSixteenth, add);     // (1024 + 16n) / 16 - (64 + z)
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t sub, uint32_t add, const UnpackConsts& k,
+                                            uint32_t* out) {
+  const uint32_t kSixteenth = 0x2C002C00u;
+  out[0] = h2_sub(and_or(w, k.lo, k.ex), sub);                // (1024 + n) - (1024 + z)
+  out[1] = h2_fma(and_or(w, k.hi, k.ex), kSixteenth, add);    // (1024 + 16n) / 16 - (64 + z)
   const uint32_t w8 = w >> 8;
-  out[2] = h2_sub((w8 & kLo) | kEx, sub);
-  out[3] = h2_fma((w8 & kHi) | kEx, kSixteenth, add);
+  out[2] = h2_sub(and_or(w8, k.lo, k.ex), sub);
+  out[3] = h2_fma(and_or(w8, k.hi, k.ex), kSixteenth, add);
 }
 
 // Activation pairs (x[k+j], x[k+j+4]) for j = 0..3 from eight consecutive fp16.
@@ -70,14 +93,15 @@ __device__ __forceinline__ void pair_x(uint4 u, uint32_t* out) {
 // tile; xb[nt][w] holds the activation pairs of word w for token tile nt.
 template <int NT>
 __device__ __forceinline__ void group_mma(uint4 qa, uint4 qb, uint32_t subA, uint32_t addA, uint32_t subB,
-                                          uint32_t addB, const uint4 (*xb)[4], float (*p0)[4], float (*p1)[4]) {
+                                          uint32_t addB, const uint4 (*xb)[4], float (*p0)[4], float (*p1)[4],
+                                          const UnpackConsts& k) {
   const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
   const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
     uint32_t pa[4], pb[4];
-    unpack_word(wa[w], subA, addA, pa);
-    unpack_word(wb[w], subB, addB, pb);
+    unpack_word(wa[w], subA, addA, k, pa);
+    unpack_word(wb[w], subB, addB, k, pb);
     const uint32_t f0[4] = {pa[0], pb[0], pa[1], pb[1]};
     const uint32_t f1[4] = {pa[2], pb[2], pa[3], pb[3]};
 #pragma unroll

@@ -470,6 +470,7 @@ __global__ void __launch_bounds__((sk_max_warps(NT) + 2) * 32, 1) w4a16_skinny_k
       }
     }
 
+  const UnpackConsts uk = unpack_consts();
   int s = 0, r = 0, it = 0, kb = 0;
   uint32_t ph = 0, rph = 0;
   for (int u = cl; u < a.NU; u += a.NC, ++kb) {
@@ -528,7 +529,7 @@ __global__ void __launch_bounds__((sk_max_warps(NT) + 2) * 32, 1) w4a16_skinny_k
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
               for (int e = 0; e < 4; ++e) p0[nt][e] = p1[nt][e] = 0.0f;
-            group_mma<NT>(qa[j], qb[j], zp_sub(za[j]), zp_add(za[j]), zp_sub(zb[j]), zp_add(zb[j]), xb[j], p0, p1);
+            group_mma<NT>(qa[j], qb[j], zp_sub(za[j]), zp_add(za[j]), zp_sub(zb[j]), zp_add(zb[j]), xb[j], p0, p1, uk);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               acc[nt][0] = fmaf(fA, p0[nt][0] + p1[nt][0], acc[nt][0]);
