@@ -19,11 +19,9 @@
 // even and odd codes, and one dp4a per plane and parity gives
 // sum (n - z) . plane exactly in int32 (the zero-point enters once per chunk
 // as z . sum(plane)).  The plane sums are combined and scaled by s_g . s_x in
-// fp32.  The two high planes alone represent every x within 2^-15 of the
-// chunk's largest |x|; that is as fine as fp16 for every element above
-// max|x| / 16, and the low plane (error 2^-22 of max|x|) is added only for
-// chunks whose largest |x| exceeds 64 times the mean |x| of the others
-// (activation outliers), decided per warp.
+// fp32.  Every x is represented within 0.75 s_x = 2^-22.4 of its chunk's
+// largest |x|, finer than fp16 itself for every element above
+// max|x| . 2^-11, however the magnitudes within the chunk are spread.
 //
 // Data path for GB300.  One CTA per SM owns a contiguous band of weight rows;
 // the band is contiguous in HBM, so a single elected thread streams it into a
@@ -288,16 +286,13 @@ __global__ void __maxnreg__(kGvMaxRegs) w4a16_gemv_kernel(const GvArgs a) {
   if (warp == 0) pdl_wait();
   named_sync(1, nct);
   GvX X;
-  const bool wide_warp = gv_load_x(a.x, j, act, X);
+  gv_load_x(a.x, j, act, X);
   const uint32_t (*xp)[8] = X.xp;
   const int* xsum = X.xsum;
-  const float sx = X.sx, xzf = X.xzf;
+  const float sx = X.sx;
 
   const uint32_t sz_base = tc::smem_u32(sz + (jc >> 2));  // this thread's group column
-  // The consume loop, instantiated once per plane count so that the common
-  // two-plane loop does not keep the low plane live.
-  auto consume = [&](auto np) {
-    constexpr int NP = decltype(np)::value;
+  {
     // The reduction of one batch runs in the same block as the dot products
     // of the next, so that the shuffles' latency overlaps the dp4a work.
     float prev[kGvRowsPerBatch];
@@ -323,8 +318,8 @@ __global__ void __maxnreg__(kGvMaxRegs) w4a16_gemv_kernel(const GvArgs a) {
       }
       const int rows_i = min(a.R, nrows - i * a.R);
       float p[kGvRowsPerBatch];
-      gv_batch<NP, B>(ring + s * a.stage_bytes + jc * 16, sz_base + (i * a.R * G) * 4, rows_i, a.RG, rg, row_bytes, G, xp,
-                   xsum, xzf, sx, p);
+      gv_batch<B>(ring + s * a.stage_bytes + jc * 16, sz_base + (i * a.R * G) * 4, rows_i, a.RG, rg, row_bytes, G, xp,
+                  xsum, sx, p);
       // The stage's codes are in registers: hand it back to the producer.
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(empty(s));
@@ -339,11 +334,7 @@ __global__ void __maxnreg__(kGvMaxRegs) w4a16_gemv_kernel(const GvArgs a) {
       prev_rows = rows_i;
     }
     if (prev_row0 >= 0) reduce_store(prev, prev_row0, prev_rows);
-  };
-  if (wide_warp)
-    consume(std::integral_constant<int, 3>());
-  else
-    consume(std::integral_constant<int, 2>());
+  }
   named_sync(1, nct);
   if (*abort_flag) return;
   for (int r = threadIdx.x; r < nrows; r += nct) {

@@ -22,14 +22,11 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 // xp[p][2w] / xp[p][2w + 1] hold byte plane p of the even / odd codes of
 // word w.  The even codes are masked to bytes in place (w & 0x0F0F0F0F); the
 // odd ones stay in the high nibble of their byte (w & 0xF0F0F0F0 = 16 n) and
-// get their own accumulators, whose factor 16 is divided out in the fp32
-// combination.  Every partial sum is an exact integer below 2^20.
-//   NP = 2: the two high planes; the zero-point term z . sum(x_fix) (xzf,
-//           rounded to fp32) is subtracted in fp32.
-//   NP = 3: all three planes, the zero-point term subtracted per plane in
-//           int32 (exact), for chunks with activation outliers.
-template <int NP>
-__device__ __forceinline__ float gv_chunk(uint4 q, const uint32_t (*xp)[8], const int* xsum, float xzf, int z) {
+// get their own accumulators (multiples of 16, shifted back exactly).  Every
+// partial sum is an exact integer below 2^20, and the zero-point term
+// z . sum(plane) is subtracted per plane in int32, so the result is
+// sum (n - z) . x_fix exactly until the one conversion to fp32 per plane.
+__device__ __forceinline__ float gv_chunk(uint4 q, const uint32_t (*xp)[8], const int* xsum, int z) {
   int he = 0, ho = 0, me = 0, mo = 0, le = 0, lo = 0;
   const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -39,23 +36,13 @@ __device__ __forceinline__ float gv_chunk(uint4 q, const uint32_t (*xp)[8], cons
     ho = dp4a_us(od, xp[0][2 * w + 1], ho);
     me = dp4a_us(ev, xp[1][2 * w], me);
     mo = dp4a_us(od, xp[1][2 * w + 1], mo);
-    if (NP == 3) {
-      le = dp4a_us(ev, xp[2][2 * w], le);
-      lo = dp4a_us(od, xp[2][2 * w + 1], lo);
-    }
+    le = dp4a_us(ev, xp[2][2 * w], le);
+    lo = dp4a_us(od, xp[2][2 * w + 1], lo);
   }
-  if (NP == 2) {
-    const float d = fmaf(static_cast<float>(he), 65536.0f,
-                         fmaf(static_cast<float>(ho), 4096.0f,
-                              fmaf(static_cast<float>(me), 256.0f, static_cast<float>(mo) * 16.0f)));
-    return fmaf(-static_cast<float>(z), xzf, d);
-  } else {
-    // (odd sums are multiples of 16: the shifts are exact)
-    const int h = he + (ho >> 4) - z * xsum[0];
-    const int m = me + (mo >> 4) - z * xsum[1];
-    const int l = le + (lo >> 4) - z * xsum[2];
-    return fmaf(static_cast<float>(h), 65536.0f, fmaf(static_cast<float>(m), 256.0f, static_cast<float>(l)));
-  }
+  const int h = he + (ho >> 4) - z * xsum[0];
+  const int m = me + (mo >> 4) - z * xsum[1];
+  const int l = le + (lo >> 4) - z * xsum[2];
+  return fmaf(static_cast<float>(h), 65536.0f, fmaf(static_cast<float>(m), 256.0f, static_cast<float>(l)));
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -81,10 +68,9 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 // shared-window offsets: cbase = the thread's chunk in the stage, sbase = its
 // group's packed {scale, zero} of the stage's first row (fp16 scale bits in
 // the low half, the zero-point in the high half).
-template <int NP, int B>
+template <int B>
 __device__ __forceinline__ void gv_batch(uint32_t cbase, uint32_t sbase, int rows_i, int RG, int rg, int row_bytes,
-                                         int G, const uint32_t (*xp)[8], const int* xsum, float xzf, float sx,
-                                         float* p) {
+                                         int G, const uint32_t (*xp)[8], const int* xsum, float sx, float* p) {
   uint4 q[B];
   uint32_t m[B];
 #pragma unroll
@@ -96,7 +82,7 @@ __device__ __forceinline__ void gv_batch(uint32_t cbase, uint32_t sbase, int row
 #pragma unroll
   for (int b = 0; b < B; ++b) {
     const float sg = __half2float(__ushort_as_half(static_cast<unsigned short>(m[b] & 0xFFFFu)));
-    p[b] = (sg * sx) * gv_chunk<NP>(q[b], xp, xsum, xzf, static_cast<int>(m[b] >> 16));
+    p[b] = (sg * sx) * gv_chunk(q[b], xp, xsum, static_cast<int>(m[b] >> 16));
   }
 }
 
@@ -105,33 +91,24 @@ struct GvX {
   uint32_t xp[3][8];  // byte planes hi, mid, lo
   int xsum[3];        // plane sums over the chunk
   float sx;           // x = x_fix . sx
-  float xzf;          // sum(x_fix) of the two high planes, in fp32
 };
 
-// Builds the planes of a chunk from its 32 activations xf (when act).  Every
-// lane of the warp must call it; returns whether the warp needs the low plane
-// (a chunk with an activation outlier).
-__device__ __forceinline__ bool gv_build_planes(const float* xf, bool act, GvX& X) {
+// Builds the planes of a chunk from its 32 activations xf (when act):
+// x_fix = round(x / sx) with sx = max|x| / (127 . 2^15), so that
+// |x - x_fix . sx| <= 0.75 sx (the rounded quotient, 2^-22.4 of the chunk's
+// largest |x|: finer than fp16 for every element above max|x| . 2^-11), in
+// three signed base-256 digits.
+__device__ __forceinline__ void gv_build_planes(const float* xf, bool act, GvX& X) {
   uint32_t (&xp)[3][8] = X.xp;
   int (&xsum)[3] = X.xsum;
   xsum[0] = xsum[1] = xsum[2] = 0;
   float sx = 1.0f;
-  float amax = 0.0f, asum = 0.0f;
   if (act) {
-    // four partial maxima / sums (short dependency chains)
-    float pm[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // four partial maxima (short dependency chains)
+    float pm[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const float ax = fabsf(xf[t]);
-      pm[t & 3] = fmaxf(pm[t & 3], ax);
-      ps[t & 3] += ax;
-    }
-    amax = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
-    asum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-  }
-  // The low plane is built only in warps holding a chunk with an outlier.
-  const bool wide_warp = __any_sync(0xffffffffu, act && amax > (64.0f / 31.0f) * (asum - amax));
-  if (act) {
+    for (int t = 0; t < 32; ++t) pm[t & 3] = fmaxf(pm[t & 3], fabsf(xf[t]));
+    const float amax = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
     sx = amax > 0.0f ? amax * (1.0f / 4161536.0f) : 1.0f;   // 4161536 = 127 . 2^15
     const float inv = 1.0f / sx;
     // x_fix + 0x8080: byte 0 ^ 0x80 = lo, byte 1 ^ 0x80 = mid, byte 2 = hi.
@@ -146,32 +123,23 @@ __device__ __forceinline__ bool gv_build_planes(const float* xf, bool act, GvX& 
         const int e = 8 * w + par;  // elements e, e + 2, e + 4, e + 6
         const uint32_t hi01 = __byte_perm(vb[e], vb[e + 2], 0x0062), hi23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0062);
         const uint32_t md01 = __byte_perm(vb[e], vb[e + 2], 0x0051), md23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0051);
+        const uint32_t lo01 = __byte_perm(vb[e], vb[e + 2], 0x0040), lo23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0040);
         xp[0][2 * w + par] = __byte_perm(hi01, hi23, 0x5410);
         xp[1][2 * w + par] = __byte_perm(md01, md23, 0x5410) ^ 0x80808080u;
-        xp[2][2 * w + par] = 0u;
-        if (wide_warp) {
-          const uint32_t lo01 = __byte_perm(vb[e], vb[e + 2], 0x0040), lo23 = __byte_perm(vb[e + 4], vb[e + 6], 0x0040);
-          xp[2][2 * w + par] = __byte_perm(lo01, lo23, 0x5410) ^ 0x80808080u;
-        }
+        xp[2][2 * w + par] = __byte_perm(lo01, lo23, 0x5410) ^ 0x80808080u;
       }
     }
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
       xsum[0] = dp4a_us(0x01010101u, xp[0][w], xsum[0]);
       xsum[1] = dp4a_us(0x01010101u, xp[1][w], xsum[1]);
-    }
-    if (wide_warp) {
-#pragma unroll
-      for (int w = 0; w < 8; ++w) xsum[2] = dp4a_us(0x01010101u, xp[2][w], xsum[2]);
+      xsum[2] = dp4a_us(0x01010101u, xp[2][w], xsum[2]);
     }
   } else {
 #pragma unroll
     for (int w = 0; w < 8; ++w) xp[0][w] = xp[1][w] = xp[2][w] = 0u;
   }
   X.sx = sx;
-  // sum(x_fix) of the two high planes (what the two-plane dot products see)
-  X.xzf = fmaf(static_cast<float>(xsum[0]), 65536.0f, static_cast<float>(xsum[1]) * 256.0f);
-  return wide_warp;
 }
 
 // 32 fp16 activations as floats from four 16-byte words.
@@ -189,7 +157,7 @@ __device__ __forceinline__ void gv_unpack_x(const uint4* u, float* xf) {
 }
 
 // Chunk j of x (when act) read through L2 only, then its planes.
-__device__ __forceinline__ bool gv_load_x(const __half* x, int j, bool act, GvX& X) {
+__device__ __forceinline__ void gv_load_x(const __half* x, int j, bool act, GvX& X) {
   float xf[32];
   if (act) {
     const uint4* xg = reinterpret_cast<const uint4*>(x + j * 32);
@@ -198,11 +166,11 @@ __device__ __forceinline__ bool gv_load_x(const __half* x, int j, bool act, GvX&
     for (int w = 0; w < 4; ++w) u[w] = ldg_cg_v4(xg + w);
     gv_unpack_x(u, xf);
   }
-  return gv_build_planes(xf, act, X);
+  gv_build_planes(xf, act, X);
 }
 
 // Chunk j of an x staged in shared memory at xs (when act), then its planes.
-__device__ __forceinline__ bool gv_load_x_smem(uint32_t xs, int j, bool act, GvX& X) {
+__device__ __forceinline__ void gv_load_x_smem(uint32_t xs, int j, bool act, GvX& X) {
   float xf[32];
   if (act) {
     uint4 u[4];
@@ -210,7 +178,7 @@ __device__ __forceinline__ bool gv_load_x_smem(uint32_t xs, int j, bool act, GvX
     for (int w = 0; w < 4; ++w) u[w] = lds128(xs + j * 64 + w * 16);
     gv_unpack_x(u, xf);
   }
-  return gv_build_planes(xf, act, X);
+  gv_build_planes(xf, act, X);
 }
 
 // Sum over the 32 lanes of each of B row values v[0..B) (B a power of two),

@@ -350,15 +350,14 @@ __global__ void __launch_bounds__(kSqThreads, 1) w4a16_seq_kernel(const __grid_c
       }
     }
     GvX X;
-    const bool wide_warp = gv_load_x_smem(xs, j, act, X);
+    gv_load_x_smem(xs, j, act, X);
 
     int r0, nrows;
     sq_split(st.N, grid, cta, r0, nrows);
     const int nst = (nrows + R - 1) / R;
     const int st_base = nst ? nrows / nst : 0, st_extra = nst ? nrows % nst : 0;  // even split into stages
     bool ok = true;
-    auto consume = [&](auto np) {
-      constexpr int NP = decltype(np)::value;
+    {
       float prev[kSqB];
       int prev_row0 = -1, prev_rows = 0;
       auto reduce_store = [&](const float* v, int row0, int rows) {
@@ -381,8 +380,8 @@ __global__ void __launch_bounds__(kSqThreads, 1) w4a16_seq_kernel(const __grid_c
         float p[kSqB];
         if (active) {
           const uint32_t base = ring + slot * a.slot_bytes;
-          gv_batch<NP, kSqB>(base + jc * 16, base + L.pk + (jc >> 2) * 4, rows_i, RG, rg, row_bytes, G, X.xp,
-                             X.xsum, X.xzf, X.sx, p);
+          gv_batch<kSqB>(base + jc * 16, base + L.pk + (jc >> 2) * 4, rows_i, RG, rg, row_bytes, G, X.xp, X.xsum,
+                         X.sx, p);
         }
         // the stage is in registers: hand the slot back
         __syncwarp();
@@ -401,11 +400,7 @@ __global__ void __launch_bounds__(kSqThreads, 1) w4a16_seq_kernel(const __grid_c
         off += rows_i;
       }
       if (active && prev_row0 >= 0) reduce_store(prev, prev_row0, prev_rows);
-    };
-    if (wide_warp)
-      consume(std::integral_constant<int, 3>());
-    else
-      consume(std::integral_constant<int, 2>());
+    }
     if (named_sync_or(1, nct, !ok)) break;
     // outputs of this step: the warps' partial sums of each row, in order
     for (int r = threadIdx.x; r < nrows; r += nct) {

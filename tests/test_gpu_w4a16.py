@@ -111,6 +111,59 @@ def test_decode_activation_outliers(qlin_gpu, scale):
     assert_within_tolerance(y, ref, "W4A16 outliers x%g" % scale)
 
 
+def _plane_bound(x, codes, s16, z):
+    """Per-output error bound of the T = 1 GEMV's fixed-point activations.
+    Each 32-element chunk c is represented as x_fix . sx_c with
+    sx_c = max|x_c| / (127 . 2^15) and |x_fix - x / sx_c| <= 0.75 (the
+    rounded quotient), so every element is off by at most 0.75 . sx_c.  The
+    dot product of those errors with |s (q - z)|, plus the final fp16
+    rounding (2^-11 relative) and slack for the fp32 combination of the
+    plane sums, bounds |y - y_exact|."""
+    xf = x.astype(np.float64).reshape(-1)
+    k = xf.size
+    amax = np.abs(xf.reshape(k // 32, 32)).max(axis=1)
+    e = np.repeat(0.75 * amax / (127.0 * 2 ** 15), 32)
+    n = codes.shape[0]
+    w = np.abs((codes.reshape(n, k // 128, 128).astype(np.float64) - z[:, :, None]) * s16.astype(np.float64)[:, :, None])
+    w = w.reshape(n, k)
+    ref = oracle.w4a16_reference(x, codes, s16, z)[0]
+    return w @ e + 2.0 ** -11 * np.abs(ref) + 1e-6 * (w @ np.abs(xf)), ref
+
+
+@pytest.mark.parametrize("ratio", [16.0, 64.0, 1024.0])
+def test_decode_fixed_point_activations(qlin_gpu, ratio):
+    """The T = 1 GEMV rounds each 32-element chunk of x to fixed point on its
+    largest |x|.  Here every chunk has one element `ratio` times the mean |x|
+    of the other 31 (random signs), outputs are large (|ref| >> 1, so the
+    relative part of the tolerance is what bites), and in half of the rows
+    the large element's code equals the zero-point, so those outputs come
+    from the small elements alone, where the fixed point is coarsest
+    relative to the value.  Every output must lie within the error bound of
+    the representation (_plane_bound) and within the parity tolerance."""
+    rng = np.random.default_rng(71)
+    n, k = 512, 4096
+    small = rng.uniform(8.0, 24.0, size=(k // 32, 31)) * rng.choice([-1.0, 1.0], size=(k // 32, 31))
+    big = np.minimum(ratio * np.abs(small).mean(axis=1), 60000.0)
+    chunks = np.concatenate([big[:, None] * rng.choice([-1.0, 1.0], size=(k // 32, 1)), small], axis=1)
+    perm = rng.permuted(np.tile(np.arange(32), (k // 32, 1)), axis=1)
+    chunks = np.take_along_axis(chunks, perm, axis=1)
+    x = chunks.reshape(1, k).astype(np.float16)
+    xf = x.astype(np.float64).reshape(k // 32, 32)
+    d = inputs.w4a16_decode(seed=72, T=1, N=n, K=k)
+    # weights scaled so that the outputs are large but stay within fp16
+    codes, s16, z = oracle.quant_w4_g128(d["w"] * (50.0 if ratio <= 64 else 3.0))
+    big_cols = np.argmax(np.abs(xf), axis=1) + 32 * np.arange(k // 32)
+    codes[: n // 2, big_cols] = z[: n // 2, big_cols // 128]
+    bound, ref = _plane_bound(x, codes, s16, z)
+    assert np.abs(ref).max() < 60000.0
+    assert np.median(np.abs(ref)) > 100.0
+    y = _gemm(qlin_gpu, _dev(x), _dev(oracle.pack_u4(codes)), _dev(s16), _dev(oracle.pack_u4(z)))[0].astype(np.float64)
+    err = np.abs(y - ref)
+    worst = int(np.argmax(err - bound))
+    assert (err <= bound).all(), "row %d: err %g > bound %g (ref %g)" % (worst, err[worst], bound[worst], ref[worst])
+    assert_within_tolerance(y[None, :], ref[None, :], "W4A16 T=1 fixed point, ratio %g" % ratio)
+
+
 def test_decode_band_split_shapes(qlin_gpu):
     """Row counts that split unevenly over the CTAs and K with a partial last
     warp of 32-code chunks (K = 1408: 44 chunks)."""
