@@ -7,9 +7,12 @@ at every configuration the workload defines:
      16 tokens: 32 blocks x {q, k, v, o: 4096x4096; gate, up: 11008x4096;
      down: 4096x11008}, 224 fused dequant GEMVs / skinny GEMMs over 3.4 GB of
      int4 weights (larger than L2, so every pass streams the weights from
-     HBM), launched with the block's dependency structure: q, k, v grouped in
-     one launch on the block input, o on v's output, gate and up grouped on
-     o's output, down on up's output (4 launches per block).
+     HBM), run with the block's dependency structure: q, k, v grouped on the
+     block input, o on v's output, gate and up grouped on o's output, down on
+     up's output (4 dependent steps per block).  By default T = 1 runs as one
+     qlin_w4a16_chain call (a launch per step) and T = 4 and 16 as one
+     persistent qlin_w4a16_decode_run launch over all 128 steps (the plan is
+     prepared once at set-up); --w4a16-path picks one path for every T.
   2. W8A8 symmetric + bias (T=2048, K=4096, N=4096): per-token int8
      quantization of X, then the int8-exact GEMM with the fused epilogue.
      By default both operands' codes are stored as exact fp16 values (the
@@ -29,10 +32,10 @@ per-tensor scale and channel order are calibrated once on X at set-up.
 224 GEMVs / time of that phase); every configuration's rate, its roofline
 fraction and the CPU oracle's rate on the same configuration are in
 `paths`.  Each phase is a captured CUDA graph, timed with CUDA events on its
-stream.  `e2e` calls the public binding without graphs (the decode stacks
-through qlin_w4a16_chain, the C ABI's host work for every layer on the
-clock), with each phase's input copied from pinned host memory and its output
-read back inside the timed region.
+stream.  `e2e` calls the public binding without graphs (each decode stack
+through one qlin_w4a16_chain or qlin_w4a16_decode_run call, the C ABI's host
+work on the clock), with each phase's input copied from pinned host memory
+and its output read back inside the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -59,14 +62,28 @@ W8A8 = dict(T=2048, K=4096, N=4096)
 W8A8_AZP = dict(T=4096, K=4096, N=14336)
 NVFP4 = dict(T=2048, K=4096, N=4096, S=128)
 PATHS = ["w4a16_t1", "w4a16_t4", "w4a16_t16", "w8a8_sym", "w8a8_azp", "nvfp4"]
-KERNEL_OF = {"w4a16_t1": "w4a16_gemv_kernel", "w4a16_t4": "w4a16_skinny_kernel", "w4a16_t16": "w4a16_skinny_kernel",
-             "w8a8_sym": None, "w8a8_azp": None,
-             "nvfp4": "block_scaled_gemm_kernel<NVFP4>"}
+KERNEL_OF = {"w8a8_sym": None, "w8a8_azp": None, "nvfp4": "block_scaled_gemm_kernel<NVFP4>"}
+# W4A16 decode stacks: the path each token count takes by default ("auto"):
+# the per-layer launch chain at T = 1, the persistent decode plan above
+# (measured faster there; slower at T = 1, where its per-stage partial-sum
+# exchange costs more than the one-token GEMV's launch overlap)
+AUTO_W4_PATH = {1: "chain", 4: "plan", 16: "plan"}
+
+
+def w4_kernel(T, path):
+    """The kernel a W4A16 decode stack at T tokens runs on `path`."""
+    if path == "plan":
+        return "w4a16_decode_kernel"
+    if path == "sequence" and T == 1:
+        return "w4a16_seq_kernel"
+    return "w4a16_gemv_kernel" if T == 1 else "w4a16_skinny_kernel"
 CSRC = os.path.join(ROOT, "quantized_linear_layer_gb300", "csrc")
 # ncu DRAM-traffic summaries, each valid for the kernel sources it names
 TRAFFIC = {
     "w4a16_gemv_kernel": (os.path.join(ROOT, "profiles", "w4a16_decode_stack_traffic.txt"),
                           ["w4a16_gemv.cu", "w4a16_gemv_common.cuh"]),
+    "w4a16_decode_kernel": (os.path.join(ROOT, "profiles", "w4a16_decode_plan_traffic.txt"),
+                            ["w4a16_decode.cu", "w4a16_mma_common.cuh"]),
     "w4a16_skinny_kernel": (os.path.join(ROOT, "profiles", "w4a16_skinny_stack_traffic.txt"),
                             ["w4a16_skinny.cu", "w4a16_mma_common.cuh"]),
 }
@@ -159,7 +176,7 @@ class Workload:
     """Device-resident inputs, weights and outputs of one step, and the
     captured phases."""
 
-    def __init__(self, q, torch, layers, w4_path="chain", w8_form="f16"):
+    def __init__(self, q, torch, layers, w4_path="auto", w8_form="f16"):
         from quantized_linear_layer_gb300 import inputs
         self.q, self.torch = q, torch
         self.w8_form = w8_form
@@ -251,15 +268,25 @@ class Workload:
         self.nv_sfx = torch.empty(q.qlin_nvfp4_sf_bytes(T, K + S, q.QLIN_SF_MMA), dtype=torch.uint8, device=dev)
         self.nv_out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
         torch.cuda.synchronize()
-        self.w4_path = w4_path
+        self.w4_path = {T: (AUTO_W4_PATH[T] if w4_path == "auto" else w4_path) for T in W4_TOKENS}
+        if self.w4_path[4] == "sequence":
+            self.w4_path[4] = self.w4_path[16] = "chain"   # the sequence is a one-token path
         self.w4_steps = {T: self.w4a16_steps(T) for T in W4_TOKENS}
         self.w4_ws = torch.zeros(q.qlin_w4a16_sequence_workspace_bytes(len(self.w4_steps[1])), dtype=torch.uint8,
                                  device=dev)
+        # decode plans (written once at set-up; a run reads them)
+        self.w4_plan = {}
+        for T in W4_TOKENS:
+            if self.w4_path[T] == "plan":
+                ws = torch.zeros(q.qlin_w4a16_decode_workspace_bytes(len(self.w4_steps[T])), dtype=torch.uint8,
+                                 device=dev)
+                self.w4_plan[T] = (ws,) + q.qlin_w4a16_decode_prepare(self.w4_steps[T], ws)
+        torch.cuda.synchronize()
         # kernel launches per phase (the sequence: a workspace memset and one launch per 128 steps)
         n_seq = (len(self.w4_steps[1]) + 127) // 128
-        self.launches = {"w4a16_t1": n_seq if w4_path == "sequence" else 4 * layers,
-                         "w4a16_t4": 4 * layers, "w4a16_t16": 4 * layers,
-                         "w8a8_sym": 2, "w8a8_azp": 2, "nvfp4": 2}
+        per_path = {"sequence": n_seq, "plan": 1, "chain": 4 * layers, "launches": 4 * layers}
+        self.launches = {"w4a16_t%d" % T: per_path[self.w4_path[T]] for T in W4_TOKENS}
+        self.launches.update({"w8a8_sym": 2, "w8a8_azp": 2, "nvfp4": 2})
         self.phase = {"w4a16_t1": lambda: self.phase_w4a16(1), "w4a16_t4": lambda: self.phase_w4a16(4),
                       "w4a16_t16": lambda: self.phase_w4a16(16), "w8a8_sym": self.phase_w8a8,
                       "w8a8_azp": self.phase_w8a8_azp, "nvfp4": self.phase_nvfp4}
@@ -285,11 +312,17 @@ class Workload:
 
     # the phases, as plain launch sequences on the current stream
     def phase_w4a16(self, T):
-        if T == 1 and self.w4_path == "sequence":
+        path = self.w4_path[T]
+        if path == "plan":
+            # one persistent launch for the whole stack (the plan written at set-up)
+            ws, n, t = self.w4_plan[T]
+            self.q.qlin_w4a16_decode_run(ws, n, t)
+            return
+        if T == 1 and path == "sequence":
             # one persistent launch for the whole stack
             self.q.qlin_w4a16_gemv_sequence(self.w4_steps[1], self.w4_ws)
             return
-        if self.w4_path == "chain":
+        if path == "chain":
             # one call for the whole stack, a launch per step
             self.q.qlin_w4a16_chain(self.w4_steps[T])
             return
@@ -580,7 +613,8 @@ def run_ours(args):
         n = "w4a16_t%d" % T
         gbs = wl.w4_bytes[T] / phase[n] / 1e9
         paths[n] = {"ms": round(phase[n] * 1e3, 4), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4),
-                    "kernel": KERNEL_OF[n], "launches": wl.launches[n], "bytes": wl.w4_bytes[T],
+                    "kernel": w4_kernel(T, wl.w4_path[T]), "path": wl.w4_path[T], "launches": wl.launches[n],
+                    "bytes": wl.w4_bytes[T],
                     "e2e_ms": round(e2e_phase[n] * 1e3, 4), "host_enqueue_ms": round(e2e_host[n] * 1e3, 4)}
     for n in ("w8a8_sym", "w8a8_azp"):
         tops = ops[n] / phase[n] / 1e12
@@ -612,9 +646,11 @@ def run_ours(args):
         achieved = ops[dom] / phase[dom] / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4)}
-    kern = KERNEL_OF[dom] or W8A8_KERNEL[args.w8a8_form].split(" ")[0]
-    if dom == "w4a16_t1" and args.w4a16_path == "sequence":
-        kern = "w4a16_seq_kernel"
+    if dom.startswith("w4a16"):
+        T_dom = int(dom[len("w4a16_t"):])
+        kern = w4_kernel(T_dom, wl.w4_path[T_dom])
+    else:
+        kern = KERNEL_OF[dom] or W8A8_KERNEL[args.w8a8_form].split(" ")[0]
     roof.update({"kernel": kern, "phase": dom, "share_of_step": round(phase[dom] / sum(phase.values()), 4),
                  "traffic": recorded_traffic(kern),
                  "peak_source": ("measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "fallback")})
@@ -635,12 +671,15 @@ def run_ours(args):
         "config": {
             "workload": "W4A16 decode at T=1, 4 and 16 over a Llama-2-7B-shaped linear stack (%d blocks x 7 layers "
                         "with the block's dependencies: q,k,v grouped on the block input, o on v, gate,up grouped "
-                        "on o, down on up; 4 launches per block; %s) + W8A8 sym+bias T=2048 K=4096 N=4096 + W8A8 "
+                        "on o, down on up; %s) + W8A8 sym+bias T=2048 K=4096 N=4096 + W8A8 "
                         "azp per-token T=4096 K=4096 N=14336 + NVFP4 ARCQuant T=2048 K=4096 N=4096 S=128" %
-                        (args.layers, {"sequence": "T=1 as one persistent launch per 128 steps",
-                                       "chain": "one qlin_w4a16_chain call per stack",
-                                       "launches": "one grouped call per step"}[args.w4a16_path]),
-            "w4a16_path": args.w4a16_path,
+                        (args.layers, "; ".join("T=%d: %s" % (T, {
+                            "sequence": "one persistent GEMV launch per 128 steps",
+                            "chain": "one qlin_w4a16_chain call per stack (a launch per step)",
+                            "launches": "one grouped call per step",
+                            "plan": "one persistent qlin_w4a16_decode_run launch per stack"}[wl.w4_path[T]])
+                            for T in W4_TOKENS)),
+            "w4a16_path": {"T=%d" % T: wl.w4_path[T] for T in W4_TOKENS},
             "w8a8_form": args.w8a8_form,
             "w4a16_layers_per_step": len(wl.w4),
             "w4a16_weight_bytes_per_pass": wl.w4_bytes[1],
@@ -659,7 +698,8 @@ def run_ours(args):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "ms_per_step": round(sum(e2e_phase.values()) * 1e3, 4),
-            "how": "public binding without CUDA graphs (the W4A16 stacks through one qlin_w4a16_chain call each, "
+            "how": "public binding without CUDA graphs (the W4A16 stacks through one qlin_w4a16_chain or "
+                   "qlin_w4a16_decode_run call each, "
                    "the other phases one call per kernel step); each phase's input copied from pinned host memory "
                    "and its output read back inside the timed region",
         },
@@ -717,9 +757,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=32, help="transformer blocks in the W4A16 decode stack")
-    ap.add_argument("--w4a16-path", choices=["chain", "launches", "sequence"], default="chain",
+    ap.add_argument("--w4a16-path", choices=["auto", "chain", "launches", "sequence", "plan"], default="auto",
                     help="decode stacks as one qlin_w4a16_chain call (a launch per step), as one grouped call per "
-                         "step, or (T=1) as one persistent launch")
+                         "step, (T=1) as one persistent GEMV launch, as one persistent decode-plan launch, or "
+                         "(auto) the chain at T=1 and the plan at T=4 and 16")
     ap.add_argument("--w8a8-form", choices=["f16", "f16b", "i8"], default="f16",
                     help="W8A8 operand codes: both as exact fp16 values (qlin_quant_act_int8_f16 + "
                          "qlin_w8a8_gemm_f16), the weights only (qlin_w8a8_gemm_f16b), or int8 (qlin_w8a8_gemm)")

@@ -284,6 +284,53 @@ typedef struct {
 qlin_status qlin_w4a16_chain(const qlin_w4a16_step* steps, int nsteps, int64_t T, int64_t group,
                              cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * a1, decode plan - a decoder's W4A16 linears at 1 .. 16 tokens in one
+ * persistent launch on the tensor cores
+ *
+ * The same steps as qlin_w4a16_chain, at T <= 16, as one launch with
+ * exactly one CTA per SM ("Chapter 9 - Quantization kernels", 9.1: decode
+ * reads every weight once per token; 9.5 / 9.7: dequantize in registers
+ * right before the tensor core, weight rows as the MMA's M side).  Every CTA
+ * streams its share of every step's weights in step order, so the copies of
+ * a step are in flight while the step before it still computes; a counter
+ * per step in the workspace orders the steps' compute.  Per output:
+ *   Y[t,n] = sum_g s[n,g] . sum_{k in g} X[t,k] . (q[n,k] - z[n,g])
+ * with exact fp16 (q - z), fp32 products and sums, one fp16 rounding; the
+ * sums are taken in a fixed order (the same on every run), which differs
+ * from qlin_w4a16_gemm's (equal within the tolerance, not bit for bit).
+ *
+ * qlin_w4a16_decode_workspace_bytes(nsteps): bytes of a workspace for up to
+ *   nsteps steps (-1 for nsteps < 0).
+ * qlin_w4a16_decode_prepare: checks the steps and writes the plan into the
+ *   workspace with kernel launches on `stream` (no host synchronization):
+ *   the step table, one TMA tensor map per matrix, zeroed counters.  The
+ *   plan keeps the device pointers of the steps (x, wq, scales, zeros, y)
+ *   and is valid as long as they are; prepare it again when they change, or
+ *   after a run that left a code in the device error word.
+ *     steps      host array [nsteps], read during the call only, as for
+ *                qlin_w4a16_chain (x of step s fp16 [T][K_s], y[p] fp16
+ *                [T][N_p]; a step may read what an earlier step wrote; a
+ *                step's outputs must not overlap its own x)
+ *     T          1 .. 16 (QLIN_ERR_UNSUPPORTED otherwise)
+ *     group      128
+ *     workspace  device memory of qlin_w4a16_decode_workspace_bytes(nsteps)
+ *                bytes, 256-byte aligned, owned by the caller
+ *   QLIN_ERR_UNSUPPORTED when a CTA's share of a step's scales and
+ *   zero-points exceeds its 20 KB staging buffer (rows per SM x (K/64 +
+ *   K/256) bytes: about 224 rows per SM, 34 k rows in all, at K = 4096), or,
+ *   for K > 2048, a CTA's share exceeds 256 rows (its buffer of sums).
+ * qlin_w4a16_decode_run: runs a prepared plan on `stream` (one cooperative
+ *   launch).  nsteps and T must be the prepared ones (a mismatch is recorded
+ *   in the device error word and nothing runs).  Two runs of one workspace
+ *   must not overlap on the GPU (they share its counters); runs on one
+ *   stream follow one another and are safe.
+ * ---------------------------------------------------------------------- */
+int64_t qlin_w4a16_decode_workspace_bytes(int64_t nsteps);
+qlin_status qlin_w4a16_decode_prepare(const qlin_w4a16_step* steps, int nsteps, int64_t T, int64_t group,
+                                      void* workspace, cudaStream_t stream);
+qlin_status qlin_w4a16_decode_run(const void* workspace, int nsteps, int64_t T, cudaStream_t stream);
+
 int64_t qlin_w4a16_sequence_workspace_bytes(int64_t nsteps);
 qlin_status qlin_w4a16_gemv_sequence(const qlin_w4a16_step* steps, int nsteps, int64_t group, void* workspace,
                                      cudaStream_t stream);

@@ -22,7 +22,7 @@ __all__ = [
     "qlin_version", "qlin_get_device_error",
     "qlin_quant_w4_g128", "qlin_w4a16_gemm", "qlin_w4a16_gemm_grouped", "qlin_w4a16_step",
     "qlin_w4a16_sequence_workspace_bytes", "qlin_w4a16_gemv_sequence", "qlin_w4a16_gemv_sequence_noalloc",
-    "qlin_w4a16_chain",
+    "qlin_w4a16_chain", "qlin_w4a16_decode_workspace_bytes", "qlin_w4a16_decode_prepare", "qlin_w4a16_decode_run",
     "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm", "qlin_int8_to_f16", "qlin_w8a8_gemm_f16b",
     "qlin_quant_act_int8_f16", "qlin_w8a8_gemm_f16",
     "qlin_nvfp4_global_scale", "qlin_arc_perm", "qlin_quant_nvfp4", "qlin_nvfp4_gemm",
@@ -64,6 +64,9 @@ _SIGS = {
     "qlin_w4a16_gemv_sequence": ([_P, _I32, _I64, _P, _P], _I32),
     "qlin_w4a16_gemv_sequence_noalloc": ([_P, _I32, _I64, _P], _I32),
     "qlin_w4a16_chain": ([_P, _I32, _I64, _I64, _P], _I32),
+    "qlin_w4a16_decode_workspace_bytes": ([_I64], _I64),
+    "qlin_w4a16_decode_prepare": ([_P, _I32, _I64, _I64, _P, _P], _I32),
+    "qlin_w4a16_decode_run": ([_P, _I32, _I64, _P], _I32),
     "qlin_quant_act_int8": ([_P, _I32, _I64, _I64, _P, _P, _P, _P], _I32),
     "qlin_int8_row_sum": ([_P, _I64, _I64, _P, _P], _I32),
     "qlin_w8a8_gemm": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I32, _P], _I32),
@@ -275,6 +278,41 @@ def qlin_w4a16_chain(steps, group=128, stream=None):
     arr = _w4a16_steps(steps)
     _check("qlin_w4a16_chain", lib().qlin_w4a16_chain(ctypes.cast(arr, ctypes.c_void_p), len(steps), t, group,
                                                      _stream(stream)))
+
+
+def qlin_w4a16_decode_workspace_bytes(nsteps):
+    return lib().qlin_w4a16_decode_workspace_bytes(nsteps)
+
+
+def _chain_tokens(steps):
+    t = steps[0][0].shape[0]
+    for i, st in enumerate(steps):
+        if st[0].dim() != 2 or st[0].shape[0] != t or any(y.shape[0] != t for y in st[4]):
+            raise ValueError("step %d: every x and y must be [T][...] with the same T" % i)
+    return t
+
+
+def qlin_w4a16_decode_prepare(steps, workspace, group=128, stream=None):
+    """Write the decode plan of `steps` (as for qlin_w4a16_chain, T = x.shape[0] <= 16) into `workspace`
+    (uint8 CUDA tensor of qlin_w4a16_decode_workspace_bytes(len(steps)) bytes or more, 256-byte aligned).
+    Returns (nsteps, T) for qlin_w4a16_decode_run."""
+    torch = _torch()
+    _need(workspace, torch.uint8, name="workspace")
+    if not steps:
+        raise ValueError("at least one step")
+    t = _chain_tokens(steps)
+    need = qlin_w4a16_decode_workspace_bytes(len(steps))
+    if workspace.numel() < need:
+        raise ValueError("workspace has %d bytes, %d needed" % (workspace.numel(), need))
+    arr = _w4a16_steps(steps)
+    _check("qlin_w4a16_decode_prepare", lib().qlin_w4a16_decode_prepare(
+        ctypes.cast(arr, ctypes.c_void_p), len(steps), t, group, _ptr(workspace), _stream(stream)))
+    return len(steps), t
+
+
+def qlin_w4a16_decode_run(workspace, nsteps, T, stream=None):
+    """Run a plan written by qlin_w4a16_decode_prepare (nsteps and T as it returned)."""
+    _check("qlin_w4a16_decode_run", lib().qlin_w4a16_decode_run(_ptr(workspace), nsteps, T, _stream(stream)))
 
 
 def qlin_quant_act_int8(x, q, scale, azp=None, stream=None):

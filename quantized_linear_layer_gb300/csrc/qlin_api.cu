@@ -266,6 +266,46 @@ qlin_status qlin_w4a16_chain(const qlin_w4a16_step* steps, int nsteps, int64_t T
   return ok();
 }
 
+int64_t qlin_w4a16_decode_workspace_bytes(int64_t nsteps) { return w4a16_decode_workspace_bytes(nsteps); }
+
+qlin_status qlin_w4a16_decode_prepare(const qlin_w4a16_step* steps, int nsteps, int64_t T, int64_t group,
+                                      void* workspace, cudaStream_t stream) {
+  QLIN_REQUIRE(nsteps >= 1 && nsteps <= (1 << 20), QLIN_ERR_INVALID_ARG, "nsteps=%d outside [1, 2^20]", nsteps);
+  QLIN_REQUIRE(steps != nullptr, QLIN_ERR_INVALID_ARG, "null steps");
+  QLIN_REQUIRE(T >= 1 && T <= 16, QLIN_ERR_UNSUPPORTED, "T=%lld: the decode plan takes 1 .. 16 tokens", (long long)T);
+  QLIN_REQUIRE(workspace != nullptr, QLIN_ERR_INVALID_ARG, "null workspace");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, QLIN_ERR_ALIGNMENT,
+               "workspace must be 256-byte aligned");
+  char what[32];
+  for (int s = 0; s < nsteps; ++s) {
+    const qlin_w4a16_step& st = steps[s];
+    snprintf(what, sizeof(what), "step %d", s);
+    int64_t total = 0;
+    const qlin_status r = check_w4a16_group(what, st.x, T, st.K, st.count, st.N, st.wq, st.scales, st.y, group,
+                                            &total);
+    if (r != QLIN_OK) return r;
+    QLIN_REQUIRE(st.x != nullptr, QLIN_ERR_INVALID_ARG, "step %d: null x", s);
+  }
+  QLIN_DEVICE();
+  int bad = -1;
+  const char* why = w4a16_decode_check(steps, nsteps, T, &bad);
+  if (why != nullptr) return fail(QLIN_ERR_UNSUPPORTED, "step %d: %s", bad, why);
+  QLIN_LAUNCH(w4a16_decode_prepare(steps, nsteps, T, workspace, stream), "w4a16_decode_prepare");
+}
+
+qlin_status qlin_w4a16_decode_run(const void* workspace, int nsteps, int64_t T, cudaStream_t stream) {
+  QLIN_REQUIRE(nsteps >= 1 && nsteps <= (1 << 20), QLIN_ERR_INVALID_ARG, "nsteps=%d outside [1, 2^20]", nsteps);
+  QLIN_REQUIRE(T >= 1 && T <= 16, QLIN_ERR_UNSUPPORTED, "T=%lld: the decode plan takes 1 .. 16 tokens", (long long)T);
+  QLIN_REQUIRE(workspace != nullptr, QLIN_ERR_INVALID_ARG, "null workspace");
+  QLIN_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, QLIN_ERR_ALIGNMENT,
+               "workspace must be 256-byte aligned");
+  QLIN_DEVICE();
+  const cudaError_t e = w4a16_decode_run(workspace, nsteps, T, stream);
+  if (e == cudaErrorCooperativeLaunchTooLarge)
+    return fail(QLIN_ERR_UNSUPPORTED, "the device cannot hold one CTA per SM for the decode plan");
+  QLIN_LAUNCH(e, "w4a16_decode_run launch");
+}
+
 qlin_status qlin_w4a16_act_order_prepare(const int32_t* g_idx, int64_t K, int64_t group, const uint8_t* wq,
                                          int64_t N, int32_t* perm, uint8_t* wq_sorted, cudaStream_t stream) {
   QLIN_REQUIRE(group == 128, QLIN_ERR_UNSUPPORTED, "group size %lld (only 128 is built)", (long long)group);

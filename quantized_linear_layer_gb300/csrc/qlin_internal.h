@@ -45,6 +45,17 @@ cudaError_t launch_w4a16_sequence(const W4A16SeqStep* steps, int nsteps, unsigne
 // zeroes them first).  The address is looked up once per device, on the
 // first call with that device current.
 cudaError_t w4a16_sequence_static_workspace(unsigned int** out);
+// W4A16 decode plan (T <= 16): the steps of a chain in one persistent launch
+// on the warp-level tensor cores.  The workspace holds the plan: the step
+// table, one tensor map per matrix and one grid-barrier counter per step.
+int64_t w4a16_decode_workspace_bytes(int64_t nsteps);
+// nullptr when the steps fit the kernel's limits, else the reason (and the
+// failing step in *bad_step, -1 for T).
+const char* w4a16_decode_check(const qlin_w4a16_step* steps, int nsteps, int64_t T, int* bad_step);
+// Writes the plan into the workspace (stream-ordered kernel writes).
+cudaError_t w4a16_decode_prepare(const qlin_w4a16_step* steps, int nsteps, int64_t T, void* workspace,
+                                 cudaStream_t stream);
+cudaError_t w4a16_decode_run(const void* workspace, int nsteps, int64_t T, cudaStream_t stream);
 // Streamed tensor-core W4A16 for up to 16 tokens over the concatenated rows
 // of `count` matrices sharing x (false / cudaErrorInvalidValue when the
 // shape has no launch plan).

@@ -107,6 +107,25 @@ def test_rejects_bad_arguments_without_gpu(built):
     st[0].K, st[0].count = 256, 5
     assert L.qlin_w4a16_gemv_sequence(sp, 1, 128, P(16), None) == 1      # count above 4
     assert L.qlin_w4a16_gemv_sequence(None, 0, 128, None, None) == 0     # empty sequence
+    # W4A16 decode plan: workspace size; tokens outside 1 .. 16, null steps, no steps, null or
+    # misaligned workspace, K not a multiple of 128 (all before the device is touched)
+    assert L.qlin_w4a16_decode_workspace_bytes(-1) == -1
+    assert L.qlin_w4a16_decode_workspace_bytes(224) >= 224 * (4 * 128 + 4)
+    st[0].K, st[0].count = 256, 1
+    assert L.qlin_w4a16_decode_prepare(sp, 1, 17, 128, P(256), None) == 3
+    assert L.qlin_w4a16_decode_prepare(sp, 1, 0, 128, P(256), None) == 3
+    assert L.qlin_w4a16_decode_prepare(None, 1, 4, 128, P(256), None) == 1
+    assert L.qlin_w4a16_decode_prepare(sp, 0, 4, 128, P(256), None) == 1
+    assert L.qlin_w4a16_decode_prepare(sp, 1, 4, 128, None, None) == 1
+    assert L.qlin_w4a16_decode_prepare(sp, 1, 4, 128, P(272), None) == 2
+    st[0].K = 200
+    assert L.qlin_w4a16_decode_prepare(sp, 1, 4, 128, P(256), None) == 1
+    st[0].K = 256
+    assert L.qlin_w4a16_decode_prepare(sp, 1, 4, 64, P(256), None) == 3
+    assert L.qlin_w4a16_decode_run(P(256), 0, 4, None) == 1
+    assert L.qlin_w4a16_decode_run(P(256), 1, 17, None) == 3
+    assert L.qlin_w4a16_decode_run(P(272), 1, 4, None) == 2
+    assert L.qlin_w4a16_decode_run(None, 1, 4, None) == 1
     # FP8: K not a multiple of 16, bad dtype, misaligned x; GEMM out dtype, bias dtype,
     # misaligned b, out row pitch (N = 12: 24 bytes)
     assert L.qlin_quant_fp8(P(16), 0, 4, 40, P(16), P(16), None) == 2
