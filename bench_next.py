@@ -175,20 +175,21 @@ def _rows(q, torch):
 
     def had(kind, n):
         def setup():
-            T, K = 2048, 4096
-            xs = [randn(T, K) for _ in range(2)]
+            # 8192 x 8192 fp16 rows, three inputs in turn: 384 MB, larger than L2
+            T, K = 8192, 8192
+            xs = [randn(T, K) for _ in range(3)]
             y = torch.empty_like(xs[0])
             signs = (torch.randint(0, 2, (K,), device=dev, generator=g) * 2 - 1).to(torch.int8)
             it = [0]
 
             def run():
                 it[0] += 1
-                q.qlin_hadamard(xs[it[0] % 2], n, y=y, kind=kind, signs=signs)
+                q.qlin_hadamard(xs[it[0] % 3], n, y=y, kind=kind, signs=signs)
             return run, 4 * T * K, "hbm"
         return setup
     for kind, name in ((q.QLIN_HADAMARD_SYLVESTER, "sylvester"), (q.QLIN_HADAMARD_REGULAR, "regular")):
         for n in ((256, 4096) if name == "sylvester" else (64, 256)):
-            rows.append(("hadamard_%s_%d" % (name, n), "online Hadamard (%s, groups of %d), 2048 x 4096 fp16" % (name, n),
+            rows.append(("hadamard_%s_%d" % (name, n), "online Hadamard (%s, groups of %d), 8192 x 8192 fp16" % (name, n),
                          had(kind, n)))
     return rows
 

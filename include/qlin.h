@@ -684,10 +684,16 @@ qlin_status qlin_mx_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
  *     Hadamard, the Kronecker power of H4 = [[1,1,1,-1],[1,1,-1,1],
  *     [1,-1,1,1],[-1,1,1,1]], applied as radix-4 stages); n in {4, 16, 64,
  *     256}.
- * The stages run in float32; the result is within float32 rounding of the
- * exact rotation (before the final rounding to the input dtype) and the same
- * on every run.  The weights take the same rotation offline (W . Q), which
- * leaves X . W^T unchanged.
+ * F32 rows and the other group sizes run butterfly stages in float32: the
+ * result is within float32 rounding of the exact rotation (before the final
+ * rounding to the input dtype).  F16 / BF16 rows with n = 256 (both kinds)
+ * or a Sylvester n = 4096 run as 16 x 16 products on the tensor cores (the
+ * order-256 matrices are Kronecker squares of a 16 x 16 factor, ConvRot's
+ * dense product cut into factors): fp32 accumulation, intermediates kept to
+ * 16 significant bits, so the result is within about 2^-16 of the exact
+ * rotation's magnitude before the final rounding.  Every path gives the same
+ * bits on every run.  The weights take the same rotation offline (W . Q),
+ * which leaves X . W^T unchanged.
  *   x      [rows][K] of dtype (F16, BF16 or F32), 16-byte aligned
  *   signs  int8 [K] of +1 / -1 (8-byte aligned), or NULL
  *   y      out, [rows][K] of dtype, 16-byte aligned (y == x allowed)

@@ -11,18 +11,22 @@
 //     radix-4 stages at strides 1, 4, 16, ..., each quad (x0, x1, x2, x3)
 //     becoming y_i = s - 2 x_(3-i) with s = (x0 + x1) + (x2 + x3) (H4 is the
 //     all-ones matrix minus twice the anti-diagonal).
-// The stages run in float32, then one multiply by c = float32(1/sqrt(n)) and
-// the signs; the result is within float32 rounding of the exact rotation and
-// the same on every run.
+// fp32 rows, and other group sizes, run the stages in float32 on the CUDA
+// cores, then one multiply by c = float32(1/sqrt(n)) and the signs; the
+// result is within float32 rounding of the exact rotation.  Each thread holds
+// 8 consecutive elements; stages inside them run in registers, stages across
+// lanes by shuffles (Sylvester up to n = 256, the regular transform up to
+// 256), and Sylvester stages beyond 256 elements through shared memory, one
+// CTA of n/8 threads per group.  That form is bound by its shuffle and
+// add instructions (0.43-0.57 of HBM at n <= 256, 0.2 at n = 4096).
 //
-// HBM-bound (read and write the rows once; a few float32 operations per
-// element and stage), so no tensor cores: the pages' ConvRot multiplies by the
-// dense N0 x N0 matrix on tensor cores, 2 N0 flops per element, where the
-// butterflies need log2(N0).  Each thread holds 8 consecutive elements;
-// stages inside them run in registers, stages across lanes by shuffles
-// (Sylvester up to n = 256, the regular transform up to 256), and Sylvester
-// stages beyond 256 elements through shared memory, one CTA of n/8 threads
-// per group.
+// fp16 and bf16 rows with n = 256 (both matrices) or a Sylvester n = 4096 run
+// on the warp-level tensor cores instead, as the dense products of ConvRot's
+// formulation cut into Kronecker factors of order 16 (kernels below): the
+// arithmetic leaves the issue slots and the kernels stream at HBM speed.
+// There the intermediates are kept to 16 significant bits (a bf16 pair), so
+// the result is within about 2^-16 of the exact rotation's magnitude before
+// the final rounding, and the same on every run.
 //
 // The kernels do not trigger a programmatic dependent launch: the quantizers
 // that read the rotated rows are launched without it and read x at their
@@ -252,6 +256,327 @@ __global__ void __launch_bounds__(1024) hadamard_cta_kernel(const void* x, int64
   }
 }
 
+// ---- groups of 256 on the tensor cores (fp16 / bf16 rows) ----------------
+//
+// A group of 256 elements is a 16 x 16 matrix M (element 16 a + b at row a,
+// column b), and both Hadamard matrices of order 256 are Kronecker squares of
+// a symmetric 16 x 16 factor F (Sylvester: H16; regular: H4 (x) H4, ConvRot's
+// construction), so the rotated group is x . (F (x) F) = F . M . F, two
+// 16 x 16 products per group on the warp-level tensor cores:
+//   stage 1: Q = F . M      (A = F, constant; B = M, read with ldmatrix.trans
+//                            from the warp's shared-memory copy of the group)
+//   stage 2: Y = Q . F      (A = Q: the m16n8k16 accumulator of stage 1 has
+//                            the layout of the next A operand; B = F)
+// Products of +-1 with the fp16 / bf16 inputs are exact and the tensor core
+// accumulates in fp32.  Q enters stage 2 as a pair of bf16 values (hi and the
+// remainder Q - hi), 16 significant bits with fp32's range, so Y is within
+// about 2^-16 |Y| of the exact product before the one rounding to the output
+// type.  Per group a warp issues ~65 instructions (one 16-byte load and store
+// per lane, 6 MMAs), against several hundred for the shuffle butterflies.
+
+constexpr int kHmWarps = 8;           // warps per CTA
+constexpr int kHmBatch = 4;           // groups in flight per warp
+constexpr int kHmGroupBytes = 512;    // 256 elements of 2 bytes
+
+// F[i][j] of the 16 x 16 factor: Sylvester (-1)^popcount(i & j); regular the
+// product of H4 entries over the two base-4 digits (H4[r][c] = -1 exactly when
+// r + c == 3).
+__device__ __forceinline__ float hm_factor(int kind, int i, int j) {
+  if (kind == 0) return (__popc(i & j) & 1) ? -1.0f : 1.0f;
+  const bool neg = (((i >> 2) + (j >> 2)) == 3) != (((i & 3) + (j & 3)) == 3);
+  return neg ? -1.0f : 1.0f;
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t hm_pack(float lo, float hi) {
+  if constexpr (DT == 0) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// D = A . B + D, m16n8k16, fp32 accumulation; DT 0: fp16 operands, 1: bf16.
+template <int DT>
+__device__ __forceinline__ void hm_mma(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                       uint32_t b1) {
+  if constexpr (DT == 0)
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// (hi, lo) bf16 pairs of two floats: hi = bf16(v), lo = bf16(v - hi).
+__device__ __forceinline__ void hm_split(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+  hi = hm_pack<1>(v0, v1);
+  const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
+  lo = hm_pack<1>(__fsub_rn(v0, h0), __fsub_rn(v1, h1));
+}
+
+// Byte offset of the 16-byte half `h` of row r of a group's 16 x 32-byte
+// tile: the halves of rows 4-7 and 12-15 are swapped, so that the eight rows
+// an ldmatrix phase reads fall in distinct banks.
+__device__ __forceinline__ uint32_t hm_off(int r, int h) { return r * 32 + ((h ^ ((r >> 2) & 1)) << 4); }
+
+template <int DT, int KIND>
+__global__ void __launch_bounds__(kHmWarps * 32) hadamard256_mma_kernel(const void* x, int64_t groups, int K,
+                                                                        const int8_t* __restrict__ signs, void* y) {
+  __shared__ __align__(128) unsigned char tile[kHmWarps][kHmBatch][kHmGroupBytes];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  // F as the A operand (rows g, g + 8; columns 2c, 2c + 1, 2c + 8, 2c + 9)
+  // in the input type for stage 1, and in bf16 for stage 2's B operand (F is
+  // symmetric, so the same four words serve as the B fragments of both
+  // column tiles: b0/b1 of tile 0 = a0/a2, of tile 1 = a1/a3)
+  uint32_t fa[4], fb[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int r = g + 8 * (q & 1), k = 2 * c + 8 * (q >> 1);
+    const float f0 = hm_factor(KIND, r, k), f1 = hm_factor(KIND, r, k + 1);
+    fa[q] = hm_pack<DT>(f0, f1);
+    fb[q] = hm_pack<1>(f0, f1);
+  }
+  const float scale = 1.0f / 16.0f;  // 1 / sqrt(256), exact
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kHmWarps;
+  const char* xb = static_cast<const char*>(x);
+  char* yb = static_cast<char*>(y);
+  const uint32_t tbase = static_cast<uint32_t>(__cvta_generic_to_shared(&tile[warp][0][0]));
+  // ldmatrix.x4.trans row addresses: matrix i = lane / 8 covers rows
+  // 8 (i & 1) .. + 7 and column half i >> 1; this lane gives row (lane % 8)
+  const int lm_row = (lane & 7) + 8 * ((lane >> 3) & 1), lm_half = lane >> 4;
+  for (int64_t g0 = (static_cast<int64_t>(blockIdx.x) * kHmWarps + warp) * kHmBatch; g0 < groups;
+       g0 += nwarps * kHmBatch) {
+    uint4 in[kHmBatch];
+#pragma unroll
+    for (int b = 0; b < kHmBatch; ++b)
+      if (g0 + b < groups) in[b] = *reinterpret_cast<const uint4*>(xb + (g0 + b) * kHmGroupBytes + lane * 16);
+    __syncwarp();  // the previous batch's output reads of the tile are done
+#pragma unroll
+    for (int b = 0; b < kHmBatch; ++b)
+      if (g0 + b < groups) {
+        const uint32_t a = tbase + b * kHmGroupBytes + hm_off(lane >> 1, lane & 1);
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(in[b].x), "r"(in[b].y), "r"(in[b].z),
+                     "r"(in[b].w)
+                     : "memory");
+      }
+    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < kHmBatch; ++b) {
+      if (g0 + b >= groups) break;
+      const uint32_t tb = tbase + b * kHmGroupBytes;
+      uint32_t m0, m1, m2, m3;  // B fragments of M: (rows 0-7 | 8-15) x (columns 0-7 | 8-15)
+      asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(m0), "=r"(m1), "=r"(m2), "=r"(m3)
+                   : "r"(tb + hm_off(lm_row, lm_half)));
+      // stage 1: Q = F . M, column tiles 0-7 and 8-15
+      float q0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, q1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      hm_mma<DT>(q0, fa[0], fa[1], fa[2], fa[3], m0, m1);
+      hm_mma<DT>(q1, fa[0], fa[1], fa[2], fa[3], m2, m3);
+      // stage 2: Y = Q . F with Q as A fragments (rows g, g + 8; columns
+      // 2c.. of tile 0, then of tile 1), hi and lo parts
+      uint32_t ah[4], al[4];
+      hm_split(q0[0], q0[1], ah[0], al[0]);
+      hm_split(q0[2], q0[3], ah[1], al[1]);
+      hm_split(q1[0], q1[1], ah[2], al[2]);
+      hm_split(q1[2], q1[3], ah[3], al[3]);
+      float y0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, y1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      hm_mma<1>(y0, al[0], al[1], al[2], al[3], fb[0], fb[2]);
+      hm_mma<1>(y0, ah[0], ah[1], ah[2], ah[3], fb[0], fb[2]);
+      hm_mma<1>(y1, al[0], al[1], al[2], al[3], fb[1], fb[3]);
+      hm_mma<1>(y1, ah[0], ah[1], ah[2], ah[3], fb[1], fb[3]);
+      // Y[g][2c..], Y[g+8][2c..] of each column tile back into the tile,
+      // scaled and rounded (the column signs come after the transpose)
+      const uint32_t o00 = hm_pack<DT>(y0[0] * scale, y0[1] * scale), o01 = hm_pack<DT>(y0[2] * scale, y0[3] * scale);
+      const uint32_t o10 = hm_pack<DT>(y1[0] * scale, y1[1] * scale), o11 = hm_pack<DT>(y1[2] * scale, y1[3] * scale);
+      __syncwarp();  // every lane's ldmatrix of this group is done
+      asm volatile("st.shared.u32 [%0], %1;" ::"r"(tb + hm_off(g, 0) + 4 * c), "r"(o00) : "memory");
+      asm volatile("st.shared.u32 [%0], %1;" ::"r"(tb + hm_off(g + 8, 0) + 4 * c), "r"(o01) : "memory");
+      asm volatile("st.shared.u32 [%0], %1;" ::"r"(tb + hm_off(g, 1) + 4 * c), "r"(o10) : "memory");
+      asm volatile("st.shared.u32 [%0], %1;" ::"r"(tb + hm_off(g + 8, 1) + 4 * c), "r"(o11) : "memory");
+    }
+    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < kHmBatch; ++b) {
+      if (g0 + b >= groups) break;
+      uint4 o;
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(o.x), "=r"(o.y), "=r"(o.z), "=r"(o.w)
+                   : "r"(tbase + b * kHmGroupBytes + hm_off(lane >> 1, lane & 1))
+                   : "memory");
+      const int64_t e0 = (g0 + b) * 256 + lane * 8;  // first element of this lane's 8
+      if (signs != nullptr) {
+        // a -1 sign flips the sign bit of the element (exact)
+        const uint2 sg = __ldg(reinterpret_cast<const uint2*>(signs + e0 % K));
+        uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t sb = (i < 4 ? sg.x : sg.y) >> (8 * (i & 3));
+          if (sb & 0x80u) w[i >> 1] ^= 0x8000u << (16 * (i & 1));
+        }
+        o = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      *reinterpret_cast<uint4*>(yb + e0 * 2) = o;
+    }
+  }
+}
+
+// ---- Sylvester groups of 4096 on the tensor cores (fp16 / bf16 rows) ------
+//
+// H_4096 = H16 (x) H_256: with the group cut into 16 sub-blocks x_a of 256,
+//   y[256 c + j] = sum_a H16[a][c] . Z_a[j],   Z_a = x_a . H_256 = F . M_a . F,
+// so each warp rotates two sub-blocks exactly as above (unnormalized), the
+// CTA collects Z (16 x 256, as bf16 hi and lo parts) in shared memory, and a
+// third 16 x 16 product Y = F . Z combines the sub-blocks, each warp 32 of
+// the 256 columns.  One CTA per group at a time; the next group's input is
+// loaded while the current one is rotated.
+
+constexpr int kH4Warps = 8;
+
+// Byte offset of element (row r, column j) of a 16 x 256 bf16 / fp16 matrix
+// (512-byte rows) with its 16-byte chunks permuted by (r & 7), so that eight
+// rows of one chunk column fall in distinct banks.
+__device__ __forceinline__ uint32_t h4_off(int r, int j) {
+  return r * 512 + ((((j >> 3) ^ (r & 7))) << 4) + (j & 7) * 2;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kH4Warps * 32) hadamard4096_mma_kernel(const void* x, int64_t groups, int K,
+                                                                         const int8_t* __restrict__ signs, void* y) {
+  __shared__ __align__(128) unsigned char stage[kH4Warps][2][kHmGroupBytes];  // inputs, then the output rows
+  __shared__ __align__(128) unsigned char zbuf[2][16 * 512];                 // Z as bf16: hi, lo
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  uint32_t fa[4], fb[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int r = g + 8 * (q & 1), k = 2 * c + 8 * (q >> 1);
+    const float f0 = hm_factor(0, r, k), f1 = hm_factor(0, r, k + 1);
+    fa[q] = hm_pack<DT>(f0, f1);
+    fb[q] = hm_pack<1>(f0, f1);
+  }
+  const float scale = 1.0f / 64.0f;  // 1 / sqrt(4096), exact
+  const char* xb = static_cast<const char*>(x);
+  char* yb = static_cast<char*>(y);
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(&stage[warp][0][0]));
+  const uint32_t sall = static_cast<uint32_t>(__cvta_generic_to_shared(&stage[0][0][0]));
+  const uint32_t zb = static_cast<uint32_t>(__cvta_generic_to_shared(&zbuf[0][0]));
+  const int lm_row = (lane & 7) + 8 * ((lane >> 3) & 1), lm_half = lane >> 4;
+  int64_t gi = blockIdx.x;
+  uint4 in[2];
+  if (gi < groups) {
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb)
+      in[sb] = *reinterpret_cast<const uint4*>(xb + gi * 8192 + (2 * warp + sb) * kHmGroupBytes + lane * 16);
+  }
+  for (; gi < groups; gi += gridDim.x) {
+    // this warp's two sub-blocks into its staging tiles; the next group's load in flight
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+      const uint32_t a = sbase + sb * kHmGroupBytes + hm_off(lane >> 1, lane & 1);
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(in[sb].x), "r"(in[sb].y), "r"(in[sb].z),
+                   "r"(in[sb].w)
+                   : "memory");
+    }
+    const int64_t gn = gi + gridDim.x;
+    if (gn < groups) {
+#pragma unroll
+      for (int sb = 0; sb < 2; ++sb)
+        in[sb] = *reinterpret_cast<const uint4*>(xb + gn * 8192 + (2 * warp + sb) * kHmGroupBytes + lane * 16);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+      const int a = 2 * warp + sb;
+      uint32_t m0, m1, m2, m3;
+      asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(m0), "=r"(m1), "=r"(m2), "=r"(m3)
+                   : "r"(sbase + sb * kHmGroupBytes + hm_off(lm_row, lm_half)));
+      float q0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, q1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      hm_mma<DT>(q0, fa[0], fa[1], fa[2], fa[3], m0, m1);
+      hm_mma<DT>(q1, fa[0], fa[1], fa[2], fa[3], m2, m3);
+      uint32_t ah[4], al[4];
+      hm_split(q0[0], q0[1], ah[0], al[0]);
+      hm_split(q0[2], q0[3], ah[1], al[1]);
+      hm_split(q1[0], q1[1], ah[2], al[2]);
+      hm_split(q1[2], q1[3], ah[3], al[3]);
+      float y0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, y1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      hm_mma<1>(y0, al[0], al[1], al[2], al[3], fb[0], fb[2]);
+      hm_mma<1>(y0, ah[0], ah[1], ah[2], ah[3], fb[0], fb[2]);
+      hm_mma<1>(y1, al[0], al[1], al[2], al[3], fb[1], fb[3]);
+      hm_mma<1>(y1, ah[0], ah[1], ah[2], ah[3], fb[1], fb[3]);
+      // Z_a[j] for j = 16 g + 2c (+1), 16 (g + 8) + 2c, then 8 columns on
+      const float zv[4][2] = {{y0[0], y0[1]}, {y0[2], y0[3]}, {y1[0], y1[1]}, {y1[2], y1[3]}};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int j = 16 * (g + 8 * (p & 1)) + 8 * (p >> 1) + 2 * c;
+        uint32_t hi, lo;
+        hm_split(zv[p][0], zv[p][1], hi, lo);
+        const uint32_t o = h4_off(a, j);
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(zb + o), "r"(hi) : "memory");
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(zb + 16 * 512 + o), "r"(lo) : "memory");
+      }
+    }
+    __syncthreads();  // Z complete; every warp's staging tiles free
+    // Y = F . Z on this warp's columns 32 w .. 32 w + 31 (four column tiles)
+#pragma unroll
+    for (int t = 0; t < 4; t += 2) {
+      const int j0 = 32 * warp + 8 * t;
+      // matrices: rows 0-7 | 8-15 of columns j0.. and j0 + 8..
+      const int r = (lane & 7) + 8 * ((lane >> 3) & 1), jj = j0 + 8 * (lane >> 4);
+      uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+      asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+                   : "r"(zb + h4_off(r, jj)));
+      asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(l0), "=r"(l1), "=r"(l2), "=r"(l3)
+                   : "r"(zb + 16 * 512 + h4_off(r, jj)));
+      float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      hm_mma<1>(d0, fb[0], fb[1], fb[2], fb[3], l0, l1);
+      hm_mma<1>(d0, fb[0], fb[1], fb[2], fb[3], h0, h1);
+      hm_mma<1>(d1, fb[0], fb[1], fb[2], fb[3], l2, l3);
+      hm_mma<1>(d1, fb[0], fb[1], fb[2], fb[3], h2, h3);
+      // y[256 c_out + j], c_out = g, g + 8, j = j0 (+8) + 2c: scaled, rounded,
+      // into the output rows (the staging area, 16 rows of 512 bytes)
+      const float dv[4][2] = {{d0[0], d0[1]}, {d0[2], d0[3]}, {d1[0], d1[1]}, {d1[2], d1[3]}};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int co = g + 8 * (p & 1), j = j0 + 8 * (p >> 1) + 2 * c;
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(sall + h4_off(co, j)),
+                     "r"(hm_pack<DT>(dv[p][0] * scale, dv[p][1] * scale))
+                     : "memory");
+      }
+    }
+    __syncthreads();  // the output rows are complete; Z may be overwritten
+    // this warp writes output rows 2w and 2w + 1 (1 KB, 16 bytes per lane per row)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int row = 2 * warp + rr;
+      uint4 o;
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(o.x), "=r"(o.y), "=r"(o.z), "=r"(o.w)
+                   : "r"(sall + h4_off(row, 8 * lane))
+                   : "memory");
+      const int64_t e0 = gi * 4096 + row * 256 + 8 * lane;
+      if (signs != nullptr) {
+        const uint2 sg = __ldg(reinterpret_cast<const uint2*>(signs + e0 % K));
+        uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t sb = (i < 4 ? sg.x : sg.y) >> (8 * (i & 3));
+          if (sb & 0x80u) w[i >> 1] ^= 0x8000u << (16 * (i & 1));
+        }
+        o = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      *reinterpret_cast<uint4*>(yb + e0 * 2) = o;
+    }
+    __syncthreads();  // the output rows are read before the next group's inputs land there
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_hadamard(const void* x, qlin_dtype dtype, int64_t rows, int64_t K, qlin_hadamard_kind kind,
@@ -261,6 +586,27 @@ cudaError_t launch_hadamard(const void* x, qlin_dtype dtype, int64_t rows, int64
   const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
   auto go = [&](auto dt) -> cudaError_t {
     constexpr int DT = decltype(dt)::value;
+    if constexpr (DT != 2) {
+      if (n == 256) {
+        // tensor cores: 4 CTAs of 8 warps per SM, each warp 4 groups at a time
+        const int64_t groups = rows * (K / 256);
+        const int64_t want = (groups + kHmWarps * kHmBatch - 1) / (kHmWarps * kHmBatch);
+        const int64_t cap4 = static_cast<int64_t>(sm_count()) * 4;
+        const unsigned grid = static_cast<unsigned>(want < cap4 ? want : cap4);
+        if (kind == QLIN_HADAMARD_SYLVESTER)
+          hadamard256_mma_kernel<DT, 0><<<grid, kHmWarps * 32, 0, stream>>>(x, groups, static_cast<int>(K), signs, y);
+        else
+          hadamard256_mma_kernel<DT, 1><<<grid, kHmWarps * 32, 0, stream>>>(x, groups, static_cast<int>(K), signs, y);
+        return cudaGetLastError();
+      }
+      if (n == 4096 && kind == QLIN_HADAMARD_SYLVESTER) {
+        const int64_t groups = rows * (K / 4096);
+        const int64_t cap4 = static_cast<int64_t>(sm_count()) * 4;
+        const unsigned grid = static_cast<unsigned>(groups < cap4 ? groups : cap4);
+        hadamard4096_mma_kernel<DT><<<grid, kH4Warps * 32, 0, stream>>>(x, groups, static_cast<int>(K), signs, y);
+        return cudaGetLastError();
+      }
+    }
     if (n <= 256) {
       const int64_t nvec = rows * (K / 8);
       const int64_t want = (nvec + kHdThreads - 1) / kHdThreads;

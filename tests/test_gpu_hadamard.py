@@ -19,9 +19,12 @@ pytestmark = pytest.mark.gpu
 def _rows(seed, rows, k):
     rng = np.random.default_rng(seed)
     x = (rng.standard_normal((rows, k)) * np.exp(rng.uniform(-3, 3, size=(rows, 1)))).astype(np.float32)
-    x[1] = 0.0
-    x[2, ::7] *= 100.0           # outlier channels, the case the rotation is for
-    x[3] = 2.5                   # a constant row (a row outlier)
+    if rows > 1:
+        x[1] = 0.0
+    if rows > 2:
+        x[2, ::7] *= 100.0       # outlier channels, the case the rotation is for
+    if rows > 3:
+        x[3] = 2.5               # a constant row (a row outlier)
     return x
 
 
@@ -87,3 +90,48 @@ def test_hadamard_page_example_on_gpu(qlin_gpu):
     y = qlin_gpu.qlin_hadamard(x, 8)
     torch.cuda.synchronize()
     assert np.all(np.abs(y.cpu().numpy()[0] - np.array(ex["xH_printed"])) <= 1e-3)
+
+
+def _ulp_bound(ref, dtype):
+    """One unit in the last place of the output dtype at each reference value."""
+    bits = 10 if dtype == torch.float16 else 7
+    mag = np.maximum(np.abs(ref), 2.0 ** (-14 if dtype == torch.float16 else -126))
+    return 2.0 ** (np.floor(np.log2(mag)) - bits)
+
+
+@pytest.mark.parametrize("kind,n,rows,k", [("sylvester", 256, 5, 256), ("regular", 256, 5, 768),
+                                           ("sylvester", 256, 37, 4096 + 256), ("regular", 256, 64, 4096),
+                                           ("sylvester", 4096, 1, 4096), ("sylvester", 4096, 3, 8192),
+                                           ("sylvester", 4096, 40, 4096)])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_hadamard_tensor_core_within_one_ulp(qlin_gpu, kind, n, rows, k, dtype):
+    """Groups of 256 (both matrices) and Sylvester groups of 4096 in fp16 /
+    bf16 run as 16 x 16 products on the tensor cores, the intermediates kept
+    to 16 significant bits (relative error 2^-17 each): every output is
+    within one ulp of the output type of the exact rotation, plus 2^-14 of
+    the row's largest output for the intermediates (the rotation is
+    orthogonal, so that is far above their error and far below any wrong
+    element), with and without column signs, ragged group counts (5, 15, 1, 6
+    groups) included."""
+    x = torch.from_numpy(_rows(7 * n + k, rows, k)).to(dtype).cuda()
+    for signs in (None, _signs(k + 1, k)):
+        y = qlin_gpu.qlin_hadamard(x, n, kind=_code(qlin_gpu, kind),
+                                   signs=None if signs is None else torch.from_numpy(signs).cuda())
+        torch.cuda.synchronize()
+        assert qlin_gpu.qlin_get_device_error() == 0
+        ref = oracle.hadamard_rotate(x.double().cpu().numpy(), n, kind, signs)
+        got = y.double().cpu().numpy()
+        slack = 2.0 ** -14 * np.abs(ref).max(axis=1, keepdims=True)
+        assert np.all(np.abs(got - ref) <= _ulp_bound(ref, dtype) * 1.0001 + slack), (kind, n, dtype)
+        assert_within_tolerance(got, ref, "%s n=%d %s" % (kind, n, dtype))
+
+
+@pytest.mark.parametrize("n", [256, 4096])
+def test_hadamard_tensor_core_in_place(qlin_gpu, n):
+    """The tensor-core paths rotate a buffer onto itself exactly as out of place."""
+    x = torch.from_numpy(_rows(11, 24, 8192)).half().cuda()
+    out = qlin_gpu.qlin_hadamard(x, n)
+    torch.cuda.synchronize()
+    qlin_gpu.qlin_hadamard(x, n, y=x)
+    torch.cuda.synchronize()
+    assert torch.equal(x.cpu().view(torch.int16), out.cpu().view(torch.int16))
