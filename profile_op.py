@@ -7,6 +7,8 @@ so that a profiler can capture it in isolation, e.g.
 Operations (sizes as flags):
   w4a16        qlin_w4a16_gemm, X [T][K] fp16, weights N x K (uint4 g128)
   w4a16_group  qlin_w4a16_gemm_grouped over --groups matrices of N x K each
+  w4a16_decode qlin_w4a16_decode_run of a plan over --blocks decoder blocks (hidden K, intermediate N:
+               q,k,v grouped; o; gate,up grouped; down), X [T][K] fp16; one launch per rep
   int8_quant   qlin_quant_act_int8, X [T][K] fp16, symmetric
   w8a8         qlin_w8a8_gemm, A [T][K] int8, B [N][K] int8, per-token / per-channel scales, bf16 out
   w8a8_f16b    qlin_w8a8_gemm_f16b, the same with B as exact fp16 codes
@@ -62,6 +64,26 @@ def _setup(args, q, torch):
             else:
                 q.qlin_w4a16_gemm_grouped(x, [b[0] for b in blk], [b[1] for b in blk], [b[2] for b in blk], ys)
         return run
+
+    if args.op == "w4a16_decode":
+        def mat(n, k):
+            wq = torch.randint(0, 256, (n, k // 2), dtype=torch.uint8, device="cuda", generator=g)
+            sc = (torch.rand((n, k // 128), device="cuda", generator=g) * 0.015 + 0.005).half()
+            zp = torch.randint(0, 256, (n, (k // 128 + 1) // 2), dtype=torch.uint8, device="cuda", generator=g)
+            return wq, sc, zp
+        act = lambda n: torch.zeros((T, n), dtype=torch.float16, device="cuda")  # noqa: E731
+        x = randn((T, K), torch.float16)
+        qkv, o, gate, up, down = [act(K) for _ in range(3)], act(K), act(N), act(N), act(K)
+        steps = []
+        for _ in range(args.blocks):
+            m = {nm: mat(*shape) for nm, shape in (("q", (K, K)), ("k", (K, K)), ("v", (K, K)), ("o", (K, K)),
+                                                   ("gate", (N, K)), ("up", (N, K)), ("down", (K, N)))}
+            for names, xin, ys in ((("q", "k", "v"), x, qkv), (("o",), qkv[2], [o]), (("gate", "up"), o, [gate, up]),
+                                   (("down",), up, [down])):
+                steps.append((xin, [m[n][0] for n in names], [m[n][1] for n in names], [m[n][2] for n in names], ys))
+        ws = torch.zeros(q.qlin_w4a16_decode_workspace_bytes(len(steps)), dtype=torch.uint8, device="cuda")
+        plan = q.qlin_w4a16_decode_prepare(steps, ws)
+        return lambda i: q.qlin_w4a16_decode_run(ws, *plan)
 
     if args.op == "int8_quant":
         xs = [randn((T, K), torch.float16) for _ in range(copies)]
@@ -199,7 +221,7 @@ def _setup(args, q, torch):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("op", choices=["w4a16", "w4a16_group", "int8_quant", "w8a8", "w8a8_f16b", "w8a8_f16", "int8_quant_f16",
+    ap.add_argument("op", choices=["w4a16", "w4a16_group", "w4a16_decode", "int8_quant", "w8a8", "w8a8_f16b", "w8a8_f16", "int8_quant_f16",
                                    "nvfp4_quant", "nvfp4_gemm",
                                    "fp8_quant", "fp8_gemm", "rmsnorm_nvfp4", "rmsnorm_int8", "mxfp8_quant",
                                    "mxfp4_quant", "mxfp8_gemm", "mxfp4_gemm", "hadamard", "w4a16_act_order"])
@@ -210,6 +232,7 @@ def main(argv=None):
     ap.add_argument("--K", type=int, default=4096)
     ap.add_argument("--S", type=int, default=128, help="NVFP4 residual channels (K includes them for nvfp4_gemm)")
     ap.add_argument("--groups", type=int, default=3, help="matrices per w4a16_group launch")
+    ap.add_argument("--blocks", type=int, default=2, help="decoder blocks of a w4a16_decode plan")
     ap.add_argument("--copies", type=int, default=4, help="weight copies rotated over the launches")
     ap.add_argument("--reps", type=int, default=4, help="launches")
     ap.add_argument("--seed", type=int, default=0)

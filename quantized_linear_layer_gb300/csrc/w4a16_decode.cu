@@ -531,11 +531,14 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
   }
 }
 
-// Compute warps: 8 for every token count.  (16 warps, each taking one MMA
-// tile of a unit, fit in 96 registers for up to 8 tokens but measured slower
-// on the decoder stacks: 1.53 against 1.45 ms at T = 1, 1.74 against 1.58 ms
-// at T = 4; the kernel is bound by the per-stage exchange, not by warps.)
-constexpr int dc_warps(int NT) { return NT == 1 ? 8 : 8; }
+// Compute warps: 8 for every token count.  Measured on the decoder stacks:
+// 16 warps, each taking one MMA tile of a unit (96 registers at up to 8
+// tokens), were slower (1.53 against 1.45 ms at T = 1, 1.74 against 1.58 ms at
+// T = 4); so was folding the producer into a compute warp, which lifts the
+// register limit from 168 to 255 and let the next chunk's activations load
+// early, but the ring then drains while that warp computes (2.6 -> 3.2 ms at
+// T = 16).
+constexpr int dc_warps(int) { return 8; }
 
 const void* dc_kernel(int NT) {
   return NT == 1 ? reinterpret_cast<const void*>(w4a16_decode_kernel<1, dc_warps(1)>)
