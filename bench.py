@@ -393,13 +393,16 @@ def whole_job_rate(units_per_rank, seconds, world):
     return units_per_rank * world / seconds
 
 
-def kernel_timed_run(wl, torch, steps, warmup, dist):
+def kernel_timed_run(wl, torch, steps, warmup, dist, graphs=True):
     """Device-resident timing: per phase, the average over `steps` of the
-    event-measured duration on the phase's stream."""
+    event-measured duration on the phase's stream (the captured graphs, or
+    with graphs=False the same calls made directly, for profilers that cannot
+    replay graphs whose kernels carry programmatic dependencies)."""
     names = PATHS
+    run = (lambda n: wl.graphs[n].replay()) if graphs else (lambda n: wl.phase[n]())  # noqa: E731
     for _ in range(warmup):
         for n in names:
-            wl.graphs[n].replay()
+            run(n)
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(steps)]
     if dist is not None:
@@ -412,7 +415,7 @@ def kernel_timed_run(wl, torch, steps, warmup, dist):
         for s in range(steps):
             ev[s][0].record()
             for i, n in enumerate(names):
-                wl.graphs[n].replay()
+                run(n)
                 ev[s][i + 1].record()
         t1.record()
     torch.cuda.synchronize()
@@ -584,12 +587,13 @@ def run_ours(args):
     q.lib()
     peaks = load_peaks()
     wl = Workload(q, torch, args.layers, args.w4a16_path, args.w8a8_form)
-    wl.capture()
+    if not args.no_graphs:
+        wl.capture()
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    total, phase = kernel_timed_run(wl, torch, args.steps, args.warmup, dist)
+    total, phase = kernel_timed_run(wl, torch, args.steps, args.warmup, dist, graphs=not args.no_graphs)
     clocks = sampler.stop() if sampler else None
     err = q.qlin_get_device_error()
     # max over ranks of the timed region and of each phase
@@ -680,6 +684,7 @@ def run_ours(args):
                             "plan": "one persistent qlin_w4a16_decode_run launch per stack"}[wl.w4_path[T]])
                             for T in W4_TOKENS)),
             "w4a16_path": {"T=%d" % T: wl.w4_path[T] for T in W4_TOKENS},
+            "phases_timed_as": "direct calls (--no-graphs)" if args.no_graphs else "captured CUDA graphs",
             "w8a8_form": args.w8a8_form,
             "w4a16_layers_per_step": len(wl.w4),
             "w4a16_weight_bytes_per_pass": wl.w4_bytes[1],
@@ -765,6 +770,9 @@ def main():
                     help="W8A8 operand codes: both as exact fp16 values (qlin_quant_act_int8_f16 + "
                          "qlin_w8a8_gemm_f16), the weights only (qlin_w8a8_gemm_f16b), or int8 (qlin_w8a8_gemm)")
     ap.add_argument("--cpu-seconds", type=float, default=4.0, help="length of each bounded oracle sample")
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="time the phases as direct calls instead of captured CUDA graphs (for ncu, whose kernel "
+                         "replay stops at the second node of a graph with programmatic dependencies)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":
