@@ -34,32 +34,58 @@ def _round_to(ref, out_dtype):
     return torch.from_numpy(np.asarray(ref, dtype=np.float64)).to(out_dtype).double().numpy()
 
 
-def assert_within_tolerance(y, ref, what="", out_dtype=None):
+def assert_within_tolerance(y, ref, what=""):
     """The floating-point parity bar for fp16 / bf16 outputs against the
     float64 oracle: max |err| <= 1e-2 (1 + |ref|) elementwise, and relative
-    Frobenius error <= 2e-3.
-
-    On outputs of fewer than SMALL_OUTPUT elements the Frobenius bound is
-    a statistic of a handful of samples, and rounding a result to bf16 alone
-    moves a single element by up to 2^-9 relative; there (only) the Frobenius
-    bound is applied to the error beyond that final rounding, i.e. against
-    the oracle rounded to `out_dtype`.  The elementwise bound always applies
-    to the unrounded oracle."""
+    Frobenius error <= 2e-3."""
     import numpy as np
     y = np.asarray(y, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
+    _elementwise(y, ref, what)
+    nref = np.linalg.norm(ref)
+    if nref > 0:
+        rel = np.linalg.norm(y - ref) / nref
+        assert rel <= 2e-3, "%s: relative Frobenius error %g" % (what, rel)
+
+
+def assert_within_tolerance_few(y, ref, what, out_dtype):
+    """The parity bar for the edge-case GEMM shapes with fewer than
+    SMALL_OUTPUT output elements (e.g. a 1 x 8 output).  There the Frobenius
+    bound is a statistic of a handful of samples, and rounding the exact
+    result to bf16 alone moves an element by up to 2^-9 relative (a correct
+    kernel measured 2.3e-3 on a 1 x 8 output); so the Frobenius bound is
+    applied to the error beyond that final rounding, i.e. against the oracle
+    rounded to `out_dtype`.  The elementwise bound uses the unrounded oracle.
+    Larger outputs are refused: they take assert_within_tolerance."""
+    import numpy as np
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert y.size < SMALL_OUTPUT, "%s: %d outputs; use assert_within_tolerance" % (what, y.size)
+    _elementwise(y, ref, what)
+    nref = np.linalg.norm(ref)
+    if nref > 0:
+        rel = np.linalg.norm(y - _round_to(ref, out_dtype)) / nref
+        assert rel <= 2e-3, "%s: relative Frobenius error %g beyond the output rounding" % (what, rel)
+
+
+def check_gemm_output(y, ref, what, out_dtype):
+    """The GEMM tests' check: the plain bar, or for the tiny edge shapes
+    (fewer than SMALL_OUTPUT outputs) assert_within_tolerance_few."""
+    import numpy as np
+    if np.asarray(y).size < SMALL_OUTPUT:
+        assert_within_tolerance_few(y, ref, what, out_dtype)
+    else:
+        assert_within_tolerance(y, ref, what)
+
+
+def _elementwise(y, ref, what):
+    import numpy as np
     assert y.shape == ref.shape, (y.shape, ref.shape)
     assert np.all(np.isfinite(y)), what + ": non-finite output"
     err = np.abs(y - ref)
     bound = 1e-2 * (1.0 + np.abs(ref))
     worst = np.unravel_index(np.argmax(err - bound), err.shape) if err.size else None
     assert np.all(err <= bound), "%s: max err %g at %s (ref %g)" % (what, err[worst], worst, ref[worst])
-    nref = np.linalg.norm(ref)
-    if nref > 0:
-        rel = np.linalg.norm(y - ref) / nref
-        if rel > 2e-3 and out_dtype is not None and y.size < SMALL_OUTPUT:
-            rel = np.linalg.norm(y - _round_to(ref, out_dtype)) / nref
-        assert rel <= 2e-3, "%s: relative Frobenius error %g" % (what, rel)
 
 
 @pytest.fixture(scope="session")

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from quantized_linear_layer_gb300 import inputs
-from conftest import assert_within_tolerance, load_golden
+from conftest import assert_within_tolerance, check_gemm_output, load_golden
 
 pytestmark = pytest.mark.gpu
 
@@ -90,7 +90,7 @@ def test_fp8_gemm_against_oracle(qlin_gpu, T, N, K, bias_dt, out_dt):
     torch.cuda.synchronize()
     assert qlin_gpu.qlin_get_device_error() == 0
     ref = oracle.fp8_gemm_reference(qa, sa, qb, sb, bias_ref)
-    assert_within_tolerance(out.float().cpu().numpy(), ref, "fp8 GEMM %dx%dx%d" % (T, N, K), out_dtype=out_dt)
+    check_gemm_output(out.float().cpu().numpy(), ref, "fp8 GEMM %dx%dx%d" % (T, N, K), out_dt)
 
 
 def test_fp8_w8a8_pipeline_sampled_rows(qlin_gpu):

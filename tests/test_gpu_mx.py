@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from quantized_linear_layer_gb300 import inputs
-from conftest import assert_within_tolerance, sf_rows_to_mma
+from conftest import assert_within_tolerance, check_gemm_output, sf_rows_to_mma
 
 pytestmark = pytest.mark.gpu
 
@@ -103,7 +103,7 @@ def test_mx_gemm_against_oracle(qlin_gpu, fmt, T, N, K, out_dt):
     torch.cuda.synchronize()
     assert qlin_gpu.qlin_get_device_error() == 0
     ref = oracle.mx_gemm_reference(qa, sfa, qb, sfb, ofmt)
-    assert_within_tolerance(out.float().cpu().numpy(), ref, "%s GEMM %dx%dx%d" % (fmt, T, N, K), out_dtype=out_dt)
+    check_gemm_output(out.float().cpu().numpy(), ref, "%s GEMM %dx%dx%d" % (fmt, T, N, K), out_dt)
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])

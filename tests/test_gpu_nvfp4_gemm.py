@@ -10,7 +10,7 @@ import torch
 import oracle
 import quantized_linear_layer_gb300 as qmod
 from quantized_linear_layer_gb300 import inputs
-from conftest import assert_within_tolerance, sf_rows_to_mma
+from conftest import assert_within_tolerance, check_gemm_output, sf_rows_to_mma
 
 pytestmark = pytest.mark.gpu
 
@@ -45,7 +45,7 @@ def test_random_operands(qlin_gpu, T, N, K, out_dtype):
     ga, gb = np.float32(0.05), np.float32(0.02)
     ref = oracle.nvfp4_gemm_reference(qa, sfa, ga, qb, sfb, gb)
     y = _gemm(qlin_gpu, qa, sfa, ga, qb, sfb, gb, out_dtype)
-    assert_within_tolerance(y, ref, "nvfp4 %dx%dx%d" % (T, N, K), out_dtype=out_dtype)
+    check_gemm_output(y, ref, "nvfp4 %dx%dx%d" % (T, N, K), out_dtype)
 
 
 @pytest.mark.parametrize("T,N", [(128, 128), (128, 256), (256, 384)])
