@@ -692,9 +692,11 @@ qlin_status qlin_mx_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
  * F32 rows and the other group sizes run butterfly stages in float32: the
  * result is within float32 rounding of the exact rotation (before the final
  * rounding to the input dtype).  F16 / BF16 rows with n = 256 (both kinds)
- * or a Sylvester n = 4096 run as 16 x 16 products on the tensor cores (the
- * order-256 matrices are Kronecker squares of a 16 x 16 factor, ConvRot's
- * dense product cut into factors): fp32 accumulation, intermediates kept to
+ * or a Sylvester n of 512 .. 4096 run as 16 x 16 products on the tensor
+ * cores (the order-256 matrices are Kronecker squares of a 16 x 16 factor,
+ * ConvRot's dense product cut into factors; for n < 4096 the groups after
+ * the buffer's last whole block of 4096 elements take the butterflies
+ * instead): fp32 accumulation, intermediates kept to
  * 16 significant bits, so the result is within about 2^-16 of the exact
  * rotation's magnitude before the final rounding.  Every path gives the same
  * bits on every run.  The weights take the same rotation offline (W . Q),

@@ -226,7 +226,8 @@ __global__ void __launch_bounds__(kHdThreads) hadamard_warp_kernel(const void* x
 template <int DT>
 __global__ void __launch_bounds__(1024) hadamard_cta_kernel(const void* x, int64_t groups, int K, int n,
                                                             float c, const int8_t* __restrict__ signs,
-                                                            void* y) {
+                                                            void* y, int64_t e_base = 0) {
+  // x and y point at element e_base of the rows (the signs' column is taken from it)
   extern __shared__ __align__(16) float buf[];
   constexpr int EB = DT == 2 ? 4 : 2;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(1024) hadamard_cta_kernel(const void* x, int64
       for (int i = 0; i < 8; ++i) v[i] = upper ? __fsub_rn(o[i], v[i]) : __fadd_rn(v[i], o[i]);
       __syncthreads();
     }
-    scale_and_sign(v, c, signs, e0 % K);
+    scale_and_sign(v, c, signs, (e_base + e0) % K);
     store8<DT>(static_cast<char*>(y) + e0 * EB, v);
   }
 }
@@ -425,15 +426,21 @@ __global__ void __launch_bounds__(kHmWarps * 32) hadamard256_mma_kernel(const vo
   }
 }
 
-// ---- Sylvester groups of 4096 on the tensor cores (fp16 / bf16 rows) ------
+// ---- Sylvester groups of 512 .. 4096 on the tensor cores (fp16 / bf16 rows) --
 //
-// H_4096 = H16 (x) H_256: with the group cut into 16 sub-blocks x_a of 256,
-//   y[256 c + j] = sum_a H16[a][c] . Z_a[j],   Z_a = x_a . H_256 = F . M_a . F,
-// so each warp rotates two sub-blocks exactly as above (unnormalized), the
-// CTA collects Z (16 x 256, as bf16 hi and lo parts) in shared memory, and a
-// third 16 x 16 product Y = F . Z combines the sub-blocks, each warp 32 of
-// the 256 columns.  One CTA per group at a time; the next group's input is
-// loaded while the current one is rotated.
+// H_n = H_m (x) H_256 with m = n / 256: with a group cut into m sub-blocks
+// x_a of 256,
+//   y[256 c + j] = sum_a H_m[a][c] . Z_a[j],   Z_a = x_a . H_256 = F . M_a . F.
+// A CTA takes 4096 consecutive elements at a time (16 sub-blocks: 16 / m
+// whole groups): each warp rotates two sub-blocks exactly as above
+// (unnormalized), the CTA collects Z (16 x 256, as bf16 hi and lo parts) in
+// shared memory, and a third 16 x 16 product Y = B . Z combines the
+// sub-blocks of each group, B = diag(H_m, ..., H_m) (for n = 4096, B = F),
+// each warp 32 of the 256 columns; then one multiply by float32(1/sqrt(n))
+// (exact for n = 1024 and 4096).  The next 4096 elements are loaded while the
+// current ones are rotated.  The kernel takes whole blocks of 4096 only (a
+// bounds check per load cost 15% here); the groups after the last whole block
+// (fewer than 4096 elements, m < 16) run through the float32 butterflies.
 
 constexpr int kH4Warps = 8;
 
@@ -444,21 +451,33 @@ __device__ __forceinline__ uint32_t h4_off(int r, int j) {
   return r * 512 + ((((j >> 3) ^ (r & 7))) << 4) + (j & 7) * 2;
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kH4Warps * 32) hadamard4096_mma_kernel(const void* x, int64_t groups, int K,
-                                                                         const int8_t* __restrict__ signs, void* y) {
+template <int DT, int m>
+__global__ void __launch_bounds__(kH4Warps * 32) hadamard4096_mma_kernel(const void* x, int64_t passes, float scale_rt,
+                                                                         int K, const int8_t* __restrict__ signs,
+                                                                         void* y) {
+  // 1 / sqrt(256 m): exact for m = 4 and 16, float32-rounded (scale_rt) otherwise
+  const float scale = m == 16 ? 1.0f / 64.0f : m == 4 ? 1.0f / 32.0f : scale_rt;
+  // passes: blocks of 4096 consecutive elements (16 sub-blocks of 256)
+  const int64_t groups = passes;
   __shared__ __align__(128) unsigned char stage[kH4Warps][2][kHmGroupBytes];  // inputs, then the output rows
   __shared__ __align__(128) unsigned char zbuf[2][16 * 512];                 // Z as bf16: hi, lo
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  uint32_t fa[4], fb[4];
+  // F (= H16) for the sub-block rotations; B = diag(H_m, ..., H_m) (rows c,
+  // columns a: H_m[c % m][a % m] when c / m == a / m, else 0) to combine them.
+  // On a diagonal block H16[c][a] = (-1)^popcount(c / m) H_m[c % m][a % m]
+  // (the bits above log2 m are equal), so B is F masked and sign-flipped.
+  // F is kept once, as bf16 (fb); the fp16 copy for stage 1 is rebuilt from
+  // its sign bits where it is used (+-1: 0x3C00 in fp16, 0x3F80 in bf16),
+  // which keeps the fp16 build within 64 registers (4 CTAs per SM)
+  uint32_t fb[4], fc[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int r = g + 8 * (q & 1), k = 2 * c + 8 * (q >> 1);
     const float f0 = hm_factor(0, r, k), f1 = hm_factor(0, r, k + 1);
-    fa[q] = hm_pack<DT>(f0, f1);
     fb[q] = hm_pack<1>(f0, f1);
+    // k is even and m >= 2, so k and k + 1 lie in the same block
+    fc[q] = m == 16 ? fb[q] : r / m != k / m ? 0u : fb[q] ^ ((__popc(r / m) & 1) ? 0x80008000u : 0u);
   }
-  const float scale = 1.0f / 64.0f;  // 1 / sqrt(4096), exact
   const char* xb = static_cast<const char*>(x);
   char* yb = static_cast<char*>(y);
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(&stage[warp][0][0]));
@@ -496,6 +515,14 @@ __global__ void __launch_bounds__(kH4Warps * 32) hadamard4096_mma_kernel(const v
                    : "=r"(m0), "=r"(m1), "=r"(m2), "=r"(m3)
                    : "r"(sbase + sb * kHmGroupBytes + hm_off(lm_row, lm_half)));
       float q0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, q1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      uint32_t fa[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if constexpr (DT == 0)
+          asm volatile("lop3.b32 %0, %1, 0x80008000, 0x3C003C00, 0xEA;" : "=r"(fa[q]) : "r"(fb[q]));
+        else
+          fa[q] = fb[q];
+      }
       hm_mma<DT>(q0, fa[0], fa[1], fa[2], fa[3], m0, m1);
       hm_mma<DT>(q1, fa[0], fa[1], fa[2], fa[3], m2, m3);
       uint32_t ah[4], al[4];
@@ -521,7 +548,7 @@ __global__ void __launch_bounds__(kH4Warps * 32) hadamard4096_mma_kernel(const v
       }
     }
     __syncthreads();  // Z complete; every warp's staging tiles free
-    // Y = F . Z on this warp's columns 32 w .. 32 w + 31 (four column tiles)
+    // Y = B . Z on this warp's columns 32 w .. 32 w + 31 (four column tiles)
 #pragma unroll
     for (int t = 0; t < 4; t += 2) {
       const int j0 = 32 * warp + 8 * t;
@@ -535,10 +562,10 @@ __global__ void __launch_bounds__(kH4Warps * 32) hadamard4096_mma_kernel(const v
                    : "=r"(l0), "=r"(l1), "=r"(l2), "=r"(l3)
                    : "r"(zb + 16 * 512 + h4_off(r, jj)));
       float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      hm_mma<1>(d0, fb[0], fb[1], fb[2], fb[3], l0, l1);
-      hm_mma<1>(d0, fb[0], fb[1], fb[2], fb[3], h0, h1);
-      hm_mma<1>(d1, fb[0], fb[1], fb[2], fb[3], l2, l3);
-      hm_mma<1>(d1, fb[0], fb[1], fb[2], fb[3], h2, h3);
+      hm_mma<1>(d0, fc[0], fc[1], fc[2], fc[3], l0, l1);
+      hm_mma<1>(d0, fc[0], fc[1], fc[2], fc[3], h0, h1);
+      hm_mma<1>(d1, fc[0], fc[1], fc[2], fc[3], l2, l3);
+      hm_mma<1>(d1, fc[0], fc[1], fc[2], fc[3], h2, h3);
       // y[256 c_out + j], c_out = g, g + 8, j = j0 (+8) + 2c: scaled, rounded,
       // into the output rows (the staging area, 16 rows of 512 bytes)
       const float dv[4][2] = {{d0[0], d0[1]}, {d0[2], d0[3]}, {d1[0], d1[1]}, {d1[2], d1[3]}};
@@ -599,11 +626,29 @@ cudaError_t launch_hadamard(const void* x, qlin_dtype dtype, int64_t rows, int64
           hadamard256_mma_kernel<DT, 1><<<grid, kHmWarps * 32, 0, stream>>>(x, groups, static_cast<int>(K), signs, y);
         return cudaGetLastError();
       }
-      if (n == 4096 && kind == QLIN_HADAMARD_SYLVESTER) {
-        const int64_t groups = rows * (K / 4096);
-        const int64_t cap4 = static_cast<int64_t>(sm_count()) * 4;
-        const unsigned grid = static_cast<unsigned>(groups < cap4 ? groups : cap4);
-        hadamard4096_mma_kernel<DT><<<grid, kH4Warps * 32, 0, stream>>>(x, groups, static_cast<int>(K), signs, y);
+      if (n >= 512 && n <= 4096 && kind == QLIN_HADAMARD_SYLVESTER) {
+        const int64_t total = rows * K, passes = total / 4096;
+        const int Ki = static_cast<int>(K);
+        if (passes > 0) {
+          const int64_t cap4 = static_cast<int64_t>(sm_count()) * 4;
+          const unsigned grid = static_cast<unsigned>(passes < cap4 ? passes : cap4);
+          switch (n) {
+            case 512: hadamard4096_mma_kernel<DT, 2><<<grid, kH4Warps * 32, 0, stream>>>(x, passes, c, Ki, signs, y); break;
+            case 1024: hadamard4096_mma_kernel<DT, 4><<<grid, kH4Warps * 32, 0, stream>>>(x, passes, c, Ki, signs, y); break;
+            case 2048: hadamard4096_mma_kernel<DT, 8><<<grid, kH4Warps * 32, 0, stream>>>(x, passes, c, Ki, signs, y); break;
+            default: hadamard4096_mma_kernel<DT, 16><<<grid, kH4Warps * 32, 0, stream>>>(x, passes, c, Ki, signs, y); break;
+          }
+          cudaError_t e = cudaGetLastError();
+          if (e != cudaSuccess) return e;
+        }
+        // whole groups after the last block of 4096 elements: the butterflies
+        const int64_t done = passes * 4096, tail_groups = (total - done) / n;
+        if (tail_groups == 0) return cudaSuccess;
+        constexpr int EB = DT == 2 ? 4 : 2;
+        const size_t smem = static_cast<size_t>(n) * sizeof(float);
+        hadamard_cta_kernel<DT><<<static_cast<unsigned>(tail_groups), static_cast<unsigned>(n / 8), smem, stream>>>(
+            static_cast<const char*>(x) + done * EB, tail_groups, Ki, static_cast<int>(n), c, signs,
+            static_cast<char*>(y) + done * EB, done);
         return cudaGetLastError();
       }
     }

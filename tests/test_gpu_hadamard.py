@@ -102,17 +102,23 @@ def _ulp_bound(ref, dtype):
 @pytest.mark.parametrize("kind,n,rows,k", [("sylvester", 256, 5, 256), ("regular", 256, 5, 768),
                                            ("sylvester", 256, 37, 4096 + 256), ("regular", 256, 64, 4096),
                                            ("sylvester", 4096, 1, 4096), ("sylvester", 4096, 3, 8192),
-                                           ("sylvester", 4096, 40, 4096)])
+                                           ("sylvester", 4096, 40, 4096), ("sylvester", 512, 3, 1536),
+                                           ("sylvester", 1024, 5, 2048), ("sylvester", 2048, 3, 2048),
+                                           ("sylvester", 512, 16, 4096), ("sylvester", 512, 15, 512),
+                                           ("sylvester", 1024, 3, 1024)])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 def test_hadamard_tensor_core_within_one_ulp(qlin_gpu, kind, n, rows, k, dtype):
-    """Groups of 256 (both matrices) and Sylvester groups of 4096 in fp16 /
-    bf16 run as 16 x 16 products on the tensor cores, the intermediates kept
+    """Groups of 256 (both matrices) and Sylvester groups of 512 .. 4096 in
+    fp16 / bf16 run as 16 x 16 products on the tensor cores, the intermediates kept
     to 16 significant bits (relative error 2^-17 each): every output is
     within one ulp of the output type of the exact rotation, plus 2^-14 of
     the row's largest output for the intermediates (the rotation is
     orthogonal, so that is far above their error and far below any wrong
     element), with and without column signs, ragged group counts (5, 15, 1, 6
-    groups) included."""
+    groups) included.  For n < 4096 the groups after the buffer's last whole
+    block of 4096 elements run through the float32 butterflies: one, two,
+    one and seven such groups here (after 1, 2, 1, 1 blocks), and a buffer
+    smaller than one block (three groups of 1024)."""
     x = torch.from_numpy(_rows(7 * n + k, rows, k)).to(dtype).cuda()
     for signs in (None, _signs(k + 1, k)):
         y = qlin_gpu.qlin_hadamard(x, n, kind=_code(qlin_gpu, kind),
