@@ -142,5 +142,4 @@ def test_mx_gemm_smallest_k(qlin_gpu, fmt, T, N, K):
     torch.cuda.synchronize()
     assert qlin_gpu.qlin_get_device_error() == 0
     ref = oracle.mx_gemm_reference(qa, sfa, qb, sfb, ofmt)
-    assert_within_tolerance(out.float().cpu().numpy(), ref, "%s GEMM %dx%dx%d" % (fmt, T, N, K),
-                            out_dtype=torch.bfloat16)
+    check_gemm_output(out.float().cpu().numpy(), ref, "%s GEMM %dx%dx%d" % (fmt, T, N, K), torch.bfloat16)
