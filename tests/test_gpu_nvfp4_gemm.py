@@ -48,6 +48,20 @@ def test_random_operands(qlin_gpu, T, N, K, out_dtype):
     check_gemm_output(y, ref, "nvfp4 %dx%dx%d" % (T, N, K), out_dtype)
 
 
+def test_many_tiles_per_cta_pair(qlin_gpu):
+    """18 M tiles x 24 N tiles (432 tiles): every persistent CTA walks about
+    three tiles, so each stage slot is refilled across tile boundaries and
+    the accumulator is handed to the epilogue several times."""
+    T, N, K = 2304, 6144, 512
+    rng = np.random.default_rng(77)
+    qa, sfa = _rand(rng, T, K)
+    qb, sfb = _rand(rng, N, K)
+    ga, gb = np.float32(0.05), np.float32(0.02)
+    ref = oracle.nvfp4_gemm_reference(qa, sfa, ga, qb, sfb, gb)
+    y = _gemm(qlin_gpu, qa, sfa, ga, qb, sfb, gb, torch.bfloat16)
+    check_gemm_output(y, ref, "nvfp4 %dx%dx%d" % (T, N, K), torch.bfloat16)
+
+
 @pytest.mark.parametrize("T,N", [(128, 128), (128, 256), (256, 384)])
 def test_scale_factor_layout(qlin_gpu, T, N):
     """Every element 1.0 and one non-unit block scale per row of A (and of B)
