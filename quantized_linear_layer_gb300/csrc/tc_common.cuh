@@ -112,6 +112,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
+// Bulk copy from this CTA's shared memory to another CTA's of the cluster
+// (dst and bar are shared::cluster addresses of that CTA, e.g. from mapa),
+// completing `bytes` on its mbarrier; both addresses 16-byte aligned, size a
+// multiple of 16.  Writes of this thread (and, after a barrier, of the others
+// that fenced) to the source must precede it behind fence_proxy_async_smem.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // L2 policy for data read exactly once (streamed weights): evicted first, so
 // that small operands shared across launches stay resident.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -230,6 +241,13 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* v) 
 }
 
 // Each thread of the warp reads 16 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t* v) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* v) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "

@@ -100,8 +100,11 @@ def test_prefill_llama_layers_sampled_rows(qlin_gpu, N, K):
 
 @pytest.mark.parametrize("T,N,K", [
     (33, 8, 128),       # the smallest prefill: one tile, one K stage (no split)
-    (257, 128, 256),    # two token tiles, two K stages: the CTA pair splits K one stage each
+    (257, 128, 256),    # three 128-token tiles, two K stages: a CTA pair splits K one stage each
     (64, 256, 384),     # an odd stage count split 1 + 2
+    (100, 4096, 1024),  # 32 tiles, each shared by a cluster of four CTAs (two K stages each)
+    (256, 11008, 512),  # 172 tiles of 128 tokens on persistent CTAs (some take two)
+    (1000, 520, 256),   # eight token tiles, the last of 104 tokens, CTA pairs
 ])
 def test_prefill_edge_shapes(qlin_gpu, T, N, K):
     d = inputs.w4a16_decode(seed=T * 3 + K, T=T, N=N, K=K)
