@@ -156,7 +156,7 @@ qlin_status qlin_quant_w4_g128(const void* w, qlin_dtype w_dtype, int64_t N, int
  *           the symmetric zero-point 8 for every group
  *   group   128
  *   y       out, fp16 [T][N]
- * K a multiple of `group`; any T >= 0.  Up to 64 tokens run the decode /
+ * K a multiple of `group`; any T >= 0.  Up to 16 tokens run the decode /
  * skinny kernels above.  More tokens (prefill) run a tcgen05 GEMM
  * ("LLM and AIGC quantization", W4A16: dequantize next to the tensor cores,
  * fp16 multiply, fp32 accumulate).  That GEMM rounds each weight once to
@@ -164,8 +164,9 @@ qlin_status qlin_quant_w4_g128(const void* w, qlin_dtype w_dtype, int64_t N, int
  * Bit stability: a given (x, W) always gives the same bits at the same T on
  * the same device.  Prefill outputs may differ in the last bit between token
  * counts or devices with another SM count: when the output tiles are few,
- * two CTAs split K and add their two fp32 half sums, a different rounding
- * order from the unsplit sum (both within the tolerance).
+ * two or four CTAs share K and their fp32 partial sums are added in a fixed
+ * order, a different rounding order from the unsplit sum (both within the
+ * tolerance).
  * ---------------------------------------------------------------------- */
 qlin_status qlin_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, const uint8_t* wq,
                             const void* scales, const uint8_t* zeros, int64_t group, void* y,

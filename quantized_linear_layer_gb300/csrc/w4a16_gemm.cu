@@ -370,9 +370,11 @@ cudaError_t launch_w4a16_mma(const void* x, int64_t T, int64_t N, int64_t K, con
 // the skinny kernel has no plan for.
 // Above this many tokens the tensor-core prefill GEMM runs instead of the
 // skinny kernel (16 tokens per launch, the weights read once per launch):
-// measured on the Llama-2-7B shapes, the skinny launches win up to 32 tokens,
-// the prefill GEMM from 48 on.
-constexpr int64_t kW4a16PrefillMinT = 32;
+// measured on the Llama-2-7B shapes, one skinny launch wins at 16 tokens, the
+// prefill GEMM (128-token tiles, K shared by up to four CTAs) from 17 on
+// (17-32 tokens: 12.6 / 25.2 / 22.2 us against 18.1 / 29.9 / 35.7 us for two
+// skinny launches on 4096x4096 / 11008x4096 / 4096x11008).
+constexpr int64_t kW4a16PrefillMinT = 16;
 
 cudaError_t launch_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int count, const int64_t* N,
                                       const uint8_t* const* wq, const void* const* scales,

@@ -375,8 +375,9 @@ def test_sequence_decoder_blocks_equal_single_launches(qlin_gpu, hid, inter):
 def test_chain_equals_grouped_calls(qlin_gpu, T, hid, inter):
     """qlin_w4a16_chain (one call, a launch per step) over two decoder blocks
     gives every output of the same grouped calls made one by one, bit for
-    bit, and the oracle within tolerance; T = 20 runs as a 16-token and a
-    4-token launch per step.  The first block's v projection is symmetric (no
+    bit, and the oracle within tolerance; T = 20 runs the prefill GEMM (a
+    128-token tile, K shared by a CTA cluster) per step.  The first block's
+    v projection is symmetric (no
     zero-points)."""
     seed = 700 + T
     blocks = []
