@@ -19,20 +19,23 @@
 // of a chunk stays within 1024 . 128 . 128 = 2^24, and each chunk's fp32
 // result is converted to int32 and added in int32, which gives D^ bit for bit.
 //
-// Persistent kernel: one CTA per SM walks 128 x 256 output tiles (groups of 8
-// row tiles share column tiles for L2 reuse), 10 warps:
+// Persistent kernel: one CTA per SM walks 128 x BN output tiles (groups of 8
+// row tiles share column tiles for L2 reuse), BN = 256, or 224 where that
+// gives fewer rounds of tiles on the SMs (2048 x 4096: 304 tiles of 224
+// columns are two full rounds on 152 SMs, where 256 tiles of 256 columns took
+// two rounds with the second a third empty), 10 warps:
 //   warp 0     TMA producer: 64 K elements (128 bytes of fp16) of the tile's
-//              128 A rows and 256 B rows per stage, in the 128-byte swizzled
+//              128 A rows and BN B rows per stage, in the 128-byte swizzled
 //              K-major layout the MMA descriptors describe, 4-stage ring of
-//              48 KB stages.
+//              48 (44) KB stages.
 //   warp 1     TMEM allocation and the MMA issuer: per stage 4 x tcgen05.mma
-//              kind::f16 (M=128, N=256, K=16, both operands in shared memory)
-//              into one of two 256-column chunk accumulators, which alternate
+//              kind::f16 (M=128, N=BN, K=16, both operands in shared memory)
+//              into one of two BN-column chunk accumulators, which alternate
 //              chunk by chunk (and across tiles).
 //   warps 2-9  epilogue: lane l of the warp with TMEM lane quadrant q owns row
-//              32q + l and columns 128h .. 128h + 127 of the tile,
+//              32q + l and columns h BN / 2 .. (h + 1) BN / 2 - 1 of the tile,
 //              h = (warp - 2) / 4.  It reads each finished chunk, adds it in
-//              int32 to 128 running totals held in registers and releases the
+//              int32 to BN / 2 running totals held in registers and releases the
 //              accumulator at once, so the MMAs of the chunk after next never
 //              wait for more than one read.  After the tile's last chunk it
 //              applies the epilogue from the registers and stores 128-byte
@@ -42,6 +45,8 @@
 // already in flight, frees TMEM and exits.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "device_common.cuh"
 #include "qlin_internal.h"
 #include "tc_common.cuh"
@@ -50,7 +55,7 @@
 namespace qlin {
 namespace {
 
-constexpr int kBM = 128, kBN = 256;
+constexpr int kBM = 128;
 constexpr int kBK = 64;                        // K elements per stage: 128 bytes of fp16 per row
 constexpr int kRowBytes = 2 * kBK;
 constexpr int kMmaPerStage = kBK / 16;
@@ -59,19 +64,26 @@ constexpr int kChunkK = 1024;                  // exact fp32 accumulation span
 constexpr int kKbPerChunk = kChunkK / kBK;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kCols = kBN / 2;                 // columns of the tile one epilogue warp owns
-constexpr int kTmemCols = 2 * kBN;             // two chunk accumulators
+constexpr int kTmemCols = 512;                 // two chunk accumulators of BN columns
 
-constexpr int kStageBytes = (kBM + kBN) * kRowBytes;  // 48 KB
-constexpr int kSmemPar = kStages * kStageBytes;
-constexpr int kParBytes = 3 * kCols * 4;              // one epilogue warp's s_b, azp_adj and bias
-constexpr int kSmemBar = kSmemPar + kEpiWarps * kParBytes;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
-constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
-constexpr int kSmemTotal = kSmemMisc + 16 + 1024;     // + alignment slack
-static_assert(kSmemTotal <= 227 * 1024, "shared memory budget");
-static_assert(kStageBytes % 1024 == 0 && (kBM * kRowBytes) % 1024 == 0,
-              "stages and the B tile keep the 1024-byte alignment of the swizzled atoms");
+// The plan of a tile width BN.
+template <int BN>
+struct F16Cfg {
+  static constexpr int kCols = BN / 2;                       // columns of the tile one epilogue warp owns
+  static constexpr int kStageBytes = (kBM + BN) * kRowBytes;  // 48 or 44 KB
+  static constexpr int kSmemPar = kStages * kStageBytes;
+  static constexpr int kParBytes = 3 * kCols * 4;            // one epilogue warp's s_b, azp_adj and bias
+  static constexpr int kSmemBar = kSmemPar + kEpiWarps * kParBytes;
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
+  static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
+  static constexpr int kSmemTotal = kSmemMisc + 16 + 1024;   // + alignment slack
+  static_assert(BN == 256 || BN == 224, "tile widths");
+  static_assert(2 * BN <= kTmemCols, "TMEM budget");
+  static_assert(kSmemTotal <= 227 * 1024, "shared memory budget");
+  static_assert(kStageBytes % 1024 == 0 && (kBM * kRowBytes) % 1024 == 0,
+                "stages and the B tile keep the 1024-byte alignment of the swizzled atoms");
+  static_assert(kCols % 16 == 0, "the epilogue reads TMEM 16 columns at a time");
+};
 
 enum { kSiteEmpty = 1, kSiteFull, kSiteAccEmpty, kSiteAccFull, kSiteDrain };
 
@@ -103,6 +115,7 @@ __device__ __forceinline__ void tile_coords(int tile, int mt_count, int nt_count
   nt = in / rows;
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) w8a8_f16_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                    const __grid_constant__ CUtensorMap tmB, int T,
                                                                    int N, int K, EpiArgs epi, void* __restrict__ out,
@@ -110,8 +123,11 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_f16_gemm_kernel(const __grid
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
+  using Cfg = F16Cfg<BN>;
+  constexpr int kCols = Cfg::kCols, kStageBytes = Cfg::kStageBytes, kSmemPar = Cfg::kSmemPar;
+  constexpr int kParBytes = Cfg::kParBytes, kSmemBar = Cfg::kSmemBar, kSmemMisc = Cfg::kSmemMisc;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt_count = (T + kBM - 1) / kBM, nt_count = (N + kBN - 1) / kBN;
+  const int mt_count = (T + kBM - 1) / kBM, nt_count = (N + BN - 1) / BN;
   const int tiles = mt_count * nt_count;
   const int my_tiles = blockIdx.x < tiles ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   const int num_kb = (K + kBK - 1) / kBK;
@@ -172,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_f16_gemm_kernel(const __grid
           // as zeros (fp16 +0)
           tc::mbar_arrive_expect_tx(full(s), kStageBytes);
           tc::tma_load_2d(dst, &tmA, kb * kRowBytes, mt * kBM, full(s));
-          tc::tma_load_2d(dst + kBM * kRowBytes, &tmB, kb * kRowBytes, nt * kBN, full(s));
+          tc::tma_load_2d(dst + kBM * kRowBytes, &tmB, kb * kRowBytes, nt * BN, full(s));
           issued = it + 1;
         }
       }
@@ -183,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_f16_gemm_kernel(const __grid
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = tc::idesc_f16(kBM, kBN, 0);  // fp16 x fp16 -> fp32
+      const uint32_t idesc = tc::idesc_f16(kBM, BN, 0);  // fp16 x fp16 -> fp32
       bool issued_any = false;
       int it = 0, g = 0;  // stage and chunk counters across tiles
       for (int ti = 0; ti < my_tiles && !*abort_flag; ++ti) {
@@ -203,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_f16_gemm_kernel(const __grid
           tc::tc_fence_after();
           const uint32_t a_base = sbase + s * kStageBytes;
           const uint32_t b_base = a_base + kBM * kRowBytes;
-          const uint32_t d = tmem + buf * kBN;
+          const uint32_t d = tmem + buf * BN;
           // MMAs that cover at least one real K element of the stage
           const int kk_valid = min(kMmaPerStage, (K - kb * kBK + 15) / 16);
 #pragma unroll
@@ -243,14 +259,15 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_f16_gemm_kernel(const __grid
     for (int ti = 0; ti < my_tiles && ok; ++ti) {
       int mt, nt;
       tile_coords(blockIdx.x + ti * gridDim.x, mt_count, nt_count, mt, nt);
-      const int c0 = nt * kBN + col0;  // first output column of this warp
+      const int c0 = nt * BN + col0;  // first output column of this warp
       // Column parameters of this tile, in a copy private to this warp (so no
       // other warp's progress matters), loaded while the MMAs run.
       __syncwarp();
       if (!raw) {
 #pragma unroll
-        for (int j = 0; j < kCols / 32; ++j) {
+        for (int j = 0; j < (kCols + 31) / 32; ++j) {
           const int col = lane + 32 * j, n = c0 + col;
+          if (col >= kCols) break;
           const bool inb = n < N;
           par_sb[col] = inb ? (epi.scale_b_per_col ? epi.scale_b[n] : epi.scale_b[0]) : 0.0f;
           par_adj[col] = (inb && epi.azp_adj != nullptr) ? epi.azp_adj[n] : 0;
@@ -278,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_f16_gemm_kernel(const __grid
           break;
         }
         tc::tc_fence_after();
-        const uint32_t ta = lane_base + buf * kBN + col0;
+        const uint32_t ta = lane_base + buf * BN + col0;
 #pragma unroll
         for (int cg = 0; cg < kCols / 16; ++cg) {
           uint32_t v[16];
@@ -310,11 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_f16_gemm_kernel(const __grid
 
       // out = s_a . ((D^ - azp . azp_adj) . s_b) + bias: the correction in
       // int32, one conversion to float, then the scales and the bias in fp32.
-      // Two blocks of 64 columns, each packed, transposed and stored in turn.
+      // Blocks of 64 columns (the last one partial when BN / 2 = 112), each
+      // packed, transposed and stored in turn.
       const int j = lane & 7;
       const int row0 = mt * kBM + q * 32 + 8 * (lane >> 3);
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < (kCols + 63) / 64; ++b) {
         uint32_t pk[32];  // this row's columns 64b .. 64b + 63, two per word
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -322,6 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_f16_gemm_kernel(const __grid
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int col = 64 * b + 2 * i + h;
+            if (col >= kCols) {
+              f[h] = 0.0f;
+              continue;
+            }
             const int32_t corr = per_tensor_adj ? par_adj[col] : za * par_adj[col];
             const float d = __int2float_rn(tot[col] - corr);
             f[h] = fmaf(sa, d * par_sb[col], par_bias[col]);
@@ -355,10 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_f16_gemm_kernel(const __grid
           }
         }
         const int col = c0 + 64 * b + 8 * j;
+        const bool in_tile = 64 * b + 8 * j < kCols;  // the 16-byte chunk is this warp's
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int r = row0 + e;
-          if (r < T && col < N)
+          if (r < T && col < N && in_tile)
             *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (int64_t)r * N + col) =
                 make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
@@ -377,16 +400,51 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_f16_gemm_kernel(const __grid
 
 }  // namespace
 
+template <int BN>
+cudaError_t launch_f16_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, int64_t T, int64_t N, int64_t K,
+                          const EpiArgs& epi, void* out, int64_t tiles, cudaStream_t stream) {
+  // the shared-memory attribute, set once per device
+  static std::once_flag once[64];
+  static cudaError_t attr[64];
+  int dev = 0;
+  cudaError_t st = cudaGetDevice(&dev);
+  if (st != cudaSuccess) return st;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [&] {
+    attr[dev] = cudaFuncSetAttribute(w8a8_f16_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     F16Cfg<BN>::kSmemTotal);
+  });
+  if (attr[dev] != cudaSuccess) return attr[dev];
+  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  // programmatic dependent launch: the prologue (barriers, TMEM, tensor maps)
+  // overlaps the end of the previous kernel (the activation quantizer)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = F16Cfg<BN>::kSmemTotal;
+  cfg.stream = stream;
+  cudaLaunchAttribute la[1];
+  la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  la[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = la;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w8a8_f16_gemm_kernel<BN>, tmA, tmB, static_cast<int>(T), static_cast<int>(N),
+                            static_cast<int>(K), epi, out, device_error_word());
+}
+
 cudaError_t launch_w8a8_gemm_f16(const void* a16, const void* b16, int64_t T, int64_t N, int64_t K,
                                  const W8A8Epilogue& e, void* out, cudaStream_t stream) {
   if (T == 0 || N == 0) return cudaSuccess;
+  // the tile width with the least (rounds of tiles on the SMs) x width
+  const int64_t sms = sm_count(), mt = (T + kBM - 1) / kBM;
+  auto cost = [&](int64_t bn) { return (mt * ((N + bn - 1) / bn) + sms - 1) / sms * bn; };
+  const int bn = cost(224) < cost(256) ? 224 : 256;
+  const int64_t tiles = mt * ((N + bn - 1) / bn);
   CUtensorMap tmA, tmB;
   cudaError_t st = make_tmap_2d_u8(&tmA, a16, static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(T), kRowBytes, kBM,
                                    /*swizzle_bytes=*/128);
   if (st != cudaSuccess) return st;
-  st = make_tmap_2d_u8(&tmB, b16, static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N), kRowBytes, kBN, 128);
-  if (st != cudaSuccess) return st;
-  st = cudaFuncSetAttribute(w8a8_f16_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
+  st = make_tmap_2d_u8(&tmB, b16, static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N), kRowBytes, bn, 128);
   if (st != cudaSuccess) return st;
   EpiArgs epi;
   epi.scale_a = e.scale_a;
@@ -398,22 +456,8 @@ cudaError_t launch_w8a8_gemm_f16(const void* a16, const void* b16, int64_t T, in
   epi.scale_b_per_col = e.scale_b_per_col ? 1 : 0;
   epi.bias_dtype = e.bias_dtype;
   epi.out_dtype = e.out_dtype;
-  const int64_t tiles = ((T + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-  // programmatic dependent launch: the prologue (barriers, TMEM, tensor maps)
-  // overlaps the end of the previous kernel (the activation quantizer)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemTotal;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, w8a8_f16_gemm_kernel, tmA, tmB, static_cast<int>(T), static_cast<int>(N),
-                            static_cast<int>(K), epi, out, device_error_word());
+  if (bn == 224) return launch_f16_bn<224>(tmA, tmB, T, N, K, epi, out, tiles, stream);
+  return launch_f16_bn<256>(tmA, tmB, T, N, K, epi, out, tiles, stream);
 }
 
 }  // namespace qlin
