@@ -166,9 +166,10 @@ def _rows(q, torch):
                 return run, byts, "hbm"
             return run, 2.0 * T * N * K, "bf16"
         return setup
-    for (N, K) in ((4096, 4096), (11008, 4096), (4096, 11008)):
-        rows.append(("w4a16_prefill_%dx%d" % (N, K), "W4A16 g128 prefill GEMM, T=2048, N=%d K=%d, fp16 out" % (N, K),
-                     w4(N, K, 2048)))
+    for T in (2048, 256, 65):
+        for (N, K) in ((4096, 4096), (11008, 4096), (4096, 11008)):
+            rows.append(("w4a16_prefill_t%d_%dx%d" % (T, N, K),
+                         "W4A16 g128 prefill GEMM, T=%d, N=%d K=%d, fp16 out" % (T, N, K), w4(N, K, T)))
     rows.append(("w4a16_act_order_t1", "W4A16 act-order decode (gather + GEMV), T=1, N=K=4096", w4(4096, 4096, 1, True)))
     rows.append(("w4a16_act_order_t2048", "W4A16 act-order prefill (gather + GEMM), T=2048, N=K=4096",
                  w4(4096, 4096, 2048, True)))
@@ -188,7 +189,7 @@ def _rows(q, torch):
             return run, 4 * T * K, "hbm"
         return setup
     for kind, name in ((q.QLIN_HADAMARD_SYLVESTER, "sylvester"), (q.QLIN_HADAMARD_REGULAR, "regular")):
-        for n in ((256, 4096) if name == "sylvester" else (64, 256)):
+        for n in ((256, 512, 1024, 2048, 4096) if name == "sylvester" else (64, 256)):
             rows.append(("hadamard_%s_%d" % (name, n), "online Hadamard (%s, groups of %d), 8192 x 8192 fp16" % (name, n),
                          had(kind, n)))
     return rows
