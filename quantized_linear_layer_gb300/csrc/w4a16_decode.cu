@@ -384,6 +384,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
       // this warp's two groups of the chunk, and their activations
       const int gg0 = j * kDcChunkGroups + 2 * kw;
       const int ngw = min(2, max(0, G - gg0));
+      // every load of the chunk first (one round trip to L2), then the pairing in place
       uint4 xb[2][NT][4];
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj)
@@ -393,20 +394,23 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
           if (jj < ngw && t < T && ub < ue) {
             const uint4* xp =
                 reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * K + (gg0 + jj) * 128 + c * 32);
-            uint4 u4[4];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) u4[w] = ldg_cg_v4(xp + w);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              uint32_t pr[4];
-              pair_x(u4[w], pr);
-              xb[jj][nt][w] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-            }
+            for (int w = 0; w < 4; ++w) xb[jj][nt][w] = ldg_cg_v4(xp + w);
           } else {
 #pragma unroll
             for (int w = 0; w < 4; ++w) xb[jj][nt][w] = make_uint4(0u, 0u, 0u, 0u);
           }
         }
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint32_t pr[4];
+            pair_x(xb[jj][nt][w], pr);
+            xb[jj][nt][w] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+          }
       int k = 0;  // segment of the current unit
       for (int u = ub; u < ue; ++u, ++si) {
         while (k + 1 < nseg && u >= seg[k].unit_end) ++k;
