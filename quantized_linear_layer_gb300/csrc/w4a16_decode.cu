@@ -380,12 +380,15 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
     const int nseg = min(max(*reinterpret_cast<const int*>(meta + sizeof(DcSeg) * kDcMaxGroup), 1), kDcMaxGroup);
     const int K = st.K, G = st.G, zpitch = st.zpitch, nch = st.nchunks, pitch = st.chunk_u64 * 8;
     const __half* x = st.x;
-    for (int j = 0; j < nch; ++j) {
-      // this warp's two groups of the chunk, and their activations
-      const int gg0 = j * kDcChunkGroups + 2 * kw;
-      const int ngw = min(2, max(0, G - gg0));
-      // every load of the chunk first (one round trip to L2), then the pairing in place
-      uint4 xb[2][NT][4];
+    // this warp's two groups of chunk j, and their activations (raw loads, then
+    // the pairing in place: every load in flight at once)
+    auto chunk_groups = [&](int j, int& gg0, int& ngw) {
+      gg0 = j * kDcChunkGroups + 2 * kw;
+      ngw = min(2, max(0, G - gg0));
+    };
+    auto load_raw = [&](int j, uint4 (*dst)[NT][4]) {
+      int gg0, ngw;
+      chunk_groups(j, gg0, ngw);
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
@@ -395,12 +398,14 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
             const uint4* xp =
                 reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * K + (gg0 + jj) * 128 + c * 32);
 #pragma unroll
-            for (int w = 0; w < 4; ++w) xb[jj][nt][w] = ldg_cg_v4(xp + w);
+            for (int w = 0; w < 4; ++w) dst[jj][nt][w] = ldg_cg_v4(xp + w);
           } else {
 #pragma unroll
-            for (int w = 0; w < 4; ++w) xb[jj][nt][w] = make_uint4(0u, 0u, 0u, 0u);
+            for (int w = 0; w < 4; ++w) dst[jj][nt][w] = make_uint4(0u, 0u, 0u, 0u);
           }
         }
+    };
+    auto pair_all = [&](uint4 (*v)[NT][4]) {
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
@@ -408,11 +413,23 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             uint32_t pr[4];
-            pair_x(xb[jj][nt][w], pr);
-            xb[jj][nt][w] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+            pair_x(v[jj][nt][w], pr);
+            v[jj][nt][w] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
           }
+    };
+    // one token tile: the next chunk's activations are loaded while the
+    // chunk's last unit computes (a second set of registers; more tiles have
+    // no room for it)
+    constexpr bool kPrefetch = NT == 1;
+    uint4 xb[2][NT][4], xn[2][NT][4];
+    load_raw(0, xb);
+    pair_all(xb);
+    for (int j = 0; j < nch; ++j) {
+      int gg0, ngw;
+      chunk_groups(j, gg0, ngw);
       int k = 0;  // segment of the current unit
       for (int u = ub; u < ue; ++u, ++si) {
+        if (kPrefetch && u == ue - 1 && j + 1 < nch) load_raw(j + 1, xn);
         while (k + 1 < nseg && u >= seg[k].unit_end) ++k;
         const int row0 = (u - seg[k].unit_begin) * kDcUnit;  // matrix row of the unit's first row
         const int nrow = seg[k].N;
@@ -515,6 +532,20 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(pe);
         }
+      }
+      // the next chunk's activations
+      if (j + 1 < nch) {
+        if (kPrefetch && ub < ue) {
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int w = 0; w < 4; ++w) xb[jj][nt][w] = xn[jj][nt][w];
+        } else {
+          load_raw(j + 1, xb);
+        }
+        pair_all(xb);
       }
     }
     // the meta buffer of this step is no longer read by this warp
