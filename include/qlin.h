@@ -473,7 +473,8 @@ qlin_status qlin_w8a8_gemm_f16b(const int8_t* a, const void* b16, int64_t T, int
  * zero-points of qlin_quant_act_int8 and writes each code as the fp16
  * number of the same value; qlin_w8a8_gemm_f16 then runs the GEMM with both
  * tiles read by TMA straight into the MMA's operand layout (no widening on
- * chip, 128 x 256 output tiles).  D^ and every output equal those of
+ * chip, 128 x 256 output tiles, or 128 x 224 where that gives fewer rounds
+ * of tiles on the SMs).  D^ and every output equal those of
  * qlin_w8a8_gemm on the int8 codes bit for bit.  The trade is 2 T K bytes of
  * activation codes instead of T K (written once, read from L2 by the tiles).
  *   qlin_quant_act_int8_f16: as qlin_quant_act_int8, q16 out fp16 [T][K]
