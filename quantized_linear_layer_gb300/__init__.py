@@ -280,6 +280,31 @@ def qlin_w4a16_chain(steps, group=128, stream=None):
                                                      _stream(stream)))
 
 
+class W4A16Chain:
+    """The steps of qlin_w4a16_chain marshalled once: run() makes the one C
+    call with the stored argument array (no per-call checks or conversions
+    in Python).  The array holds the tensors' device pointers, so it is valid
+    while they are; the object keeps the tensors referenced."""
+
+    def __init__(self, steps, group=128):
+        if not steps:
+            raise ValueError("at least one step")
+        self._t = _chain_tokens(steps)
+        self._arr = _w4a16_steps(steps)
+        self._n = len(steps)
+        self._group = group
+        self._steps = steps
+
+    def run(self, stream=None):
+        _check("qlin_w4a16_chain", lib().qlin_w4a16_chain(ctypes.cast(self._arr, ctypes.c_void_p), self._n, self._t,
+                                                         self._group, _stream(stream)))
+
+
+def qlin_w4a16_chain_prepare(steps, group=128):
+    """qlin_w4a16_chain's argument array built once, for repeated runs (W4A16Chain.run)."""
+    return W4A16Chain(steps, group)
+
+
 def qlin_w4a16_decode_workspace_bytes(nsteps):
     return lib().qlin_w4a16_decode_workspace_bytes(nsteps)
 

@@ -431,6 +431,38 @@ int gv_warps_shape_r(const GvShapeInfo& si, int warps) {
   return (w + kGvMaxComputeWarps + 1) * si.regs_per_warp <= si.rf ? w : 0;
 }
 
+// Both kernels' attributes, once per device: dynamic shared memory up to the
+// per-block maximum (each launch asks for its own amount), and the largest
+// shared-memory carveout, so that the SM can hold a CTA and the neighbouring
+// layer's whatever launch shape reached it first.
+struct GvAttrs {
+  std::once_flag once;
+  cudaError_t status = cudaSuccess;
+};
+GvAttrs g_gv_attrs[64];
+
+cudaError_t gv_set_attrs() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  GvAttrs& g = g_gv_attrs[dev];
+  std::call_once(g.once, [&] {
+    int block_smem = 0;
+    g.status = cudaDeviceGetAttribute(&block_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    const void* fns[2] = {reinterpret_cast<const void*>(w4a16_gemv_kernel<8>),
+                          reinterpret_cast<const void*>(w4a16_gemv_kernel<4>)};
+    for (const void* fn : fns) {
+      if (g.status == cudaSuccess)
+        g.status = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, block_smem);
+      if (g.status == cudaSuccess)
+        g.status = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                        cudaSharedmemCarveoutMaxShared);
+    }
+  });
+  return g.status;
+}
+
 }  // namespace
 
 bool w4a16_gemv_supported(int64_t T, int64_t N, int64_t K) {
@@ -470,8 +502,6 @@ cudaError_t launch_w4a16_gemv_grouped(const void* x, int64_t K, int count, const
   a.K = static_cast<int>(K);
   a.zpitch = static_cast<int>((K / 128 + 1) / 2);
   const bool b8 = gv_rows_per_batch(a.RG) == 8;
-  const void* fn = b8 ? reinterpret_cast<const void*>(w4a16_gemv_kernel<8>)
-                      : reinterpret_cast<const void*>(w4a16_gemv_kernel<4>);
   int threads = (a.RG * a.WPR + 1) * 32;
   int dyn = smem;
   if (shape == 1) {
@@ -481,11 +511,7 @@ cudaError_t launch_w4a16_gemv_grouped(const void* x, int64_t K, int count, const
     dyn = std::max(smem, gv_smem_shape_s(si));
     if (dyn > si.block_smem) dyn = smem;
   }
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-  if (e != cudaSuccess) return e;
-  // the largest shared-memory carveout, so that the SM can hold this CTA and
-  // the neighbouring layer's whatever launch shape reached it first
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  const cudaError_t e = gv_set_attrs();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

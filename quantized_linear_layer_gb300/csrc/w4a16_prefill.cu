@@ -54,6 +54,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "device_common.cuh"
 #include "qlin_internal.h"
 #include "tc_common.cuh"
@@ -549,9 +551,18 @@ cudaError_t launch_prefill_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, co
                               const uint8_t* zeros, int64_t T, int64_t N, int64_t K, void* y, int split,
                               cudaStream_t stream) {
   using Cfg = PfCfg<BN>;
-  cudaError_t st = cudaFuncSetAttribute(w4a16_prefill_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        Cfg::kSmemTotal);
+  // the shared-memory attribute, set once per device
+  static std::once_flag once[64];
+  static cudaError_t attr_status[64];
+  int dev = 0;
+  cudaError_t st = cudaGetDevice(&dev);
   if (st != cudaSuccess) return st;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [&] {
+    attr_status[dev] = cudaFuncSetAttribute(w4a16_prefill_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            Cfg::kSmemTotal);
+  });
+  if (attr_status[dev] != cudaSuccess) return attr_status[dev];
   const int64_t tiles = ((N + kPfBM - 1) / kPfBM) * ((T + BN - 1) / BN);
   const int grid = split > 1 ? static_cast<int>(split * tiles) : static_cast<int>(tiles < sm_count() ? tiles : sm_count());
   cudaLaunchConfig_t cfg = {};

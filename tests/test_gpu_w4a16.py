@@ -373,9 +373,10 @@ def test_sequence_decoder_blocks_equal_single_launches(qlin_gpu, hid, inter):
 @pytest.mark.parametrize("T,hid,inter", [(1, 1024, 2816), (4, 1024, 2816), (16, 1024, 2816), (20, 512, 1408),
                                           (4, 4096, 11008)])
 def test_chain_equals_grouped_calls(qlin_gpu, T, hid, inter):
-    """qlin_w4a16_chain (one call, a launch per step) over two decoder blocks
-    gives every output of the same grouped calls made one by one, bit for
-    bit, and the oracle within tolerance; T = 20 runs the prefill GEMM (a
+    """qlin_w4a16_chain (one call, a launch per step) over two decoder blocks,
+    and the same chain prepared once (qlin_w4a16_chain_prepare) and run
+    twice, give every output of the same grouped calls made one by one, bit
+    for bit, and the oracle within tolerance; T = 20 runs the prefill GEMM (a
     128-token tile, K shared by a CTA cluster) per step.  The first block's
     v projection is symmetric (no
     zero-points)."""
@@ -398,7 +399,7 @@ def test_chain_equals_grouped_calls(qlin_gpu, T, hid, inter):
             d[name] = (wq[0], sc[0], zp[0])
         devs.append(d)
 
-    def run(chain):
+    def run(mode):
         outs = [{n: torch.full((T, blocks[0][n][0].shape[0]), float("nan"), dtype=torch.float16, device="cuda")
                  for n in blocks[0]} for _ in blocks]
         steps = []
@@ -411,8 +412,12 @@ def test_chain_equals_grouped_calls(qlin_gpu, T, hid, inter):
                           [d[n][2] for n in ("gate", "up")], [o[n] for n in ("gate", "up")]))
             steps.append((o["up"], [d["down"][0]], [d["down"][1]], [d["down"][2]], [o["down"]]))
             h = o["down"]
-        if chain:
+        if mode == "chain":
             qlin_gpu.qlin_w4a16_chain(steps)
+        elif mode == "prepared":
+            prepared = qlin_gpu.qlin_w4a16_chain_prepare(steps)
+            prepared.run()
+            prepared.run()  # a second run over the same buffers gives the same outputs
         else:
             for (x, wqs, scs, zps, ys) in steps:
                 qlin_gpu.qlin_w4a16_gemm_grouped(x, wqs, scs, zps, ys)
@@ -420,10 +425,11 @@ def test_chain_equals_grouped_calls(qlin_gpu, T, hid, inter):
         assert qlin_gpu.qlin_get_device_error() == 0
         return outs
 
-    got, ref = run(True), run(False)
+    got, ref, prep = run("chain"), run("grouped"), run("prepared")
     for bi in range(2):
         for n in blocks[0]:
             assert torch.equal(got[bi][n], ref[bi][n]), "block %d %s" % (bi, n)
+            assert torch.equal(prep[bi][n], ref[bi][n]), "prepared chain, block %d %s" % (bi, n)
     codes, s16, z = blocks[0]["q"]
     assert_within_tolerance(got[0]["q"].cpu().numpy(), oracle.w4a16_reference(x0, codes, s16, z), "chain q")
     codes, s16, z = blocks[1]["down"]
