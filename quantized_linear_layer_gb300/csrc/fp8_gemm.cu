@@ -325,7 +325,7 @@ cudaError_t launch_fp8_gemm(const uint8_t* a, const uint8_t* b, int64_t T, int64
   if (st != cudaSuccess) return st;
   st = make_tmap_2d_u8(&tmB, b, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBK, kBN, 128);
   if (st != cudaSuccess) return st;
-  st = cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
+  st = ensure_max_dynamic_smem(reinterpret_cast<const void*>(fp8_gemm_kernel));
   if (st != cudaSuccess) return st;
   const int64_t tiles = ((T + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());

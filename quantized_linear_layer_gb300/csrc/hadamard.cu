@@ -668,8 +668,7 @@ cudaError_t launch_hadamard(const void* x, qlin_dtype dtype, int64_t rows, int64
     const unsigned grid = static_cast<unsigned>(groups < cap ? groups : cap);
     const size_t smem = static_cast<size_t>(n) * sizeof(float);
     if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(hadamard_cta_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
+      cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(hadamard_cta_kernel<DT>));
       if (e != cudaSuccess) return e;
     }
     hadamard_cta_kernel<DT><<<grid, static_cast<unsigned>(n / 8), smem, stream>>>(x, groups, static_cast<int>(K),

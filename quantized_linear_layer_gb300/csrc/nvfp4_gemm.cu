@@ -435,7 +435,7 @@ cudaError_t launch_block_scaled_gemm(const uint8_t* a, const uint8_t* sfa, const
   if (st != cudaSuccess) return st;
   st = make_tmap_2d_u8(&tmB, b, row_bytes, static_cast<uint64_t>(N), kBKB, kBN, 128);
   if (st != cudaSuccess) return st;
-  st = cudaFuncSetAttribute(block_scaled_gemm_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
+  st = ensure_max_dynamic_smem(reinterpret_cast<const void*>(block_scaled_gemm_kernel<F>));
   if (st != cudaSuccess) return st;
   const int64_t tiles = ((T + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());

@@ -418,8 +418,7 @@ cudaError_t launch_quant_nvfp4(const void* x, qlin_dtype x_dtype, int64_t rows, 
       auto kern = nvfp4_quant_kernel<DT, R, NORM>;
       // the opt-in covers dynamic plus static shared memory above the 48 KB default
       if (smem + 4 * 1024 > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern));
         if (e != cudaSuccess) return e;
       }
       kern<<<static_cast<unsigned>((rows + R - 1) / R), kNvThreads, smem, stream>>>(
@@ -487,7 +486,7 @@ cudaError_t launch_arc_perm(const void* x, qlin_dtype x_dtype, int64_t rows, int
   while (n < K) n <<= 1;
   const size_t smem = sizeof(unsigned long long) * n;
   if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(perm_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(perm_sort_kernel));
     if (e != cudaSuccess) return e;
   }
   perm_sort_kernel<<<1, 1024, smem, stream>>>(perm, static_cast<int>(K), n);

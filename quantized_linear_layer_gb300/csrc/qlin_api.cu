@@ -4,6 +4,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "qlin_internal.h"
 
@@ -95,6 +96,32 @@ int32_t* device_error_word() {
 int sm_count() {
   DeviceInfo* d = current_info();
   return (d != nullptr && d->sm_count > 0) ? d->sm_count : 152;
+}
+
+cudaError_t ensure_max_dynamic_smem(const void* fn) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  struct Done {
+    int dev;
+    const void* fn;
+    cudaError_t status;
+  };
+  static std::vector<Done> done;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Done& d : done)
+    if (d.dev == dev && d.fn == fn) return d.status;
+  int optin = 0;
+  cudaFuncAttributes fa = {};
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, fn);
+  // the limit covers the dynamic part; static shared memory comes on top
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - static_cast<int>(fa.sharedSizeBytes));
+  done.push_back({dev, fn, e});
+  return e;
 }
 
 }  // namespace qlin

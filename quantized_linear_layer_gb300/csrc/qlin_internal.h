@@ -17,6 +17,11 @@ int32_t* device_error_word();
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Raises fn's dynamic shared-memory limit to the device's per-block maximum
+// (less fn's static shared memory), once per device and kernel; every launch
+// then asks for its own amount.  Returns the status of that one setting.
+cudaError_t ensure_max_dynamic_smem(const void* fn);
+
 cudaError_t launch_quant_w4_g128(const void* w, qlin_dtype w_dtype, int64_t N, int64_t K, uint8_t* wq,
                                  void* scales, uint8_t* zeros, cudaStream_t stream);
 

@@ -122,8 +122,7 @@ cudaError_t launch_x_permute(const void* x, int64_t T, int64_t K, const int32_t*
   if (T == 0) return cudaSuccess;
   const size_t smem = static_cast<size_t>(K) * 2;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(x_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(x_permute_kernel));
     if (e != cudaSuccess) return e;
   }
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;

@@ -20,6 +20,8 @@
 // partial sums are added in a fixed order through shared memory.
 //
 // The fragment mapping and the unpack are in w4a16_mma_common.cuh.
+#include <mutex>
+
 #include "device_common.cuh"
 #include "qlin_internal.h"
 #include "tc_common.cuh"
@@ -313,10 +315,24 @@ cudaError_t launch_chunk(const __half* x, int Tc, int N, int K, const uint8_t* w
   const int W = 8;  // the scale / zero-point staging below assumes 256 threads
   const int GPW = (GC + W - 1) / W;
   const W4Smem plan = w4_smem_plan(W, GPW, GC, Tc, NT, C);
-  cudaError_t e = cudaFuncSetAttribute(w4a16_mma_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.total);
+  const void* fn = reinterpret_cast<const void*>(w4a16_mma_kernel<NT>);
+  cudaError_t e = ensure_max_dynamic_smem(fn);
   if (e != cudaSuccess) return e;
   if (C > 8) {
-    e = cudaFuncSetAttribute(w4a16_mma_kernel<NT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    // clusters above the portable 8 CTAs: allowed once per device
+    static std::once_flag once[64];
+    static cudaError_t status[64];
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    } else {
+      std::call_once(once[dev], [&] {
+        status[dev] = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      });
+      e = status[dev];
+    }
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};

@@ -787,7 +787,7 @@ cudaError_t launch_w4a16_skinny_grouped(const void* x, int64_t T, int64_t K, int
                                      static_cast<uint32_t>(8 * Gc), kSkTile);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(p.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
+  cudaError_t e = ensure_max_dynamic_smem(p.fn);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.NC * p.C);

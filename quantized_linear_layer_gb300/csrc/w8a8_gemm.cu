@@ -542,7 +542,7 @@ cudaError_t launch_w8a8_gemm(const int8_t* a, const void* b, bool b_f16, int64_t
   const void* fn = b_f16 ? reinterpret_cast<const void*>(w8a8_gemm_kernel<true>)
                          : reinterpret_cast<const void*>(w8a8_gemm_kernel<false>);
   const int smem = b_f16 ? W8Plan<true>::kSmemTotal : W8Plan<false>::kSmemTotal;
-  st = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  st = ensure_max_dynamic_smem(fn);
   if (st != cudaSuccess) return st;
   EpiArgs epi;
   epi.scale_a = e.scale_a;
