@@ -199,6 +199,18 @@ qlin_status qlin_w4a16_gemm_grouped(const void* x, int64_t T, int64_t K, int cou
                                     const uint8_t* const* zeros, int64_t group, void* const* y,
                                     cudaStream_t stream);
 
+/* Launch placement of the T = 1 GEMV on the current device.  Consecutive
+   GEMV launches alternate between two launch shapes of one kernel (one
+   holding more than half of an SM's registers, the other more than half of
+   its shared memory), so that each layer's CTAs take one slot per SM beside
+   the previous layer's; the shapes are derived from the device's limits and
+   the kernel's register count, and every launch keeps the plain shape when
+   they cannot be met (a slower placement, same results).
+   *alternating (host pointer, may be NULL) receives 1 when the two shapes are
+   in use, else 0; *registers (may be NULL) the kernel's registers per
+   thread.  No launch, no synchronization. */
+qlin_status qlin_w4a16_gemv_launch_info(int* alternating, int* registers);
+
 /* ------------------------------------------------------------------------
  * next 3 - W4A16 with act-order (g_idx)
  *

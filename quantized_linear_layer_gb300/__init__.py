@@ -20,7 +20,8 @@ __all__ = [
     "QLIN_F16", "QLIN_BF16", "QLIN_F32", "QLIN_I32", "QLIN_NVFP4_RESIDUAL", "QLIN_NVFP4_DUPLICATE",
     "QLIN_SF_ROWS", "QLIN_SF_MMA", "qlin_nvfp4_sf_bytes", "qlin_nvfp4_sf_to_mma",
     "qlin_version", "qlin_get_device_error",
-    "qlin_quant_w4_g128", "qlin_w4a16_gemm", "qlin_w4a16_gemm_grouped", "qlin_w4a16_step",
+    "qlin_quant_w4_g128", "qlin_w4a16_gemm", "qlin_w4a16_gemm_grouped", "qlin_w4a16_gemv_launch_info",
+    "qlin_w4a16_step",
     "qlin_w4a16_sequence_workspace_bytes", "qlin_w4a16_gemv_sequence", "qlin_w4a16_gemv_sequence_noalloc",
     "qlin_w4a16_chain", "qlin_w4a16_decode_workspace_bytes", "qlin_w4a16_decode_prepare", "qlin_w4a16_decode_run",
     "qlin_quant_act_int8", "qlin_int8_row_sum", "qlin_w8a8_gemm", "qlin_int8_to_f16", "qlin_w8a8_gemm_f16b",
@@ -57,6 +58,7 @@ _SIGS = {
     "qlin_status_string": ([_I32], ctypes.c_char_p),
     "qlin_last_error_message": ([], ctypes.c_char_p),
     "qlin_get_device_error": ([_P, _P], _I32),
+    "qlin_w4a16_gemv_launch_info": ([_P, _P], _I32),
     "qlin_quant_w4_g128": ([_P, _I32, _I64, _I64, _I64, _P, _P, _P, _P], _I32),
     "qlin_w4a16_gemm": ([_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P], _I32),
     "qlin_w4a16_gemm_grouped": ([_P, _I64, _I64, _I32, _P, _P, _P, _P, _I64, _P, _P], _I32),
@@ -160,6 +162,14 @@ def qlin_get_device_error(stream=None):
     if st not in (0, 5):
         _check("qlin_get_device_error", st)
     return code.value
+
+
+def qlin_w4a16_gemv_launch_info():
+    """(alternating, registers): whether the T = 1 GEMV's two alternating launch
+    shapes are in use on the current device, and its registers per thread."""
+    alt, regs = ctypes.c_int(0), ctypes.c_int(0)
+    _check("qlin_w4a16_gemv_launch_info", lib().qlin_w4a16_gemv_launch_info(ctypes.byref(alt), ctypes.byref(regs)))
+    return alt.value, regs.value
 
 
 def qlin_quant_w4_g128(w, wq, scales, zeros, group=128, stream=None):

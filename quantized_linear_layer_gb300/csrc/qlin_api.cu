@@ -165,6 +165,13 @@ const char* qlin_last_error_message(void) { return g_last_error; }
 
 int qlin_version(void) { return 100; }
 
+qlin_status qlin_w4a16_gemv_launch_info(int* alternating, int* registers) {
+  QLIN_DEVICE();
+  const cudaError_t e = w4a16_gemv_launch_info(alternating, registers);
+  if (e != cudaSuccess) return cuda_fail(e, "w4a16_gemv_launch_info");
+  return ok();
+}
+
 qlin_status qlin_get_device_error(cudaStream_t stream, int32_t* code_out) {
   DeviceInfo* info = nullptr;
   qlin_status st = probe_current_device(&info);

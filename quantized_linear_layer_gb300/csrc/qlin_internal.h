@@ -31,6 +31,9 @@ cudaError_t launch_w4a16_gemm(const void* x, int64_t T, int64_t N, int64_t K, co
 // One-token W4A16 GEMV on the CUDA cores (T == 1, K <= 12288, the CTA's
 // band of scales small enough for its shared-memory plan).
 bool w4a16_gemv_supported(int64_t T, int64_t N, int64_t K);
+// Whether the GEMV's alternating launch shapes are in use on the current
+// device, and the kernel's registers per thread.
+cudaError_t w4a16_gemv_launch_info(int* alternating, int* registers);
 cudaError_t launch_w4a16_gemv(const void* x, int64_t N, int64_t K, const uint8_t* wq, const void* scales,
                               const uint8_t* zeros, void* y, cudaStream_t stream);
 // One GEMV launch over the concatenated rows of `count` matrices sharing x

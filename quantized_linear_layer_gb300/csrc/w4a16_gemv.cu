@@ -526,6 +526,19 @@ cudaError_t launch_w4a16_gemv_grouped(const void* x, int64_t K, int count, const
   return b8 ? cudaLaunchKernelEx(&cfg, w4a16_gemv_kernel<8>, a) : cudaLaunchKernelEx(&cfg, w4a16_gemv_kernel<4>, a);
 }
 
+cudaError_t w4a16_gemv_launch_info(int* alternating, int* registers) {
+  const GvShapeInfo& si = gv_shape_info();
+  if (alternating) *alternating = si.ok ? 1 : 0;
+  if (registers) {
+    cudaFuncAttributes f8 = {}, f4 = {};
+    cudaError_t e = cudaFuncGetAttributes(&f8, reinterpret_cast<const void*>(w4a16_gemv_kernel<8>));
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&f4, reinterpret_cast<const void*>(w4a16_gemv_kernel<4>));
+    if (e != cudaSuccess) return e;
+    *registers = std::max(f8.numRegs, f4.numRegs);
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_w4a16_gemv(const void* x, int64_t N, int64_t K, const uint8_t* wq, const void* scales,
                               const uint8_t* zeros, void* y, cudaStream_t stream) {
   if (N == 0) return cudaSuccess;

@@ -175,6 +175,18 @@ def test_decode_band_split_shapes(qlin_gpu):
         assert_within_tolerance(y, ref, "W4A16 N=%d K=%d" % (n, k))
 
 
+def test_gemv_alternating_launch_shapes_in_use(qlin_gpu):
+    """The T = 1 GEMV places each layer's CTAs one per SM beside the previous
+    layer's by alternating two launch shapes, which are derived from the
+    device's limits and the kernel's register count; when they cannot be met
+    every launch silently keeps the plain shape (same results, a slower
+    stack).  Pin that the two shapes are in use here, so that a change of
+    the kernel's registers that breaks the plan fails this test."""
+    alternating, registers = qlin_gpu.qlin_w4a16_gemv_launch_info()
+    assert 0 < registers <= 72, "GEMV kernel uses %d registers per thread" % registers
+    assert alternating == 1, "the GEMV's alternating launch shapes are not in use (%d registers)" % registers
+
+
 @pytest.mark.parametrize("T", [1, 4])
 def test_decode_chain_ping_pong(qlin_gpu, T):
     """Six layers launched back to back on one stream, each reading the
