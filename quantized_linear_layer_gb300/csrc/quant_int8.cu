@@ -33,11 +33,17 @@ namespace {
 
 constexpr int kQuantThreads = 256;
 constexpr int kMaxVecPerThread = 4;  // 4 x 8 elements held in registers
+// The row quantizers are bound by the latency of each CTA's life (row loads,
+// the max reduction and its barrier, the divisions), so their rate is the
+// rows each SM holds at once: 48 registers per thread fit five CTAs per SM
+// instead of four (a few bytes of spill) and measured 8% faster for int8 and
+// 4% for FP8 (2048 x 4096 and 4096 x 4096 fp16 rows).
+constexpr int kQuantMinCtasPerSm = 5;
 
 // F16: the codes are written as the fp16 numbers of the same values (exact,
 // |q| <= 128), the operand form of the W8A8 GEMM that widens nothing on chip.
 template <int DT, bool ASYM, bool F16>
-__global__ void __launch_bounds__(kQuantThreads) quant_int8_rows_kernel(const void* __restrict__ x, int K,
+__global__ void __launch_bounds__(kQuantThreads, kQuantMinCtasPerSm) quant_int8_rows_kernel(const void* __restrict__ x, int K,
                                                                          void* __restrict__ q,
                                                                          float* __restrict__ scale,
                                                                          int32_t* __restrict__ azp) {
@@ -161,7 +167,7 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
 // One CTA per row, the same shape as the int8 quantizer: 16-byte loads kept
 // in registers, block absmax, then IEEE division and the E4M3 encode.
 template <int DT>
-__global__ void __launch_bounds__(kQuantThreads) quant_fp8_rows_kernel(const void* __restrict__ x, int K,
+__global__ void __launch_bounds__(kQuantThreads, kQuantMinCtasPerSm) quant_fp8_rows_kernel(const void* __restrict__ x, int K,
                                                                       uint8_t* __restrict__ q,
                                                                       float* __restrict__ scale) {
   pdl_launch_dependents();  // the GEMM that reads the codes may start setting up
